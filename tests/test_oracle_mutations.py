@@ -1,0 +1,96 @@
+"""Plants plausible mistakes in copies of the oracle (CPU only) and checks the pins catch each one.
+
+Every mutant is compiled from a string-edited copy of ``oracle/dplr_oracle.c``
+into a temporary directory, swapped in for the real library, and run through
+the pin functions of ``test_oracle_pins``. A mutant that passes every pin
+would mean the pins leave that part of the oracle unchecked.
+"""
+
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "dplr_oracle.c")
+
+MUTANTS = {
+    # generic mode
+    "generic_sign_of_low_rank": ("s -= At[(size_t)i * dk + c] * w[i * nc + n];",
+                                 "s += At[(size_t)i * dk + c] * w[i * nc + n];"),
+    "generic_drops_decay": ("double s = d * S[c * nc + n];", "double s = S[c * nc + n];"),
+    "generic_drops_write": ("for (int l = 0; l < p; ++l)\n", "for (int l = 0; l < 0; ++l)\n"),
+    "generic_swaps_A_and_B": ("s += Bt[(size_t)i * dk + c] * S[c * nc + n];",
+                              "s += At[(size_t)i * dk + c] * S[c * nc + n];"),
+    # GDN mode
+    "gdn_gate_on_write_too": ("S[c * nc + n] = gate * (S[c * nc + n] - bt * kt[c] * w[n])\n"
+                              "                                        + bt * kt[c] * vt[c0 + n];",
+                              "S[c * nc + n] = gate * (S[c * nc + n] - bt * kt[c] * w[n]\n"
+                              "                                        + bt * kt[c] * vt[c0 + n]);"),
+    "gdn_drops_erase": ("gate * (S[c * nc + n] - bt * kt[c] * w[n])", "gate * (S[c * nc + n])"),
+    # HDLA mode
+    "hdla_drops_first_erase": ("for (int n = 0; n < nc; ++n) S[c * nc + n] -= bt * kt[c] * w[n];\n"
+                               "                /* 2:",
+                               "for (int n = 0; n < nc; ++n) S[c * nc + n] -= 0.0 * w[n];\n"
+                               "                /* 2:"),
+    "hdla_write_sign": ("w[n] = s - vt[c0 + n];", "w[n] = s + vt[c0 + n];"),
+    "hdla_decay_inverted": ("const double lam = exp(lt[c]);", "const double lam = exp(-lt[c]);"),
+    # readout
+    "readout_before_update_index": ("double* ot = a->o + (size_t)t * dv + c0;",
+                                    "double* ot = a->o + (size_t)(t > 0 ? t - 1 : 0) * dv + c0;"),
+    "readout_uses_k_not_q": ("for (int c = 0; c < dk; ++c) s += S[c * nc + n] * qt[c];",
+                             "for (int c = 0; c < dk; ++c) s += S[c * nc + n] * (a->k ? a->k[(size_t)t * dk + c] : qt[c]);"),
+    "initial_state_ignored": ("S[i * nc + n] = a->S0 ? a->S0[(size_t)i * dv + c0 + n] : 0.0;",
+                              "S[i * nc + n] = 0.0;"),
+    "initial_state_transposed": ("S[i * nc + n] = a->S0 ? a->S0[(size_t)i * dv + c0 + n] : 0.0;",
+                                 "S[i * nc + n] = a->S0 ? a->S0[(size_t)(c0 + n) * dv + i % dv] : 0.0;"),
+}
+
+PIN_CALLS = [
+    lambda: pins.test_hand_worked_examples("gdn_two_tokens"),
+    lambda: pins.test_hand_worked_examples("hdla_two_tokens"),
+    lambda: pins.test_hand_worked_examples("generic_one_token"),
+    pins.test_no_decay_reduces_to_causal_linear_attention,
+    pins.test_diagonal_decay_reduces_to_gla,
+    pins.test_gdn_zero_beta_is_pure_gate,
+    pins.test_gdn_delta_rule_closed_form_same_key,
+    pins.test_hdla_reflection_without_forgetting_is_linear_attention,
+    pins.test_hdla_transition_is_similar_to_its_diagonal,
+    lambda: pins.test_explicit_transition_matrices("gdn"),
+    lambda: pins.test_explicit_transition_matrices("hdla"),
+    pins.test_generic_explicit_transition,
+]
+
+
+def _build_mutant(tmp_path, name, old, new):
+    text = open(SRC).read()
+    assert text.count(old) == 1, f"mutation anchor for {name} not unique/found"
+    src = tmp_path / f"{name}.c"
+    src.write_text(text.replace(old, new))
+    so = tmp_path / f"{name}.so"
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fopenmp", "-fPIC", "-shared", str(src), "-o", str(so), "-lm"],
+                   check=True)
+    lib = ctypes.CDLL(str(so))
+    dp = ctypes.POINTER(ctypes.c_double)
+    lib.oracle_forward.restype = ctypes.c_int
+    lib.oracle_forward.argtypes = [ctypes.c_int] * 8 + [dp] * 12 + [ctypes.c_int]
+    lib.oracle_max_threads.restype = ctypes.c_int
+    return lib
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path, monkeypatch):
+    old, new = MUTANTS[name]
+    lib = _build_mutant(tmp_path, name, old, new)
+    oracle._lib()                                  # make sure the real one is initialised first
+    monkeypatch.setattr(oracle, "_handle", lib)
+    caught = 0
+    for call in PIN_CALLS:
+        try:
+            call()
+        except AssertionError:
+            caught += 1
+    assert caught > 0, f"no pin failed for mutant {name}"
