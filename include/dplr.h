@@ -1,0 +1,147 @@
+/*
+ * dplr.h -- C ABI of libdplr: the chunkwise-parallel forward of linear attention
+ * with a diagonal-plus-low-rank (DPLR) decay, for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (per batch b and head h, state S in R^{dk x dv}, tokens t = 1..T):
+ *
+ *     S_t = (D_t - A_t B_t^T) S_{t-1} + K_t V_t^T,        o_t = S_t^T q_t
+ *
+ * is the general recurrence of "Householder-Diagonalized Linear Attention"
+ * (HDLA page, Key design 3, displayed equation), with A_t, B_t in R^{dk x r_ab},
+ * K_t in R^{dk x r_kv}, V_t in R^{dv x r_kv}, D_t diagonal. Two structured cases
+ * build the factors from (k, v, decay, beta) on the device:
+ *
+ *   DPLR_GDN   Gated DeltaNet, P_t = exp(g_t)(I - beta_t k_t k_t^T), write
+ *              beta_t k_t v_t^T (HLA page, Prerequisites and Method step 1).
+ *   DPLR_HDLA  P_t = (I - beta_t k_t k_t^T) Diag(lambda_t) (I - beta_t k_t k_t^T),
+ *              write beta_t k_t v_t^T (HDLA page, Key design 2).
+ *   DPLR_GENERIC  A, B, K, V and log(diag D) given directly (Key design 3).
+ *
+ * The readout uses the state after token t's update (o_t = S_t^T q_t); there is
+ * no 1/sqrt(dk) factor (pre-scale q if wanted). The state enters as S0 and
+ * leaves as S_T, so a sequence can be continued across calls.
+ *
+ * The method is the two-stage chunkwise algorithm of the HDLA page (Key design
+ * 3): stage 1 computes, for every chunk independently, its exact affine map
+ * S -> P_j S + c_j and its readout map (the rank-generalised WY/UT transform);
+ * stage 2 scans the chunk maps in order and reads out o.
+ *
+ * Layouts: every tensor is contiguous, row-major, on the device of `stream`.
+ *   q      [B,H,T,dk]   in_dtype
+ *   k      [B,H,T,dk]   in_dtype   (GDN, HDLA)
+ *   v      [B,H,T,dv]   in_dtype   (GDN, HDLA)
+ *   decay  fp32, log-space: GDN [B,H,T] (log gate g <= 0);
+ *          HDLA and GENERIC [B,H,T,dk] (log lambda; D_t = Diag(exp(decay_t)))
+ *   beta   [B,H,T]      fp32       (GDN, HDLA; ignored for GENERIC)
+ *   A, Bm  [B,H,T,r_ab,dk] in_dtype (GENERIC; row i is column i of A_t / B_t)
+ *   K      [B,H,T,r_kv,dk] in_dtype (GENERIC)
+ *   V      [B,H,T,r_kv,dv] in_dtype (GENERIC)
+ *   S0     [B,H,dk,dv]  fp32, may be NULL (zero initial state)
+ *   o      [B,H,T,dv]   fp32 (written)
+ *   S_T    [B,H,dk,dv]  fp32, may be NULL (final state not returned)
+ *
+ * Ownership: the caller allocates every buffer, including the workspace
+ * (size from dplr_la_workspace_size). The library allocates no device memory
+ * and keeps no state between calls, apart from per-device kernel attributes
+ * set once. All calls are asynchronous on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream). Calls that share a workspace must not overlap.
+ *
+ * Errors: argument, shape and alignment problems return a status code before
+ * anything is launched (nothing is written). A failed launch returns
+ * DPLR_ERR_CUDA. Every pointer must be 16-byte aligned.
+ *
+ * Supported sizes: dk, dv in {32, 64, 128}; chunk = 64; B, H >= 1; T >= 0 with
+ * B*H*T < 2^31; GDN has r_ab = r_kv = 1, HDLA r_ab = 2, r_kv = 1; GENERIC
+ * 1 <= r_ab <= 8 and 0 <= r_kv <= 8.
+ */
+#ifndef DPLR_H
+#define DPLR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DPLR_API __attribute__((visibility("default")))
+#else
+#define DPLR_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DPLR_OK = 0,
+    DPLR_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad shape or enum value */
+    DPLR_ERR_UNSUPPORTED = 2,   /* well-formed but outside the supported sizes */
+    DPLR_ERR_WORKSPACE = 3,     /* workspace pointer null or smaller than required */
+    DPLR_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
+    DPLR_ERR_TIMEOUT = 5        /* reserved: a bounded device-side wait gave up */
+} dplr_status;
+
+typedef enum { DPLR_GDN = 1, DPLR_HDLA = 2, DPLR_GENERIC = 3 } dplr_mode;
+typedef enum { DPLR_F32 = 0, DPLR_BF16 = 1 } dplr_dtype;
+
+/* Problem descriptor. r_ab / r_kv are fixed by the structured modes (GDN 1/1,
+ * HDLA 2/1) and must be given with those values. */
+typedef struct {
+    int32_t mode;      /* dplr_mode */
+    int32_t in_dtype;  /* dplr_dtype of q, k, v, A, Bm, K, V */
+    int32_t B, H, T;   /* batch, heads, sequence length */
+    int32_t dk, dv;    /* key / value head dimensions */
+    int32_t r_ab;      /* rank of the low-rank decay term A_t B_t^T */
+    int32_t r_kv;      /* rank of the write term K_t V_t^T */
+    int32_t chunk;     /* chunk length C of the chunkwise algorithm (64) */
+} dplr_desc;
+
+/* Bytes of device workspace dplr_la_forward needs for `desc`; 0 if `desc` is
+ * invalid or unsupported (call dplr_la_check for the reason). */
+DPLR_API size_t dplr_la_workspace_size(const dplr_desc* desc);
+
+/* Validates `desc` alone (no pointers). DPLR_OK if the shape is supported. */
+DPLR_API dplr_status dplr_la_check(const dplr_desc* desc);
+
+/* The whole forward: o and (optionally) S_T from the inputs and S0.
+ * Structured modes read q, k, v, decay, beta and ignore A, Bm, K, V;
+ * GENERIC reads q, decay, A, Bm, K (if r_kv > 0), V (if r_kv > 0) and ignores
+ * k, v, beta. */
+DPLR_API dplr_status dplr_la_forward(const dplr_desc* desc,
+                            const void* q, const void* k, const void* v,
+                            const float* decay, const float* beta,
+                            const void* A, const void* Bm, const void* K, const void* V,
+                            const float* S0, float* o, float* S_T,
+                            void* workspace, size_t ws_bytes, void* stream);
+
+/* Stage 1 alone (HDLA page, Key design 3, stage "compute each chunk's
+ * quantities in parallel"): per chunk, the cumulative decay, the factor build,
+ * the Gram blocks, the UT/WY triangular solve, and from them the chunk's affine
+ * map (P_j, c_j) and readout map (Q'_j, local output). Writes the maps to the
+ * workspace and each chunk's zero-initial-state output into o. Arguments as for
+ * dplr_la_forward. */
+DPLR_API dplr_status dplr_la_chunk_maps(const dplr_desc* desc,
+                               const void* q, const void* k, const void* v,
+                               const float* decay, const float* beta,
+                               const void* A, const void* Bm, const void* K, const void* V,
+                               float* o, void* workspace, size_t ws_bytes, void* stream);
+
+/* Stage 2 alone (HDLA page, Key design 3, "serially compute the chunk-state
+ * checkpoints"): scans the chunk maps written by dplr_la_chunk_maps in chunk
+ * order, S_j = P_j S_{j-1} + c_j from S0, adds each chunk's state readout
+ * Q'_j S_{j-1} into o and writes S_T. Must follow dplr_la_chunk_maps with the
+ * same descriptor and workspace on the same stream. */
+DPLR_API dplr_status dplr_la_state_scan(const dplr_desc* desc, const float* S0, float* o, float* S_T,
+                               void* workspace, size_t ws_bytes, void* stream);
+
+/* Human-readable name of a status code (static storage). */
+DPLR_API const char* dplr_status_string(dplr_status status);
+
+/* Number of CUDA kernels one dplr_la_forward launches for `desc` (0 if the
+ * descriptor is invalid). dplr_la_chunk_maps and dplr_la_state_scan each
+ * launch one. */
+DPLR_API int dplr_la_kernel_count(const dplr_desc* desc);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DPLR_H */

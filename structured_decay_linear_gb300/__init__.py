@@ -1,0 +1,13 @@
+"""Chunkwise-parallel forward of linear attention with a diagonal-plus-low-rank decay,
+as hand-written CUDA for GB300 (sm_103a) behind the C ABI of libdplr (include/dplr.h).
+
+``forward`` / ``Forward`` marshal torch device tensors into ``dplr_la_forward``;
+the C-ABI mirrors (``dplr_la_forward``, ``dplr_la_chunk_maps``, ...) take raw
+pointers. There is no CPU fallback: without libdplr.so the calls raise.
+"""
+
+from .dplr import (  # noqa: F401
+    DPLR_BF16, DPLR_F32, DPLR_GDN, DPLR_GENERIC, DPLR_HDLA, DPLR_OK, DplrError, Forward, LIB_PATH,
+    dplr_desc, dplr_la_check, dplr_la_chunk_maps, dplr_la_forward, dplr_la_kernel_count, dplr_la_state_scan,
+    dplr_la_workspace_size, forward, library, make_desc, status_string,
+)

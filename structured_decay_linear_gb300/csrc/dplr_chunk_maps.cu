@@ -1,0 +1,338 @@
+// Stage 1 of the chunkwise DPLR forward: one CTA per (head, WY block).
+//
+// For a block of C_w tokens with state S_0 at its start, the recurrence
+// S_t = (D_t - A_t B_t^T) S_{t-1} + K_t V_t^T is rewritten with the cumulative
+// log-decay G_t = sum_{s<=t} log d_s and the scaled state X_t = e^{-G_t} S_t:
+//
+//   X_t = X_{t-1} - A~_t E_t + K~_t V_t^T,   E_t = B~_t^T X_{t-1}  (r x dv)
+//   A~_s = e^{-G_s} A_s,  K~_s = e^{-G_s} K_s,  B~_t = e^{G_{t-1}} B_t.
+//
+// Stacking the r rows of every token, E solves the unit lower-triangular system
+// (I + L) E = B~ S_0 + G_BK V, with L = strict_block_tril(B~ A~^T) and
+// G_BK = strict_block_tril(B~ K~^T) -- the rank-generalised WY/UT form whose
+// block-triangular operator treats each r x r block as one element (HDLA page,
+// Key design 3, the triu_{r1 x r2} operator). With Y = (I+L)^{-1} B~ and
+// U = (I+L)^{-1} G_BK V the block's exact affine and readout maps are
+//
+//   S_end = P S_0 + c,   P = Diag(gamma) - A^^T Y,   c = -A^^T U + K^^T V
+//   o_t   = Q'_t S_0 + O_t,  Q' = q~ - (q~ A~^T (.) M) Y,
+//                             O  = -(q~ A~^T (.) M) U + (q~ K~^T (.) M) V
+//
+// where gamma = e^{G_C}, A^ = e^{G_C - G_s} A_s, K^ likewise, q~_t = e^{G_t} q_t
+// and M is the inclusive causal mask. In the structured modes the write term is
+// folded into A (GDN: A = beta k, B = e^g k, K V^T = A v^T; HDLA: A = [k, Lk],
+// B = [beta Lk - beta^2 (k^T L k) k, beta k], K V^T = A_0 (beta v)^T), so the
+// right-hand side is -W instead of G_BK V and no K~ term exists.
+//
+// The exponentials are anchored at a = G_C / 2 per channel: every scaled
+// factor carries e^{+-(G - a)}, so products that cancel the anchor (L, Q'A~^T,
+// A^^T Y ...) are formed from factors within e^{+-|G_C|/2} instead of e^{|G_C|}.
+#include <cuda_bf16.h>
+
+#include "dplr_internal.h"
+
+namespace dplr {
+namespace {
+
+template <class T> __device__ __forceinline__ float ld(const T* p, size_t i);
+template <> __device__ __forceinline__ float ld<float>(const float* p, size_t i) { return p[i]; }
+template <> __device__ __forceinline__ float ld<__nv_bfloat16>(const __nv_bfloat16* p, size_t i) {
+    return __bfloat162float(p[i]);
+}
+
+// C(m, n) = sum_k a(m, k) b(k, n) over an M x N output, TM x TN register tiles per
+// thread (M % TM == 0, N % TN == 0), result handed to epi(m, n, value).
+template <int TM, int TN, class FA, class FB, class Epi>
+__device__ __forceinline__ void block_gemm(int M, int N, int K, FA a, FB b, Epi epi) {
+    const int tiles_n = N / TN;
+    const int tiles = (M / TM) * tiles_n;
+    for (int tile = threadIdx.x; tile < tiles; tile += blockDim.x) {
+        const int m0 = (tile / tiles_n) * TM, n0 = (tile % tiles_n) * TN;
+        float acc[TM][TN];
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+        for (int kk = 0; kk < K; ++kk) {
+            float av[TM], bv[TN];
+#pragma unroll
+            for (int i = 0; i < TM; ++i) av[i] = a(m0 + i, kk);
+#pragma unroll
+            for (int j = 0; j < TN; ++j) bv[j] = b(kk, n0 + j);
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        }
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) epi(m0 + i, n0 + j, acc[i][j]);
+    }
+}
+
+// Shared-memory carve-up (floats) for one WY block; identical on host and device.
+struct PrepLayout {
+    int lg, G, beta, ea, egca, gam, At, Bt, Qt, Z, L, QA, Kt, Vs, GBK, QK, total;
+    __host__ __device__ PrepLayout(int mode, int dk, int dv, int cw, int r, int p) {
+        const int dkg = (mode == DPLR_GDN) ? 1 : dk;
+        const int cr = cw * r, cp = cw * p;
+        int o = 0;
+        lg = o;   o += cw * dkg;
+        G = o;    o += cw * dkg;
+        beta = o; o += cw;
+        ea = o;   o += dk;
+        egca = o; o += dk;
+        gam = o;  o += dk;
+        At = o;   o += cr * dk;
+        Bt = o;   o += cr * dk;
+        Qt = o;   o += cw * dk;
+        Z = o;    o += cr * dv;
+        L = o;    o += cr * cr;
+        QA = o;   o += cw * cr;
+        Kt = o;   o += cp * dk;
+        Vs = o;   o += cp * dv;
+        GBK = o;  o += cr * cp;
+        QK = o;   o += cw * cp;
+        total = o;
+    }
+};
+
+template <int MODE, class IT>
+__global__ void __launch_bounds__(kPrepThreads)
+chunk_maps_kernel(Plan pl, ChunkMapArgs args) {
+    extern __shared__ float sm[];
+    const int dk = pl.dk, dv = pl.dv, cw = pl.cw, T = pl.T;
+    const int R = (MODE == DPLR_GDN) ? 1 : (MODE == DPLR_HDLA ? 2 : pl.r);
+    const int P = (MODE == DPLR_GENERIC) ? pl.p : 0;
+    const int cr = cw * R, cp = cw * P;
+    const int dkg = (MODE == DPLR_GDN) ? 1 : dk;
+    const PrepLayout Ly(MODE, dk, dv, cw, R, P);
+    float *lg = sm + Ly.lg, *G = sm + Ly.G, *bet = sm + Ly.beta;
+    float *ea = sm + Ly.ea, *egca = sm + Ly.egca, *gam = sm + Ly.gam;
+    float *At = sm + Ly.At, *Bt = sm + Ly.Bt, *Qt = sm + Ly.Qt, *Z = sm + Ly.Z;
+    float *L = sm + Ly.L, *QA = sm + Ly.QA, *Kt = sm + Ly.Kt, *Vs = sm + Ly.Vs;
+    float *GBK = sm + Ly.GBK, *QK = sm + Ly.QK;
+
+    const int blk = blockIdx.x % pl.nb;
+    const size_t bh = blockIdx.x / pl.nb;
+    const int t0 = blk * cw;
+    const size_t tok0 = bh * (size_t)T + t0;   // flat token index of the block's first token
+    const int tid = threadIdx.x, nth = blockDim.x;
+
+    // ---- a1/a2: stage decay and beta; inclusive cumulative log-decay per channel.
+    for (int i = tid; i < cw * dkg; i += nth) {
+        const int t = i / dkg, c = i % dkg;
+        lg[i] = (t0 + t < T) ? args.decay[(tok0 + t) * dkg + c] : 0.f;   // padding: identity
+    }
+    if (MODE != DPLR_GENERIC)
+        for (int t = tid; t < cw; t += nth) bet[t] = (t0 + t < T) ? args.beta[tok0 + t] : 0.f;
+    __syncthreads();
+    for (int c = tid; c < dkg; c += nth) {
+        float s = 0.f;
+        for (int t = 0; t < cw; ++t) { s += lg[t * dkg + c]; G[t * dkg + c] = s; }
+    }
+    __syncthreads();
+    for (int c = tid; c < dk; c += nth) {
+        const float gc = G[(cw - 1) * dkg + (MODE == DPLR_GDN ? 0 : c)];
+        const float a = 0.5f * gc;
+        ea[c] = expf(a);
+        egca[c] = expf(gc - a);
+        gam[c] = expf(gc);
+    }
+    // ---- a3: factor build (anchored, decay-scaled rows).
+    // G'_t = G_t - a (inclusive), Gx'_t = G_{t-1} - a (exclusive).
+    auto Gi = [&](int t, int c) { return G[t * dkg + (MODE == DPLR_GDN ? 0 : c)]; };
+    auto Gx = [&](int t, int c) { return t > 0 ? Gi(t - 1, c) : 0.f; };
+    auto anc = [&](int c) { return 0.5f * G[(cw - 1) * dkg + (MODE == DPLR_GDN ? 0 : c)]; };
+    const IT* qp = static_cast<const IT*>(args.q);
+    for (int i = tid; i < cw * dk; i += nth) {
+        const int t = i / dk, c = i % dk;
+        const float x = (t0 + t < T) ? ld(qp, (tok0 + t) * dk + c) : 0.f;
+        Qt[i] = x * expf(Gi(t, c) - anc(c));
+    }
+    if (MODE == DPLR_GDN) {
+        const IT* kp = static_cast<const IT*>(args.k);
+        const IT* vp = static_cast<const IT*>(args.v);
+        for (int i = tid; i < cw * dk; i += nth) {
+            const int t = i / dk, c = i % dk;
+            const float kk = (t0 + t < T) ? ld(kp, (tok0 + t) * dk + c) : 0.f;
+            const float gp = Gi(t, c) - anc(c);
+            At[i] = expf(-gp) * bet[t] * kk;   // A = beta k
+            Bt[i] = expf(gp) * kk;             // e^{G_{t-1}} B_t with B = e^{g} k
+        }
+        for (int i = tid; i < cw * dv; i += nth) {
+            const int t = i / dv, n = i % dv;
+            Z[i] = (t0 + t < T) ? -ld(vp, (tok0 + t) * dv + n) : 0.f;   // -W, W = v
+        }
+    } else if (MODE == DPLR_HDLA) {
+        const IT* kp = static_cast<const IT*>(args.k);
+        const IT* vp = static_cast<const IT*>(args.v);
+        // c_t = k^T Lambda k per token: one warp per token.
+        float* cdot = L;   // scratch, L is filled later
+        const int warp = tid / 32, lane = tid % 32, nwarp = nth / 32;
+        for (int t = warp; t < cw; t += nwarp) {
+            float s = 0.f;
+            if (t0 + t < T)
+                for (int c = lane; c < dk; c += 32) {
+                    const float kk = ld(kp, (tok0 + t) * dk + c);
+                    s += kk * kk * expf(lg[t * dk + c]);
+                }
+            for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+            if (lane == 0) cdot[t] = s;
+        }
+        __syncthreads();
+        for (int i = tid; i < cw * dk; i += nth) {
+            const int t = i / dk, c = i % dk;
+            const float kk = (t0 + t < T) ? ld(kp, (tok0 + t) * dk + c) : 0.f;
+            const float u = expf(lg[i]) * kk;             // Lambda k
+            const float b = bet[t];
+            const float ei = expf(-(Gi(t, c) - anc(c)));  // e^{-G'_t}
+            const float ex = expf(Gx(t, c) - anc(c));     // e^{G'_{t-1}}
+            At[(2 * t) * dk + c] = ei * kk;
+            At[(2 * t + 1) * dk + c] = ei * u;
+            Bt[(2 * t) * dk + c] = ex * (b * u - b * b * cdot[t] * kk);
+            Bt[(2 * t + 1) * dk + c] = ex * b * kk;
+        }
+        for (int i = tid; i < cw * dv; i += nth) {
+            const int t = i / dv, n = i % dv;
+            Z[(2 * t) * dv + n] = (t0 + t < T) ? -bet[t] * ld(vp, (tok0 + t) * dv + n) : 0.f;
+            Z[(2 * t + 1) * dv + n] = 0.f;
+        }
+    } else {
+        const IT* Ap = static_cast<const IT*>(args.A);
+        const IT* Bp = static_cast<const IT*>(args.Bm);
+        const IT* Kp = static_cast<const IT*>(args.K);
+        const IT* Vp = static_cast<const IT*>(args.V);
+        for (int i = tid; i < cr * dk; i += nth) {
+            const int row = i / dk, c = i % dk, t = row / R, j = row % R;
+            const bool ok = t0 + t < T;
+            const size_t src = ((tok0 + t) * R + j) * dk + c;
+            At[i] = ok ? expf(-(Gi(t, c) - anc(c))) * ld(Ap, src) : 0.f;
+            Bt[i] = ok ? expf(Gx(t, c) - anc(c)) * ld(Bp, src) : 0.f;
+        }
+        for (int i = tid; i < cp * dk; i += nth) {
+            const int row = i / dk, c = i % dk, t = row / P, l = row % P;
+            Kt[i] = (t0 + t < T) ? expf(-(Gi(t, c) - anc(c))) * ld(Kp, ((tok0 + t) * P + l) * dk + c) : 0.f;
+        }
+        for (int i = tid; i < cp * dv; i += nth) {
+            const int row = i / dv, n = i % dv, t = row / P, l = row % P;
+            Vs[i] = (t0 + t < T) ? ld(Vp, ((tok0 + t) * P + l) * dv + n) : 0.f;
+        }
+    }
+    __syncthreads();
+
+    // ---- a4: Gram blocks. L = strict_block_tril(B~ A~^T); QA = tril_incl(q~ A~^T).
+    block_gemm<4, 4>(cr, cr, dk,
+        [&](int m, int kk) { return Bt[m * dk + kk]; },
+        [&](int kk, int n) { return At[n * dk + kk]; },
+        [&](int m, int n, float x) { L[m * cr + n] = (n / R < m / R) ? x : 0.f; });
+    block_gemm<4, 4>(cw, cr, dk,
+        [&](int m, int kk) { return Qt[m * dk + kk]; },
+        [&](int kk, int n) { return At[n * dk + kk]; },
+        [&](int m, int n, float x) { QA[m * cr + n] = (n / R <= m) ? x : 0.f; });
+    if (MODE == DPLR_GENERIC && P > 0) {
+        block_gemm<4, 4>(cr, cp, dk,
+            [&](int m, int kk) { return Bt[m * dk + kk]; },
+            [&](int kk, int n) { return Kt[n * dk + kk]; },
+            [&](int m, int n, float x) { GBK[m * cp + n] = (n / P < m / R) ? x : 0.f; });
+        block_gemm<4, 4>(cw, cp, dk,
+            [&](int m, int kk) { return Qt[m * dk + kk]; },
+            [&](int kk, int n) { return Kt[n * dk + kk]; },
+            [&](int m, int n, float x) { QK[m * cp + n] = (n / P <= m) ? x : 0.f; });
+    }
+    __syncthreads();
+    if (MODE == DPLR_GENERIC) {
+        // Right-hand side of the value part: Z = G_BK V (zero when r_kv = 0).
+        if (P > 0) {
+            block_gemm<4, 4>(cr, dv, cp,
+                [&](int m, int kk) { return GBK[m * cp + kk]; },
+                [&](int kk, int n) { return Vs[kk * dv + n]; },
+                [&](int m, int n, float x) { Z[m * dv + n] = x; });
+        } else {
+            for (int i = tid; i < cr * dv; i += nth) Z[i] = 0.f;
+        }
+        __syncthreads();
+    }
+
+    // ---- a5: UT/WY solve (I + L) [Y' | U] = [B~' | Z], in place, one column per thread.
+    for (int col = tid; col < dk + dv; col += nth) {
+        float* x = (col < dk) ? (Bt + col) : (Z + (col - dk));
+        const int ld_x = (col < dk) ? dk : dv;
+        for (int row = R; row < cr; ++row) {
+            const int lim = (row / R) * R;   // rows of earlier tokens only
+            float s = x[row * ld_x];
+            for (int j = 0; j < lim; ++j) s = fmaf(-L[row * cr + j], x[j * ld_x], s);
+            x[row * ld_x] = s;
+        }
+    }
+    __syncthreads();
+
+    // ---- outputs: chunk transition, offset, readout map and zero-state output.
+    const size_t unit = bh * (size_t)pl.nb + blk;
+    float* Pout = args.Pm + unit * (size_t)dk * dk;
+    float* Cout = args.Cm + unit * (size_t)dk * dv;
+    float* Qout = args.Qm + unit * (size_t)cw * dk;
+    // P[i][k] = gamma_i delta_ik - e^{G_C,i - a_i} (A~'^T Y')[i][k] e^{a_k}
+    block_gemm<4, 4>(dk, dk, cr,
+        [&](int m, int kk) { return At[kk * dk + m]; },
+        [&](int kk, int n) { return Bt[kk * dk + n]; },
+        [&](int m, int n, float x) {
+            Pout[m * dk + n] = (m == n ? gam[m] : 0.f) - egca[m] * x * ea[n];
+        });
+    // c[i][n] = e^{G_C,i - a_i} (-(A~'^T U) + K~'^T V)[i][n]
+    block_gemm<4, 4>(dk, dv, cr + cp,
+        [&](int m, int kk) { return kk < cr ? -At[kk * dk + m] : Kt[(kk - cr) * dk + m]; },
+        [&](int kk, int n) { return kk < cr ? Z[kk * dv + n] : Vs[(kk - cr) * dv + n]; },
+        [&](int m, int n, float x) { Cout[m * dv + n] = egca[m] * x; });
+    // Q'[t][k] = (q~'_t - sum QA Y')[k] e^{a_k}
+    block_gemm<4, 4>(cw, dk, cr,
+        [&](int m, int kk) { return QA[m * cr + kk]; },
+        [&](int kk, int n) { return Bt[kk * dk + n]; },
+        [&](int m, int n, float x) { Qout[m * dk + n] = (Qt[m * dk + n] - x) * ea[n]; });
+    // O[t][n] = -(QA U)[t][n] + (QK V)[t][n]   -> o (zero-initial-state part)
+    block_gemm<4, 4>(cw, dv, cr + cp,
+        [&](int m, int kk) { return kk < cr ? -QA[m * cr + kk] : QK[m * cp + (kk - cr)]; },
+        [&](int kk, int n) { return kk < cr ? Z[kk * dv + n] : Vs[(kk - cr) * dv + n]; },
+        [&](int m, int n, float x) {
+            if (t0 + m < T) args.o[(tok0 + m) * dv + n] = x;
+        });
+}
+
+template <int MODE, class IT>
+cudaError_t launch_mode(const Plan& pl, const ChunkMapArgs& a, cudaStream_t s) {
+    const size_t smem = prep_smem_bytes(pl);
+    auto kern = chunk_maps_kernel<MODE, IT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const long long grid = (long long)pl.BH * pl.nb;
+    kern<<<(unsigned)grid, kPrepThreads, smem, s>>>(pl, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t prep_smem_bytes(const Plan& pl) {
+    const int R = pl.mode == DPLR_GDN ? 1 : (pl.mode == DPLR_HDLA ? 2 : pl.r);
+    const int P = pl.mode == DPLR_GENERIC ? pl.p : 0;
+    PrepLayout Ly(pl.mode, pl.dk, pl.dv, pl.cw, R, P);
+    return (size_t)Ly.total * sizeof(float);
+}
+
+cudaError_t launch_chunk_maps(const Plan& pl, const ChunkMapArgs& a, cudaStream_t s) {
+    if (pl.T == 0) return cudaSuccess;
+    if (pl.bf16) {
+        switch (pl.mode) {
+            case DPLR_GDN: return launch_mode<DPLR_GDN, __nv_bfloat16>(pl, a, s);
+            case DPLR_HDLA: return launch_mode<DPLR_HDLA, __nv_bfloat16>(pl, a, s);
+            default: return launch_mode<DPLR_GENERIC, __nv_bfloat16>(pl, a, s);
+        }
+    }
+    switch (pl.mode) {
+        case DPLR_GDN: return launch_mode<DPLR_GDN, float>(pl, a, s);
+        case DPLR_HDLA: return launch_mode<DPLR_HDLA, float>(pl, a, s);
+        default: return launch_mode<DPLR_GENERIC, float>(pl, a, s);
+    }
+}
+
+}  // namespace dplr

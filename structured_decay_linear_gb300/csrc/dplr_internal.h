@@ -1,0 +1,51 @@
+// Internal declarations shared by the libdplr translation units (not part of the ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/dplr.h"
+
+namespace dplr {
+
+// Largest stacked rank-row count C_w * max(r_ab, r_kv) a WY block may hold. The
+// chunk given in the descriptor is split into WY blocks of C_w tokens so that
+// the Gram / triangular-solve tiles stay within shared memory.
+constexpr int kMaxStackedRows = 64;
+constexpr int kPrepThreads = 256;
+constexpr int kScanThreads = 256;
+constexpr int kScanCols = 32;  // state columns per scan CTA (dv split)
+
+// Everything the launches need, derived from a validated descriptor.
+struct Plan {
+    int mode, bf16;
+    int BH, T, dk, dv, r, p;   // p = 0 in the structured modes (write term folded into A)
+    int cw;                    // WY block length in tokens
+    int nb;                    // WY blocks per head = ceil(T / cw)
+    size_t off_P, off_c, off_Q, ws_bytes;
+};
+
+// Per-launch arguments of the chunk-map kernel.
+struct ChunkMapArgs {
+    const void* q; const void* k; const void* v;
+    const float* decay; const float* beta;
+    const void* A; const void* Bm; const void* K; const void* V;
+    float* o;
+    float* Pm;  // [BH, nb, dk, dk]   chunk transition P_j
+    float* Cm;  // [BH, nb, dk, dv]   chunk offset c_j
+    float* Qm;  // [BH, nb, cw, dk]   chunk readout Q'_j
+};
+
+struct ScanArgs {
+    const float* S0; float* o; float* ST;
+    const float* Pm; const float* Cm; const float* Qm;
+};
+
+dplr_status make_plan(const dplr_desc* d, Plan* plan);
+size_t prep_smem_bytes(const Plan& pl);
+size_t scan_smem_bytes(const Plan& pl);
+cudaError_t launch_chunk_maps(const Plan& pl, const ChunkMapArgs& a, cudaStream_t s);
+cudaError_t launch_state_scan(const Plan& pl, const ScanArgs& a, cudaStream_t s);
+
+}  // namespace dplr

@@ -1,0 +1,220 @@
+"""Thin ctypes binding of libdplr (argument marshalling only).
+
+Every step of the forward runs in the CUDA kernels of libdplr.so; PyTorch only
+provides device memory and the stream. If the library is missing the calls
+raise: there is no CPU or PyTorch fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdplr.so")
+
+DPLR_OK, DPLR_ERR_INVALID_ARG, DPLR_ERR_UNSUPPORTED, DPLR_ERR_WORKSPACE, DPLR_ERR_CUDA, DPLR_ERR_TIMEOUT = range(6)
+DPLR_GDN, DPLR_HDLA, DPLR_GENERIC = 1, 2, 3
+DPLR_F32, DPLR_BF16 = 0, 1
+MODES = {"gdn": DPLR_GDN, "hdla": DPLR_HDLA, "generic": DPLR_GENERIC}
+
+
+class dplr_desc(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int32), ("in_dtype", ctypes.c_int32), ("B", ctypes.c_int32),
+                ("H", ctypes.c_int32), ("T", ctypes.c_int32), ("dk", ctypes.c_int32), ("dv", ctypes.c_int32),
+                ("r_ab", ctypes.c_int32), ("r_kv", ctypes.c_int32), ("chunk", ctypes.c_int32)]
+
+
+class DplrError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)}")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+_vp = ctypes.c_void_p
+
+
+def library() -> ctypes.CDLL:
+    """Loads libdplr.so (built in-tree by ``__graft_entry__.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+            lib = ctypes.CDLL(LIB_PATH)
+            dp = ctypes.POINTER(dplr_desc)
+            lib.dplr_la_workspace_size.restype = ctypes.c_size_t
+            lib.dplr_la_workspace_size.argtypes = [dp]
+            lib.dplr_la_check.restype = ctypes.c_int
+            lib.dplr_la_check.argtypes = [dp]
+            lib.dplr_la_kernel_count.restype = ctypes.c_int
+            lib.dplr_la_kernel_count.argtypes = [dp]
+            lib.dplr_status_string.restype = ctypes.c_char_p
+            lib.dplr_status_string.argtypes = [ctypes.c_int]
+            lib.dplr_la_forward.restype = ctypes.c_int
+            lib.dplr_la_forward.argtypes = [dp] + [_vp] * 12 + [_vp, ctypes.c_size_t, _vp]
+            lib.dplr_la_chunk_maps.restype = ctypes.c_int
+            lib.dplr_la_chunk_maps.argtypes = [dp] + [_vp] * 10 + [_vp, ctypes.c_size_t, _vp]
+            lib.dplr_la_state_scan.restype = ctypes.c_int
+            lib.dplr_la_state_scan.argtypes = [dp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return library().dplr_status_string(int(status)).decode()
+
+
+def make_desc(mode: str | int, in_dtype, B: int, H: int, T: int, dk: int, dv: int,
+              r_ab: Optional[int] = None, r_kv: Optional[int] = None, chunk: int = 64) -> dplr_desc:
+    m = MODES[mode] if isinstance(mode, str) else int(mode)
+    if in_dtype in (torch.bfloat16, "bf16", DPLR_BF16):
+        dt = DPLR_BF16
+    elif in_dtype in (torch.float32, "f32", DPLR_F32):
+        dt = DPLR_F32
+    else:
+        raise ValueError(f"unsupported input dtype {in_dtype}")
+    if r_ab is None:
+        r_ab = {DPLR_GDN: 1, DPLR_HDLA: 2}.get(m, 1)
+    if r_kv is None:
+        r_kv = 1
+    return dplr_desc(m, dt, B, H, T, dk, dv, r_ab, r_kv, chunk)
+
+
+# ----------------------------------------------------------------------------
+# C-ABI mirrors (raw pointers as Python ints, stream as an int handle).
+# ----------------------------------------------------------------------------
+
+def dplr_la_workspace_size(desc: dplr_desc) -> int:
+    return int(library().dplr_la_workspace_size(ctypes.byref(desc)))
+
+
+def dplr_la_check(desc: dplr_desc) -> int:
+    return int(library().dplr_la_check(ctypes.byref(desc)))
+
+
+def dplr_la_kernel_count(desc: dplr_desc) -> int:
+    return int(library().dplr_la_kernel_count(ctypes.byref(desc)))
+
+
+def dplr_la_forward(desc, q, k, v, decay, beta, A, Bm, K, V, S0, o, S_T, workspace, ws_bytes, stream) -> int:
+    return int(library().dplr_la_forward(ctypes.byref(desc), q, k, v, decay, beta, A, Bm, K, V, S0, o, S_T,
+                                         workspace, ctypes.c_size_t(ws_bytes), stream))
+
+
+def dplr_la_chunk_maps(desc, q, k, v, decay, beta, A, Bm, K, V, o, workspace, ws_bytes, stream) -> int:
+    return int(library().dplr_la_chunk_maps(ctypes.byref(desc), q, k, v, decay, beta, A, Bm, K, V, o,
+                                            workspace, ctypes.c_size_t(ws_bytes), stream))
+
+
+def dplr_la_state_scan(desc, S0, o, S_T, workspace, ws_bytes, stream) -> int:
+    return int(library().dplr_la_state_scan(ctypes.byref(desc), S0, o, S_T, workspace,
+                                            ctypes.c_size_t(ws_bytes), stream))
+
+
+# ----------------------------------------------------------------------------
+# Tensor-level wrapper.
+# ----------------------------------------------------------------------------
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _need(t, name, device, dtype, shape):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+class Forward:
+    """Prepared forward for one descriptor: owns the output and workspace tensors so that
+    repeated calls (benchmarks, CUDA graphs) allocate nothing."""
+
+    def __init__(self, mode: str, in_dtype: torch.dtype, B: int, H: int, T: int, dk: int, dv: int,
+                 r_ab: Optional[int] = None, r_kv: Optional[int] = None, chunk: int = 64,
+                 device: Optional[torch.device] = None):
+        self.desc = make_desc(mode, in_dtype, B, H, T, dk, dv, r_ab, r_kv, chunk)
+        st = dplr_la_check(self.desc)
+        if st != DPLR_OK:
+            raise DplrError(st, "dplr_la_check")
+        self.mode, self.in_dtype = MODES[mode] if isinstance(mode, str) else mode, in_dtype
+        self.B, self.H, self.T, self.dk, self.dv = B, H, T, dk, dv
+        self.r_ab, self.r_kv = self.desc.r_ab, self.desc.r_kv
+        self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        self.ws_bytes = dplr_la_workspace_size(self.desc)
+        self.workspace = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=self.device)
+        self.o = torch.empty((B, H, T, dv), dtype=torch.float32, device=self.device)
+        self.S_T = torch.empty((B, H, dk, dv), dtype=torch.float32, device=self.device)
+        self.kernels = dplr_la_kernel_count(self.desc)
+
+    def _check(self, q, k, v, decay, beta, A, Bm, K, V, S0):
+        B, H, T, dk, dv, dev, dt = self.B, self.H, self.T, self.dk, self.dv, self.device, self.in_dtype
+        _need(q, "q", dev, dt, (B, H, T, dk))
+        if self.mode == DPLR_GENERIC:
+            _need(decay, "decay", dev, torch.float32, (B, H, T, dk))
+            _need(A, "A", dev, dt, (B, H, T, self.r_ab, dk))
+            _need(Bm, "Bm", dev, dt, (B, H, T, self.r_ab, dk))
+            if self.r_kv > 0:
+                _need(K, "K", dev, dt, (B, H, T, self.r_kv, dk))
+                _need(V, "V", dev, dt, (B, H, T, self.r_kv, dv))
+        else:
+            _need(k, "k", dev, dt, (B, H, T, dk))
+            _need(v, "v", dev, dt, (B, H, T, dv))
+            _need(decay, "decay", dev, torch.float32, (B, H, T) if self.mode == DPLR_GDN else (B, H, T, dk))
+            _need(beta, "beta", dev, torch.float32, (B, H, T))
+        if S0 is not None:
+            _need(S0, "S0", dev, torch.float32, (B, H, dk, dv))
+
+    def __call__(self, q, k=None, v=None, decay=None, beta=None, A=None, Bm=None, K=None, V=None, S0=None,
+                 stream: Optional[torch.cuda.Stream] = None, check: bool = True) -> Tuple[torch.Tensor, torch.Tensor]:
+        if check:
+            self._check(q, k, v, decay, beta, A, Bm, K, V, S0)
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        st = dplr_la_forward(self.desc, _ptr(q), _ptr(k), _ptr(v), _ptr(decay), _ptr(beta), _ptr(A), _ptr(Bm),
+                             _ptr(K), _ptr(V), _ptr(S0), _ptr(self.o), _ptr(self.S_T), _ptr(self.workspace),
+                             self.ws_bytes, s.cuda_stream)
+        if st != DPLR_OK:
+            raise DplrError(st, "dplr_la_forward")
+        return self.o, self.S_T
+
+    def chunk_maps(self, q, k=None, v=None, decay=None, beta=None, A=None, Bm=None, K=None, V=None,
+                   stream: Optional[torch.cuda.Stream] = None):
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        st = dplr_la_chunk_maps(self.desc, _ptr(q), _ptr(k), _ptr(v), _ptr(decay), _ptr(beta), _ptr(A), _ptr(Bm),
+                                _ptr(K), _ptr(V), _ptr(self.o), _ptr(self.workspace), self.ws_bytes, s.cuda_stream)
+        if st != DPLR_OK:
+            raise DplrError(st, "dplr_la_chunk_maps")
+
+    def state_scan(self, S0=None, stream: Optional[torch.cuda.Stream] = None):
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        st = dplr_la_state_scan(self.desc, _ptr(S0), _ptr(self.o), _ptr(self.S_T), _ptr(self.workspace),
+                                self.ws_bytes, s.cuda_stream)
+        if st != DPLR_OK:
+            raise DplrError(st, "dplr_la_state_scan")
+        return self.o, self.S_T
+
+
+def forward(mode: str, q, k=None, v=None, decay=None, beta=None, A=None, Bm=None, K=None, V=None, S0=None,
+            chunk: int = 64) -> Tuple[torch.Tensor, torch.Tensor]:
+    """One-shot forward on device tensors; returns fresh (o [B,H,T,dv] fp32, S_T [B,H,dk,dv] fp32)."""
+    B, H, T, dk = q.shape
+    if mode == "generic":
+        r_ab, r_kv = A.shape[3], (K.shape[3] if K is not None else 0)
+        dv = V.shape[4] if V is not None else S0.shape[3]
+    else:
+        r_ab, r_kv, dv = None, None, v.shape[3]
+    f = Forward(mode, q.dtype, B, H, T, dk, dv, r_ab, r_kv, chunk, device=q.device)
+    return f(q, k, v, decay, beta, A, Bm, K, V, S0)

@@ -1,0 +1,159 @@
+"""Host-side tests of the C ABI (no GPU): the library loads, exports every symbol
+declared in include/dplr.h, validates descriptors and rejects bad arguments before
+launching anything."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dplr.h")
+
+
+@pytest.fixture(scope="module")
+def sdl():
+    from structured_decay_linear_gb300 import build as nvbuild
+    nvbuild.build()
+    import structured_decay_linear_gb300 as s
+    s.library()
+    return s
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"DPLR_API\s+[\w\s\*]*?\b(dplr_\w+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    syms = declared_symbols()
+    for name in ("dplr_la_forward", "dplr_la_workspace_size", "dplr_status_string", "dplr_la_chunk_maps",
+                 "dplr_la_state_scan", "dplr_la_check", "dplr_la_kernel_count"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(sdl):
+    lib = sdl.library()
+    for name in declared_symbols():
+        assert hasattr(lib, name), f"{name} declared in dplr.h but not exported"
+    out = subprocess.run(["nm", "-D", "--defined-only", sdl.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (dplr_\w+)", out))
+    assert set(declared_symbols()) == exported, f"exported {sorted(exported)} vs declared {declared_symbols()}"
+
+
+def test_header_compiles_as_c():
+    src = '#include "dplr.h"\nint main(void){ dplr_desc d; (void)d; return (int)sizeof(dplr_desc) - 40; }\n'
+    path = "/tmp/_dplr_hdr_test.c"
+    with open(path, "w") as f:
+        f.write(src)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), path, "-o",
+                    "/tmp/_dplr_hdr_test"], check=True)
+    assert subprocess.run(["/tmp/_dplr_hdr_test"]).returncode == 0
+
+
+def test_status_strings(sdl):
+    for code in range(6):
+        assert sdl.status_string(code).startswith("DPLR_")
+    assert "unknown" in sdl.status_string(99)
+
+
+@pytest.mark.parametrize("mode,dt,B,H,T,dk,dv,r,p,expect", [
+    ("gdn", "f32", 1, 2, 256, 32, 32, 1, 1, 0),
+    ("hdla", "bf16", 4, 16, 4096, 128, 128, 2, 1, 0),
+    ("generic", "f32", 2, 8, 8192, 64, 64, 4, 2, 0),
+    ("generic", "bf16", 1, 1, 10, 128, 64, 8, 8, 0),
+    ("generic", "f32", 1, 1, 0, 32, 32, 1, 0, 0),
+    ("gdn", "f32", 1, 1, 8, 48, 32, 1, 1, 2),       # dk not in {32, 64, 128}
+    ("gdn", "f32", 1, 1, 8, 32, 256, 1, 1, 2),      # dv too large
+    ("gdn", "f32", 1, 1, 8, 32, 32, 2, 1, 1),       # GDN rank is fixed
+    ("hdla", "f32", 1, 1, 8, 32, 32, 1, 1, 1),      # HDLA rank is fixed
+    ("generic", "f32", 1, 1, 8, 32, 32, 9, 1, 2),   # rank above 8
+    ("generic", "f32", 1, 1, 8, 32, 32, 0, 1, 2),   # generic needs r_ab >= 1
+    ("gdn", "f32", 0, 1, 8, 32, 32, 1, 1, 1),       # empty batch
+    ("gdn", "f32", 1, 1, -1, 32, 32, 1, 1, 1),      # negative length
+])
+def test_descriptor_validation(sdl, mode, dt, B, H, T, dk, dv, r, p, expect):
+    d = sdl.make_desc(mode, dt, B, H, T, dk, dv, r, p)
+    assert sdl.dplr_la_check(d) == expect
+    ws = sdl.dplr_la_workspace_size(d)
+    if expect != 0:
+        assert ws == 0
+    elif T > 0:
+        assert ws > 0
+
+
+def test_bad_enum_and_chunk(sdl):
+    d = sdl.make_desc("gdn", "f32", 1, 1, 8, 32, 32)
+    d.mode = 7
+    assert sdl.dplr_la_check(d) == sdl.dplr.DPLR_ERR_INVALID_ARG
+    d = sdl.make_desc("gdn", "f32", 1, 1, 8, 32, 32)
+    d.in_dtype = 5
+    assert sdl.dplr_la_check(d) == sdl.dplr.DPLR_ERR_INVALID_ARG
+    d = sdl.make_desc("gdn", "f32", 1, 1, 8, 32, 32, chunk=32)
+    assert sdl.dplr_la_check(d) == sdl.dplr.DPLR_ERR_UNSUPPORTED
+    assert sdl.library().dplr_la_check(None) == sdl.dplr.DPLR_ERR_INVALID_ARG
+
+
+def test_workspace_grows_with_length(sdl):
+    sizes = [sdl.dplr_la_workspace_size(sdl.make_desc("hdla", "bf16", 1, 2, T, 128, 128)) for T in (64, 128, 4096)]
+    assert sizes[0] < sizes[1] < sizes[2]
+    assert all(s % 256 == 0 for s in sizes)
+
+
+FAKE = 1 << 20   # 16-byte aligned, never dereferenced: validation fails before any launch
+
+
+def _fwd(sdl, d, **kw):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, decay=FAKE, beta=FAKE, A=None, Bm=None, K=None, V=None, S0=None,
+                o=FAKE, S_T=None, workspace=FAKE, ws_bytes=sdl.dplr_la_workspace_size(d), stream=None)
+    args.update(kw)
+    return sdl.dplr_la_forward(d, **args)
+
+
+@pytest.mark.parametrize("field", ["q", "k", "v", "decay", "beta", "o"])
+def test_forward_rejects_null_input_before_launch(sdl, field):
+    d = sdl.make_desc("hdla", "bf16", 1, 1, 64, 32, 32)
+    assert _fwd(sdl, d, **{field: None}) == sdl.dplr.DPLR_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("field", ["q", "k", "decay", "o", "S0", "S_T"])
+def test_forward_rejects_misaligned_pointer(sdl, field):
+    d = sdl.make_desc("hdla", "bf16", 1, 1, 64, 32, 32)
+    assert _fwd(sdl, d, **{field: FAKE + 4}) == sdl.dplr.DPLR_ERR_INVALID_ARG
+
+
+def test_forward_rejects_small_or_missing_workspace(sdl):
+    d = sdl.make_desc("gdn", "f32", 1, 1, 64, 32, 32)
+    need = sdl.dplr_la_workspace_size(d)
+    assert _fwd(sdl, d, ws_bytes=need - 1) == sdl.dplr.DPLR_ERR_WORKSPACE
+    assert _fwd(sdl, d, workspace=None) == sdl.dplr.DPLR_ERR_WORKSPACE
+    assert _fwd(sdl, d, workspace=FAKE + 16) == sdl.dplr.DPLR_ERR_WORKSPACE
+
+
+def test_generic_requires_factor_pointers(sdl):
+    d = sdl.make_desc("generic", "f32", 1, 1, 64, 32, 32, 2, 1)
+    base = dict(k=None, v=None, beta=None, A=FAKE, Bm=FAKE, K=FAKE, V=FAKE)
+    for field in ("A", "Bm", "K", "V"):
+        kw = dict(base)
+        kw[field] = None
+        assert _fwd(sdl, d, **kw) == sdl.dplr.DPLR_ERR_INVALID_ARG
+    d0 = sdl.make_desc("generic", "f32", 1, 1, 64, 32, 32, 2, 0)   # r_kv = 0: K, V unused
+    kw = dict(base)
+    kw.update(K=None, V=None, q=None)
+    assert _fwd(sdl, d0, **kw) == sdl.dplr.DPLR_ERR_INVALID_ARG   # q still required
+
+
+def test_stage_entry_points_validate(sdl):
+    d = sdl.make_desc("gdn", "f32", 1, 1, 64, 32, 32)
+    ws = sdl.dplr_la_workspace_size(d)
+    assert sdl.dplr_la_chunk_maps(d, None, FAKE, FAKE, FAKE, FAKE, None, None, None, None, FAKE, FAKE, ws,
+                                  None) == sdl.dplr.DPLR_ERR_INVALID_ARG
+    assert sdl.dplr_la_state_scan(d, None, FAKE, None, FAKE, ws - 1, None) == sdl.dplr.DPLR_ERR_WORKSPACE
+    assert sdl.dplr_la_state_scan(d, FAKE + 8, FAKE, None, FAKE, ws, None) == sdl.dplr.DPLR_ERR_INVALID_ARG
+
+
+def test_kernel_count(sdl):
+    assert sdl.dplr_la_kernel_count(sdl.make_desc("gdn", "f32", 1, 1, 64, 32, 32)) >= 1
+    assert sdl.dplr_la_kernel_count(sdl.make_desc("gdn", "f32", 1, 1, 64, 48, 32)) == 0

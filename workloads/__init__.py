@@ -10,7 +10,7 @@ Recipe (one independent NumPy ``Generator`` per (batch, head), seeded with
 ``SeedSequence([seed, workload_id, b, h])``; draws in this order per head):
 
 * structured modes (GDN, HDLA): q, k, v ~ N(0, 1) [T, d]; k is l2-normalised per
-  token (norm taken in float64, result stored as float32); then the decay
+  token (in float32); then the decay
   Gaussian, then the beta Gaussian.
     - GDN:  decay g_t = logsigmoid(N(0,1))  (one scalar per token, log-space),
             beta_t = sigmoid(N(0,1)).
@@ -33,7 +33,9 @@ rounded values as float32, so upcasting them to bf16 (device) or float64
 
 from __future__ import annotations
 
+import concurrent.futures
 import dataclasses
+import os
 from typing import Optional, Sequence
 
 import numpy as np
@@ -74,22 +76,20 @@ WORKLOADS = {
 
 
 def round_to_bf16(x: np.ndarray) -> np.ndarray:
-    """Round float32 values to the nearest bf16 (ties to even); return float32."""
+    """Round finite float32 values to the nearest bf16 (ties to even); return float32."""
     x = np.ascontiguousarray(x, dtype=np.float32)
-    bits = x.view(np.uint32).astype(np.uint64)
-    rounded = (bits + 0x7FFF + ((bits >> 16) & 1)) >> 16
-    out = (rounded.astype(np.uint32) << 16).view(np.float32)
-    return out.reshape(x.shape)
+    bits = x.view(np.uint32)
+    # finite inputs stay below 2^32 after adding at most 0x8000
+    rounded = (bits + np.uint32(0x7FFF) + ((bits >> np.uint32(16)) & np.uint32(1))) & np.uint32(0xFFFF0000)
+    return rounded.view(np.float32).reshape(x.shape)
 
 
 def _logsigmoid(x: np.ndarray) -> np.ndarray:
-    x = x.astype(np.float64)
-    return -np.logaddexp(0.0, -x)
+    return -np.logaddexp(np.float32(0.0), -x)
 
 
 def _sigmoid(x: np.ndarray) -> np.ndarray:
-    x = x.astype(np.float64)
-    return 0.5 * (1.0 + np.tanh(0.5 * x))
+    return np.float32(0.5) * (np.float32(1.0) + np.tanh(np.float32(0.5) * x))
 
 
 def _head_rng(seed: int, wid: int, b: int, h: int) -> np.random.Generator:
@@ -105,23 +105,23 @@ def _draw_head(w: Workload, T: int, rng: np.random.Generator) -> dict:
         q = rng.standard_normal((T, dk), dtype=f32)
         k = rng.standard_normal((T, dk), dtype=f32)
         v = rng.standard_normal((T, dv), dtype=f32)
-        nrm = np.sqrt(np.einsum("td,td->t", k.astype(np.float64), k.astype(np.float64)))
-        nrm = np.where(nrm > 0, nrm, 1.0)
-        k = (k.astype(np.float64) / nrm[:, None]).astype(f32)
+        nrm = np.sqrt(np.einsum("td,td->t", k, k))
+        nrm = np.where(nrm > 0, nrm, np.float32(1.0))
+        k = k / nrm[:, None]
         if w.mode == MODE_GDN:
-            decay = _logsigmoid(rng.standard_normal(T, dtype=f32)).astype(f32)
-            beta = _sigmoid(rng.standard_normal(T, dtype=f32)).astype(f32)
+            decay = _logsigmoid(rng.standard_normal(T, dtype=f32))
+            beta = _sigmoid(rng.standard_normal(T, dtype=f32))
         else:
-            decay = _logsigmoid(rng.standard_normal((T, dk), dtype=f32) + 2.0).astype(f32)
-            beta = (2.0 * _sigmoid(rng.standard_normal(T, dtype=f32))).astype(f32)
+            decay = _logsigmoid(rng.standard_normal((T, dk), dtype=f32) + f32(2.0))
+            beta = f32(2.0) * _sigmoid(rng.standard_normal(T, dtype=f32))
         if w.dtype == "bf16":
             q, k, v = round_to_bf16(q), round_to_bf16(k), round_to_bf16(v)
         out.update(q=q, k=k, v=v, decay=decay, beta=beta)
     else:
         r, p = w.r_ab, w.r_kv
         q = rng.standard_normal((T, dk), dtype=f32)
-        decay = _logsigmoid(rng.standard_normal((T, dk), dtype=f32) + 2.0).astype(f32)
-        beta = 2.0 * _sigmoid(rng.standard_normal((T, r), dtype=f32))
+        decay = _logsigmoid(rng.standard_normal((T, dk), dtype=f32) + f32(2.0))
+        beta = (f32(2.0) * _sigmoid(rng.standard_normal((T, r), dtype=f32))).astype(np.float64)
         g = rng.standard_normal((T, dk, r), dtype=f32).astype(np.float64)
         U, _ = np.linalg.qr(g, mode="reduced")                  # [T, dk, r]
         lam = np.exp(decay.astype(np.float64))                    # [T, dk]
@@ -156,13 +156,26 @@ def generate(w: Workload | int, seed: int = 0, heads: Optional[Sequence[tuple]] 
         w = WORKLOADS[w]
     T = w.T if T is None else int(T)
     pairs = [(b, h) for b in range(w.B) for h in range(w.H)] if heads is None else list(heads)
-    per = [_draw_head(w, T, _head_rng(seed, w.wid, b, h)) for (b, h) in pairs]
-    keys = per[0].keys()
-    res = {key: np.stack([d[key] for d in per]) for key in keys}
     if heads is None:
         B, H = w.B, w.H
     else:
         B, H = 1, len(pairs)
+    first = _draw_head(w, T, _head_rng(seed, w.wid, *pairs[0]))
+    res = {key: np.empty((B * H,) + x.shape, dtype=x.dtype) for key, x in first.items()}
+    for key, x in first.items():
+        res[key][0] = x
+    del first
+
+    def fill(i):
+        d = _draw_head(w, T, _head_rng(seed, w.wid, *pairs[i]))
+        for key, x in d.items():
+            res[key][i] = x
+
+    n = len(pairs)
+    if n > 1:
+        workers = max(1, min(n - 1, os.cpu_count() or 1, 32))
+        with concurrent.futures.ThreadPoolExecutor(workers) as pool:
+            list(pool.map(fill, range(1, n)))
     for key in list(res):
         res[key] = res[key].reshape((B, H) + res[key].shape[1:])
     for key in ("q", "k", "v", "decay", "beta", "A", "Bm", "K", "V", "S0"):
