@@ -140,6 +140,23 @@ DPLR_API const char* dplr_status_string(dplr_status status);
  * launch one. */
 DPLR_API int dplr_la_kernel_count(const dplr_desc* desc);
 
+/* The whole forward without a workspace argument (no counterpart in the paper:
+ * an addition for callers that cannot allocate device memory at call time, such
+ * as an inference engine that reserved the device up front or a plugin whose
+ * host framework owns the allocator). Scratch comes from a 64 MiB array compiled
+ * into the library, which every device that loads the library holds until the
+ * process exits; descriptors whose dplr_la_workspace_size exceeds 64 MiB return
+ * DPLR_ERR_UNSUPPORTED before anything is launched. Allocates nothing. Runs on
+ * the current device (make the stream's device current). The first call on a
+ * device looks up the array's device address: make it before any stream
+ * capture. Every call shares the array, so calls whose GPU work overlaps race
+ * and must be serialised. Other arguments and errors as for dplr_la_forward. */
+DPLR_API dplr_status dplr_la_forward_noalloc(const dplr_desc* desc,
+                                    const void* q, const void* k, const void* v,
+                                    const float* decay, const float* beta,
+                                    const void* A, const void* Bm, const void* K, const void* V,
+                                    const float* S0, float* o, float* S_T, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

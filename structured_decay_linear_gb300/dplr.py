@@ -63,6 +63,8 @@ def library() -> ctypes.CDLL:
             lib.dplr_la_chunk_maps.argtypes = [dp] + [_vp] * 10 + [_vp, ctypes.c_size_t, _vp]
             lib.dplr_la_state_scan.restype = ctypes.c_int
             lib.dplr_la_state_scan.argtypes = [dp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+            lib.dplr_la_forward_noalloc.restype = ctypes.c_int
+            lib.dplr_la_forward_noalloc.argtypes = [dp] + [_vp] * 12 + [_vp]
             _lib = lib
     return _lib
 
@@ -106,6 +108,12 @@ def dplr_la_kernel_count(desc: dplr_desc) -> int:
 def dplr_la_forward(desc, q, k, v, decay, beta, A, Bm, K, V, S0, o, S_T, workspace, ws_bytes, stream) -> int:
     return int(library().dplr_la_forward(ctypes.byref(desc), q, k, v, decay, beta, A, Bm, K, V, S0, o, S_T,
                                          workspace, ctypes.c_size_t(ws_bytes), stream))
+
+
+def dplr_la_forward_noalloc(desc, q, k, v, decay, beta, A, Bm, K, V, S0, o, S_T, stream) -> int:
+    """dplr_la_forward with scratch from the library's fixed device array (no workspace argument)."""
+    return int(library().dplr_la_forward_noalloc(ctypes.byref(desc), q, k, v, decay, beta, A, Bm, K, V, S0, o,
+                                                 S_T, stream))
 
 
 def dplr_la_chunk_maps(desc, q, k, v, decay, beta, A, Bm, K, V, o, workspace, ws_bytes, stream) -> int:
