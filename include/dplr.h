@@ -95,8 +95,17 @@ typedef struct {
 } dplr_desc;
 
 /* Bytes of device workspace dplr_la_forward needs for `desc`; 0 if `desc` is
- * invalid or unsupported (call dplr_la_check for the reason). */
+ * invalid or unsupported (call dplr_la_check for the reason). When the forward
+ * runs the fused per-head kernel (GDN/HDLA, bf16, dk = dv = 128) this is 256
+ * bytes: the first int32 is a device status word that a kernel sets to
+ * DPLR_ERR_TIMEOUT if one of its bounded waits gives up, and never clears; zero
+ * it once after allocating the workspace to observe that. Otherwise it holds the
+ * chunk maps of the two-stage path. */
 DPLR_API size_t dplr_la_workspace_size(const dplr_desc* desc);
+
+/* Bytes of device workspace dplr_la_chunk_maps and dplr_la_state_scan need for
+ * `desc` (the chunk maps of every chunk); 0 if `desc` is invalid. */
+DPLR_API size_t dplr_la_stage_workspace_size(const dplr_desc* desc);
 
 /* Validates `desc` alone (no pointers). DPLR_OK if the shape is supported. */
 DPLR_API dplr_status dplr_la_check(const dplr_desc* desc);
@@ -116,8 +125,8 @@ DPLR_API dplr_status dplr_la_forward(const dplr_desc* desc,
  * quantities in parallel"): per chunk, the cumulative decay, the factor build,
  * the Gram blocks, the UT/WY triangular solve, and from them the chunk's affine
  * map (P_j, c_j) and readout map (Q'_j, local output). Writes the maps to the
- * workspace and each chunk's zero-initial-state output into o. Arguments as for
- * dplr_la_forward. */
+ * workspace (dplr_la_stage_workspace_size bytes) and each chunk's
+ * zero-initial-state output into o. Other arguments as for dplr_la_forward. */
 DPLR_API dplr_status dplr_la_chunk_maps(const dplr_desc* desc,
                                const void* q, const void* k, const void* v,
                                const float* decay, const float* beta,
@@ -136,8 +145,8 @@ DPLR_API dplr_status dplr_la_state_scan(const dplr_desc* desc, const float* S0, 
 DPLR_API const char* dplr_status_string(dplr_status status);
 
 /* Number of CUDA kernels one dplr_la_forward launches for `desc` (0 if the
- * descriptor is invalid). dplr_la_chunk_maps and dplr_la_state_scan each
- * launch one. */
+ * descriptor is invalid): 1 for the fused per-head kernel, else 2 (one per
+ * stage). dplr_la_chunk_maps and dplr_la_state_scan each launch one. */
 DPLR_API int dplr_la_kernel_count(const dplr_desc* desc);
 
 /* The whole forward without a workspace argument (no counterpart in the paper:

@@ -54,7 +54,9 @@ dplr_status make_plan(const dplr_desc* d, Plan* pl) {
     p.off_P = off; off = round_up(off + units * (size_t)p.dk * p.dk * sizeof(float));
     p.off_c = off; off = round_up(off + units * (size_t)p.dk * p.dv * sizeof(float));
     p.off_Q = off; off = round_up(off + units * (size_t)p.cw * p.dk * sizeof(float));
-    p.ws_bytes = off;
+    p.ws_stages = off;
+    p.fused = fused_supported(p) ? 1 : 0;
+    p.ws_bytes = p.fused ? kAlign : p.ws_stages;   // fused: one device status word
     if (prep_smem_bytes(p) > 227 * 1024 || scan_smem_bytes(p) > 227 * 1024) return DPLR_ERR_UNSUPPORTED;
     *pl = p;
     return DPLR_OK;
@@ -78,10 +80,9 @@ dplr_status check_inputs(const Plan& pl, const void* q, const void* k, const voi
     return DPLR_OK;
 }
 
-dplr_status check_workspace(const Plan& pl, const void* ws, size_t ws_bytes) {
-    if (pl.ws_bytes == 0) return DPLR_OK;
-    if (!ws || ws_bytes < pl.ws_bytes || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0)
-        return DPLR_ERR_WORKSPACE;
+dplr_status check_workspace(size_t need, const void* ws, size_t ws_bytes) {
+    if (need == 0) return DPLR_OK;
+    if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return DPLR_ERR_WORKSPACE;
     return DPLR_OK;
 }
 
@@ -126,9 +127,16 @@ size_t dplr_la_workspace_size(const dplr_desc* desc) {
     return pl.ws_bytes;
 }
 
+size_t dplr_la_stage_workspace_size(const dplr_desc* desc) {
+    Plan pl;
+    if (make_plan(desc, &pl) != DPLR_OK) return 0;
+    return pl.ws_stages;
+}
+
 int dplr_la_kernel_count(const dplr_desc* desc) {
     Plan pl;
     if (make_plan(desc, &pl) != DPLR_OK) return 0;
+    if (pl.fused) return 1;
     return pl.T > 0 ? 2 : 1;
 }
 
@@ -140,7 +148,7 @@ dplr_status dplr_la_chunk_maps(const dplr_desc* desc, const void* q, const void*
     dplr_status st = make_plan(desc, &pl);
     if (st != DPLR_OK) return st;
     if ((st = check_inputs(pl, q, k, v, decay, beta, A, Bm, K, V, o)) != DPLR_OK) return st;
-    if ((st = check_workspace(pl, workspace, ws_bytes)) != DPLR_OK) return st;
+    if ((st = check_workspace(pl.ws_stages, workspace, ws_bytes)) != DPLR_OK) return st;
     const ChunkMapArgs a = map_args(pl, q, k, v, decay, beta, A, Bm, K, V, o, workspace);
     if (launch_chunk_maps(pl, a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return DPLR_ERR_CUDA;
     return DPLR_OK;
@@ -153,7 +161,7 @@ dplr_status dplr_la_state_scan(const dplr_desc* desc, const float* S0, float* o,
     if (st != DPLR_OK) return st;
     if ((S0 && !aligned16(S0)) || (S_T && !aligned16(S_T))) return DPLR_ERR_INVALID_ARG;
     if (pl.T > 0 && (!o || !aligned16(o))) return DPLR_ERR_INVALID_ARG;
-    if ((st = check_workspace(pl, workspace, ws_bytes)) != DPLR_OK) return st;
+    if ((st = check_workspace(pl.ws_stages, workspace, ws_bytes)) != DPLR_OK) return st;
     const ScanArgs a = scan_args(pl, S0, o, S_T, workspace);
     if (launch_state_scan(pl, a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return DPLR_ERR_CUDA;
     return DPLR_OK;
@@ -168,8 +176,13 @@ dplr_status dplr_la_forward(const dplr_desc* desc, const void* q, const void* k,
     if (st != DPLR_OK) return st;
     if ((st = check_inputs(pl, q, k, v, decay, beta, A, Bm, K, V, o)) != DPLR_OK) return st;
     if ((S0 && !aligned16(S0)) || (S_T && !aligned16(S_T))) return DPLR_ERR_INVALID_ARG;
-    if ((st = check_workspace(pl, workspace, ws_bytes)) != DPLR_OK) return st;
+    if ((st = check_workspace(pl.ws_bytes, workspace, ws_bytes)) != DPLR_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (pl.fused) {
+        if (launch_fused(pl, q, k, v, decay, beta, S0, o, S_T, static_cast<int*>(workspace), s) != cudaSuccess)
+            return DPLR_ERR_CUDA;
+        return DPLR_OK;
+    }
     if (launch_chunk_maps(pl, map_args(pl, q, k, v, decay, beta, A, Bm, K, V, o, workspace), s) != cudaSuccess)
         return DPLR_ERR_CUDA;
     if (launch_state_scan(pl, scan_args(pl, S0, o, S_T, workspace), s) != cudaSuccess) return DPLR_ERR_CUDA;

@@ -106,6 +106,7 @@ chunk_maps_kernel(Plan pl, ChunkMapArgs args) {
     const int R = (MODE == DPLR_GDN) ? 1 : (MODE == DPLR_HDLA ? 2 : pl.r);
     const int P = (MODE == DPLR_GENERIC) ? pl.p : 0;
     const int cr = cw * R, cp = cw * P;
+    const int Pd = P > 0 ? P : 1;   // divisor for the (generic-only) K/V row loops
     const int dkg = (MODE == DPLR_GDN) ? 1 : dk;
     const PrepLayout Ly(MODE, dk, dv, cw, R, P);
     float *lg = sm + Ly.lg, *G = sm + Ly.G, *bet = sm + Ly.beta;
@@ -212,11 +213,11 @@ chunk_maps_kernel(Plan pl, ChunkMapArgs args) {
             Bt[i] = ok ? expf(Gx(t, c) - anc(c)) * ld(Bp, src) : 0.f;
         }
         for (int i = tid; i < cp * dk; i += nth) {
-            const int row = i / dk, c = i % dk, t = row / P, l = row % P;
+            const int row = i / dk, c = i % dk, t = row / Pd, l = row % Pd;
             Kt[i] = (t0 + t < T) ? expf(-(Gi(t, c) - anc(c))) * ld(Kp, ((tok0 + t) * P + l) * dk + c) : 0.f;
         }
         for (int i = tid; i < cp * dv; i += nth) {
-            const int row = i / dv, n = i % dv, t = row / P, l = row % P;
+            const int row = i / dv, n = i % dv, t = row / Pd, l = row % Pd;
             Vs[i] = (t0 + t < T) ? ld(Vp, ((tok0 + t) * P + l) * dv + n) : 0.f;
         }
     }
@@ -235,11 +236,11 @@ chunk_maps_kernel(Plan pl, ChunkMapArgs args) {
         block_gemm<4, 4>(cr, cp, dk,
             [&](int m, int kk) { return Bt[m * dk + kk]; },
             [&](int kk, int n) { return Kt[n * dk + kk]; },
-            [&](int m, int n, float x) { GBK[m * cp + n] = (n / P < m / R) ? x : 0.f; });
+            [&](int m, int n, float x) { GBK[m * cp + n] = (n / Pd < m / R) ? x : 0.f; });
         block_gemm<4, 4>(cw, cp, dk,
             [&](int m, int kk) { return Qt[m * dk + kk]; },
             [&](int kk, int n) { return Kt[n * dk + kk]; },
-            [&](int m, int n, float x) { QK[m * cp + n] = (n / P <= m) ? x : 0.f; });
+            [&](int m, int n, float x) { QK[m * cp + n] = (n / Pd <= m) ? x : 0.f; });
     }
     __syncthreads();
     if (MODE == DPLR_GENERIC) {

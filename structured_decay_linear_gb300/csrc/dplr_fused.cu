@@ -1,0 +1,593 @@
+// Fused per-head forward for Gated DeltaNet with bf16 inputs and dk = dv = 128: one
+// CTA owns one (batch, head), walks its chunks of C = 64 tokens in order and keeps
+// everything of a chunk on chip -- the Gram blocks, the UT/WY triangular inverse, the
+// state-dependent products and the fp32 state itself -- so HBM sees the inputs once and
+// the outputs once.
+//
+// GDN's decay is one scalar per token, so every decay factor of the chunkwise form
+// ("Householder-Diagonalized Linear Attention", Key design 3; GDN as the rank-1 case,
+// HLA page, Prerequisites) can be moved out of the contractions into row/column
+// scalings applied in fp32. With G_t the inclusive cumulative log-gate inside the chunk,
+// anchor a = G_C / 2, ef_t = e^{G_t - a}, eb_t = e^{-(G_t - a)} and the folded factors
+// A = beta k, B = e^{g} k, W = v, the tensor cores only ever see the raw bf16 q, k, v
+// (exact) and a few rounded intermediates:
+//
+//   D     = [K ; Q] K^T                          (tcgen05 M=128 N=64  K=dk)
+//   L_ts  = ef_t D_ts beta_s eb_s  (s < t)       (fp32 epilogue)
+//   QK    = tril_incl(Q K^T)                     (bf16 hi + lo)
+//   M     = (I + L)^{-1}                         (CUDA cores, fp32, blocked 16/32/64)
+//   Y^T   = K^T (M Diag(ef))^T                   (tcgen05 M=128 N=64  K=C)
+//   E^T   = S'^T Y^T - V^T M^T,  S' = e^{a} S    (tcgen05 M=128 N=64  K=dk+C)
+//   Es    = Diag(beta eb) E                      (bf16 hi + lo)
+//   X     = K^T Es                               (tcgen05 M=128 N=dv  K=C)
+//   O'^T  = S'^T Q^T - Es^T QK^T, o_t = ef_t O'_t (tcgen05 M=128 N=64 K=dk+C)
+//   S_j   = e^{G_C} S_{j-1} - e^{G_C - a} X      (fp32, registers)
+//
+// E_t = e^{g_t} k_t^T S_{t-1} - v_t is the delta-rule prediction error. Computing the
+// transposes E^T, Y^T and O'^T keeps every MMA at M = 128 (full tensor-core rate). The
+// rounding of E, QK and of S' in the output product is compensated with a second bf16
+// term (x = hi + lo), which keeps the result within ~2e-3 of the float64 recurrence
+// (relative to the output RMS) where plain bf16 operands reach ~4e-2.
+//
+// Operand tiles. Every bf16 operand lives in shared memory as 8x8 core matrices (8 rows
+// of 16 bytes). Two arrangements are used:
+//   RBM (row-block major, C columns): (r, c) -> (r/8)*C*16 + (c/8)*128 + (r%8)*16 + (c%8)*2
+//   CBM (col-block major, R rows):    (r, c) -> (c/8)*R*16 + (r/8)*128 + (r%8)*16 + (c%8)*2
+// Either one feeds an MMA K-major (contracting over columns) or MN-major (contracting
+// over rows) by choosing the descriptor's LBO/SBO, so no tile is ever transposed. q, k and
+// v arrive by TMA tensor copies (one 8-column box per column block) directly in CBM;
+// tiles written from registers use RBM, whose 16-byte rows of a warp land in distinct
+// bank groups.
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "dplr_internal.h"
+#include "sm100_ops.cuh"
+
+namespace dplr {
+namespace {
+
+using namespace sm100;
+
+constexpr int FD = 128;    // dk = dv
+constexpr int FC = 64;     // tokens per chunk
+constexpr int FNT = 256;   // threads per CTA
+constexpr uint32_t kTmemCols = 512;
+constexpr int kLdL = 65;   // padded row stride (floats) of the fp32 L and M buffers
+
+// Tile geometry: byte strides between core matrices.
+constexpr uint32_t KQ_CB = 128 * 16;   // T_KQ: CBM with 128 rows (k rows 0-63, q rows 64-127)
+constexpr uint32_t V_CB = 64 * 16;     // T_V:  CBM with 64 rows
+constexpr uint32_t S_RB = 128 * 16;    // T_S / T_SLO: RBM with 128 columns
+constexpr uint32_t N64_RB = 64 * 16;   // RBM tiles with 64 columns
+
+struct GdnLayout {
+    static constexpr int T_KQ0 = 0;                         // [128][128] CBM, two buffers
+    static constexpr int T_KQ1 = T_KQ0 + 128 * FD * 2;
+    static constexpr int T_V = T_KQ1 + 128 * FD * 2;        // [64][128] CBM  v
+    static constexpr int T_S = T_V + FC * FD * 2;           // [128 c][128 n] RBM  S' hi
+    // region R1 (32 KB): -M, M Diag(ef), Y^T; after E it holds S' lo
+    static constexpr int R1 = T_S + FD * FD * 2;
+    static constexpr int T_MN = R1;                         // [64 rho][64 sigma] RBM  -M
+    static constexpr int T_MY = R1 + FC * FC * 2;           // [64][64] RBM  M Diag(ef)
+    static constexpr int T_YT = R1 + 2 * FC * FC * 2;       // [128 c][64 rho] RBM  Y^T
+    static constexpr int T_SLO = R1;                        // [128][128] RBM  S' lo
+    // region R2 (32 KB): Es^T hi / lo; aliased by the fp32 L buffer before E
+    static constexpr int R2 = R1 + FD * FD * 2;
+    static constexpr int T_ESH = R2;                        // [128 n][64 rho] RBM
+    static constexpr int T_ESL = R2 + FD * FC * 2;
+    static constexpr int F_L = R2;                          // fp32 [64][65]
+    static constexpr int T_QKH = R2 + 2 * FD * FC * 2;      // [64 t][64 sigma] RBM  -QK hi
+    static constexpr int T_QKL = T_QKH + FC * FC * 2;       //                       -QK lo
+    static constexpr int F_M = T_QKL + FC * FC * 2;         // fp32 [64][65]
+    static constexpr int SCR = F_M + FC * kLdL * 4;         // fp32 scratch of the inverse (1024)
+    static constexpr int VEC = SCR + 4096;
+    static constexpr int V_EF = VEC, V_EB = VEC + 256, V_BS = VEC + 512, V_SC = VEC + 768;
+    static constexpr int RAW_G = VEC + 1024;                // [2][64] log gate
+    static constexpr int RAW_B = RAW_G + 512;               // [2][64] beta
+    static constexpr int BAR = RAW_B + 512;
+    static constexpr int TOTAL = BAR + 64;
+};
+static_assert(GdnLayout::T_SLO + FD * FD * 2 == GdnLayout::R2, "S' lo must exactly fill region R1");
+static_assert(GdnLayout::F_L + FC * kLdL * 4 <= GdnLayout::T_QKH, "L must fit in region R2");
+static_assert(GdnLayout::TOTAL <= 227 * 1024, "shared memory budget");
+
+struct FusedArgs {
+    const __nv_bfloat16* q; const __nv_bfloat16* k; const __nv_bfloat16* v;
+    const float* decay; const float* beta; const float* S0;
+    float* o; float* ST; int* status;
+};
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ uint32_t rbm_off(int r, int c, int cols) {
+    return static_cast<uint32_t>((r >> 3) * (cols * 16) + (c >> 3) * 128 + (r & 7) * 16 + (c & 7) * 2);
+}
+
+// 8 consecutive fp32 values (cols c..c+7, c % 8 == 0) of row r into an RBM bf16 tile.
+__device__ __forceinline__ void rbm_store8(uint32_t tile, int cols, int r, int c, const float* x) {
+    st_shared_v4(tile + rbm_off(r, c, cols), pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
+                 pack_bf16(x[6], x[7]));
+}
+
+// x = hi + lo with both parts bf16.
+__device__ __forceinline__ void rbm_store8_split(uint32_t th, uint32_t tl, int cols, int r, int c, const float* x) {
+    float hi[8], lo[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        hi[i] = __bfloat162float(__float2bfloat16_rn(x[i]));
+        lo[i] = x[i] - hi[i];
+    }
+    rbm_store8(th, cols, r, c, hi);
+    rbm_store8(tl, cols, r, c, lo);
+}
+
+// (I + L)^{-1} for a 64x64 strictly lower-triangular fp32 L (row stride kLdL): right-looking
+// solves of the four 16x16 diagonal blocks, then merges 16->32->64 with
+// [[A,0],[C,B]]^{-1} = [[A^{-1},0],[-B^{-1} C A^{-1}, B^{-1}]], each thread keeping several
+// independent accumulators. Writes -M and M Diag(ef) as bf16 RBM tiles.
+__device__ __forceinline__ void unit_lower_inverse64(const float* L, float* Mf, float* scr, uint32_t t_mn,
+                                                     uint32_t t_my, const float* ef, int tid) {
+    if (tid < 64) {
+        const int b = tid >> 4, j = tid & 15, o = 16 * b;
+        float s[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) s[i] = (i == j) ? 1.f : 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const float xk = s[k];
+#pragma unroll
+            for (int i = k + 1; i < 16; ++i) s[i] = fmaf(-L[(o + i) * kLdL + o + k], xk, s[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) Mf[(o + i) * kLdL + o + j] = s[i];
+    }
+    __syncthreads();
+    {   // 32x32 blocks (0,1) and (2,3)
+        const int p = tid >> 7, e = tid & 127, o = 32 * p, i = e >> 3, jq = e & 7;
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const float l = L[(o + 16 + i) * kLdL + o + k];
+            a0 = fmaf(l, Mf[(o + k) * kLdL + o + jq], a0);
+            a1 = fmaf(l, Mf[(o + k) * kLdL + o + jq + 8], a1);
+        }
+        scr[p * 256 + i * 16 + jq] = a0;
+        scr[p * 256 + i * 16 + jq + 8] = a1;
+        Mf[(o + i) * kLdL + o + 16 + jq] = 0.f;          // block above the diagonal
+        Mf[(o + i) * kLdL + o + 16 + jq + 8] = 0.f;
+        __syncthreads();
+        float c0 = 0.f, c1 = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const float bb = Mf[(o + 16 + i) * kLdL + o + 16 + k];
+            c0 = fmaf(bb, scr[p * 256 + k * 16 + jq], c0);
+            c1 = fmaf(bb, scr[p * 256 + k * 16 + jq + 8], c1);
+        }
+        Mf[(o + 16 + i) * kLdL + o + jq] = -c0;
+        Mf[(o + 16 + i) * kLdL + o + jq + 8] = -c1;
+        __syncthreads();
+    }
+    {   // 64x64: rows 32-63, columns 0-31
+        const int i = tid >> 3, jq = tid & 7;
+        float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+        for (int k = 0; k < 32; ++k) {
+            const float l = L[(32 + i) * kLdL + k];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) a[u] = fmaf(l, Mf[k * kLdL + jq + 8 * u], a[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) scr[i * 32 + jq + 8 * u] = a[u];
+        __syncthreads();
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+        for (int k = 0; k < 32; ++k) {
+            const float bb = Mf[(32 + i) * kLdL + 32 + k];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) c[u] = fmaf(bb, scr[k * 32 + jq + 8 * u], c[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) Mf[(32 + i) * kLdL + jq + 8 * u] = -c[u];
+        __syncthreads();
+    }
+    // bf16 tiles -M and M Diag(ef); the 32x32 block above the diagonal is zero
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int item = tid + 256 * h, r = item & 63, c = (item >> 6) * 8;
+        float x[8], y[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float m = ((c >> 5) > (r >> 5)) ? 0.f : Mf[r * kLdL + c + i];
+            x[i] = -m;
+            y[i] = m * ef[c + i];
+        }
+        rbm_store8(t_mn, FC, r, c, x);
+        rbm_store8(t_my, FC, r, c, y);
+    }
+}
+
+__global__ void __launch_bounds__(FNT, 1)
+gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
+    using Ly = GdnLayout;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const uint32_t sbase = smem_addr(smem);
+    uint64_t* mbar_mma = reinterpret_cast<uint64_t*>(smem + Ly::BAR);
+    uint64_t* mbar_kq = reinterpret_cast<uint64_t*>(smem + Ly::BAR + 8);    // [2]
+    uint64_t* mbar_v = reinterpret_cast<uint64_t*>(smem + Ly::BAR + 24);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Ly::BAR + 32);
+    float* v_ef = reinterpret_cast<float*>(smem + Ly::V_EF);
+    float* v_eb = reinterpret_cast<float*>(smem + Ly::V_EB);
+    float* v_bs = reinterpret_cast<float*>(smem + Ly::V_BS);
+    float* v_sc = reinterpret_cast<float*>(smem + Ly::V_SC);   // [0] e^{a}, [1] e^{G_C - a}, [2] e^{G_C}
+    float* scr = reinterpret_cast<float*>(smem + Ly::SCR);
+    float* F_L = reinterpret_cast<float*>(smem + Ly::F_L);
+    float* F_M = reinterpret_cast<float*>(smem + Ly::F_M);
+    float* rawG = reinterpret_cast<float*>(smem + Ly::RAW_G);
+    float* rawB = reinterpret_cast<float*>(smem + Ly::RAW_B);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, half = warp >> 2;
+    const int row = tid & 127;                  // TMEM lane of this thread
+    const size_t bh = blockIdx.x;
+    const int T = pl.T;
+    const int nchunk = (T + FC - 1) / FC;
+    const int nfull = T / FC;                   // chunks loaded by TMA
+    const size_t tok_base = bh * (size_t)T;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
+
+    if (tid == 0) {
+        mbar_init(mbar_mma, 1);
+        mbar_init(&mbar_kq[0], 1);
+        mbar_init(&mbar_kq[1], 1);
+        mbar_init(mbar_v, 1);
+        mbar_fence_init();
+    }
+    if (warp == 0) tmem_alloc(tmem_holder, kTmemCols);
+    if (tid < FC) {
+        rawG[tid] = (tid < T) ? args.decay[tok_base + tid] : 0.f;
+        rawB[tid] = (tid < T) ? args.beta[tok_base + tid] : 0.f;
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tmem_holder;
+
+    auto issue_kq = [&](int j) {   // thread 0
+        const int y = static_cast<int>(tok_base + (size_t)j * FC);
+        unsigned char* dst = smem + ((j & 1) ? Ly::T_KQ1 : Ly::T_KQ0);
+        mbar_expect_tx(&mbar_kq[j & 1], 2u * FC * FD * 2);
+        for (int cb = 0; cb < FD / 8; ++cb) {
+            tma_load_2d(dst + cb * KQ_CB, &tm_k, 8 * cb, y, &mbar_kq[j & 1]);
+            tma_load_2d(dst + cb * KQ_CB + FC * 16, &tm_q, 8 * cb, y, &mbar_kq[j & 1]);
+        }
+    };
+    auto issue_v = [&](int j) {    // thread 0
+        const int y = static_cast<int>(tok_base + (size_t)j * FC);
+        mbar_expect_tx(mbar_v, FC * FD * 2);
+        for (int cb = 0; cb < FD / 8; ++cb) tma_load_2d(smem + Ly::T_V + cb * V_CB, &tm_v, 8 * cb, y, mbar_v);
+    };
+    if (tid == 0) {
+        if (nfull > 0) { issue_kq(0); issue_v(0); }
+        if (nfull > 1) issue_kq(1);
+    }
+
+    // fp32 state: row `row` of S, columns [64*half, 64*half + 64)
+    float S[64];
+#pragma unroll
+    for (int i = 0; i < 64; ++i) S[i] = args.S0 ? args.S0[(bh * FD + row) * FD + 64 * half + i] : 0.f;
+
+    uint32_t mma_phase = 0;
+    bool failed = false;
+    // thread 0 tracks outstanding bulk loads so an early exit can drain them
+    int kq_issued = (nfull > 0) + (nfull > 1), kq_done = 0, v_issued = (nfull > 0), v_done = 0;
+    auto wait_mma = [&]() -> bool {
+        const bool got = mbar_wait(mbar_mma, mma_phase);
+        mma_phase ^= 1u;
+        const bool bad = __syncthreads_or(!got) != 0;
+        fence_after_sync();
+        return !bad;
+    };
+
+    for (int j = 0; j < nchunk; ++j) {
+        const int t0 = j * FC;
+        const int valid = min(FC, T - t0);
+        const size_t g0 = tok_base + t0;
+        const int b = j & 1;
+        const uint32_t tKQ = sbase + (b ? Ly::T_KQ1 : Ly::T_KQ0);
+        const uint32_t tQ = tKQ + FC * 16;        // q rows start at row 64 of the CBM tile
+        float* gcur = rawG + b * FC;
+        float* bcur = rawB + b * FC;
+        // prefetch the next chunk's k, q (its buffer was last read by chunk j - 1) and gate/beta
+        if (tid == 0 && j >= 1 && j + 1 < nfull) { issue_kq(j + 1); ++kq_issued; }
+        float g_next = 0.f, b_next = 0.f;
+        if (tid < FC && t0 + FC + tid < T) {
+            g_next = args.decay[g0 + FC + tid];
+            b_next = args.beta[g0 + FC + tid];
+        }
+
+        // ---- a2: cumulative log-gate, anchor a = G_C / 2, per-token factors
+        if (warp == 0) {
+            const float x0 = gcur[2 * lane], x1 = gcur[2 * lane + 1];
+            float s = x0 + x1;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, s, off);
+                if (lane >= off) s += y;
+            }
+            const float gc = __shfl_sync(0xffffffffu, s, 31);
+            const float a = 0.5f * gc;
+            const float G1 = s, G0 = s - x1;
+            const float e0 = __expf(a - G0), e1 = __expf(a - G1);
+            v_ef[2 * lane] = __expf(G0 - a);
+            v_ef[2 * lane + 1] = __expf(G1 - a);
+            v_eb[2 * lane] = e0;
+            v_eb[2 * lane + 1] = e1;
+            v_bs[2 * lane] = bcur[2 * lane] * e0;
+            v_bs[2 * lane + 1] = bcur[2 * lane + 1] * e1;
+            if (lane == 0) {
+                v_sc[0] = __expf(a);
+                v_sc[1] = __expf(gc - a);
+                v_sc[2] = __expf(gc);
+            }
+        }
+        // ragged last chunk: plain loads (zero rows past the end) straight into the CBM tiles
+        if (valid < FC) {
+            for (int i = tid; i < FC * (FD / 8); i += FNT) {
+                const int t = i & (FC - 1), cb = i >> 6;
+                uint4 zq = make_uint4(0, 0, 0, 0), zk = zq, zv = zq;
+                if (t < valid) {
+                    zq = *reinterpret_cast<const uint4*>(args.q + (g0 + t) * FD + 8 * cb);
+                    zk = *reinterpret_cast<const uint4*>(args.k + (g0 + t) * FD + 8 * cb);
+                    zv = *reinterpret_cast<const uint4*>(args.v + (g0 + t) * FD + 8 * cb);
+                }
+                st_shared_v4(tKQ + cb * KQ_CB + t * 16, zk.x, zk.y, zk.z, zk.w);
+                st_shared_v4(tQ + cb * KQ_CB + t * 16, zq.x, zq.y, zq.z, zq.w);
+                st_shared_v4(sbase + Ly::T_V + cb * V_CB + t * 16, zv.x, zv.y, zv.z, zv.w);
+            }
+        }
+        __syncthreads();
+        // S' hi = bf16(e^{a} S_{j-1}), RBM [c][n]
+        {
+            const float ea = v_sc[0];
+#pragma unroll
+            for (int i = 0; i < 64; i += 8) {
+                float x[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) x[u] = ea * S[i + u];
+                rbm_store8(sbase + Ly::T_S, FD, row, 64 * half + i, x);
+            }
+        }
+        fence_async_smem();
+        __syncthreads();
+
+        // ---- a4: D = [K ; Q] K^T (M = 128 rows of k then q, N = 64 rows of k)
+        if (tid == 0) {
+            bool ok = true;
+            if (valid == FC) { ok = mbar_wait(&mbar_kq[b], (j >> 1) & 1); ++kq_done; }
+            if (!ok) atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
+            fence_after_sync();
+            mma_chain(tmem + 0, smem_desc(tKQ, KQ_CB, 128), 2 * KQ_CB, smem_desc(tKQ, KQ_CB, 128), 2 * KQ_CB,
+                      idesc_bf16(128, FC, false, false), FD, false);
+            mma_commit(mbar_mma);
+        }
+        if (!wait_mma()) { failed = true; break; }
+        {
+            float x[32];
+            tmem_ld32(tmem + lane_off + 32 * half, x);
+            if (row < FC) {              // L row t: ef_t D_ts beta_s eb_s for s < t
+                const int t = row;
+                const float eft = v_ef[t];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int sg = 32 * half + i;
+                    F_L[t * kLdL + sg] = (sg < t) ? eft * x[i] * v_bs[sg] : 0.f;
+                }
+            } else {                     // -QK row t (inclusive causal), hi + lo
+                const int t = row - FC;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int sg = 32 * half + i;
+                    x[i] = (sg <= t) ? -x[i] : 0.f;
+                }
+#pragma unroll
+                for (int i = 0; i < 32; i += 8)
+                    rbm_store8_split(sbase + Ly::T_QKH, sbase + Ly::T_QKL, FC, t, 32 * half + i, x + i);
+            }
+        }
+        fence_before_sync();
+        __syncthreads();
+
+        // ---- a5: M = (I + L)^{-1}; tiles -M and M Diag(ef)
+        unit_lower_inverse64(F_L, F_M, scr, sbase + Ly::T_MN, sbase + Ly::T_MY, v_ef, tid);
+        fence_async_smem();
+        __syncthreads();
+
+        // ---- Y^T = K^T (M Diag(ef))^T   (A: k rows as MN-major, B: M Diag(ef) K-major)
+        if (tid == 0) {
+            fence_after_sync();
+            mma_chain(tmem + 64, smem_desc(tKQ, 128, KQ_CB), 256, smem_desc(sbase + Ly::T_MY, 128, N64_RB), 256,
+                      idesc_bf16(128, FC, true, false), FC, false);
+            mma_commit(mbar_mma);
+        }
+        if (!wait_mma()) { failed = true; break; }
+        {
+            float x[32];
+            tmem_ld32(tmem + 64 + lane_off + 32 * half, x);
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) rbm_store8(sbase + Ly::T_YT, FC, row, 32 * half + i, x + i);
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+
+        // ---- a6: E^T = S'^T Y^T + V^T (-M)^T
+        if (tid == 0) {
+            bool ok = true;
+            if (valid == FC) { ok = mbar_wait(mbar_v, j & 1); ++v_done; }
+            if (!ok) atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
+            fence_after_sync();
+            mma_chain(tmem + 128, smem_desc(sbase + Ly::T_S, S_RB, 128), 2 * S_RB,
+                      smem_desc(sbase + Ly::T_YT, N64_RB, 128), 2 * N64_RB, idesc_bf16(128, FC, true, true), FD, false);
+            mma_chain(tmem + 128, smem_desc(sbase + Ly::T_V, 128, V_CB), 256, smem_desc(sbase + Ly::T_MN, 128, N64_RB), 256,
+                      idesc_bf16(128, FC, true, false), FC, true);
+            mma_commit(mbar_mma);
+        }
+        if (!wait_mma()) { failed = true; break; }
+        // v is consumed: prefetch the next full chunk's v
+        if (tid == 0 && j + 1 < nfull) { issue_v(j + 1); ++v_issued; }
+        {
+            float x[32];
+            tmem_ld32(tmem + 128 + lane_off + 32 * half, x);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[i] *= v_bs[32 * half + i];     // Es^T[n][rho] = beta eb_rho E[rho][n]
+#pragma unroll
+            for (int i = 0; i < 32; i += 8)
+                rbm_store8_split(sbase + Ly::T_ESH, sbase + Ly::T_ESL, FC, row, 32 * half + i, x + i);
+        }
+        {   // S' lo = e^{a} S - bf16(e^{a} S), into region R1 (M, M Diag(ef), Y^T are consumed)
+            const float ea = v_sc[0];
+#pragma unroll
+            for (int i = 0; i < 64; i += 8) {
+                float x[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const float sp = ea * S[i + u];
+                    x[u] = sp - __bfloat162float(__float2bfloat16_rn(sp));
+                }
+                rbm_store8(sbase + Ly::T_SLO, FD, row, 64 * half + i, x);
+            }
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+
+        // ---- a6/a7: X = K^T Es (state update), O'^T = S'^T Q^T - Es^T QK^T (chunk output)
+        if (tid == 0) {
+            fence_after_sync();
+            const uint64_t dKmn = smem_desc(tKQ, 128, KQ_CB);                 // k rows, MN-major A
+            const uint32_t idX = idesc_bf16(128, FD, true, false);
+            mma_chain(tmem + 256, dKmn, 256, smem_desc(sbase + Ly::T_ESH, 128, N64_RB), 256, idX, FC, false);
+            mma_chain(tmem + 256, dKmn, 256, smem_desc(sbase + Ly::T_ESL, 128, N64_RB), 256, idX, FC, true);
+            const uint64_t dQ = smem_desc(tQ, KQ_CB, 128);                    // q rows, K-major B
+            const uint32_t idO = idesc_bf16(128, FC, true, false), idO2 = idesc_bf16(128, FC, false, false);
+            mma_chain(tmem + 384, smem_desc(sbase + Ly::T_S, S_RB, 128), 2 * S_RB, dQ, 2 * KQ_CB, idO, FD, false);
+            mma_chain(tmem + 384, smem_desc(sbase + Ly::T_SLO, S_RB, 128), 2 * S_RB, dQ, 2 * KQ_CB, idO, FD, true);
+            mma_chain(tmem + 384, smem_desc(sbase + Ly::T_ESH, 128, N64_RB), 256,
+                      smem_desc(sbase + Ly::T_QKH, 128, N64_RB), 256, idO2, FC, true);
+            mma_chain(tmem + 384, smem_desc(sbase + Ly::T_ESL, 128, N64_RB), 256,
+                      smem_desc(sbase + Ly::T_QKH, 128, N64_RB), 256, idO2, FC, true);
+            mma_chain(tmem + 384, smem_desc(sbase + Ly::T_ESH, 128, N64_RB), 256,
+                      smem_desc(sbase + Ly::T_QKL, 128, N64_RB), 256, idO2, FC, true);
+            mma_commit(mbar_mma);
+        }
+        if (!wait_mma()) { failed = true; break; }
+        {
+            const float gam = v_sc[2], egca = v_sc[1];
+            float x[32];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                tmem_ld32(tmem + 256 + lane_off + 64 * half + 32 * h, x);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) S[32 * h + i] = fmaf(gam, S[32 * h + i], -egca * x[i]);
+            }
+            tmem_ld32(tmem + 384 + lane_off + 32 * half, x);      // O'^T row n = row, tokens 32*half + i
+            float* orow = args.o + g0 * FD + row;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int t = 32 * half + i;
+                if (t < valid) orow[(size_t)t * FD] = v_ef[t] * x[i];
+            }
+        }
+        if (tid < FC) {
+            rawG[(b ^ 1) * FC + tid] = g_next;
+            rawB[(b ^ 1) * FC + tid] = b_next;
+        }
+        fence_before_sync();
+        __syncthreads();
+    }
+
+    if (failed) {
+        if (tid == 0) {
+            atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
+            // drain the loads still in flight (bounded) before the CTA exits
+            for (int i = kq_done; i < kq_issued; ++i) mbar_wait(&mbar_kq[i & 1], (i >> 1) & 1, 400000000LL);
+            for (int i = v_done; i < v_issued; ++i) mbar_wait(mbar_v, i & 1, 400000000LL);
+        }
+        mbar_wait(mbar_mma, mma_phase, 400000000LL);
+    } else if (args.ST) {
+#pragma unroll
+        for (int i = 0; i < 64; i += 4)
+            *reinterpret_cast<float4*>(args.ST + (bh * FD + row) * FD + 64 * half + i) =
+                make_float4(S[i], S[i + 1], S[i + 2], S[i + 3]);
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---- host side: tensor maps (driver entry point looked up once)
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// [rows][128] bf16 row-major, boxes of 8 columns x 64 rows.
+bool make_map(CUtensorMap* map, const void* base, uint64_t rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {FD, rows};
+    cuuint64_t strides[1] = {FD * 2};
+    cuuint32_t box[2] = {8, FC};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool fused_supported(const Plan& pl) {
+    return pl.mode == DPLR_GDN && pl.bf16 && pl.dk == FD && pl.dv == FD;
+}
+
+cudaError_t launch_fused(const Plan& pl, const void* q, const void* k, const void* v, const float* decay,
+                         const float* beta, const float* S0, float* o, float* ST, int* status, cudaStream_t s) {
+    FusedArgs a;
+    a.q = static_cast<const __nv_bfloat16*>(q);
+    a.k = static_cast<const __nv_bfloat16*>(k);
+    a.v = static_cast<const __nv_bfloat16*>(v);
+    a.decay = decay; a.beta = beta; a.S0 = S0; a.o = o; a.ST = ST; a.status = status;
+    CUtensorMap mq, mk, mv;
+    std::memset(&mq, 0, sizeof(mq));
+    std::memset(&mk, 0, sizeof(mk));
+    std::memset(&mv, 0, sizeof(mv));
+    if (pl.T >= FC) {   // only full chunks are loaded by TMA
+        const uint64_t rows = (uint64_t)pl.BH * (uint64_t)pl.T;
+        if (!make_map(&mq, q, rows) || !make_map(&mk, k, rows) || !make_map(&mv, v, rows))
+            return cudaErrorInvalidValue;
+    }
+    cudaError_t e = cudaFuncSetAttribute(gdn_fused_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         GdnLayout::TOTAL);
+    if (e != cudaSuccess) return e;
+    gdn_fused_head_kernel<<<(unsigned)pl.BH, FNT, GdnLayout::TOTAL, s>>>(pl, a, mq, mk, mv);
+    return cudaGetLastError();
+}
+
+size_t fused_smem_bytes(int) { return (size_t)GdnLayout::TOTAL; }
+
+}  // namespace dplr

@@ -21,9 +21,12 @@ constexpr int kScanCols = 32;  // state columns per scan CTA (dv split)
 struct Plan {
     int mode, bf16;
     int BH, T, dk, dv, r, p;   // p = 0 in the structured modes (write term folded into A)
-    int cw;                    // WY block length in tokens
+    int cw;                    // WY block length in tokens (two-stage path)
     int nb;                    // WY blocks per head = ceil(T / cw)
-    size_t off_P, off_c, off_Q, ws_bytes;
+    int fused;                 // dplr_la_forward runs the fused per-head kernel
+    size_t off_P, off_c, off_Q;
+    size_t ws_stages;          // workspace of the two-stage entry points
+    size_t ws_bytes;           // workspace of dplr_la_forward
 };
 
 // Per-launch arguments of the chunk-map kernel.
@@ -47,5 +50,11 @@ size_t prep_smem_bytes(const Plan& pl);
 size_t scan_smem_bytes(const Plan& pl);
 cudaError_t launch_chunk_maps(const Plan& pl, const ChunkMapArgs& a, cudaStream_t s);
 cudaError_t launch_state_scan(const Plan& pl, const ScanArgs& a, cudaStream_t s);
+
+// Fused per-head kernel (structured modes, bf16 inputs, dk = dv = 128).
+bool fused_supported(const Plan& pl);
+size_t fused_smem_bytes(int mode);
+cudaError_t launch_fused(const Plan& pl, const void* q, const void* k, const void* v, const float* decay,
+                         const float* beta, const float* S0, float* o, float* ST, int* status, cudaStream_t s);
 
 }  // namespace dplr

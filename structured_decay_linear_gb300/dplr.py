@@ -51,6 +51,8 @@ def library() -> ctypes.CDLL:
             dp = ctypes.POINTER(dplr_desc)
             lib.dplr_la_workspace_size.restype = ctypes.c_size_t
             lib.dplr_la_workspace_size.argtypes = [dp]
+            lib.dplr_la_stage_workspace_size.restype = ctypes.c_size_t
+            lib.dplr_la_stage_workspace_size.argtypes = [dp]
             lib.dplr_la_check.restype = ctypes.c_int
             lib.dplr_la_check.argtypes = [dp]
             lib.dplr_la_kernel_count.restype = ctypes.c_int
@@ -95,6 +97,10 @@ def make_desc(mode: str | int, in_dtype, B: int, H: int, T: int, dk: int, dv: in
 
 def dplr_la_workspace_size(desc: dplr_desc) -> int:
     return int(library().dplr_la_workspace_size(ctypes.byref(desc)))
+
+
+def dplr_la_stage_workspace_size(desc: dplr_desc) -> int:
+    return int(library().dplr_la_stage_workspace_size(ctypes.byref(desc)))
 
 
 def dplr_la_check(desc: dplr_desc) -> int:
@@ -163,7 +169,10 @@ class Forward:
         self.r_ab, self.r_kv = self.desc.r_ab, self.desc.r_kv
         self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
         self.ws_bytes = dplr_la_workspace_size(self.desc)
-        self.workspace = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=self.device)
+        # zeroed once: on the fused path its first int32 is the device status word
+        self.workspace = torch.zeros(max(self.ws_bytes, 256), dtype=torch.uint8, device=self.device)
+        self.stage_ws_bytes = dplr_la_stage_workspace_size(self.desc)
+        self._stage_ws = None
         self.o = torch.empty((B, H, T, dv), dtype=torch.float32, device=self.device)
         self.S_T = torch.empty((B, H, dk, dv), dtype=torch.float32, device=self.device)
         self.kernels = dplr_la_kernel_count(self.desc)
@@ -198,18 +207,28 @@ class Forward:
             raise DplrError(st, "dplr_la_forward")
         return self.o, self.S_T
 
+    def device_status(self) -> int:
+        """The device status word of the fused path (0, or DPLR_ERR_TIMEOUT after a bounded wait gave up)."""
+        return int(self.workspace[:4].view(torch.int32).item())
+
+    def _stage_workspace(self):
+        if self._stage_ws is None:
+            self._stage_ws = torch.empty(max(self.stage_ws_bytes, 256), dtype=torch.uint8, device=self.device)
+        return self._stage_ws
+
     def chunk_maps(self, q, k=None, v=None, decay=None, beta=None, A=None, Bm=None, K=None, V=None,
                    stream: Optional[torch.cuda.Stream] = None):
         s = stream if stream is not None else torch.cuda.current_stream(self.device)
         st = dplr_la_chunk_maps(self.desc, _ptr(q), _ptr(k), _ptr(v), _ptr(decay), _ptr(beta), _ptr(A), _ptr(Bm),
-                                _ptr(K), _ptr(V), _ptr(self.o), _ptr(self.workspace), self.ws_bytes, s.cuda_stream)
+                                _ptr(K), _ptr(V), _ptr(self.o), _ptr(self._stage_workspace()), self.stage_ws_bytes,
+                                s.cuda_stream)
         if st != DPLR_OK:
             raise DplrError(st, "dplr_la_chunk_maps")
 
     def state_scan(self, S0=None, stream: Optional[torch.cuda.Stream] = None):
         s = stream if stream is not None else torch.cuda.current_stream(self.device)
-        st = dplr_la_state_scan(self.desc, _ptr(S0), _ptr(self.o), _ptr(self.S_T), _ptr(self.workspace),
-                                self.ws_bytes, s.cuda_stream)
+        st = dplr_la_state_scan(self.desc, _ptr(S0), _ptr(self.o), _ptr(self.S_T), _ptr(self._stage_workspace()),
+                                self.stage_ws_bytes, s.cuda_stream)
         if st != DPLR_OK:
             raise DplrError(st, "dplr_la_state_scan")
         return self.o, self.S_T

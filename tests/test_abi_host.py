@@ -30,7 +30,7 @@ def declared_symbols():
 def test_header_declares_expected_entry_points():
     syms = declared_symbols()
     for name in ("dplr_la_forward", "dplr_la_workspace_size", "dplr_status_string", "dplr_la_chunk_maps",
-                 "dplr_la_state_scan", "dplr_la_check", "dplr_la_kernel_count"):
+                 "dplr_la_state_scan", "dplr_la_check", "dplr_la_kernel_count", "dplr_la_stage_workspace_size"):
         assert name in syms
 
 
@@ -97,7 +97,7 @@ def test_bad_enum_and_chunk(sdl):
 
 
 def test_workspace_grows_with_length(sdl):
-    sizes = [sdl.dplr_la_workspace_size(sdl.make_desc("hdla", "bf16", 1, 2, T, 128, 128)) for T in (64, 128, 4096)]
+    sizes = [sdl.dplr_la_stage_workspace_size(sdl.make_desc("hdla", "bf16", 1, 2, T, 128, 128)) for T in (64, 128, 4096)]
     assert sizes[0] < sizes[1] < sizes[2]
     assert all(s % 256 == 0 for s in sizes)
 
@@ -150,8 +150,17 @@ def test_stage_entry_points_validate(sdl):
     ws = sdl.dplr_la_workspace_size(d)
     assert sdl.dplr_la_chunk_maps(d, None, FAKE, FAKE, FAKE, FAKE, None, None, None, None, FAKE, FAKE, ws,
                                   None) == sdl.dplr.DPLR_ERR_INVALID_ARG
+    ws = sdl.dplr_la_stage_workspace_size(d)
     assert sdl.dplr_la_state_scan(d, None, FAKE, None, FAKE, ws - 1, None) == sdl.dplr.DPLR_ERR_WORKSPACE
     assert sdl.dplr_la_state_scan(d, FAKE + 8, FAKE, None, FAKE, ws, None) == sdl.dplr.DPLR_ERR_INVALID_ARG
+
+
+def test_fused_path_workspace_is_a_status_word(sdl):
+    d = sdl.make_desc("gdn", "bf16", 8, 16, 8192, 128, 128)
+    assert sdl.dplr_la_workspace_size(d) == 256
+    assert sdl.dplr_la_stage_workspace_size(d) > 256
+    assert sdl.dplr_la_kernel_count(d) == 1
+    assert _fwd(sdl, d, ws_bytes=255) == sdl.dplr.DPLR_ERR_WORKSPACE
 
 
 def test_kernel_count(sdl):
