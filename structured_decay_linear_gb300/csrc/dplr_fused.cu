@@ -55,7 +55,7 @@ constexpr int FD = 128;    // dk = dv
 constexpr int FC = 64;     // tokens per chunk
 constexpr int FNT = 256;   // threads per CTA
 constexpr uint32_t kTmemCols = 512;
-constexpr int kLdL = 65;   // padded row stride (floats) of the fp32 L and M buffers
+constexpr int kLdL = 68;   // padded row stride (floats) of the fp32 L and M buffers (16-byte rows)
 
 // Tile geometry: byte strides between core matrices.
 constexpr uint32_t KQ_CB = 128 * 16;   // T_KQ: CBM with 128 rows (k rows 0-63, q rows 64-127)
@@ -78,12 +78,12 @@ struct GdnLayout {
     static constexpr int R2 = R1 + FD * FD * 2;
     static constexpr int T_ESH = R2;                        // [128 n][64 rho] RBM
     static constexpr int T_ESL = R2 + FD * FC * 2;
-    static constexpr int F_L = R2;                          // fp32 [64][65]
+    static constexpr int F_L = R2;                          // fp32 [64][68]
     static constexpr int T_QKH = R2 + 2 * FD * FC * 2;      // [64 t][64 sigma] RBM  -QK hi
     static constexpr int T_QKL = T_QKH + FC * FC * 2;       //                       -QK lo
-    static constexpr int F_M = T_QKL + FC * FC * 2;         // fp32 [64][65]
-    static constexpr int SCR = F_M + FC * kLdL * 4;         // fp32 scratch of the inverse (1024)
-    static constexpr int VEC = SCR + 4096;
+    static constexpr int F_M = T_QKL + FC * FC * 2;         // fp32 [64][68]
+    static constexpr int SCR = F_M + FC * kLdL * 4;         // fp32 scratch of the inverse (32 x 36)
+    static constexpr int VEC = SCR + 32 * 36 * 4;
     static constexpr int V_EF = VEC, V_EB = VEC + 256, V_BS = VEC + 512, V_SC = VEC + 768;
     static constexpr int RAW_G = VEC + 1024;                // [2][64] log gate
     static constexpr int RAW_B = RAW_G + 512;               // [2][64] beta
@@ -114,85 +114,110 @@ __device__ __forceinline__ void rbm_store8(uint32_t tile, int cols, int r, int c
                  pack_bf16(x[6], x[7]));
 }
 
-// x = hi + lo with both parts bf16.
+// x = hi + lo with both parts bf16 (one packed conversion per pair for each part).
 __device__ __forceinline__ void rbm_store8_split(uint32_t th, uint32_t tl, int cols, int r, int c, const float* x) {
-    float hi[8], lo[8];
+    uint32_t h[4], l[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        hi[i] = __bfloat162float(__float2bfloat16_rn(x[i]));
-        lo[i] = x[i] - hi[i];
+    for (int i = 0; i < 4; ++i) {
+        h[i] = pack_bf16(x[2 * i], x[2 * i + 1]);
+        const float h0 = __uint_as_float(h[i] << 16), h1 = __uint_as_float(h[i] & 0xFFFF0000u);
+        l[i] = pack_bf16(x[2 * i] - h0, x[2 * i + 1] - h1);
     }
-    rbm_store8(th, cols, r, c, hi);
-    rbm_store8(tl, cols, r, c, lo);
+    const uint32_t off = rbm_off(r, c, cols);
+    st_shared_v4(th + off, h[0], h[1], h[2], h[3]);
+    st_shared_v4(tl + off, l[0], l[1], l[2], l[3]);
 }
 
-// (I + L)^{-1} for a 64x64 strictly lower-triangular fp32 L (row stride kLdL): right-looking
-// solves of the four 16x16 diagonal blocks, then merges 16->32->64 with
-// [[A,0],[C,B]]^{-1} = [[A^{-1},0],[-B^{-1} C A^{-1}, B^{-1}]], each thread keeping several
-// independent accumulators. Writes -M and M Diag(ef) as bf16 RBM tiles.
+// (I + L)^{-1} for a 64x64 strictly lower-triangular fp32 L (row stride kLdL = 68 floats, so
+// rows are 16-byte aligned). The four 16x16 diagonal blocks are solved row by row (left-looking,
+// one column per thread, rows of L read as 16-byte broadcasts); the blocks are merged
+// 16 -> 32 -> 64 with [[A,0],[C,B]]^{-1} = [[A^{-1},0],[-B^{-1} C A^{-1}, B^{-1}]], the merge
+// products on the tensor cores in tf32 (their ~1e-3 relative error is below the bf16 rounding
+// the result gets next). Writes -M and M Diag(ef) as bf16 RBM tiles.
+__device__ __forceinline__ float4 lds4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+
+constexpr int kLds = 36;   // row stride (floats) of the merge scratch (32 rows)
+
+// Warp-level C[16x8] = A[16xK] * B[Kx8] with fp32 operands read as tf32 (mma.sync m16n8k8, fp32
+// accumulate); A and B row-major in shared memory with row strides lda / ldb. Fragment layout of
+// the PTX ISA: g = lane / 4, q = lane % 4; A (g, q), (g+8, q), (g, q+4), (g+8, q+4); B (q, g),
+// (q+4, g); C (g, 2q), (g, 2q+1), (g+8, 2q), (g+8, 2q+1).
+__device__ __forceinline__ void warp_mma_tf32(const float* A, int lda, const float* B, int ldb, int K, float (&c)[4]) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+    c[0] = c[1] = c[2] = c[3] = 0.f;
+    for (int k0 = 0; k0 < K; k0 += 8) {
+        const uint32_t a0 = __float_as_uint(A[g * lda + k0 + q]), a1 = __float_as_uint(A[(g + 8) * lda + k0 + q]);
+        const uint32_t a2 = __float_as_uint(A[g * lda + k0 + q + 4]), a3 = __float_as_uint(A[(g + 8) * lda + k0 + q + 4]);
+        const uint32_t b0 = __float_as_uint(B[(k0 + q) * ldb + g]), b1 = __float_as_uint(B[(k0 + q + 4) * ldb + g]);
+        asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                     "{%0,%1,%2,%3};"
+                     : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                     : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+}
+
+__device__ __forceinline__ void store_tile_16x8(float* C, int ldc, const float (&c)[4], float scale) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+    C[g * ldc + 2 * q] = scale * c[0];
+    C[g * ldc + 2 * q + 1] = scale * c[1];
+    C[(g + 8) * ldc + 2 * q] = scale * c[2];
+    C[(g + 8) * ldc + 2 * q + 1] = scale * c[3];
+}
+
 __device__ __forceinline__ void unit_lower_inverse64(const float* L, float* Mf, float* scr, uint32_t t_mn,
                                                      uint32_t t_my, const float* ef, int tid) {
-    if (tid < 64) {
+    if (tid < 64) {   // diagonal 16x16 blocks: M[i][j] = delta_ij - sum_{k<i} L[i][k] M[k][j]
         const int b = tid >> 4, j = tid & 15, o = 16 * b;
-        float s[16];
+        float m[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) s[i] = (i == j) ? 1.f : 0.f;
+        for (int i = 0; i < 16; ++i) {
+            const float* Lr = L + (o + i) * kLdL + o;
+            float acc0 = (i == j) ? 1.f : 0.f, acc1 = 0.f;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const float xk = s[k];
-#pragma unroll
-            for (int i = k + 1; i < 16; ++i) s[i] = fmaf(-L[(o + i) * kLdL + o + k], xk, s[i]);
+            for (int k4 = 0; k4 < 4; ++k4) {
+                if (4 * k4 < i) {
+                    const float4 l = lds4(Lr + 4 * k4);
+                    if (4 * k4 + 0 < i) acc0 = fmaf(-l.x, m[4 * k4 + 0], acc0);
+                    if (4 * k4 + 1 < i) acc1 = fmaf(-l.y, m[4 * k4 + 1], acc1);
+                    if (4 * k4 + 2 < i) acc0 = fmaf(-l.z, m[4 * k4 + 2], acc0);
+                    if (4 * k4 + 3 < i) acc1 = fmaf(-l.w, m[4 * k4 + 3], acc1);
+                }
+            }
+            m[i] = acc0 + acc1;
         }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) Mf[(o + i) * kLdL + o + j] = s[i];
+        for (int i = 0; i < 16; ++i) Mf[(o + i) * kLdL + o + j] = m[i];
     }
     __syncthreads();
-    {   // 32x32 blocks (0,1) and (2,3)
-        const int p = tid >> 7, e = tid & 127, o = 32 * p, i = e >> 3, jq = e & 7;
-        float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const float l = L[(o + 16 + i) * kLdL + o + k];
-            a0 = fmaf(l, Mf[(o + k) * kLdL + o + jq], a0);
-            a1 = fmaf(l, Mf[(o + k) * kLdL + o + jq + 8], a1);
+    // merges on the tensor cores (mma.sync tf32, fp32 accumulate): one 16x8 output tile per warp
+    const int warp = tid >> 5, lane = tid & 31;
+    {   // 16 -> 32 for the pairs of diagonal blocks (0,1) and (2,3); warps 0-3, warps 4-7 zero the
+        // blocks above the diagonal inside each 32x32 block
+        const int p = warp >> 1, ct = warp & 1, o = 32 * p;
+        if (warp < 4) {
+            float c[4];
+            warp_mma_tf32(L + (o + 16) * kLdL + o, kLdL, Mf + o * kLdL + o + 8 * ct, kLdL, 16, c);   // T = C A^{-1}
+            store_tile_16x8(scr + p * 16 * kLds + 8 * ct, kLds, c, 1.f);
+        } else {
+            const int e = tid - 128, r = e >> 2, cc = 4 * (e & 3), pp = r >> 4, rr = r & 15;
+            *reinterpret_cast<float4*>(Mf + (32 * pp + rr) * kLdL + 32 * pp + 16 + cc) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        scr[p * 256 + i * 16 + jq] = a0;
-        scr[p * 256 + i * 16 + jq + 8] = a1;
-        Mf[(o + i) * kLdL + o + 16 + jq] = 0.f;          // block above the diagonal
-        Mf[(o + i) * kLdL + o + 16 + jq + 8] = 0.f;
         __syncthreads();
-        float c0 = 0.f, c1 = 0.f;
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const float bb = Mf[(o + 16 + i) * kLdL + o + 16 + k];
-            c0 = fmaf(bb, scr[p * 256 + k * 16 + jq], c0);
-            c1 = fmaf(bb, scr[p * 256 + k * 16 + jq + 8], c1);
+        if (warp < 4) {
+            float c[4];
+            warp_mma_tf32(Mf + (o + 16) * kLdL + o + 16, kLdL, scr + p * 16 * kLds + 8 * ct, kLds, 16, c);  // B^{-1} T
+            store_tile_16x8(Mf + (o + 16) * kLdL + o + 8 * ct, kLdL, c, -1.f);
         }
-        Mf[(o + 16 + i) * kLdL + o + jq] = -c0;
-        Mf[(o + 16 + i) * kLdL + o + jq + 8] = -c1;
         __syncthreads();
     }
-    {   // 64x64: rows 32-63, columns 0-31
-        const int i = tid >> 3, jq = tid & 7;
-        float a[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-        for (int k = 0; k < 32; ++k) {
-            const float l = L[(32 + i) * kLdL + k];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) a[u] = fmaf(l, Mf[k * kLdL + jq + 8 * u], a[u]);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) scr[i * 32 + jq + 8 * u] = a[u];
+    {   // 32 -> 64: M[32:64, 0:32] = -B^{-1} (C A^{-1}); eight 16x8 tiles, one per warp
+        const int rt = warp >> 2, ct = warp & 3;
+        float c[4];
+        warp_mma_tf32(L + (32 + 16 * rt) * kLdL, kLdL, Mf + 8 * ct, kLdL, 32, c);
+        store_tile_16x8(scr + 16 * rt * kLds + 8 * ct, kLds, c, 1.f);
         __syncthreads();
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-        for (int k = 0; k < 32; ++k) {
-            const float bb = Mf[(32 + i) * kLdL + 32 + k];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) c[u] = fmaf(bb, scr[k * 32 + jq + 8 * u], c[u]);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) Mf[(32 + i) * kLdL + jq + 8 * u] = -c[u];
+        warp_mma_tf32(Mf + (32 + 16 * rt) * kLdL + 32, kLdL, scr + 8 * ct, kLds, 32, c);
+        store_tile_16x8(Mf + (32 + 16 * rt) * kLdL + 8 * ct, kLdL, c, -1.f);
         __syncthreads();
     }
     // bf16 tiles -M and M Diag(ef); the 32x32 block above the diagonal is zero
@@ -200,11 +225,14 @@ __device__ __forceinline__ void unit_lower_inverse64(const float* L, float* Mf, 
     for (int h = 0; h < 2; ++h) {
         const int item = tid + 256 * h, r = item & 63, c = (item >> 6) * 8;
         float x[8], y[8];
+        if ((c >> 5) > (r >> 5)) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float m = ((c >> 5) > (r >> 5)) ? 0.f : Mf[r * kLdL + c + i];
-            x[i] = -m;
-            y[i] = m * ef[c + i];
+            for (int i = 0; i < 8; ++i) { x[i] = 0.f; y[i] = 0.f; }
+        } else {
+            const float4 m0 = lds4(Mf + r * kLdL + c), m1 = lds4(Mf + r * kLdL + c + 4);
+            const float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) { x[i] = -m[i]; y[i] = m[i] * ef[c + i]; }
         }
         rbm_store8(t_mn, FC, r, c, x);
         rbm_store8(t_my, FC, r, c, y);
@@ -375,6 +403,10 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
             mma_chain(tmem + 0, smem_desc(tKQ, KQ_CB, 128), 2 * KQ_CB, smem_desc(tKQ, KQ_CB, 128), 2 * KQ_CB,
                       idesc_bf16(128, FC, false, false), FD, false);
             mma_commit(mbar_mma);
+            // O'^T = S'hi^T Q^T only needs the state and q: start it now, it finishes in the
+            // shadow of the CUDA-core phases (the later commits cover it)
+            mma_chain(tmem + 384, smem_desc(sbase + Ly::T_S, S_RB, 128), 2 * S_RB, smem_desc(tQ, KQ_CB, 128),
+                      2 * KQ_CB, idesc_bf16(128, FC, true, false), FD, false);
         }
         if (!wait_mma()) { failed = true; break; }
         {
@@ -384,9 +416,14 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
                 const int t = row;
                 const float eft = v_ef[t];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int sg = 32 * half + i;
-                    F_L[t * kLdL + sg] = (sg < t) ? eft * x[i] * v_bs[sg] : 0.f;
+                for (int i = 0; i < 32; i += 4) {
+                    float y[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int sg = 32 * half + i + u;
+                        y[u] = (sg < t) ? eft * x[i + u] * v_bs[sg] : 0.f;
+                    }
+                    *reinterpret_cast<float4*>(F_L + t * kLdL + 32 * half + i) = make_float4(y[0], y[1], y[2], y[3]);
                 }
             } else {                     // -QK row t (inclusive causal), hi + lo
                 const int t = row - FC;
@@ -454,13 +491,14 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
             const float ea = v_sc[0];
 #pragma unroll
             for (int i = 0; i < 64; i += 8) {
-                float x[8];
+                uint32_t l[4];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const float sp = ea * S[i + u];
-                    x[u] = sp - __bfloat162float(__float2bfloat16_rn(sp));
+                for (int u = 0; u < 4; ++u) {
+                    const float s0 = ea * S[i + 2 * u], s1 = ea * S[i + 2 * u + 1];
+                    const uint32_t h = pack_bf16(s0, s1);
+                    l[u] = pack_bf16(s0 - __uint_as_float(h << 16), s1 - __uint_as_float(h & 0xFFFF0000u));
                 }
-                rbm_store8(sbase + Ly::T_SLO, FD, row, 64 * half + i, x);
+                st_shared_v4(sbase + Ly::T_SLO + rbm_off(row, 64 * half + i, FD), l[0], l[1], l[2], l[3]);
             }
         }
         fence_async_smem();
@@ -476,7 +514,6 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
             mma_chain(tmem + 256, dKmn, 256, smem_desc(sbase + Ly::T_ESL, 128, N64_RB), 256, idX, FC, true);
             const uint64_t dQ = smem_desc(tQ, KQ_CB, 128);                    // q rows, K-major B
             const uint32_t idO = idesc_bf16(128, FC, true, false), idO2 = idesc_bf16(128, FC, false, false);
-            mma_chain(tmem + 384, smem_desc(sbase + Ly::T_S, S_RB, 128), 2 * S_RB, dQ, 2 * KQ_CB, idO, FD, false);
             mma_chain(tmem + 384, smem_desc(sbase + Ly::T_SLO, S_RB, 128), 2 * S_RB, dQ, 2 * KQ_CB, idO, FD, true);
             mma_chain(tmem + 384, smem_desc(sbase + Ly::T_ESH, 128, N64_RB), 256,
                       smem_desc(sbase + Ly::T_QKH, 128, N64_RB), 256, idO2, FC, true);
