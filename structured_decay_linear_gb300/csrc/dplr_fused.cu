@@ -53,46 +53,46 @@ using namespace sm100;
 
 constexpr int FD = 128;    // dk = dv
 constexpr int FC = 64;     // tokens per chunk
-constexpr int FNT = 256;   // threads per CTA
+constexpr int FNT = 288;   // threads per CTA: warps 0-7 CUDA-core work, warp 8 issues MMAs and copies
+constexpr int kSimt = 256; // threads of the CUDA-core group (named barrier 1)
 constexpr uint32_t kTmemCols = 512;
 constexpr int kLdL = 68;   // padded row stride (floats) of the fp32 L and M buffers (16-byte rows)
 
 // Tile geometry: byte strides between core matrices.
 constexpr uint32_t KQ_CB = 128 * 16;   // T_KQ: CBM with 128 rows (k rows 0-63, q rows 64-127)
 constexpr uint32_t V_CB = 64 * 16;     // T_V:  CBM with 64 rows
-constexpr uint32_t S_RB = 128 * 16;    // T_S / T_SLO: RBM with 128 columns
 constexpr uint32_t N64_RB = 64 * 16;   // RBM tiles with 64 columns
 
 struct GdnLayout {
-    static constexpr int T_KQ0 = 0;                         // [128][128] CBM, two buffers
+    static constexpr int T_KQ0 = 0;                         // [128][128] CBM (k rows 0-63, q rows 64-127), 2 buffers
     static constexpr int T_KQ1 = T_KQ0 + 128 * FD * 2;
     static constexpr int T_V = T_KQ1 + 128 * FD * 2;        // [64][128] CBM  v
-    static constexpr int T_S = T_V + FC * FD * 2;           // [128 c][128 n] RBM  S' hi
-    // region R1 (32 KB): -M, M Diag(ef), Y^T; after E it holds S' lo
-    static constexpr int R1 = T_S + FD * FD * 2;
-    static constexpr int T_MN = R1;                         // [64 rho][64 sigma] RBM  -M
-    static constexpr int T_MY = R1 + FC * FC * 2;           // [64][64] RBM  M Diag(ef)
-    static constexpr int T_YT = R1 + 2 * FC * FC * 2;       // [128 c][64 rho] RBM  Y^T
-    static constexpr int T_SLO = R1;                        // [128][128] RBM  S' lo
-    // region R2 (32 KB): Es^T hi / lo; aliased by the fp32 L buffer before E
-    static constexpr int R2 = R1 + FD * FD * 2;
-    static constexpr int T_ESH = R2;                        // [128 n][64 rho] RBM
-    static constexpr int T_ESL = R2 + FD * FC * 2;
-    static constexpr int F_L = R2;                          // fp32 [64][68]
-    static constexpr int T_QKH = R2 + 2 * FD * FC * 2;      // [64 t][64 sigma] RBM  -QK hi
-    static constexpr int T_QKL = T_QKH + FC * FC * 2;       //                       -QK lo
-    static constexpr int F_M = T_QKL + FC * FC * 2;         // fp32 [64][68]
+    static constexpr int T_MN = T_V + FC * FD * 2;          // [64 rho][64 sigma] RBM  -M
+    static constexpr int T_MY = T_MN + FC * FC * 2;         // [64][64] RBM  M Diag(ef)
+    static constexpr int T_YT = T_MY + FC * FC * 2;         // [128 c][64 rho] RBM  Y^T
+    static constexpr int T_ESH = T_YT + FD * FC * 2;        // [128 n][64 rho] RBM  Es^T hi
+    static constexpr int T_ESL = T_ESH + FD * FC * 2;       //                      Es^T lo
+    static constexpr int T_QK = T_ESL + FD * FC * 2;        // 2 buffers x {hi, lo} [64 t][64 sigma] RBM  -QK
+    static constexpr int F_L = T_QK + 4 * FC * FC * 2;      // fp32 [64][68]
+    static constexpr int F_M = F_L + FC * kLdL * 4;         // fp32 [64][68]
     static constexpr int SCR = F_M + FC * kLdL * 4;         // fp32 scratch of the inverse (32 x 36)
-    static constexpr int VEC = SCR + 32 * 36 * 4;
-    static constexpr int V_EF = VEC, V_EB = VEC + 256, V_BS = VEC + 512, V_SC = VEC + 768;
-    static constexpr int RAW_G = VEC + 1024;                // [2][64] log gate
+    static constexpr int VEC = SCR + 32 * 36 * 4;          // 2 buffers x {ef[64], eb[64], bs[64], sc[..]}
+    static constexpr int kVec = 1024;
+    static constexpr int RAW_G = VEC + 2 * kVec;            // [2][64] log gate
     static constexpr int RAW_B = RAW_G + 512;               // [2][64] beta
-    static constexpr int BAR = RAW_B + 512;
-    static constexpr int TOTAL = BAR + 64;
+    static constexpr int BAR = RAW_B + 512;                 // 13 mbarriers + TMEM address
+    static constexpr int TOTAL = BAR + 112;
 };
-static_assert(GdnLayout::T_SLO + FD * FD * 2 == GdnLayout::R2, "S' lo must exactly fill region R1");
-static_assert(GdnLayout::F_L + FC * kLdL * 4 <= GdnLayout::T_QKH, "L must fit in region R2");
 static_assert(GdnLayout::TOTAL <= 227 * 1024, "shared memory budget");
+
+// TMEM columns (512 allocated)
+constexpr uint32_t TM_D = 0;      // [K;Q] K^T          128 lanes x 64
+constexpr uint32_t TM_Y = 64;     // Y^T                128 x 64
+constexpr uint32_t TM_E = 128;    // E^T                128 x 64
+constexpr uint32_t TM_X = 192;    // X^T                128 x 128
+constexpr uint32_t TM_O = 320;    // O'^T               128 x 64
+constexpr uint32_t TM_SH = 384;   // S'^T hi (A operand, bf16 pairs) 128 x 64
+constexpr uint32_t TM_SL = 448;   // S'^T lo
 
 struct FusedArgs {
     const __nv_bfloat16* q; const __nv_bfloat16* k; const __nv_bfloat16* v;
@@ -188,9 +188,9 @@ __device__ __forceinline__ void unit_lower_inverse64(const float* L, float* Mf, 
 #pragma unroll
         for (int i = 0; i < 16; ++i) Mf[(o + i) * kLdL + o + j] = m[i];
     }
-    __syncthreads();
+    named_sync(1, kSimt);
     // merges on the tensor cores (mma.sync tf32, fp32 accumulate): one 16x8 output tile per warp
-    const int warp = tid >> 5, lane = tid & 31;
+    const int warp = tid >> 5;
     {   // 16 -> 32 for the pairs of diagonal blocks (0,1) and (2,3); warps 0-3, warps 4-7 zero the
         // blocks above the diagonal inside each 32x32 block
         const int p = warp >> 1, ct = warp & 1, o = 32 * p;
@@ -202,23 +202,23 @@ __device__ __forceinline__ void unit_lower_inverse64(const float* L, float* Mf, 
             const int e = tid - 128, r = e >> 2, cc = 4 * (e & 3), pp = r >> 4, rr = r & 15;
             *reinterpret_cast<float4*>(Mf + (32 * pp + rr) * kLdL + 32 * pp + 16 + cc) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        __syncthreads();
+        named_sync(1, kSimt);
         if (warp < 4) {
             float c[4];
             warp_mma_tf32(Mf + (o + 16) * kLdL + o + 16, kLdL, scr + p * 16 * kLds + 8 * ct, kLds, 16, c);  // B^{-1} T
             store_tile_16x8(Mf + (o + 16) * kLdL + o + 8 * ct, kLdL, c, -1.f);
         }
-        __syncthreads();
+        named_sync(1, kSimt);
     }
     {   // 32 -> 64: M[32:64, 0:32] = -B^{-1} (C A^{-1}); eight 16x8 tiles, one per warp
         const int rt = warp >> 2, ct = warp & 3;
         float c[4];
         warp_mma_tf32(L + (32 + 16 * rt) * kLdL, kLdL, Mf + 8 * ct, kLdL, 32, c);
         store_tile_16x8(scr + 16 * rt * kLds + 8 * ct, kLds, c, 1.f);
-        __syncthreads();
+        named_sync(1, kSimt);
         warp_mma_tf32(Mf + (32 + 16 * rt) * kLdL + 32, kLdL, scr + 8 * ct, kLds, 32, c);
         store_tile_16x8(Mf + (32 + 16 * rt) * kLdL + 8 * ct, kLdL, c, -1.f);
-        __syncthreads();
+        named_sync(1, kSimt);
     }
     // bf16 tiles -M and M Diag(ef); the 32x32 block above the diagonal is zero
 #pragma unroll
@@ -245,103 +245,234 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
     using Ly = GdnLayout;
     extern __shared__ __align__(1024) unsigned char smem[];
     const uint32_t sbase = smem_addr(smem);
-    uint64_t* mbar_mma = reinterpret_cast<uint64_t*>(smem + Ly::BAR);
-    uint64_t* mbar_kq = reinterpret_cast<uint64_t*>(smem + Ly::BAR + 8);    // [2]
-    uint64_t* mbar_v = reinterpret_cast<uint64_t*>(smem + Ly::BAR + 24);
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Ly::BAR + 32);
-    float* v_ef = reinterpret_cast<float*>(smem + Ly::V_EF);
-    float* v_eb = reinterpret_cast<float*>(smem + Ly::V_EB);
-    float* v_bs = reinterpret_cast<float*>(smem + Ly::V_BS);
-    float* v_sc = reinterpret_cast<float*>(smem + Ly::V_SC);   // [0] e^{a}, [1] e^{G_C - a}, [2] e^{G_C}
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Ly::BAR);
+    // MMA completions (issuer -> CUDA-core group)
+    uint64_t* mbar_E = bars + 0;
+    uint64_t* mbar_D = bars + 1;
+    uint64_t* mbar_XO = bars + 2;
+    uint64_t* mbar_Y = bars + 3;
+    // bulk copies
+    uint64_t* mbar_kq = bars + 4;    // [2]
+    uint64_t* mbar_v = bars + 6;
+    // CUDA-core group -> issuer: prologue staged, S' in TMEM, Es tiles, M tiles
+    uint64_t* rdy_P = bars + 7;
+    uint64_t* rdy_S = bars + 8;
+    uint64_t* rdy_E = bars + 9;
+    uint64_t* rdy_M = bars + 10;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 11);
     float* scr = reinterpret_cast<float*>(smem + Ly::SCR);
     float* F_L = reinterpret_cast<float*>(smem + Ly::F_L);
     float* F_M = reinterpret_cast<float*>(smem + Ly::F_M);
     float* rawG = reinterpret_cast<float*>(smem + Ly::RAW_G);
     float* rawB = reinterpret_cast<float*>(smem + Ly::RAW_B);
+    auto vec = [&](int buf) { return reinterpret_cast<float*>(smem + Ly::VEC + buf * Ly::kVec); };
+    // vec(b): [0,64) ef, [64,128) eb, [128,192) bs = beta eb, [192] e^{a}, [193] e^{G_C - a}, [194] e^{G_C}
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quad = warp & 3, half = warp >> 2;
-    const int row = tid & 127;                  // TMEM lane of this thread
+    const int quad = warp & 3, half = (warp >> 2) & 1;
+    const int row = tid & 127;                  // TMEM lane of this thread (CUDA-core group)
+    const bool issuer = warp == 8;
     const size_t bh = blockIdx.x;
     const int T = pl.T;
     const int nchunk = (T + FC - 1) / FC;
-    const int nfull = T / FC;                   // chunks loaded by TMA
+    const int nfull = T / FC;                   // chunks loaded by TMA (only the last may be ragged)
     const size_t tok_base = bh * (size_t)T;
     const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
 
     if (tid == 0) {
-        mbar_init(mbar_mma, 1);
-        mbar_init(&mbar_kq[0], 1);
-        mbar_init(&mbar_kq[1], 1);
-        mbar_init(mbar_v, 1);
+        for (int i = 0; i < 11; ++i) mbar_init(bars + i, 1);
         mbar_fence_init();
     }
     if (warp == 0) tmem_alloc(tmem_holder, kTmemCols);
-    if (tid < FC) {
-        rawG[tid] = (tid < T) ? args.decay[tok_base + tid] : 0.f;
-        rawB[tid] = (tid < T) ? args.beta[tok_base + tid] : 0.f;
+    if (tid < 2 * FC) {   // gates of chunks 0 and 1
+        const int t = tid;
+        rawG[t] = (t < T) ? args.decay[tok_base + t] : 0.f;
+        rawB[t] = (t < T) ? args.beta[tok_base + t] : 0.f;
     }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = *tmem_holder;
-
-    auto issue_kq = [&](int j) {   // thread 0
-        const int y = static_cast<int>(tok_base + (size_t)j * FC);
-        unsigned char* dst = smem + ((j & 1) ? Ly::T_KQ1 : Ly::T_KQ0);
-        mbar_expect_tx(&mbar_kq[j & 1], 2u * FC * FD * 2);
-        for (int cb = 0; cb < FD / 8; ++cb) {
-            tma_load_2d(dst + cb * KQ_CB, &tm_k, 8 * cb, y, &mbar_kq[j & 1]);
-            tma_load_2d(dst + cb * KQ_CB + FC * 16, &tm_q, 8 * cb, y, &mbar_kq[j & 1]);
-        }
-    };
-    auto issue_v = [&](int j) {    // thread 0
-        const int y = static_cast<int>(tok_base + (size_t)j * FC);
-        mbar_expect_tx(mbar_v, FC * FD * 2);
-        for (int cb = 0; cb < FD / 8; ++cb) tma_load_2d(smem + Ly::T_V + cb * V_CB, &tm_v, 8 * cb, y, mbar_v);
-    };
-    if (tid == 0) {
-        if (nfull > 0) { issue_kq(0); issue_v(0); }
-        if (nfull > 1) issue_kq(1);
-    }
-
-    // fp32 state: row `row` of S, columns [64*half, 64*half + 64)
-    float S[64];
-#pragma unroll
-    for (int i = 0; i < 64; ++i) S[i] = args.S0 ? args.S0[(bh * FD + row) * FD + 64 * half + i] : 0.f;
-
-    uint32_t mma_phase = 0;
+    auto tKQ_of = [&](int jj) -> uint32_t { return sbase + ((jj & 1) ? Ly::T_KQ1 : Ly::T_KQ0); };
+    auto tQK_of = [&](int jj, int lo) -> uint32_t { return sbase + Ly::T_QK + ((jj & 1) * 2 + lo) * FC * FC * 2; };
     bool failed = false;
-    // thread 0 tracks outstanding bulk loads so an early exit can drain them
-    int kq_issued = (nfull > 0) + (nfull > 1), kq_done = 0, v_issued = (nfull > 0), v_done = 0;
-    auto wait_mma = [&]() -> bool {
-        const bool got = mbar_wait(mbar_mma, mma_phase);
-        mma_phase ^= 1u;
-        const bool bad = __syncthreads_or(!got) != 0;
-        fence_after_sync();
-        return !bad;
-    };
 
-    for (int j = 0; j < nchunk; ++j) {
-        const int t0 = j * FC;
-        const int valid = min(FC, T - t0);
-        const size_t g0 = tok_base + t0;
-        const int b = j & 1;
-        const uint32_t tKQ = sbase + (b ? Ly::T_KQ1 : Ly::T_KQ0);
-        const uint32_t tQ = tKQ + FC * 16;        // q rows start at row 64 of the CBM tile
-        float* gcur = rawG + b * FC;
-        float* bcur = rawB + b * FC;
-        // prefetch the next chunk's k, q (its buffer was last read by chunk j - 1) and gate/beta
-        if (tid == 0 && j >= 1 && j + 1 < nfull) { issue_kq(j + 1); ++kq_issued; }
-        float g_next = 0.f, b_next = 0.f;
-        if (tid < FC && t0 + FC + tid < T) {
-            g_next = args.decay[g0 + FC + tid];
-            b_next = args.beta[g0 + FC + tid];
+    if (issuer) {
+        // ======================= issuer warp: MMAs (lane 0) and bulk copies (all lanes) =======================
+        uint32_t kq_pend = 0;   // bit b: a k/q copy into buffer b is in flight
+        bool v_pend = false;
+        auto issue_kq = [&](int jj) {     // 32 boxes, one per lane
+            const int y = static_cast<int>(tok_base + (size_t)jj * FC);
+            unsigned char* dst = smem + ((jj & 1) ? Ly::T_KQ1 : Ly::T_KQ0);
+            if (lane == 0) mbar_expect_tx(&mbar_kq[jj & 1], 2u * FC * FD * 2);
+            __syncwarp();
+            const int cb = lane & 15;
+            if (lane < 16) tma_load_2d(dst + cb * KQ_CB, &tm_k, 8 * cb, y, &mbar_kq[jj & 1]);
+            else tma_load_2d(dst + cb * KQ_CB + FC * 16, &tm_q, 8 * cb, y, &mbar_kq[jj & 1]);
+            kq_pend |= 1u << (jj & 1);
+        };
+        auto issue_v = [&](int jj) {      // 16 boxes
+            const int y = static_cast<int>(tok_base + (size_t)jj * FC);
+            if (lane == 0) mbar_expect_tx(mbar_v, FC * FD * 2);
+            __syncwarp();
+            if (lane < 16) tma_load_2d(smem + Ly::T_V + lane * V_CB, &tm_v, 8 * lane, y, mbar_v);
+            v_pend = true;
+        };
+        auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait(bar, parity);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            fence_after_sync();
+            return ok;
+        };
+        auto wait_kq = [&](int jj) -> bool {
+            if (jj >= nfull) return true;
+            const bool ok = wait_warp(&mbar_kq[jj & 1], (jj >> 1) & 1);
+            kq_pend &= ~(1u << (jj & 1));
+            return ok;
+        };
+        auto wait_v = [&](int jj) -> bool {
+            if (jj >= nfull) return true;
+            const bool ok = wait_warp(mbar_v, jj & 1);
+            v_pend = false;
+            return ok;
+        };
+        auto issue_D = [&](int jj) {
+            if (lane == 0) {
+                const uint32_t tk = tKQ_of(jj);
+                mma_chain(tmem + TM_D, smem_desc(tk, KQ_CB, 128), 2 * KQ_CB, smem_desc(tk, KQ_CB, 128), 2 * KQ_CB,
+                          idesc_bf16(128, FC, false, false), FD, false);
+                mma_commit(mbar_D);
+            }
+            __syncwarp();
+        };
+        auto issue_Y = [&](int jj) {   // Y^T = K^T (M Diag(ef))^T
+            if (lane == 0) {
+                mma_chain(tmem + TM_Y, smem_desc(tKQ_of(jj), 128, KQ_CB), 256, smem_desc(sbase + Ly::T_MY, 128, N64_RB),
+                          256, idesc_bf16(128, FC, true, false), FC, false);
+                mma_commit(mbar_Y);
+            }
+            __syncwarp();
+        };
+        if (nchunk > 0) {
+            if (nfull > 0) { issue_kq(0); issue_v(0); }
+            if (nfull > 1) issue_kq(1);
+            // prologue: D(0), then Y(0) once the CUDA-core group has the M tiles
+            failed = !wait_warp(rdy_P, 0) || !wait_kq(0);
+            if (!failed) {
+                issue_D(0);
+                failed = !wait_warp(rdy_M, 0);
+            }
+            if (!failed) issue_Y(0);
         }
-
-        // ---- a2: cumulative log-gate, anchor a = G_C / 2, per-token factors
-        if (warp == 0) {
-            const float x0 = gcur[2 * lane], x1 = gcur[2 * lane + 1];
+        for (int j = 0; j < nchunk && !failed; ++j) {
+            const int b = j & 1;
+            const bool has_next = j + 1 < nchunk;
+            // E(j), O'(j) from the state; D(j+1) right behind them
+            if (!wait_warp(rdy_S, b) || !wait_v(j)) { failed = true; break; }
+            if (lane == 0) {
+                const uint32_t tk = tKQ_of(j);
+                mma_chain_tmem_a(tmem + TM_E, tmem + TM_SH, smem_desc(sbase + Ly::T_YT, N64_RB, 128), 2 * N64_RB,
+                                 idesc_bf16(128, FC, false, true), FD, false);                    // S'^T Y^T
+                mma_chain(tmem + TM_E, smem_desc(sbase + Ly::T_V, 128, V_CB), 256,
+                          smem_desc(sbase + Ly::T_MN, 128, N64_RB), 256, idesc_bf16(128, FC, true, false), FC,
+                          true);                                                                  // + V^T (-M)^T
+                mma_commit(mbar_E);
+                const uint64_t dQ = smem_desc(tk + FC * 16, KQ_CB, 128);                          // q rows, K-major
+                mma_chain_tmem_a(tmem + TM_O, tmem + TM_SH, dQ, 2 * KQ_CB, idesc_bf16(128, FC, false, false), FD, false);
+                mma_chain_tmem_a(tmem + TM_O, tmem + TM_SL, dQ, 2 * KQ_CB, idesc_bf16(128, FC, false, false), FD, true);
+            }
+            __syncwarp();
+            if (has_next) {
+                if (!wait_kq(j + 1)) { failed = true; break; }
+                issue_D(j + 1);
+            }
+            // v of the next chunk once E(j) has read it
+            if (!wait_warp(mbar_E, b)) { failed = true; break; }
+            if (has_next && j + 1 < nfull) issue_v(j + 1);
+            // X(j), O'(j) from Es
+            if (!wait_warp(rdy_E, b)) { failed = true; break; }
+            if (lane == 0) {
+                const uint32_t tk = tKQ_of(j);
+                const uint64_t dK = smem_desc(tk, 128, KQ_CB);               // k rows, MN-major B (K = rho)
+                const uint32_t idX = idesc_bf16(128, FD, false, true), idO = idesc_bf16(128, FC, false, false);
+                mma_chain(tmem + TM_X, smem_desc(sbase + Ly::T_ESH, 128, N64_RB), 256, dK, 256, idX, FC, false);
+                mma_chain(tmem + TM_X, smem_desc(sbase + Ly::T_ESL, 128, N64_RB), 256, dK, 256, idX, FC, true);
+                mma_chain(tmem + TM_O, smem_desc(sbase + Ly::T_ESH, 128, N64_RB), 256,
+                          smem_desc(tQK_of(j, 0), 128, N64_RB), 256, idO, FC, true);
+                mma_chain(tmem + TM_O, smem_desc(sbase + Ly::T_ESL, 128, N64_RB), 256,
+                          smem_desc(tQK_of(j, 0), 128, N64_RB), 256, idO, FC, true);
+                mma_chain(tmem + TM_O, smem_desc(sbase + Ly::T_ESH, 128, N64_RB), 256,
+                          smem_desc(tQK_of(j, 1), 128, N64_RB), 256, idO, FC, true);
+                mma_commit(mbar_XO);
+            }
+            __syncwarp();
+            // Y(j+1) once its M tiles are ready
+            if (has_next) {
+                if (!wait_warp(rdy_M, (j + 1) & 1)) { failed = true; break; }
+                issue_Y(j + 1);
+            }
+            // k, q of chunk j + 2 into buffer b once X(j), O(j) are done
+            if (!wait_warp(mbar_XO, b)) { failed = true; break; }
+            if (j + 2 < nfull) issue_kq(j + 2);
+        }
+        if (failed) {
+            if (lane == 0) {
+                atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
+                uint64_t* drain = bars + 12;   // spare slot: a commit now tracks every earlier MMA
+                mbar_init(drain, 1);
+                mbar_fence_init();
+                mma_commit(drain);
+                mbar_wait(drain, 0, 400000000LL);
+                for (int i = 0; i < 2; ++i)
+                    if (kq_pend & (1u << i)) { mbar_wait(&mbar_kq[i], 0, 400000000LL); mbar_wait(&mbar_kq[i], 1, 400000000LL); }
+                if (v_pend) { mbar_wait(mbar_v, 0, 400000000LL); mbar_wait(mbar_v, 1, 400000000LL); }
+            }
+            __syncwarp();
+        }
+    } else {
+        // ======================= CUDA-core group (warps 0-7) =======================
+        auto sync = [&]() { named_sync(1, kSimt); };
+        auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
+            const bool got = mbar_wait(bar, parity);
+            const bool bad = named_sync_or(1, kSimt, !got);
+            fence_after_sync();
+            return !bad;
+        };
+        auto signal = [&](uint64_t* bar) {   // after a group sync: one arrival
+            if (tid == 0) mbar_arrive(bar);
+        };
+        auto plain_kq = [&](int jj) {        // ragged (last) chunk: zero rows past the end
+            const int valid = T - jj * FC;
+            const size_t g0 = tok_base + (size_t)jj * FC;
+            const uint32_t tk = tKQ_of(jj), tq = tk + FC * 16;
+            for (int i = tid; i < FC * (FD / 8); i += kSimt) {
+                const int t = i & (FC - 1), cb = i >> 6;
+                uint4 zq = make_uint4(0, 0, 0, 0), zk = zq;
+                if (t < valid) {
+                    zq = *reinterpret_cast<const uint4*>(args.q + (g0 + t) * FD + 8 * cb);
+                    zk = *reinterpret_cast<const uint4*>(args.k + (g0 + t) * FD + 8 * cb);
+                }
+                st_shared_v4(tk + cb * KQ_CB + t * 16, zk.x, zk.y, zk.z, zk.w);
+                st_shared_v4(tq + cb * KQ_CB + t * 16, zq.x, zq.y, zq.z, zq.w);
+            }
+        };
+        auto plain_v = [&](int jj) {
+            const int valid = T - jj * FC;
+            const size_t g0 = tok_base + (size_t)jj * FC;
+            for (int i = tid; i < FC * (FD / 8); i += kSimt) {
+                const int t = i & (FC - 1), cb = i >> 6;
+                uint4 zv = make_uint4(0, 0, 0, 0);
+                if (t < valid) zv = *reinterpret_cast<const uint4*>(args.v + (g0 + t) * FD + 8 * cb);
+                st_shared_v4(sbase + Ly::T_V + cb * V_CB + t * 16, zv.x, zv.y, zv.z, zv.w);
+            }
+        };
+        auto gate_factors = [&](int jj) {    // warp 0
+            if (warp != 0) return;
+            const float* g = rawG + (jj & 1) * FC;
+            const float* be = rawB + (jj & 1) * FC;
+            float* vf = vec(jj & 1);
+            const float x0 = g[2 * lane], x1 = g[2 * lane + 1];
             float s = x0 + x1;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -352,76 +483,33 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
             const float a = 0.5f * gc;
             const float G1 = s, G0 = s - x1;
             const float e0 = __expf(a - G0), e1 = __expf(a - G1);
-            v_ef[2 * lane] = __expf(G0 - a);
-            v_ef[2 * lane + 1] = __expf(G1 - a);
-            v_eb[2 * lane] = e0;
-            v_eb[2 * lane + 1] = e1;
-            v_bs[2 * lane] = bcur[2 * lane] * e0;
-            v_bs[2 * lane + 1] = bcur[2 * lane + 1] * e1;
+            vf[2 * lane] = __expf(G0 - a);
+            vf[2 * lane + 1] = __expf(G1 - a);
+            vf[64 + 2 * lane] = e0;
+            vf[64 + 2 * lane + 1] = e1;
+            vf[128 + 2 * lane] = be[2 * lane] * e0;
+            vf[128 + 2 * lane + 1] = be[2 * lane + 1] * e1;
             if (lane == 0) {
-                v_sc[0] = __expf(a);
-                v_sc[1] = __expf(gc - a);
-                v_sc[2] = __expf(gc);
+                vf[192] = __expf(a);
+                vf[193] = __expf(gc - a);
+                vf[194] = __expf(gc);
             }
-        }
-        // ragged last chunk: plain loads (zero rows past the end) straight into the CBM tiles
-        if (valid < FC) {
-            for (int i = tid; i < FC * (FD / 8); i += FNT) {
-                const int t = i & (FC - 1), cb = i >> 6;
-                uint4 zq = make_uint4(0, 0, 0, 0), zk = zq, zv = zq;
-                if (t < valid) {
-                    zq = *reinterpret_cast<const uint4*>(args.q + (g0 + t) * FD + 8 * cb);
-                    zk = *reinterpret_cast<const uint4*>(args.k + (g0 + t) * FD + 8 * cb);
-                    zv = *reinterpret_cast<const uint4*>(args.v + (g0 + t) * FD + 8 * cb);
-                }
-                st_shared_v4(tKQ + cb * KQ_CB + t * 16, zk.x, zk.y, zk.z, zk.w);
-                st_shared_v4(tQ + cb * KQ_CB + t * 16, zq.x, zq.y, zq.z, zq.w);
-                st_shared_v4(sbase + Ly::T_V + cb * V_CB + t * 16, zv.x, zv.y, zv.z, zv.w);
-            }
-        }
-        __syncthreads();
-        // S' hi = bf16(e^{a} S_{j-1}), RBM [c][n]
-        {
-            const float ea = v_sc[0];
-#pragma unroll
-            for (int i = 0; i < 64; i += 8) {
-                float x[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) x[u] = ea * S[i + u];
-                rbm_store8(sbase + Ly::T_S, FD, row, 64 * half + i, x);
-            }
-        }
-        fence_async_smem();
-        __syncthreads();
-
-        // ---- a4: D = [K ; Q] K^T (M = 128 rows of k then q, N = 64 rows of k)
-        if (tid == 0) {
-            bool ok = true;
-            if (valid == FC) { ok = mbar_wait(&mbar_kq[b], (j >> 1) & 1); ++kq_done; }
-            if (!ok) atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
-            fence_after_sync();
-            mma_chain(tmem + 0, smem_desc(tKQ, KQ_CB, 128), 2 * KQ_CB, smem_desc(tKQ, KQ_CB, 128), 2 * KQ_CB,
-                      idesc_bf16(128, FC, false, false), FD, false);
-            mma_commit(mbar_mma);
-            // O'^T = S'hi^T Q^T only needs the state and q: start it now, it finishes in the
-            // shadow of the CUDA-core phases (the later commits cover it)
-            mma_chain(tmem + 384, smem_desc(sbase + Ly::T_S, S_RB, 128), 2 * S_RB, smem_desc(tQ, KQ_CB, 128),
-                      2 * KQ_CB, idesc_bf16(128, FC, true, false), FD, false);
-        }
-        if (!wait_mma()) { failed = true; break; }
-        {
+        };
+        // L and -QK of chunk jj from D: L -> F_L (fp32), -QK -> QK tiles (hi + lo) of buffer jj & 1
+        auto epi_D = [&](int jj) {
+            const float* vf = vec(jj & 1);
             float x[32];
-            tmem_ld32(tmem + lane_off + 32 * half, x);
+            tmem_ld32(tmem + TM_D + lane_off + 32 * half, x);
             if (row < FC) {              // L row t: ef_t D_ts beta_s eb_s for s < t
                 const int t = row;
-                const float eft = v_ef[t];
+                const float eft = vf[t];
 #pragma unroll
                 for (int i = 0; i < 32; i += 4) {
                     float y[4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         const int sg = 32 * half + i + u;
-                        y[u] = (sg < t) ? eft * x[i + u] * v_bs[sg] : 0.f;
+                        y[u] = (sg < t) ? eft * x[i + u] * vf[128 + sg] : 0.f;
                     }
                     *reinterpret_cast<float4*>(F_L + t * kLdL + 32 * half + i) = make_float4(y[0], y[1], y[2], y[3]);
                 }
@@ -434,134 +522,156 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
                 }
 #pragma unroll
                 for (int i = 0; i < 32; i += 8)
-                    rbm_store8_split(sbase + Ly::T_QKH, sbase + Ly::T_QKL, FC, t, 32 * half + i, x + i);
+                    rbm_store8_split(tQK_of(jj, 0), tQK_of(jj, 1), FC, t, 32 * half + i, x + i);
             }
-        }
-        fence_before_sync();
-        __syncthreads();
-
-        // ---- a5: M = (I + L)^{-1}; tiles -M and M Diag(ef)
-        unit_lower_inverse64(F_L, F_M, scr, sbase + Ly::T_MN, sbase + Ly::T_MY, v_ef, tid);
-        fence_async_smem();
-        __syncthreads();
-
-        // ---- Y^T = K^T (M Diag(ef))^T   (A: k rows as MN-major, B: M Diag(ef) K-major)
-        if (tid == 0) {
-            fence_after_sync();
-            mma_chain(tmem + 64, smem_desc(tKQ, 128, KQ_CB), 256, smem_desc(sbase + Ly::T_MY, 128, N64_RB), 256,
-                      idesc_bf16(128, FC, true, false), FC, false);
-            mma_commit(mbar_mma);
-        }
-        if (!wait_mma()) { failed = true; break; }
-        {
+        };
+        auto epi_Y = [&]() {
             float x[32];
-            tmem_ld32(tmem + 64 + lane_off + 32 * half, x);
+            tmem_ld32(tmem + TM_Y + lane_off + 32 * half, x);
 #pragma unroll
             for (int i = 0; i < 32; i += 8) rbm_store8(sbase + Ly::T_YT, FC, row, 32 * half + i, x + i);
-        }
-        fence_async_smem();
-        fence_before_sync();
-        __syncthreads();
+        };
 
-        // ---- a6: E^T = S'^T Y^T + V^T (-M)^T
-        if (tid == 0) {
-            bool ok = true;
-            if (valid == FC) { ok = mbar_wait(mbar_v, j & 1); ++v_done; }
-            if (!ok) atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
-            fence_after_sync();
-            mma_chain(tmem + 128, smem_desc(sbase + Ly::T_S, S_RB, 128), 2 * S_RB,
-                      smem_desc(sbase + Ly::T_YT, N64_RB, 128), 2 * N64_RB, idesc_bf16(128, FC, true, true), FD, false);
-            mma_chain(tmem + 128, smem_desc(sbase + Ly::T_V, 128, V_CB), 256, smem_desc(sbase + Ly::T_MN, 128, N64_RB), 256,
-                      idesc_bf16(128, FC, true, false), FC, true);
-            mma_commit(mbar_mma);
+        // fp32 state, transposed: this thread holds S^T[n = row][c] for c in [64*half, 64*half + 64)
+        float S[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) S[i] = args.S0 ? args.S0[(bh * FD + 64 * half + i) * FD + row] : 0.f;
+
+        if (nchunk > 0) {
+            // ---- prologue: the state-independent part of chunk 0
+            gate_factors(0);
+            if (nfull == 0) { plain_kq(0); plain_v(0); }
+            fence_async_smem();
+            sync();
+            signal(rdy_P);
+            failed = !wait_all(mbar_D, 0);
+            if (!failed) {
+                epi_D(0);
+                fence_async_smem();
+                fence_before_sync();
+                sync();
+                unit_lower_inverse64(F_L, F_M, scr, sbase + Ly::T_MN, sbase + Ly::T_MY, vec(0), tid);
+                fence_async_smem();
+                sync();
+                signal(rdy_M);
+                failed = !wait_all(mbar_Y, 0);
+            }
+            if (!failed) {
+                epi_Y();
+                fence_async_smem();
+                fence_before_sync();
+                sync();
+            }
         }
-        if (!wait_mma()) { failed = true; break; }
-        // v is consumed: prefetch the next full chunk's v
-        if (tid == 0 && j + 1 < nfull) { issue_v(j + 1); ++v_issued; }
-        {
-            float x[32];
-            tmem_ld32(tmem + 128 + lane_off + 32 * half, x);
+
+        for (int j = 0; j < nchunk && !failed; ++j) {
+            const int b = j & 1;
+            const bool has_next = j + 1 < nchunk;
+            const int valid = min(FC, T - j * FC);
+            const size_t g0 = tok_base + (size_t)j * FC;
+            const float* vf = vec(b);
+            float g_n2 = 0.f, b_n2 = 0.f;    // gates of chunk j + 2 (stored into buffer b after this chunk)
+            if (tid < FC && (j + 2) * FC + tid < T) {
+                g_n2 = args.decay[tok_base + (size_t)(j + 2) * FC + tid];
+                b_n2 = args.beta[tok_base + (size_t)(j + 2) * FC + tid];
+            }
+
+            // ---- S'^T = e^{a} S^T of chunk j into TMEM as bf16 hi + lo (A operand of E and O)
+            {
+                const float ea = vf[192];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) x[i] *= v_bs[32 * half + i];     // Es^T[n][rho] = beta eb_rho E[rho][n]
+                for (int part = 0; part < 2; ++part) {
+                    uint32_t hi[16], lo[16];
 #pragma unroll
-            for (int i = 0; i < 32; i += 8)
-                rbm_store8_split(sbase + Ly::T_ESH, sbase + Ly::T_ESL, FC, row, 32 * half + i, x + i);
-        }
-        {   // S' lo = e^{a} S - bf16(e^{a} S), into region R1 (M, M Diag(ef), Y^T are consumed)
-            const float ea = v_sc[0];
-#pragma unroll
-            for (int i = 0; i < 64; i += 8) {
-                uint32_t l[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float s0 = ea * S[i + 2 * u], s1 = ea * S[i + 2 * u + 1];
-                    const uint32_t h = pack_bf16(s0, s1);
-                    l[u] = pack_bf16(s0 - __uint_as_float(h << 16), s1 - __uint_as_float(h & 0xFFFF0000u));
+                    for (int i = 0; i < 16; ++i) {
+                        const float s0 = ea * S[32 * part + 2 * i], s1 = ea * S[32 * part + 2 * i + 1];
+                        hi[i] = pack_bf16(s0, s1);
+                        lo[i] = pack_bf16(s0 - __uint_as_float(hi[i] << 16), s1 - __uint_as_float(hi[i] & 0xFFFF0000u));
+                    }
+                    tmem_st16(tmem + TM_SH + lane_off + 32 * half + 16 * part, hi);
+                    tmem_st16(tmem + TM_SL + lane_off + 32 * half + 16 * part, lo);
                 }
-                st_shared_v4(sbase + Ly::T_SLO + rbm_off(row, 64 * half + i, FD), l[0], l[1], l[2], l[3]);
             }
-        }
-        fence_async_smem();
-        fence_before_sync();
-        __syncthreads();
+            if (has_next && j + 1 >= nfull) plain_kq(j + 1);      // ragged next chunk (its buffer is free)
+            fence_async_smem();
+            fence_before_sync();
+            sync();
+            signal(rdy_S);
 
-        // ---- a6/a7: X = K^T Es (state update), O'^T = S'^T Q^T - Es^T QK^T (chunk output)
-        if (tid == 0) {
-            fence_after_sync();
-            const uint64_t dKmn = smem_desc(tKQ, 128, KQ_CB);                 // k rows, MN-major A
-            const uint32_t idX = idesc_bf16(128, FD, true, false);
-            mma_chain(tmem + 256, dKmn, 256, smem_desc(sbase + Ly::T_ESH, 128, N64_RB), 256, idX, FC, false);
-            mma_chain(tmem + 256, dKmn, 256, smem_desc(sbase + Ly::T_ESL, 128, N64_RB), 256, idX, FC, true);
-            const uint64_t dQ = smem_desc(tQ, KQ_CB, 128);                    // q rows, K-major B
-            const uint32_t idO = idesc_bf16(128, FC, true, false), idO2 = idesc_bf16(128, FC, false, false);
-            mma_chain(tmem + 384, smem_desc(sbase + Ly::T_SLO, S_RB, 128), 2 * S_RB, dQ, 2 * KQ_CB, idO, FD, true);
-            mma_chain(tmem + 384, smem_desc(sbase + Ly::T_ESH, 128, N64_RB), 256,
-                      smem_desc(sbase + Ly::T_QKH, 128, N64_RB), 256, idO2, FC, true);
-            mma_chain(tmem + 384, smem_desc(sbase + Ly::T_ESL, 128, N64_RB), 256,
-                      smem_desc(sbase + Ly::T_QKH, 128, N64_RB), 256, idO2, FC, true);
-            mma_chain(tmem + 384, smem_desc(sbase + Ly::T_ESH, 128, N64_RB), 256,
-                      smem_desc(sbase + Ly::T_QKL, 128, N64_RB), 256, idO2, FC, true);
-            mma_commit(mbar_mma);
-        }
-        if (!wait_mma()) { failed = true; break; }
-        {
-            const float gam = v_sc[2], egca = v_sc[1];
-            float x[32];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                tmem_ld32(tmem + 256 + lane_off + 64 * half + 32 * h, x);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) S[32 * h + i] = fmaf(gam, S[32 * h + i], -egca * x[i]);
-            }
-            tmem_ld32(tmem + 384 + lane_off + 32 * half, x);      // O'^T row n = row, tokens 32*half + i
-            float* orow = args.o + g0 * FD + row;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int t = 32 * half + i;
-                if (t < valid) orow[(size_t)t * FD] = v_ef[t] * x[i];
-            }
-        }
-        if (tid < FC) {
-            rawG[(b ^ 1) * FC + tid] = g_next;
-            rawB[(b ^ 1) * FC + tid] = b_next;
-        }
-        fence_before_sync();
-        __syncthreads();
-    }
+            // ---- gate factors of chunk j + 1 (warp 0), while E and O run
+            if (has_next) gate_factors(j + 1);
 
-    if (failed) {
-        if (tid == 0) {
-            atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
-            // drain the loads still in flight (bounded) before the CTA exits
-            for (int i = kq_done; i < kq_issued; ++i) mbar_wait(&mbar_kq[i & 1], (i >> 1) & 1, 400000000LL);
-            for (int i = v_done; i < v_issued; ++i) mbar_wait(mbar_v, i & 1, 400000000LL);
-        }
-        mbar_wait(mbar_mma, mma_phase, 400000000LL);
-    } else if (args.ST) {
+            // ---- Es^T = Diag(beta eb) E^T of chunk j (hi + lo)
+            if (!wait_all(mbar_E, b)) { failed = true; break; }
+            {
+                float x[32];
+                tmem_ld32(tmem + TM_E + lane_off + 32 * half, x);
 #pragma unroll
-        for (int i = 0; i < 64; i += 4)
-            *reinterpret_cast<float4*>(args.ST + (bh * FD + row) * FD + 64 * half + i) =
-                make_float4(S[i], S[i + 1], S[i + 2], S[i + 3]);
+                for (int i = 0; i < 32; ++i) x[i] *= vf[128 + 32 * half + i];
+#pragma unroll
+                for (int i = 0; i < 32; i += 8)
+                    rbm_store8_split(sbase + Ly::T_ESH, sbase + Ly::T_ESL, FC, row, 32 * half + i, x + i);
+            }
+            if (has_next && j + 1 >= nfull) plain_v(j + 1);        // ragged next chunk (v of chunk j is consumed)
+            fence_async_smem();
+            fence_before_sync();
+            sync();
+            signal(rdy_E);
+
+            // ---- state-independent part of chunk j + 1, in the shadow of X(j), O(j)
+            if (has_next) {
+                if (!wait_all(mbar_D, (j + 1) & 1)) { failed = true; break; }
+                epi_D(j + 1);
+                fence_async_smem();
+                fence_before_sync();
+                sync();
+                unit_lower_inverse64(F_L, F_M, scr, sbase + Ly::T_MN, sbase + Ly::T_MY, vec(b ^ 1), tid);
+                fence_async_smem();
+                sync();
+                signal(rdy_M);
+            }
+
+            // ---- state update and chunk output of chunk j
+            if (!wait_all(mbar_XO, b)) { failed = true; break; }
+            {
+                const float gam = vf[194], egca = vf[193];
+                float x[32];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    tmem_ld32(tmem + TM_X + lane_off + 64 * half + 32 * h, x);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) S[32 * h + i] = fmaf(gam, S[32 * h + i], -egca * x[i]);
+                }
+                tmem_ld32(tmem + TM_O + lane_off + 32 * half, x);      // O'^T row n = row, tokens 32*half + i
+                float* orow = args.o + g0 * FD + row;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int t = 32 * half + i;
+                    if (t < valid) orow[(size_t)t * FD] = vf[t] * x[i];
+                }
+            }
+            if (tid < FC) {
+                rawG[b * FC + tid] = g_n2;
+                rawB[b * FC + tid] = b_n2;
+            }
+            fence_before_sync();
+            sync();
+
+            // ---- Y^T of chunk j + 1 into its tile
+            if (has_next) {
+                if (!wait_all(mbar_Y, (j + 1) & 1)) { failed = true; break; }
+                epi_Y();
+                fence_async_smem();
+                fence_before_sync();
+                sync();
+            }
+        }
+        if (failed) {
+            if (tid == 0) atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
+        } else if (args.ST) {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) args.ST[(bh * FD + 64 * half + i) * FD + row] = S[i];
+        }
     }
     fence_before_sync();
     __syncthreads();
