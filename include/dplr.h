@@ -96,9 +96,11 @@ typedef struct {
 
 /* Bytes of device workspace dplr_la_forward needs for `desc`; 0 if `desc` is
  * invalid or unsupported (call dplr_la_check for the reason). When the forward
- * runs the fused per-head kernel (GDN/HDLA, bf16, dk = dv = 128) this is 256
+ * runs the fused per-head kernel (GDN, bf16, dk = dv = 128) this is 256
  * bytes: the first int32 is a device status word that a kernel sets to
- * DPLR_ERR_TIMEOUT if one of its bounded waits gives up, and never clears; zero
+ * DPLR_ERR_TIMEOUT if one of its bounded waits gives up (DPLR_ERR_CUDA if its
+ * shared memory is not 1024-byte aligned, in which case it computes nothing), and
+ * never clears; zero
  * it once after allocating the workspace to observe that. Otherwise it holds the
  * chunk maps of the two-stage path. */
 DPLR_API size_t dplr_la_workspace_size(const dplr_desc* desc);

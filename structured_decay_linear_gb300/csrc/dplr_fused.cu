@@ -29,15 +29,14 @@
 // term (x = hi + lo), which keeps the result within ~2e-3 of the float64 recurrence
 // (relative to the output RMS) where plain bf16 operands reach ~4e-2.
 //
-// Operand tiles. Every bf16 operand lives in shared memory as 8x8 core matrices (8 rows
-// of 16 bytes). Two arrangements are used:
+// Operand tiles. q, k and v arrive by TMA tensor copies of 64 tokens x 64 features
+// (128-byte rows) in the 128-byte swizzled layout: token t of a half-tile at t*128, its
+// 16-byte chunk c at chunk position c ^ (t % 8). One such tile feeds an MMA K-major
+// (contracting over features) or MN-major (contracting over tokens) by the descriptor
+// alone. Tiles written from registers use the unswizzled core-matrix layout
 //   RBM (row-block major, C columns): (r, c) -> (r/8)*C*16 + (c/8)*128 + (r%8)*16 + (c%8)*2
-//   CBM (col-block major, R rows):    (r, c) -> (c/8)*R*16 + (r/8)*128 + (r%8)*16 + (c%8)*2
-// Either one feeds an MMA K-major (contracting over columns) or MN-major (contracting
-// over rows) by choosing the descriptor's LBO/SBO, so no tile is ever transposed. q, k and
-// v arrive by TMA tensor copies (one 8-column box per column block) directly in CBM;
-// tiles written from registers use RBM, whose 16-byte rows of a warp land in distinct
-// bank groups.
+// (8x8 core matrices of 16-byte rows), whose 16-byte rows of a warp land in distinct bank
+// groups; it too serves either major order through LBO/SBO, so no tile is ever transposed.
 #include <cudaTypedefs.h>
 
 #include <cstring>
@@ -58,15 +57,16 @@ constexpr int kSimt = 256; // threads of the CUDA-core group (named barrier 1)
 constexpr uint32_t kTmemCols = 512;
 constexpr int kLdL = 68;   // padded row stride (floats) of the fp32 L and M buffers (16-byte rows)
 
-// Tile geometry: byte strides between core matrices.
-constexpr uint32_t KQ_CB = 128 * 16;   // T_KQ: CBM with 128 rows (k rows 0-63, q rows 64-127)
-constexpr uint32_t V_CB = 64 * 16;     // T_V:  CBM with 64 rows
+// Tile geometry. A swizzled half-tile is 64 tokens x 128 bytes = 8 KB; a k/q buffer holds
+// [k features 0-63][q features 0-63][k features 64-127][q features 64-127].
+constexpr uint32_t SWH = FC * 128;     // bytes of one swizzled half-tile
+constexpr uint32_t KQ_H = 2 * SWH;     // k/q buffer: stride between the two feature halves
 constexpr uint32_t N64_RB = 64 * 16;   // RBM tiles with 64 columns
 
 struct GdnLayout {
-    static constexpr int T_KQ0 = 0;                         // [128][128] CBM (k rows 0-63, q rows 64-127), 2 buffers
+    static constexpr int T_KQ0 = 0;                         // k, q of a chunk (4 swizzled half-tiles), 2 buffers
     static constexpr int T_KQ1 = T_KQ0 + 128 * FD * 2;
-    static constexpr int T_V = T_KQ1 + 128 * FD * 2;        // [64][128] CBM  v
+    static constexpr int T_V = T_KQ1 + 128 * FD * 2;        // v of a chunk (2 swizzled half-tiles)
     static constexpr int T_MN = T_V + FC * FD * 2;          // [64 rho][64 sigma] RBM  -M
     static constexpr int T_MY = T_MN + FC * FC * 2;         // [64][64] RBM  M Diag(ef)
     static constexpr int T_YT = T_MY + FC * FC * 2;         // [128 c][64 rho] RBM  Y^T
@@ -84,6 +84,7 @@ struct GdnLayout {
     static constexpr int TOTAL = BAR + 112;
 };
 static_assert(GdnLayout::TOTAL <= 227 * 1024, "shared memory budget");
+static_assert(GdnLayout::T_KQ1 % 1024 == 0 && GdnLayout::T_V % 1024 == 0, "swizzled tiles are 1024-byte aligned");
 
 // TMEM columns (512 allocated)
 constexpr uint32_t TM_D = 0;      // [K;Q] K^T          128 lanes x 64
@@ -245,6 +246,10 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
     using Ly = GdnLayout;
     extern __shared__ __align__(1024) unsigned char smem[];
     const uint32_t sbase = smem_addr(smem);
+    if (sbase & 1023u) {   // the swizzled tiles need 1024-byte alignment
+        if (threadIdx.x == 0) atomicExch(args.status, (int)DPLR_ERR_CUDA);
+        return;
+    }
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Ly::BAR);
     // MMA completions (issuer -> CUDA-core group)
     uint64_t* mbar_E = bars + 0;
@@ -301,21 +306,19 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
         // ======================= issuer warp: MMAs (lane 0) and bulk copies (all lanes) =======================
         uint32_t kq_pend = 0;   // bit b: a k/q copy into buffer b is in flight
         bool v_pend = false;
-        auto issue_kq = [&](int jj) {     // 32 boxes, one per lane
+        auto issue_kq = [&](int jj) {     // 4 boxes of 64 tokens x 64 features: lane = 2 * half + (q ? 1 : 0)
             const int y = static_cast<int>(tok_base + (size_t)jj * FC);
             unsigned char* dst = smem + ((jj & 1) ? Ly::T_KQ1 : Ly::T_KQ0);
             if (lane == 0) mbar_expect_tx(&mbar_kq[jj & 1], 2u * FC * FD * 2);
             __syncwarp();
-            const int cb = lane & 15;
-            if (lane < 16) tma_load_2d(dst + cb * KQ_CB, &tm_k, 8 * cb, y, &mbar_kq[jj & 1]);
-            else tma_load_2d(dst + cb * KQ_CB + FC * 16, &tm_q, 8 * cb, y, &mbar_kq[jj & 1]);
+            if (lane < 4) tma_load_2d(dst + lane * SWH, (lane & 1) ? &tm_q : &tm_k, 64 * (lane >> 1), y, &mbar_kq[jj & 1]);
             kq_pend |= 1u << (jj & 1);
         };
-        auto issue_v = [&](int jj) {      // 16 boxes
+        auto issue_v = [&](int jj) {      // 2 boxes
             const int y = static_cast<int>(tok_base + (size_t)jj * FC);
             if (lane == 0) mbar_expect_tx(mbar_v, FC * FD * 2);
             __syncwarp();
-            if (lane < 16) tma_load_2d(smem + Ly::T_V + lane * V_CB, &tm_v, 8 * lane, y, mbar_v);
+            if (lane < 2) tma_load_2d(smem + Ly::T_V + lane * SWH, &tm_v, 64 * lane, y, mbar_v);
             v_pend = true;
         };
         auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -339,17 +342,20 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
         };
         auto issue_D = [&](int jj) {
             if (lane == 0) {
-                const uint32_t tk = tKQ_of(jj);
-                mma_chain(tmem + TM_D, smem_desc(tk, KQ_CB, 128), 2 * KQ_CB, smem_desc(tk, KQ_CB, 128), 2 * KQ_CB,
-                          idesc_bf16(128, FC, false, false), FD, false);
+                const uint32_t tk = tKQ_of(jj);   // rows 0-63 k, 64-127 q of each feature half
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint64_t d = smem_desc_sw128(tk + h * KQ_H, 16, 1024);
+                    mma_chain(tmem + TM_D, d, 32, d, 32, idesc_bf16(128, FC, false, false), 64, h > 0);
+                }
                 mma_commit(mbar_D);
             }
             __syncwarp();
         };
         auto issue_Y = [&](int jj) {   // Y^T = K^T (M Diag(ef))^T
             if (lane == 0) {
-                mma_chain(tmem + TM_Y, smem_desc(tKQ_of(jj), 128, KQ_CB), 256, smem_desc(sbase + Ly::T_MY, 128, N64_RB),
-                          256, idesc_bf16(128, FC, true, false), FC, false);
+                mma_chain(tmem + TM_Y, smem_desc_sw128(tKQ_of(jj), KQ_H, 1024), 2048,
+                          smem_desc(sbase + Ly::T_MY, 128, N64_RB), 256, idesc_bf16(128, FC, true, false), FC, false);
                 mma_commit(mbar_Y);
             }
             __syncwarp();
@@ -374,13 +380,18 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
                 const uint32_t tk = tKQ_of(j);
                 mma_chain_tmem_a(tmem + TM_E, tmem + TM_SH, smem_desc(sbase + Ly::T_YT, N64_RB, 128), 2 * N64_RB,
                                  idesc_bf16(128, FC, false, true), FD, false);                    // S'^T Y^T
-                mma_chain(tmem + TM_E, smem_desc(sbase + Ly::T_V, 128, V_CB), 256,
+                mma_chain(tmem + TM_E, smem_desc_sw128(sbase + Ly::T_V, SWH, 1024), 2048,
                           smem_desc(sbase + Ly::T_MN, 128, N64_RB), 256, idesc_bf16(128, FC, true, false), FC,
                           true);                                                                  // + V^T (-M)^T
                 mma_commit(mbar_E);
-                const uint64_t dQ = smem_desc(tk + FC * 16, KQ_CB, 128);                          // q rows, K-major
-                mma_chain_tmem_a(tmem + TM_O, tmem + TM_SH, dQ, 2 * KQ_CB, idesc_bf16(128, FC, false, false), FD, false);
-                mma_chain_tmem_a(tmem + TM_O, tmem + TM_SL, dQ, 2 * KQ_CB, idesc_bf16(128, FC, false, false), FD, true);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {                                                    // q rows, K-major
+                    const uint64_t dQ = smem_desc_sw128(tk + SWH + h * KQ_H, 16, 1024);
+                    mma_chain_tmem_a(tmem + TM_O, tmem + TM_SH + 32 * h, dQ, 32, idesc_bf16(128, FC, false, false), 64,
+                                     h > 0);
+                    mma_chain_tmem_a(tmem + TM_O, tmem + TM_SL + 32 * h, dQ, 32, idesc_bf16(128, FC, false, false), 64,
+                                     true);
+                }
             }
             __syncwarp();
             if (has_next) {
@@ -394,10 +405,10 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
             if (!wait_warp(rdy_E, b)) { failed = true; break; }
             if (lane == 0) {
                 const uint32_t tk = tKQ_of(j);
-                const uint64_t dK = smem_desc(tk, 128, KQ_CB);               // k rows, MN-major B (K = rho)
+                const uint64_t dK = smem_desc_sw128(tk, KQ_H, 1024);         // k rows, MN-major B (K = rho)
                 const uint32_t idX = idesc_bf16(128, FD, false, true), idO = idesc_bf16(128, FC, false, false);
-                mma_chain(tmem + TM_X, smem_desc(sbase + Ly::T_ESH, 128, N64_RB), 256, dK, 256, idX, FC, false);
-                mma_chain(tmem + TM_X, smem_desc(sbase + Ly::T_ESL, 128, N64_RB), 256, dK, 256, idX, FC, true);
+                mma_chain(tmem + TM_X, smem_desc(sbase + Ly::T_ESH, 128, N64_RB), 256, dK, 2048, idX, FC, false);
+                mma_chain(tmem + TM_X, smem_desc(sbase + Ly::T_ESL, 128, N64_RB), 256, dK, 2048, idX, FC, true);
                 mma_chain(tmem + TM_O, smem_desc(sbase + Ly::T_ESH, 128, N64_RB), 256,
                           smem_desc(tQK_of(j, 0), 128, N64_RB), 256, idO, FC, true);
                 mma_chain(tmem + TM_O, smem_desc(sbase + Ly::T_ESL, 128, N64_RB), 256,
@@ -445,26 +456,28 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
         auto plain_kq = [&](int jj) {        // ragged (last) chunk: zero rows past the end
             const int valid = T - jj * FC;
             const size_t g0 = tok_base + (size_t)jj * FC;
-            const uint32_t tk = tKQ_of(jj), tq = tk + FC * 16;
+            const uint32_t tk = tKQ_of(jj);
             for (int i = tid; i < FC * (FD / 8); i += kSimt) {
-                const int t = i & (FC - 1), cb = i >> 6;
+                const int cb = i & 15, t = i >> 4;   // 16-byte chunk cb of token t, in the swizzled layout
                 uint4 zq = make_uint4(0, 0, 0, 0), zk = zq;
                 if (t < valid) {
                     zq = *reinterpret_cast<const uint4*>(args.q + (g0 + t) * FD + 8 * cb);
                     zk = *reinterpret_cast<const uint4*>(args.k + (g0 + t) * FD + 8 * cb);
                 }
-                st_shared_v4(tk + cb * KQ_CB + t * 16, zk.x, zk.y, zk.z, zk.w);
-                st_shared_v4(tq + cb * KQ_CB + t * 16, zq.x, zq.y, zq.z, zq.w);
+                const uint32_t off = (cb >> 3) * KQ_H + t * 128 + (((cb & 7) ^ (t & 7)) << 4);
+                st_shared_v4(tk + off, zk.x, zk.y, zk.z, zk.w);
+                st_shared_v4(tk + SWH + off, zq.x, zq.y, zq.z, zq.w);
             }
         };
         auto plain_v = [&](int jj) {
             const int valid = T - jj * FC;
             const size_t g0 = tok_base + (size_t)jj * FC;
             for (int i = tid; i < FC * (FD / 8); i += kSimt) {
-                const int t = i & (FC - 1), cb = i >> 6;
+                const int cb = i & 15, t = i >> 4;
                 uint4 zv = make_uint4(0, 0, 0, 0);
                 if (t < valid) zv = *reinterpret_cast<const uint4*>(args.v + (g0 + t) * FD + 8 * cb);
-                st_shared_v4(sbase + Ly::T_V + cb * V_CB + t * 16, zv.x, zv.y, zv.z, zv.w);
+                const uint32_t off = (cb >> 3) * SWH + t * 128 + (((cb & 7) ^ (t & 7)) << 4);
+                st_shared_v4(sbase + Ly::T_V + off, zv.x, zv.y, zv.z, zv.w);
             }
         };
         auto gate_factors = [&](int jj) {    // warp 0
@@ -591,6 +604,7 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
                     tmem_st16(tmem + TM_SH + lane_off + 32 * half + 16 * part, hi);
                     tmem_st16(tmem + TM_SL + lane_off + 32 * half + 16 * part, lo);
                 }
+                tmem_wait_st();
             }
             if (has_next && j + 1 >= nfull) plain_kq(j + 1);      // ragged next chunk (its buffer is free)
             fence_async_smem();
@@ -693,16 +707,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// [rows][128] bf16 row-major, boxes of 8 columns x 64 rows.
+// [rows][128] bf16 row-major, boxes of 64 columns x 64 rows, 128-byte swizzle.
 bool make_map(CUtensorMap* map, const void* base, uint64_t rows) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {FD, rows};
     cuuint64_t strides[1] = {FD * 2};
-    cuuint32_t box[2] = {8, FC};
+    cuuint32_t box[2] = {64, FC};
     cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -36,6 +36,14 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
     return d;
 }
 
+// The same for a tile in the 128-byte swizzled layout (rows of 128 bytes whose 16-byte chunks
+// are permuted by XOR with the row index mod 8, as the TMA writes them with SWIZZLE_128B).
+// K-major: SBO = stride of 8-row groups (LBO unused). MN-major: LBO = stride between
+// 64-element blocks along MN, SBO = stride of 8-row groups along K. Base 1024-byte aligned.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return smem_desc(saddr, lbo, sbo) | (static_cast<uint64_t>(2) << 61);
+}
+
 // Descriptor of tile (base, cols) used K-major (contract over cols) or MN-major (contract over rows).
 __device__ __forceinline__ uint64_t desc_kmajor(uint32_t base, int cols) { return smem_desc(base, 128, cols * 16); }
 __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, int cols) { return smem_desc(base, cols * 16, 128); }
@@ -87,7 +95,7 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// 16 consecutive 32-bit columns of this thread's TMEM lane (then waits for completion).
+// Stores 16 consecutive 32-bit columns of this thread's TMEM lane (completion: tmem_wait_st).
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -95,8 +103,9 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
         :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
            "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
+// Waits until this thread's earlier tcgen05.st have completed.
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Named barrier `id` over the first `n` threads (a multiple of 32) of the CTA.
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t n) {
