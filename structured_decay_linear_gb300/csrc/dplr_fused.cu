@@ -14,20 +14,31 @@
 //
 //   D     = [K ; Q] K^T                          (tcgen05 M=128 N=64  K=dk)
 //   L_ts  = ef_t D_ts beta_s eb_s  (s < t)       (fp32 epilogue)
-//   QK    = tril_incl(Q K^T)                     (bf16 hi + lo)
+//   QK~   = tril_incl(Q K^T) / c,  c = e^{G_C-a} (bf16 hi + lo)
 //   M     = (I + L)^{-1}                         (CUDA cores, fp32, blocked 16/32/64)
 //   Y^T   = K^T (M Diag(ef))^T                   (tcgen05 M=128 N=64  K=C)
 //   E^T   = S'^T Y^T - V^T M^T,  S' = e^{a} S    (tcgen05 M=128 N=64  K=dk+C)
-//   Es    = Diag(beta eb) E                      (bf16 hi + lo)
-//   X     = K^T Es                               (tcgen05 M=128 N=dv  K=C)
-//   O'^T  = S'^T Q^T - Es^T QK^T, o_t = ef_t O'_t (tcgen05 M=128 N=64 K=dk+C)
-//   S_j   = e^{G_C} S_{j-1} - e^{G_C - a} X      (fp32, registers)
+//   Es~   = -c Diag(beta eb) E                   (bf16 hi + lo, in tensor memory)
+//   S_j   = e^{G_C} S_{j-1} + K^T Es~            (fp32 accumulator in tensor memory)
+//   O'^T  = S'^T Q^T + Es~^T QK~^T, o_t = ef_t O'_t (tcgen05 M=128 N=64 K=dk+C)
 //
 // E_t = e^{g_t} k_t^T S_{t-1} - v_t is the delta-rule prediction error. Computing the
 // transposes E^T, Y^T and O'^T keeps every MMA at M = 128 (full tensor-core rate). The
 // rounding of E, QK and of S' in the output product is compensated with a second bf16
 // term (x = hi + lo), which keeps the result within ~2e-3 of the float64 recurrence
 // (relative to the output RMS) where plain bf16 operands reach ~4e-2.
+//
+// Work split. Only the chain S_{j-1} -> S' -> E -> Es~ -> S_j is sequential; the WY build
+// of a chunk (D, L, M, Y) and its output epilogue are not. Three groups of four warps (one
+// thread per tensor-memory lane) and one issuing warp run them concurrently:
+//   A  state chain: S' (hi, lo) and e^{G_C} S into tensor memory, then Es~ in place of E;
+//   B  WY build: L and QK~ from D, the triangular inverse, the M tiles;
+//   C  Y^T tiles and the chunk outputs o_t.
+// The issuer queues the MMAs of chunk j in the order E(j), O(j), X(j), O~(j), then the
+// state-independent Y(j+1), Z(j+1) = V^T (-M)^T and D(j+2), so the tensor cores run the
+// chain's products as soon as their operands exist and fill the CUDA-core phases of the
+// chain with the rest. The state S^T (lane n, column c) stays in tensor memory as the
+// accumulator of X for the whole sequence.
 //
 // Operand tiles. q, k and v arrive by TMA tensor copies of 64 tokens x 64 features
 // (128-byte rows) in the 128-byte swizzled layout: token t of a half-tile at t*128, its
@@ -52,48 +63,48 @@ using namespace sm100;
 
 constexpr int FD = 128;    // dk = dv
 constexpr int FC = 64;     // tokens per chunk
-constexpr int FNT = 288;   // threads per CTA: warps 0-7 CUDA-core work, warp 8 issues MMAs and copies
-constexpr int kSimt = 256; // threads of the CUDA-core group (named barrier 1)
+constexpr int kGrp = 128;  // threads of each CUDA-core group (one per TMEM lane)
+// Warps 0-3: state chain (group A). Warps 4-7: WY build (group B). Warps 8-11: Y^T tiles and
+// outputs (group C). Warp 12: MMA / copy issuer.
+constexpr int FNT = 3 * kGrp + 32;
+constexpr uint32_t kBarA = 1, kBarB = 2, kBarC = 3;   // named barriers of the groups
 constexpr uint32_t kTmemCols = 512;
 constexpr int kLdL = 68;   // padded row stride (floats) of the fp32 L and M buffers (16-byte rows)
+constexpr int kKQBuf = 3;  // k/q buffers: chunk j's are read until X(j); chunk j+2's are needed for D(j+2)
 
 // Tile geometry. A swizzled half-tile is 64 tokens x 128 bytes = 8 KB; a k/q buffer holds
 // [k features 0-63][q features 0-63][k features 64-127][q features 64-127].
 constexpr uint32_t SWH = FC * 128;     // bytes of one swizzled half-tile
 constexpr uint32_t KQ_H = 2 * SWH;     // k/q buffer: stride between the two feature halves
+constexpr uint32_t KQ_BYTES = 2 * KQ_H;
 constexpr uint32_t N64_RB = 64 * 16;   // RBM tiles with 64 columns
 
 struct GdnLayout {
-    static constexpr int T_KQ0 = 0;                         // k, q of a chunk (4 swizzled half-tiles), 2 buffers
-    static constexpr int T_KQ1 = T_KQ0 + 128 * FD * 2;
-    static constexpr int T_V = T_KQ1 + 128 * FD * 2;        // v of a chunk (2 swizzled half-tiles)
+    static constexpr int T_KQ = 0;                          // k, q of a chunk (4 swizzled half-tiles), 3 buffers
+    static constexpr int T_V = T_KQ + kKQBuf * KQ_BYTES;    // v of a chunk (2 swizzled half-tiles)
     static constexpr int T_MN = T_V + FC * FD * 2;          // [64 rho][64 sigma] RBM  -M
     static constexpr int T_MY = T_MN + FC * FC * 2;         // [64][64] RBM  M Diag(ef)
     static constexpr int T_YT = T_MY + FC * FC * 2;         // [128 c][64 rho] RBM  Y^T
-    static constexpr int T_ESH = T_YT + FD * FC * 2;        // [128 n][64 rho] RBM  Es^T hi
-    static constexpr int T_ESL = T_ESH + FD * FC * 2;       //                      Es^T lo
-    static constexpr int T_QK = T_ESL + FD * FC * 2;        // 2 buffers x {hi, lo} [64 t][64 sigma] RBM  -QK
+    static constexpr int T_QK = T_YT + FD * FC * 2;         // 2 buffers x {hi, lo} [64 t][64 sigma] RBM  QK / c
     static constexpr int F_L = T_QK + 4 * FC * FC * 2;      // fp32 [64][68]
     static constexpr int F_M = F_L + FC * kLdL * 4;         // fp32 [64][68]
     static constexpr int SCR = F_M + FC * kLdL * 4;         // fp32 scratch of the inverse (32 x 36)
-    static constexpr int VEC = SCR + 32 * 36 * 4;          // 2 buffers x {ef[64], eb[64], bs[64], sc[..]}
+    static constexpr int VEC = SCR + 32 * 36 * 4;          // per group, 2 buffers of 256 floats
     static constexpr int kVec = 1024;
-    static constexpr int RAW_G = VEC + 2 * kVec;            // [2][64] log gate
-    static constexpr int RAW_B = RAW_G + 512;               // [2][64] beta
-    static constexpr int BAR = RAW_B + 512;                 // 13 mbarriers + TMEM address
-    static constexpr int TOTAL = BAR + 112;
+    static constexpr int BAR = VEC + 6 * kVec;              // mbarriers, TMEM address, counter
+    static constexpr int TOTAL = BAR + 160;
 };
 static_assert(GdnLayout::TOTAL <= 227 * 1024, "shared memory budget");
-static_assert(GdnLayout::T_KQ1 % 1024 == 0 && GdnLayout::T_V % 1024 == 0, "swizzled tiles are 1024-byte aligned");
+static_assert(GdnLayout::T_V % 1024 == 0 && KQ_BYTES % 1024 == 0, "swizzled tiles are 1024-byte aligned");
 
 // TMEM columns (512 allocated)
-constexpr uint32_t TM_D = 0;      // [K;Q] K^T          128 lanes x 64
-constexpr uint32_t TM_Y = 64;     // Y^T                128 x 64
-constexpr uint32_t TM_E = 128;    // E^T                128 x 64
-constexpr uint32_t TM_X = 192;    // X^T                128 x 128
-constexpr uint32_t TM_O = 320;    // O'^T               128 x 64
-constexpr uint32_t TM_SH = 384;   // S'^T hi (A operand, bf16 pairs) 128 x 64
-constexpr uint32_t TM_SL = 448;   // S'^T lo
+constexpr uint32_t TM_S = 0;      // S^T fp32 (lane n, column c)            128 lanes x 128
+constexpr uint32_t TM_SH = 128;   // S'^T hi (A operand, bf16 pairs)         128 x 64
+constexpr uint32_t TM_SL = 192;   // S'^T lo
+constexpr uint32_t TM_E = 256;    // E^T fp32, then Es~^T hi/lo in place     128 x 64
+constexpr uint32_t TM_O = 320;    // O'^T                                    128 x 64
+constexpr uint32_t TM_D = 384;    // [K;Q] K^T                               128 x 64
+constexpr uint32_t TM_Y = 448;    // Y^T                                     128 x 64
 
 struct FusedArgs {
     const __nv_bfloat16* q; const __nv_bfloat16* k; const __nv_bfloat16* v;
@@ -115,26 +126,21 @@ __device__ __forceinline__ void rbm_store8(uint32_t tile, int cols, int r, int c
                  pack_bf16(x[6], x[7]));
 }
 
-// x = hi + lo with both parts bf16 (one packed conversion per pair for each part).
+// x = hi + lo with both parts bf16: packed pairs (element 2i in the low half).
+__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& h, uint32_t& l) {
+    h = pack_bf16(x0, x1);
+    l = pack_bf16(x0 - __uint_as_float(h << 16), x1 - __uint_as_float(h & 0xFFFF0000u));
+}
+
 __device__ __forceinline__ void rbm_store8_split(uint32_t th, uint32_t tl, int cols, int r, int c, const float* x) {
     uint32_t h[4], l[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        h[i] = pack_bf16(x[2 * i], x[2 * i + 1]);
-        const float h0 = __uint_as_float(h[i] << 16), h1 = __uint_as_float(h[i] & 0xFFFF0000u);
-        l[i] = pack_bf16(x[2 * i] - h0, x[2 * i + 1] - h1);
-    }
+    for (int i = 0; i < 4; ++i) split_pair(x[2 * i], x[2 * i + 1], h[i], l[i]);
     const uint32_t off = rbm_off(r, c, cols);
     st_shared_v4(th + off, h[0], h[1], h[2], h[3]);
     st_shared_v4(tl + off, l[0], l[1], l[2], l[3]);
 }
 
-// (I + L)^{-1} for a 64x64 strictly lower-triangular fp32 L (row stride kLdL = 68 floats, so
-// rows are 16-byte aligned). The four 16x16 diagonal blocks are solved row by row (left-looking,
-// one column per thread, rows of L read as 16-byte broadcasts); the blocks are merged
-// 16 -> 32 -> 64 with [[A,0],[C,B]]^{-1} = [[A^{-1},0],[-B^{-1} C A^{-1}, B^{-1}]], the merge
-// products on the tensor cores in tf32 (their ~1e-3 relative error is below the bf16 rounding
-// the result gets next). Writes -M and M Diag(ef) as bf16 RBM tiles.
 __device__ __forceinline__ float4 lds4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 
 constexpr int kLds = 36;   // row stride (floats) of the merge scratch (32 rows)
@@ -165,10 +171,17 @@ __device__ __forceinline__ void store_tile_16x8(float* C, int ldc, const float (
     C[(g + 8) * ldc + 2 * q + 1] = scale * c[3];
 }
 
+// (I + L)^{-1} for a 64x64 strictly lower-triangular fp32 L (row stride kLdL = 68 floats, so
+// rows are 16-byte aligned), by the 128 threads of group B (t = 0..127, named barrier kBarB).
+// The four 16x16 diagonal blocks are solved row by row (left-looking, one column per thread,
+// rows of L read as 16-byte broadcasts); the blocks are merged 16 -> 32 -> 64 with
+// [[A,0],[C,B]]^{-1} = [[A^{-1},0],[-B^{-1} C A^{-1}, B^{-1}]], the merge products on the tensor
+// cores in tf32 (their ~1e-3 relative error is below the bf16 rounding the result gets next).
+// Writes -M and M Diag(ef) as bf16 RBM tiles.
 __device__ __forceinline__ void unit_lower_inverse64(const float* L, float* Mf, float* scr, uint32_t t_mn,
-                                                     uint32_t t_my, const float* ef, int tid) {
-    if (tid < 64) {   // diagonal 16x16 blocks: M[i][j] = delta_ij - sum_{k<i} L[i][k] M[k][j]
-        const int b = tid >> 4, j = tid & 15, o = 16 * b;
+                                                     uint32_t t_my, const float* ef, int t) {
+    if (t < 64) {   // diagonal 16x16 blocks: M[i][j] = delta_ij - sum_{k<i} L[i][k] M[k][j]
+        const int b = t >> 4, j = t & 15, o = 16 * b;
         float m[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -188,43 +201,44 @@ __device__ __forceinline__ void unit_lower_inverse64(const float* L, float* Mf, 
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i) Mf[(o + i) * kLdL + o + j] = m[i];
-    }
-    named_sync(1, kSimt);
-    // merges on the tensor cores (mma.sync tf32, fp32 accumulate): one 16x8 output tile per warp
-    const int warp = tid >> 5;
-    {   // 16 -> 32 for the pairs of diagonal blocks (0,1) and (2,3); warps 0-3, warps 4-7 zero the
-        // blocks above the diagonal inside each 32x32 block
-        const int p = warp >> 1, ct = warp & 1, o = 32 * p;
-        if (warp < 4) {
-            float c[4];
-            warp_mma_tf32(L + (o + 16) * kLdL + o, kLdL, Mf + o * kLdL + o + 8 * ct, kLdL, 16, c);   // T = C A^{-1}
-            store_tile_16x8(scr + p * 16 * kLds + 8 * ct, kLds, c, 1.f);
-        } else {
-            const int e = tid - 128, r = e >> 2, cc = 4 * (e & 3), pp = r >> 4, rr = r & 15;
+    } else {        // zero the 16x16 blocks above the diagonal inside each 32x32 diagonal block
+        const int e = t - 64;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int f = e + 64 * h, r = f >> 2, cc = 4 * (f & 3), pp = r >> 4, rr = r & 15;
             *reinterpret_cast<float4*>(Mf + (32 * pp + rr) * kLdL + 32 * pp + 16 + cc) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        named_sync(1, kSimt);
-        if (warp < 4) {
-            float c[4];
-            warp_mma_tf32(Mf + (o + 16) * kLdL + o + 16, kLdL, scr + p * 16 * kLds + 8 * ct, kLds, 16, c);  // B^{-1} T
-            store_tile_16x8(Mf + (o + 16) * kLdL + o + 8 * ct, kLdL, c, -1.f);
-        }
-        named_sync(1, kSimt);
     }
-    {   // 32 -> 64: M[32:64, 0:32] = -B^{-1} (C A^{-1}); eight 16x8 tiles, one per warp
-        const int rt = warp >> 2, ct = warp & 3;
+    named_sync(kBarB, kGrp);
+    // merges on the tensor cores (mma.sync tf32, fp32 accumulate)
+    const int warp = t >> 5;
+    {   // 16 -> 32 for the pairs of diagonal blocks (0,1) and (2,3): one 16x8 tile per warp
+        const int p = warp >> 1, ct = warp & 1, o = 32 * p;
         float c[4];
-        warp_mma_tf32(L + (32 + 16 * rt) * kLdL, kLdL, Mf + 8 * ct, kLdL, 32, c);
-        store_tile_16x8(scr + 16 * rt * kLds + 8 * ct, kLds, c, 1.f);
-        named_sync(1, kSimt);
-        warp_mma_tf32(Mf + (32 + 16 * rt) * kLdL + 32, kLdL, scr + 8 * ct, kLds, 32, c);
-        store_tile_16x8(Mf + (32 + 16 * rt) * kLdL + 8 * ct, kLdL, c, -1.f);
-        named_sync(1, kSimt);
+        warp_mma_tf32(L + (o + 16) * kLdL + o, kLdL, Mf + o * kLdL + o + 8 * ct, kLdL, 16, c);   // T = C A^{-1}
+        store_tile_16x8(scr + p * 16 * kLds + 8 * ct, kLds, c, 1.f);
+        named_sync(kBarB, kGrp);
+        warp_mma_tf32(Mf + (o + 16) * kLdL + o + 16, kLdL, scr + p * 16 * kLds + 8 * ct, kLds, 16, c);  // B^{-1} T
+        store_tile_16x8(Mf + (o + 16) * kLdL + o + 8 * ct, kLdL, c, -1.f);
+        named_sync(kBarB, kGrp);
+    }
+    {   // 32 -> 64: M[32:64, 0:32] = -B^{-1} (C A^{-1}); eight 16x8 tiles, two per warp
+        float c0[4], c1[4];
+        warp_mma_tf32(L + 32 * kLdL, kLdL, Mf + 8 * warp, kLdL, 32, c0);
+        warp_mma_tf32(L + 48 * kLdL, kLdL, Mf + 8 * warp, kLdL, 32, c1);
+        store_tile_16x8(scr + 8 * warp, kLds, c0, 1.f);
+        store_tile_16x8(scr + 16 * kLds + 8 * warp, kLds, c1, 1.f);
+        named_sync(kBarB, kGrp);
+        warp_mma_tf32(Mf + 32 * kLdL + 32, kLdL, scr + 8 * warp, kLds, 32, c0);
+        warp_mma_tf32(Mf + 48 * kLdL + 32, kLdL, scr + 8 * warp, kLds, 32, c1);
+        store_tile_16x8(Mf + 32 * kLdL + 8 * warp, kLdL, c0, -1.f);
+        store_tile_16x8(Mf + 48 * kLdL + 8 * warp, kLdL, c1, -1.f);
+        named_sync(kBarB, kGrp);
     }
     // bf16 tiles -M and M Diag(ef); the 32x32 block above the diagonal is zero
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int item = tid + 256 * h, r = item & 63, c = (item >> 6) * 8;
+    for (int h = 0; h < 4; ++h) {
+        const int item = t + kGrp * h, r = item & 63, c = (item >> 6) * 8;
         float x[8], y[8];
         if ((c >> 5) > (r >> 5)) {
 #pragma unroll
@@ -240,6 +254,25 @@ __device__ __forceinline__ void unit_lower_inverse64(const float* L, float* Mf, 
     }
 }
 
+// Inclusive scan of a chunk's log-gates by one warp (lane holds tokens 2*lane, 2*lane+1).
+struct ChunkGates {
+    float G0, G1, GC;   // G at tokens 2*lane, 2*lane+1; G at the chunk end
+};
+__device__ __forceinline__ ChunkGates scan_gates(float g0, float g1) {
+    const int lane = threadIdx.x & 31;
+    float s = g0 + g1;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, s, off);
+        if (lane >= off) s += y;
+    }
+    ChunkGates r;
+    r.GC = __shfl_sync(0xffffffffu, s, 31);
+    r.G1 = s;
+    r.G0 = s - g1;
+    return r;
+}
+
 __global__ void __launch_bounds__(FNT, 1)
 gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
@@ -251,108 +284,153 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
         return;
     }
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Ly::BAR);
-    // MMA completions (issuer -> CUDA-core group)
-    uint64_t* mbar_E = bars + 0;
-    uint64_t* mbar_D = bars + 1;
-    uint64_t* mbar_XO = bars + 2;
-    uint64_t* mbar_Y = bars + 3;
+    // MMA completions (issuer -> groups)
+    uint64_t* mbar_D = bars + 0;     // D(j)                              -> B
+    uint64_t* mbar_Y = bars + 1;     // Y(j)                              -> C
+    uint64_t* mbar_Z = bars + 2;     // Z(j) (and everything before)      -> B, issuer
+    uint64_t* mbar_E = bars + 3;     // E(j)                              -> A, C
+    uint64_t* mbar_X = bars + 4;     // X(j), O(j)                        -> A
+    uint64_t* mbar_O = bars + 5;     // O~(j), the last product of chunk j -> C, issuer
     // bulk copies
-    uint64_t* mbar_kq = bars + 4;    // [2]
-    uint64_t* mbar_v = bars + 6;
-    // CUDA-core group -> issuer: prologue staged, S' in TMEM, Es tiles, M tiles
-    uint64_t* rdy_P = bars + 7;
-    uint64_t* rdy_S = bars + 8;
-    uint64_t* rdy_E = bars + 9;
-    uint64_t* rdy_M = bars + 10;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 11);
+    uint64_t* mbar_kq = bars + 6;    // [kKQBuf]
+    uint64_t* mbar_v = bars + 9;
+    // groups -> issuer
+    uint64_t* rdy_S = bars + 10;     // A: S'(j) in TMEM, e^{G_C} S in the accumulator
+    uint64_t* rdy_E = bars + 11;     // A: Es~(j) in TMEM
+    uint64_t* rdy_M = bars + 12;     // B: M(j) tiles (and D(j) consumed)
+    uint64_t* rdy_Yt = bars + 13;    // C: Y^T(j) tile (and Y(j) consumed)
+    uint64_t* o_free = bars + 14;    // C: O(j) consumed
+    uint64_t* drain = bars + 15;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 16);
+    int* o_seen = reinterpret_cast<int*>(bars + 17);    // C: chunks whose last product has completed
     float* scr = reinterpret_cast<float*>(smem + Ly::SCR);
     float* F_L = reinterpret_cast<float*>(smem + Ly::F_L);
     float* F_M = reinterpret_cast<float*>(smem + Ly::F_M);
-    float* rawG = reinterpret_cast<float*>(smem + Ly::RAW_G);
-    float* rawB = reinterpret_cast<float*>(smem + Ly::RAW_B);
-    auto vec = [&](int buf) { return reinterpret_cast<float*>(smem + Ly::VEC + buf * Ly::kVec); };
-    // vec(b): [0,64) ef, [64,128) eb, [128,192) bs = beta eb, [192] e^{a}, [193] e^{G_C - a}, [194] e^{G_C}
+    auto vec = [&](int grp, int buf) { return reinterpret_cast<float*>(smem + Ly::VEC + (2 * grp + buf) * Ly::kVec); };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quad = warp & 3, half = (warp >> 2) & 1;
-    const int row = tid & 127;                  // TMEM lane of this thread (CUDA-core group)
-    const bool issuer = warp == 8;
+    const int grp = warp >> 2;                  // 0 = A, 1 = B, 2 = C, 3 = issuer
+    const int gt = tid & (kGrp - 1);            // thread within its group = TMEM lane
     const size_t bh = blockIdx.x;
     const int T = pl.T;
     const int nchunk = (T + FC - 1) / FC;
     const int nfull = T / FC;                   // chunks loaded by TMA (only the last may be ragged)
     const size_t tok_base = bh * (size_t)T;
-    const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
 
     if (tid == 0) {
-        for (int i = 0; i < 11; ++i) mbar_init(bars + i, 1);
+        for (int i = 0; i < 16; ++i) mbar_init(bars + i, 1);
+        *o_seen = 0;
         mbar_fence_init();
     }
     if (warp == 0) tmem_alloc(tmem_holder, kTmemCols);
-    if (tid < 2 * FC) {   // gates of chunks 0 and 1
-        const int t = tid;
-        rawG[t] = (t < T) ? args.decay[tok_base + t] : 0.f;
-        rawB[t] = (t < T) ? args.beta[tok_base + t] : 0.f;
-    }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = *tmem_holder;
-    auto tKQ_of = [&](int jj) -> uint32_t { return sbase + ((jj & 1) ? Ly::T_KQ1 : Ly::T_KQ0); };
+    auto tKQ_of = [&](int jj) -> uint32_t { return sbase + Ly::T_KQ + (jj % kKQBuf) * KQ_BYTES; };
     auto tQK_of = [&](int jj, int lo) -> uint32_t { return sbase + Ly::T_QK + ((jj & 1) * 2 + lo) * FC * FC * 2; };
+    // raw gates of chunk jj for one warp: tokens 2*lane, 2*lane+1 (zero past the end)
+    auto load_gates = [&](int jj, float (&r)[4]) {
+        const int t0 = jj * FC + 2 * lane;
+        r[0] = (t0 < T) ? args.decay[tok_base + t0] : 0.f;
+        r[1] = (t0 + 1 < T) ? args.decay[tok_base + t0 + 1] : 0.f;
+        r[2] = (t0 < T) ? args.beta[tok_base + t0] : 0.f;
+        r[3] = (t0 + 1 < T) ? args.beta[tok_base + t0 + 1] : 0.f;
+    };
+    // bounded wait of a whole group on an mbarrier phase; false (for every thread) if it gave up.
+    // One thread polls; the others sleep on the group's hardware barrier, so the polling does
+    // not take issue slots from the warps that work (the issuer above all).
+    auto group_wait = [&](uint64_t* bar, uint32_t parity, uint32_t barid) -> bool {
+        bool got = true;
+        if (gt == 0) got = mbar_wait(bar, parity);
+        const bool bad = named_sync_or(barid, kGrp, !got);
+        fence_after_sync();
+        return !bad;
+    };
     bool failed = false;
 
-    if (issuer) {
-        // ======================= issuer warp: MMAs (lane 0) and bulk copies (all lanes) =======================
-        uint32_t kq_pend = 0;   // bit b: a k/q copy into buffer b is in flight
+    if (grp == 3) {
+        // ======================= issuer warp: MMAs and copies (lane 0), ragged loads (all lanes) ==========
+        uint32_t kq_pend = 0;   // bit b: a copy into k/q buffer b is in flight
         bool v_pend = false;
-        auto issue_kq = [&](int jj) {     // 4 boxes of 64 tokens x 64 features: lane = 2 * half + (q ? 1 : 0)
-            const int y = static_cast<int>(tok_base + (size_t)jj * FC);
-            unsigned char* dst = smem + ((jj & 1) ? Ly::T_KQ1 : Ly::T_KQ0);
-            if (lane == 0) mbar_expect_tx(&mbar_kq[jj & 1], 2u * FC * FD * 2);
-            __syncwarp();
-            if (lane < 4) tma_load_2d(dst + lane * SWH, (lane & 1) ? &tm_q : &tm_k, 64 * (lane >> 1), y, &mbar_kq[jj & 1]);
-            kq_pend |= 1u << (jj & 1);
-        };
-        auto issue_v = [&](int jj) {      // 2 boxes
-            const int y = static_cast<int>(tok_base + (size_t)jj * FC);
-            if (lane == 0) mbar_expect_tx(mbar_v, FC * FD * 2);
-            __syncwarp();
-            if (lane < 2) tma_load_2d(smem + Ly::T_V + lane * SWH, &tm_v, 64 * lane, y, mbar_v);
-            v_pend = true;
-        };
-        auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
+        auto wait1 = [&](uint64_t* bar, uint32_t parity) -> bool {
             bool ok = true;
             if (lane == 0) ok = mbar_wait(bar, parity);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             fence_after_sync();
             return ok;
         };
+        auto ragged_rows = [&](int jj, const __nv_bfloat16* src, uint32_t dst, uint32_t half_stride) {
+            const int valid = T - jj * FC;
+            const size_t g0 = tok_base + (size_t)jj * FC;
+            for (int i = lane; i < FC * (FD / 8); i += 32) {
+                const int cb = i & 15, t = i >> 4;   // 16-byte chunk cb of token t, in the swizzled layout
+                uint4 z = make_uint4(0, 0, 0, 0);
+                if (t < valid) z = *reinterpret_cast<const uint4*>(src + (g0 + t) * FD + 8 * cb);
+                st_shared_v4(dst + (cb >> 3) * half_stride + t * 128 + (((cb & 7) ^ (t & 7)) << 4), z.x, z.y, z.z, z.w);
+            }
+        };
+        auto load_kq = [&](int jj) {
+            const int b = jj % kKQBuf;
+            if (jj < nfull) {
+                const int y = static_cast<int>(tok_base + (size_t)jj * FC);
+                unsigned char* dst = smem + Ly::T_KQ + b * KQ_BYTES;
+                if (lane == 0) {
+                    mbar_expect_tx(&mbar_kq[b], KQ_BYTES);
+                    for (int x = 0; x < 4; ++x)   // x = 2 * half + (q ? 1 : 0)
+                        tma_load_2d(dst + x * SWH, (x & 1) ? &tm_q : &tm_k, 64 * (x >> 1), y, &mbar_kq[b]);
+                }
+                kq_pend |= 1u << b;
+            } else {   // ragged last chunk: plain loads, zero rows past the end
+                ragged_rows(jj, args.k, tKQ_of(jj), KQ_H);
+                ragged_rows(jj, args.q, tKQ_of(jj) + SWH, KQ_H);
+                fence_async_smem();
+            }
+            __syncwarp();
+        };
         auto wait_kq = [&](int jj) -> bool {
             if (jj >= nfull) return true;
-            const bool ok = wait_warp(&mbar_kq[jj & 1], (jj >> 1) & 1);
-            kq_pend &= ~(1u << (jj & 1));
+            const int b = jj % kKQBuf;
+            const bool ok = wait1(&mbar_kq[b], (jj / kKQBuf) & 1);
+            if (ok) kq_pend &= ~(1u << b);
             return ok;
+        };
+        auto load_v = [&](int jj) {
+            if (jj < nfull) {
+                const int y = static_cast<int>(tok_base + (size_t)jj * FC);
+                if (lane == 0) {
+                    mbar_expect_tx(mbar_v, FC * FD * 2);
+                    for (int x = 0; x < 2; ++x) tma_load_2d(smem + Ly::T_V + x * SWH, &tm_v, 64 * x, y, mbar_v);
+                }
+                v_pend = true;
+            } else {
+                ragged_rows(jj, args.v, sbase + Ly::T_V, SWH);
+                fence_async_smem();
+            }
+            __syncwarp();
         };
         auto wait_v = [&](int jj) -> bool {
             if (jj >= nfull) return true;
-            const bool ok = wait_warp(mbar_v, jj & 1);
-            v_pend = false;
+            const bool ok = wait1(mbar_v, jj & 1);
+            if (ok) v_pend = false;
             return ok;
         };
-        auto issue_D = [&](int jj) {
+        const uint32_t idN64 = idesc_bf16(128, FC, false, false);
+        // ---- the MMA groups (lane 0 issues, the warp re-converges after each)
+        auto mma_D = [&](int jj) {   // D = [K;Q] K^T: rows 0-63 k, 64-127 q of each feature half
             if (lane == 0) {
-                const uint32_t tk = tKQ_of(jj);   // rows 0-63 k, 64-127 q of each feature half
-#pragma unroll
+                const uint32_t tk = tKQ_of(jj);
+#pragma unroll 1
                 for (int h = 0; h < 2; ++h) {
                     const uint64_t d = smem_desc_sw128(tk + h * KQ_H, 16, 1024);
-                    mma_chain(tmem + TM_D, d, 32, d, 32, idesc_bf16(128, FC, false, false), 64, h > 0);
+                    mma_chain(tmem + TM_D, d, 32, d, 32, idN64, 64, h > 0);
                 }
                 mma_commit(mbar_D);
             }
             __syncwarp();
         };
-        auto issue_Y = [&](int jj) {   // Y^T = K^T (M Diag(ef))^T
+        auto mma_Y = [&](int jj) {   // Y^T = K^T (M Diag(ef))^T
             if (lane == 0) {
                 mma_chain(tmem + TM_Y, smem_desc_sw128(tKQ_of(jj), KQ_H, 1024), 2048,
                           smem_desc(sbase + Ly::T_MY, 128, N64_RB), 256, idesc_bf16(128, FC, true, false), FC, false);
@@ -360,332 +438,329 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
             }
             __syncwarp();
         };
-        if (nchunk > 0) {
-            if (nfull > 0) { issue_kq(0); issue_v(0); }
-            if (nfull > 1) issue_kq(1);
-            // prologue: D(0), then Y(0) once the CUDA-core group has the M tiles
-            failed = !wait_warp(rdy_P, 0) || !wait_kq(0);
-            if (!failed) {
-                issue_D(0);
-                failed = !wait_warp(rdy_M, 0);
-            }
-            if (!failed) issue_Y(0);
-        }
-        for (int j = 0; j < nchunk && !failed; ++j) {
-            const int b = j & 1;
-            const bool has_next = j + 1 < nchunk;
-            // E(j), O'(j) from the state; D(j+1) right behind them
-            if (!wait_warp(rdy_S, b) || !wait_v(j)) { failed = true; break; }
+        auto mma_Z = [&]() {         // E^T := V^T (-M)^T
             if (lane == 0) {
-                const uint32_t tk = tKQ_of(j);
-                mma_chain_tmem_a(tmem + TM_E, tmem + TM_SH, smem_desc(sbase + Ly::T_YT, N64_RB, 128), 2 * N64_RB,
-                                 idesc_bf16(128, FC, false, true), FD, false);                    // S'^T Y^T
                 mma_chain(tmem + TM_E, smem_desc_sw128(sbase + Ly::T_V, SWH, 1024), 2048,
-                          smem_desc(sbase + Ly::T_MN, 128, N64_RB), 256, idesc_bf16(128, FC, true, false), FC,
-                          true);                                                                  // + V^T (-M)^T
+                          smem_desc(sbase + Ly::T_MN, 128, N64_RB), 256, idesc_bf16(128, FC, true, false), FC, false);
+                mma_commit(mbar_Z);
+            }
+            __syncwarp();
+        };
+        auto mma_E = [&]() {         // E^T += S'^T Y^T
+            if (lane == 0) {
+                mma_chain_tmem_a(tmem + TM_E, tmem + TM_SH, smem_desc(sbase + Ly::T_YT, N64_RB, 128), 2 * N64_RB,
+                                 idesc_bf16(128, FC, false, true), FD, true);
                 mma_commit(mbar_E);
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {                                                    // q rows, K-major
-                    const uint64_t dQ = smem_desc_sw128(tk + SWH + h * KQ_H, 16, 1024);
-                    mma_chain_tmem_a(tmem + TM_O, tmem + TM_SH + 32 * h, dQ, 32, idesc_bf16(128, FC, false, false), 64,
-                                     h > 0);
-                    mma_chain_tmem_a(tmem + TM_O, tmem + TM_SL + 32 * h, dQ, 32, idesc_bf16(128, FC, false, false), 64,
-                                     true);
+            }
+            __syncwarp();
+        };
+        auto mma_O = [&](int j) {    // O'^T = S'^T Q^T with S' = hi + lo (q rows, K-major)
+            if (lane == 0) {
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h) {
+                    const uint64_t dQ = smem_desc_sw128(tKQ_of(j) + SWH + h * KQ_H, 16, 1024);
+                    mma_chain_tmem_a(tmem + TM_O, tmem + TM_SH + 32 * h, dQ, 32, idN64, 64, h > 0);
+                    mma_chain_tmem_a(tmem + TM_O, tmem + TM_SL + 32 * h, dQ, 32, idN64, 64, true);
                 }
             }
             __syncwarp();
-            if (has_next) {
-                if (!wait_kq(j + 1)) { failed = true; break; }
-                issue_D(j + 1);
-            }
-            // v of the next chunk once E(j) has read it
-            if (!wait_warp(mbar_E, b)) { failed = true; break; }
-            if (has_next && j + 1 < nfull) issue_v(j + 1);
-            // X(j), O'(j) from Es
-            if (!wait_warp(rdy_E, b)) { failed = true; break; }
+        };
+        auto mma_X = [&](int j) {    // S^T += Es~^T K (hi + lo); Es~ hi at 32*(s/2) + 8*(s%2), lo 16 further
             if (lane == 0) {
-                const uint32_t tk = tKQ_of(j);
-                const uint64_t dK = smem_desc_sw128(tk, KQ_H, 1024);         // k rows, MN-major B (K = rho)
-                const uint32_t idX = idesc_bf16(128, FD, false, true), idO = idesc_bf16(128, FC, false, false);
-                mma_chain(tmem + TM_X, smem_desc(sbase + Ly::T_ESH, 128, N64_RB), 256, dK, 2048, idX, FC, false);
-                mma_chain(tmem + TM_X, smem_desc(sbase + Ly::T_ESL, 128, N64_RB), 256, dK, 2048, idX, FC, true);
-                mma_chain(tmem + TM_O, smem_desc(sbase + Ly::T_ESH, 128, N64_RB), 256,
-                          smem_desc(tQK_of(j, 0), 128, N64_RB), 256, idO, FC, true);
-                mma_chain(tmem + TM_O, smem_desc(sbase + Ly::T_ESL, 128, N64_RB), 256,
-                          smem_desc(tQK_of(j, 0), 128, N64_RB), 256, idO, FC, true);
-                mma_chain(tmem + TM_O, smem_desc(sbase + Ly::T_ESH, 128, N64_RB), 256,
-                          smem_desc(tQK_of(j, 1), 128, N64_RB), 256, idO, FC, true);
-                mma_commit(mbar_XO);
+                const uint64_t dK = smem_desc_sw128(tKQ_of(j), KQ_H, 1024);   // k rows, MN-major B (K = rho)
+                const uint32_t idX = idesc_bf16(128, FD, false, true);
+#pragma unroll 1
+                for (int sl = 0; sl < 4; ++sl) {
+                    const uint32_t ah = tmem + TM_E + 32 * (sl >> 1) + 8 * (sl & 1);
+                    const uint64_t b = dK + static_cast<uint64_t>((2048u * sl) >> 4);
+                    mma_bf16_tmem_a(tmem + TM_S, ah, b, idX, 1u);
+                    mma_bf16_tmem_a(tmem + TM_S, ah + 16, b, idX, 1u);
+                }
+                mma_commit(mbar_X);
             }
             __syncwarp();
-            // Y(j+1) once its M tiles are ready
-            if (has_next) {
-                if (!wait_warp(rdy_M, (j + 1) & 1)) { failed = true; break; }
-                issue_Y(j + 1);
+        };
+        auto mma_Oes = [&](int j) {  // O'^T += Es~^T QK~^T: hi*hi + lo*hi + hi*lo
+            if (lane == 0) {
+#pragma unroll 1
+                for (int sl = 0; sl < 4; ++sl) {
+                    const uint32_t ah = tmem + TM_E + 32 * (sl >> 1) + 8 * (sl & 1);
+                    const uint64_t bh_ = smem_desc(tQK_of(j, 0) + 256 * sl, 128, N64_RB);
+                    const uint64_t bl_ = smem_desc(tQK_of(j, 1) + 256 * sl, 128, N64_RB);
+                    mma_bf16_tmem_a(tmem + TM_O, ah, bh_, idN64, 1u);
+                    mma_bf16_tmem_a(tmem + TM_O, ah + 16, bh_, idN64, 1u);
+                    mma_bf16_tmem_a(tmem + TM_O, ah, bl_, idN64, 1u);
+                }
+                mma_commit(mbar_O);
             }
-            // k, q of chunk j + 2 into buffer b once X(j), O(j) are done
-            if (!wait_warp(mbar_XO, b)) { failed = true; break; }
-            if (j + 2 < nfull) issue_kq(j + 2);
+            __syncwarp();
+        };
+
+        if (nchunk > 0) {
+            load_kq(0);
+            if (nchunk > 1) load_kq(1);
+            load_v(0);
+        }
+        // j = -2, -1: the WY build of chunks 0 and 1 only
+        for (int j = -2; j < nchunk && !failed; ++j) {
+            const bool next = j + 1 < nchunk;
+            if (j >= 0) {
+                // E(j) once S'(j) and Y^T(j) are in place
+                if (!wait1(rdy_S, j & 1) || !wait1(rdy_Yt, j & 1)) { failed = true; break; }
+                mma_E();
+                // copies: k/q of chunk j+2 (its buffer held chunk j-1), v of chunk j+1 (v(j) was read by Z(j))
+                if (j + 2 < nchunk) {
+                    if (j >= 1 && !wait1(mbar_O, (j - 1) & 1)) { failed = true; break; }
+                    load_kq(j + 2);
+                }
+                if (next) {
+                    if (!wait1(mbar_Z, j & 1)) { failed = true; break; }
+                    load_v(j + 1);
+                }
+                // O(j) while group A forms Es~(j)
+                if (j >= 1 && !wait1(o_free, (j - 1) & 1)) { failed = true; break; }
+                mma_O(j);
+                // X(j): the state update
+                if (!wait1(rdy_E, j & 1)) { failed = true; break; }
+                mma_X(j);
+                mma_Oes(j);
+            }
+            // state-independent products of the next chunks
+            if (j >= -1 && next) {
+                if (!wait1(rdy_M, (j + 1) & 1)) { failed = true; break; }
+                mma_Y(j + 1);
+                if (!wait_v(j + 1)) { failed = true; break; }
+                mma_Z();
+            }
+            if (j + 2 < nchunk) {
+                if (!wait_kq(j + 2)) { failed = true; break; }
+                mma_D(j + 2);
+            }
         }
         if (failed) {
             if (lane == 0) {
                 atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
-                uint64_t* drain = bars + 12;   // spare slot: a commit now tracks every earlier MMA
-                mbar_init(drain, 1);
-                mbar_fence_init();
-                mma_commit(drain);
+                mma_commit(drain);   // tracks every MMA issued so far
                 mbar_wait(drain, 0, 400000000LL);
-                for (int i = 0; i < 2; ++i)
-                    if (kq_pend & (1u << i)) { mbar_wait(&mbar_kq[i], 0, 400000000LL); mbar_wait(&mbar_kq[i], 1, 400000000LL); }
+                for (int b = 0; b < kKQBuf; ++b)
+                    if (kq_pend & (1u << b)) { mbar_wait(&mbar_kq[b], 0, 400000000LL); mbar_wait(&mbar_kq[b], 1, 400000000LL); }
                 if (v_pend) { mbar_wait(mbar_v, 0, 400000000LL); mbar_wait(mbar_v, 1, 400000000LL); }
             }
             __syncwarp();
         }
-    } else {
-        // ======================= CUDA-core group (warps 0-7) =======================
-        auto sync = [&]() { named_sync(1, kSimt); };
-        auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
-            const bool got = mbar_wait(bar, parity);
-            const bool bad = named_sync_or(1, kSimt, !got);
-            fence_after_sync();
-            return !bad;
-        };
-        auto signal = [&](uint64_t* bar) {   // after a group sync: one arrival
-            if (tid == 0) mbar_arrive(bar);
-        };
-        auto plain_kq = [&](int jj) {        // ragged (last) chunk: zero rows past the end
-            const int valid = T - jj * FC;
-            const size_t g0 = tok_base + (size_t)jj * FC;
-            const uint32_t tk = tKQ_of(jj);
-            for (int i = tid; i < FC * (FD / 8); i += kSimt) {
-                const int cb = i & 15, t = i >> 4;   // 16-byte chunk cb of token t, in the swizzled layout
-                uint4 zq = make_uint4(0, 0, 0, 0), zk = zq;
-                if (t < valid) {
-                    zq = *reinterpret_cast<const uint4*>(args.q + (g0 + t) * FD + 8 * cb);
-                    zk = *reinterpret_cast<const uint4*>(args.k + (g0 + t) * FD + 8 * cb);
-                }
-                const uint32_t off = (cb >> 3) * KQ_H + t * 128 + (((cb & 7) ^ (t & 7)) << 4);
-                st_shared_v4(tk + off, zk.x, zk.y, zk.z, zk.w);
-                st_shared_v4(tk + SWH + off, zq.x, zq.y, zq.z, zq.w);
-            }
-        };
-        auto plain_v = [&](int jj) {
-            const int valid = T - jj * FC;
-            const size_t g0 = tok_base + (size_t)jj * FC;
-            for (int i = tid; i < FC * (FD / 8); i += kSimt) {
-                const int cb = i & 15, t = i >> 4;
-                uint4 zv = make_uint4(0, 0, 0, 0);
-                if (t < valid) zv = *reinterpret_cast<const uint4*>(args.v + (g0 + t) * FD + 8 * cb);
-                const uint32_t off = (cb >> 3) * SWH + t * 128 + (((cb & 7) ^ (t & 7)) << 4);
-                st_shared_v4(sbase + Ly::T_V + off, zv.x, zv.y, zv.z, zv.w);
-            }
-        };
-        auto gate_factors = [&](int jj) {    // warp 0
+    } else if (grp == 0) {
+        // ======================= group A: the state chain =======================
+        float graw[4];
+        if (warp == 0 && nchunk > 0) load_gates(0, graw);
+        auto gates = [&](int jj) {   // warp 0: e^{a}, gamma = e^{G_C}, nc_bs = -beta e^{G_C - G}
             if (warp != 0) return;
-            const float* g = rawG + (jj & 1) * FC;
-            const float* be = rawB + (jj & 1) * FC;
-            float* vf = vec(jj & 1);
-            const float x0 = g[2 * lane], x1 = g[2 * lane + 1];
-            float s = x0 + x1;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, s, off);
-                if (lane >= off) s += y;
-            }
-            const float gc = __shfl_sync(0xffffffffu, s, 31);
-            const float a = 0.5f * gc;
-            const float G1 = s, G0 = s - x1;
-            const float e0 = __expf(a - G0), e1 = __expf(a - G1);
-            vf[2 * lane] = __expf(G0 - a);
-            vf[2 * lane + 1] = __expf(G1 - a);
-            vf[64 + 2 * lane] = e0;
-            vf[64 + 2 * lane + 1] = e1;
-            vf[128 + 2 * lane] = be[2 * lane] * e0;
-            vf[128 + 2 * lane + 1] = be[2 * lane + 1] * e1;
+            float* vf = vec(0, jj & 1);
+            const ChunkGates g = scan_gates(graw[0], graw[1]);
+            vf[64 + 2 * lane] = -graw[2] * __expf(g.GC - g.G0);
+            vf[64 + 2 * lane + 1] = -graw[3] * __expf(g.GC - g.G1);
             if (lane == 0) {
-                vf[192] = __expf(a);
-                vf[193] = __expf(gc - a);
-                vf[194] = __expf(gc);
+                vf[0] = __expf(0.5f * g.GC);
+                vf[1] = __expf(g.GC);
             }
+            if (jj + 1 < nchunk) load_gates(jj + 1, graw);
         };
-        // L and -QK of chunk jj from D: L -> F_L (fp32), -QK -> QK tiles (hi + lo) of buffer jj & 1
-        auto epi_D = [&](int jj) {
-            const float* vf = vec(jj & 1);
-            float x[32];
-            tmem_ld32(tmem + TM_D + lane_off + 32 * half, x);
-            if (row < FC) {              // L row t: ef_t D_ts beta_s eb_s for s < t
-                const int t = row;
-                const float eft = vf[t];
-#pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    float y[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int sg = 32 * half + i + u;
-                        y[u] = (sg < t) ? eft * x[i + u] * vf[128 + sg] : 0.f;
-                    }
-                    *reinterpret_cast<float4*>(F_L + t * kLdL + 32 * half + i) = make_float4(y[0], y[1], y[2], y[3]);
-                }
-            } else {                     // -QK row t (inclusive causal), hi + lo
-                const int t = row - FC;
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int sg = 32 * half + i;
-                    x[i] = (sg <= t) ? -x[i] : 0.f;
-                }
-#pragma unroll
-                for (int i = 0; i < 32; i += 8)
-                    rbm_store8_split(tQK_of(jj, 0), tQK_of(jj, 1), FC, t, 32 * half + i, x + i);
-            }
-        };
-        auto epi_Y = [&]() {
-            float x[32];
-            tmem_ld32(tmem + TM_Y + lane_off + 32 * half, x);
-#pragma unroll
-            for (int i = 0; i < 32; i += 8) rbm_store8(sbase + Ly::T_YT, FC, row, 32 * half + i, x + i);
-        };
-
-        // fp32 state, transposed: this thread holds S^T[n = row][c] for c in [64*half, 64*half + 64)
-        float S[64];
-#pragma unroll
-        for (int i = 0; i < 64; ++i) S[i] = args.S0 ? args.S0[(bh * FD + 64 * half + i) * FD + row] : 0.f;
-
         if (nchunk > 0) {
-            // ---- prologue: the state-independent part of chunk 0
-            gate_factors(0);
-            if (nfull == 0) { plain_kq(0); plain_v(0); }
-            fence_async_smem();
-            sync();
-            signal(rdy_P);
-            failed = !wait_all(mbar_D, 0);
-            if (!failed) {
-                epi_D(0);
-                fence_async_smem();
-                fence_before_sync();
-                sync();
-                unit_lower_inverse64(F_L, F_M, scr, sbase + Ly::T_MN, sbase + Ly::T_MY, vec(0), tid);
-                fence_async_smem();
-                sync();
-                signal(rdy_M);
-                failed = !wait_all(mbar_Y, 0);
-            }
-            if (!failed) {
-                epi_Y();
-                fence_async_smem();
-                fence_before_sync();
-                sync();
-            }
-        }
-
-        for (int j = 0; j < nchunk && !failed; ++j) {
-            const int b = j & 1;
-            const bool has_next = j + 1 < nchunk;
-            const int valid = min(FC, T - j * FC);
-            const size_t g0 = tok_base + (size_t)j * FC;
-            const float* vf = vec(b);
-            float g_n2 = 0.f, b_n2 = 0.f;    // gates of chunk j + 2 (stored into buffer b after this chunk)
-            if (tid < FC && (j + 2) * FC + tid < T) {
-                g_n2 = args.decay[tok_base + (size_t)(j + 2) * FC + tid];
-                b_n2 = args.beta[tok_base + (size_t)(j + 2) * FC + tid];
-            }
-
-            // ---- S'^T = e^{a} S^T of chunk j into TMEM as bf16 hi + lo (A operand of E and O)
-            {
-                const float ea = vf[192];
+            gates(0);
+#pragma unroll 1
+            for (int p = 0; p < 4; ++p) {   // S0^T into the accumulator
+                uint32_t x[32];
 #pragma unroll
-                for (int part = 0; part < 2; ++part) {
+                for (int i = 0; i < 32; ++i)
+                    x[i] = __float_as_uint(args.S0 ? args.S0[(bh * FD + 32 * p + i) * FD + gt] : 0.f);
+                tmem_st32(tmem + TM_S + lane_off + 32 * p, x);
+            }
+            tmem_wait_st();
+        }
+        named_sync(kBarA, kGrp);
+        for (int j = 0; j < nchunk && !failed; ++j) {
+            const float* vf = vec(0, j & 1);
+            if (j > 0 && !group_wait(mbar_X, (j - 1) & 1, kBarA)) { failed = true; break; }
+            {   // ---- S'^T (hi, lo) and gamma S^T
+                const float ea = vf[0], gam = vf[1];
+#pragma unroll 1
+                for (int p = 0; p < 4; ++p) {
+                    float x[32];
+                    tmem_ld32(tmem + TM_S + lane_off + 32 * p, x);
                     uint32_t hi[16], lo[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float s0 = ea * S[32 * part + 2 * i], s1 = ea * S[32 * part + 2 * i + 1];
-                        hi[i] = pack_bf16(s0, s1);
-                        lo[i] = pack_bf16(s0 - __uint_as_float(hi[i] << 16), s1 - __uint_as_float(hi[i] & 0xFFFF0000u));
-                    }
-                    tmem_st16(tmem + TM_SH + lane_off + 32 * half + 16 * part, hi);
-                    tmem_st16(tmem + TM_SL + lane_off + 32 * half + 16 * part, lo);
+                    for (int i = 0; i < 16; ++i) split_pair(ea * x[2 * i], ea * x[2 * i + 1], hi[i], lo[i]);
+                    tmem_st16(tmem + TM_SH + lane_off + 16 * p, hi);
+                    tmem_st16(tmem + TM_SL + lane_off + 16 * p, lo);
+                    uint32_t g[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) g[i] = __float_as_uint(gam * x[i]);
+                    tmem_st32(tmem + TM_S + lane_off + 32 * p, g);
                 }
                 tmem_wait_st();
             }
-            if (has_next && j + 1 >= nfull) plain_kq(j + 1);      // ragged next chunk (its buffer is free)
-            fence_async_smem();
             fence_before_sync();
-            sync();
-            signal(rdy_S);
-
-            // ---- gate factors of chunk j + 1 (warp 0), while E and O run
-            if (has_next) gate_factors(j + 1);
-
-            // ---- Es^T = Diag(beta eb) E^T of chunk j (hi + lo)
-            if (!wait_all(mbar_E, b)) { failed = true; break; }
-            {
+            named_sync(kBarA, kGrp);
+            if (gt == 0) mbar_arrive(rdy_S);
+            // ---- Es~^T of chunk j, in place of E^T
+            if (!group_wait(mbar_E, j & 1, kBarA)) { failed = true; break; }
+#pragma unroll 1
+            for (int p = 0; p < 2; ++p) {
                 float x[32];
-                tmem_ld32(tmem + TM_E + lane_off + 32 * half, x);
+                tmem_ld32(tmem + TM_E + lane_off + 32 * p, x);
+                uint32_t hi[16], lo[16];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) x[i] *= vf[128 + 32 * half + i];
-#pragma unroll
-                for (int i = 0; i < 32; i += 8)
-                    rbm_store8_split(sbase + Ly::T_ESH, sbase + Ly::T_ESL, FC, row, 32 * half + i, x + i);
+                for (int i = 0; i < 16; ++i)
+                    split_pair(vf[64 + 32 * p + 2 * i] * x[2 * i], vf[64 + 32 * p + 2 * i + 1] * x[2 * i + 1], hi[i], lo[i]);
+                tmem_st16(tmem + TM_E + lane_off + 32 * p, hi);
+                tmem_st16(tmem + TM_E + lane_off + 32 * p + 16, lo);
             }
-            if (has_next && j + 1 >= nfull) plain_v(j + 1);        // ragged next chunk (v of chunk j is consumed)
-            fence_async_smem();
+            tmem_wait_st();
             fence_before_sync();
-            sync();
-            signal(rdy_E);
-
-            // ---- state-independent part of chunk j + 1, in the shadow of X(j), O(j)
-            if (has_next) {
-                if (!wait_all(mbar_D, (j + 1) & 1)) { failed = true; break; }
-                epi_D(j + 1);
-                fence_async_smem();
-                fence_before_sync();
-                sync();
-                unit_lower_inverse64(F_L, F_M, scr, sbase + Ly::T_MN, sbase + Ly::T_MY, vec(b ^ 1), tid);
-                fence_async_smem();
-                sync();
-                signal(rdy_M);
-            }
-
-            // ---- state update and chunk output of chunk j
-            if (!wait_all(mbar_XO, b)) { failed = true; break; }
-            {
-                const float gam = vf[194], egca = vf[193];
-                float x[32];
+            if (j + 1 < nchunk) gates(j + 1);
+            named_sync(kBarA, kGrp);
+            if (gt == 0) mbar_arrive(rdy_E);
+        }
+        if (!failed) {   // final state
+            if (nchunk > 0 && !group_wait(mbar_X, (nchunk - 1) & 1, kBarA)) failed = true;
+            if (!failed && args.ST) {
+#pragma unroll 1
+                for (int p = 0; p < 4; ++p) {
+                    float x[32];
+                    if (nchunk == 0) {
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    tmem_ld32(tmem + TM_X + lane_off + 64 * half + 32 * h, x);
+                        for (int i = 0; i < 32; ++i)
+                            x[i] = args.S0 ? args.S0[(bh * FD + 32 * p + i) * FD + gt] : 0.f;
+                    } else {
+                        tmem_ld32(tmem + TM_S + lane_off + 32 * p, x);
+                    }
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) S[32 * h + i] = fmaf(gam, S[32 * h + i], -egca * x[i]);
-                }
-                tmem_ld32(tmem + TM_O + lane_off + 32 * half, x);      // O'^T row n = row, tokens 32*half + i
-                float* orow = args.o + g0 * FD + row;
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int t = 32 * half + i;
-                    if (t < valid) orow[(size_t)t * FD] = vf[t] * x[i];
+                    for (int i = 0; i < 32; ++i) args.ST[(bh * FD + 32 * p + i) * FD + gt] = x[i];
                 }
             }
-            if (tid < FC) {
-                rawG[b * FC + tid] = g_n2;
-                rawB[b * FC + tid] = b_n2;
+        }
+        if (failed && gt == 0) atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
+    } else if (grp == 1) {
+        // ======================= group B: the WY build of each chunk =======================
+        float graw[4];
+        if (warp == 4 && nchunk > 0) load_gates(0, graw);
+        for (int jj = 0; jj < nchunk && !failed; ++jj) {
+            float* vf = vec(1, jj & 1);
+            if (warp == 4) {   // ef = e^{G - a}, bs = beta e^{a - G}, 1/c = e^{a - G_C}
+                const ChunkGates g = scan_gates(graw[0], graw[1]);
+                const float a = 0.5f * g.GC;
+                vf[2 * lane] = __expf(g.G0 - a);
+                vf[2 * lane + 1] = __expf(g.G1 - a);
+                vf[64 + 2 * lane] = graw[2] * __expf(a - g.G0);
+                vf[64 + 2 * lane + 1] = graw[3] * __expf(a - g.G1);
+                if (lane == 0) vf[128] = __expf(a - g.GC);
+                if (jj + 1 < nchunk) load_gates(jj + 1, graw);
+            }
+            if (!group_wait(mbar_D, jj & 1, kBarB)) { failed = true; break; }   // also orders the gates
+            if (jj >= 2) {   // QK~ tiles of buffer jj & 1 were read by the last product of chunk jj - 2
+                bool ok = true;
+                if (gt == 0) {
+                    const long long t0 = clock64();
+                    while (ld_acquire_shared(o_seen) < jj - 1)
+                        if (clock64() - t0 > 4000000000LL) { ok = false; break; }
+                }
+                if (named_sync_or(kBarB, kGrp, !ok)) { failed = true; break; }
+            }
+            {   // ---- L (rows 0-63 of D) and QK~ (rows 64-127), one TMEM lane per thread
+                const float inv_c = vf[128];
+#pragma unroll 1
+                for (int hh = 0; hh < 2; ++hh) {
+                    float x[32];
+                    tmem_ld32(tmem + TM_D + lane_off + 32 * hh, x);
+                    if (gt < FC) {
+                        const int t = gt;
+                        const float eft = vf[t];
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4) {
+                            float y[4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const int sg = 32 * hh + i + u;
+                                y[u] = (sg < t) ? eft * x[i + u] * vf[64 + sg] : 0.f;
+                            }
+                            *reinterpret_cast<float4*>(F_L + t * kLdL + 32 * hh + i) = make_float4(y[0], y[1], y[2], y[3]);
+                        }
+                    } else {
+                        const int t = gt - FC;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) x[i] = (32 * hh + i <= t) ? x[i] * inv_c : 0.f;
+#pragma unroll
+                        for (int i = 0; i < 32; i += 8)
+                            rbm_store8_split(tQK_of(jj, 0), tQK_of(jj, 1), FC, t, 32 * hh + i, x + i);
+                    }
+                }
             }
             fence_before_sync();
-            sync();
-
-            // ---- Y^T of chunk j + 1 into its tile
-            if (has_next) {
-                if (!wait_all(mbar_Y, (j + 1) & 1)) { failed = true; break; }
+            if (jj >= 1 && !group_wait(mbar_Z, (jj - 1) & 1, kBarB)) { failed = true; break; }   // M tiles free
+            unit_lower_inverse64(F_L, F_M, scr, sbase + Ly::T_MN, sbase + Ly::T_MY, vf, gt);
+            fence_async_smem();
+            fence_before_sync();
+            named_sync(kBarB, kGrp);
+            if (gt == 0) mbar_arrive(rdy_M);
+        }
+        if (failed && gt == 0) atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
+    } else {
+        // ======================= group C: Y^T tiles and the chunk outputs =======================
+        float graw[4];
+        if (warp == 8 && nchunk > 0) load_gates(0, graw);
+        auto epi_Y = [&]() {
+#pragma unroll 1
+            for (int hh = 0; hh < 2; ++hh) {
+                float x[32];
+                tmem_ld32(tmem + TM_Y + lane_off + 32 * hh, x);
+#pragma unroll
+                for (int i = 0; i < 32; i += 8) rbm_store8(sbase + Ly::T_YT, FC, gt, 32 * hh + i, x + i);
+            }
+            fence_async_smem();
+            fence_before_sync();
+            named_sync(kBarC, kGrp);
+            if (gt == 0) mbar_arrive(rdy_Yt);
+        };
+        if (nchunk > 0) {
+            if (!group_wait(mbar_Y, 0, kBarC)) failed = true;
+            else epi_Y();
+        }
+        for (int j = 0; j < nchunk && !failed; ++j) {
+            float* vf = vec(2, j & 1);
+            if (warp == 8) {   // ef of chunk j
+                const ChunkGates g = scan_gates(graw[0], graw[1]);
+                const float a = 0.5f * g.GC;
+                vf[2 * lane] = __expf(g.G0 - a);
+                vf[2 * lane + 1] = __expf(g.G1 - a);
+                if (j + 1 < nchunk) load_gates(j + 1, graw);
+            }
+            if (j + 1 < nchunk) {   // Y^T of chunk j + 1 (its tile was read by E(j))
+                if (!group_wait(mbar_Y, (j + 1) & 1, kBarC) || !group_wait(mbar_E, j & 1, kBarC)) {
+                    failed = true;
+                    break;
+                }
                 epi_Y();
-                fence_async_smem();
-                fence_before_sync();
-                sync();
             }
-        }
-        if (failed) {
-            if (tid == 0) atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
-        } else if (args.ST) {
+            if (!group_wait(mbar_O, j & 1, kBarC)) { failed = true; break; }   // also orders ef
+            if (gt == 0) st_release_shared(o_seen, j + 1);
+            {   // ---- o_t = ef_t O'_t
+                const int valid = min(FC, T - j * FC);
+                float* ocol = args.o + (tok_base + (size_t)j * FC) * FD + gt;
+#pragma unroll 1
+                for (int hh = 0; hh < 2; ++hh) {
+                    float x[32];
+                    tmem_ld32(tmem + TM_O + lane_off + 32 * hh, x);
 #pragma unroll
-            for (int i = 0; i < 64; ++i) args.ST[(bh * FD + 64 * half + i) * FD + row] = S[i];
+                    for (int i = 0; i < 32; ++i) {
+                        const int t = 32 * hh + i;
+                        if (t < valid) ocol[(size_t)t * FD] = vf[t] * x[i];
+                    }
+                }
+            }
+            fence_before_sync();
+            named_sync(kBarC, kGrp);
+            if (gt == 0) mbar_arrive(o_free);
         }
+        if (failed && gt == 0) atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
     }
     fence_before_sync();
     __syncthreads();

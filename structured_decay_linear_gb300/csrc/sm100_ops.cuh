@@ -76,6 +76,7 @@ __device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem
 // Chain of K/16 MMAs with A in tensor memory (8 columns per K=16 slice).
 __device__ __forceinline__ void mma_chain_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t b_step,
                                                  uint32_t idesc, int K, bool accumulate) {
+#pragma unroll 1
     for (int ks = 0; ks < K / 16; ++ks)
         mma_bf16_tmem_a(d_tmem, a_tmem + 8 * ks, b + static_cast<uint64_t>((b_step * ks) >> 4), idesc,
                         (accumulate || ks > 0) ? 1u : 0u);
@@ -128,6 +129,7 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* mbar) {
 // Chain of K/16 MMAs; a_step/b_step: byte advance of each operand per K=16 slice.
 __device__ __forceinline__ void mma_chain(uint32_t d_tmem, uint64_t a, uint32_t a_step, uint64_t b, uint32_t b_step,
                                           uint32_t idesc, int K, bool accumulate) {
+#pragma unroll 1
     for (int ks = 0; ks < K / 16; ++ks) {
         mma_bf16(d_tmem, a + static_cast<uint64_t>((a_step * ks) >> 4), b + static_cast<uint64_t>((b_step * ks) >> 4),
                  idesc, (accumulate || ks > 0) ? 1u : 0u);
@@ -181,6 +183,16 @@ __device__ __forceinline__ void mbar_fence_init() { asm volatile("fence.mbarrier
 
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* mbar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(smem_addr(mbar)), "r"(bytes) : "memory");
+}
+
+// Shared-memory counters with acquire / release ordering (CTA scope).
+__device__ __forceinline__ int ld_acquire_shared(const int* p) {
+    int v;
+    asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_shared(int* p, int v) {
+    asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" :: "r"(smem_addr(p)), "r"(v) : "memory");
 }
 
 // Bounded wait for the phase with the given parity. Returns false if it gave up
