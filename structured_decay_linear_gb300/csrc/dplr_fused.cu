@@ -421,7 +421,7 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
         auto mma_D = [&](int jj) {   // D = [K;Q] K^T: rows 0-63 k, 64-127 q of each feature half
             if (lane == 0) {
                 const uint32_t tk = tKQ_of(jj);
-#pragma unroll 1
+#pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const uint64_t d = smem_desc_sw128(tk + h * KQ_H, 16, 1024);
                     mma_chain(tmem + TM_D, d, 32, d, 32, idN64, 64, h > 0);
@@ -456,7 +456,7 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
         };
         auto mma_O = [&](int j) {    // O'^T = S'^T Q^T with S' = hi + lo (q rows, K-major)
             if (lane == 0) {
-#pragma unroll 1
+#pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const uint64_t dQ = smem_desc_sw128(tKQ_of(j) + SWH + h * KQ_H, 16, 1024);
                     mma_chain_tmem_a(tmem + TM_O, tmem + TM_SH + 32 * h, dQ, 32, idN64, 64, h > 0);
@@ -469,7 +469,7 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
             if (lane == 0) {
                 const uint64_t dK = smem_desc_sw128(tKQ_of(j), KQ_H, 1024);   // k rows, MN-major B (K = rho)
                 const uint32_t idX = idesc_bf16(128, FD, false, true);
-#pragma unroll 1
+#pragma unroll
                 for (int sl = 0; sl < 4; ++sl) {
                     const uint32_t ah = tmem + TM_E + 32 * (sl >> 1) + 8 * (sl & 1);
                     const uint64_t b = dK + static_cast<uint64_t>((2048u * sl) >> 4);
@@ -482,7 +482,7 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
         };
         auto mma_Oes = [&](int j) {  // O'^T += Es~^T QK~^T: hi*hi + lo*hi + hi*lo
             if (lane == 0) {
-#pragma unroll 1
+#pragma unroll
                 for (int sl = 0; sl < 4; ++sl) {
                     const uint32_t ah = tmem + TM_E + 32 * (sl >> 1) + 8 * (sl & 1);
                     const uint64_t bh_ = smem_desc(tQK_of(j, 0) + 256 * sl, 128, N64_RB);

@@ -76,7 +76,7 @@ __device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem
 // Chain of K/16 MMAs with A in tensor memory (8 columns per K=16 slice).
 __device__ __forceinline__ void mma_chain_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t b_step,
                                                  uint32_t idesc, int K, bool accumulate) {
-#pragma unroll 1
+#pragma unroll
     for (int ks = 0; ks < K / 16; ++ks)
         mma_bf16_tmem_a(d_tmem, a_tmem + 8 * ks, b + static_cast<uint64_t>((b_step * ks) >> 4), idesc,
                         (accumulate || ks > 0) ? 1u : 0u);
@@ -129,7 +129,7 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* mbar) {
 // Chain of K/16 MMAs; a_step/b_step: byte advance of each operand per K=16 slice.
 __device__ __forceinline__ void mma_chain(uint32_t d_tmem, uint64_t a, uint32_t a_step, uint64_t b, uint32_t b_step,
                                           uint32_t idesc, int K, bool accumulate) {
-#pragma unroll 1
+#pragma unroll
     for (int ks = 0; ks < K / 16; ++ks) {
         mma_bf16(d_tmem, a + static_cast<uint64_t>((a_step * ks) >> 4), b + static_cast<uint64_t>((b_step * ks) >> 4),
                  idesc, (accumulate || ks > 0) ? 1u : 0u);
