@@ -65,8 +65,8 @@ constexpr int FD = 128;    // dk = dv
 constexpr int FC = 64;     // tokens per chunk
 constexpr int kGrp = 128;  // threads of each CUDA-core group (one per TMEM lane)
 // Warps 0-3: state chain (group A). Warps 4-7: WY build (group B). Warps 8-11: Y^T tiles and
-// outputs (group C). Warp 12: MMA / copy issuer.
-constexpr int FNT = 3 * kGrp + 32;
+// outputs (group C). Warp 12: MMA issuer. Warp 13: copies of k, q, v into shared memory.
+constexpr int FNT = 3 * kGrp + 64;
 constexpr uint32_t kBarA = 1, kBarB = 2, kBarC = 3;   // named barriers of the groups
 constexpr uint32_t kTmemCols = 512;
 constexpr int kLdL = 68;   // padded row stride (floats) of the fp32 L and M buffers (16-byte rows)
@@ -350,20 +350,14 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
     };
     bool failed = false;
 
-    if (grp == 3) {
-        // ======================= issuer warp: MMAs and copies (lane 0), ragged loads (all lanes) ==========
-        uint32_t kq_pend = 0;   // bit b: a copy into k/q buffer b is in flight
+    if (warp == 13) {
+        // ======================= copy warp: TMA (lane 0) and the ragged last chunk (all lanes) ==========
+        uint32_t kq_pend = 0;   // bit b: a copy into k/q buffer b was issued and not yet seen to land
         bool v_pend = false;
-        auto wait1 = [&](uint64_t* bar, uint32_t parity) -> bool {
-            bool ok = true;
-            if (lane == 0) ok = mbar_wait(bar, parity);
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-            fence_after_sync();
-            return ok;
-        };
         auto ragged_rows = [&](int jj, const __nv_bfloat16* src, uint32_t dst, uint32_t half_stride) {
             const int valid = T - jj * FC;
             const size_t g0 = tok_base + (size_t)jj * FC;
+#pragma unroll 1
             for (int i = lane; i < FC * (FD / 8); i += 32) {
                 const int cb = i & 15, t = i >> 4;   // 16-byte chunk cb of token t, in the swizzled layout
                 uint4 z = make_uint4(0, 0, 0, 0);
@@ -382,19 +376,14 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
                         tma_load_2d(dst + x * SWH, (x & 1) ? &tm_q : &tm_k, 64 * (x >> 1), y, &mbar_kq[b]);
                 }
                 kq_pend |= 1u << b;
-            } else {   // ragged last chunk: plain loads, zero rows past the end
+            } else {   // ragged last chunk: plain loads, zero rows past the end; then a plain arrival
                 ragged_rows(jj, args.k, tKQ_of(jj), KQ_H);
                 ragged_rows(jj, args.q, tKQ_of(jj) + SWH, KQ_H);
                 fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&mbar_kq[b]);
             }
             __syncwarp();
-        };
-        auto wait_kq = [&](int jj) -> bool {
-            if (jj >= nfull) return true;
-            const int b = jj % kKQBuf;
-            const bool ok = wait1(&mbar_kq[b], (jj / kKQBuf) & 1);
-            if (ok) kq_pend &= ~(1u << b);
-            return ok;
         };
         auto load_v = [&](int jj) {
             if (jj < nfull) {
@@ -407,15 +396,58 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
             } else {
                 ragged_rows(jj, args.v, sbase + Ly::T_V, SWH);
                 fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(mbar_v);
             }
             __syncwarp();
         };
-        auto wait_v = [&](int jj) -> bool {
-            if (jj >= nfull) return true;
-            const bool ok = wait1(mbar_v, jj & 1);
-            if (ok) v_pend = false;
+        if (nchunk > 0) {
+            load_kq(0);
+            if (nchunk > 1) load_kq(1);
+            load_v(0);
+        }
+        for (int j = 0; j < nchunk && !failed; ++j) {
+            // k/q of chunk j+2 into the buffer of chunk j-1 once its last product O~(j-1) is done
+            if (j + 2 < nchunk) {
+                bool ok = true;
+                if (lane == 0) {
+                    const long long t0 = clock64();
+                    while (ld_acquire_shared(o_seen) < j)
+                        if (clock64() - t0 > 4000000000LL) { ok = false; break; }
+                }
+                if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) { failed = true; break; }
+                load_kq(j + 2);
+            }
+            // v of chunk j+1 once Z(j) has read v(j)
+            if (j + 1 < nchunk) {
+                bool ok = true;
+                if (lane == 0) ok = mbar_wait(mbar_Z, j & 1);
+                if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) { failed = true; break; }
+                load_v(j + 1);
+            }
+        }
+        if (failed) {
+            if (lane == 0) {
+                atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
+                for (int b = 0; b < kKQBuf; ++b)
+                    if (kq_pend & (1u << b)) { mbar_wait(&mbar_kq[b], 0, 400000000LL); mbar_wait(&mbar_kq[b], 1, 400000000LL); }
+                if (v_pend) { mbar_wait(mbar_v, 0, 400000000LL); mbar_wait(mbar_v, 1, 400000000LL); }
+            }
+            __syncwarp();
+        }
+    } else if (grp == 3) {
+        // ======================= issuer warp: the MMAs (lane 0) =======================
+        auto wait1 = [&](uint64_t* bar, uint32_t parity) -> bool {
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait(bar, parity);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            fence_after_sync();
             return ok;
         };
+        auto wait_kq = [&](int jj) -> bool {   // (the ragged last chunk completes the phase by a plain arrival)
+            return wait1(&mbar_kq[jj % kKQBuf], (jj / kKQBuf) & 1);
+        };
+        auto wait_v = [&](int jj) -> bool { return wait1(mbar_v, jj & 1); };
         const uint32_t idN64 = idesc_bf16(128, FC, false, false);
         // ---- the MMA groups (lane 0 issues, the warp re-converges after each)
         auto mma_D = [&](int jj) {   // D = [K;Q] K^T: rows 0-63 k, 64-127 q of each feature half
@@ -456,11 +488,12 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
         };
         auto mma_O = [&](int j) {    // O'^T = S'^T Q^T with S' = hi + lo (q rows, K-major)
             if (lane == 0) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint64_t dQ = smem_desc_sw128(tKQ_of(j) + SWH + h * KQ_H, 16, 1024);
-                    mma_chain_tmem_a(tmem + TM_O, tmem + TM_SH + 32 * h, dQ, 32, idN64, 64, h > 0);
-                    mma_chain_tmem_a(tmem + TM_O, tmem + TM_SL + 32 * h, dQ, 32, idN64, 64, true);
+                const uint32_t tq = tKQ_of(j) + SWH;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {   // c = 2 * half + (lo ? 1 : 0)
+                    const int h = c >> 1;
+                    const uint64_t dQ = smem_desc_sw128(tq + h * KQ_H, 16, 1024);
+                    mma_chain_tmem_a(tmem + TM_O, tmem + ((c & 1) ? TM_SL : TM_SH) + 32 * h, dQ, 32, idN64, 64, c > 0);
                 }
             }
             __syncwarp();
@@ -482,11 +515,11 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
         };
         auto mma_Oes = [&](int j) {  // O'^T += Es~^T QK~^T: hi*hi + lo*hi + hi*lo
             if (lane == 0) {
+                const uint64_t bh0 = smem_desc(tQK_of(j, 0), 128, N64_RB), bl0 = smem_desc(tQK_of(j, 1), 128, N64_RB);
 #pragma unroll
                 for (int sl = 0; sl < 4; ++sl) {
                     const uint32_t ah = tmem + TM_E + 32 * (sl >> 1) + 8 * (sl & 1);
-                    const uint64_t bh_ = smem_desc(tQK_of(j, 0) + 256 * sl, 128, N64_RB);
-                    const uint64_t bl_ = smem_desc(tQK_of(j, 1) + 256 * sl, 128, N64_RB);
+                    const uint64_t bh_ = bh0 + static_cast<uint64_t>(16 * sl), bl_ = bl0 + static_cast<uint64_t>(16 * sl);
                     mma_bf16_tmem_a(tmem + TM_O, ah, bh_, idN64, 1u);
                     mma_bf16_tmem_a(tmem + TM_O, ah + 16, bh_, idN64, 1u);
                     mma_bf16_tmem_a(tmem + TM_O, ah, bl_, idN64, 1u);
@@ -496,11 +529,6 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
             __syncwarp();
         };
 
-        if (nchunk > 0) {
-            load_kq(0);
-            if (nchunk > 1) load_kq(1);
-            load_v(0);
-        }
         // j = -2, -1: the WY build of chunks 0 and 1 only
         for (int j = -2; j < nchunk && !failed; ++j) {
             const bool next = j + 1 < nchunk;
@@ -508,15 +536,6 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
                 // E(j) once S'(j) and Y^T(j) are in place
                 if (!wait1(rdy_S, j & 1) || !wait1(rdy_Yt, j & 1)) { failed = true; break; }
                 mma_E();
-                // copies: k/q of chunk j+2 (its buffer held chunk j-1), v of chunk j+1 (v(j) was read by Z(j))
-                if (j + 2 < nchunk) {
-                    if (j >= 1 && !wait1(mbar_O, (j - 1) & 1)) { failed = true; break; }
-                    load_kq(j + 2);
-                }
-                if (next) {
-                    if (!wait1(mbar_Z, j & 1)) { failed = true; break; }
-                    load_v(j + 1);
-                }
                 // O(j) while group A forms Es~(j)
                 if (j >= 1 && !wait1(o_free, (j - 1) & 1)) { failed = true; break; }
                 mma_O(j);
@@ -542,9 +561,6 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
                 atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
                 mma_commit(drain);   // tracks every MMA issued so far
                 mbar_wait(drain, 0, 400000000LL);
-                for (int b = 0; b < kKQBuf; ++b)
-                    if (kq_pend & (1u << b)) { mbar_wait(&mbar_kq[b], 0, 400000000LL); mbar_wait(&mbar_kq[b], 1, 400000000LL); }
-                if (v_pend) { mbar_wait(mbar_v, 0, 400000000LL); mbar_wait(mbar_v, 1, 400000000LL); }
             }
             __syncwarp();
         }
