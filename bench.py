@@ -1,8 +1,10 @@
 """Benchmark of the chunkwise DPLR-decay linear-attention forward on GB300.
 
-One step = one whole forward (stage 1 chunk maps + stage 2 state scan, every row
-of the hot path) over one batch of the synthetic workload, inputs resident in
-HBM. Prints ONE JSON line (rank 0).
+One step = one whole forward (every row of the hot path) over one batch of the
+synthetic workload, inputs resident in HBM: the fused per-head kernel for Gated
+DeltaNet with bf16 inputs at d = 128, the two stages (chunk maps, then state scan)
+otherwise. Prints ONE JSON line (rank 0). The default workload is Gated DeltaNet
+B=8 H=16 T=8192 d=128 bf16 (the training-shaped case, T = 8K).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 0..4] [--impl ours|reference]
 
@@ -31,7 +33,7 @@ import numpy as np  # noqa: E402
 
 import workloads  # noqa: E402
 
-DEFAULT_WORKLOAD = 4
+DEFAULT_WORKLOAD = 2
 METRIC = None            # filled from the baseline record's metric string
 L2_BYTES = 129 * 2 ** 20
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -427,8 +429,13 @@ def main():
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seq-len", type=int, default=0,
+                    help="override the workload's T (smaller cases for profiling; not a benchmark line)")
     args = ap.parse_args()
     w = workloads.WORKLOADS[args.workload]
+    if args.seq_len > 0:
+        import dataclasses
+        w = dataclasses.replace(w, T=args.seq_len, name=f"{w.name}_T{args.seq_len}")
     if args.impl == "reference":
         run_reference(args, w)
     else:
