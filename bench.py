@@ -142,6 +142,22 @@ class ClockSampler:
 # Helpers.
 # ----------------------------------------------------------------------------
 
+def slowest_ms(ms, world, device):
+    """The largest per-rank time of a step (all ranks call it; single process: ms itself)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as tdist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank, world, slowest):
+    """Whole-job throughput: every rank processes its own replica of the workload."""
+    return world * tokens_per_rank / (slowest * 1e-3)
+
+
 def smi_id(dev):
     """nvidia-smi --id for a torch device: its UUID when torch exposes it, else the ordinal."""
     import torch
@@ -320,13 +336,9 @@ def run_ours(args, w):
     clocks = sampler.stop()
     k1 = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     k2 = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
-    step_ms = sum(a + b for a, b in zip(k1, k2)) / K
-    if world > 1:
-        t = torch.tensor([step_ms], device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = slowest_ms(sum(a + b for a, b in zip(k1, k2)) / K, world, dev)
     toks = w.B * w.H * w.T
-    value = world * toks / (step_ms * 1e-3)
+    value = job_tokens_per_s(toks, world, step_ms)
     flops = flops_per_token(w) * w.B * w.H * w.T
     sbytes = step_bytes(w)
 
@@ -354,11 +366,7 @@ def run_ours(args, w):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / ke
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = slowest_ms(e0.elapsed_time(e1) / ke, world, dev)
     h2d = in_bytes
     d2h = int(o_host.numel() * 4 + s_host.numel() * 4)
 
@@ -408,7 +416,7 @@ def run_ours(args, w):
             "kernels_ms": {n: ms for n, ms in kern},
             "cpu_baseline": {"value": cpu_v, "unit": "tokens/s", "cores": cpu_cores, "kind": "oracle",
                              "sample": cpu_sample},
-            "e2e": {"value": world * toks / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "e2e": {"value": job_tokens_per_s(toks, world, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": K * f.kernels,
             "clocks": clocks,
