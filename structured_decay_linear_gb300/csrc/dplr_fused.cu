@@ -34,10 +34,10 @@
 //   A  state chain: S' (hi, lo) and e^{G_C} S into tensor memory, then Es~ in place of E;
 //   B  WY build: L and QK~ from D, the triangular inverse, the M tiles;
 //   C  Y^T tiles and the chunk outputs o_t.
-// The issuer queues the MMAs of chunk j in the order E(j), O(j), X(j), O~(j), then the
-// state-independent Y(j+1), Z(j+1) = V^T (-M)^T and D(j+2), so the tensor cores run the
-// chain's products as soon as their operands exist and fill the CUDA-core phases of the
-// chain with the rest. The state S^T (lane n, column c) stays in tensor memory as the
+// The issuer queues the MMAs of chunk j in the order E(j), O(j), X(j), then Y(j+1), D(j+2),
+// O~(j) and Z(j+1) = V^T (-M)^T, so the tensor cores run the chain's products as soon as
+// their operands exist and fill the CUDA-core phases of the chain (Es~ while O runs, S'
+// while the rest runs) with the others. The state S^T (lane n, column c) stays in tensor memory as the
 // accumulator of X for the whole sequence.
 //
 // Operand tiles. q, k and v arrive by TMA tensor copies of 64 tokens x 64 features
@@ -447,7 +447,6 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
         auto wait_kq = [&](int jj) -> bool {   // (the ragged last chunk completes the phase by a plain arrival)
             return wait1(&mbar_kq[jj % kKQBuf], (jj / kKQBuf) & 1);
         };
-        auto wait_v = [&](int jj) -> bool { return wait1(mbar_v, jj & 1); };
         const uint32_t idN64 = idesc_bf16(128, FC, false, false);
         // ---- the MMA groups (lane 0 issues, the warp re-converges after each)
         auto mma_D = [&](int jj) {   // D = [K;Q] K^T: rows 0-63 k, 64-127 q of each feature half
@@ -542,18 +541,22 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
                 // X(j): the state update
                 if (!wait1(rdy_E, j & 1)) { failed = true; break; }
                 mma_X(j);
-                mma_Oes(j);
             }
-            // state-independent products of the next chunks
+            // while group A rebuilds S' from X(j): Y(j+1) first (its Y^T tile gates E(j+1)), D(j+2)
+            // (its D accumulator was read with the M(j+1) build), then O~(j) and Z(j+1) (which reuses
+            // the E accumulator that O~(j) reads)
             if (j >= -1 && next) {
                 if (!wait1(rdy_M, (j + 1) & 1)) { failed = true; break; }
                 mma_Y(j + 1);
-                if (!wait_v(j + 1)) { failed = true; break; }
-                mma_Z();
             }
             if (j + 2 < nchunk) {
                 if (!wait_kq(j + 2)) { failed = true; break; }
                 mma_D(j + 2);
+            }
+            if (j >= 0) mma_Oes(j);
+            if (j >= -1 && next) {
+                if (!wait1(mbar_v, (j + 1) & 1)) { failed = true; break; }
+                mma_Z();
             }
         }
         if (failed) {
