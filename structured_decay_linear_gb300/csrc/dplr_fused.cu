@@ -92,7 +92,7 @@ struct GdnLayout {
     static constexpr int VEC = SCR + 32 * 36 * 4;          // per group, 2 buffers of 256 floats
     static constexpr int kVec = 1024;
     static constexpr int BAR = VEC + 6 * kVec;              // mbarriers, TMEM address, counter
-    static constexpr int TOTAL = BAR + 160;
+    static constexpr int TOTAL = BAR + 160;   // 18 mbarriers, TMEM address, two counters
 };
 static_assert(GdnLayout::TOTAL <= 227 * 1024, "shared memory budget");
 static_assert(GdnLayout::T_V % 1024 == 0 && KQ_BYTES % 1024 == 0, "swizzled tiles are 1024-byte aligned");
@@ -287,22 +287,24 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
     // MMA completions (issuer -> groups)
     uint64_t* mbar_D = bars + 0;     // D(j)                              -> B
     uint64_t* mbar_Y = bars + 1;     // Y(j)                              -> C
-    uint64_t* mbar_Z = bars + 2;     // Z(j) (and everything before)      -> B, issuer
-    uint64_t* mbar_E = bars + 3;     // E(j)                              -> A, C
-    uint64_t* mbar_X = bars + 4;     // X(j), O(j)                        -> A
-    uint64_t* mbar_O = bars + 5;     // O~(j), the last product of chunk j -> C, issuer
+    uint64_t* mbar_Z = bars + 2;     // Z(j) (and the issuer's MMAs before) -> A, B, copy warp
+    uint64_t* mbar_E = bars + 3;     // E(j), issued by A                 -> A, C
+    uint64_t* mbar_X = bars + 4;     // E(j), X(j), issued by A           -> A, issuer
+    uint64_t* mbar_O = bars + 5;     // O~(j), the issuer's last product of chunk j -> C
     // bulk copies
     uint64_t* mbar_kq = bars + 6;    // [kKQBuf]
     uint64_t* mbar_v = bars + 9;
     // groups -> issuer
-    uint64_t* rdy_S = bars + 10;     // A: S'(j) in TMEM, e^{G_C} S in the accumulator
-    uint64_t* rdy_E = bars + 11;     // A: Es~(j) in TMEM
+    uint64_t* rdy_S = bars + 10;     // A: S'(j) in TMEM (for O(j))
+    uint64_t* rdy_E = bars + 11;     // A: Es~(j) in TMEM (for O~(j))
     uint64_t* rdy_M = bars + 12;     // B: M(j) tiles (and D(j) consumed)
     uint64_t* rdy_Yt = bars + 13;    // C: Y^T(j) tile (and Y(j) consumed)
     uint64_t* o_free = bars + 14;    // C: O(j) consumed
-    uint64_t* drain = bars + 15;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 16);
-    int* o_seen = reinterpret_cast<int*>(bars + 17);    // C: chunks whose last product has completed
+    uint64_t* drain = bars + 15;     // [2]: the issuer's and group A's MMAs
+    uint64_t* mbar_O1 = bars + 17;   // O(j) = S'^T Q^T, issued by the issuer -> A
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 18);
+    int* o_seen = reinterpret_cast<int*>(bars + 19);    // C: chunks whose O~ has completed
+    int* x_seen = reinterpret_cast<int*>(bars + 19) + 1;   // A: chunks whose X has completed
     float* scr = reinterpret_cast<float*>(smem + Ly::SCR);
     float* F_L = reinterpret_cast<float*>(smem + Ly::F_L);
     float* F_M = reinterpret_cast<float*>(smem + Ly::F_M);
@@ -319,8 +321,9 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
 
     if (tid == 0) {
-        for (int i = 0; i < 16; ++i) mbar_init(bars + i, 1);
+        for (int i = 0; i < 18; ++i) mbar_init(bars + i, 1);
         *o_seen = 0;
+        *x_seen = 0;
         mbar_fence_init();
     }
     if (warp == 0) tmem_alloc(tmem_holder, kTmemCols);
@@ -407,12 +410,13 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
             load_v(0);
         }
         for (int j = 0; j < nchunk && !failed; ++j) {
-            // k/q of chunk j+2 into the buffer of chunk j-1 once its last product O~(j-1) is done
+            // k/q of chunk j+2 into the buffer of chunk j-1 once the products that read it, O~(j-1)
+            // (issuer) and X(j-1) (group A), are done
             if (j + 2 < nchunk) {
                 bool ok = true;
                 if (lane == 0) {
                     const long long t0 = clock64();
-                    while (ld_acquire_shared(o_seen) < j)
+                    while (ld_acquire_shared(o_seen) < j || ld_acquire_shared(x_seen) < j)
                         if (clock64() - t0 > 4000000000LL) { ok = false; break; }
                 }
                 if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) { failed = true; break; }
@@ -477,14 +481,6 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
             }
             __syncwarp();
         };
-        auto mma_E = [&]() {         // E^T += S'^T Y^T
-            if (lane == 0) {
-                mma_chain_tmem_a(tmem + TM_E, tmem + TM_SH, smem_desc(sbase + Ly::T_YT, N64_RB, 128), 2 * N64_RB,
-                                 idesc_bf16(128, FC, false, true), FD, true);
-                mma_commit(mbar_E);
-            }
-            __syncwarp();
-        };
         auto mma_O = [&](int j) {    // O'^T = S'^T Q^T with S' = hi + lo (q rows, K-major)
             if (lane == 0) {
                 const uint32_t tq = tKQ_of(j) + SWH;
@@ -494,21 +490,7 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
                     const uint64_t dQ = smem_desc_sw128(tq + h * KQ_H, 16, 1024);
                     mma_chain_tmem_a(tmem + TM_O, tmem + ((c & 1) ? TM_SL : TM_SH) + 32 * h, dQ, 32, idN64, 64, c > 0);
                 }
-            }
-            __syncwarp();
-        };
-        auto mma_X = [&](int j) {    // S^T += Es~^T K (hi + lo); Es~ hi at 32*(s/2) + 8*(s%2), lo 16 further
-            if (lane == 0) {
-                const uint64_t dK = smem_desc_sw128(tKQ_of(j), KQ_H, 1024);   // k rows, MN-major B (K = rho)
-                const uint32_t idX = idesc_bf16(128, FD, false, true);
-#pragma unroll
-                for (int sl = 0; sl < 4; ++sl) {
-                    const uint32_t ah = tmem + TM_E + 32 * (sl >> 1) + 8 * (sl & 1);
-                    const uint64_t b = dK + static_cast<uint64_t>((2048u * sl) >> 4);
-                    mma_bf16_tmem_a(tmem + TM_S, ah, b, idX, 1u);
-                    mma_bf16_tmem_a(tmem + TM_S, ah + 16, b, idX, 1u);
-                }
-                mma_commit(mbar_X);
+                mma_commit(mbar_O1);
             }
             __syncwarp();
         };
@@ -528,23 +510,17 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
             __syncwarp();
         };
 
-        // j = -2, -1: the WY build of chunks 0 and 1 only
+        // j = -2, -1: the WY build of chunks 0 and 1 only. E(j) and X(j) are issued by group A.
         for (int j = -2; j < nchunk && !failed; ++j) {
             const bool next = j + 1 < nchunk;
             if (j >= 0) {
-                // E(j) once S'(j) and Y^T(j) are in place
-                if (!wait1(rdy_S, j & 1) || !wait1(rdy_Yt, j & 1)) { failed = true; break; }
-                mma_E();
-                // O(j) while group A forms Es~(j)
+                // O(j) once S'(j) is in place and the outputs of chunk j-1 have been read
+                if (!wait1(rdy_S, j & 1)) { failed = true; break; }
                 if (j >= 1 && !wait1(o_free, (j - 1) & 1)) { failed = true; break; }
                 mma_O(j);
-                // X(j): the state update
-                if (!wait1(rdy_E, j & 1)) { failed = true; break; }
-                mma_X(j);
             }
-            // while group A rebuilds S' from X(j): Y(j+1) first (its Y^T tile gates E(j+1)), D(j+2)
-            // (its D accumulator was read with the M(j+1) build), then O~(j) and Z(j+1) (which reuses
-            // the E accumulator that O~(j) reads)
+            // Y(j+1) (its Y^T tile gates E(j+1)) and D(j+2) (its D accumulator was read with the
+            // M(j+1) build)
             if (j >= -1 && next) {
                 if (!wait1(rdy_M, (j + 1) & 1)) { failed = true; break; }
                 mma_Y(j + 1);
@@ -553,16 +529,21 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
                 if (!wait_kq(j + 2)) { failed = true; break; }
                 mma_D(j + 2);
             }
-            if (j >= 0) mma_Oes(j);
+            // O~(j) once Es~(j) is in place (after O(j), in this thread's order)
+            if (j >= 0) {
+                if (!wait1(rdy_E, j & 1)) { failed = true; break; }
+                mma_Oes(j);
+            }
+            // Z(j+1) reuses the E accumulator: after O~(j) (this thread) and X(j) (group A)
             if (j >= -1 && next) {
-                if (!wait1(mbar_v, (j + 1) & 1)) { failed = true; break; }
+                if ((j >= 0 && !wait1(mbar_X, j & 1)) || !wait1(mbar_v, (j + 1) & 1)) { failed = true; break; }
                 mma_Z();
             }
         }
         if (failed) {
             if (lane == 0) {
                 atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
-                mma_commit(drain);   // tracks every MMA issued so far
+                mma_commit(drain);   // tracks every MMA this thread issued
                 mbar_wait(drain, 0, 400000000LL);
             }
             __syncwarp();
@@ -596,9 +577,19 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
             tmem_wait_st();
         }
         named_sync(kBarA, kGrp);
+        // The leader thread issues this group's own MMAs, E(j) and X(j), straight after the group
+        // barrier that publishes their tensor-memory operand: no hand-off to another warp on the chain.
+        const uint32_t idE = idesc_bf16(128, FC, false, true), idX = idesc_bf16(128, FD, false, true);
+        const uint64_t dYt = smem_desc(sbase + Ly::T_YT, N64_RB, 128);
         for (int j = 0; j < nchunk && !failed; ++j) {
             const float* vf = vec(0, j & 1);
-            if (j > 0 && !group_wait(mbar_X, (j - 1) & 1, kBarA)) { failed = true; break; }
+            if (j > 0) {   // S_{j-1} complete (X(j-1)); S'(j-1) read by E(j-1) and O(j-1)
+                if (!group_wait(mbar_X, (j - 1) & 1, kBarA) || !group_wait(mbar_O1, (j - 1) & 1, kBarA)) {
+                    failed = true;
+                    break;
+                }
+                if (gt == 0) st_release_shared(x_seen, j);
+            }
             {   // ---- S'^T (hi, lo) and gamma S^T
                 const float ea = vf[0], gam = vf[1];
 #pragma unroll 1
@@ -619,7 +610,15 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
             }
             fence_before_sync();
             named_sync(kBarA, kGrp);
-            if (gt == 0) mbar_arrive(rdy_S);
+            if (gt == 0) {
+                mbar_arrive(rdy_S);
+                // E(j) += S'^T Y^T onto Z(j) (issuer), once Z(j) is done and Y^T(j) is in place
+                if (mbar_wait(mbar_Z, j & 1) && mbar_wait(rdy_Yt, j & 1)) {
+                    fence_after_sync();
+                    mma_chain_tmem_a(tmem + TM_E, tmem + TM_SH, dYt, 2 * N64_RB, idE, FD, true);
+                    mma_commit(mbar_E);
+                }
+            }
             // ---- Es~^T of chunk j, in place of E^T
             if (!group_wait(mbar_E, j & 1, kBarA)) { failed = true; break; }
 #pragma unroll 1
@@ -635,9 +634,23 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
             }
             tmem_wait_st();
             fence_before_sync();
-            if (j + 1 < nchunk) gates(j + 1);
             named_sync(kBarA, kGrp);
-            if (gt == 0) mbar_arrive(rdy_E);
+            if (gt == 0) {
+                // X(j): S^T += Es~^T K (hi + lo); Es~ hi at 32*(s/2) + 8*(s%2), lo 16 columns further
+                fence_after_sync();
+                const uint64_t dK = smem_desc_sw128(tKQ_of(j), KQ_H, 1024);   // k rows, MN-major B (K = rho)
+#pragma unroll
+                for (int sl = 0; sl < 4; ++sl) {
+                    const uint32_t ah = tmem + TM_E + 32 * (sl >> 1) + 8 * (sl & 1);
+                    const uint64_t b = dK + static_cast<uint64_t>((2048u * sl) >> 4);
+                    mma_bf16_tmem_a(tmem + TM_S, ah, b, idX, 1u);
+                    mma_bf16_tmem_a(tmem + TM_S, ah + 16, b, idX, 1u);
+                }
+                mma_commit(mbar_X);
+                mbar_arrive(rdy_E);
+            }
+            if (j + 1 < nchunk) gates(j + 1);
+            named_sync(kBarA, kGrp);   // gates of chunk j + 1 visible to the group
         }
         if (!failed) {   // final state
             if (nchunk > 0 && !group_wait(mbar_X, (nchunk - 1) & 1, kBarA)) failed = true;
@@ -657,7 +670,11 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
                 }
             }
         }
-        if (failed && gt == 0) atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
+        if (failed && gt == 0) {
+            atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
+            mma_commit(drain + 1);   // tracks every MMA this thread issued
+            mbar_wait(drain + 1, 0, 400000000LL);
+        }
     } else if (grp == 1) {
         // ======================= group B: the WY build of each chunk =======================
         float graw[4];
