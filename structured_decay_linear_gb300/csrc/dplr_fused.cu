@@ -65,7 +65,8 @@ constexpr int FD = 128;    // dk = dv
 constexpr int FC = 64;     // tokens per chunk
 constexpr int kGrp = 128;  // threads of each CUDA-core group (one per TMEM lane)
 // Warps 0-3: state chain (group A). Warps 4-7: WY build (group B). Warps 8-11: Y^T tiles and
-// outputs (group C). Warp 12: MMA issuer. Warp 13: copies of k, q, v into shared memory.
+// outputs (group C). Warp 12: copies of k, q, v into shared memory. Warp 13: MMA issuer
+// (on another scheduler than the copy warp).
 constexpr int FNT = 3 * kGrp + 64;
 constexpr uint32_t kBarA = 1, kBarB = 2, kBarC = 3;   // named barriers of the groups
 constexpr uint32_t kTmemCols = 512;
@@ -92,7 +93,7 @@ struct GdnLayout {
     static constexpr int VEC = SCR + 32 * 36 * 4;          // per group, 2 buffers of 256 floats
     static constexpr int kVec = 1024;
     static constexpr int BAR = VEC + 6 * kVec;              // mbarriers, TMEM address, counter
-    static constexpr int TOTAL = BAR + 160;   // 18 mbarriers, TMEM address, two counters
+    static constexpr int TOTAL = BAR + 176;   // 19 mbarriers, TMEM address, two counters
 };
 static_assert(GdnLayout::TOTAL <= 227 * 1024, "shared memory budget");
 static_assert(GdnLayout::T_V % 1024 == 0 && KQ_BYTES % 1024 == 0, "swizzled tiles are 1024-byte aligned");
@@ -297,14 +298,15 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
     // groups -> issuer
     uint64_t* rdy_S = bars + 10;     // A: S'(j) in TMEM (for O(j))
     uint64_t* rdy_E = bars + 11;     // A: Es~(j) in TMEM (for O~(j))
-    uint64_t* rdy_M = bars + 12;     // B: M(j) tiles (and D(j) consumed)
+    uint64_t* rdy_M = bars + 12;     // B: M(j) tiles
     uint64_t* rdy_Yt = bars + 13;    // C: Y^T(j) tile (and Y(j) consumed)
     uint64_t* o_free = bars + 14;    // C: O(j) consumed
     uint64_t* drain = bars + 15;     // [2]: the issuer's and group A's MMAs
     uint64_t* mbar_O1 = bars + 17;   // O(j) = S'^T Q^T, issued by the issuer -> A
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 18);
-    int* o_seen = reinterpret_cast<int*>(bars + 19);    // C: chunks whose O~ has completed
-    int* x_seen = reinterpret_cast<int*>(bars + 19) + 1;   // A: chunks whose X has completed
+    uint64_t* d_free = bars + 18;    // B: D(j) read (its accumulator may take D(j+1))
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 19);
+    int* o_seen = reinterpret_cast<int*>(bars + 20);    // C: chunks whose O~ has completed
+    int* x_seen = reinterpret_cast<int*>(bars + 20) + 1;   // A: chunks whose X has completed
     float* scr = reinterpret_cast<float*>(smem + Ly::SCR);
     float* F_L = reinterpret_cast<float*>(smem + Ly::F_L);
     float* F_M = reinterpret_cast<float*>(smem + Ly::F_M);
@@ -321,7 +323,7 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
 
     if (tid == 0) {
-        for (int i = 0; i < 18; ++i) mbar_init(bars + i, 1);
+        for (int i = 0; i < 19; ++i) mbar_init(bars + i, 1);
         *o_seen = 0;
         *x_seen = 0;
         mbar_fence_init();
@@ -353,7 +355,7 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
     };
     bool failed = false;
 
-    if (warp == 13) {
+    if (warp == 12) {
         // ======================= copy warp: TMA (lane 0) and the ragged last chunk (all lanes) ==========
         uint32_t kq_pend = 0;   // bit b: a copy into k/q buffer b was issued and not yet seen to land
         bool v_pend = false;
@@ -416,8 +418,10 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
                 bool ok = true;
                 if (lane == 0) {
                     const long long t0 = clock64();
-                    while (ld_acquire_shared(o_seen) < j || ld_acquire_shared(x_seen) < j)
+                    while (ld_acquire_shared(o_seen) < j || ld_acquire_shared(x_seen) < j) {
                         if (clock64() - t0 > 4000000000LL) { ok = false; break; }
+                        __nanosleep(100);
+                    }
                 }
                 if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) { failed = true; break; }
                 load_kq(j + 2);
@@ -439,7 +443,7 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
             }
             __syncwarp();
         }
-    } else if (grp == 3) {
+    } else if (warp == 13) {
         // ======================= issuer warp: the MMAs (lane 0) =======================
         auto wait1 = [&](uint64_t* bar, uint32_t parity) -> bool {
             bool ok = true;
@@ -519,15 +523,15 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
                 if (j >= 1 && !wait1(o_free, (j - 1) & 1)) { failed = true; break; }
                 mma_O(j);
             }
-            // Y(j+1) (its Y^T tile gates E(j+1)) and D(j+2) (its D accumulator was read with the
-            // M(j+1) build)
+            // D(j+2) as soon as group B has read D(j+1) out of the accumulator
+            if (j + 2 < nchunk) {
+                if ((j >= -1 && !wait1(d_free, (j + 1) & 1)) || !wait_kq(j + 2)) { failed = true; break; }
+                mma_D(j + 2);
+            }
+            // Y(j+1): its Y^T tile gates E(j+1)
             if (j >= -1 && next) {
                 if (!wait1(rdy_M, (j + 1) & 1)) { failed = true; break; }
                 mma_Y(j + 1);
-            }
-            if (j + 2 < nchunk) {
-                if (!wait_kq(j + 2)) { failed = true; break; }
-                mma_D(j + 2);
             }
             // O~(j) once Es~(j) is in place (after O(j), in this thread's order)
             if (j >= 0) {
@@ -696,8 +700,10 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
                 bool ok = true;
                 if (gt == 0) {
                     const long long t0 = clock64();
-                    while (ld_acquire_shared(o_seen) < jj - 1)
+                    while (ld_acquire_shared(o_seen) < jj - 1) {
                         if (clock64() - t0 > 4000000000LL) { ok = false; break; }
+                        __nanosleep(100);
+                    }
                 }
                 if (named_sync_or(kBarB, kGrp, !ok)) { failed = true; break; }
             }
@@ -731,6 +737,8 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
                 }
             }
             fence_before_sync();
+            named_sync(kBarB, kGrp);
+            if (gt == 0) mbar_arrive(d_free);   // every thread's tcgen05.ld of D(jj) has completed
             if (jj >= 1 && !group_wait(mbar_Z, (jj - 1) & 1, kBarB)) { failed = true; break; }   // M tiles free
             unit_lower_inverse64(F_L, F_M, scr, sbase + Ly::T_MN, sbase + Ly::T_MY, vf, gt);
             fence_async_smem();

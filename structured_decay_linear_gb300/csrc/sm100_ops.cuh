@@ -196,15 +196,17 @@ __device__ __forceinline__ void st_release_shared(int* p, int v) {
 }
 
 // Bounded wait for the phase with the given parity. Returns false if it gave up
-// (after roughly `max_cycles` SM cycles).
+// (after roughly `max_cycles` SM cycles). Each try_wait may suspend the thread until the
+// phase completes (at most ~0.1 ms per attempt), so a waiting thread takes no issue slots
+// from the warps that share its scheduler.
 __device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity, long long max_cycles = 4000000000LL) {
     const uint32_t a = smem_addr(mbar);
     const long long t0 = clock64();
     for (;;) {
         uint32_t done;
         asm volatile(
-            "{\n\t.reg .pred q;\n\tmbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-            : "=r"(done) : "r"(a), "r"(parity) : "memory");
+            "{\n\t.reg .pred q;\n\tmbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+            : "=r"(done) : "r"(a), "r"(parity), "r"(100000u) : "memory");
         if (done) return true;
         if (clock64() - t0 > max_cycles) return false;
     }
