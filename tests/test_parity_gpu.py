@@ -207,6 +207,25 @@ def test_stage_calls_match_forward_and_are_deterministic(sdl):
     assert fwd.device_status() == 0
 
 
+@pytest.mark.parametrize("B,H,T", [(1, 2, 1), (1, 2, 63), (1, 2, 64), (1, 2, 65), (2, 3, 191), (1, 1, 1024)])
+def test_fused_kernel_edges(sdl, B, H, T):
+    """The fused GDN kernel on sequences shorter than a chunk, exactly one chunk, one past it,
+    several heads with a ragged tail, and a longer run (S0 nonzero throughout)."""
+    w = W("gdn", "bf16", 128, 128, s0=True)
+    assert sdl.dplr_la_kernel_count(sdl.make_desc("gdn", "bf16", B, H, T, 128, 128)) == 1
+    inp = workloads.generate(w, heads=[(b, h) for b in range(B) for h in range(H)], T=T)
+    o, ST = run_gpu(sdl, inp)
+    check(inp, o, ST)
+
+
+def test_fused_kernel_empty_sequence(sdl):
+    w = W("gdn", "bf16", 128, 128, s0=True)
+    inp = workloads.generate(w, heads=[(0, 0), (0, 1)], T=0)
+    o, ST = run_gpu(sdl, inp)
+    assert o.shape == (1, 2, 0, 128)
+    assert np.array_equal(ST, inp["S0"].astype(np.float64))
+
+
 def test_fused_path_selection(sdl):
     """GDN with bf16 inputs at d=128 runs one fused kernel with a status-word workspace; others two stages."""
     d = sdl.make_desc("gdn", "bf16", 8, 16, 8192, 128, 128)

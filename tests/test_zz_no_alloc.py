@@ -62,8 +62,10 @@ def test_noalloc_matches_forward_on_two_calls_in_a_row(sdl):
     cases = [
         workloads.Workload(98, "hdla_noalloc", "hdla", "bf16", 1, 1, 0, 128, 128, 2, 1, 64, True),
         workloads.Workload(97, "gdn_noalloc", "gdn", "f32", 1, 1, 0, 64, 32, 1, 1, 64, True),
+        # GDN bf16 d=128 runs the fused kernel: its scratch is the status word
+        workloads.Workload(96, "gdn_fused_noalloc", "gdn", "bf16", 1, 1, 0, 128, 128, 1, 1, 64, True),
     ]
-    for w, heads, T in ((cases[0], 3, 300), (cases[1], 2, 130)):
+    for w, heads, T in ((cases[0], 3, 300), (cases[1], 2, 130), (cases[2], 3, 257)):
         inp, dt, args = _case(w, heads, T)
         ref = sdl.Forward(w.mode, dt, 1, heads, T, w.dk, w.dv)
         o_ref, S_ref = [x.clone() for x in ref(**args)]
