@@ -168,6 +168,36 @@ DPLR_API dplr_status dplr_la_forward_noalloc(const dplr_desc* desc,
                                     const void* A, const void* Bm, const void* K, const void* V,
                                     const float* S0, float* o, float* S_T, void* stream);
 
+/* Bytes of device staging area dplr_la_forward_host needs for `desc` split into
+ * `groups` groups of heads with `slots` staging slots (1 <= slots <= 8); 0 if the
+ * descriptor is invalid, B*H is not a multiple of `groups` or `slots` is out of range. */
+DPLR_API size_t dplr_la_host_workspace_size(const dplr_desc* desc, int groups, int slots);
+
+/* The whole forward with HOST inputs and outputs (no counterpart in the paper: the
+ * transfers a caller would otherwise make around dplr_la_forward, overlapped with it).
+ * q .. S0 are host pointers in the layouts above (S0 may be NULL), o and S_T host
+ * outputs (S_T may be NULL); pinned host memory gives full transfer bandwidth, other host
+ * memory works but the copies then do not overlap. The B*H heads are split into `groups`
+ * equal groups (B*H must be a multiple of it); each group is copied into one of `slots`
+ * staging slots in `staging` (device memory, 256-byte aligned, at least
+ * dplr_la_host_workspace_size bytes, owned by the caller), computed there with
+ * dplr_la_forward, and copied back, so copies in, forwards and copies out of different
+ * groups overlap. The work starts after the work already queued on `stream` and `stream`
+ * waits for all of it (synchronise `stream` before reading o and S_T); the host buffers
+ * must stay valid until then. The library keeps, per device, two copy streams, 8 compute
+ * streams and their events, created on the first call made while that device is current;
+ * calls on one device run in call order. Allocates no device memory. Errors: as
+ * dplr_la_forward, plus DPLR_ERR_INVALID_ARG for a bad group or slot count and
+ * DPLR_ERR_WORKSPACE for a missing, misaligned or small staging area; a CUDA error after
+ * some groups were queued returns DPLR_ERR_CUDA. */
+DPLR_API dplr_status dplr_la_forward_host(const dplr_desc* desc,
+                                 const void* q, const void* k, const void* v,
+                                 const float* decay, const float* beta,
+                                 const void* A, const void* Bm, const void* K, const void* V,
+                                 const float* S0, float* o, float* S_T,
+                                 void* staging, size_t staging_bytes, int groups, int slots,
+                                 void* stream);
+
 #ifdef __cplusplus
 }
 #endif

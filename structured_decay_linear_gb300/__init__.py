@@ -2,12 +2,15 @@
 as hand-written CUDA for GB300 (sm_103a) behind the C ABI of libdplr (include/dplr.h).
 
 ``forward`` / ``Forward`` marshal torch device tensors into ``dplr_la_forward``;
-the C-ABI mirrors (``dplr_la_forward``, ``dplr_la_chunk_maps``, ...) take raw
-pointers. There is no CPU fallback: without libdplr.so the calls raise.
+``ForwardHost`` marshals host tensors into ``dplr_la_forward_host`` (transfers
+overlapped with the kernels); the C-ABI mirrors (``dplr_la_forward``,
+``dplr_la_chunk_maps``, ...) take raw pointers. There is no CPU fallback: without
+libdplr.so the calls raise.
 """
 
 from .dplr import (  # noqa: F401
-    DPLR_BF16, DPLR_F32, DPLR_GDN, DPLR_GENERIC, DPLR_HDLA, DPLR_OK, DplrError, Forward, LIB_PATH,
-    dplr_desc, dplr_la_check, dplr_la_chunk_maps, dplr_la_forward, dplr_la_forward_noalloc, dplr_la_kernel_count, dplr_la_stage_workspace_size,
+    DPLR_BF16, DPLR_F32, DPLR_GDN, DPLR_GENERIC, DPLR_HDLA, DPLR_OK, DplrError, Forward, ForwardHost, LIB_PATH,
+    default_groups, dplr_desc, dplr_la_check, dplr_la_chunk_maps, dplr_la_forward, dplr_la_forward_host,
+    dplr_la_forward_noalloc, dplr_la_host_workspace_size, dplr_la_kernel_count, dplr_la_stage_workspace_size,
     dplr_la_state_scan, dplr_la_workspace_size, forward, library, make_desc, status_string,
 )

@@ -31,7 +31,8 @@ def _sources():
 
 
 def _deps():
-    return _sources() + sorted(glob.glob(os.path.join(CSRC, "*.h"))) + [os.path.join(INCLUDE, "dplr.h")]
+    return (_sources() + sorted(glob.glob(os.path.join(CSRC, "*.h"))) + sorted(glob.glob(os.path.join(CSRC, "*.cuh")))
+            + [os.path.join(INCLUDE, "dplr.h")])
 
 
 def up_to_date() -> bool:

@@ -166,3 +166,32 @@ def test_fused_path_workspace_is_a_status_word(sdl):
 def test_kernel_count(sdl):
     assert sdl.dplr_la_kernel_count(sdl.make_desc("gdn", "f32", 1, 1, 64, 32, 32)) >= 1
     assert sdl.dplr_la_kernel_count(sdl.make_desc("gdn", "f32", 1, 1, 64, 48, 32)) == 0
+
+
+def test_host_workspace_size_validates_groups_and_slots(sdl):
+    d = sdl.make_desc("gdn", "bf16", 2, 8, 256, 128, 128)
+    assert sdl.dplr_la_host_workspace_size(d, 4, 2) > 0
+    assert sdl.dplr_la_host_workspace_size(d, 3, 2) == 0      # 16 heads are not a multiple of 3
+    assert sdl.dplr_la_host_workspace_size(d, 0, 2) == 0
+    assert sdl.dplr_la_host_workspace_size(d, 4, 0) == 0
+    assert sdl.dplr_la_host_workspace_size(d, 4, 9) == 0
+    # one slot per group at most: more slots than groups cost no more
+    assert sdl.dplr_la_host_workspace_size(d, 2, 8) == sdl.dplr_la_host_workspace_size(d, 2, 2)
+    # slots scale the size linearly
+    assert sdl.dplr_la_host_workspace_size(d, 4, 2) == 2 * sdl.dplr_la_host_workspace_size(d, 4, 1)
+
+
+def test_forward_host_rejects_bad_arguments_before_launch(sdl):
+    d = sdl.make_desc("gdn", "bf16", 1, 4, 128, 128, 128)
+    need = sdl.dplr_la_host_workspace_size(d, 2, 2)
+    fake = 1 << 20      # never dereferenced: every check below comes first
+    args = [fake] * 5 + [None] * 4 + [None, fake, None]
+    call = lambda staging, nbytes, groups, slots, a=args: sdl.dplr_la_forward_host(d, *a, staging, nbytes, groups,
+                                                                                    slots, None)
+    assert call(fake, need, 3, 2) == sdl.dplr.DPLR_ERR_INVALID_ARG        # groups does not divide B*H
+    assert call(fake, need, 2, 0) == sdl.dplr.DPLR_ERR_INVALID_ARG        # no slot
+    assert call(fake, 4096, 2, 2) == sdl.dplr.DPLR_ERR_WORKSPACE          # staging too small
+    assert call(fake + 16, need, 2, 2) == sdl.dplr.DPLR_ERR_WORKSPACE     # staging misaligned
+    assert call(None, need, 2, 2) == sdl.dplr.DPLR_ERR_WORKSPACE
+    no_k = [fake, None] + [fake] * 3 + [None] * 4 + [None, fake, None]
+    assert call(fake, need, 2, 2, no_k) == sdl.dplr.DPLR_ERR_INVALID_ARG  # k missing

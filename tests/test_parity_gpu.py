@@ -259,3 +259,32 @@ def test_full_size_workload_sampled_heads(sdl, wid):
         es = rel_err(ST[b, h], S_ref[0, i])
         assert eo <= tau, f"workload {wid} head {(b, h)}: o err {eo:.3e}"
         assert es <= tau, f"workload {wid} head {(b, h)}: S_T err {es:.3e}"
+
+
+@pytest.mark.parametrize("mode,groups,slots,s0", [("gdn", 4, 2, True), ("gdn", 8, 8, False), ("hdla", 2, 1, True)])
+def test_forward_host_matches_device_forward(sdl, mode, groups, slots, s0):
+    """dplr_la_forward_host (host buffers, heads split into groups through a ring of staging
+    slots) gives the same bits as dplr_la_forward on device buffers, on two calls in a row."""
+    import torch
+    w = W(mode, "bf16", 128, 128, s0=s0)
+    B, H, T = 2, 4, 200
+    inp = workloads.generate(w, heads=[(b, h) for b in range(B) for h in range(H)], T=T)
+    host = {}
+    for key in ("q", "k", "v", "decay", "beta", "S0"):
+        x = inp[key]
+        if x is None:
+            host[key] = None
+            continue
+        x = np.ascontiguousarray(x).reshape((B, H) + x.shape[2:])
+        t = torch.from_numpy(x)
+        host[key] = (t.to(torch.bfloat16) if key in ("q", "k", "v") else t).pin_memory()
+    dev = {k_: (None if t is None else t.to("cuda")) for k_, t in host.items()}
+    ref = sdl.Forward(mode, torch.bfloat16, B, H, T, 128, 128)
+    o_ref, S_ref = [x.clone() for x in ref(**dev)]
+    fh = sdl.ForwardHost(mode, torch.bfloat16, B, H, T, 128, 128, groups=groups, slots=slots)
+    for _ in range(2):
+        fh.o.fill_(float("nan"))
+        fh.S_T.fill_(float("nan"))
+        o, S = fh(**host)
+        torch.cuda.current_stream().synchronize()
+        assert torch.equal(o, o_ref.cpu()) and torch.equal(S, S_ref.cpu())
