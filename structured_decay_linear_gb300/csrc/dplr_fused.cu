@@ -127,6 +127,26 @@ __device__ __forceinline__ void rbm_store8(uint32_t tile, int cols, int r, int c
                  pack_bf16(x[6], x[7]));
 }
 
+// Forms predicated by `issue`: a warp issues MMAs from one lane without diverging, so that it
+// does not have to re-converge afterwards (which costs hundreds of cycles after MMAs).
+__device__ __forceinline__ void mma_tmem_a_if(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc,
+                                              uint32_t issue) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        :: "r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc), "r"(issue));
+}
+__device__ __forceinline__ void mma_commit_if(uint64_t* mbar, uint32_t issue) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
+        "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
+        :: "r"(smem_addr(mbar)), "r"(issue) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_if(uint64_t* mbar, uint32_t issue) {
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t@q mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}"
+                 :: "r"(smem_addr(mbar)), "r"(issue) : "memory");
+}
+
 // x = hi + lo with both parts bf16: packed pairs (element 2i in the low half).
 __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& h, uint32_t& l) {
     h = pack_bf16(x0, x1);
@@ -348,7 +368,7 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
     // not take issue slots from the warps that work (the issuer above all).
     auto group_wait = [&](uint64_t* bar, uint32_t parity, uint32_t barid) -> bool {
         bool got = true;
-        if (gt == 0) got = mbar_wait(bar, parity);
+        if (gt < 32) got = mbar_wait(bar, parity);   // the group's first warp, converged
         const bool bad = named_sync_or(barid, kGrp, !got);
         fence_after_sync();
         return !bad;
@@ -444,11 +464,11 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
             __syncwarp();
         }
     } else if (warp == 13) {
-        // ======================= issuer warp: the MMAs (lane 0) =======================
+        // ======================= issuer warp: the MMAs =======================
+        // Lane 0 runs the whole loop alone; lanes 1-31 wait at the warp barrier after it. (A warp
+        // that re-converges right after one lane has issued MMAs loses hundreds of cycles there.)
         auto wait1 = [&](uint64_t* bar, uint32_t parity) -> bool {
-            bool ok = true;
-            if (lane == 0) ok = mbar_wait(bar, parity);
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            const bool ok = mbar_wait(bar, parity);
             fence_after_sync();
             return ok;
         };
@@ -456,66 +476,51 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
             return wait1(&mbar_kq[jj % kKQBuf], (jj / kKQBuf) & 1);
         };
         const uint32_t idN64 = idesc_bf16(128, FC, false, false);
-        // ---- the MMA groups (lane 0 issues, the warp re-converges after each)
+        // ---- the MMA groups
         auto mma_D = [&](int jj) {   // D = [K;Q] K^T: rows 0-63 k, 64-127 q of each feature half
-            if (lane == 0) {
-                const uint32_t tk = tKQ_of(jj);
+            const uint32_t tk = tKQ_of(jj);
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint64_t d = smem_desc_sw128(tk + h * KQ_H, 16, 1024);
-                    mma_chain(tmem + TM_D, d, 32, d, 32, idN64, 64, h > 0);
-                }
-                mma_commit(mbar_D);
+            for (int h = 0; h < 2; ++h) {
+                const uint64_t d = smem_desc_sw128(tk + h * KQ_H, 16, 1024);
+                mma_chain(tmem + TM_D, d, 32, d, 32, idN64, 64, h > 0);
             }
-            __syncwarp();
+            mma_commit(mbar_D);
         };
         auto mma_Y = [&](int jj) {   // Y^T = K^T (M Diag(ef))^T
-            if (lane == 0) {
-                mma_chain(tmem + TM_Y, smem_desc_sw128(tKQ_of(jj), KQ_H, 1024), 2048,
-                          smem_desc(sbase + Ly::T_MY, 128, N64_RB), 256, idesc_bf16(128, FC, true, false), FC, false);
-                mma_commit(mbar_Y);
-            }
-            __syncwarp();
+            mma_chain(tmem + TM_Y, smem_desc_sw128(tKQ_of(jj), KQ_H, 1024), 2048,
+                      smem_desc(sbase + Ly::T_MY, 128, N64_RB), 256, idesc_bf16(128, FC, true, false), FC, false);
+            mma_commit(mbar_Y);
         };
         auto mma_Z = [&]() {         // E^T := V^T (-M)^T
-            if (lane == 0) {
-                mma_chain(tmem + TM_E, smem_desc_sw128(sbase + Ly::T_V, SWH, 1024), 2048,
-                          smem_desc(sbase + Ly::T_MN, 128, N64_RB), 256, idesc_bf16(128, FC, true, false), FC, false);
-                mma_commit(mbar_Z);
-            }
-            __syncwarp();
+            mma_chain(tmem + TM_E, smem_desc_sw128(sbase + Ly::T_V, SWH, 1024), 2048,
+                      smem_desc(sbase + Ly::T_MN, 128, N64_RB), 256, idesc_bf16(128, FC, true, false), FC, false);
+            mma_commit(mbar_Z);
         };
         auto mma_O = [&](int j) {    // O'^T = S'^T Q^T with S' = hi + lo (q rows, K-major)
-            if (lane == 0) {
-                const uint32_t tq = tKQ_of(j) + SWH;
+            const uint32_t tq = tKQ_of(j) + SWH;
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {   // c = 2 * half + (lo ? 1 : 0)
-                    const int h = c >> 1;
-                    const uint64_t dQ = smem_desc_sw128(tq + h * KQ_H, 16, 1024);
-                    mma_chain_tmem_a(tmem + TM_O, tmem + ((c & 1) ? TM_SL : TM_SH) + 32 * h, dQ, 32, idN64, 64, c > 0);
-                }
-                mma_commit(mbar_O1);
+            for (int c = 0; c < 4; ++c) {   // c = 2 * half + (lo ? 1 : 0)
+                const int h = c >> 1;
+                const uint64_t dQ = smem_desc_sw128(tq + h * KQ_H, 16, 1024);
+                mma_chain_tmem_a(tmem + TM_O, tmem + ((c & 1) ? TM_SL : TM_SH) + 32 * h, dQ, 32, idN64, 64, c > 0);
             }
-            __syncwarp();
+            mma_commit(mbar_O1);
         };
         auto mma_Oes = [&](int j) {  // O'^T += Es~^T QK~^T: hi*hi + lo*hi + hi*lo
-            if (lane == 0) {
-                const uint64_t bh0 = smem_desc(tQK_of(j, 0), 128, N64_RB), bl0 = smem_desc(tQK_of(j, 1), 128, N64_RB);
+            const uint64_t bh0 = smem_desc(tQK_of(j, 0), 128, N64_RB), bl0 = smem_desc(tQK_of(j, 1), 128, N64_RB);
 #pragma unroll
-                for (int sl = 0; sl < 4; ++sl) {
-                    const uint32_t ah = tmem + TM_E + 32 * (sl >> 1) + 8 * (sl & 1);
-                    const uint64_t bh_ = bh0 + static_cast<uint64_t>(16 * sl), bl_ = bl0 + static_cast<uint64_t>(16 * sl);
-                    mma_bf16_tmem_a(tmem + TM_O, ah, bh_, idN64, 1u);
-                    mma_bf16_tmem_a(tmem + TM_O, ah + 16, bh_, idN64, 1u);
-                    mma_bf16_tmem_a(tmem + TM_O, ah, bl_, idN64, 1u);
-                }
-                mma_commit(mbar_O);
+            for (int sl = 0; sl < 4; ++sl) {
+                const uint32_t ah = tmem + TM_E + 32 * (sl >> 1) + 8 * (sl & 1);
+                const uint64_t bh_ = bh0 + static_cast<uint64_t>(16 * sl), bl_ = bl0 + static_cast<uint64_t>(16 * sl);
+                mma_bf16_tmem_a(tmem + TM_O, ah, bh_, idN64, 1u);
+                mma_bf16_tmem_a(tmem + TM_O, ah + 16, bh_, idN64, 1u);
+                mma_bf16_tmem_a(tmem + TM_O, ah, bl_, idN64, 1u);
             }
-            __syncwarp();
+            mma_commit(mbar_O);
         };
 
         // j = -2, -1: the WY build of chunks 0 and 1 only. E(j) and X(j) are issued by group A.
-        for (int j = -2; j < nchunk && !failed; ++j) {
+        for (int j = -2; lane == 0 && j < nchunk && !failed; ++j) {
             const bool next = j + 1 < nchunk;
             if (j >= 0) {
                 // O(j) once S'(j) is in place and the outputs of chunk j-1 have been read
@@ -544,14 +549,12 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
                 mma_Z();
             }
         }
-        if (failed) {
-            if (lane == 0) {
-                atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
-                mma_commit(drain);   // tracks every MMA this thread issued
-                mbar_wait(drain, 0, 400000000LL);
-            }
-            __syncwarp();
+        if (failed) {   // (lane 0 only)
+            atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
+            mma_commit(drain);   // tracks every MMA this thread issued
+            mbar_wait(drain, 0, 400000000LL);
         }
+        __syncwarp();
     } else if (grp == 0) {
         // ======================= group A: the state chain =======================
         float graw[4];
@@ -614,13 +617,17 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
             }
             fence_before_sync();
             named_sync(kBarA, kGrp);
-            if (gt == 0) {
-                mbar_arrive(rdy_S);
+            if (warp == 0) {   // converged; lane 0 issues through a predicate
+                const uint32_t lead = lane == 0;
+                mbar_arrive_if(rdy_S, lead);
                 // E(j) += S'^T Y^T onto Z(j) (issuer), once Z(j) is done and Y^T(j) is in place
                 if (mbar_wait(mbar_Z, j & 1) && mbar_wait(rdy_Yt, j & 1)) {
                     fence_after_sync();
-                    mma_chain_tmem_a(tmem + TM_E, tmem + TM_SH, dYt, 2 * N64_RB, idE, FD, true);
-                    mma_commit(mbar_E);
+#pragma unroll
+                    for (int ks = 0; ks < FD / 16; ++ks)
+                        mma_tmem_a_if(tmem + TM_E, tmem + TM_SH + 8 * ks, dYt + static_cast<uint64_t>(ks * (2 * N64_RB / 16)),
+                                      idE, 1u, lead);
+                    mma_commit_if(mbar_E, lead);
                 }
             }
             // ---- Es~^T of chunk j, in place of E^T
@@ -639,7 +646,8 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
             tmem_wait_st();
             fence_before_sync();
             named_sync(kBarA, kGrp);
-            if (gt == 0) {
+            if (warp == 0) {   // converged; lane 0 issues through a predicate
+                const uint32_t lead = lane == 0;
                 // X(j): S^T += Es~^T K (hi + lo); Es~ hi at 32*(s/2) + 8*(s%2), lo 16 columns further
                 fence_after_sync();
                 const uint64_t dK = smem_desc_sw128(tKQ_of(j), KQ_H, 1024);   // k rows, MN-major B (K = rho)
@@ -647,11 +655,11 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
                 for (int sl = 0; sl < 4; ++sl) {
                     const uint32_t ah = tmem + TM_E + 32 * (sl >> 1) + 8 * (sl & 1);
                     const uint64_t b = dK + static_cast<uint64_t>((2048u * sl) >> 4);
-                    mma_bf16_tmem_a(tmem + TM_S, ah, b, idX, 1u);
-                    mma_bf16_tmem_a(tmem + TM_S, ah + 16, b, idX, 1u);
+                    mma_tmem_a_if(tmem + TM_S, ah, b, idX, 1u, lead);
+                    mma_tmem_a_if(tmem + TM_S, ah + 16, b, idX, 1u, lead);
                 }
-                mma_commit(mbar_X);
-                mbar_arrive(rdy_E);
+                mma_commit_if(mbar_X, lead);
+                mbar_arrive_if(rdy_E, lead);
             }
             if (j + 1 < nchunk) gates(j + 1);
             named_sync(kBarA, kGrp);   // gates of chunk j + 1 visible to the group
