@@ -150,8 +150,10 @@ __device__ __forceinline__ void mbar_arrive_if(uint64_t* mbar, uint32_t issue) {
 // x = hi + lo with both parts bf16: packed pairs (element 2i in the low half).
 __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& h, uint32_t& l) {
     h = pack_bf16(x0, x1);
-    l = pack_bf16(x0 - __uint_as_float(h << 16), x1 - __uint_as_float(h & 0xFFFF0000u));
+    const float2 r = __fadd2_rn(make_float2(x0, x1), make_float2(-__uint_as_float(h << 16), -__uint_as_float(h & 0xFFFF0000u)));
+    l = pack_bf16(r.x, r.y);
 }
+__device__ __forceinline__ void split_pair(float2 x, uint32_t& h, uint32_t& l) { split_pair(x.x, x.y, h, l); }
 
 __device__ __forceinline__ void rbm_store8_split(uint32_t th, uint32_t tl, int cols, int r, int c, const float* x) {
     uint32_t h[4], l[4];
@@ -605,12 +607,17 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
                     tmem_ld32(tmem + TM_S + lane_off + 32 * p, x);
                     uint32_t hi[16], lo[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) split_pair(ea * x[2 * i], ea * x[2 * i + 1], hi[i], lo[i]);
+                    for (int i = 0; i < 16; ++i)
+                        split_pair(__fmul2_rn(make_float2(ea, ea), make_float2(x[2 * i], x[2 * i + 1])), hi[i], lo[i]);
                     tmem_st16(tmem + TM_SH + lane_off + 16 * p, hi);
                     tmem_st16(tmem + TM_SL + lane_off + 16 * p, lo);
                     uint32_t g[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) g[i] = __float_as_uint(gam * x[i]);
+                    for (int i = 0; i < 16; ++i) {
+                        const float2 y = __fmul2_rn(make_float2(gam, gam), make_float2(x[2 * i], x[2 * i + 1]));
+                        g[2 * i] = __float_as_uint(y.x);
+                        g[2 * i + 1] = __float_as_uint(y.y);
+                    }
                     tmem_st32(tmem + TM_S + lane_off + 32 * p, g);
                 }
                 tmem_wait_st();
@@ -639,7 +646,8 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
                 uint32_t hi[16], lo[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
-                    split_pair(vf[64 + 32 * p + 2 * i] * x[2 * i], vf[64 + 32 * p + 2 * i + 1] * x[2 * i + 1], hi[i], lo[i]);
+                    split_pair(__fmul2_rn(*reinterpret_cast<const float2*>(vf + 64 + 32 * p + 2 * i), make_float2(x[2 * i], x[2 * i + 1])),
+                               hi[i], lo[i]);
                 tmem_st16(tmem + TM_E + lane_off + 32 * p, hi);
                 tmem_st16(tmem + TM_E + lane_off + 32 * p + 16, lo);
             }
