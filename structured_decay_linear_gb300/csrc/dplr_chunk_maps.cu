@@ -71,10 +71,13 @@ __device__ __forceinline__ void block_gemm(int M, int N, int K, FA a, FB b, Epi 
     }
 }
 
-// Shared-memory carve-up (floats) for one WY block; identical on host and device.
+// Shared-memory carve-up (floats) for one WY block; identical on host and device. The rows of
+// the dk-wide factor tiles (A~, B~, q~, K~) are one float longer than dk: the Gram products
+// read a column of them across a warp, and the odd stride puts those reads in distinct banks.
 struct PrepLayout {
-    int lg, G, beta, ea, egca, gam, At, Bt, Qt, Z, L, QA, Kt, Vs, GBK, QK, total;
+    int ldk, lg, G, beta, ea, egca, gam, At, Bt, Qt, Z, L, QA, Kt, Vs, GBK, QK, total;
     __host__ __device__ PrepLayout(int mode, int dk, int dv, int cw, int r, int p) {
+        ldk = dk + 1;
         const int dkg = (mode == DPLR_GDN) ? 1 : dk;
         const int cr = cw * r, cp = cw * p;
         int o = 0;
@@ -84,13 +87,13 @@ struct PrepLayout {
         ea = o;   o += dk;
         egca = o; o += dk;
         gam = o;  o += dk;
-        At = o;   o += cr * dk;
-        Bt = o;   o += cr * dk;
-        Qt = o;   o += cw * dk;
+        At = o;   o += cr * ldk;
+        Bt = o;   o += cr * ldk;
+        Qt = o;   o += cw * ldk;
         Z = o;    o += cr * dv;
         L = o;    o += cr * cr;
         QA = o;   o += cw * cr;
-        Kt = o;   o += cp * dk;
+        Kt = o;   o += cp * ldk;
         Vs = o;   o += cp * dv;
         GBK = o;  o += cr * cp;
         QK = o;   o += cw * cp;
@@ -109,6 +112,7 @@ chunk_maps_kernel(Plan pl, ChunkMapArgs args) {
     const int Pd = P > 0 ? P : 1;   // divisor for the (generic-only) K/V row loops
     const int dkg = (MODE == DPLR_GDN) ? 1 : dk;
     const PrepLayout Ly(MODE, dk, dv, cw, R, P);
+    const int ldk = Ly.ldk;
     float *lg = sm + Ly.lg, *G = sm + Ly.G, *bet = sm + Ly.beta;
     float *ea = sm + Ly.ea, *egca = sm + Ly.egca, *gam = sm + Ly.gam;
     float *At = sm + Ly.At, *Bt = sm + Ly.Bt, *Qt = sm + Ly.Qt, *Z = sm + Ly.Z;
@@ -150,7 +154,7 @@ chunk_maps_kernel(Plan pl, ChunkMapArgs args) {
     for (int i = tid; i < cw * dk; i += nth) {
         const int t = i / dk, c = i % dk;
         const float x = (t0 + t < T) ? ld(qp, (tok0 + t) * dk + c) : 0.f;
-        Qt[i] = x * expf(Gi(t, c) - anc(c));
+        Qt[t * ldk + c] = x * expf(Gi(t, c) - anc(c));
     }
     if (MODE == DPLR_GDN) {
         const IT* kp = static_cast<const IT*>(args.k);
@@ -159,8 +163,8 @@ chunk_maps_kernel(Plan pl, ChunkMapArgs args) {
             const int t = i / dk, c = i % dk;
             const float kk = (t0 + t < T) ? ld(kp, (tok0 + t) * dk + c) : 0.f;
             const float gp = Gi(t, c) - anc(c);
-            At[i] = expf(-gp) * bet[t] * kk;   // A = beta k
-            Bt[i] = expf(gp) * kk;             // e^{G_{t-1}} B_t with B = e^{g} k
+            At[t * ldk + c] = expf(-gp) * bet[t] * kk;   // A = beta k
+            Bt[t * ldk + c] = expf(gp) * kk;             // e^{G_{t-1}} B_t with B = e^{g} k
         }
         for (int i = tid; i < cw * dv; i += nth) {
             const int t = i / dv, n = i % dv;
@@ -190,10 +194,10 @@ chunk_maps_kernel(Plan pl, ChunkMapArgs args) {
             const float b = bet[t];
             const float ei = expf(-(Gi(t, c) - anc(c)));  // e^{-G'_t}
             const float ex = expf(Gx(t, c) - anc(c));     // e^{G'_{t-1}}
-            At[(2 * t) * dk + c] = ei * kk;
-            At[(2 * t + 1) * dk + c] = ei * u;
-            Bt[(2 * t) * dk + c] = ex * (b * u - b * b * cdot[t] * kk);
-            Bt[(2 * t + 1) * dk + c] = ex * b * kk;
+            At[(2 * t) * ldk + c] = ei * kk;
+            At[(2 * t + 1) * ldk + c] = ei * u;
+            Bt[(2 * t) * ldk + c] = ex * (b * u - b * b * cdot[t] * kk);
+            Bt[(2 * t + 1) * ldk + c] = ex * b * kk;
         }
         for (int i = tid; i < cw * dv; i += nth) {
             const int t = i / dv, n = i % dv;
@@ -209,12 +213,12 @@ chunk_maps_kernel(Plan pl, ChunkMapArgs args) {
             const int row = i / dk, c = i % dk, t = row / R, j = row % R;
             const bool ok = t0 + t < T;
             const size_t src = ((tok0 + t) * R + j) * dk + c;
-            At[i] = ok ? expf(-(Gi(t, c) - anc(c))) * ld(Ap, src) : 0.f;
-            Bt[i] = ok ? expf(Gx(t, c) - anc(c)) * ld(Bp, src) : 0.f;
+            At[row * ldk + c] = ok ? expf(-(Gi(t, c) - anc(c))) * ld(Ap, src) : 0.f;
+            Bt[row * ldk + c] = ok ? expf(Gx(t, c) - anc(c)) * ld(Bp, src) : 0.f;
         }
         for (int i = tid; i < cp * dk; i += nth) {
             const int row = i / dk, c = i % dk, t = row / Pd, l = row % Pd;
-            Kt[i] = (t0 + t < T) ? expf(-(Gi(t, c) - anc(c))) * ld(Kp, ((tok0 + t) * P + l) * dk + c) : 0.f;
+            Kt[row * ldk + c] = (t0 + t < T) ? expf(-(Gi(t, c) - anc(c))) * ld(Kp, ((tok0 + t) * P + l) * dk + c) : 0.f;
         }
         for (int i = tid; i < cp * dv; i += nth) {
             const int row = i / dv, n = i % dv, t = row / Pd, l = row % Pd;
@@ -225,21 +229,21 @@ chunk_maps_kernel(Plan pl, ChunkMapArgs args) {
 
     // ---- a4: Gram blocks. L = strict_block_tril(B~ A~^T); QA = tril_incl(q~ A~^T).
     block_gemm<4, 4>(cr, cr, dk,
-        [&](int m, int kk) { return Bt[m * dk + kk]; },
-        [&](int kk, int n) { return At[n * dk + kk]; },
+        [&](int m, int kk) { return Bt[m * ldk + kk]; },
+        [&](int kk, int n) { return At[n * ldk + kk]; },
         [&](int m, int n, float x) { L[m * cr + n] = (n / R < m / R) ? x : 0.f; });
     block_gemm<4, 4>(cw, cr, dk,
-        [&](int m, int kk) { return Qt[m * dk + kk]; },
-        [&](int kk, int n) { return At[n * dk + kk]; },
+        [&](int m, int kk) { return Qt[m * ldk + kk]; },
+        [&](int kk, int n) { return At[n * ldk + kk]; },
         [&](int m, int n, float x) { QA[m * cr + n] = (n / R <= m) ? x : 0.f; });
     if (MODE == DPLR_GENERIC && P > 0) {
         block_gemm<4, 4>(cr, cp, dk,
-            [&](int m, int kk) { return Bt[m * dk + kk]; },
-            [&](int kk, int n) { return Kt[n * dk + kk]; },
+            [&](int m, int kk) { return Bt[m * ldk + kk]; },
+            [&](int kk, int n) { return Kt[n * ldk + kk]; },
             [&](int m, int n, float x) { GBK[m * cp + n] = (n / Pd < m / R) ? x : 0.f; });
         block_gemm<4, 4>(cw, cp, dk,
-            [&](int m, int kk) { return Qt[m * dk + kk]; },
-            [&](int kk, int n) { return Kt[n * dk + kk]; },
+            [&](int m, int kk) { return Qt[m * ldk + kk]; },
+            [&](int kk, int n) { return Kt[n * ldk + kk]; },
             [&](int m, int n, float x) { QK[m * cp + n] = (n / Pd <= m) ? x : 0.f; });
     }
     __syncthreads();
@@ -259,7 +263,7 @@ chunk_maps_kernel(Plan pl, ChunkMapArgs args) {
     // ---- a5: UT/WY solve (I + L) [Y' | U] = [B~' | Z], in place, one column per thread.
     for (int col = tid; col < dk + dv; col += nth) {
         float* x = (col < dk) ? (Bt + col) : (Z + (col - dk));
-        const int ld_x = (col < dk) ? dk : dv;
+        const int ld_x = (col < dk) ? ldk : dv;
         for (int row = R; row < cr; ++row) {
             const int lim = (row / R) * R;   // rows of earlier tokens only
             float s = x[row * ld_x];
@@ -276,21 +280,21 @@ chunk_maps_kernel(Plan pl, ChunkMapArgs args) {
     float* Qout = args.Qm + unit * (size_t)cw * dk;
     // P[i][k] = gamma_i delta_ik - e^{G_C,i - a_i} (A~'^T Y')[i][k] e^{a_k}
     block_gemm<4, 4>(dk, dk, cr,
-        [&](int m, int kk) { return At[kk * dk + m]; },
-        [&](int kk, int n) { return Bt[kk * dk + n]; },
+        [&](int m, int kk) { return At[kk * ldk + m]; },
+        [&](int kk, int n) { return Bt[kk * ldk + n]; },
         [&](int m, int n, float x) {
             Pout[m * dk + n] = (m == n ? gam[m] : 0.f) - egca[m] * x * ea[n];
         });
     // c[i][n] = e^{G_C,i - a_i} (-(A~'^T U) + K~'^T V)[i][n]
     block_gemm<4, 4>(dk, dv, cr + cp,
-        [&](int m, int kk) { return kk < cr ? -At[kk * dk + m] : Kt[(kk - cr) * dk + m]; },
+        [&](int m, int kk) { return kk < cr ? -At[kk * ldk + m] : Kt[(kk - cr) * ldk + m]; },
         [&](int kk, int n) { return kk < cr ? Z[kk * dv + n] : Vs[(kk - cr) * dv + n]; },
         [&](int m, int n, float x) { Cout[m * dv + n] = egca[m] * x; });
     // Q'[t][k] = (q~'_t - sum QA Y')[k] e^{a_k}
     block_gemm<4, 4>(cw, dk, cr,
         [&](int m, int kk) { return QA[m * cr + kk]; },
-        [&](int kk, int n) { return Bt[kk * dk + n]; },
-        [&](int m, int n, float x) { Qout[m * dk + n] = (Qt[m * dk + n] - x) * ea[n]; });
+        [&](int kk, int n) { return Bt[kk * ldk + n]; },
+        [&](int m, int n, float x) { Qout[m * dk + n] = (Qt[m * ldk + n] - x) * ea[n]; });
     // O[t][n] = -(QA U)[t][n] + (QK V)[t][n]   -> o (zero-initial-state part)
     block_gemm<4, 4>(cw, dv, cr + cp,
         [&](int m, int kk) { return kk < cr ? -QA[m * cr + kk] : QK[m * cp + (kk - cr)]; },
