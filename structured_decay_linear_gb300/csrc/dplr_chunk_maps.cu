@@ -260,15 +260,34 @@ chunk_maps_kernel(Plan pl, ChunkMapArgs args) {
         __syncthreads();
     }
 
-    // ---- a5: UT/WY solve (I + L) [Y' | U] = [B~' | Z], in place, one column per thread.
+    // ---- a5: UT/WY solve (I + L) [Y' | U] = [B~' | Z], in place, one column per thread, by
+    // blocks of 16 rows: first the rows of earlier blocks are subtracted (16 independent
+    // accumulators per row of those blocks), then the block is solved by substitution in
+    // registers. L is zero outside the strict block-lower triangle, so each row may take every
+    // earlier row.
     for (int col = tid; col < dk + dv; col += nth) {
         float* x = (col < dk) ? (Bt + col) : (Z + (col - dk));
         const int ld_x = (col < dk) ? ldk : dv;
-        for (int row = R; row < cr; ++row) {
-            const int lim = (row / R) * R;   // rows of earlier tokens only
-            float s = x[row * ld_x];
-            for (int j = 0; j < lim; ++j) s = fmaf(-L[row * cr + j], x[j * ld_x], s);
-            x[row * ld_x] = s;
+#pragma unroll 1
+        for (int rb = 0; rb < cr; rb += 16) {
+            float xb[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) xb[i] = (rb + i < cr) ? x[(rb + i) * ld_x] : 0.f;
+#pragma unroll 1
+            for (int j = 0; j < rb; ++j) {
+                const float xj = x[j * ld_x];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    if (rb + i < cr) xb[i] = fmaf(-L[(rb + i) * cr + j], xj, xb[i]);
+            }
+#pragma unroll
+            for (int i = 1; i < 16; ++i)
+#pragma unroll
+                for (int k = 0; k < i; ++k)
+                    if (rb + i < cr) xb[i] = fmaf(-L[(rb + i) * cr + rb + k], xb[k], xb[i]);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if (rb + i < cr) x[(rb + i) * ld_x] = xb[i];
         }
     }
     __syncthreads();
