@@ -40,63 +40,137 @@ template <> __device__ __forceinline__ float ld<__nv_bfloat16>(const __nv_bfloat
     return __bfloat162float(p[i]);
 }
 
-// C(m, n) = sum_k a(m, k) b(k, n) over an M x N output, TM x TN register tiles per
-// thread (M % TM == 0, N % TN == 0), result handed to epi(m, n, value).
-template <int TM, int TN, class FA, class FB, class Epi>
-__device__ __forceinline__ void block_gemm(int M, int N, int K, FA a, FB b, Epi epi) {
-    const int tiles_n = N / TN;
-    const int tiles = (M / TM) * tiles_n;
+// Block-wide fp32 products on shared-memory tiles, one 4 x 4 tile of C per thread per step,
+// operands read as float4 (rows 16-byte aligned, M, N, K multiples of 4). The result goes to
+// epi(m, n, value).
+__device__ __forceinline__ float4 lds4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float f4(const float4& v, int i) { return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w)); }
+
+// C = A B^T: A [M][K] (row stride lda), B [N][K] (ldb). A thread's four columns are N/4 apart,
+// so that the rows of B it reads fall in distinct banks across the warp (ldb = 4 mod 32).
+template <class Epi>
+__device__ __forceinline__ void gemm_nt(int M, int N, int K, const float* A, int lda, const float* B, int ldb, Epi epi) {
+    const int nq = N / 4, tiles = (M / 4) * nq;
     for (int tile = threadIdx.x; tile < tiles; tile += blockDim.x) {
-        const int m0 = (tile / tiles_n) * TM, n0 = (tile % tiles_n) * TN;
-        float acc[TM][TN];
+        const int m0 = (tile / nq) * 4, nb = tile % nq;
+        float acc[4][4] = {};
+        for (int k = 0; k < K; k += 4) {
+            float4 a[4], b[4];
 #pragma unroll
-        for (int i = 0; i < TM; ++i)
+            for (int i = 0; i < 4; ++i) a[i] = lds4(A + (m0 + i) * lda + k);
 #pragma unroll
-            for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
-        for (int kk = 0; kk < K; ++kk) {
-            float av[TM], bv[TN];
+            for (int j = 0; j < 4; ++j) b[j] = lds4(B + (nb + nq * j) * ldb + k);
 #pragma unroll
-            for (int i = 0; i < TM; ++i) av[i] = a(m0 + i, kk);
+            for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int j = 0; j < TN; ++j) bv[j] = b(kk, n0 + j);
+                for (int j = 0; j < 4; ++j)
 #pragma unroll
-            for (int i = 0; i < TM; ++i)
-#pragma unroll
-                for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+                    for (int kk = 0; kk < 4; ++kk) acc[i][j] = fmaf(f4(a[i], kk), f4(b[j], kk), acc[i][j]);
         }
 #pragma unroll
-        for (int i = 0; i < TM; ++i)
+        for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int j = 0; j < TN; ++j) epi(m0 + i, n0 + j, acc[i][j]);
+            for (int j = 0; j < 4; ++j) epi(m0 + i, nb + nq * j, acc[i][j]);
     }
 }
 
-// Shared-memory carve-up (floats) for one WY block; identical on host and device. The rows of
-// the dk-wide factor tiles (A~, B~, q~, K~) are one float longer than dk: the Gram products
-// read a column of them across a warp, and the odd stride puts those reads in distinct banks.
+// C = s1 A1^T B1 + s2 A2^T B2: A [K][M] (lda), B [K][N] (ldb); the second pair is skipped when
+// K2 = 0.
+template <class Epi>
+__device__ __forceinline__ void gemm_tn(int M, int N, int K1, const float* A1, int lda1, const float* B1, int ldb1,
+                                        float s1, int K2, const float* A2, int lda2, const float* B2, int ldb2,
+                                        float s2, Epi epi) {
+    const int nq = N / 4, tiles = (M / 4) * nq;
+    for (int tile = threadIdx.x; tile < tiles; tile += blockDim.x) {
+        const int m0 = (tile / nq) * 4, n0 = (tile % nq) * 4;
+        float acc[4][4] = {};
+        for (int pass = 0; pass < 2; ++pass) {
+            const int K = pass ? K2 : K1, lda = pass ? lda2 : lda1, ldb = pass ? ldb2 : ldb1;
+            const float* A = pass ? A2 : A1;
+            const float* B = pass ? B2 : B1;
+            const float sc = pass ? s2 : s1;
+            for (int k = 0; k < K; ++k) {
+                const float4 a = lds4(A + k * lda + m0), b = lds4(B + k * ldb + n0);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float ai = sc * f4(a, i);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(ai, f4(b, j), acc[i][j]);
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) epi(m0 + i, n0 + j, acc[i][j]);
+    }
+}
+
+// C = s1 A1 B1 + s2 A2 B2: A [M][K] (lda), B [K][N] (ldb); the second pair is skipped when K2 = 0.
+template <class Epi>
+__device__ __forceinline__ void gemm_nn(int M, int N, int K1, const float* A1, int lda1, const float* B1, int ldb1,
+                                        float s1, int K2, const float* A2, int lda2, const float* B2, int ldb2,
+                                        float s2, Epi epi) {
+    const int nq = N / 4, tiles = (M / 4) * nq;
+    for (int tile = threadIdx.x; tile < tiles; tile += blockDim.x) {
+        const int m0 = (tile / nq) * 4, n0 = (tile % nq) * 4;
+        float acc[4][4] = {};
+        for (int pass = 0; pass < 2; ++pass) {
+            const int K = pass ? K2 : K1, lda = pass ? lda2 : lda1, ldb = pass ? ldb2 : ldb1;
+            const float* A = pass ? A2 : A1;
+            const float* B = pass ? B2 : B1;
+            const float sc = pass ? s2 : s1;
+            for (int k = 0; k < K; k += 4) {
+                float4 a[4], b[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) a[i] = lds4(A + (m0 + i) * lda + k);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) b[kk] = lds4(B + (k + kk) * ldb + n0);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const float ai = sc * f4(a[i], kk);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(ai, f4(b[kk], j), acc[i][j]);
+                    }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) epi(m0 + i, n0 + j, acc[i][j]);
+    }
+}
+
+// Shared-memory carve-up (floats) for one WY block; identical on host and device. Every tile
+// starts on a 16-byte boundary. The rows of the dk-wide factor tiles (A~, B~, q~, K~) are dk + 4
+// floats: 16-byte aligned, and 4 banks apart, so that a warp reading one float4 from each of
+// eight rows touches every bank once.
 struct PrepLayout {
     int ldk, lg, G, beta, ea, egca, gam, At, Bt, Qt, Z, L, QA, Kt, Vs, GBK, QK, total;
     __host__ __device__ PrepLayout(int mode, int dk, int dv, int cw, int r, int p) {
-        ldk = dk + 1;
+        ldk = dk + 4;
         const int dkg = (mode == DPLR_GDN) ? 1 : dk;
         const int cr = cw * r, cp = cw * p;
         int o = 0;
-        lg = o;   o += cw * dkg;
-        G = o;    o += cw * dkg;
-        beta = o; o += cw;
-        ea = o;   o += dk;
-        egca = o; o += dk;
-        gam = o;  o += dk;
-        At = o;   o += cr * ldk;
-        Bt = o;   o += cr * ldk;
-        Qt = o;   o += cw * ldk;
-        Z = o;    o += cr * dv;
-        L = o;    o += cr * cr;
-        QA = o;   o += cw * cr;
-        Kt = o;   o += cp * ldk;
-        Vs = o;   o += cp * dv;
-        GBK = o;  o += cr * cp;
-        QK = o;   o += cw * cp;
+        auto take = [&o](int n) { const int at = o; o += (n + 3) & ~3; return at; };
+        lg = take(cw * dkg);
+        G = take(cw * dkg);
+        beta = take(cw);
+        ea = take(dk);
+        egca = take(dk);
+        gam = take(dk);
+        At = take(cr * ldk);
+        Bt = take(cr * ldk);
+        Qt = take(cw * ldk);
+        Z = take(cr * dv);
+        L = take(cr * cr);
+        QA = take(cw * cr);
+        Kt = take(cp * ldk);
+        Vs = take(cp * dv);
+        GBK = take(cr * cp);
+        QK = take(cw * cp);
         total = o;
     }
 };
@@ -228,32 +302,22 @@ chunk_maps_kernel(Plan pl, ChunkMapArgs args) {
     __syncthreads();
 
     // ---- a4: Gram blocks. L = strict_block_tril(B~ A~^T); QA = tril_incl(q~ A~^T).
-    block_gemm<4, 4>(cr, cr, dk,
-        [&](int m, int kk) { return Bt[m * ldk + kk]; },
-        [&](int kk, int n) { return At[n * ldk + kk]; },
-        [&](int m, int n, float x) { L[m * cr + n] = (n / R < m / R) ? x : 0.f; });
-    block_gemm<4, 4>(cw, cr, dk,
-        [&](int m, int kk) { return Qt[m * ldk + kk]; },
-        [&](int kk, int n) { return At[n * ldk + kk]; },
-        [&](int m, int n, float x) { QA[m * cr + n] = (n / R <= m) ? x : 0.f; });
+    gemm_nt(cr, cr, dk, Bt, ldk, At, ldk,
+            [&](int m, int n, float x) { L[m * cr + n] = (n / R < m / R) ? x : 0.f; });
+    gemm_nt(cw, cr, dk, Qt, ldk, At, ldk,
+            [&](int m, int n, float x) { QA[m * cr + n] = (n / R <= m) ? x : 0.f; });
     if (MODE == DPLR_GENERIC && P > 0) {
-        block_gemm<4, 4>(cr, cp, dk,
-            [&](int m, int kk) { return Bt[m * ldk + kk]; },
-            [&](int kk, int n) { return Kt[n * ldk + kk]; },
-            [&](int m, int n, float x) { GBK[m * cp + n] = (n / Pd < m / R) ? x : 0.f; });
-        block_gemm<4, 4>(cw, cp, dk,
-            [&](int m, int kk) { return Qt[m * ldk + kk]; },
-            [&](int kk, int n) { return Kt[n * ldk + kk]; },
-            [&](int m, int n, float x) { QK[m * cp + n] = (n / Pd <= m) ? x : 0.f; });
+        gemm_nt(cr, cp, dk, Bt, ldk, Kt, ldk,
+                [&](int m, int n, float x) { GBK[m * cp + n] = (n / Pd < m / R) ? x : 0.f; });
+        gemm_nt(cw, cp, dk, Qt, ldk, Kt, ldk,
+                [&](int m, int n, float x) { QK[m * cp + n] = (n / Pd <= m) ? x : 0.f; });
     }
     __syncthreads();
     if (MODE == DPLR_GENERIC) {
         // Right-hand side of the value part: Z = G_BK V (zero when r_kv = 0).
         if (P > 0) {
-            block_gemm<4, 4>(cr, dv, cp,
-                [&](int m, int kk) { return GBK[m * cp + kk]; },
-                [&](int kk, int n) { return Vs[kk * dv + n]; },
-                [&](int m, int n, float x) { Z[m * dv + n] = x; });
+            gemm_nn(cr, dv, cp, GBK, cp, Vs, dv, 1.f, 0, nullptr, 0, nullptr, 0, 0.f,
+                    [&](int m, int n, float x) { Z[m * dv + n] = x; });
         } else {
             for (int i = tid; i < cr * dv; i += nth) Z[i] = 0.f;
         }
@@ -298,29 +362,19 @@ chunk_maps_kernel(Plan pl, ChunkMapArgs args) {
     float* Cout = args.Cm + unit * (size_t)dk * dv;
     float* Qout = args.Qm + unit * (size_t)cw * dk;
     // P[i][k] = gamma_i delta_ik - e^{G_C,i - a_i} (A~'^T Y')[i][k] e^{a_k}
-    block_gemm<4, 4>(dk, dk, cr,
-        [&](int m, int kk) { return At[kk * ldk + m]; },
-        [&](int kk, int n) { return Bt[kk * ldk + n]; },
-        [&](int m, int n, float x) {
-            Pout[m * dk + n] = (m == n ? gam[m] : 0.f) - egca[m] * x * ea[n];
-        });
+    gemm_tn(dk, dk, cr, At, ldk, Bt, ldk, 1.f, 0, nullptr, 0, nullptr, 0, 0.f,
+            [&](int m, int n, float x) { Pout[m * dk + n] = (m == n ? gam[m] : 0.f) - egca[m] * x * ea[n]; });
     // c[i][n] = e^{G_C,i - a_i} (-(A~'^T U) + K~'^T V)[i][n]
-    block_gemm<4, 4>(dk, dv, cr + cp,
-        [&](int m, int kk) { return kk < cr ? -At[kk * ldk + m] : Kt[(kk - cr) * ldk + m]; },
-        [&](int kk, int n) { return kk < cr ? Z[kk * dv + n] : Vs[(kk - cr) * dv + n]; },
-        [&](int m, int n, float x) { Cout[m * dv + n] = egca[m] * x; });
+    gemm_tn(dk, dv, cr, At, ldk, Z, dv, -1.f, cp, Kt, ldk, Vs, dv, 1.f,
+            [&](int m, int n, float x) { Cout[m * dv + n] = egca[m] * x; });
     // Q'[t][k] = (q~'_t - sum QA Y')[k] e^{a_k}
-    block_gemm<4, 4>(cw, dk, cr,
-        [&](int m, int kk) { return QA[m * cr + kk]; },
-        [&](int kk, int n) { return Bt[kk * ldk + n]; },
-        [&](int m, int n, float x) { Qout[m * dk + n] = (Qt[m * ldk + n] - x) * ea[n]; });
+    gemm_nn(cw, dk, cr, QA, cr, Bt, ldk, 1.f, 0, nullptr, 0, nullptr, 0, 0.f,
+            [&](int m, int n, float x) { Qout[m * dk + n] = (Qt[m * ldk + n] - x) * ea[n]; });
     // O[t][n] = -(QA U)[t][n] + (QK V)[t][n]   -> o (zero-initial-state part)
-    block_gemm<4, 4>(cw, dv, cr + cp,
-        [&](int m, int kk) { return kk < cr ? -QA[m * cr + kk] : QK[m * cp + (kk - cr)]; },
-        [&](int kk, int n) { return kk < cr ? Z[kk * dv + n] : Vs[(kk - cr) * dv + n]; },
-        [&](int m, int n, float x) {
-            if (t0 + m < T) args.o[(tok0 + m) * dv + n] = x;
-        });
+    gemm_nn(cw, dv, cr, QA, cr, Z, dv, -1.f, cp, QK, cp, Vs, dv, 1.f,
+            [&](int m, int n, float x) {
+                if (t0 + m < T) args.o[(tok0 + m) * dv + n] = x;
+            });
 }
 
 template <int MODE, class IT>
