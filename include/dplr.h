@@ -189,7 +189,11 @@ DPLR_API size_t dplr_la_host_workspace_size(const dplr_desc* desc, int groups, i
  * calls on one device run in call order. Allocates no device memory. Errors: as
  * dplr_la_forward, plus DPLR_ERR_INVALID_ARG for a bad group or slot count and
  * DPLR_ERR_WORKSPACE for a missing, misaligned or small staging area; a CUDA error after
- * some groups were queued returns DPLR_ERR_CUDA. */
+ * some groups were queued returns DPLR_ERR_CUDA, and the groups already queued may still be
+ * running: synchronise the device before freeing `staging` or the host buffers. A
+ * device-side timeout (DPLR_ERR_TIMEOUT in dplr_la_forward) is written to the status word of
+ * the group's staging slot, which the next group in that slot clears; callers that need to
+ * read it use dplr_la_forward. */
 DPLR_API dplr_status dplr_la_forward_host(const dplr_desc* desc,
                                  const void* q, const void* k, const void* v,
                                  const float* decay, const float* beta,
