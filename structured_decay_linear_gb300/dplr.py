@@ -256,7 +256,7 @@ def default_groups(desc: dplr_desc) -> int:
     group keeps enough heads to occupy the GPU (the fused kernel runs one CTA per head for the
     whole sequence, the two-stage kernels parallelise over chunks and want more heads)."""
     bh = desc.B * desc.H
-    min_heads = 8 if dplr_la_kernel_count(desc) == 1 else 32
+    min_heads = 16 if dplr_la_kernel_count(desc) == 1 else 32
     best = 1
     for g in range(1, 17):
         if bh % g == 0 and bh // g >= min_heads:
@@ -270,7 +270,7 @@ class ForwardHost:
 
     def __init__(self, mode: str, in_dtype: torch.dtype, B: int, H: int, T: int, dk: int, dv: int,
                  r_ab: Optional[int] = None, r_kv: Optional[int] = None, chunk: int = 64,
-                 groups: Optional[int] = None, slots: int = 4, device: Optional[torch.device] = None):
+                 groups: Optional[int] = None, slots: int = 8, device: Optional[torch.device] = None):
         self.desc = make_desc(mode, in_dtype, B, H, T, dk, dv, r_ab, r_kv, chunk)
         st = dplr_la_check(self.desc)
         if st != DPLR_OK:
