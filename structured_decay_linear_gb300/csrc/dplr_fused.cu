@@ -732,20 +732,25 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
                     if (gt < FC) {
                         const int t = gt;
                         const float eft = vf[t];
+                        const float2 ef2 = make_float2(eft, eft);
 #pragma unroll
                         for (int i = 0; i < 32; i += 4) {
-                            float y[4];
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                const int sg = 32 * hh + i + u;
-                                y[u] = (sg < t) ? eft * x[i + u] * vf[64 + sg] : 0.f;
-                            }
-                            *reinterpret_cast<float4*>(F_L + t * kLdL + 32 * hh + i) = make_float4(y[0], y[1], y[2], y[3]);
+                            const float4 bs = *reinterpret_cast<const float4*>(vf + 64 + 32 * hh + i);
+                            const float2 y01 = __fmul2_rn(__fmul2_rn(ef2, make_float2(x[i], x[i + 1])), make_float2(bs.x, bs.y));
+                            const float2 y23 = __fmul2_rn(__fmul2_rn(ef2, make_float2(x[i + 2], x[i + 3])), make_float2(bs.z, bs.w));
+                            const int sg = 32 * hh + i;
+                            *reinterpret_cast<float4*>(F_L + t * kLdL + sg) =
+                                make_float4(sg < t ? y01.x : 0.f, sg + 1 < t ? y01.y : 0.f, sg + 2 < t ? y23.x : 0.f, sg + 3 < t ? y23.y : 0.f);
                         }
                     } else {
                         const int t = gt - FC;
+                        const float2 ic2 = make_float2(inv_c, inv_c);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) x[i] = (32 * hh + i <= t) ? x[i] * inv_c : 0.f;
+                        for (int i = 0; i < 32; i += 2) {
+                            const float2 y = __fmul2_rn(ic2, make_float2(x[i], x[i + 1]));
+                            x[i] = (32 * hh + i <= t) ? y.x : 0.f;
+                            x[i + 1] = (32 * hh + i + 1 <= t) ? y.y : 0.f;
+                        }
 #pragma unroll
                         for (int i = 0; i < 32; i += 8)
                             rbm_store8_split(tQK_of(jj, 0), tQK_of(jj, 1), FC, t, 32 * hh + i, x + i);
