@@ -73,6 +73,10 @@ def test_status_strings(sdl):
     ("generic", "f32", 1, 1, 8, 32, 32, 0, 1, 2),   # generic needs r_ab >= 1
     ("gdn", "f32", 0, 1, 8, 32, 32, 1, 1, 1),       # empty batch
     ("gdn", "f32", 1, 1, -1, 32, 32, 1, 1, 1),      # negative length
+    # the largest shared-memory footprints of the two-stage kernels must still be accepted
+    ("gdn", "f32", 1, 1, 64, 128, 128, 1, 1, 0),    # 64-token WY blocks with d = 128
+    ("generic", "f32", 1, 1, 64, 128, 128, 4, 2, 0),
+    ("generic", "f32", 1, 1, 64, 128, 128, 8, 8, 0),
 ])
 def test_descriptor_validation(sdl, mode, dt, B, H, T, dk, dv, r, p, expect):
     d = sdl.make_desc(mode, dt, B, H, T, dk, dv, r, p)
@@ -195,3 +199,13 @@ def test_forward_host_rejects_bad_arguments_before_launch(sdl):
     assert call(None, need, 2, 2) == sdl.dplr.DPLR_ERR_WORKSPACE
     no_k = [fake, None] + [fake] * 3 + [None] * 4 + [None, fake, None]
     assert call(fake, need, 2, 2, no_k) == sdl.dplr.DPLR_ERR_INVALID_ARG  # k missing
+
+
+def test_host_path_default_groups(sdl):
+    """Head groups of the host-buffer path: at least 16 heads per group on the fused kernel, 32 on
+    the two-stage kernels, and at most 16 groups."""
+    dg = sdl.dplr.default_groups
+    assert dg(sdl.make_desc("gdn", "bf16", 8, 16, 8192, 128, 128)) == 8
+    assert dg(sdl.make_desc("hdla", "bf16", 4, 16, 4096, 128, 128)) == 2
+    assert dg(sdl.make_desc("hdla", "bf16", 1, 16, 4096, 128, 128)) == 1
+    assert dg(sdl.make_desc("gdn", "bf16", 32, 16, 1024, 128, 128)) == 16

@@ -108,6 +108,7 @@ SMALL_STRUCTURED = [
     ("gdn", "f32", 32, 32, 2, 256, False),
     ("gdn", "f32", 128, 64, 2, 1, True),
     ("gdn", "f32", 64, 128, 3, 200, True),
+    ("gdn", "f32", 128, 128, 1, 300, True),   # two-stage path with its largest scan staging (64-token blocks, d = 128)
     ("gdn", "bf16", 128, 128, 3, 200, False),
     ("gdn", "bf16", 32, 64, 2, 5, True),
     ("hdla", "bf16", 128, 128, 2, 130, True),
