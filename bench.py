@@ -393,7 +393,8 @@ def run_ours(args, w):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "bf16" if fused else "f32",
+            "dtype": "bf16" if fused else "f32",          # arithmetic of the path's products
+            "input_dtype": w.dtype,                        # storage type of q, k, v (A, B, K, V)
             "data": "synthetic (seeded workload recipe, resident in HBM)",
             "config": {"workload": w.name, "mode": w.mode, "B": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv,
                        "r_ab": w.r_ab, "r_kv": w.r_kv, "chunk": w.chunk, "in_dtype": w.dtype,
@@ -425,6 +426,66 @@ def run_ours(args, w):
         tdist.destroy_process_group()
 
 
+def run_host_overhead(args):
+    """Host time of one dplr_la_forward call (argument checks, plan, cached tensor maps, launch),
+    measured through the C ABI on T = 64 problems. Calls are timed in bursts of 100 that start on
+    an idle GPU, so that the launch queue never fills and the host never waits for the device; the
+    best of 20 bursts is kept. The ctypes overhead is measured on dplr_la_check (no launch)."""
+    import torch
+    import structured_decay_linear_gb300 as sdl
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    lines = []
+    for mode, heads in (("gdn", 1), ("gdn", 16), ("hdla", 1), ("hdla", 16)):
+        w = dataclasses_replace(workloads.WORKLOADS[2 if mode == "gdn" else 4], B=1, H=heads, T=64,
+                                name=f"{mode}_bf16_b1h{heads}_t64_d128")
+        inp = workloads.generate(w, heads=[(0, h) for h in range(heads)], T=64)
+        dt = torch.bfloat16
+        t = {k: (None if inp[k] is None else torch.from_numpy(np.ascontiguousarray(inp[k])).to(dev))
+             for k in ("q", "k", "v", "decay", "beta", "S0")}
+        for k in ("q", "k", "v"):
+            t[k] = t[k].to(dt)
+        f = sdl.Forward(mode, dt, 1, heads, 64, 128, 128, device=dev)
+        ptr = lambda x: None if x is None else x.data_ptr()
+        call = lambda: sdl.dplr_la_forward(f.desc, ptr(t["q"]), ptr(t["k"]), ptr(t["v"]), ptr(t["decay"]),
+                                           ptr(t["beta"]), None, None, None, None, ptr(t["S0"]), ptr(f.o),
+                                           ptr(f.S_T), ptr(f.workspace), f.ws_bytes, stream)
+        for _ in range(50):
+            assert call() == 0
+        torch.cuda.synchronize(dev)
+        n, best = 100, float("inf")
+        for _ in range(20):
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            for _ in range(n):
+                call()
+            best = min(best, (time.perf_counter() - t0) / n * 1e6)
+        host_us = best
+        torch.cuda.synchronize(dev)
+        n = 5000
+        t0 = time.perf_counter()
+        for _ in range(n):
+            sdl.dplr_la_check(f.desc)
+        ctypes_us = (time.perf_counter() - t0) / n * 1e6
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(200):
+            call()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        lines.append({"workload": w.name, "kernels_per_call": f.kernels,
+                      "host_us_per_call": host_us, "ctypes_us_per_check_call": ctypes_us,
+                      "gpu_us_per_call_back_to_back": e0.elapsed_time(e1) / 200 * 1e3})
+    print(json.dumps({"mode": "host_overhead", "burst": 100, "bursts": 20, "results": lines}), flush=True)
+
+
+def dataclasses_replace(w, **kw):
+    import dataclasses
+    return dataclasses.replace(w, **kw)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -433,9 +494,14 @@ def main():
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--host-overhead", action="store_true",
+                    help="time the host side of dplr_la_forward on T = 64 problems (not a benchmark line)")
     ap.add_argument("--seq-len", type=int, default=0,
                     help="override the workload's T (smaller cases for profiling; not a benchmark line)")
     args = ap.parse_args()
+    if args.host_overhead:
+        run_host_overhead(args)
+        return
     w = workloads.WORKLOADS[args.workload]
     if args.seq_len > 0:
         import dataclasses

@@ -76,7 +76,7 @@ typedef enum {
     DPLR_ERR_UNSUPPORTED = 2,   /* well-formed but outside the supported sizes */
     DPLR_ERR_WORKSPACE = 3,     /* workspace pointer null or smaller than required */
     DPLR_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
-    DPLR_ERR_TIMEOUT = 5        /* reserved: a bounded device-side wait gave up */
+    DPLR_ERR_TIMEOUT = 5        /* a bounded device-side wait gave up (device status word) */
 } dplr_status;
 
 typedef enum { DPLR_GDN = 1, DPLR_HDLA = 2, DPLR_GENERIC = 3 } dplr_mode;
@@ -95,14 +95,13 @@ typedef struct {
 } dplr_desc;
 
 /* Bytes of device workspace dplr_la_forward needs for `desc`; 0 if `desc` is
- * invalid or unsupported (call dplr_la_check for the reason). When the forward
- * runs the fused per-head kernel (GDN, bf16, dk = dv = 128) this is 256
- * bytes: the first int32 is a device status word that a kernel sets to
- * DPLR_ERR_TIMEOUT if one of its bounded waits gives up (DPLR_ERR_CUDA if its
- * shared memory is not 1024-byte aligned, in which case it computes nothing), and
- * never clears; zero
- * it once after allocating the workspace to observe that. Otherwise it holds the
- * chunk maps of the two-stage path. */
+ * invalid or unsupported (call dplr_la_check for the reason). The first 256 bytes
+ * of every workspace hold the device status word (its first int32): a kernel whose
+ * bounded wait gives up sets it to DPLR_ERR_TIMEOUT (DPLR_ERR_CUDA if its shared
+ * memory is not 1024-byte aligned, in which case it computes nothing). Kernels
+ * never clear it: zero it once after allocating the workspace, and read it with
+ * dplr_la_read_status. The rest holds the per-chunk maps of the paths that keep
+ * them between kernels. */
 DPLR_API size_t dplr_la_workspace_size(const dplr_desc* desc);
 
 /* Bytes of device workspace dplr_la_chunk_maps and dplr_la_state_scan need for
@@ -143,6 +142,26 @@ DPLR_API dplr_status dplr_la_chunk_maps(const dplr_desc* desc,
 DPLR_API dplr_status dplr_la_state_scan(const dplr_desc* desc, const float* S0, float* o, float* S_T,
                                void* workspace, size_t ws_bytes, void* stream);
 
+/* Synchronous check of the device status word (no counterpart in the paper). Waits
+ * for the work queued on `stream`, then copies the first int32 of `workspace` (a
+ * dplr_la_forward / stage workspace of `ws_bytes` bytes) into *status: DPLR_OK, or
+ * the code a kernel left there (DPLR_ERR_TIMEOUT after a bounded device-side wait
+ * gave up). With `clear` nonzero the word is zeroed afterwards on `stream`. Returns
+ * DPLR_ERR_WORKSPACE for a null or undersized workspace, DPLR_ERR_INVALID_ARG for a
+ * null `status`, DPLR_ERR_CUDA if a CUDA call fails (including an earlier
+ * asynchronous failure of the stream's work). Blocks the calling thread. */
+DPLR_API dplr_status dplr_la_read_status(const void* workspace, size_t ws_bytes, int clear, int* status,
+                                         void* stream);
+
+/* Sets the limit, in SM clock cycles, of every bounded device-side wait that a kernel
+ * makes on another part of the same launch (no counterpart in the paper). It applies
+ * to the launches of later calls in the process; `cycles` <= 0 restores the default
+ * (4e9 cycles, about 2 s). A wait that reaches the limit gives up: the kernel sets the
+ * status word to DPLR_ERR_TIMEOUT, waits for its own copies and tensor-core work
+ * already in flight, and returns with its outputs incomplete. Meant for tests of that
+ * path; a small limit makes correct launches give up too. */
+DPLR_API void dplr_la_set_wait_limit(long long cycles);
+
 /* Human-readable name of a status code (static storage). */
 DPLR_API const char* dplr_status_string(dplr_status status);
 
@@ -155,18 +174,33 @@ DPLR_API int dplr_la_kernel_count(const dplr_desc* desc);
  * an addition for callers that cannot allocate device memory at call time, such
  * as an inference engine that reserved the device up front or a plugin whose
  * host framework owns the allocator). Scratch comes from a 64 MiB array compiled
- * into the library, which every device that loads the library holds until the
- * process exits; descriptors whose dplr_la_workspace_size exceeds 64 MiB return
- * DPLR_ERR_UNSUPPORTED before anything is launched. Allocates nothing. Runs on
- * the current device (make the stream's device current). The first call on a
- * device looks up the array's device address: make it before any stream
- * capture. Every call shares the array, so calls whose GPU work overlaps race
- * and must be serialised. Other arguments and errors as for dplr_la_forward. */
+ * into the library; descriptors whose dplr_la_workspace_size exceeds 64 MiB return
+ * DPLR_ERR_UNSUPPORTED before anything is launched. Allocates nothing. Runs on the
+ * current device (make the stream's device current).
+ * Memory: the array is part of the library's device code. Under CUDA's default
+ * lazy module loading a device reserves it when the first call on that device
+ * looks up its address; from then on the device holds it until the process exits.
+ * Make that first call (or a warm-up call) before reserving the rest of the
+ * device's memory, and before any stream capture. A device reset (for instance
+ * cudaDeviceReset) invalidates the looked-up address: do not call this entry point
+ * on a device after resetting it.
+ * Sharing: every call shares the array, so calls whose GPU work overlaps race and
+ * must be serialised. Each call first zeroes the array's status word on `stream`;
+ * dplr_la_noalloc_status reads it after the call. Other arguments and errors as
+ * for dplr_la_forward. */
 DPLR_API dplr_status dplr_la_forward_noalloc(const dplr_desc* desc,
                                     const void* q, const void* k, const void* v,
                                     const float* decay, const float* beta,
                                     const void* A, const void* Bm, const void* K, const void* V,
                                     const float* S0, float* o, float* S_T, void* stream);
+
+/* Synchronous status check for dplr_la_forward_noalloc (no counterpart in the paper):
+ * waits for the work queued on `stream`, then copies the status word of the
+ * library's scratch array on the current device into *status (DPLR_OK, or the code
+ * a kernel of the last call left there, such as DPLR_ERR_TIMEOUT). Allocates
+ * nothing. DPLR_ERR_INVALID_ARG for a null `status`; DPLR_ERR_CUDA if a CUDA call
+ * fails or no dplr_la_forward_noalloc call has run on the current device yet. */
+DPLR_API dplr_status dplr_la_noalloc_status(int* status, void* stream);
 
 /* Bytes of device staging area dplr_la_forward_host needs for `desc` split into
  * `groups` groups of heads with `slots` staging slots (1 <= slots <= 8); 0 if the
@@ -186,7 +220,9 @@ DPLR_API size_t dplr_la_host_workspace_size(const dplr_desc* desc, int groups, i
  * waits for all of it (synchronise `stream` before reading o and S_T); the host buffers
  * must stay valid until then. The library keeps, per device, two copy streams, 8 compute
  * streams and their events, created on the first call made while that device is current;
- * calls on one device run in call order. Allocates no device memory. Errors: as
+ * calls on one device run in call order when they are made on one stream; calls on
+ * different streams that share a staging area must be serialised by the caller (wait for
+ * the earlier call's stream before making the next call). Allocates no device memory. Errors: as
  * dplr_la_forward, plus DPLR_ERR_INVALID_ARG for a bad group or slot count and
  * DPLR_ERR_WORKSPACE for a missing, misaligned or small staging area; a CUDA error after
  * some groups were queued returns DPLR_ERR_CUDA, and the groups already queued may still be

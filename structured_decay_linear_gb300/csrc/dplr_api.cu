@@ -14,6 +14,8 @@ bool valid_dim(int d) { return d == 32 || d == 64 || d == 128; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+std::atomic<long long> g_wait_cycles{kDefaultWaitCycles};
+
 // Largest power-of-two WY block (<= chunk) whose stacked rank rows fit.
 int wy_block(int chunk, int r, int p) {
     const int m = r > p ? r : p;
@@ -50,13 +52,14 @@ dplr_status make_plan(const dplr_desc* d, Plan* pl) {
     p.cw = wy_block(d->chunk, p.r, p.p);
     p.nb = (d->T + p.cw - 1) / p.cw;
     const size_t units = (size_t)p.BH * p.nb;
-    size_t off = 0;
+    size_t off = kAlign;   // the first 256 bytes hold the device status word
     p.off_P = off; off = round_up(off + units * (size_t)p.dk * p.dk * sizeof(float));
     p.off_c = off; off = round_up(off + units * (size_t)p.dk * p.dv * sizeof(float));
     p.off_Q = off; off = round_up(off + units * (size_t)p.cw * p.dk * sizeof(float));
     p.ws_stages = off;
     p.fused = fused_supported(p) ? 1 : 0;
-    p.ws_bytes = p.fused ? kAlign : p.ws_stages;   // fused: one device status word
+    p.wait_cycles = g_wait_cycles.load(std::memory_order_relaxed);
+    p.ws_bytes = p.fused ? kAlign : p.ws_stages;   // fused: the status word alone
     if (prep_smem_bytes(p) > 227 * 1024 || scan_smem_bytes(p) > 227 * 1024) return DPLR_ERR_UNSUPPORTED;
     *pl = p;
     return DPLR_OK;
@@ -186,6 +189,22 @@ dplr_status dplr_la_forward(const dplr_desc* desc, const void* q, const void* k,
     if (launch_chunk_maps(pl, map_args(pl, q, k, v, decay, beta, A, Bm, K, V, o, workspace), s) != cudaSuccess)
         return DPLR_ERR_CUDA;
     if (launch_state_scan(pl, scan_args(pl, S0, o, S_T, workspace), s) != cudaSuccess) return DPLR_ERR_CUDA;
+    return DPLR_OK;
+}
+
+void dplr_la_set_wait_limit(long long cycles) {
+    g_wait_cycles.store(cycles > 0 ? cycles : kDefaultWaitCycles, std::memory_order_relaxed);
+}
+
+dplr_status dplr_la_read_status(const void* workspace, size_t ws_bytes, int clear, int* status, void* stream) {
+    if (status == nullptr) return DPLR_ERR_INVALID_ARG;
+    if (workspace == nullptr || ws_bytes < sizeof(int)) return DPLR_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int word = 0;
+    if (cudaMemcpyAsync(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return DPLR_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return DPLR_ERR_CUDA;
+    *status = word;
+    if (clear && cudaMemsetAsync(const_cast<void*>(workspace), 0, sizeof(int), s) != cudaSuccess) return DPLR_ERR_CUDA;
     return DPLR_OK;
 }
 

@@ -381,7 +381,9 @@ template <int MODE, class IT>
 cudaError_t launch_mode(const Plan& pl, const ChunkMapArgs& a, cudaStream_t s) {
     const size_t smem = prep_smem_bytes(pl);
     auto kern = chunk_maps_kernel<MODE, IT>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    // one instance per template: the limit is raised to the largest footprint once per device
+    static std::atomic<uint64_t> done{0};
+    cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(kern), 227 * 1024, done);
     if (e != cudaSuccess) return e;
     const long long grid = (long long)pl.BH * pl.nb;
     kern<<<(unsigned)grid, kPrepThreads, smem, s>>>(pl, a);

@@ -365,12 +365,13 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
         r[2] = (t0 < T) ? args.beta[tok_base + t0] : 0.f;
         r[3] = (t0 + 1 < T) ? args.beta[tok_base + t0 + 1] : 0.f;
     };
+    const long long wl = pl.wait_cycles;   // limit of every wait on another role (drains excepted)
     // bounded wait of a whole group on an mbarrier phase; false (for every thread) if it gave up.
     // One thread polls; the others sleep on the group's hardware barrier, so the polling does
     // not take issue slots from the warps that work (the issuer above all).
     auto group_wait = [&](uint64_t* bar, uint32_t parity, uint32_t barid) -> bool {
         bool got = true;
-        if (gt < 32) got = mbar_wait(bar, parity);   // the group's first warp, converged
+        if (gt < 32) got = mbar_wait(bar, parity, wl);   // the group's first warp, converged
         const bool bad = named_sync_or(barid, kGrp, !got);
         fence_after_sync();
         return !bad;
@@ -379,8 +380,10 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
 
     if (warp == 12) {
         // ======================= copy warp: TMA (lane 0) and the ragged last chunk (all lanes) ==========
-        uint32_t kq_pend = 0;   // bit b: a copy into k/q buffer b was issued and not yet seen to land
-        bool v_pend = false;
+        // the last chunk copied into each k/q buffer and into the v buffer (-1: none): the phase of
+        // that copy is the one a drain waits for
+        int last_kq[kKQBuf], last_v = -1;
+        for (int b = 0; b < kKQBuf; ++b) last_kq[b] = -1;
         auto ragged_rows = [&](int jj, const __nv_bfloat16* src, uint32_t dst, uint32_t half_stride) {
             const int valid = T - jj * FC;
             const size_t g0 = tok_base + (size_t)jj * FC;
@@ -402,7 +405,6 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
                     for (int x = 0; x < 4; ++x)   // x = 2 * half + (q ? 1 : 0)
                         tma_load_2d(dst + x * SWH, (x & 1) ? &tm_q : &tm_k, 64 * (x >> 1), y, &mbar_kq[b]);
                 }
-                kq_pend |= 1u << b;
             } else {   // ragged last chunk: plain loads, zero rows past the end; then a plain arrival
                 ragged_rows(jj, args.k, tKQ_of(jj), KQ_H);
                 ragged_rows(jj, args.q, tKQ_of(jj) + SWH, KQ_H);
@@ -410,6 +412,7 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&mbar_kq[b]);
             }
+            last_kq[b] = jj;
             __syncwarp();
         };
         auto load_v = [&](int jj) {
@@ -419,13 +422,13 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
                     mbar_expect_tx(mbar_v, FC * FD * 2);
                     for (int x = 0; x < 2; ++x) tma_load_2d(smem + Ly::T_V + x * SWH, &tm_v, 64 * x, y, mbar_v);
                 }
-                v_pend = true;
             } else {
                 ragged_rows(jj, args.v, sbase + Ly::T_V, SWH);
                 fence_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(mbar_v);
             }
+            last_v = jj;
             __syncwarp();
         };
         if (nchunk > 0) {
@@ -441,7 +444,7 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
                 if (lane == 0) {
                     const long long t0 = clock64();
                     while (ld_acquire_shared(o_seen) < j || ld_acquire_shared(x_seen) < j) {
-                        if (clock64() - t0 > 4000000000LL) { ok = false; break; }
+                        if (clock64() - t0 > wl) { ok = false; break; }
                         __nanosleep(100);
                     }
                 }
@@ -451,7 +454,7 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
             // v of chunk j+1 once Z(j) has read v(j)
             if (j + 1 < nchunk) {
                 bool ok = true;
-                if (lane == 0) ok = mbar_wait(mbar_Z, j & 1);
+                if (lane == 0) ok = mbar_wait(mbar_Z, j & 1, wl);
                 if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) { failed = true; break; }
                 load_v(j + 1);
             }
@@ -459,9 +462,11 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
         if (failed) {
             if (lane == 0) {
                 atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
+                // no copy may land in shared memory after the CTA has exited: wait for the phase of
+                // the last copy into each buffer (copy n into k/q buffer b completes phase n / kKQBuf)
                 for (int b = 0; b < kKQBuf; ++b)
-                    if (kq_pend & (1u << b)) { mbar_wait(&mbar_kq[b], 0, 400000000LL); mbar_wait(&mbar_kq[b], 1, 400000000LL); }
-                if (v_pend) { mbar_wait(mbar_v, 0, 400000000LL); mbar_wait(mbar_v, 1, 400000000LL); }
+                    if (last_kq[b] >= 0) mbar_wait(&mbar_kq[b], (last_kq[b] / kKQBuf) & 1, 400000000LL);
+                if (last_v >= 0) mbar_wait(mbar_v, last_v & 1, 400000000LL);
             }
             __syncwarp();
         }
@@ -470,7 +475,7 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
         // Lane 0 runs the whole loop alone; lanes 1-31 wait at the warp barrier after it. (A warp
         // that re-converges right after one lane has issued MMAs loses hundreds of cycles there.)
         auto wait1 = [&](uint64_t* bar, uint32_t parity) -> bool {
-            const bool ok = mbar_wait(bar, parity);
+            const bool ok = mbar_wait(bar, parity, wl);
             fence_after_sync();
             return ok;
         };
@@ -628,7 +633,7 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
                 const uint32_t lead = lane == 0;
                 mbar_arrive_if(rdy_S, lead);
                 // E(j) += S'^T Y^T onto Z(j) (issuer), once Z(j) is done and Y^T(j) is in place
-                if (mbar_wait(mbar_Z, j & 1) && mbar_wait(rdy_Yt, j & 1)) {
+                if (mbar_wait(mbar_Z, j & 1, wl) && mbar_wait(rdy_Yt, j & 1, wl)) {
                     fence_after_sync();
 #pragma unroll
                     for (int ks = 0; ks < FD / 16; ++ks)
@@ -717,7 +722,7 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
                 if (gt == 0) {
                     const long long t0 = clock64();
                     while (ld_acquire_shared(o_seen) < jj - 1) {
-                        if (clock64() - t0 > 4000000000LL) { ok = false; break; }
+                        if (clock64() - t0 > wl) { ok = false; break; }
                         __nanosleep(100);
                     }
                 }
@@ -848,7 +853,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // [rows][128] bf16 row-major, boxes of 64 columns x 64 rows, 128-byte swizzle.
-bool make_map(CUtensorMap* map, const void* base, uint64_t rows) {
+bool encode_map(CUtensorMap* map, const void* base, uint64_t rows) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {FD, rows};
@@ -859,6 +864,26 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t rows) {
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+// The same, from a small per-thread cache keyed on (pointer, rows): repeated calls on the same
+// buffers (a training loop, a benchmark, the host-buffer path's staging slots) encode nothing.
+bool make_map(CUtensorMap* map, const void* base, uint64_t rows) {
+    struct Entry { const void* base; uint64_t rows; CUtensorMap map; };
+    constexpr int kEntries = 16;
+    thread_local Entry cache[kEntries] = {};
+    thread_local int next = 0;
+    for (int i = 0; i < kEntries; ++i)
+        if (cache[i].base == base && cache[i].rows == rows) {
+            *map = cache[i].map;
+            return true;
+        }
+    if (!encode_map(map, base, rows)) return false;
+    cache[next] = Entry{base, rows, *map};
+    next = (next + 1) % kEntries;
+    return true;
+}
+
+std::atomic<uint64_t> g_fused_smem_set{0};
 
 }  // namespace
 
@@ -882,8 +907,8 @@ cudaError_t launch_fused(const Plan& pl, const void* q, const void* k, const voi
         if (!make_map(&mq, q, rows) || !make_map(&mk, k, rows) || !make_map(&mv, v, rows))
             return cudaErrorInvalidValue;
     }
-    cudaError_t e = cudaFuncSetAttribute(gdn_fused_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         GdnLayout::TOTAL);
+    cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(gdn_fused_head_kernel), GdnLayout::TOTAL,
+                                        g_fused_smem_set);
     if (e != cudaSuccess) return e;
     gdn_fused_head_kernel<<<(unsigned)pl.BH, FNT, GdnLayout::TOTAL, s>>>(pl, a, mq, mk, mv);
     return cudaGetLastError();

@@ -1,6 +1,7 @@
 // Internal declarations shared by the libdplr translation units (not part of the ABI).
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -24,6 +25,7 @@ struct Plan {
     int cw;                    // WY block length in tokens (two-stage path)
     int nb;                    // WY blocks per head = ceil(T / cw)
     int fused;                 // dplr_la_forward runs the fused per-head kernel
+    long long wait_cycles;     // limit (SM cycles) of a kernel's bounded waits on other roles
     size_t off_P, off_c, off_Q;
     size_t ws_stages;          // workspace of the two-stage entry points
     size_t ws_bytes;           // workspace of dplr_la_forward
@@ -46,6 +48,23 @@ struct ScanArgs {
 };
 
 dplr_status make_plan(const dplr_desc* d, Plan* plan);
+
+constexpr long long kDefaultWaitCycles = 4000000000LL;   // ~2 s at 2 GHz
+
+// Raises a kernel's dynamic shared-memory limit to `bytes` once per device: the attribute
+// belongs to the device's copy of the function, so later launches skip the driver call.
+// `done` holds one bit per device ordinal (64 devices at most).
+inline cudaError_t set_smem_limit_once(const void* func, int bytes, std::atomic<uint64_t>& done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    const uint64_t bit = uint64_t(1) << dev;
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
 size_t prep_smem_bytes(const Plan& pl);
 size_t scan_smem_bytes(const Plan& pl);
 cudaError_t launch_chunk_maps(const Plan& pl, const ChunkMapArgs& a, cudaStream_t s);

@@ -13,12 +13,20 @@
 // Host code cannot use the array's name as a device pointer (on the host it is a
 // stand-in symbol); its device address is looked up with cudaGetSymbolAddress
 // once per device, with that device current, on the first call made while the
-// device is current. Make that first call before any stream capture.
+// device is current. Make that first call before any stream capture. The library
+// is built without relocatable device code, so this file is a module of its own:
+// under CUDA's lazy module loading the array is reserved on a device only when that
+// first lookup loads the module. Callers that reserve a device's memory up front
+// therefore make one call (or a warm-up call) first. The address stays valid until
+// the device is reset; a reset (cudaDeviceReset) reloads the module elsewhere, and
+// this entry point must not be used on that device afterwards.
 //
 // Every call shares the one array and the array keeps the previous call's
-// contents. The forward needs nothing in it zeroed: stage 1 writes every map
-// before stage 2 reads it. Calls whose work overlaps on the GPU (two streams, or
-// two threads on one device) race on the array; serialise them.
+// contents. Its first 256 bytes are the device status word, which each call zeroes
+// on its stream before launching (a kernel sets it when a bounded wait gives up);
+// dplr_la_noalloc_status reads it. Nothing else needs zeroing: the kernels write
+// every map before they read it. Calls whose work overlaps on the GPU (two streams,
+// or two threads on one device) race on the array; serialise them.
 #include <mutex>
 
 #include "dplr_internal.h"
@@ -65,5 +73,21 @@ extern "C" dplr_status dplr_la_forward_noalloc(const dplr_desc* desc, const void
     if (pl.ws_bytes > kNoallocScratchBytes) return DPLR_ERR_UNSUPPORTED;   // problem too large for the array
     void* ws = nullptr;
     if (scratch_address(&ws) != cudaSuccess) return DPLR_ERR_CUDA;
+    // a fresh status word for this call (a memset allocates nothing)
+    if (cudaMemsetAsync(ws, 0, 256, static_cast<cudaStream_t>(stream)) != cudaSuccess) return DPLR_ERR_CUDA;
     return dplr_la_forward(desc, q, k, v, decay, beta, A, Bm, K, V, S0, o, S_T, ws, kNoallocScratchBytes, stream);
+}
+
+extern "C" dplr_status dplr_la_noalloc_status(int* status, void* stream) {
+    using namespace dplr;
+    if (status == nullptr) return DPLR_ERR_INVALID_ARG;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DPLR_ERR_CUDA;
+    void* ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_scratch_mu);
+        ws = g_scratch_addr[dev];
+    }
+    if (ws == nullptr) return DPLR_ERR_CUDA;   // no call has looked the array up on this device
+    return dplr_la_read_status(ws, kNoallocScratchBytes, 0, status, stream);
 }

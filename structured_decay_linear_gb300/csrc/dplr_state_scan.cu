@@ -170,7 +170,8 @@ size_t scan_smem_bytes(const Plan& pl) { return sizeof(float) * (size_t)ScanLayo
 cudaError_t launch_state_scan(const Plan& pl, const ScanArgs& a, cudaStream_t s) {
     const int nv = ScanLayout(pl.dk, pl.dv, pl.cw).nv;
     const size_t smem = scan_smem_bytes(pl);
-    cudaError_t e = cudaFuncSetAttribute(state_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static std::atomic<uint64_t> done{0};   // raised to the largest footprint once per device
+    cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(state_scan_kernel), 227 * 1024, done);
     if (e != cudaSuccess) return e;
     const long long grid = (long long)pl.BH * (pl.dv / nv);
     state_scan_kernel<<<(unsigned)grid, kScanThreads, smem, s>>>(pl, a);

@@ -67,6 +67,12 @@ def library() -> ctypes.CDLL:
             lib.dplr_la_state_scan.argtypes = [dp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
             lib.dplr_la_forward_noalloc.restype = ctypes.c_int
             lib.dplr_la_forward_noalloc.argtypes = [dp] + [_vp] * 12 + [_vp]
+            lib.dplr_la_set_wait_limit.restype = None
+            lib.dplr_la_set_wait_limit.argtypes = [ctypes.c_longlong]
+            lib.dplr_la_read_status.restype = ctypes.c_int
+            lib.dplr_la_read_status.argtypes = [_vp, ctypes.c_size_t, ctypes.c_int, ctypes.POINTER(ctypes.c_int), _vp]
+            lib.dplr_la_noalloc_status.restype = ctypes.c_int
+            lib.dplr_la_noalloc_status.argtypes = [ctypes.POINTER(ctypes.c_int), _vp]
             lib.dplr_la_host_workspace_size.restype = ctypes.c_size_t
             lib.dplr_la_host_workspace_size.argtypes = [dp, ctypes.c_int, ctypes.c_int]
             lib.dplr_la_forward_host.restype = ctypes.c_int
@@ -125,6 +131,26 @@ def dplr_la_forward_noalloc(desc, q, k, v, decay, beta, A, Bm, K, V, S0, o, S_T,
     """dplr_la_forward with scratch from the library's fixed device array (no workspace argument)."""
     return int(library().dplr_la_forward_noalloc(ctypes.byref(desc), q, k, v, decay, beta, A, Bm, K, V, S0, o,
                                                  S_T, stream))
+
+
+def dplr_la_set_wait_limit(cycles: int) -> None:
+    """Limit (SM cycles) of the kernels' bounded device-side waits; <= 0 restores the default."""
+    library().dplr_la_set_wait_limit(int(cycles))
+
+
+def dplr_la_read_status(workspace, ws_bytes, clear, stream) -> Tuple[int, int]:
+    """Synchronous read of a workspace's device status word: (call status, word)."""
+    word = ctypes.c_int(-1)
+    st = int(library().dplr_la_read_status(workspace, ctypes.c_size_t(ws_bytes), int(clear), ctypes.byref(word),
+                                           stream))
+    return st, int(word.value)
+
+
+def dplr_la_noalloc_status(stream) -> Tuple[int, int]:
+    """Synchronous read of the no-alloc scratch array's status word: (call status, word)."""
+    word = ctypes.c_int(-1)
+    st = int(library().dplr_la_noalloc_status(ctypes.byref(word), stream))
+    return st, int(word.value)
 
 
 def dplr_la_host_workspace_size(desc, groups: int, slots: int) -> int:
@@ -224,9 +250,14 @@ class Forward:
             raise DplrError(st, "dplr_la_forward")
         return self.o, self.S_T
 
-    def device_status(self) -> int:
-        """The device status word of the fused path (0, or DPLR_ERR_TIMEOUT after a bounded wait gave up)."""
-        return int(self.workspace[:4].view(torch.int32).item())
+    def device_status(self, clear: bool = False) -> int:
+        """The workspace's device status word (0, or DPLR_ERR_TIMEOUT after a bounded wait gave up),
+        read synchronously through dplr_la_read_status."""
+        s = torch.cuda.current_stream(self.device)
+        st, word = dplr_la_read_status(_ptr(self.workspace), self.workspace.numel(), clear, s.cuda_stream)
+        if st != DPLR_OK:
+            raise DplrError(st, "dplr_la_read_status")
+        return word
 
     def _stage_workspace(self):
         if self._stage_ws is None:

@@ -69,11 +69,17 @@ def test_noalloc_matches_forward_on_two_calls_in_a_row(sdl):
         inp, dt, args = _case(w, heads, T)
         ref = sdl.Forward(w.mode, dt, 1, heads, T, w.dk, w.dv)
         o_ref, S_ref = [x.clone() for x in ref(**args)]
-        for _ in range(2):   # two calls in a row reuse the same scratch array
+        for call in range(2):   # two calls in a row reuse the same scratch array
             o = torch.full_like(o_ref, float("nan"))
             ST = torch.full_like(S_ref, float("nan"))
+            torch.cuda.synchronize()
+            free_before = torch.cuda.mem_get_info()[0]
             assert _noalloc(sdl, ref.desc, args, o, ST) == sdl.DPLR_OK
             torch.cuda.synchronize()
+            if call == 1:   # the array is reserved by the first call on the device; later calls take nothing
+                assert torch.cuda.mem_get_info()[0] == free_before
+            st, word = sdl.dplr_la_noalloc_status(torch.cuda.current_stream().cuda_stream)
+            assert st == sdl.DPLR_OK and word == sdl.DPLR_OK
             assert _rel(o, o_ref) <= TAU[w.dtype]
             assert _rel(ST, S_ref) <= TAU[w.dtype]
 
