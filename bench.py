@@ -373,6 +373,8 @@ def run_ours(args, w):
         peaks, peak_kind = load_peaks()
         if fused:
             kern = [("dplr_fused_head", sum(k1) / K)]
+        elif f.path == "hdla_tcgen05":
+            kern = [("hdla_chunk_kernel", sum(k1) / K), ("hdla_chain_kernel", sum(k2) / K)]
         else:
             kern = [("dplr_chunk_maps", sum(k1) / K), ("dplr_state_scan", sum(k2) / K)]
         dom_name, dom_ms = max(kern, key=lambda x: x[1])
@@ -393,8 +395,11 @@ def run_ours(args, w):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "bf16" if fused else "f32",          # arithmetic of the path's products
+            # arithmetic of the path's products: bf16 tensor-core operands (fp32 accumulation and state;
+            # bf16 hi + lo pairs where one term is too coarse) or fp32 on the CUDA cores
+            "dtype": "f32" if f.path == "two_stage_fp32" else "bf16",
             "input_dtype": w.dtype,                        # storage type of q, k, v (A, B, K, V)
+            "path": f.path,
             "data": "synthetic (seeded workload recipe, resident in HBM)",
             "config": {"workload": w.name, "mode": w.mode, "B": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv,
                        "r_ab": w.r_ab, "r_kv": w.r_kv, "chunk": w.chunk, "in_dtype": w.dtype,

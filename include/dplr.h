@@ -162,6 +162,14 @@ DPLR_API dplr_status dplr_la_read_status(const void* workspace, size_t ws_bytes,
  * path; a small limit makes correct launches give up too. */
 DPLR_API void dplr_la_set_wait_limit(long long cycles);
 
+/* Name of the kernel path that dplr_la_forward runs for `desc` (no counterpart in the
+ * paper; static storage): "gdn_fused_tcgen05" (GDN, bf16, dk = dv = 128: one fused
+ * per-head kernel on the tensor cores), "hdla_tcgen05" (HDLA, bf16, dk = dv = 128: the
+ * chunk-map and chain kernels on the tensor cores), "two_stage_fp32" (every other case:
+ * the chunk-map and state-scan kernels in fp32 on the CUDA cores), or "" if `desc` is
+ * invalid or unsupported. */
+DPLR_API const char* dplr_la_path(const dplr_desc* desc);
+
 /* Human-readable name of a status code (static storage). */
 DPLR_API const char* dplr_status_string(dplr_status status);
 

@@ -1,5 +1,8 @@
 // Host side of the libdplr C ABI: descriptor validation, workspace plan, launches.
+#include <cudaTypedefs.h>
+
 #include <cstring>
+#include <mutex>
 
 #include "dplr_internal.h"
 
@@ -24,7 +27,56 @@ int wy_block(int chunk, int r, int p) {
     return cw;
 }
 
+// cuTensorMapEncodeTiled from the driver (looked up once).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool encode_map_2d(CUtensorMap* map, const void* base, bool bf16, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                   uint32_t box_cols) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const uint64_t esize = bf16 ? 2 : 4;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * esize};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base),
+              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
+
+bool tensor_map_2d(CUtensorMap* map, const void* base, bool bf16, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                   uint32_t box_cols) {
+    struct Entry { const void* base; uint64_t rows, cols; uint32_t br, bc; bool bf16; CUtensorMap map; };
+    constexpr int kEntries = 32;
+    thread_local Entry cache[kEntries] = {};
+    thread_local int next = 0;
+    for (int i = 0; i < kEntries; ++i) {
+        const Entry& e = cache[i];
+        if (e.base == base && e.rows == rows && e.cols == cols && e.br == box_rows && e.bc == box_cols &&
+            e.bf16 == bf16) {
+            *map = e.map;
+            return true;
+        }
+    }
+    if (!encode_map_2d(map, base, bf16, rows, cols, box_rows, box_cols)) return false;
+    cache[next] = Entry{base, rows, cols, box_rows, box_cols, bf16, *map};
+    next = (next + 1) % kEntries;
+    return true;
+}
 
 dplr_status make_plan(const dplr_desc* d, Plan* pl) {
     if (!d) return DPLR_ERR_INVALID_ARG;
@@ -51,16 +103,29 @@ dplr_status make_plan(const dplr_desc* d, Plan* pl) {
     p.p = d->mode == DPLR_GENERIC ? d->r_kv : 0;
     p.cw = wy_block(d->chunk, p.r, p.p);
     p.nb = (d->T + p.cw - 1) / p.cw;
-    const size_t units = (size_t)p.BH * p.nb;
-    size_t off = kAlign;   // the first 256 bytes hold the device status word
-    p.off_P = off; off = round_up(off + units * (size_t)p.dk * p.dk * sizeof(float));
-    p.off_c = off; off = round_up(off + units * (size_t)p.dk * p.dv * sizeof(float));
-    p.off_Q = off; off = round_up(off + units * (size_t)p.cw * p.dk * sizeof(float));
-    p.ws_stages = off;
     p.fused = fused_supported(p) ? 1 : 0;
+    p.tc = (!p.fused && hdla_tc_supported(p)) ? 1 : 0;
     p.wait_cycles = g_wait_cycles.load(std::memory_order_relaxed);
-    p.ws_bytes = p.fused ? kAlign : p.ws_stages;   // fused: the status word alone
-    if (prep_smem_bytes(p) > 227 * 1024 || scan_smem_bytes(p) > 227 * 1024) return DPLR_ERR_UNSUPPORTED;
+    if (p.tc) {
+        // one unit per (head, 64-token chunk): P_j has 128 rows, addressed as int by the copies
+        const long long rows = bh * (long long)((d->T + 63) / 64) * 128;
+        if (rows >= (1LL << 31)) return DPLR_ERR_UNSUPPORTED;
+        p.cw = 64;
+        p.nb = (d->T + 63) / 64;
+        size_t total = 0;
+        hdla_tc_offsets(p, &p.off_P, &p.off_c, &p.off_Q, &total);
+        p.ws_stages = total;
+        p.ws_bytes = total;
+    } else {
+        const size_t units = (size_t)p.BH * p.nb;
+        size_t off = kAlign;   // the first 256 bytes hold the device status word
+        p.off_P = off; off = round_up(off + units * (size_t)p.dk * p.dk * sizeof(float));
+        p.off_c = off; off = round_up(off + units * (size_t)p.dk * p.dv * sizeof(float));
+        p.off_Q = off; off = round_up(off + units * (size_t)p.cw * p.dk * sizeof(float));
+        p.ws_stages = off;
+        p.ws_bytes = p.fused ? kAlign : p.ws_stages;   // fused: the status word alone
+        if (prep_smem_bytes(p) > 227 * 1024 || scan_smem_bytes(p) > 227 * 1024) return DPLR_ERR_UNSUPPORTED;
+    }
     *pl = p;
     return DPLR_OK;
 }
@@ -152,6 +217,11 @@ dplr_status dplr_la_chunk_maps(const dplr_desc* desc, const void* q, const void*
     if (st != DPLR_OK) return st;
     if ((st = check_inputs(pl, q, k, v, decay, beta, A, Bm, K, V, o)) != DPLR_OK) return st;
     if ((st = check_workspace(pl.ws_stages, workspace, ws_bytes)) != DPLR_OK) return st;
+    if (pl.tc) {
+        if (launch_hdla_chunks(pl, q, k, v, decay, beta, o, workspace, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return DPLR_ERR_CUDA;
+        return DPLR_OK;
+    }
     const ChunkMapArgs a = map_args(pl, q, k, v, decay, beta, A, Bm, K, V, o, workspace);
     if (launch_chunk_maps(pl, a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return DPLR_ERR_CUDA;
     return DPLR_OK;
@@ -165,6 +235,11 @@ dplr_status dplr_la_state_scan(const dplr_desc* desc, const float* S0, float* o,
     if ((S0 && !aligned16(S0)) || (S_T && !aligned16(S_T))) return DPLR_ERR_INVALID_ARG;
     if (pl.T > 0 && (!o || !aligned16(o))) return DPLR_ERR_INVALID_ARG;
     if ((st = check_workspace(pl.ws_stages, workspace, ws_bytes)) != DPLR_OK) return st;
+    if (pl.tc) {
+        if (launch_hdla_chain(pl, S0, o, S_T, workspace, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return DPLR_ERR_CUDA;
+        return DPLR_OK;
+    }
     const ScanArgs a = scan_args(pl, S0, o, S_T, workspace);
     if (launch_state_scan(pl, a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return DPLR_ERR_CUDA;
     return DPLR_OK;
@@ -186,10 +261,23 @@ dplr_status dplr_la_forward(const dplr_desc* desc, const void* q, const void* k,
             return DPLR_ERR_CUDA;
         return DPLR_OK;
     }
+    if (pl.tc) {
+        if (launch_hdla_chunks(pl, q, k, v, decay, beta, o, workspace, s) != cudaSuccess) return DPLR_ERR_CUDA;
+        if (launch_hdla_chain(pl, S0, o, S_T, workspace, s) != cudaSuccess) return DPLR_ERR_CUDA;
+        return DPLR_OK;
+    }
     if (launch_chunk_maps(pl, map_args(pl, q, k, v, decay, beta, A, Bm, K, V, o, workspace), s) != cudaSuccess)
         return DPLR_ERR_CUDA;
     if (launch_state_scan(pl, scan_args(pl, S0, o, S_T, workspace), s) != cudaSuccess) return DPLR_ERR_CUDA;
     return DPLR_OK;
+}
+
+const char* dplr_la_path(const dplr_desc* desc) {
+    Plan pl;
+    if (make_plan(desc, &pl) != DPLR_OK) return "";
+    if (pl.fused) return "gdn_fused_tcgen05";
+    if (pl.tc) return "hdla_tcgen05";
+    return "two_stage_fp32";
 }
 
 void dplr_la_set_wait_limit(long long cycles) {

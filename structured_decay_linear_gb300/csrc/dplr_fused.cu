@@ -48,10 +48,7 @@
 //   RBM (row-block major, C columns): (r, c) -> (r/8)*C*16 + (c/8)*128 + (r%8)*16 + (c%8)*2
 // (8x8 core matrices of 16-byte rows), whose 16-byte rows of a warp land in distinct bank
 // groups; it too serves either major order through LBO/SBO, so no tile is ever transposed.
-#include <cudaTypedefs.h>
-
 #include <cstring>
-#include <mutex>
 
 #include "dplr_internal.h"
 #include "sm100_ops.cuh"
@@ -167,32 +164,6 @@ __device__ __forceinline__ void rbm_store8_split(uint32_t th, uint32_t tl, int c
 __device__ __forceinline__ float4 lds4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 
 constexpr int kLds = 36;   // row stride (floats) of the merge scratch (32 rows)
-
-// Warp-level C[16x8] = A[16xK] * B[Kx8] with fp32 operands read as tf32 (mma.sync m16n8k8, fp32
-// accumulate); A and B row-major in shared memory with row strides lda / ldb. Fragment layout of
-// the PTX ISA: g = lane / 4, q = lane % 4; A (g, q), (g+8, q), (g, q+4), (g+8, q+4); B (q, g),
-// (q+4, g); C (g, 2q), (g, 2q+1), (g+8, 2q), (g+8, 2q+1).
-__device__ __forceinline__ void warp_mma_tf32(const float* A, int lda, const float* B, int ldb, int K, float (&c)[4]) {
-    const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
-    c[0] = c[1] = c[2] = c[3] = 0.f;
-    for (int k0 = 0; k0 < K; k0 += 8) {
-        const uint32_t a0 = __float_as_uint(A[g * lda + k0 + q]), a1 = __float_as_uint(A[(g + 8) * lda + k0 + q]);
-        const uint32_t a2 = __float_as_uint(A[g * lda + k0 + q + 4]), a3 = __float_as_uint(A[(g + 8) * lda + k0 + q + 4]);
-        const uint32_t b0 = __float_as_uint(B[(k0 + q) * ldb + g]), b1 = __float_as_uint(B[(k0 + q + 4) * ldb + g]);
-        asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-                     "{%0,%1,%2,%3};"
-                     : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-                     : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-    }
-}
-
-__device__ __forceinline__ void store_tile_16x8(float* C, int ldc, const float (&c)[4], float scale) {
-    const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
-    C[g * ldc + 2 * q] = scale * c[0];
-    C[g * ldc + 2 * q + 1] = scale * c[1];
-    C[(g + 8) * ldc + 2 * q] = scale * c[2];
-    C[(g + 8) * ldc + 2 * q + 1] = scale * c[3];
-}
 
 // (I + L)^{-1} for a 64x64 strictly lower-triangular fp32 L (row stride kLdL = 68 floats, so
 // rows are 16-byte aligned), by the 128 threads of group B (t = 0..127, named barrier kBarB).
@@ -837,50 +808,9 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-// ---- host side: tensor maps (driver entry point looked up once)
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
 // [rows][128] bf16 row-major, boxes of 64 columns x 64 rows, 128-byte swizzle.
-bool encode_map(CUtensorMap* map, const void* base, uint64_t rows) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {FD, rows};
-    cuuint64_t strides[1] = {FD * 2};
-    cuuint32_t box[2] = {64, FC};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// The same, from a small per-thread cache keyed on (pointer, rows): repeated calls on the same
-// buffers (a training loop, a benchmark, the host-buffer path's staging slots) encode nothing.
 bool make_map(CUtensorMap* map, const void* base, uint64_t rows) {
-    struct Entry { const void* base; uint64_t rows; CUtensorMap map; };
-    constexpr int kEntries = 16;
-    thread_local Entry cache[kEntries] = {};
-    thread_local int next = 0;
-    for (int i = 0; i < kEntries; ++i)
-        if (cache[i].base == base && cache[i].rows == rows) {
-            *map = cache[i].map;
-            return true;
-        }
-    if (!encode_map(map, base, rows)) return false;
-    cache[next] = Entry{base, rows, *map};
-    next = (next + 1) % kEntries;
-    return true;
+    return tensor_map_2d(map, base, true, rows, FD, FC, 64);
 }
 
 std::atomic<uint64_t> g_fused_smem_set{0};

@@ -1,0 +1,1032 @@
+// HDLA (rank-2 decay P_t = (I - b k k^T) Diag(lambda_t) (I - b k k^T), write b k v^T) with bf16
+// inputs and dk = dv = 128, on the tensor cores: the two-stage chunkwise algorithm of
+// "Householder-Diagonalized Linear Attention" (Key design 3) with both stages on tcgen05.
+//
+// Stage 1, hdla_chunk_kernel: one CTA per (head, chunk of C = 64 tokens), all chunks in parallel.
+// With G_t the inclusive cumulative log-decay of the chunk (one value per key channel), anchor
+// a = G_C / 2, F_t = e^{G_t - a}, R_t = e^{a - G_t} (elementwise over channels) and the rank-2
+// factors A_t = [k, Lambda k], B_t = [b Lambda k - b^2 (k^T Lambda k) k, b k] (Key design 2, written
+// as D - A B^T), the chunk's rows s = 2t + i are
+//
+//   A~_{2t} = R_t k_t,  A~_{2t+1} = R_{t-1} k_t            (e^{-(G_t - a)} A_t; R_t lambda_t = R_{t-1})
+//   B~_{2t} = b F_t k_t - b^2 c_t F_{t-1} k_t,  B~_{2t+1} = b F_{t-1} k_t   (e^{G_{t-1} - a} B_t)
+//   Q~_t = F_t q_t,   c_t = k_t^T Lambda_t k_t
+//
+// and the chunk's exact maps follow from the UT/WY transform with the block operator that treats
+// every token's 2 x 2 block as one element:
+//
+//   L   = strict_block_tril(B~ A~^T)            M = (I + L)^{-1}
+//   Y   = M B~,  MW = M W  (W_{2t} = b_t v_t, W_{2t+1} = 0)
+//   P_j = Diag(e^{G_C}) - Diag(e^a) (A~^T Y) Diag(e^a)      S_j = P_j S_{j-1} + c_j
+//   c_j = Diag(e^a) A~^T MW
+//   QA  = tril_incl(Q~ A~^T)   Q'_j = (Q~ - QA Y) Diag(e^a)   O_j = QA MW      o_t = Q'_t S_{j-1} + O_t
+//
+// The products run on tcgen05 (kind::f16, fp32 accumulators in tensor memory). Operands whose
+// bf16 rounding alone would cost more than the output tolerance are split into two bf16 terms
+// x = hi + lo (A~ and Q~ in QA and c, M in MW, MW and QA in O): a float64 emulation of these
+// rounding points over the benchmark's distributions gives max |err| / RMS = 4.2e-3 for o, while a
+// single bf16 term everywhere gives 4.2e-2. L, Y, P_j and QA Y tolerate one term. The inverse is
+// fp32: 16 x 16 diagonal blocks by substitution, merged 16 -> 32 -> 64 -> 128 with warp-level tf32
+// products. Stage 1 writes P_j (bf16), c_j (fp32) and Q'_j (bf16 hi and lo) to the workspace and
+// O_j into o.
+//
+// Stage 2, hdla_chain_kernel: one CTA per (head, 32 state columns). It walks the chunks in order,
+// S_j = P_j S_{j-1} + c_j with P_j as one bf16 term and S_{j-1} as bf16 hi + lo (the decay makes
+// P_j contracting, so its rounding does not accumulate from chunk to chunk), and o_t += Q'_t S_{j-1}
+// with both operands split into bf16 hi + lo (three terms).
+// The state stays in registers in fp32; P_j and Q'_j arrive by TMA two chunks ahead.
+//
+// Every wait is bounded by Plan::wait_cycles; a wait that gives up sets DPLR_ERR_TIMEOUT in the
+// status word and the kernel drains its own copies and products before it frees tensor memory.
+#include <cuda_bf16.h>
+
+#include <cstring>
+
+#include "dplr_internal.h"
+#include "sm100_ops.cuh"
+
+namespace dplr {
+namespace {
+
+using namespace sm100;
+
+constexpr int HD = 128;    // dk = dv
+constexpr int HCK = 64;    // tokens per chunk
+constexpr int K1T = 256;   // threads of the chunk kernel: two threads per tensor-memory lane
+constexpr int kLdX = 68;   // row stride (floats) of the inverse's fp32 blocks (16-byte rows, 4 banks apart)
+
+// ---- 128-byte-swizzled tiles (the layout the TMA writes with SWIZZLE_128B): rows of 128 bytes whose
+// 16-byte chunks are permuted by XOR with the row index mod 8. A bf16 [R][128] tile is two half-tiles
+// (columns 0-63, 64-127) of R rows; an fp32 [R][128] tile is four column boxes of 32.
+__device__ __forceinline__ uint32_t swz(int r, int chunk) { return (uint32_t)(r * 128 + (((chunk) ^ (r & 7)) << 4)); }
+__device__ __forceinline__ uint32_t sw_bf16(int r, int c, int R) {
+    return (uint32_t)((c >> 6) * (R * 128)) + swz(r, (c & 63) >> 3) + (uint32_t)((c & 7) << 1);
+}
+__device__ __forceinline__ uint32_t sw_f32(int r, int c, int R) {
+    return (uint32_t)((c >> 5) * (R * 128)) + swz(r, (c & 31) >> 2) + (uint32_t)((c & 3) << 2);
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ void sts16(uint32_t addr, uint16_t v) {
+    asm volatile("st.shared.b16 [%0], %1;" :: "r"(addr), "h"(v) : "memory");
+}
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ float lds_bf16(uint32_t addr) {
+    uint16_t v;
+    asm volatile("ld.shared.b16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return __uint_as_float(static_cast<uint32_t>(v) << 16);
+}
+__device__ __forceinline__ uint16_t bf16_bits(float x) {
+    __nv_bfloat16 h = __float2bfloat16_rn(x);
+    return *reinterpret_cast<uint16_t*>(&h);
+}
+__device__ __forceinline__ float bf16_value(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
+__device__ __forceinline__ float tf32_rn(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
+// x = hi + lo with both parts bf16 (scalar): the pair of bit patterns.
+__device__ __forceinline__ void split1(float x, uint16_t& h, uint16_t& l) {
+    h = bf16_bits(x);
+    l = bf16_bits(x - bf16_value(h));
+}
+// x = hi + lo for a pair of values, packed (element 0 in the low half).
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& h, uint32_t& l) {
+    h = pack_bf16(x0, x1);
+    l = pack_bf16(x0 - __uint_as_float(h << 16), x1 - __uint_as_float(h & 0xFFFF0000u));
+}
+
+// MMAs issued by lane 0 of a converged warp through a predicate (no divergence, so no costly
+// re-convergence after the issue).
+__device__ __forceinline__ void mma_ss_if(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc, uint32_t issue) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(issue));
+}
+__device__ __forceinline__ void mma_ts_if(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc,
+                                          uint32_t issue) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        :: "r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc), "r"(issue));
+}
+__device__ __forceinline__ void commit_if(uint64_t* mbar, uint32_t issue) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
+        "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
+        :: "r"(smem_addr(mbar)), "r"(issue) : "memory");
+}
+__device__ __forceinline__ uint64_t dadd(uint64_t desc, uint32_t bytes) { return desc + static_cast<uint64_t>(bytes >> 4); }
+
+// Warp-level C[16x8] = A[16xK] B[Kx8] (mma.sync m16n8k8 tf32, fp32 accumulate) with the operands
+// rounded to tf32 (cvt.rna); A, B row-major fp32 in shared memory. Fragments as in the PTX ISA.
+__device__ __forceinline__ void warp_mma_tf32_rn(const float* A, int lda, const float* B, int ldb, int K, float (&c)[4]) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+    c[0] = c[1] = c[2] = c[3] = 0.f;
+    for (int k0 = 0; k0 < K; k0 += 8) {
+        const uint32_t a0 = __float_as_uint(tf32_rn(A[g * lda + k0 + q]));
+        const uint32_t a1 = __float_as_uint(tf32_rn(A[(g + 8) * lda + k0 + q]));
+        const uint32_t a2 = __float_as_uint(tf32_rn(A[g * lda + k0 + q + 4]));
+        const uint32_t a3 = __float_as_uint(tf32_rn(A[(g + 8) * lda + k0 + q + 4]));
+        const uint32_t b0 = __float_as_uint(tf32_rn(B[(k0 + q) * ldb + g]));
+        const uint32_t b1 = __float_as_uint(tf32_rn(B[(k0 + q + 4) * ldb + g]));
+        asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                     "{%0,%1,%2,%3};"
+                     : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                     : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+}
+
+// In place, for the 128 threads t of one group (named barrier `bar`): X (64 x 64, row stride kLdX)
+// holds a strictly lower-triangular L on entry (zeros on and above the diagonal) and
+// M = (I + L)^{-1} on exit. Diagonal 16 x 16 blocks by substitution (one column per thread), then
+// the block merges [[A,0],[C,B]]^{-1} = [[A^{-1},0],[-B^{-1} C A^{-1}, B^{-1}]] for 16 -> 32 -> 64,
+// each product formed in registers and written over C once every warp has read C.
+__device__ void inv64_inplace(float* X, int t, uint32_t bar) {
+    const int w = t >> 5;
+    if (t < 64) {
+        const int b = t >> 4, jj = t & 15, o = 16 * b;
+        float m[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float* Lr = X + (o + i) * kLdX + o;
+            float acc0 = (i == jj) ? 1.f : 0.f, acc1 = 0.f;
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+                if (4 * k4 < i) {
+                    const float4 l = *reinterpret_cast<const float4*>(Lr + 4 * k4);
+                    if (4 * k4 + 0 < i) acc0 = fmaf(-l.x, m[4 * k4 + 0], acc0);
+                    if (4 * k4 + 1 < i) acc1 = fmaf(-l.y, m[4 * k4 + 1], acc1);
+                    if (4 * k4 + 2 < i) acc0 = fmaf(-l.z, m[4 * k4 + 2], acc0);
+                    if (4 * k4 + 3 < i) acc1 = fmaf(-l.w, m[4 * k4 + 3], acc1);
+                }
+            }
+            m[i] = acc0 + acc1;
+        }
+        named_sync(bar, 128);   // every row of the diagonal blocks read
+#pragma unroll
+        for (int i = 0; i < 16; ++i) X[(o + i) * kLdX + o + jj] = m[i];
+    } else {
+        named_sync(bar, 128);
+    }
+    named_sync(bar, 128);
+    {   // 16 -> 32 for the pairs of diagonal blocks (0,1) and (2,3): one 16 x 8 tile per warp
+        const int p = w >> 1, ct = w & 1, o = 32 * p;
+        float c[4];
+        warp_mma_tf32_rn(X + (o + 16) * kLdX + o, kLdX, X + o * kLdX + o + 8 * ct, kLdX, 16, c);   // T = C A^{-1}
+        named_sync(bar, 128);
+        store_tile_16x8(X + (o + 16) * kLdX + o + 8 * ct, kLdX, c, 1.f);
+        named_sync(bar, 128);
+        warp_mma_tf32_rn(X + (o + 16) * kLdX + o + 16, kLdX, X + (o + 16) * kLdX + o + 8 * ct, kLdX, 16, c);   // B^{-1} T
+        named_sync(bar, 128);
+        store_tile_16x8(X + (o + 16) * kLdX + o + 8 * ct, kLdX, c, -1.f);
+        named_sync(bar, 128);
+    }
+    {   // 32 -> 64: rows 32-63, columns 0-31; two 16 x 8 tiles per warp (column block 8w)
+        float c0[4], c1[4];
+        warp_mma_tf32_rn(X + 32 * kLdX, kLdX, X + 8 * w, kLdX, 32, c0);
+        warp_mma_tf32_rn(X + 48 * kLdX, kLdX, X + 8 * w, kLdX, 32, c1);
+        named_sync(bar, 128);
+        store_tile_16x8(X + 32 * kLdX + 8 * w, kLdX, c0, 1.f);
+        store_tile_16x8(X + 48 * kLdX + 8 * w, kLdX, c1, 1.f);
+        named_sync(bar, 128);
+        warp_mma_tf32_rn(X + 32 * kLdX + 32, kLdX, X + 32 * kLdX + 8 * w, kLdX, 32, c0);
+        warp_mma_tf32_rn(X + 48 * kLdX + 32, kLdX, X + 32 * kLdX + 8 * w, kLdX, 32, c1);
+        named_sync(bar, 128);
+        store_tile_16x8(X + 32 * kLdX + 8 * w, kLdX, c0, -1.f);
+        store_tile_16x8(X + 48 * kLdX + 8 * w, kLdX, c1, -1.f);
+        named_sync(bar, 128);
+    }
+}
+
+// ================================================================================================
+// Stage 1: chunk maps
+// ================================================================================================
+
+// Shared memory (bytes from the 1024-aligned base).
+struct K1Smem {
+    static constexpr int A_HI = 0;                // A~ hi: bf16 [128][128], swizzled
+    static constexpr int A_LO = A_HI + 32768;     // A~ lo
+    static constexpr int BT = A_LO + 32768;       // B~ (bf16); later Y
+    static constexpr int Q_HI = BT + 32768;       // Q~ hi: bf16 [64][128]
+    static constexpr int Q_LO = Q_HI + 16384;     // Q~ lo
+    static constexpr int V = Q_LO + 16384;        // v: bf16 [64][128] (TMA); later QA hi [128][64]
+    static constexpr int R0 = V + 16384;          // 64 KB shared by, in turn:
+    static constexpr int K_ = R0;                 //   k [64][128] bf16 (TMA)
+    static constexpr int Q_ = R0 + 16384;         //   q [64][128] bf16 (TMA)
+    static constexpr int LAM = R0 + 32768;        //   log lambda [64][128] fp32 (TMA)
+    static constexpr int X22 = R0 + 128 * kLdX * 4;  //   the inverse's fp32 blocks X11, X21, X22 (64 x kLdX each)
+    static constexpr int MB_HI = R0;              //   M Diag(beta) restricted to the even columns, hi / lo:
+    static constexpr int MB_LO = R0 + 16384;      //   bf16 [128][64]
+    static constexpr int QA_LO = R0 + 32768;      //   QA^T lo: bf16 [128][64]
+    static constexpr int VEC = R0 + 65536;        // fp32 vectors (see below)
+    static constexpr int BAR = VEC + 4096;        // mbarriers and the tensor-memory address
+    static constexpr int TOTAL = BAR + 64;
+};
+static_assert(K1Smem::X22 + 64 * kLdX * 4 <= K1Smem::R0 + 65536, "inverse blocks fit the shared region");
+static_assert(K1Smem::TOTAL <= 227 * 1024, "shared memory budget");
+
+// Tensor-memory columns of the chunk kernel (512 allocated).
+constexpr uint32_t TL = 0;       // L, then Y, then the product A~^T Y                 128
+constexpr uint32_t TQA = 128;    // QA^T (lane s, column t), then O^T = (QA MW)^T          64
+constexpr uint32_t TM = 192;     // M as a bf16 A operand, then Zq = (QA Y)^T             64
+constexpr uint32_t TMW = 256;    // MW^T (lane n, column s), then c^T                      128
+constexpr uint32_t TMWH = 384;   // MW^T hi (bf16 A operand)                               64
+constexpr uint32_t TMWL = 448;   // MW^T lo                                                 64
+
+struct K1Args {
+    const __nv_bfloat16* q; const __nv_bfloat16* k; const __nv_bfloat16* v;
+    const float* decay; const float* beta;
+    float* o; __nv_bfloat16* P; float* Cm; __nv_bfloat16* Qm; int* status;
+};
+
+__global__ void __launch_bounds__(K1T, 1)
+hdla_chunk_kernel(Plan pl, K1Args args, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_l) {
+    using S = K1Smem;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const uint32_t sb = smem_addr(smem);
+    if (sb & 1023u) {   // the swizzled tiles need 1024-byte alignment
+        if (threadIdx.x == 0) atomicExch(args.status, (int)DPLR_ERR_CUDA);
+        return;
+    }
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::BAR);
+    uint64_t* mb_tma = bars + 0;
+    uint64_t* mb_mma = bars + 1;
+    uint64_t* mb_drain = bars + 2;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3);
+    float* vec = reinterpret_cast<float*>(smem + S::VEC);
+    float* cdot = vec;          // [64]  k_t^T Lambda_t k_t
+    float* betav = vec + 64;    // [64]
+    float* ea = vec + 128;      // [128] e^{a}
+    float* gam = vec + 256;     // [128] e^{G_C}
+    float* gh = vec + 384;      // [128] G after token 31
+    float* av = vec + 512;      // [128] a = G_C / 2
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int NC = (pl.T + HCK - 1) / HCK;
+    const int j = blockIdx.x % NC;
+    const size_t bh = blockIdx.x / NC;
+    const int valid = min(HCK, pl.T - j * HCK);
+    const size_t tok0 = bh * (size_t)pl.T + (size_t)j * HCK;
+    const size_t unit = bh * (size_t)NC + j;
+    const long long wl = pl.wait_cycles;
+    const bool full = valid == HCK;
+
+    if (tid == 0) {
+        mbar_init(mb_tma, 1);
+        mbar_init(mb_mma, 1);
+        mbar_init(mb_drain, 1);
+        mbar_fence_init();
+    }
+    if (warp == 0) tmem_alloc(tmem_holder, 512);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tmem_holder;
+    uint32_t mma_phase = 0;   // phases of mb_mma completed so far
+    bool failed = false;
+
+    // ---- a1: stage k, q, v and the log-decay of the chunk (TMA; plain loads for a ragged chunk)
+    if (full) {
+        if (tid == 0) {
+            mbar_expect_tx(mb_tma, 3 * 16384 + 32768);
+            const int y = static_cast<int>(tok0);
+            for (int h = 0; h < 2; ++h) {
+                tma_load_2d(smem + S::K_ + h * 8192, &tm_k, 64 * h, y, mb_tma);
+                tma_load_2d(smem + S::Q_ + h * 8192, &tm_q, 64 * h, y, mb_tma);
+                tma_load_2d(smem + S::V + h * 8192, &tm_v, 64 * h, y, mb_tma);
+            }
+            for (int b = 0; b < 4; ++b) tma_load_2d(smem + S::LAM + b * 8192, &tm_l, 32 * b, y, mb_tma);
+        }
+    } else {   // identity padding past the end: k = q = v = 0, log-decay 0, beta 0
+        for (int i = tid; i < HCK * 16; i += K1T) {
+            const int t = i >> 4, cb = i & 15;
+            uint4 zk = make_uint4(0, 0, 0, 0), zq = zk, zv = zk;
+            if (t < valid) {
+                const size_t g = (tok0 + t) * HD + 8 * cb;
+                zk = *reinterpret_cast<const uint4*>(args.k + g);
+                zq = *reinterpret_cast<const uint4*>(args.q + g);
+                zv = *reinterpret_cast<const uint4*>(args.v + g);
+            }
+            const uint32_t off = (uint32_t)((cb >> 3) * 8192) + swz(t, cb & 7);
+            sts128(sb + S::K_ + off, zk.x, zk.y, zk.z, zk.w);
+            sts128(sb + S::Q_ + off, zq.x, zq.y, zq.z, zq.w);
+            sts128(sb + S::V + off, zv.x, zv.y, zv.z, zv.w);
+        }
+        for (int i = tid; i < HCK * 32; i += K1T) {
+            const int t = i >> 5, cb = i & 31;
+            float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (t < valid) z = *reinterpret_cast<const float4*>(args.decay + (tok0 + t) * HD + 4 * cb);
+            const uint32_t off = (uint32_t)((cb >> 3) * 8192) + swz(t, cb & 7);
+            sts128(sb + S::LAM + off, __float_as_uint(z.x), __float_as_uint(z.y), __float_as_uint(z.z), __float_as_uint(z.w));
+        }
+        fence_async_smem();   // v is read by the tensor cores
+    }
+    if (tid < HCK) betav[tid] = tid < valid ? args.beta[tok0 + tid] : 0.f;
+    if (full) {
+        const bool ok = mbar_wait(mb_tma, 0, wl);
+        if (__syncthreads_or(!ok)) failed = true;
+    } else {
+        __syncthreads();
+    }
+
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const int s = tid & 127;   // tensor-memory lane of this thread (row of the chunk's 128-row tiles)
+    const int hf = tid >> 7;   // which half of the columns this thread takes in the lane-mapped phases
+
+    if (!failed) {
+        // ---- a2: per-channel sums of the log-decay (G after 32 tokens and at the chunk end),
+        // and c_t = k_t^T Lambda_t k_t per token (one warp per 16 tokens)
+        if (warp < 4) {
+            const int c = tid;
+            float s1 = 0.f, s2 = 0.f;
+#pragma unroll 8
+            for (int t = 0; t < 32; ++t) s1 += lds_f32(sb + S::LAM + sw_f32(t, c, HCK));
+#pragma unroll 8
+            for (int t = 32; t < 64; ++t) s2 += lds_f32(sb + S::LAM + sw_f32(t, c, HCK));
+            const float GC = s1 + s2, a = 0.5f * GC;
+            gh[c] = s1;
+            av[c] = a;
+            ea[c] = __expf(a);
+            gam[c] = __expf(GC);
+        } else {
+            for (int tt = 0; tt < 16; ++tt) {
+                const int t = 16 * (warp - 4) + tt;
+                float acc = 0.f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int c = lane + 32 * i;
+                    const float kk = lds_bf16(sb + S::K_ + sw_bf16(t, c, HCK));
+                    acc = fmaf(__expf(lds_f32(sb + S::LAM + sw_f32(t, c, HCK))) * kk, kk, acc);
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+                if (lane == 0) cdot[t] = acc;
+            }
+        }
+        __syncthreads();
+
+        // ---- a3: the decay-scaled factor tiles, one key channel per thread, 32 tokens per thread
+        {
+            const int c = s;
+            const float a = av[c];
+            float G = hf ? gh[c] : 0.f;
+            float Fp = __expf(G - a), Rp = __expf(a - G);
+#pragma unroll 2
+            for (int tt = 0; tt < 32; ++tt) {
+                const int t = 32 * hf + tt;
+                G += lds_f32(sb + S::LAM + sw_f32(t, c, HCK));
+                const float F = __expf(G - a), R = __expf(a - G);
+                const float kk = lds_bf16(sb + S::K_ + sw_bf16(t, c, HCK));
+                const float qq = lds_bf16(sb + S::Q_ + sw_bf16(t, c, HCK));
+                const float b = betav[t], cd = cdot[t];
+                const float at0 = R * kk, at1 = Rp * kk;
+                const float bt1 = b * Fp * kk;
+                const float bt0 = b * F * kk - b * cd * bt1;
+                uint16_t h, l;
+                const uint32_t o0 = sw_bf16(2 * t, c, 128), o1 = sw_bf16(2 * t + 1, c, 128);
+                split1(at0, h, l);
+                sts16(sb + S::A_HI + o0, h);
+                sts16(sb + S::A_LO + o0, l);
+                split1(at1, h, l);
+                sts16(sb + S::A_HI + o1, h);
+                sts16(sb + S::A_LO + o1, l);
+                sts16(sb + S::BT + o0, bf16_bits(bt0));
+                sts16(sb + S::BT + o1, bf16_bits(bt1));
+                split1(F * qq, h, l);
+                const uint32_t oq = sw_bf16(t, c, HCK);
+                sts16(sb + S::Q_HI + oq, h);
+                sts16(sb + S::Q_LO + oq, l);
+                Fp = F;
+                Rp = R;
+            }
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+
+        // ---- a4: L = B~ A~^T and QA^T = A~ Q~^T (three terms) on the tensor cores
+        if (warp == 0) {
+            const uint32_t lead = lane == 0;
+            const uint32_t idL = idesc_bf16(128, 128, false, false);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                mma_ss_if(tmem + TL, smem_desc_sw128(sb + S::BT + off, 16, 1024), smem_desc_sw128(sb + S::A_HI + off, 16, 1024),
+                          idL, kk > 0, lead);
+            }
+            const uint32_t idQ = idesc_bf16(128, 64, false, false);
+            const uint32_t aop[3] = {sb + S::A_HI, sb + S::A_LO, sb + S::A_HI};
+            const uint32_t bop[3] = {sb + S::Q_HI, sb + S::Q_HI, sb + S::Q_LO};
+#pragma unroll
+            for (int term = 0; term < 3; ++term)
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss_if(tmem + TQA, smem_desc_sw128(aop[term] + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                              smem_desc_sw128(bop[term] + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), idQ,
+                              (term > 0 || kk > 0), lead);
+            commit_if(mb_mma, lead);
+        }
+        {
+            const bool ok = mbar_wait(mb_mma, mma_phase & 1, wl);
+            ++mma_phase;
+            if (__syncthreads_or(!ok)) failed = true;
+            fence_after_sync();
+        }
+    }
+
+    if (!failed) {
+        // ---- a5: L into the inverse's fp32 blocks (strict lower part by token), then M = (I + L)^{-1}
+        {
+            float* X = reinterpret_cast<float*>(smem + S::R0);
+#pragma unroll 1
+            for (int p = 0; p < 2; ++p) {
+                float x[32];
+                tmem_ld32(tmem + lane_base + TL + 64 * hf + 32 * p, x);
+                const int c0 = 64 * hf + 32 * p;
+                float* dst = nullptr;
+                if (hf == 0) dst = (s < 64) ? X + s * kLdX : X + (64 + (s - 64)) * kLdX;   // X11 or X21 row
+                else if (s >= 64) dst = X + (128 + (s - 64)) * kLdX - 64;                // X22 row, columns shifted
+                if (dst) {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4) {
+                        const int c = c0 + i;
+                        float4 y;
+                        y.x = ((c + 0) >> 1) < (s >> 1) ? x[i + 0] : 0.f;
+                        y.y = ((c + 1) >> 1) < (s >> 1) ? x[i + 1] : 0.f;
+                        y.z = ((c + 2) >> 1) < (s >> 1) ? x[i + 2] : 0.f;
+                        y.w = ((c + 3) >> 1) < (s >> 1) ? x[i + 3] : 0.f;
+                        *reinterpret_cast<float4*>(dst + c) = y;
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        {
+            float* X = reinterpret_cast<float*>(smem + S::R0);
+            if (warp < 4) inv64_inplace(X, tid, 1);                  // M11 in place of L11
+            else inv64_inplace(X + 128 * kLdX, tid - 128, 2);        // M22 in place of L22
+            __syncthreads();
+            // 64 -> 128: M21 = -M22 (L21 M11), 32 tiles of 16 x 8 per product, four per warp
+            float* X11 = X;
+            float* X21 = X + 64 * kLdX;
+            float* X22 = X + 128 * kLdX;
+            float c[4][4];
+#pragma unroll
+            for (int rb = 0; rb < 4; ++rb) warp_mma_tf32_rn(X21 + 16 * rb * kLdX, kLdX, X11 + 8 * warp, kLdX, 64, c[rb]);
+            __syncthreads();
+#pragma unroll
+            for (int rb = 0; rb < 4; ++rb) store_tile_16x8(X21 + 16 * rb * kLdX + 8 * warp, kLdX, c[rb], 1.f);
+            __syncthreads();
+#pragma unroll
+            for (int rb = 0; rb < 4; ++rb) warp_mma_tf32_rn(X22 + 16 * rb * kLdX, kLdX, X21 + 8 * warp, kLdX, 64, c[rb]);
+            __syncthreads();
+#pragma unroll
+            for (int rb = 0; rb < 4; ++rb) store_tile_16x8(X21 + 16 * rb * kLdX + 8 * warp, kLdX, c[rb], -1.f);
+            __syncthreads();
+        }
+
+        // ---- M as the bf16 A operand of Y (tensor memory), and M Diag(beta) on the even columns
+        // (the columns that meet W) as hi + lo tiles for MW
+        {
+            const float* X = reinterpret_cast<const float*>(smem + S::R0);
+            const float* row = nullptr;   // columns 64 hf .. 64 hf + 63 of row s of M (nullptr: zero)
+            if (hf == 0) row = (s < 64) ? X + s * kLdX : X + s * kLdX;   // X11 row s or X21 row s - 64
+            else if (s >= 64) row = X + (128 + (s - 64)) * kLdX;          // X22 row s - 64
+            uint32_t pk[32];
+            uint32_t mbh[16], mbl[16];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float m0 = row ? row[2 * i] : 0.f, m1 = row ? row[2 * i + 1] : 0.f;
+                pk[i] = pack_bf16(m0, m1);
+                const float mb = m0 * betav[32 * hf + i];   // column 2t of M, t = 32 hf + i
+                uint16_t h, l;
+                split1(mb, h, l);
+                if (i & 1) {
+                    mbh[i >> 1] |= static_cast<uint32_t>(h) << 16;
+                    mbl[i >> 1] |= static_cast<uint32_t>(l) << 16;
+                } else {
+                    mbh[i >> 1] = h;
+                    mbl[i >> 1] = l;
+                }
+            }
+            tmem_st32(tmem + lane_base + TM + 32 * hf, pk);
+            __syncthreads();   // every row of M read: its region takes the M Diag(beta) tiles
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                const uint32_t off = swz(s, 4 * hf + ch);   // columns t = 32 hf + 8 ch ..
+                sts128(sb + S::MB_HI + off, mbh[4 * ch], mbh[4 * ch + 1], mbh[4 * ch + 2], mbh[4 * ch + 3]);
+                sts128(sb + S::MB_LO + off, mbl[4 * ch], mbl[4 * ch + 1], mbl[4 * ch + 2], mbl[4 * ch + 3]);
+            }
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+
+        // ---- a5 (applications): Y = M B~ and MW^T = V^T (M Diag(beta))^T on the tensor cores
+        if (warp == 0) {
+            const uint32_t lead = lane == 0;
+            const uint32_t idY = idesc_bf16(128, 128, false, true);
+            const uint64_t bY = smem_desc_sw128(sb + S::BT, 16384, 1024);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) mma_ts_if(tmem + TL, tmem + TM + 8 * kk, dadd(bY, 2048 * kk), idY, kk > 0, lead);
+            const uint32_t idW = idesc_bf16(128, 128, true, false);
+            const uint64_t aW = smem_desc_sw128(sb + S::V, 8192, 1024);
+#pragma unroll
+            for (int term = 0; term < 2; ++term) {
+                const uint64_t bW = smem_desc_sw128(sb + (term ? S::MB_LO : S::MB_HI), 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_ss_if(tmem + TMW, dadd(aW, 2048 * kk), dadd(bW, 32 * kk), idW, (term > 0 || kk > 0), lead);
+            }
+            commit_if(mb_mma, lead);
+        }
+        {
+            const bool ok = mbar_wait(mb_mma, mma_phase & 1, wl);
+            ++mma_phase;
+            if (__syncthreads_or(!ok)) failed = true;
+            fence_after_sync();
+        }
+    }
+
+    if (!failed) {
+        // ---- operand tiles for the last products: Y (bf16, over B~), MW^T hi/lo (tensor memory),
+        // QA^T hi/lo (masked t >= token of s)
+#pragma unroll 1
+        for (int p = 0; p < 2; ++p) {
+            float x[32];
+            tmem_ld32(tmem + lane_base + TL + 64 * hf + 32 * p, x);
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                const int c = 64 * hf + 32 * p + 8 * ch;
+                sts128(sb + S::BT + sw_bf16(s, c, 128), pack_bf16(x[8 * ch + 0], x[8 * ch + 1]),
+                       pack_bf16(x[8 * ch + 2], x[8 * ch + 3]), pack_bf16(x[8 * ch + 4], x[8 * ch + 5]),
+                       pack_bf16(x[8 * ch + 6], x[8 * ch + 7]));
+            }
+            tmem_ld32(tmem + lane_base + TMW + 64 * hf + 32 * p, x);
+            uint32_t h[16], l[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) split2(x[2 * i], x[2 * i + 1], h[i], l[i]);
+            tmem_st16(tmem + lane_base + TMWH + 32 * hf + 16 * p, h);
+            tmem_st16(tmem + lane_base + TMWL + 32 * hf + 16 * p, l);
+        }
+        {
+            float x[32];
+            tmem_ld32(tmem + lane_base + TQA + 32 * hf, x);
+            const int tok_s = s >> 1;
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t h[4], l[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int t0 = 32 * hf + 8 * ch + 2 * i;
+                    split2(t0 >= tok_s ? x[8 * ch + 2 * i] : 0.f, t0 + 1 >= tok_s ? x[8 * ch + 2 * i + 1] : 0.f, h[i], l[i]);
+                }
+                const uint32_t off = swz(s, 4 * hf + ch);
+                sts128(sb + S::V + off, h[0], h[1], h[2], h[3]);       // QA hi over v
+                sts128(sb + S::QA_LO + off, l[0], l[1], l[2], l[3]);
+            }
+        }
+        tmem_wait_st();
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+
+        // ---- a6/a7 (chunk part): A~^T Y, c^T = MW^T A~ (3 terms), Zq = Y^T QA^T, O^T = MW^T QA^T (3 terms)
+        if (warp == 0) {
+            const uint32_t lead = lane == 0;
+            const uint32_t idP = idesc_bf16(128, 128, true, true);
+            const uint64_t aP = smem_desc_sw128(sb + S::A_HI, 16384, 1024), bP = smem_desc_sw128(sb + S::BT, 16384, 1024);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) mma_ss_if(tmem + TL, dadd(aP, 2048 * kk), dadd(bP, 2048 * kk), idP, kk > 0, lead);
+            const uint32_t idC = idesc_bf16(128, 128, false, true);
+            const uint32_t ta[3] = {tmem + TMWH, tmem + TMWL, tmem + TMWH};
+            const uint32_t sbB[3] = {sb + S::A_HI, sb + S::A_HI, sb + S::A_LO};
+#pragma unroll
+            for (int term = 0; term < 3; ++term) {
+                const uint64_t b = smem_desc_sw128(sbB[term], 16384, 1024);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ts_if(tmem + TMW, ta[term] + 8 * kk, dadd(b, 2048 * kk), idC, (term > 0 || kk > 0), lead);
+            }
+            const uint32_t idZ = idesc_bf16(128, 64, true, true);
+            const uint64_t aZ = smem_desc_sw128(sb + S::BT, 16384, 1024), bZ = smem_desc_sw128(sb + S::V, 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) mma_ss_if(tmem + TM, dadd(aZ, 2048 * kk), dadd(bZ, 2048 * kk), idZ, kk > 0, lead);
+            const uint32_t idO = idesc_bf16(128, 64, false, true);
+            const uint32_t sbQ[3] = {sb + S::V, sb + S::V, sb + S::QA_LO};
+#pragma unroll
+            for (int term = 0; term < 3; ++term) {
+                const uint64_t b = smem_desc_sw128(sbQ[term], 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ts_if(tmem + TQA, ta[term] + 8 * kk, dadd(b, 2048 * kk), idO, (term > 0 || kk > 0), lead);
+            }
+            commit_if(mb_mma, lead);
+        }
+        {
+            const bool ok = mbar_wait(mb_mma, mma_phase & 1, wl);
+            ++mma_phase;
+            if (__syncthreads_or(!ok)) failed = true;
+            fence_after_sync();
+        }
+    }
+
+    if (!failed) {
+        // ---- epilogues: P_j, Q'_j (warps 0-3, lane = key channel), c_j, O_j (warps 4-7, lane = value channel)
+        if (hf == 0) {
+            const int i = s;
+            __nv_bfloat16* Prow = args.P + (unit * HD + i) * HD;
+            const float ei = ea[i], gi = gam[i];
+#pragma unroll 1
+            for (int p = 0; p < 4; ++p) {
+                float x[32];
+                tmem_ld32(tmem + lane_base + TL + 32 * p, x);
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int k0 = 32 * p + 8 * ch + 2 * e;
+                        const float p0 = (k0 == i ? gi : 0.f) - ei * x[8 * ch + 2 * e] * ea[k0];
+                        const float p1 = (k0 + 1 == i ? gi : 0.f) - ei * x[8 * ch + 2 * e + 1] * ea[k0 + 1];
+                        w[e] = pack_bf16(p0, p1);
+                    }
+                    *reinterpret_cast<uint4*>(Prow + 32 * p + 8 * ch) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+            // Q'[t][c] = e^{a_c} (Q~[t][c] - Zq[c][t]), c = lane; Q~ from its hi and lo tiles. Q'_j is stored
+            // as bf16 hi (rows 0-63) and lo (rows 64-127) of a [128][128] block.
+            const int c = s;
+            __nv_bfloat16* Qcol = args.Qm + unit * (size_t)(2 * HCK * HD) + c;
+#pragma unroll 1
+            for (int p = 0; p < 2; ++p) {
+                float x[32];
+                tmem_ld32(tmem + lane_base + TM + 32 * p, x);
+#pragma unroll 4
+                for (int i2 = 0; i2 < 32; ++i2) {
+                    const int t = 32 * p + i2;
+                    const uint32_t oq = sw_bf16(t, c, HCK);
+                    const float qt = lds_bf16(sb + S::Q_HI + oq) + lds_bf16(sb + S::Q_LO + oq);
+                    uint16_t h, l;
+                    split1(ei * (qt - x[i2]), h, l);
+                    reinterpret_cast<uint16_t*>(Qcol)[(size_t)t * HD] = h;
+                    reinterpret_cast<uint16_t*>(Qcol)[(size_t)(HCK + t) * HD] = l;
+                }
+            }
+        } else {
+            const int n = s;
+            float* Ccol = args.Cm + unit * (size_t)(HD * HD) + n;
+#pragma unroll 1
+            for (int p = 0; p < 4; ++p) {
+                float x[32];
+                tmem_ld32(tmem + lane_base + TMW + 32 * p, x);
+#pragma unroll
+                for (int i2 = 0; i2 < 32; ++i2) Ccol[(size_t)(32 * p + i2) * HD] = ea[32 * p + i2] * x[i2];
+            }
+            float* ocol = args.o + tok0 * HD + n;
+#pragma unroll 1
+            for (int p = 0; p < 2; ++p) {
+                float x[32];
+                tmem_ld32(tmem + lane_base + TQA + 32 * p, x);
+#pragma unroll
+                for (int i2 = 0; i2 < 32; ++i2) {
+                    const int t = 32 * p + i2;
+                    if (t < valid) ocol[(size_t)t * HD] = x[i2];
+                }
+            }
+        }
+    }
+
+    if (failed) {
+        if (tid == 0) {
+            atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
+            // no copy may land after the CTA exits, and no product may touch freed tensor memory
+            if (full) mbar_wait(mb_tma, 0, 400000000LL);
+            mma_commit(mb_drain);   // tracks every product issued by this thread
+            mbar_wait(mb_drain, 0, 400000000LL);
+        }
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// ================================================================================================
+// Stage 2: the chain over chunks, per (head, block of state columns)
+// ================================================================================================
+
+constexpr int NV = 32;       // state columns per chain CTA
+constexpr int K2T = 160;     // warps 0-3: the state (thread = key channel = tensor-memory lane); warp 4: copies
+
+struct K2Smem {
+    static constexpr int P0 = 0;                  // P_j: bf16 [128][128] swizzled, two buffers
+    // Q'_j hi and lo: bf16 swizzled tiles of 192 rows (two 64-column halves each); chunk j's 64 rows at
+    // row 64 (j % 2); rows 128-191 stay zero
+    static constexpr int QHALF = 192 * 128;
+    static constexpr int QH = 2 * 32768;
+    static constexpr int QL = QH + 2 * QHALF;
+    static constexpr int SB = QL + 2 * QHALF;     // S_{j-1} hi: bf16 [128][NV] core-matrix tiles, two buffers
+    static constexpr int SBB = 128 * NV * 2;
+    static constexpr int SL = SB + 2 * SBB;       // S_{j-1} lo, two buffers
+    static constexpr int BAR = SL + 2 * SBB;
+    static constexpr int TOTAL = BAR + 128;
+};
+static_assert(K2Smem::TOTAL <= 227 * 1024, "shared memory budget");
+
+struct K2Args {
+    const __nv_bfloat16* P; const float* Cm; const float* S0;
+    float* o; float* ST; int* status;
+};
+
+__global__ void __launch_bounds__(K2T, 1)
+hdla_chain_kernel(Plan pl, K2Args args, const __grid_constant__ CUtensorMap tm_P, const __grid_constant__ CUtensorMap tm_Q) {
+    using S = K2Smem;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const uint32_t sb = smem_addr(smem);
+    if (sb & 1023u) {
+        if (threadIdx.x == 0) atomicExch(args.status, (int)DPLR_ERR_CUDA);
+        return;
+    }
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::BAR);
+    uint64_t* full = bars + 0;     // [2] P_j and Q'_j landed
+    uint64_t* freed = bars + 2;    // [2] both products of the chunk that used the buffer are done
+    uint64_t* mS = bars + 4;       // the chain product of the chunk
+    // [2] the output product of the chunks using accumulator j % 2: one barrier per accumulator, so that
+    // the commit of chunk j + 1 cannot complete a phase before the wait for chunk j has seen its own
+    uint64_t* mO = bars + 5;
+    uint64_t* drain = bars + 7;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 8);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int T = pl.T;
+    const int NC = (T + HCK - 1) / HCK;
+    constexpr int kSlices = HD / NV;
+    const size_t bh = blockIdx.x / kSlices;
+    const int n0 = (blockIdx.x % kSlices) * NV;
+    const long long wl = pl.wait_cycles;
+
+    if (tid == 0) {
+        for (int i = 0; i < 8; ++i) mbar_init(bars + i, 1);
+        mbar_fence_init();
+    }
+    // the third block of 64 Q' rows is never loaded: rows 64-127 of the output product read it
+    for (int i = tid; i < 4 * 64 * 32; i += K2T) {
+        const int b = i / (64 * 32), e = i % (64 * 32);   // half-tile b of Q' hi, hi, lo, lo
+        reinterpret_cast<uint32_t*>(smem + S::QH + b * S::QHALF + 128 * 128)[e] = 0u;
+    }
+    if (warp == 0) tmem_alloc(tmem_holder, 128);
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tmem_holder;   // columns 0-31: S_j = P_j S_{j-1}; 32-95: two output accumulators
+    bool failed = false;
+
+    if (warp == 4) {
+        // ---- copies: P_j and Q'_j of chunk j into buffer j % 2, once the products of chunk j - 2 are done
+        int last = -1;
+        for (int j = 0; j < NC && lane == 0; ++j) {
+            const int u = j & 1;
+            if (j >= 2 && !mbar_wait(&freed[u], ((j - 2) >> 1) & 1, wl)) { failed = true; break; }
+            mbar_expect_tx(&full[u], 32768 + 32768);
+            const int yP = static_cast<int>((bh * NC + j) * HD), yQ = static_cast<int>((bh * NC + j) * 2 * HCK);
+            for (int h = 0; h < 2; ++h) {
+                tma_load_2d(smem + S::P0 + u * 32768 + h * 16384, &tm_P, 64 * h, yP, &full[u]);
+                tma_load_2d(smem + S::QH + h * S::QHALF + u * 8192, &tm_Q, 64 * h, yQ, &full[u]);
+                tma_load_2d(smem + S::QL + h * S::QHALF + u * 8192, &tm_Q, 64 * h, yQ + HCK, &full[u]);
+            }
+            last = j;
+        }
+        if (failed) {   // (lane 0) wait for the copies in flight before leaving
+            atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
+            for (int jj = last - 1; jj <= last; ++jj)
+                if (jj >= 0) mbar_wait(&full[jj & 1], (jj >> 1) & 1, 400000000LL);
+        }
+        __syncwarp();
+    } else {
+        // ---- the state: thread i holds row i of S (NV columns) in fp32
+        const int i = tid;
+        const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
+        float st[NV];
+#pragma unroll
+        for (int n = 0; n < NV; ++n) st[n] = args.S0 ? args.S0[(bh * HD + i) * HD + n0 + n] : 0.f;
+        // S_{j-1} into buffer b as bf16 hi + lo, core-matrix layout (MN-major operand: K = row i)
+        auto write_state = [&](int b) {
+            const uint32_t r0 = (i >> 3) * (NV / 8) * 128 + (i & 7) * 16;
+#pragma unroll
+            for (int ch = 0; ch < NV / 8; ++ch) {
+                uint32_t h[4], l[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) split2(st[8 * ch + 2 * e], st[8 * ch + 2 * e + 1], h[e], l[e]);
+                sts128(sb + S::SB + b * S::SBB + r0 + ch * 128, h[0], h[1], h[2], h[3]);
+                sts128(sb + S::SL + b * S::SBB + r0 + ch * 128, l[0], l[1], l[2], l[3]);
+            }
+        };
+        // the two products of chunk j (warp 0, lane 0 issues through a predicate)
+        auto issue = [&](int j) -> bool {
+            const int u = j & 1;
+            const uint32_t lead = lane == 0;
+            bool ok = true;
+            if (lead) ok = mbar_wait(&full[u], (j >> 1) & 1, wl);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) return false;
+            fence_after_sync();
+            // S_j - c_j = P_j (S_hi + S_lo): the state keeps its fp32 precision in the chain (a chunk whose decay
+            // is weak, such as a short last chunk, has P_j of order one)
+            const uint32_t idS = idesc_bf16(128, NV, false, true);
+            const uint64_t aS = smem_desc_sw128(sb + S::P0 + u * 32768, 16, 1024);
+#pragma unroll
+            for (int term = 0; term < 2; ++term) {
+                const uint64_t bS = smem_desc(sb + (term ? S::SL : S::SB) + (j & 1) * S::SBB, (NV / 8) * 128, 128);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss_if(tmem, dadd(aS, (kk >> 2) * 16384 + (kk & 3) * 32), dadd(bS, kk * 2 * (NV / 8) * 128), idS,
+                              (term > 0 || kk > 0), lead);
+            }
+            commit_if(mS, lead);
+            // O = Q'_hi S_hi + Q'_lo S_hi + Q'_hi S_lo over rows 64u .. 64u + 127 of the Q' tiles
+            const uint32_t qa[3] = {sb + S::QH, sb + S::QL, sb + S::QH};
+            const uint32_t sbm[3] = {sb + S::SB, sb + S::SB, sb + S::SL};
+#pragma unroll
+            for (int term = 0; term < 3; ++term) {
+                const uint64_t aO = smem_desc_sw128(qa[term] + u * 8192, 16, 1024);
+                const uint64_t bO = smem_desc(sbm[term] + (j & 1) * S::SBB, (NV / 8) * 128, 128);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss_if(tmem + 32 + 32 * (j & 1), dadd(aO, (kk >> 2) * S::QHALF + (kk & 3) * 32),
+                              dadd(bO, kk * 2 * (NV / 8) * 128), idS, (term > 0 || kk > 0), lead);
+            }
+            commit_if(&mO[j & 1], lead);
+            commit_if(&freed[u], lead);
+            return true;
+        };
+        write_state(0);
+        fence_async_smem();
+        fence_before_sync();
+        named_sync(1, 128);
+        fence_after_sync();
+        if (NC > 0 && warp == 0 && !issue(0)) failed = true;
+        if (named_sync_or(1, 128, failed)) failed = true;
+
+        for (int j = 0; j < NC && !failed; ++j) {
+            const size_t unit = bh * (size_t)NC + j;
+            // c_j (rows i, this CTA's columns) and the chunk-local outputs O_j (rows t = i < 64)
+            float4 cv[NV / 4], ov[NV / 4];
+            const float4* csrc = reinterpret_cast<const float4*>(args.Cm + unit * (size_t)(HD * HD) + (size_t)i * HD + n0);
+#pragma unroll
+            for (int q4 = 0; q4 < NV / 4; ++q4) cv[q4] = csrc[q4];
+            const int valid = min(HCK, T - j * HCK);
+            float* orow = args.o + (bh * (size_t)T + (size_t)j * HCK + i) * HD + n0;
+            const bool has_o = i < valid;
+#pragma unroll
+            for (int q4 = 0; q4 < NV / 4; ++q4)
+                ov[q4] = has_o ? reinterpret_cast<const float4*>(orow)[q4] : make_float4(0.f, 0.f, 0.f, 0.f);
+            // S_j = P_j S_{j-1} + c_j
+            bool ok = true;
+            if ((i & 31) == 0) ok = mbar_wait(mS, j & 1, wl);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (named_sync_or(1, 128, !ok)) { failed = true; break; }
+            fence_after_sync();
+            {
+                float x[32];
+                tmem_ld32(tmem + lane_base, x);
+#pragma unroll
+                for (int q4 = 0; q4 < NV / 4; ++q4) {
+                    st[4 * q4 + 0] = x[4 * q4 + 0] + cv[q4].x;
+                    st[4 * q4 + 1] = x[4 * q4 + 1] + cv[q4].y;
+                    st[4 * q4 + 2] = x[4 * q4 + 2] + cv[q4].z;
+                    st[4 * q4 + 3] = x[4 * q4 + 3] + cv[q4].w;
+                }
+            }
+            if (j + 1 < NC) write_state((j + 1) & 1);
+            fence_async_smem();
+            fence_before_sync();
+            named_sync(1, 128);
+            fence_after_sync();
+            if (j + 1 < NC && warp == 0 && !issue(j + 1)) failed = true;
+            // o_t += Q'_t S_{j-1} for the chunk's tokens (rows 0-63 of the output accumulator)
+            ok = true;
+            if ((i & 31) == 0) ok = mbar_wait(&mO[j & 1], (j >> 1) & 1, wl);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (named_sync_or(1, 128, failed || !ok)) { failed = true; break; }
+            fence_after_sync();
+            {
+                float x[32];
+                tmem_ld32(tmem + lane_base + 32 + 32 * (j & 1), x);
+                if (has_o) {
+#pragma unroll
+                    for (int q4 = 0; q4 < NV / 4; ++q4)
+                        reinterpret_cast<float4*>(orow)[q4] =
+                            make_float4(ov[q4].x + x[4 * q4], ov[q4].y + x[4 * q4 + 1], ov[q4].z + x[4 * q4 + 2],
+                                        ov[q4].w + x[4 * q4 + 3]);
+                }
+            }
+            fence_before_sync();
+        }
+        if (!failed && args.ST) {
+            float* dst = args.ST + (bh * HD + i) * HD + n0;
+#pragma unroll
+            for (int q4 = 0; q4 < NV / 4; ++q4)
+                reinterpret_cast<float4*>(dst)[q4] = make_float4(st[4 * q4], st[4 * q4 + 1], st[4 * q4 + 2], st[4 * q4 + 3]);
+        }
+        if (failed && i == 0) {   // the issuing thread: no product may outlive the tensor memory
+            atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
+            mma_commit(drain);
+            mbar_wait(drain, 0, 400000000LL);
+        }
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
+std::atomic<uint64_t> g_k1_smem_set{0}, g_k2_smem_set{0};
+
+}  // namespace
+
+bool hdla_tc_supported(const Plan& pl) {
+    return pl.mode == DPLR_HDLA && pl.bf16 && pl.dk == HD && pl.dv == HD;
+}
+
+// Workspace of the tensor-core HDLA path after the 256-byte status word: per (head, chunk) unit,
+// P_j bf16 [128][128], then c_j fp32 [128][128], then Q'_j bf16 [2][64][128] (hi rows, then lo rows).
+void hdla_tc_offsets(const Plan& pl, size_t* off_P, size_t* off_c, size_t* off_Q, size_t* total) {
+    const size_t units = (size_t)pl.BH * (size_t)((pl.T + HCK - 1) / HCK);
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    size_t off = 256;
+    *off_P = off; off = up(off + units * HD * HD * 2);
+    *off_c = off; off = up(off + units * HD * HD * 4);
+    *off_Q = off; off = up(off + units * 2 * HCK * HD * 2);
+    *total = off;
+}
+
+cudaError_t launch_hdla_chunks(const Plan& pl, const void* q, const void* k, const void* v, const float* decay,
+                               const float* beta, float* o, void* workspace, cudaStream_t s) {
+    if (pl.T == 0) return cudaSuccess;
+    size_t oP, oC, oQ, total;
+    hdla_tc_offsets(pl, &oP, &oC, &oQ, &total);
+    char* ws = static_cast<char*>(workspace);
+    K1Args a;
+    a.q = static_cast<const __nv_bfloat16*>(q);
+    a.k = static_cast<const __nv_bfloat16*>(k);
+    a.v = static_cast<const __nv_bfloat16*>(v);
+    a.decay = decay; a.beta = beta; a.o = o;
+    a.P = reinterpret_cast<__nv_bfloat16*>(ws + oP);
+    a.Cm = reinterpret_cast<float*>(ws + oC);
+    a.Qm = reinterpret_cast<__nv_bfloat16*>(ws + oQ);
+    a.status = reinterpret_cast<int*>(ws);
+    CUtensorMap mq, mk, mv, ml;
+    std::memset(&mq, 0, sizeof(mq)); std::memset(&mk, 0, sizeof(mk));
+    std::memset(&mv, 0, sizeof(mv)); std::memset(&ml, 0, sizeof(ml));
+    if (pl.T >= HCK) {   // only full chunks are loaded by TMA
+        const uint64_t rows = (uint64_t)pl.BH * (uint64_t)pl.T;
+        if (!tensor_map_2d(&mq, q, true, rows, HD, HCK, 64) || !tensor_map_2d(&mk, k, true, rows, HD, HCK, 64) ||
+            !tensor_map_2d(&mv, v, true, rows, HD, HCK, 64) || !tensor_map_2d(&ml, decay, false, rows, HD, HCK, 32))
+            return cudaErrorInvalidValue;
+    }
+    cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(hdla_chunk_kernel), K1Smem::TOTAL, g_k1_smem_set);
+    if (e != cudaSuccess) return e;
+    const long long grid = (long long)pl.BH * ((pl.T + HCK - 1) / HCK);
+    hdla_chunk_kernel<<<(unsigned)grid, K1T, K1Smem::TOTAL, s>>>(pl, a, mq, mk, mv, ml);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_hdla_chain(const Plan& pl, const float* S0, float* o, float* ST, void* workspace, cudaStream_t s) {
+    size_t oP, oC, oQ, total;
+    hdla_tc_offsets(pl, &oP, &oC, &oQ, &total);
+    char* ws = static_cast<char*>(workspace);
+    K2Args a;
+    a.P = reinterpret_cast<const __nv_bfloat16*>(ws + oP);
+    a.Cm = reinterpret_cast<const float*>(ws + oC);
+    a.S0 = S0; a.o = o; a.ST = ST;
+    a.status = reinterpret_cast<int*>(ws);
+    CUtensorMap mP, mQ;
+    std::memset(&mP, 0, sizeof(mP)); std::memset(&mQ, 0, sizeof(mQ));
+    const int NC = (pl.T + HCK - 1) / HCK;
+    if (NC > 0) {
+        const uint64_t units = (uint64_t)pl.BH * (uint64_t)NC;
+        if (!tensor_map_2d(&mP, ws + oP, true, units * HD, HD, HD, 64) ||
+            !tensor_map_2d(&mQ, ws + oQ, true, units * 2 * HCK, HD, HCK, 64))
+            return cudaErrorInvalidValue;
+    }
+    cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(hdla_chain_kernel), K2Smem::TOTAL, g_k2_smem_set);
+    if (e != cudaSuccess) return e;
+    hdla_chain_kernel<<<(unsigned)(pl.BH * (HD / NV)), K2T, K2Smem::TOTAL, s>>>(pl, a, mP, mQ);
+    return cudaGetLastError();
+}
+
+}  // namespace dplr

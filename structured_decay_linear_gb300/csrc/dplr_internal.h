@@ -4,6 +4,7 @@
 #include <atomic>
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/dplr.h"
@@ -24,7 +25,8 @@ struct Plan {
     int BH, T, dk, dv, r, p;   // p = 0 in the structured modes (write term folded into A)
     int cw;                    // WY block length in tokens (two-stage path)
     int nb;                    // WY blocks per head = ceil(T / cw)
-    int fused;                 // dplr_la_forward runs the fused per-head kernel
+    int fused;                 // dplr_la_forward runs the fused per-head kernel (GDN)
+    int tc;                    // the stages run the tensor-core HDLA kernels
     long long wait_cycles;     // limit (SM cycles) of a kernel's bounded waits on other roles
     size_t off_P, off_c, off_Q;
     size_t ws_stages;          // workspace of the two-stage entry points
@@ -69,6 +71,19 @@ size_t prep_smem_bytes(const Plan& pl);
 size_t scan_smem_bytes(const Plan& pl);
 cudaError_t launch_chunk_maps(const Plan& pl, const ChunkMapArgs& a, cudaStream_t s);
 cudaError_t launch_state_scan(const Plan& pl, const ScanArgs& a, cudaStream_t s);
+
+// A 2-D tensor map of a row-major [rows][cols] matrix (fp32 or bf16) read in 128-byte-swizzled
+// boxes of box_rows x box_cols elements (box_cols * element size = 128 bytes). Encoded once and
+// then served from a small per-thread cache keyed on (base, rows, cols, box, type).
+bool tensor_map_2d(CUtensorMap* map, const void* base, bool bf16, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                   uint32_t box_cols);
+
+// Tensor-core HDLA path (bf16 inputs, dk = dv = 128): chunk maps, then the chain over chunks.
+bool hdla_tc_supported(const Plan& pl);
+void hdla_tc_offsets(const Plan& pl, size_t* off_P, size_t* off_c, size_t* off_Q, size_t* total);
+cudaError_t launch_hdla_chunks(const Plan& pl, const void* q, const void* k, const void* v, const float* decay,
+                               const float* beta, float* o, void* workspace, cudaStream_t s);
+cudaError_t launch_hdla_chain(const Plan& pl, const float* S0, float* o, float* ST, void* workspace, cudaStream_t s);
 
 // Fused per-head kernel (structured modes, bf16 inputs, dk = dv = 128).
 bool fused_supported(const Plan& pl);

@@ -230,6 +230,32 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
+// Warp-level C[16x8] = A[16xK] * B[Kx8] with fp32 operands read as tf32 (mma.sync m16n8k8, fp32
+// accumulate); A and B row-major in shared memory with row strides lda / ldb. Fragment layout of
+// the PTX ISA: g = lane / 4, q = lane % 4; A (g, q), (g+8, q), (g, q+4), (g+8, q+4); B (q, g),
+// (q+4, g); C (g, 2q), (g, 2q+1), (g+8, 2q), (g+8, 2q+1).
+__device__ __forceinline__ void warp_mma_tf32(const float* A, int lda, const float* B, int ldb, int K, float (&c)[4]) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+    c[0] = c[1] = c[2] = c[3] = 0.f;
+    for (int k0 = 0; k0 < K; k0 += 8) {
+        const uint32_t a0 = __float_as_uint(A[g * lda + k0 + q]), a1 = __float_as_uint(A[(g + 8) * lda + k0 + q]);
+        const uint32_t a2 = __float_as_uint(A[g * lda + k0 + q + 4]), a3 = __float_as_uint(A[(g + 8) * lda + k0 + q + 4]);
+        const uint32_t b0 = __float_as_uint(B[(k0 + q) * ldb + g]), b1 = __float_as_uint(B[(k0 + q + 4) * ldb + g]);
+        asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                     "{%0,%1,%2,%3};"
+                     : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                     : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+}
+
+__device__ __forceinline__ void store_tile_16x8(float* C, int ldc, const float (&c)[4], float scale) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+    C[g * ldc + 2 * q] = scale * c[0];
+    C[g * ldc + 2 * q + 1] = scale * c[1];
+    C[(g + 8) * ldc + 2 * q] = scale * c[2];
+    C[(g + 8) * ldc + 2 * q + 1] = scale * c[3];
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);

@@ -67,6 +67,8 @@ def library() -> ctypes.CDLL:
             lib.dplr_la_state_scan.argtypes = [dp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
             lib.dplr_la_forward_noalloc.restype = ctypes.c_int
             lib.dplr_la_forward_noalloc.argtypes = [dp] + [_vp] * 12 + [_vp]
+            lib.dplr_la_path.restype = ctypes.c_char_p
+            lib.dplr_la_path.argtypes = [dp]
             lib.dplr_la_set_wait_limit.restype = None
             lib.dplr_la_set_wait_limit.argtypes = [ctypes.c_longlong]
             lib.dplr_la_read_status.restype = ctypes.c_int
@@ -120,6 +122,10 @@ def dplr_la_check(desc: dplr_desc) -> int:
 
 def dplr_la_kernel_count(desc: dplr_desc) -> int:
     return int(library().dplr_la_kernel_count(ctypes.byref(desc)))
+
+
+def dplr_la_path(desc: dplr_desc) -> str:
+    return library().dplr_la_path(ctypes.byref(desc)).decode()
 
 
 def dplr_la_forward(desc, q, k, v, decay, beta, A, Bm, K, V, S0, o, S_T, workspace, ws_bytes, stream) -> int:
@@ -219,6 +225,7 @@ class Forward:
         self.o = torch.empty((B, H, T, dv), dtype=torch.float32, device=self.device)
         self.S_T = torch.empty((B, H, dk, dv), dtype=torch.float32, device=self.device)
         self.kernels = dplr_la_kernel_count(self.desc)
+        self.path = dplr_la_path(self.desc)
 
     def _check(self, q, k, v, decay, beta, A, Bm, K, V, S0):
         B, H, T, dk, dv, dev, dt = self.B, self.H, self.T, self.dk, self.dv, self.device, self.in_dtype

@@ -227,6 +227,49 @@ def test_fused_kernel_empty_sequence(sdl):
     assert np.array_equal(ST, inp["S0"].astype(np.float64))
 
 
+@pytest.mark.parametrize("B,H,T", [(1, 2, 1), (1, 2, 63), (1, 2, 64), (1, 2, 65), (2, 3, 191), (1, 1, 1024)])
+def test_hdla_tensor_core_path_edges(sdl, B, H, T):
+    """The tensor-core HDLA stages (bf16, d = 128) on sequences shorter than a chunk, exactly one
+    chunk, one past it, several heads with a ragged tail, and a longer run (S0 nonzero throughout)."""
+    w = W("hdla", "bf16", 128, 128, s0=True)
+    d = sdl.make_desc("hdla", "bf16", B, H, T, 128, 128)
+    assert sdl.dplr_la_kernel_count(d) == 2
+    inp = workloads.generate(w, heads=[(b, h) for b in range(B) for h in range(H)], T=T)
+    o, ST = run_gpu(sdl, inp)
+    check(inp, o, ST)
+
+
+def test_hdla_tensor_core_path_empty_sequence(sdl):
+    w = W("hdla", "bf16", 128, 128, s0=True)
+    inp = workloads.generate(w, heads=[(0, 0), (0, 1)], T=0)
+    o, ST = run_gpu(sdl, inp)
+    assert o.shape == (1, 2, 0, 128)
+    assert np.array_equal(ST, inp["S0"].astype(np.float64))
+
+
+def test_hdla_stage_calls_match_forward_and_are_deterministic(sdl):
+    """On the tensor-core HDLA path, dplr_la_chunk_maps then dplr_la_state_scan give the same bits as
+    dplr_la_forward, call after call, and the status word stays clear."""
+    import torch
+    w = W("hdla", "bf16", 128, 128, s0=True)
+    inp = workloads.generate(w, heads=[(0, 0), (0, 1), (0, 2)], T=257)
+    dt = torch.bfloat16
+    fwd = sdl.Forward("hdla", dt, 1, 3, 257, 128, 128)
+    assert fwd.ws_bytes == fwd.stage_ws_bytes
+    args = dict(q=_to_dev(inp["q"], dt), k=_to_dev(inp["k"], dt), v=_to_dev(inp["v"], dt),
+                decay=_to_dev(inp["decay"], torch.float32), beta=_to_dev(inp["beta"], torch.float32))
+    S0 = _to_dev(inp["S0"], torch.float32)
+    o1, S1 = [x.clone() for x in fwd(**args, S0=S0)]
+    o2, S2 = [x.clone() for x in fwd(**args, S0=S0)]
+    fwd.chunk_maps(**args)
+    o3, S3 = [x.clone() for x in fwd.state_scan(S0)]
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(S1, S2)
+    assert torch.equal(o1, o3) and torch.equal(S1, S3)
+    assert fwd.device_status() == 0
+    check(inp, o1.double().cpu().numpy(), S1.double().cpu().numpy())
+
+
 def test_fused_path_selection(sdl):
     """GDN with bf16 inputs at d=128 runs one fused kernel with a status-word workspace; others two stages."""
     d = sdl.make_desc("gdn", "bf16", 8, 16, 8192, 128, 128)
@@ -234,6 +277,11 @@ def test_fused_path_selection(sdl):
     d = sdl.make_desc("gdn", "f32", 1, 2, 256, 32, 32)
     assert sdl.dplr_la_kernel_count(d) == 2
     assert sdl.dplr_la_workspace_size(d) == sdl.dplr_la_stage_workspace_size(d) > 0
+    # HDLA bf16 d = 128: the tensor-core stages, whose workspace holds per chunk P_j (bf16 128 x 128),
+    # c_j (fp32 128 x 128) and Q'_j (bf16 hi and lo, 64 x 128 each) after the status word
+    d = sdl.make_desc("hdla", "bf16", 4, 16, 4096, 128, 128)
+    assert sdl.dplr_la_kernel_count(d) == 2
+    assert sdl.dplr_la_workspace_size(d) == 256 + 64 * 64 * (32768 + 65536 + 32768)
 
 
 # ---------------------------------------------------------------------------
