@@ -33,7 +33,9 @@
 // Stage 2, hdla_chain_kernel: one CTA per (head, 32 state columns). It walks the chunks in order,
 // S_j = P_j S_{j-1} + c_j with P_j as one bf16 term and S_{j-1} as bf16 hi + lo (the decay makes
 // P_j contracting, so its rounding does not accumulate from chunk to chunk), and o_t += Q'_t S_{j-1}
-// with both operands split into bf16 hi + lo (three terms).
+// with both operands split into bf16 hi + lo. The kernel's warps take roles: a copy warp stages each chunk's
+// maps by TMA (after an L2 prefetch four chunks earlier), an issuing warp starts a chunk's products as soon as
+// S_{j-1} is in place, and four warps update the state and write the outputs while the tensor cores work.
 // The state stays in registers in fp32; P_j and Q'_j arrive by TMA two chunks ahead.
 //
 // Every wait is bounded by Plan::wait_cycles; a wait that gives up sets DPLR_ERR_TIMEOUT in the
@@ -68,9 +70,6 @@ __device__ __forceinline__ uint32_t sw_f32(int r, int c, int R) {
 
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-__device__ __forceinline__ void sts16(uint32_t addr, uint16_t v) {
-    asm volatile("st.shared.b16 [%0], %1;" :: "r"(addr), "h"(v) : "memory");
 }
 __device__ __forceinline__ float lds_f32(uint32_t addr) {
     float v;
@@ -151,7 +150,7 @@ __device__ __forceinline__ void warp_mma_tf32_rn(const float* A, int lda, const 
 // M = (I + L)^{-1} on exit. Diagonal 16 x 16 blocks by substitution (one column per thread), then
 // the block merges [[A,0],[C,B]]^{-1} = [[A^{-1},0],[-B^{-1} C A^{-1}, B^{-1}]] for 16 -> 32 -> 64,
 // each product formed in registers and written over C once every warp has read C.
-__device__ void inv64_inplace(float* X, int t, uint32_t bar) {
+__device__ __forceinline__ void inv64_inplace(float* X, int t, uint32_t bar) {
     const int w = t >> 5;
     if (t < 64) {
         const int b = t >> 4, jj = t & 15, o = 16 * b;
@@ -229,7 +228,7 @@ struct K1Smem {
     static constexpr int MB_LO = R0 + 16384;      //   bf16 [128][64]
     static constexpr int QA_LO = R0 + 32768;      //   QA^T lo: bf16 [128][64]
     static constexpr int VEC = R0 + 65536;        // fp32 vectors (see below)
-    static constexpr int BAR = VEC + 4096;        // mbarriers and the tensor-memory address
+    static constexpr int BAR = VEC + 4096;        // mbarriers and the tensor-memory address (vectors: 896 floats)
     static constexpr int TOTAL = BAR + 64;
 };
 static_assert(K1Smem::X22 + 64 * kLdX * 4 <= K1Smem::R0 + 65536, "inverse blocks fit the shared region");
@@ -269,8 +268,8 @@ hdla_chunk_kernel(Plan pl, K1Args args, const __grid_constant__ CUtensorMap tm_q
     float* betav = vec + 64;    // [64]
     float* ea = vec + 128;      // [128] e^{a}
     float* gam = vec + 256;     // [128] e^{G_C}
-    float* gh = vec + 384;      // [128] G after token 31
-    float* av = vec + 512;      // [128] a = G_C / 2
+    float* gq = vec + 384;      // [3][128] G after tokens 15, 31, 47 (the start of token quarters 1-3)
+    float* av = vec + 768;      // [128] a = G_C / 2
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int NC = (pl.T + HCK - 1) / HCK;
@@ -278,7 +277,7 @@ hdla_chunk_kernel(Plan pl, K1Args args, const __grid_constant__ CUtensorMap tm_q
     const size_t bh = blockIdx.x / NC;
     const int valid = min(HCK, pl.T - j * HCK);
     const size_t tok0 = bh * (size_t)pl.T + (size_t)j * HCK;
-    const size_t unit = bh * (size_t)NC + j;
+    const size_t unit = (size_t)j * pl.BH + bh;   // maps are stored chunk-major: a chunk's heads side by side
     const long long wl = pl.wait_cycles;
     const bool full = valid == HCK;
 
@@ -349,16 +348,17 @@ hdla_chunk_kernel(Plan pl, K1Args args, const __grid_constant__ CUtensorMap tm_q
         // and c_t = k_t^T Lambda_t k_t per token (one warp per 16 tokens)
         if (warp < 4) {
             const int c = tid;
-            float s1 = 0.f, s2 = 0.f;
+            float G = 0.f;
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
 #pragma unroll 8
-            for (int t = 0; t < 32; ++t) s1 += lds_f32(sb + S::LAM + sw_f32(t, c, HCK));
-#pragma unroll 8
-            for (int t = 32; t < 64; ++t) s2 += lds_f32(sb + S::LAM + sw_f32(t, c, HCK));
-            const float GC = s1 + s2, a = 0.5f * GC;
-            gh[c] = s1;
+                for (int t = 16 * qq; t < 16 * qq + 16; ++t) G += lds_f32(sb + S::LAM + sw_f32(t, c, HCK));
+                if (qq < 3) gq[128 * qq + c] = G;
+            }
+            const float a = 0.5f * G;
             av[c] = a;
             ea[c] = __expf(a);
-            gam[c] = __expf(GC);
+            gam[c] = __expf(G);
         } else {
             for (int tt = 0; tt < 16; ++tt) {
                 const int t = 16 * (warp - 4) + tt;
@@ -376,39 +376,40 @@ hdla_chunk_kernel(Plan pl, K1Args args, const __grid_constant__ CUtensorMap tm_q
         }
         __syncthreads();
 
-        // ---- a3: the decay-scaled factor tiles, one key channel per thread, 32 tokens per thread
+        // ---- a3: the decay-scaled factor tiles. Warp w takes key channels 64 (w % 2) .. + 63 (two per lane,
+        // stored as bf16 pairs) and tokens 16 (w / 2) .. + 15, starting from the quarter's prefix of G.
         {
-            const int c = s;
-            const float a = av[c];
-            float G = hf ? gh[c] : 0.f;
-            float Fp = __expf(G - a), Rp = __expf(a - G);
+            const int c0 = 64 * (warp & 1) + 2 * lane, qq = warp >> 1;
+            const float a0 = av[c0], a1 = av[c0 + 1];
+            float G0 = qq ? gq[128 * (qq - 1) + c0] : 0.f, G1 = qq ? gq[128 * (qq - 1) + c0 + 1] : 0.f;
+            float Fp0 = __expf(G0 - a0), Fp1 = __expf(G1 - a1), Rp0 = __expf(a0 - G0), Rp1 = __expf(a1 - G1);
 #pragma unroll 2
-            for (int tt = 0; tt < 32; ++tt) {
-                const int t = 32 * hf + tt;
-                G += lds_f32(sb + S::LAM + sw_f32(t, c, HCK));
-                const float F = __expf(G - a), R = __expf(a - G);
-                const float kk = lds_bf16(sb + S::K_ + sw_bf16(t, c, HCK));
-                const float qq = lds_bf16(sb + S::Q_ + sw_bf16(t, c, HCK));
-                const float b = betav[t], cd = cdot[t];
-                const float at0 = R * kk, at1 = Rp * kk;
-                const float bt1 = b * Fp * kk;
-                const float bt0 = b * F * kk - b * cd * bt1;
-                uint16_t h, l;
-                const uint32_t o0 = sw_bf16(2 * t, c, 128), o1 = sw_bf16(2 * t + 1, c, 128);
-                split1(at0, h, l);
-                sts16(sb + S::A_HI + o0, h);
-                sts16(sb + S::A_LO + o0, l);
-                split1(at1, h, l);
-                sts16(sb + S::A_HI + o1, h);
-                sts16(sb + S::A_LO + o1, l);
-                sts16(sb + S::BT + o0, bf16_bits(bt0));
-                sts16(sb + S::BT + o1, bf16_bits(bt1));
-                split1(F * qq, h, l);
-                const uint32_t oq = sw_bf16(t, c, HCK);
-                sts16(sb + S::Q_HI + oq, h);
-                sts16(sb + S::Q_LO + oq, l);
-                Fp = F;
-                Rp = R;
+            for (int tt = 0; tt < 16; ++tt) {
+                const int t = 16 * qq + tt;
+                const float2 ll = *reinterpret_cast<const float2*>(smem + S::LAM + sw_f32(t, c0, HCK));
+                const uint32_t kb = *reinterpret_cast<const uint32_t*>(smem + S::K_ + sw_bf16(t, c0, HCK));
+                const uint32_t qb = *reinterpret_cast<const uint32_t*>(smem + S::Q_ + sw_bf16(t, c0, HCK));
+                const float k0 = __uint_as_float(kb << 16), k1 = __uint_as_float(kb & 0xFFFF0000u);
+                const float q0 = __uint_as_float(qb << 16), q1 = __uint_as_float(qb & 0xFFFF0000u);
+                G0 += ll.x;
+                G1 += ll.y;
+                const float F0 = __expf(G0 - a0), F1 = __expf(G1 - a1), R0 = __expf(a0 - G0), R1 = __expf(a1 - G1);
+                const float b = betav[t], bcd = b * cdot[t];
+                const float bt10 = b * Fp0 * k0, bt11 = b * Fp1 * k1;
+                uint32_t h, l;
+                const uint32_t o0 = sw_bf16(2 * t, c0, 128), o1 = sw_bf16(2 * t + 1, c0, 128), oq = sw_bf16(t, c0, HCK);
+                split2(R0 * k0, R1 * k1, h, l);            // A~ row 2t
+                *reinterpret_cast<uint32_t*>(smem + S::A_HI + o0) = h;
+                *reinterpret_cast<uint32_t*>(smem + S::A_LO + o0) = l;
+                split2(Rp0 * k0, Rp1 * k1, h, l);          // A~ row 2t + 1
+                *reinterpret_cast<uint32_t*>(smem + S::A_HI + o1) = h;
+                *reinterpret_cast<uint32_t*>(smem + S::A_LO + o1) = l;
+                *reinterpret_cast<uint32_t*>(smem + S::BT + o0) = pack_bf16(b * F0 * k0 - bcd * bt10, b * F1 * k1 - bcd * bt11);
+                *reinterpret_cast<uint32_t*>(smem + S::BT + o1) = pack_bf16(bt10, bt11);
+                split2(F0 * q0, F1 * q1, h, l);            // Q~ row t
+                *reinterpret_cast<uint32_t*>(smem + S::Q_HI + oq) = h;
+                *reinterpret_cast<uint32_t*>(smem + S::Q_LO + oq) = l;
+                Fp0 = F0; Fp1 = F1; Rp0 = R0; Rp1 = R1;
             }
         }
         fence_async_smem();
@@ -507,19 +508,12 @@ hdla_chunk_kernel(Plan pl, K1Args args, const __grid_constant__ CUtensorMap tm_q
             uint32_t pk[32];
             uint32_t mbh[16], mbl[16];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float m0 = row ? row[2 * i] : 0.f, m1 = row ? row[2 * i + 1] : 0.f;
-                pk[i] = pack_bf16(m0, m1);
-                const float mb = m0 * betav[32 * hf + i];   // column 2t of M, t = 32 hf + i
-                uint16_t h, l;
-                split1(mb, h, l);
-                if (i & 1) {
-                    mbh[i >> 1] |= static_cast<uint32_t>(h) << 16;
-                    mbl[i >> 1] |= static_cast<uint32_t>(l) << 16;
-                } else {
-                    mbh[i >> 1] = h;
-                    mbl[i >> 1] = l;
-                }
+            for (int i = 0; i < 32; ++i) pk[i] = row ? pack_bf16(row[2 * i], row[2 * i + 1]) : 0u;
+            // M Diag(beta) on columns 2t of M, t = 32 hf + 2 i2, 32 hf + 2 i2 + 1 (pairs of t)
+#pragma unroll
+            for (int i2 = 0; i2 < 16; ++i2) {
+                const float m0 = row ? row[4 * i2] : 0.f, m1 = row ? row[4 * i2 + 2] : 0.f;
+                split2(m0 * betav[32 * hf + 2 * i2], m1 * betav[32 * hf + 2 * i2 + 1], mbh[i2], mbl[i2]);
             }
             tmem_st32(tmem + lane_base + TM + 32 * hf, pk);
             __syncthreads();   // every row of M read: its region takes the M Diag(beta) tiles
@@ -669,22 +663,25 @@ hdla_chunk_kernel(Plan pl, K1Args args, const __grid_constant__ CUtensorMap tm_q
                 }
             }
             // Q'[t][c] = e^{a_c} (Q~[t][c] - Zq[c][t]), c = lane; Q~ from its hi and lo tiles. Q'_j is stored
-            // as bf16 hi (rows 0-63) and lo (rows 64-127) of a [128][128] block.
+            // as a bf16 [128][128] block whose rows 32 g .. 32 g + 15 hold the hi parts of tokens 16 g .. 16 g + 15
+            // and rows 32 g + 16 .. 32 g + 31 their lo parts: one product of the block with S_{j-1} then puts a
+            // token's two partial outputs in lanes l and l + 16 of the same warp.
             const int c = s;
             __nv_bfloat16* Qcol = args.Qm + unit * (size_t)(2 * HCK * HD) + c;
 #pragma unroll 1
             for (int p = 0; p < 2; ++p) {
                 float x[32];
                 tmem_ld32(tmem + lane_base + TM + 32 * p, x);
-#pragma unroll 4
+#pragma unroll
                 for (int i2 = 0; i2 < 32; ++i2) {
                     const int t = 32 * p + i2;
                     const uint32_t oq = sw_bf16(t, c, HCK);
                     const float qt = lds_bf16(sb + S::Q_HI + oq) + lds_bf16(sb + S::Q_LO + oq);
                     uint16_t h, l;
                     split1(ei * (qt - x[i2]), h, l);
-                    reinterpret_cast<uint16_t*>(Qcol)[(size_t)t * HD] = h;
-                    reinterpret_cast<uint16_t*>(Qcol)[(size_t)(HCK + t) * HD] = l;
+                    const int rh = 32 * (t >> 4) + (t & 15);
+                    reinterpret_cast<uint16_t*>(Qcol)[(size_t)rh * HD] = h;
+                    reinterpret_cast<uint16_t*>(Qcol)[(size_t)(rh + 16) * HD] = l;
                 }
             }
         } else {
@@ -730,16 +727,17 @@ hdla_chunk_kernel(Plan pl, K1Args args, const __grid_constant__ CUtensorMap tm_q
 // ================================================================================================
 
 constexpr int NV = 32;       // state columns per chain CTA
-constexpr int K2T = 160;     // warps 0-3: the state (thread = key channel = tensor-memory lane); warp 4: copies
+constexpr int K2T = 192;     // warps 0-3: the state (thread = key channel = tensor-memory lane); 4: copies; 5: MMAs
+constexpr int K2S = 2;       // stages of the per-chunk maps in shared memory
+constexpr int K2PF = 4;      // chunks between the L2 prefetch of a chunk's maps and their copy into shared memory
 
+// Shared memory of the chain kernel. A stage holds one chunk's P_j (bf16 [128][128]), Q'_j (bf16 [128][128], hi/lo
+// rows interleaved by 16), this CTA's columns of c_j (fp32 [128][32]) and of the chunk-local outputs O_j
+// (fp32 [64][32]), all in the TMA's 128-byte swizzled layout.
 struct K2Smem {
-    static constexpr int P0 = 0;                  // P_j: bf16 [128][128] swizzled, two buffers
-    // Q'_j hi and lo: bf16 swizzled tiles of 192 rows (two 64-column halves each); chunk j's 64 rows at
-    // row 64 (j % 2); rows 128-191 stay zero
-    static constexpr int QHALF = 192 * 128;
-    static constexpr int QH = 2 * 32768;
-    static constexpr int QL = QH + 2 * QHALF;
-    static constexpr int SB = QL + 2 * QHALF;     // S_{j-1} hi: bf16 [128][NV] core-matrix tiles, two buffers
+    static constexpr int STAGE = 32768 + 32768 + 16384 + 8192;
+    static constexpr int P_ = 0, Q_ = 32768, C_ = 65536, O_ = 81920;
+    static constexpr int SB = K2S * STAGE;        // S_{j-1} hi: bf16 [128][NV] core-matrix tiles, two buffers
     static constexpr int SBB = 128 * NV * 2;
     static constexpr int SL = SB + 2 * SBB;       // S_{j-1} lo, two buffers
     static constexpr int BAR = SL + 2 * SBB;
@@ -748,12 +746,17 @@ struct K2Smem {
 static_assert(K2Smem::TOTAL <= 227 * 1024, "shared memory budget");
 
 struct K2Args {
-    const __nv_bfloat16* P; const float* Cm; const float* S0;
-    float* o; float* ST; int* status;
+    const float* S0; float* o; float* ST; int* status;
 };
 
+__device__ __forceinline__ void prefetch_l2_tile(const CUtensorMap* map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 :: "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y) : "memory");
+}
+
 __global__ void __launch_bounds__(K2T, 1)
-hdla_chain_kernel(Plan pl, K2Args args, const __grid_constant__ CUtensorMap tm_P, const __grid_constant__ CUtensorMap tm_Q) {
+hdla_chain_kernel(Plan pl, K2Args args, const __grid_constant__ CUtensorMap tm_P, const __grid_constant__ CUtensorMap tm_Q,
+                  const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_O) {
     using S = K2Smem;
     extern __shared__ __align__(1024) unsigned char smem[];
     const uint32_t sb = smem_addr(smem);
@@ -762,59 +765,112 @@ hdla_chain_kernel(Plan pl, K2Args args, const __grid_constant__ CUtensorMap tm_P
         return;
     }
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::BAR);
-    uint64_t* full = bars + 0;     // [2] P_j and Q'_j landed
-    uint64_t* freed = bars + 2;    // [2] both products of the chunk that used the buffer are done
-    uint64_t* mS = bars + 4;       // the chain product of the chunk
-    // [2] the output product of the chunks using accumulator j % 2: one barrier per accumulator, so that
-    // the commit of chunk j + 1 cannot complete a phase before the wait for chunk j has seen its own
-    uint64_t* mO = bars + 5;
-    uint64_t* drain = bars + 7;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 8);
+    uint64_t* full = bars + 0;            // [K2S] a chunk's maps landed
+    uint64_t* freed = bars + K2S;         // [K2S] the stage was read by both products and by the state warps (2 arrivals)
+    uint64_t* mS = bars + 2 * K2S;        // the chain product of the chunk (issuer -> state warps)
+    uint64_t* mO = bars + 2 * K2S + 1;    // [2] the output product of the chunks using accumulator j % 2
+    uint64_t* ready = bars + 2 * K2S + 3; // S_{j-1} tiles written (4 arrivals, one per state warp; -> issuer)
+    uint64_t* drain = bars + 2 * K2S + 4;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * K2S + 5);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int T = pl.T;
     const int NC = (T + HCK - 1) / HCK;
     constexpr int kSlices = HD / NV;
+    const int slice = blockIdx.x % kSlices;
     const size_t bh = blockIdx.x / kSlices;
-    const int n0 = (blockIdx.x % kSlices) * NV;
+    const int n0 = slice * NV;
     const long long wl = pl.wait_cycles;
 
     if (tid == 0) {
-        for (int i = 0; i < 8; ++i) mbar_init(bars + i, 1);
+        for (int u = 0; u < K2S; ++u) {
+            mbar_init(&full[u], 1);
+            mbar_init(&freed[u], 2);
+        }
+        mbar_init(mS, 1);
+        mbar_init(&mO[0], 1);
+        mbar_init(&mO[1], 1);
+        mbar_init(ready, 4);
+        mbar_init(drain, 1);
         mbar_fence_init();
     }
-    // the third block of 64 Q' rows is never loaded: rows 64-127 of the output product read it
-    for (int i = tid; i < 4 * 64 * 32; i += K2T) {
-        const int b = i / (64 * 32), e = i % (64 * 32);   // half-tile b of Q' hi, hi, lo, lo
-        reinterpret_cast<uint32_t*>(smem + S::QH + b * S::QHALF + 128 * 128)[e] = 0u;
-    }
     if (warp == 0) tmem_alloc(tmem_holder, 128);
-    fence_async_smem();
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    const uint32_t tmem = *tmem_holder;   // columns 0-31: S_j = P_j S_{j-1}; 32-95: two output accumulators
+    const uint32_t tmem = *tmem_holder;   // columns 0-31: P_j S_{j-1}; 32-95: two output accumulators
     bool failed = false;
 
     if (warp == 4) {
-        // ---- copies: P_j and Q'_j of chunk j into buffer j % 2, once the products of chunk j - 2 are done
+        // ---- copies. Chunk j's maps go to stage j % K2S once the stage's previous chunk is done with; the maps of
+        // chunk j + K2PF are prefetched into L2 at the same time.
+        auto unit_of = [&](int jj) { return (size_t)jj * pl.BH + bh; };
+        auto prefetch = [&](int jj) {
+            const int y = static_cast<int>(unit_of(jj) * HD);
+            prefetch_l2_tile(&tm_P, 0, y);
+            prefetch_l2_tile(&tm_P, 64, y);
+            prefetch_l2_tile(&tm_Q, 0, y);
+            prefetch_l2_tile(&tm_Q, 64, y);
+            prefetch_l2_tile(&tm_C, n0, y);
+            prefetch_l2_tile(&tm_O, n0, static_cast<int>(bh * T + (size_t)jj * HCK));
+        };
         int last = -1;
+        if (lane == 0)
+            for (int jj = 0; jj < K2PF && jj < NC; ++jj) prefetch(jj);
         for (int j = 0; j < NC && lane == 0; ++j) {
-            const int u = j & 1;
-            if (j >= 2 && !mbar_wait(&freed[u], ((j - 2) >> 1) & 1, wl)) { failed = true; break; }
-            mbar_expect_tx(&full[u], 32768 + 32768);
-            const int yP = static_cast<int>((bh * NC + j) * HD), yQ = static_cast<int>((bh * NC + j) * 2 * HCK);
+            const int u = j % K2S;
+            if (j >= K2S && !mbar_wait(&freed[u], ((j - K2S) / K2S) & 1, wl)) { failed = true; break; }
+            if (j + K2PF < NC) prefetch(j + K2PF);
+            mbar_expect_tx(&full[u], S::STAGE);
+            const int y = static_cast<int>(unit_of(j) * HD);
+            unsigned char* st = smem + u * S::STAGE;
             for (int h = 0; h < 2; ++h) {
-                tma_load_2d(smem + S::P0 + u * 32768 + h * 16384, &tm_P, 64 * h, yP, &full[u]);
-                tma_load_2d(smem + S::QH + h * S::QHALF + u * 8192, &tm_Q, 64 * h, yQ, &full[u]);
-                tma_load_2d(smem + S::QL + h * S::QHALF + u * 8192, &tm_Q, 64 * h, yQ + HCK, &full[u]);
+                tma_load_2d(st + S::P_ + h * 16384, &tm_P, 64 * h, y, &full[u]);
+                tma_load_2d(st + S::Q_ + h * 16384, &tm_Q, 64 * h, y, &full[u]);
             }
+            tma_load_2d(st + S::C_, &tm_C, n0, y, &full[u]);
+            // rows past the end of the sequence read the next head's rows (or zeros past the tensor): unused
+            tma_load_2d(st + S::O_, &tm_O, n0, static_cast<int>(bh * T + (size_t)j * HCK), &full[u]);
             last = j;
         }
         if (failed) {   // (lane 0) wait for the copies in flight before leaving
             atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
-            for (int jj = last - 1; jj <= last; ++jj)
-                if (jj >= 0) mbar_wait(&full[jj & 1], (jj >> 1) & 1, 400000000LL);
+            for (int jj = last - K2S + 1; jj <= last; ++jj)
+                if (jj >= 0) mbar_wait(&full[jj % K2S], (jj / K2S) & 1, 400000000LL);
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        // ---- the products of chunk j, issued by lane 0 once S_{j-1} is in place and the maps have landed:
+        // P_j (S_hi + S_lo) into columns 0-31, then [Q'_hi; Q'_lo] (S_hi + S_lo) into accumulator j % 2
+        const uint32_t idS = idesc_bf16(128, NV, false, true);
+        for (int j = 0; j < NC && lane == 0; ++j) {
+            const int u = j % K2S;
+            if (!mbar_wait(ready, j & 1, wl) || !mbar_wait(&full[u], (j / K2S) & 1, wl)) { failed = true; break; }
+            fence_after_sync();
+            const uint64_t aS = smem_desc_sw128(sb + u * S::STAGE + S::P_, 16, 1024);
+            const uint64_t aO = smem_desc_sw128(sb + u * S::STAGE + S::Q_, 16, 1024);
+            const uint64_t bH = smem_desc(sb + S::SB + (j & 1) * S::SBB, (NV / 8) * 128, 128);
+            const uint64_t bL = smem_desc(sb + S::SL + (j & 1) * S::SBB, (NV / 8) * 128, 128);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t ao = (kk >> 2) * 16384 + (kk & 3) * 32, bo = kk * 2 * (NV / 8) * 128;
+                mma_bf16(tmem, dadd(aS, ao), dadd(bH, bo), idS, kk > 0);
+                mma_bf16(tmem, dadd(aS, ao), dadd(bL, bo), idS, 1u);
+            }
+            mma_commit(mS);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t ao = (kk >> 2) * 16384 + (kk & 3) * 32, bo = kk * 2 * (NV / 8) * 128;
+                mma_bf16(tmem + 32 + 32 * (j & 1), dadd(aO, ao), dadd(bH, bo), idS, kk > 0);
+                mma_bf16(tmem + 32 + 32 * (j & 1), dadd(aO, ao), dadd(bL, bo), idS, 1u);
+            }
+            mma_commit(&mO[j & 1]);
+            mma_commit(&freed[u]);
+        }
+        if (failed) {   // (lane 0) no product may outlive the tensor memory
+            atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
+            mma_commit(drain);
+            mbar_wait(drain, 0, 400000000LL);
         }
         __syncwarp();
     } else {
@@ -836,106 +892,75 @@ hdla_chain_kernel(Plan pl, K2Args args, const __grid_constant__ CUtensorMap tm_P
                 sts128(sb + S::SL + b * S::SBB + r0 + ch * 128, l[0], l[1], l[2], l[3]);
             }
         };
-        // the two products of chunk j (warp 0, lane 0 issues through a predicate)
-        auto issue = [&](int j) -> bool {
-            const int u = j & 1;
-            const uint32_t lead = lane == 0;
+        // a wait of the four state warps: each warp's lane 0 polls, and the group takes one decision (a warp
+        // must not leave the loop while the others go on to the group barrier)
+        auto wait_all = [&](uint64_t* bar, uint32_t parity, uint64_t* bar2, uint32_t parity2) -> bool {
             bool ok = true;
-            if (lead) ok = mbar_wait(&full[u], (j >> 1) & 1, wl);
+            if (lane == 0) ok = mbar_wait(bar, parity, wl) && (bar2 == nullptr || mbar_wait(bar2, parity2, wl));
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-            if (!ok) return false;
-            fence_after_sync();
-            // S_j - c_j = P_j (S_hi + S_lo): the state keeps its fp32 precision in the chain (a chunk whose decay
-            // is weak, such as a short last chunk, has P_j of order one)
-            const uint32_t idS = idesc_bf16(128, NV, false, true);
-            const uint64_t aS = smem_desc_sw128(sb + S::P0 + u * 32768, 16, 1024);
-#pragma unroll
-            for (int term = 0; term < 2; ++term) {
-                const uint64_t bS = smem_desc(sb + (term ? S::SL : S::SB) + (j & 1) * S::SBB, (NV / 8) * 128, 128);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ss_if(tmem, dadd(aS, (kk >> 2) * 16384 + (kk & 3) * 32), dadd(bS, kk * 2 * (NV / 8) * 128), idS,
-                              (term > 0 || kk > 0), lead);
-            }
-            commit_if(mS, lead);
-            // O = Q'_hi S_hi + Q'_lo S_hi + Q'_hi S_lo over rows 64u .. 64u + 127 of the Q' tiles
-            const uint32_t qa[3] = {sb + S::QH, sb + S::QL, sb + S::QH};
-            const uint32_t sbm[3] = {sb + S::SB, sb + S::SB, sb + S::SL};
-#pragma unroll
-            for (int term = 0; term < 3; ++term) {
-                const uint64_t aO = smem_desc_sw128(qa[term] + u * 8192, 16, 1024);
-                const uint64_t bO = smem_desc(sbm[term] + (j & 1) * S::SBB, (NV / 8) * 128, 128);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ss_if(tmem + 32 + 32 * (j & 1), dadd(aO, (kk >> 2) * S::QHALF + (kk & 3) * 32),
-                              dadd(bO, kk * 2 * (NV / 8) * 128), idS, (term > 0 || kk > 0), lead);
-            }
-            commit_if(&mO[j & 1], lead);
-            commit_if(&freed[u], lead);
-            return true;
+            return !named_sync_or(1, 128, !ok);
         };
+        // output rows: warp g, lane l holds token t = 16 g + (l % 16) and writes columns 16 (l / 16) .. + 15
+        const int tok = 16 * warp + (lane & 15), cseg = 16 * (lane >> 4);
         write_state(0);
         fence_async_smem();
         fence_before_sync();
-        named_sync(1, 128);
-        fence_after_sync();
-        if (NC > 0 && warp == 0 && !issue(0)) failed = true;
-        if (named_sync_or(1, 128, failed)) failed = true;
-
-        for (int j = 0; j < NC && !failed; ++j) {
-            const size_t unit = bh * (size_t)NC + j;
-            // c_j (rows i, this CTA's columns) and the chunk-local outputs O_j (rows t = i < 64)
-            float4 cv[NV / 4], ov[NV / 4];
-            const float4* csrc = reinterpret_cast<const float4*>(args.Cm + unit * (size_t)(HD * HD) + (size_t)i * HD + n0);
-#pragma unroll
-            for (int q4 = 0; q4 < NV / 4; ++q4) cv[q4] = csrc[q4];
-            const int valid = min(HCK, T - j * HCK);
-            float* orow = args.o + (bh * (size_t)T + (size_t)j * HCK + i) * HD + n0;
-            const bool has_o = i < valid;
-#pragma unroll
-            for (int q4 = 0; q4 < NV / 4; ++q4)
-                ov[q4] = has_o ? reinterpret_cast<const float4*>(orow)[q4] : make_float4(0.f, 0.f, 0.f, 0.f);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ready);
+        for (int j = 0; j < NC; ++j) {
+            const int u = j % K2S;
+            const uint32_t stg = sb + u * S::STAGE;
             // S_j = P_j S_{j-1} + c_j
-            bool ok = true;
-            if ((i & 31) == 0) ok = mbar_wait(mS, j & 1, wl);
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-            if (named_sync_or(1, 128, !ok)) { failed = true; break; }
+            if (!wait_all(mS, j & 1, &full[u], (j / K2S) & 1)) { failed = true; break; }
             fence_after_sync();
             {
                 float x[32];
                 tmem_ld32(tmem + lane_base, x);
 #pragma unroll
-                for (int q4 = 0; q4 < NV / 4; ++q4) {
-                    st[4 * q4 + 0] = x[4 * q4 + 0] + cv[q4].x;
-                    st[4 * q4 + 1] = x[4 * q4 + 1] + cv[q4].y;
-                    st[4 * q4 + 2] = x[4 * q4 + 2] + cv[q4].z;
-                    st[4 * q4 + 3] = x[4 * q4 + 3] + cv[q4].w;
+                for (int ch = 0; ch < NV / 4; ++ch) {   // c_j row i, columns 4 ch .. 4 ch + 3 (fp32 swizzled box)
+                    float4 c4;
+                    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(c4.x), "=f"(c4.y), "=f"(c4.z), "=f"(c4.w)
+                                 : "r"(stg + S::C_ + swz(i, ch)));
+                    st[4 * ch + 0] = x[4 * ch + 0] + c4.x;
+                    st[4 * ch + 1] = x[4 * ch + 1] + c4.y;
+                    st[4 * ch + 2] = x[4 * ch + 2] + c4.z;
+                    st[4 * ch + 3] = x[4 * ch + 3] + c4.w;
                 }
             }
-            if (j + 1 < NC) write_state((j + 1) & 1);
-            fence_async_smem();
+            if (j + 1 < NC) {
+                write_state((j + 1) & 1);
+                fence_async_smem();
+            }
             fence_before_sync();
-            named_sync(1, 128);
-            fence_after_sync();
-            if (j + 1 < NC && warp == 0 && !issue(j + 1)) failed = true;
-            // o_t += Q'_t S_{j-1} for the chunk's tokens (rows 0-63 of the output accumulator)
-            ok = true;
-            if ((i & 31) == 0) ok = mbar_wait(&mO[j & 1], (j >> 1) & 1, wl);
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-            if (named_sync_or(1, 128, failed || !ok)) { failed = true; break; }
+            __syncwarp();
+            if (lane == 0 && j + 1 < NC) mbar_arrive(ready);
+            // o_t = O_t + Q'_t S_{j-1}: a token's hi and lo partial outputs sit in lanes l and l + 16
+            if (!wait_all(&mO[j & 1], (j >> 1) & 1, nullptr, 0)) { failed = true; break; }
             fence_after_sync();
             {
                 float x[32];
                 tmem_ld32(tmem + lane_base + 32 + 32 * (j & 1), x);
-                if (has_o) {
 #pragma unroll
-                    for (int q4 = 0; q4 < NV / 4; ++q4)
-                        reinterpret_cast<float4*>(orow)[q4] =
-                            make_float4(ov[q4].x + x[4 * q4], ov[q4].y + x[4 * q4 + 1], ov[q4].z + x[4 * q4 + 2],
-                                        ov[q4].w + x[4 * q4 + 3]);
+                for (int e = 0; e < 32; ++e) x[e] += __shfl_xor_sync(0xffffffffu, x[e], 16);
+                const int valid = min(HCK, T - j * HCK);
+                if (tok < valid) {
+                    const bool upper = lane >= 16;   // (selects keep x in registers)
+                    float4* orow = reinterpret_cast<float4*>(args.o + (bh * (size_t)T + (size_t)j * HCK + tok) * HD + n0 + cseg);
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        float4 ol;
+                        asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(ol.x), "=f"(ol.y), "=f"(ol.z), "=f"(ol.w)
+                                     : "r"(stg + S::O_ + swz(tok, 4 * (lane >> 4) + q4)));
+                        orow[q4] = make_float4(ol.x + (upper ? x[16 + 4 * q4] : x[4 * q4]),
+                                               ol.y + (upper ? x[17 + 4 * q4] : x[4 * q4 + 1]),
+                                               ol.z + (upper ? x[18 + 4 * q4] : x[4 * q4 + 2]),
+                                               ol.w + (upper ? x[19 + 4 * q4] : x[4 * q4 + 3]));
+                    }
                 }
             }
             fence_before_sync();
+            named_sync(1, 128);   // every state warp is done with the stage's c_j and O_j
+            if (tid == 0) mbar_arrive(&freed[u]);
         }
         if (!failed && args.ST) {
             float* dst = args.ST + (bh * HD + i) * HD + n0;
@@ -943,11 +968,7 @@ hdla_chain_kernel(Plan pl, K2Args args, const __grid_constant__ CUtensorMap tm_P
             for (int q4 = 0; q4 < NV / 4; ++q4)
                 reinterpret_cast<float4*>(dst)[q4] = make_float4(st[4 * q4], st[4 * q4 + 1], st[4 * q4 + 2], st[4 * q4 + 3]);
         }
-        if (failed && i == 0) {   // the issuing thread: no product may outlive the tensor memory
-            atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
-            mma_commit(drain);
-            mbar_wait(drain, 0, 400000000LL);
-        }
+        if (failed && lane == 0) atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
     }
     fence_before_sync();
     __syncthreads();
@@ -962,7 +983,8 @@ bool hdla_tc_supported(const Plan& pl) {
     return pl.mode == DPLR_HDLA && pl.bf16 && pl.dk == HD && pl.dv == HD;
 }
 
-// Workspace of the tensor-core HDLA path after the 256-byte status word: per (head, chunk) unit,
+// Workspace of the tensor-core HDLA path after the 256-byte status word: per (chunk, head) unit, chunk-major
+// (the chain reads one chunk of every head at a time),
 // P_j bf16 [128][128], then c_j fp32 [128][128], then Q'_j bf16 [2][64][128] (hi rows, then lo rows).
 void hdla_tc_offsets(const Plan& pl, size_t* off_P, size_t* off_c, size_t* off_Q, size_t* total) {
     const size_t units = (size_t)pl.BH * (size_t)((pl.T + HCK - 1) / HCK);
@@ -1010,22 +1032,23 @@ cudaError_t launch_hdla_chain(const Plan& pl, const float* S0, float* o, float* 
     hdla_tc_offsets(pl, &oP, &oC, &oQ, &total);
     char* ws = static_cast<char*>(workspace);
     K2Args a;
-    a.P = reinterpret_cast<const __nv_bfloat16*>(ws + oP);
-    a.Cm = reinterpret_cast<const float*>(ws + oC);
     a.S0 = S0; a.o = o; a.ST = ST;
     a.status = reinterpret_cast<int*>(ws);
-    CUtensorMap mP, mQ;
+    CUtensorMap mP, mQ, mC, mO;
     std::memset(&mP, 0, sizeof(mP)); std::memset(&mQ, 0, sizeof(mQ));
+    std::memset(&mC, 0, sizeof(mC)); std::memset(&mO, 0, sizeof(mO));
     const int NC = (pl.T + HCK - 1) / HCK;
     if (NC > 0) {
         const uint64_t units = (uint64_t)pl.BH * (uint64_t)NC;
         if (!tensor_map_2d(&mP, ws + oP, true, units * HD, HD, HD, 64) ||
-            !tensor_map_2d(&mQ, ws + oQ, true, units * 2 * HCK, HD, HCK, 64))
+            !tensor_map_2d(&mQ, ws + oQ, true, units * HD, HD, HD, 64) ||
+            !tensor_map_2d(&mC, ws + oC, false, units * HD, HD, HD, 32) ||
+            !tensor_map_2d(&mO, o, false, (uint64_t)pl.BH * pl.T, HD, HCK, 32))
             return cudaErrorInvalidValue;
     }
     cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(hdla_chain_kernel), K2Smem::TOTAL, g_k2_smem_set);
     if (e != cudaSuccess) return e;
-    hdla_chain_kernel<<<(unsigned)(pl.BH * (HD / NV)), K2T, K2Smem::TOTAL, s>>>(pl, a, mP, mQ);
+    hdla_chain_kernel<<<(unsigned)(pl.BH * (HD / NV)), K2T, K2Smem::TOTAL, s>>>(pl, a, mP, mQ, mC, mO);
     return cudaGetLastError();
 }
 
