@@ -42,6 +42,7 @@
 // status word and the kernel drains its own copies and products before it frees tensor memory.
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cstring>
 
 #include "dplr_internal.h"
@@ -54,7 +55,7 @@ using namespace sm100;
 
 constexpr int HD = 128;    // dk = dv
 constexpr int HCK = 64;    // tokens per chunk
-constexpr int K1T = 256;   // threads of the chunk kernel: two threads per tensor-memory lane
+constexpr int K1T = 512;   // threads of the chunk kernel: four per tensor-memory lane
 constexpr int kLdX = 68;   // row stride (floats) of the inverse's fp32 blocks (16-byte rows, 4 banks apart)
 
 // ---- 128-byte-swizzled tiles (the layout the TMA writes with SWIZZLE_128B): rows of 128 bytes whose
@@ -126,6 +127,19 @@ __device__ __forceinline__ void commit_if(uint64_t* mbar, uint32_t issue) {
 }
 __device__ __forceinline__ uint64_t dadd(uint64_t desc, uint32_t bytes) { return desc + static_cast<uint64_t>(bytes >> 4); }
 
+// 16 consecutive fp32 columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // Warp-level C[16x8] = A[16xK] B[Kx8] (mma.sync m16n8k8 tf32, fp32 accumulate) with the operands
 // rounded to tf32 (cvt.rna); A, B row-major fp32 in shared memory. Fragments as in the PTX ISA.
 __device__ __forceinline__ void warp_mma_tf32_rn(const float* A, int lda, const float* B, int ldb, int K, float (&c)[4]) {
@@ -145,7 +159,7 @@ __device__ __forceinline__ void warp_mma_tf32_rn(const float* A, int lda, const 
     }
 }
 
-// In place, for the 128 threads t of one group (named barrier `bar`): X (64 x 64, row stride kLdX)
+// In place, for the 256 threads t of one group (named barrier `bar`): X (64 x 64, row stride kLdX)
 // holds a strictly lower-triangular L on entry (zeros on and above the diagonal) and
 // M = (I + L)^{-1} on exit. Diagonal 16 x 16 blocks by substitution (one column per thread), then
 // the block merges [[A,0],[C,B]]^{-1} = [[A^{-1},0],[-B^{-1} C A^{-1}, B^{-1}]] for 16 -> 32 -> 64,
@@ -171,39 +185,36 @@ __device__ __forceinline__ void inv64_inplace(float* X, int t, uint32_t bar) {
             }
             m[i] = acc0 + acc1;
         }
-        named_sync(bar, 128);   // every row of the diagonal blocks read
+        named_sync(bar, 256);   // every row of the diagonal blocks read
 #pragma unroll
         for (int i = 0; i < 16; ++i) X[(o + i) * kLdX + o + jj] = m[i];
     } else {
-        named_sync(bar, 128);
+        named_sync(bar, 256);
     }
-    named_sync(bar, 128);
-    {   // 16 -> 32 for the pairs of diagonal blocks (0,1) and (2,3): one 16 x 8 tile per warp
-        const int p = w >> 1, ct = w & 1, o = 32 * p;
+    named_sync(bar, 256);
+    {   // 16 -> 32 for the pairs of diagonal blocks (0,1) and (2,3): one 16 x 8 tile for each of warps 0-3
+        const int p = (w >> 1) & 1, ct = w & 1, o = 32 * p;
         float c[4];
-        warp_mma_tf32_rn(X + (o + 16) * kLdX + o, kLdX, X + o * kLdX + o + 8 * ct, kLdX, 16, c);   // T = C A^{-1}
-        named_sync(bar, 128);
-        store_tile_16x8(X + (o + 16) * kLdX + o + 8 * ct, kLdX, c, 1.f);
-        named_sync(bar, 128);
-        warp_mma_tf32_rn(X + (o + 16) * kLdX + o + 16, kLdX, X + (o + 16) * kLdX + o + 8 * ct, kLdX, 16, c);   // B^{-1} T
-        named_sync(bar, 128);
-        store_tile_16x8(X + (o + 16) * kLdX + o + 8 * ct, kLdX, c, -1.f);
-        named_sync(bar, 128);
+        if (w < 4) warp_mma_tf32_rn(X + (o + 16) * kLdX + o, kLdX, X + o * kLdX + o + 8 * ct, kLdX, 16, c);   // C A^{-1}
+        named_sync(bar, 256);
+        if (w < 4) store_tile_16x8(X + (o + 16) * kLdX + o + 8 * ct, kLdX, c, 1.f);
+        named_sync(bar, 256);
+        if (w < 4) warp_mma_tf32_rn(X + (o + 16) * kLdX + o + 16, kLdX, X + (o + 16) * kLdX + o + 8 * ct, kLdX, 16, c);
+        named_sync(bar, 256);
+        if (w < 4) store_tile_16x8(X + (o + 16) * kLdX + o + 8 * ct, kLdX, c, -1.f);
+        named_sync(bar, 256);
     }
-    {   // 32 -> 64: rows 32-63, columns 0-31; two 16 x 8 tiles per warp (column block 8w)
-        float c0[4], c1[4];
-        warp_mma_tf32_rn(X + 32 * kLdX, kLdX, X + 8 * w, kLdX, 32, c0);
-        warp_mma_tf32_rn(X + 48 * kLdX, kLdX, X + 8 * w, kLdX, 32, c1);
-        named_sync(bar, 128);
-        store_tile_16x8(X + 32 * kLdX + 8 * w, kLdX, c0, 1.f);
-        store_tile_16x8(X + 48 * kLdX + 8 * w, kLdX, c1, 1.f);
-        named_sync(bar, 128);
-        warp_mma_tf32_rn(X + 32 * kLdX + 32, kLdX, X + 32 * kLdX + 8 * w, kLdX, 32, c0);
-        warp_mma_tf32_rn(X + 48 * kLdX + 32, kLdX, X + 32 * kLdX + 8 * w, kLdX, 32, c1);
-        named_sync(bar, 128);
-        store_tile_16x8(X + 32 * kLdX + 8 * w, kLdX, c0, -1.f);
-        store_tile_16x8(X + 48 * kLdX + 8 * w, kLdX, c1, -1.f);
-        named_sync(bar, 128);
+    {   // 32 -> 64: rows 32-63, columns 0-31; one 16 x 8 tile per warp (row block 16 (w / 4), column block 8 (w % 4))
+        const int rb = w >> 2, cb = w & 3;
+        float c[4];
+        warp_mma_tf32_rn(X + (32 + 16 * rb) * kLdX, kLdX, X + 8 * cb, kLdX, 32, c);
+        named_sync(bar, 256);
+        store_tile_16x8(X + (32 + 16 * rb) * kLdX + 8 * cb, kLdX, c, 1.f);
+        named_sync(bar, 256);
+        warp_mma_tf32_rn(X + (32 + 16 * rb) * kLdX + 32, kLdX, X + 32 * kLdX + 8 * cb, kLdX, 32, c);
+        named_sync(bar, 256);
+        store_tile_16x8(X + (32 + 16 * rb) * kLdX + 8 * cb, kLdX, c, -1.f);
+        named_sync(bar, 256);
     }
 }
 
@@ -228,7 +239,7 @@ struct K1Smem {
     static constexpr int MB_LO = R0 + 16384;      //   bf16 [128][64]
     static constexpr int QA_LO = R0 + 32768;      //   QA^T lo: bf16 [128][64]
     static constexpr int VEC = R0 + 65536;        // fp32 vectors (see below)
-    static constexpr int BAR = VEC + 4096;        // mbarriers and the tensor-memory address (vectors: 896 floats)
+    static constexpr int BAR = VEC + 6144;        // mbarriers and the tensor-memory address (vectors: 1408 floats)
     static constexpr int TOTAL = BAR + 64;
 };
 static_assert(K1Smem::X22 + 64 * kLdX * 4 <= K1Smem::R0 + 65536, "inverse blocks fit the shared region");
@@ -248,9 +259,25 @@ struct K1Args {
     float* o; __nv_bfloat16* P; float* Cm; __nv_bfloat16* Qm; int* status;
 };
 
+// Bulk stores (shared -> global) by tensor map, and their completion.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];"
+                 :: "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(src) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void prefetch_l2_tile(const CUtensorMap* map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 :: "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y) : "memory");
+}
+
+// Persistent: CTA b takes the units b, b + gridDim.x, ... in head-major order (chunk j of head bh is unit
+// bh * NC + j), so the CTAs running at once read neighbouring chunks. The next unit's inputs are prefetched
+// into L2 while the current one is computed.
 __global__ void __launch_bounds__(K1T, 1)
 hdla_chunk_kernel(Plan pl, K1Args args, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_l) {
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_l,
+                  const __grid_constant__ CUtensorMap tm_P, const __grid_constant__ CUtensorMap tm_Q) {
     using S = K1Smem;
     extern __shared__ __align__(1024) unsigned char smem[];
     const uint32_t sb = smem_addr(smem);
@@ -268,18 +295,13 @@ hdla_chunk_kernel(Plan pl, K1Args args, const __grid_constant__ CUtensorMap tm_q
     float* betav = vec + 64;    // [64]
     float* ea = vec + 128;      // [128] e^{a}
     float* gam = vec + 256;     // [128] e^{G_C}
-    float* gq = vec + 384;      // [3][128] G after tokens 15, 31, 47 (the start of token quarters 1-3)
-    float* av = vec + 768;      // [128] a = G_C / 2
+    float* gq = vec + 384;      // [7][128] G after tokens 7, 15, ..., 55 (the start of token eighths 1-7)
+    float* av = vec + 1280;     // [128] a = G_C / 2
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int NC = (pl.T + HCK - 1) / HCK;
-    const int j = blockIdx.x % NC;
-    const size_t bh = blockIdx.x / NC;
-    const int valid = min(HCK, pl.T - j * HCK);
-    const size_t tok0 = bh * (size_t)pl.T + (size_t)j * HCK;
-    const size_t unit = (size_t)j * pl.BH + bh;   // maps are stored chunk-major: a chunk's heads side by side
+    const long long total = (long long)pl.BH * NC;
     const long long wl = pl.wait_cycles;
-    const bool full = valid == HCK;
 
     if (tid == 0) {
         mbar_init(mb_tma, 1);
@@ -293,7 +315,33 @@ hdla_chunk_kernel(Plan pl, K1Args args, const __grid_constant__ CUtensorMap tm_q
     fence_after_sync();
     const uint32_t tmem = *tmem_holder;
     uint32_t mma_phase = 0;   // phases of mb_mma completed so far
+    uint32_t tma_phase = 0;   // phases of mb_tma completed so far
     bool failed = false;
+    bool tma_pending = false;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const int s = tid & 127;   // tensor-memory lane of this thread (row of the chunk's 128-row tiles)
+    const int qd = tid >> 7;   // which quarter of the columns this thread takes in the lane-mapped phases
+
+  for (long long uidx = blockIdx.x; uidx < total && !failed; uidx += gridDim.x) {
+    const int j = static_cast<int>(uidx % NC);
+    const size_t bh = static_cast<size_t>(uidx / NC);
+    const int valid = min(HCK, pl.T - j * HCK);
+    const size_t tok0 = bh * (size_t)pl.T + (size_t)j * HCK;
+    const size_t unit = (size_t)j * pl.BH + bh;   // maps are stored chunk-major: a chunk's heads side by side
+    const bool full = valid == HCK;
+    if (tid == 0 && uidx + gridDim.x < total) {   // the next unit's inputs into L2
+        const long long nx = uidx + gridDim.x;
+        const int jn = static_cast<int>(nx % NC);
+        if (pl.T - jn * HCK >= HCK) {
+            const int y = static_cast<int>((nx / NC) * pl.T + (long long)jn * HCK);
+            for (int h = 0; h < 2; ++h) {
+                prefetch_l2_tile(&tm_k, 64 * h, y);
+                prefetch_l2_tile(&tm_q, 64 * h, y);
+                prefetch_l2_tile(&tm_v, 64 * h, y);
+            }
+            for (int b = 0; b < 4; ++b) prefetch_l2_tile(&tm_l, 32 * b, y);
+        }
+    }
 
     // ---- a1: stage k, q, v and the log-decay of the chunk (TMA; plain loads for a ragged chunk)
     if (full) {
@@ -333,35 +381,33 @@ hdla_chunk_kernel(Plan pl, K1Args args, const __grid_constant__ CUtensorMap tm_q
     }
     if (tid < HCK) betav[tid] = tid < valid ? args.beta[tok0 + tid] : 0.f;
     if (full) {
-        const bool ok = mbar_wait(mb_tma, 0, wl);
+        tma_pending = true;
+        const bool ok = mbar_wait(mb_tma, tma_phase & 1, wl);
         if (__syncthreads_or(!ok)) failed = true;
+        else { tma_pending = false; ++tma_phase; }
     } else {
         __syncthreads();
     }
 
-    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    const int s = tid & 127;   // tensor-memory lane of this thread (row of the chunk's 128-row tiles)
-    const int hf = tid >> 7;   // which half of the columns this thread takes in the lane-mapped phases
-
     if (!failed) {
-        // ---- a2: per-channel sums of the log-decay (G after 32 tokens and at the chunk end),
-        // and c_t = k_t^T Lambda_t k_t per token (one warp per 16 tokens)
+        // ---- a2: per-channel prefixes of the log-decay at every eighth of the chunk and at its end (warps 0-3),
+        // and c_t = k_t^T Lambda_t k_t per token (warps 4-11, eight tokens each)
         if (warp < 4) {
             const int c = tid;
             float G = 0.f;
 #pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {
-#pragma unroll 8
-                for (int t = 16 * qq; t < 16 * qq + 16; ++t) G += lds_f32(sb + S::LAM + sw_f32(t, c, HCK));
-                if (qq < 3) gq[128 * qq + c] = G;
+            for (int e8 = 0; e8 < 8; ++e8) {
+#pragma unroll
+                for (int t = 8 * e8; t < 8 * e8 + 8; ++t) G += lds_f32(sb + S::LAM + sw_f32(t, c, HCK));
+                if (e8 < 7) gq[128 * e8 + c] = G;
             }
             const float a = 0.5f * G;
             av[c] = a;
             ea[c] = __expf(a);
             gam[c] = __expf(G);
-        } else {
-            for (int tt = 0; tt < 16; ++tt) {
-                const int t = 16 * (warp - 4) + tt;
+        } else if (warp < 12) {
+            for (int tt = 0; tt < 8; ++tt) {
+                const int t = 8 * (warp - 4) + tt;
                 float acc = 0.f;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -374,21 +420,27 @@ hdla_chunk_kernel(Plan pl, K1Args args, const __grid_constant__ CUtensorMap tm_q
                 if (lane == 0) cdot[t] = acc;
             }
         }
+        if (tid == 0) bulk_wait_read();   // the previous unit's P_j and Q'_j have left A~ hi / lo
         __syncthreads();
 
         // ---- a3: the decay-scaled factor tiles. Warp w takes key channels 64 (w % 2) .. + 63 (two per lane,
-        // stored as bf16 pairs) and tokens 16 (w / 2) .. + 15, starting from the quarter's prefix of G.
+        // stored as bf16 pairs) and tokens 8 (w / 2) .. + 7, starting from that eighth's prefix of G.
         {
-            const int c0 = 64 * (warp & 1) + 2 * lane, qq = warp >> 1;
+            const int c0 = 64 * (warp & 1) + 2 * lane, e8 = warp >> 1;
             const float a0 = av[c0], a1 = av[c0 + 1];
-            float G0 = qq ? gq[128 * (qq - 1) + c0] : 0.f, G1 = qq ? gq[128 * (qq - 1) + c0 + 1] : 0.f;
+            float G0 = e8 ? gq[128 * (e8 - 1) + c0] : 0.f, G1 = e8 ? gq[128 * (e8 - 1) + c0 + 1] : 0.f;
             float Fp0 = __expf(G0 - a0), Fp1 = __expf(G1 - a1), Rp0 = __expf(a0 - G0), Rp1 = __expf(a1 - G1);
-#pragma unroll 2
-            for (int tt = 0; tt < 16; ++tt) {
-                const int t = 16 * qq + tt;
-                const float2 ll = *reinterpret_cast<const float2*>(smem + S::LAM + sw_f32(t, c0, HCK));
-                const uint32_t kb = *reinterpret_cast<const uint32_t*>(smem + S::K_ + sw_bf16(t, c0, HCK));
-                const uint32_t qb = *reinterpret_cast<const uint32_t*>(smem + S::Q_ + sw_bf16(t, c0, HCK));
+            // byte offsets of channel c0 inside a swizzled row, for each row residue mod 8
+            const uint32_t col_f32 = (uint32_t)((c0 >> 5) * (HCK * 128) + ((c0 & 3) << 2));
+            const int chunk16 = (c0 & 63) >> 3, chunk32 = (c0 & 31) >> 2;
+#pragma unroll
+            for (int tt = 0; tt < 8; ++tt) {
+                const int t = 8 * e8 + tt;   // t % 8 == tt
+                const uint32_t rowl = (uint32_t)(t * 128) + (uint32_t)(((chunk32 ^ tt)) << 4) + col_f32;
+                const uint32_t rowb = (uint32_t)((c0 >> 6) * (HCK * 128) + t * 128 + ((chunk16 ^ tt) << 4) + ((c0 & 7) << 1));
+                const float2 ll = *reinterpret_cast<const float2*>(smem + S::LAM + rowl);
+                const uint32_t kb = *reinterpret_cast<const uint32_t*>(smem + S::K_ + rowb);
+                const uint32_t qb = *reinterpret_cast<const uint32_t*>(smem + S::Q_ + rowb);
                 const float k0 = __uint_as_float(kb << 16), k1 = __uint_as_float(kb & 0xFFFF0000u);
                 const float q0 = __uint_as_float(qb << 16), q1 = __uint_as_float(qb & 0xFFFF0000u);
                 G0 += ll.x;
@@ -397,7 +449,9 @@ hdla_chunk_kernel(Plan pl, K1Args args, const __grid_constant__ CUtensorMap tm_q
                 const float b = betav[t], bcd = b * cdot[t];
                 const float bt10 = b * Fp0 * k0, bt11 = b * Fp1 * k1;
                 uint32_t h, l;
-                const uint32_t o0 = sw_bf16(2 * t, c0, 128), o1 = sw_bf16(2 * t + 1, c0, 128), oq = sw_bf16(t, c0, HCK);
+                // rows 2t and 2t + 1 of the 128-row tiles (2t % 8 = (2 tt) % 8), row t of the 64-row tile
+                const uint32_t o0 = (uint32_t)((c0 >> 6) * 16384 + (2 * t) * 128 + ((chunk16 ^ ((2 * tt) & 7)) << 4) + ((c0 & 7) << 1));
+                const uint32_t o1 = (uint32_t)((c0 >> 6) * 16384 + (2 * t + 1) * 128 + ((chunk16 ^ ((2 * tt + 1) & 7)) << 4) + ((c0 & 7) << 1));
                 split2(R0 * k0, R1 * k1, h, l);            // A~ row 2t
                 *reinterpret_cast<uint32_t*>(smem + S::A_HI + o0) = h;
                 *reinterpret_cast<uint32_t*>(smem + S::A_LO + o0) = l;
@@ -407,8 +461,8 @@ hdla_chunk_kernel(Plan pl, K1Args args, const __grid_constant__ CUtensorMap tm_q
                 *reinterpret_cast<uint32_t*>(smem + S::BT + o0) = pack_bf16(b * F0 * k0 - bcd * bt10, b * F1 * k1 - bcd * bt11);
                 *reinterpret_cast<uint32_t*>(smem + S::BT + o1) = pack_bf16(bt10, bt11);
                 split2(F0 * q0, F1 * q1, h, l);            // Q~ row t
-                *reinterpret_cast<uint32_t*>(smem + S::Q_HI + oq) = h;
-                *reinterpret_cast<uint32_t*>(smem + S::Q_LO + oq) = l;
+                *reinterpret_cast<uint32_t*>(smem + S::Q_HI + rowb) = h;
+                *reinterpret_cast<uint32_t*>(smem + S::Q_LO + rowb) = l;
                 Fp0 = F0; Fp1 = F1; Rp0 = R0; Rp1 = R1;
             }
         }
@@ -451,75 +505,75 @@ hdla_chunk_kernel(Plan pl, K1Args args, const __grid_constant__ CUtensorMap tm_q
         // ---- a5: L into the inverse's fp32 blocks (strict lower part by token), then M = (I + L)^{-1}
         {
             float* X = reinterpret_cast<float*>(smem + S::R0);
-#pragma unroll 1
-            for (int p = 0; p < 2; ++p) {
-                float x[32];
-                tmem_ld32(tmem + lane_base + TL + 64 * hf + 32 * p, x);
-                const int c0 = 64 * hf + 32 * p;
-                float* dst = nullptr;
-                if (hf == 0) dst = (s < 64) ? X + s * kLdX : X + (64 + (s - 64)) * kLdX;   // X11 or X21 row
-                else if (s >= 64) dst = X + (128 + (s - 64)) * kLdX - 64;                // X22 row, columns shifted
-                if (dst) {
+            float x[32];
+            tmem_ld32(tmem + lane_base + TL + 32 * qd, x);
+            const int c0 = 32 * qd;
+            float* dst = nullptr;   // row s of X11 / X21 (columns 0-63), or of X22 (columns 64-127, shifted)
+            if (qd < 2) dst = X + s * kLdX;
+            else if (s >= 64) dst = X + (128 + (s - 64)) * kLdX - 64;
+            if (dst) {
 #pragma unroll
-                    for (int i = 0; i < 32; i += 4) {
-                        const int c = c0 + i;
-                        float4 y;
-                        y.x = ((c + 0) >> 1) < (s >> 1) ? x[i + 0] : 0.f;
-                        y.y = ((c + 1) >> 1) < (s >> 1) ? x[i + 1] : 0.f;
-                        y.z = ((c + 2) >> 1) < (s >> 1) ? x[i + 2] : 0.f;
-                        y.w = ((c + 3) >> 1) < (s >> 1) ? x[i + 3] : 0.f;
-                        *reinterpret_cast<float4*>(dst + c) = y;
-                    }
+                for (int i = 0; i < 32; i += 4) {
+                    const int c = c0 + i;
+                    float4 y;
+                    y.x = ((c + 0) >> 1) < (s >> 1) ? x[i + 0] : 0.f;
+                    y.y = ((c + 1) >> 1) < (s >> 1) ? x[i + 1] : 0.f;
+                    y.z = ((c + 2) >> 1) < (s >> 1) ? x[i + 2] : 0.f;
+                    y.w = ((c + 3) >> 1) < (s >> 1) ? x[i + 3] : 0.f;
+                    *reinterpret_cast<float4*>(dst + c) = y;
                 }
             }
         }
         __syncthreads();
         {
             float* X = reinterpret_cast<float*>(smem + S::R0);
-            if (warp < 4) inv64_inplace(X, tid, 1);                  // M11 in place of L11
-            else inv64_inplace(X + 128 * kLdX, tid - 128, 2);        // M22 in place of L22
+            if (warp < 8) inv64_inplace(X, tid, 1);                  // M11 in place of L11
+            else inv64_inplace(X + 128 * kLdX, tid - 256, 2);        // M22 in place of L22
             __syncthreads();
-            // 64 -> 128: M21 = -M22 (L21 M11), 32 tiles of 16 x 8 per product, four per warp
+            // 64 -> 128: M21 = -M22 (L21 M11), 32 tiles of 16 x 8 per product: warp w takes column block
+            // w % 8 and row blocks 2 (w / 8), 2 (w / 8) + 1
             float* X11 = X;
             float* X21 = X + 64 * kLdX;
             float* X22 = X + 128 * kLdX;
-            float c[4][4];
+            const int cb = warp & 7, rb0 = 2 * (warp >> 3);
+            float c[2][4];
 #pragma unroll
-            for (int rb = 0; rb < 4; ++rb) warp_mma_tf32_rn(X21 + 16 * rb * kLdX, kLdX, X11 + 8 * warp, kLdX, 64, c[rb]);
+            for (int r = 0; r < 2; ++r) warp_mma_tf32_rn(X21 + 16 * (rb0 + r) * kLdX, kLdX, X11 + 8 * cb, kLdX, 64, c[r]);
             __syncthreads();
 #pragma unroll
-            for (int rb = 0; rb < 4; ++rb) store_tile_16x8(X21 + 16 * rb * kLdX + 8 * warp, kLdX, c[rb], 1.f);
+            for (int r = 0; r < 2; ++r) store_tile_16x8(X21 + 16 * (rb0 + r) * kLdX + 8 * cb, kLdX, c[r], 1.f);
             __syncthreads();
 #pragma unroll
-            for (int rb = 0; rb < 4; ++rb) warp_mma_tf32_rn(X22 + 16 * rb * kLdX, kLdX, X21 + 8 * warp, kLdX, 64, c[rb]);
+            for (int r = 0; r < 2; ++r) warp_mma_tf32_rn(X22 + 16 * (rb0 + r) * kLdX, kLdX, X21 + 8 * cb, kLdX, 64, c[r]);
             __syncthreads();
 #pragma unroll
-            for (int rb = 0; rb < 4; ++rb) store_tile_16x8(X21 + 16 * rb * kLdX + 8 * warp, kLdX, c[rb], -1.f);
+            for (int r = 0; r < 2; ++r) store_tile_16x8(X21 + 16 * (rb0 + r) * kLdX + 8 * cb, kLdX, c[r], -1.f);
             __syncthreads();
         }
 
-        // ---- M as the bf16 A operand of Y (tensor memory), and M Diag(beta) on the even columns
-        // (the columns that meet W) as hi + lo tiles for MW
+        // ---- M as the bf16 A operand of Y (tensor memory), and M Diag(beta) on the even columns (the columns
+        // that meet W) as hi + lo tiles for MW. Thread (s, qd) takes columns 32 qd .. 32 qd + 31 of row s of M.
         {
             const float* X = reinterpret_cast<const float*>(smem + S::R0);
-            const float* row = nullptr;   // columns 64 hf .. 64 hf + 63 of row s of M (nullptr: zero)
-            if (hf == 0) row = (s < 64) ? X + s * kLdX : X + s * kLdX;   // X11 row s or X21 row s - 64
-            else if (s >= 64) row = X + (128 + (s - 64)) * kLdX;          // X22 row s - 64
-            uint32_t pk[32];
-            uint32_t mbh[16], mbl[16];
+            const float* row = nullptr;   // nullptr: zero (above the diagonal blocks)
+            if (qd < 2) row = X + s * kLdX + 32 * qd;                       // X11 row s or X21 row s - 64
+            else if (s >= 64) row = X + (128 + (s - 64)) * kLdX + 32 * (qd - 2);   // X22 row s - 64
+            uint32_t pk[16];
+            uint32_t mbh[8], mbl[8];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) pk[i] = row ? pack_bf16(row[2 * i], row[2 * i + 1]) : 0u;
-            // M Diag(beta) on columns 2t of M, t = 32 hf + 2 i2, 32 hf + 2 i2 + 1 (pairs of t)
+            for (int i = 0; i < 16; ++i) pk[i] = row ? pack_bf16(row[2 * i], row[2 * i + 1]) : 0u;
+            // M Diag(beta) on columns 2t of M, t = 16 qd + 2 i2, 16 qd + 2 i2 + 1 (pairs of t)
 #pragma unroll
-            for (int i2 = 0; i2 < 16; ++i2) {
+            for (int i2 = 0; i2 < 8; ++i2) {
                 const float m0 = row ? row[4 * i2] : 0.f, m1 = row ? row[4 * i2 + 2] : 0.f;
-                split2(m0 * betav[32 * hf + 2 * i2], m1 * betav[32 * hf + 2 * i2 + 1], mbh[i2], mbl[i2]);
+                split2(m0 * betav[16 * qd + 2 * i2], m1 * betav[16 * qd + 2 * i2 + 1], mbh[i2], mbl[i2]);
             }
-            tmem_st32(tmem + lane_base + TM + 32 * hf, pk);
+            tmem_st16(tmem + lane_base + TM + 16 * qd, pk);
+            tmem_wait_st();
             __syncthreads();   // every row of M read: its region takes the M Diag(beta) tiles
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-                const uint32_t off = swz(s, 4 * hf + ch);   // columns t = 32 hf + 8 ch ..
+            for (int ch = 0; ch < 2; ++ch) {
+                const uint32_t off = swz(s, 2 * qd + ch);   // columns t = 16 qd + 8 ch ..
                 sts128(sb + S::MB_HI + off, mbh[4 * ch], mbh[4 * ch + 1], mbh[4 * ch + 2], mbh[4 * ch + 3]);
                 sts128(sb + S::MB_LO + off, mbl[4 * ch], mbl[4 * ch + 1], mbl[4 * ch + 2], mbl[4 * ch + 3]);
             }
@@ -557,38 +611,37 @@ hdla_chunk_kernel(Plan pl, K1Args args, const __grid_constant__ CUtensorMap tm_q
 
     if (!failed) {
         // ---- operand tiles for the last products: Y (bf16, over B~), MW^T hi/lo (tensor memory),
-        // QA^T hi/lo (masked t >= token of s)
-#pragma unroll 1
-        for (int p = 0; p < 2; ++p) {
+        // QA^T hi/lo (masked t >= token of s); thread (s, qd) takes a quarter of the columns
+        {
             float x[32];
-            tmem_ld32(tmem + lane_base + TL + 64 * hf + 32 * p, x);
+            tmem_ld32(tmem + lane_base + TL + 32 * qd, x);
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) {
-                const int c = 64 * hf + 32 * p + 8 * ch;
+                const int c = 32 * qd + 8 * ch;
                 sts128(sb + S::BT + sw_bf16(s, c, 128), pack_bf16(x[8 * ch + 0], x[8 * ch + 1]),
                        pack_bf16(x[8 * ch + 2], x[8 * ch + 3]), pack_bf16(x[8 * ch + 4], x[8 * ch + 5]),
                        pack_bf16(x[8 * ch + 6], x[8 * ch + 7]));
             }
-            tmem_ld32(tmem + lane_base + TMW + 64 * hf + 32 * p, x);
+            tmem_ld32(tmem + lane_base + TMW + 32 * qd, x);
             uint32_t h[16], l[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) split2(x[2 * i], x[2 * i + 1], h[i], l[i]);
-            tmem_st16(tmem + lane_base + TMWH + 32 * hf + 16 * p, h);
-            tmem_st16(tmem + lane_base + TMWL + 32 * hf + 16 * p, l);
+            tmem_st16(tmem + lane_base + TMWH + 16 * qd, h);
+            tmem_st16(tmem + lane_base + TMWL + 16 * qd, l);
         }
         {
-            float x[32];
-            tmem_ld32(tmem + lane_base + TQA + 32 * hf, x);
+            float x[16];
+            tmem_ld16(tmem + lane_base + TQA + 16 * qd, x);
             const int tok_s = s >> 1;
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
+            for (int ch = 0; ch < 2; ++ch) {
                 uint32_t h[4], l[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const int t0 = 32 * hf + 8 * ch + 2 * i;
+                    const int t0 = 16 * qd + 8 * ch + 2 * i;
                     split2(t0 >= tok_s ? x[8 * ch + 2 * i] : 0.f, t0 + 1 >= tok_s ? x[8 * ch + 2 * i + 1] : 0.f, h[i], l[i]);
                 }
-                const uint32_t off = swz(s, 4 * hf + ch);
+                const uint32_t off = swz(s, 2 * qd + ch);
                 sts128(sb + S::V + off, h[0], h[1], h[2], h[3]);       // QA hi over v
                 sts128(sb + S::QA_LO + off, l[0], l[1], l[2], l[3]);
             }
@@ -640,82 +693,89 @@ hdla_chunk_kernel(Plan pl, K1Args args, const __grid_constant__ CUtensorMap tm_q
     }
 
     if (!failed) {
-        // ---- epilogues: P_j, Q'_j (warps 0-3, lane = key channel), c_j, O_j (warps 4-7, lane = value channel)
-        if (hf == 0) {
+        // ---- epilogues: thread (s, qd) takes a quarter of the columns of each result. P_j and Q'_j go to
+        // shared staging tiles over A~ hi and A~ lo (no longer read by then) and leave by TMA bulk stores;
+        // c_j and O_j are stored directly, a column per thread.
+        {   // P_j row i = s: bf16 [128][128]
             const int i = s;
-            __nv_bfloat16* Prow = args.P + (unit * HD + i) * HD;
             const float ei = ea[i], gi = gam[i];
-#pragma unroll 1
-            for (int p = 0; p < 4; ++p) {
-                float x[32];
-                tmem_ld32(tmem + lane_base + TL + 32 * p, x);
+            float x[32];
+            tmem_ld32(tmem + lane_base + TL + 32 * qd, x);
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    uint32_t w[4];
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t w[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int k0 = 32 * p + 8 * ch + 2 * e;
-                        const float p0 = (k0 == i ? gi : 0.f) - ei * x[8 * ch + 2 * e] * ea[k0];
-                        const float p1 = (k0 + 1 == i ? gi : 0.f) - ei * x[8 * ch + 2 * e + 1] * ea[k0 + 1];
-                        w[e] = pack_bf16(p0, p1);
-                    }
-                    *reinterpret_cast<uint4*>(Prow + 32 * p + 8 * ch) = make_uint4(w[0], w[1], w[2], w[3]);
+                for (int e = 0; e < 4; ++e) {
+                    const int k0 = 32 * qd + 8 * ch + 2 * e;
+                    const float p0 = (k0 == i ? gi : 0.f) - ei * x[8 * ch + 2 * e] * ea[k0];
+                    const float p1 = (k0 + 1 == i ? gi : 0.f) - ei * x[8 * ch + 2 * e + 1] * ea[k0 + 1];
+                    w[e] = pack_bf16(p0, p1);
                 }
+                sts128(sb + S::A_HI + sw_bf16(i, 32 * qd + 8 * ch, 128), w[0], w[1], w[2], w[3]);
             }
-            // Q'[t][c] = e^{a_c} (Q~[t][c] - Zq[c][t]), c = lane; Q~ from its hi and lo tiles. Q'_j is stored
-            // as a bf16 [128][128] block whose rows 32 g .. 32 g + 15 hold the hi parts of tokens 16 g .. 16 g + 15
+        }
+        {   // c_j column n = s: c[i][n] = e^{a_i} (MW^T A~)[n][i] (each warp store writes 128 contiguous bytes)
+            const int n = s;
+            float* Ccol = args.Cm + unit * (size_t)(HD * HD) + n;
+            float x[32];
+            tmem_ld32(tmem + lane_base + TMW + 32 * qd, x);
+#pragma unroll
+            for (int i2 = 0; i2 < 32; ++i2) Ccol[(size_t)(32 * qd + i2) * HD] = ea[32 * qd + i2] * x[i2];
+        }
+        {   // Q'[t][c] = e^{a_c} (Q~[t][c] - Zq[c][t]), c = s, t = 16 qd ..; Q~ from its hi and lo tiles. Q'_j is
+            // a bf16 [128][128] block whose rows 32 g .. 32 g + 15 hold the hi parts of tokens 16 g .. 16 g + 15
             // and rows 32 g + 16 .. 32 g + 31 their lo parts: one product of the block with S_{j-1} then puts a
             // token's two partial outputs in lanes l and l + 16 of the same warp.
             const int c = s;
-            __nv_bfloat16* Qcol = args.Qm + unit * (size_t)(2 * HCK * HD) + c;
-#pragma unroll 1
-            for (int p = 0; p < 2; ++p) {
-                float x[32];
-                tmem_ld32(tmem + lane_base + TM + 32 * p, x);
+            const float ec = ea[c];
+            float x[16];
+            tmem_ld16(tmem + lane_base + TM + 16 * qd, x);
 #pragma unroll
-                for (int i2 = 0; i2 < 32; ++i2) {
-                    const int t = 32 * p + i2;
-                    const uint32_t oq = sw_bf16(t, c, HCK);
-                    const float qt = lds_bf16(sb + S::Q_HI + oq) + lds_bf16(sb + S::Q_LO + oq);
-                    uint16_t h, l;
-                    split1(ei * (qt - x[i2]), h, l);
-                    const int rh = 32 * (t >> 4) + (t & 15);
-                    reinterpret_cast<uint16_t*>(Qcol)[(size_t)rh * HD] = h;
-                    reinterpret_cast<uint16_t*>(Qcol)[(size_t)(rh + 16) * HD] = l;
-                }
-            }
-        } else {
-            const int n = s;
-            float* Ccol = args.Cm + unit * (size_t)(HD * HD) + n;
-#pragma unroll 1
-            for (int p = 0; p < 4; ++p) {
-                float x[32];
-                tmem_ld32(tmem + lane_base + TMW + 32 * p, x);
-#pragma unroll
-                for (int i2 = 0; i2 < 32; ++i2) Ccol[(size_t)(32 * p + i2) * HD] = ea[32 * p + i2] * x[i2];
-            }
-            float* ocol = args.o + tok0 * HD + n;
-#pragma unroll 1
-            for (int p = 0; p < 2; ++p) {
-                float x[32];
-                tmem_ld32(tmem + lane_base + TQA + 32 * p, x);
-#pragma unroll
-                for (int i2 = 0; i2 < 32; ++i2) {
-                    const int t = 32 * p + i2;
-                    if (t < valid) ocol[(size_t)t * HD] = x[i2];
-                }
+            for (int i2 = 0; i2 < 16; ++i2) {
+                const int t = 16 * qd + i2;
+                const uint32_t oq = sw_bf16(t, c, HCK);
+                const float qt = lds_bf16(sb + S::Q_HI + oq) + lds_bf16(sb + S::Q_LO + oq);
+                uint16_t h, l;
+                split1(ec * (qt - x[i2]), h, l);
+                *reinterpret_cast<uint16_t*>(smem + S::A_LO + sw_bf16(32 * qd + i2, c, 128)) = h;   // g = t / 16 = qd
+                *reinterpret_cast<uint16_t*>(smem + S::A_LO + sw_bf16(32 * qd + 16 + i2, c, 128)) = l;
             }
         }
+        {   // O_j column n = s, tokens t = 16 qd ..
+            const int n = s;
+            float x[16];
+            tmem_ld16(tmem + lane_base + TQA + 16 * qd, x);
+            float* ocol = args.o + tok0 * HD + n;
+#pragma unroll
+            for (int i2 = 0; i2 < 16; ++i2)
+                if (16 * qd + i2 < valid) ocol[(size_t)(16 * qd + i2) * HD] = x[i2];
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {   // (the next unit waits for these reads before its factor build rewrites A~)
+            const int yu = static_cast<int>(unit * HD);
+            for (int h = 0; h < 2; ++h) {
+                tma_store_2d(&tm_P, 64 * h, yu, sb + S::A_HI + h * 16384);
+                tma_store_2d(&tm_Q, 64 * h, yu, sb + S::A_LO + h * 16384);
+            }
+            bulk_commit();
+        }
     }
+  }   // units
 
     if (failed) {
         if (tid == 0) {
             atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
             // no copy may land after the CTA exits, and no product may touch freed tensor memory
-            if (full) mbar_wait(mb_tma, 0, 400000000LL);
+            if (tma_pending) mbar_wait(mb_tma, tma_phase & 1, 400000000LL);
             mma_commit(mb_drain);   // tracks every product issued by this thread
             mbar_wait(mb_drain, 0, 400000000LL);
         }
+    }
+    if (tid == 0) {   // bulk stores still in flight read shared memory: wait before the CTA exits
+        bulk_commit();
+        bulk_wait_read();
     }
     fence_before_sync();
     __syncthreads();
@@ -748,11 +808,6 @@ static_assert(K2Smem::TOTAL <= 227 * 1024, "shared memory budget");
 struct K2Args {
     const float* S0; float* o; float* ST; int* status;
 };
-
-__device__ __forceinline__ void prefetch_l2_tile(const CUtensorMap* map, int x, int y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
-                 :: "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y) : "memory");
-}
 
 __global__ void __launch_bounds__(K2T, 1)
 hdla_chain_kernel(Plan pl, K2Args args, const __grid_constant__ CUtensorMap tm_P, const __grid_constant__ CUtensorMap tm_Q,
@@ -977,6 +1032,19 @@ hdla_chain_kernel(Plan pl, K2Args args, const __grid_constant__ CUtensorMap tm_P
 
 std::atomic<uint64_t> g_k1_smem_set{0}, g_k2_smem_set{0};
 
+// Number of SMs of the current device (looked up once per device).
+int sm_count() {
+    static std::atomic<int> cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cached[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
 }  // namespace
 
 bool hdla_tc_supported(const Plan& pl) {
@@ -1011,19 +1079,22 @@ cudaError_t launch_hdla_chunks(const Plan& pl, const void* q, const void* k, con
     a.Cm = reinterpret_cast<float*>(ws + oC);
     a.Qm = reinterpret_cast<__nv_bfloat16*>(ws + oQ);
     a.status = reinterpret_cast<int*>(ws);
-    CUtensorMap mq, mk, mv, ml;
+    CUtensorMap mq, mk, mv, ml, mP, mQ;
     std::memset(&mq, 0, sizeof(mq)); std::memset(&mk, 0, sizeof(mk));
     std::memset(&mv, 0, sizeof(mv)); std::memset(&ml, 0, sizeof(ml));
-    if (pl.T >= HCK) {   // only full chunks are loaded by TMA
+    const uint64_t units = (uint64_t)pl.BH * (uint64_t)((pl.T + HCK - 1) / HCK);
+    if (pl.T >= HCK) {   // only full chunks are loaded and their outputs stored by TMA
         const uint64_t rows = (uint64_t)pl.BH * (uint64_t)pl.T;
         if (!tensor_map_2d(&mq, q, true, rows, HD, HCK, 64) || !tensor_map_2d(&mk, k, true, rows, HD, HCK, 64) ||
             !tensor_map_2d(&mv, v, true, rows, HD, HCK, 64) || !tensor_map_2d(&ml, decay, false, rows, HD, HCK, 32))
             return cudaErrorInvalidValue;
     }
+    if (!tensor_map_2d(&mP, ws + oP, true, units * HD, HD, HD, 64) || !tensor_map_2d(&mQ, ws + oQ, true, units * HD, HD, HD, 64))
+        return cudaErrorInvalidValue;
     cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(hdla_chunk_kernel), K1Smem::TOTAL, g_k1_smem_set);
     if (e != cudaSuccess) return e;
-    const long long grid = (long long)pl.BH * ((pl.T + HCK - 1) / HCK);
-    hdla_chunk_kernel<<<(unsigned)grid, K1T, K1Smem::TOTAL, s>>>(pl, a, mq, mk, mv, ml);
+    const long long grid = std::min<long long>((long long)units, (long long)sm_count());
+    hdla_chunk_kernel<<<(unsigned)grid, K1T, K1Smem::TOTAL, s>>>(pl, a, mq, mk, mv, ml, mP, mQ);
     return cudaGetLastError();
 }
 
