@@ -98,3 +98,28 @@ def test_fused_kernel_timeout_returns_and_reports(sdl):
     o_ref, S_ref = oracle.forward_inputs(inp)
     assert _rel(o.double().cpu().numpy(), o_ref) <= TAU
     assert _rel(ST.double().cpu().numpy(), S_ref) <= TAU
+
+
+def test_hdla_tensor_core_kernels_timeout_returns_and_reports(sdl):
+    """The same for the tensor-core HDLA stages (chunk maps, then the chain): with every wait limited
+    to 1000 cycles the launches end and report DPLR_ERR_TIMEOUT; with the default limit the same
+    context gives a correct forward."""
+    import torch
+    w = workloads.Workload(94, "hdla_status", "hdla", "bf16", 1, 1, 0, 128, 128, 2, 1, 64, True)
+    inp = workloads.generate(w, heads=[(0, 0), (0, 1)], T=256)
+    args = _dev_args(inp)
+    f = sdl.Forward("hdla", torch.bfloat16, 1, 2, 256, 128, 128)
+    assert f.path == "hdla_tcgen05"
+    sdl.dplr_la_set_wait_limit(1000)
+    try:
+        f(**args)
+        torch.cuda.synchronize()
+        assert f.device_status(clear=True) == sdl.dplr.DPLR_ERR_TIMEOUT
+    finally:
+        sdl.dplr_la_set_wait_limit(0)
+    o, ST = f(**args)
+    torch.cuda.synchronize()
+    assert f.device_status() == sdl.DPLR_OK
+    o_ref, S_ref = oracle.forward_inputs(inp)
+    assert _rel(o.double().cpu().numpy(), o_ref) <= TAU
+    assert _rel(ST.double().cpu().numpy(), S_ref) <= TAU
