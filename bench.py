@@ -486,6 +486,67 @@ def run_host_overhead(args):
     print(json.dumps({"mode": "host_overhead", "burst": 100, "bursts": 20, "results": lines}), flush=True)
 
 
+def run_decode(args):
+    """Time of one decode step (dplr_la_decode_step, one token for every head) for the head counts of
+    workloads 2 (GDN, B=8 H=16) and 4 (HDLA, B=1 H=16) at d = 128, bf16 inputs. The step reads and writes
+    each head's fp32 state once: 2 * dk * dv * 4 bytes per head, plus the token's inputs. Timed with CUDA
+    events over 200 steps launched back to back, and over 200 steps captured in one CUDA graph (no launch
+    gaps). The state (8 MB and 1 MB) stays in L2 from step to step, so the figure is an L2-resident one."""
+    import torch
+    import structured_decay_linear_gb300 as sdl
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks, peak_kind = load_peaks()
+    lines = []
+    for wid in (2, 4):
+        w = workloads.WORKLOADS[wid]
+        inp = workloads.generate(w, T=1)
+        t = {k: (None if inp[k] is None else torch.from_numpy(np.ascontiguousarray(inp[k])).to(dev))
+             for k in ("q", "k", "v", "decay", "beta", "S0")}
+        for k in ("q", "k", "v"):
+            t[k] = t[k].to(torch.bfloat16)
+        step = sdl.Decode(w.mode, torch.bfloat16, w.B, w.H, w.dk, w.dv, S0=t["S0"], device=dev)
+        call = lambda: step(q=t["q"], k=t["k"], v=t["v"], decay=t["decay"], beta=t["beta"])
+        for _ in range(20):
+            call()
+        torch.cuda.synchronize(dev)
+        n = 200
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            call()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        us_launch = e0.elapsed_time(e1) / n * 1e3
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(dev)
+        s.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(s):
+            call()
+            with torch.cuda.graph(g, stream=s):
+                for _ in range(n):
+                    call()
+        torch.cuda.synchronize(dev)
+        g.replay()
+        torch.cuda.synchronize(dev)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        us_graph = e0.elapsed_time(e1) / n * 1e3
+        heads = w.B * w.H
+        state_bytes = heads * 2 * w.dk * w.dv * 4
+        in_bytes = heads * (2 * (2 * w.dk + w.dv) + 4 + 4 * (1 if w.mode == "gdn" else w.dk)) + heads * w.dv * 4
+        gbs = (state_bytes + in_bytes) / (us_graph * 1e-6) / 1e9
+        lines.append({"workload": f"{w.mode}_bf16_b{w.B}h{w.H}_d128_decode", "heads": heads,
+                      "us_per_step_launched": us_launch, "us_per_step_graph": us_graph,
+                      "tokens_per_s_graph": heads / (us_graph * 1e-6), "bytes_per_step": state_bytes + in_bytes,
+                      "achieved_gbs_graph": gbs, "frac_of_hbm_peak": gbs / peaks["hbm_gbs"],
+                      "peak": f"{peak_kind} hbm_gbs {peaks['hbm_gbs']}"})
+    print(json.dumps({"mode": "decode", "steps": 200, "results": lines}), flush=True)
+
+
 def dataclasses_replace(w, **kw):
     import dataclasses
     return dataclasses.replace(w, **kw)
@@ -499,6 +560,8 @@ def main():
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode", action="store_true",
+                    help="time the one-token decode step (not a benchmark line)")
     ap.add_argument("--host-overhead", action="store_true",
                     help="time the host side of dplr_la_forward on T = 64 problems (not a benchmark line)")
     ap.add_argument("--seq-len", type=int, default=0,
@@ -506,6 +569,9 @@ def main():
     args = ap.parse_args()
     if args.host_overhead:
         run_host_overhead(args)
+        return
+    if args.decode:
+        run_decode(args)
         return
     w = workloads.WORKLOADS[args.workload]
     if args.seq_len > 0:

@@ -162,6 +162,20 @@ DPLR_API dplr_status dplr_la_read_status(const void* workspace, size_t ws_bytes,
  * path; a small limit makes correct launches give up too. */
 DPLR_API void dplr_la_set_wait_limit(long long cycles);
 
+/* One recurrent step for every (batch, head): the decode-time form of the recurrence, whose
+ * state has constant size (HDLA page, research background; HLA page, results: per-token decode
+ * cost). S <- (D_t - A_t B_t^T) S + K_t V_t^T in place, then o = S^T q_t, exactly as one token
+ * of dplr_la_forward (GDN and HDLA build the factors from k, v, decay, beta as there).
+ * desc->T must be 1: the inputs are the layouts above with T = 1 (q [B,H,1,dk], ...).
+ * S: [B,H,dk,dv] fp32, read and written in place (device, 16-byte aligned). o: [B,H,1,dv]
+ * fp32. All arithmetic is fp32. Needs no workspace and allocates nothing; asynchronous on
+ * `stream`. Errors: as dplr_la_forward; DPLR_ERR_INVALID_ARG when desc->T != 1. */
+DPLR_API dplr_status dplr_la_decode_step(const dplr_desc* desc,
+                                const void* q, const void* k, const void* v,
+                                const float* decay, const float* beta,
+                                const void* A, const void* Bm, const void* K, const void* V,
+                                float* S, float* o, void* stream);
+
 /* Name of the kernel path that dplr_la_forward runs for `desc` (no counterpart in the
  * paper; static storage): "gdn_fused_tcgen05" (GDN, bf16, dk = dv = 128: one fused
  * per-head kernel on the tensor cores), "hdla_tcgen05" (HDLA, bf16, dk = dv = 128: the

@@ -67,6 +67,8 @@ def library() -> ctypes.CDLL:
             lib.dplr_la_state_scan.argtypes = [dp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
             lib.dplr_la_forward_noalloc.restype = ctypes.c_int
             lib.dplr_la_forward_noalloc.argtypes = [dp] + [_vp] * 12 + [_vp]
+            lib.dplr_la_decode_step.restype = ctypes.c_int
+            lib.dplr_la_decode_step.argtypes = [dp] + [_vp] * 11 + [_vp]
             lib.dplr_la_path.restype = ctypes.c_char_p
             lib.dplr_la_path.argtypes = [dp]
             lib.dplr_la_set_wait_limit.restype = None
@@ -122,6 +124,11 @@ def dplr_la_check(desc: dplr_desc) -> int:
 
 def dplr_la_kernel_count(desc: dplr_desc) -> int:
     return int(library().dplr_la_kernel_count(ctypes.byref(desc)))
+
+
+def dplr_la_decode_step(desc, q, k, v, decay, beta, A, Bm, K, V, S, o, stream) -> int:
+    """One recurrent step (desc.T == 1): S updated in place, o = S^T q."""
+    return int(library().dplr_la_decode_step(ctypes.byref(desc), q, k, v, decay, beta, A, Bm, K, V, S, o, stream))
 
 
 def dplr_la_path(desc: dplr_desc) -> str:
@@ -350,3 +357,30 @@ def forward(mode: str, q, k=None, v=None, decay=None, beta=None, A=None, Bm=None
         r_ab, r_kv, dv = None, None, v.shape[3]
     f = Forward(mode, q.dtype, B, H, T, dk, dv, r_ab, r_kv, chunk, device=q.device)
     return f(q, k, v, decay, beta, A, Bm, K, V, S0)
+
+
+class Decode:
+    """Prepared one-token step for B x H heads (dplr_la_decode_step): owns the state S and the output o."""
+
+    def __init__(self, mode: str, in_dtype: torch.dtype, B: int, H: int, dk: int, dv: int,
+                 r_ab: Optional[int] = None, r_kv: Optional[int] = None, S0: Optional[torch.Tensor] = None,
+                 device: Optional[torch.device] = None):
+        self.desc = make_desc(mode, in_dtype, B, H, 1, dk, dv, r_ab, r_kv)
+        st = dplr_la_check(self.desc)
+        if st != DPLR_OK:
+            raise DplrError(st, "dplr_la_check")
+        self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        self.S = torch.zeros((B, H, dk, dv), dtype=torch.float32, device=self.device)
+        if S0 is not None:
+            self.S.copy_(S0)
+        self.o = torch.empty((B, H, 1, dv), dtype=torch.float32, device=self.device)
+
+    def __call__(self, q, k=None, v=None, decay=None, beta=None, A=None, Bm=None, K=None, V=None,
+                 stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+        """One token (tensors with T = 1, contiguous, on the device). Returns o [B,H,1,dv]."""
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        st = dplr_la_decode_step(self.desc, _ptr(q), _ptr(k), _ptr(v), _ptr(decay), _ptr(beta), _ptr(A), _ptr(Bm),
+                                 _ptr(K), _ptr(V), _ptr(self.S), _ptr(self.o), s.cuda_stream)
+        if st != DPLR_OK:
+            raise DplrError(st, "dplr_la_decode_step")
+        return self.o
