@@ -58,6 +58,19 @@ bool encode_map_2d(CUtensorMap* map, const void* base, bool bf16, uint64_t rows,
 
 }  // namespace
 
+// Number of SMs of the current device (looked up once per device).
+int sm_count() {
+    static std::atomic<int> cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cached[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
 bool tensor_map_2d(CUtensorMap* map, const void* base, bool bf16, uint64_t rows, uint64_t cols, uint32_t box_rows,
                    uint32_t box_cols) {
     struct Entry { const void* base; uint64_t rows, cols; uint32_t br, bc; bool bf16; CUtensorMap map; };
@@ -105,6 +118,11 @@ dplr_status make_plan(const dplr_desc* d, Plan* pl) {
     p.nb = (d->T + p.cw - 1) / p.cw;
     p.fused = fused_supported(p) ? 1 : 0;
     p.tc = (!p.fused && hdla_tc_supported(p)) ? 1 : 0;
+    p.gtc = (!p.fused && !p.tc && generic_tc_supported(p)) ? 1 : 0;
+    if (p.gtc) {
+        p.cw = generic_tc_block();
+        p.nb = (d->T + p.cw - 1) / p.cw;
+    }
     p.wait_cycles = g_wait_cycles.load(std::memory_order_relaxed);
     if (p.tc) {
         // one unit per (head, 64-token chunk): P_j has 128 rows, addressed as int by the copies
@@ -124,7 +142,7 @@ dplr_status make_plan(const dplr_desc* d, Plan* pl) {
         p.off_Q = off; off = round_up(off + units * (size_t)p.cw * p.dk * sizeof(float));
         p.ws_stages = off;
         p.ws_bytes = p.fused ? kAlign : p.ws_stages;   // fused: the status word alone
-        if (prep_smem_bytes(p) > 227 * 1024 || scan_smem_bytes(p) > 227 * 1024) return DPLR_ERR_UNSUPPORTED;
+        if ((!p.gtc && prep_smem_bytes(p) > 227 * 1024) || scan_smem_bytes(p) > 227 * 1024) return DPLR_ERR_UNSUPPORTED;
     }
     *pl = p;
     return DPLR_OK;
@@ -223,7 +241,9 @@ dplr_status dplr_la_chunk_maps(const dplr_desc* desc, const void* q, const void*
         return DPLR_OK;
     }
     const ChunkMapArgs a = map_args(pl, q, k, v, decay, beta, A, Bm, K, V, o, workspace);
-    if (launch_chunk_maps(pl, a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return DPLR_ERR_CUDA;
+    const cudaError_t e = pl.gtc ? launch_generic_chunks(pl, a, workspace, static_cast<cudaStream_t>(stream))
+                                 : launch_chunk_maps(pl, a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return DPLR_ERR_CUDA;
     return DPLR_OK;
 }
 
@@ -266,7 +286,8 @@ dplr_status dplr_la_forward(const dplr_desc* desc, const void* q, const void* k,
         if (launch_hdla_chain(pl, S0, o, S_T, workspace, s) != cudaSuccess) return DPLR_ERR_CUDA;
         return DPLR_OK;
     }
-    if (launch_chunk_maps(pl, map_args(pl, q, k, v, decay, beta, A, Bm, K, V, o, workspace), s) != cudaSuccess)
+    const ChunkMapArgs a = map_args(pl, q, k, v, decay, beta, A, Bm, K, V, o, workspace);
+    if ((pl.gtc ? launch_generic_chunks(pl, a, workspace, s) : launch_chunk_maps(pl, a, s)) != cudaSuccess)
         return DPLR_ERR_CUDA;
     if (launch_state_scan(pl, scan_args(pl, S0, o, S_T, workspace), s) != cudaSuccess) return DPLR_ERR_CUDA;
     return DPLR_OK;
@@ -277,6 +298,7 @@ const char* dplr_la_path(const dplr_desc* desc) {
     if (make_plan(desc, &pl) != DPLR_OK) return "";
     if (pl.fused) return "gdn_fused_tcgen05";
     if (pl.tc) return "hdla_tcgen05";
+    if (pl.gtc) return "generic_tcgen05";
     return "two_stage_fp32";
 }
 

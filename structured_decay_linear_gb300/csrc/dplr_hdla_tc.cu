@@ -47,176 +47,17 @@
 
 #include "dplr_internal.h"
 #include "sm100_ops.cuh"
+#include "tc_common.cuh"
 
 namespace dplr {
 namespace {
 
 using namespace sm100;
+using namespace tc;
 
 constexpr int HD = 128;    // dk = dv
 constexpr int HCK = 64;    // tokens per chunk
 constexpr int K1T = 512;   // threads of the chunk kernel: four per tensor-memory lane
-constexpr int kLdX = 68;   // row stride (floats) of the inverse's fp32 blocks (16-byte rows, 4 banks apart)
-
-// ---- 128-byte-swizzled tiles (the layout the TMA writes with SWIZZLE_128B): rows of 128 bytes whose
-// 16-byte chunks are permuted by XOR with the row index mod 8. A bf16 [R][128] tile is two half-tiles
-// (columns 0-63, 64-127) of R rows; an fp32 [R][128] tile is four column boxes of 32.
-__device__ __forceinline__ uint32_t swz(int r, int chunk) { return (uint32_t)(r * 128 + (((chunk) ^ (r & 7)) << 4)); }
-__device__ __forceinline__ uint32_t sw_bf16(int r, int c, int R) {
-    return (uint32_t)((c >> 6) * (R * 128)) + swz(r, (c & 63) >> 3) + (uint32_t)((c & 7) << 1);
-}
-__device__ __forceinline__ uint32_t sw_f32(int r, int c, int R) {
-    return (uint32_t)((c >> 5) * (R * 128)) + swz(r, (c & 31) >> 2) + (uint32_t)((c & 3) << 2);
-}
-
-__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-__device__ __forceinline__ float lds_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
-    return v;
-}
-__device__ __forceinline__ float lds_bf16(uint32_t addr) {
-    uint16_t v;
-    asm volatile("ld.shared.b16 %0, [%1];" : "=h"(v) : "r"(addr));
-    return __uint_as_float(static_cast<uint32_t>(v) << 16);
-}
-__device__ __forceinline__ uint16_t bf16_bits(float x) {
-    __nv_bfloat16 h = __float2bfloat16_rn(x);
-    return *reinterpret_cast<uint16_t*>(&h);
-}
-__device__ __forceinline__ float bf16_value(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
-__device__ __forceinline__ float tf32_rn(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
-}
-
-// x = hi + lo with both parts bf16 (scalar): the pair of bit patterns.
-__device__ __forceinline__ void split1(float x, uint16_t& h, uint16_t& l) {
-    h = bf16_bits(x);
-    l = bf16_bits(x - bf16_value(h));
-}
-// x = hi + lo for a pair of values, packed (element 0 in the low half).
-__device__ __forceinline__ void split2(float x0, float x1, uint32_t& h, uint32_t& l) {
-    h = pack_bf16(x0, x1);
-    l = pack_bf16(x0 - __uint_as_float(h << 16), x1 - __uint_as_float(h & 0xFFFF0000u));
-}
-
-// MMAs issued by lane 0 of a converged warp through a predicate (no divergence, so no costly
-// re-convergence after the issue).
-__device__ __forceinline__ void mma_ss_if(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc, uint32_t issue) {
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
-        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(issue));
-}
-__device__ __forceinline__ void mma_ts_if(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc,
-                                          uint32_t issue) {
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
-        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-        :: "r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc), "r"(issue));
-}
-__device__ __forceinline__ void commit_if(uint64_t* mbar, uint32_t issue) {
-    asm volatile(
-        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
-        "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
-        :: "r"(smem_addr(mbar)), "r"(issue) : "memory");
-}
-__device__ __forceinline__ uint64_t dadd(uint64_t desc, uint32_t bytes) { return desc + static_cast<uint64_t>(bytes >> 4); }
-
-// 16 consecutive fp32 columns of this thread's tensor-memory lane.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// Warp-level C[16x8] = A[16xK] B[Kx8] (mma.sync m16n8k8 tf32, fp32 accumulate) with the operands
-// rounded to tf32 (cvt.rna); A, B row-major fp32 in shared memory. Fragments as in the PTX ISA.
-__device__ __forceinline__ void warp_mma_tf32_rn(const float* A, int lda, const float* B, int ldb, int K, float (&c)[4]) {
-    const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
-    c[0] = c[1] = c[2] = c[3] = 0.f;
-    for (int k0 = 0; k0 < K; k0 += 8) {
-        const uint32_t a0 = __float_as_uint(tf32_rn(A[g * lda + k0 + q]));
-        const uint32_t a1 = __float_as_uint(tf32_rn(A[(g + 8) * lda + k0 + q]));
-        const uint32_t a2 = __float_as_uint(tf32_rn(A[g * lda + k0 + q + 4]));
-        const uint32_t a3 = __float_as_uint(tf32_rn(A[(g + 8) * lda + k0 + q + 4]));
-        const uint32_t b0 = __float_as_uint(tf32_rn(B[(k0 + q) * ldb + g]));
-        const uint32_t b1 = __float_as_uint(tf32_rn(B[(k0 + q + 4) * ldb + g]));
-        asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-                     "{%0,%1,%2,%3};"
-                     : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-                     : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-    }
-}
-
-// In place, for the 256 threads t of one group (named barrier `bar`): X (64 x 64, row stride kLdX)
-// holds a strictly lower-triangular L on entry (zeros on and above the diagonal) and
-// M = (I + L)^{-1} on exit. Diagonal 16 x 16 blocks by substitution (one column per thread), then
-// the block merges [[A,0],[C,B]]^{-1} = [[A^{-1},0],[-B^{-1} C A^{-1}, B^{-1}]] for 16 -> 32 -> 64,
-// each product formed in registers and written over C once every warp has read C.
-__device__ __forceinline__ void inv64_inplace(float* X, int t, uint32_t bar) {
-    const int w = t >> 5;
-    if (t < 64) {
-        const int b = t >> 4, jj = t & 15, o = 16 * b;
-        float m[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float* Lr = X + (o + i) * kLdX + o;
-            float acc0 = (i == jj) ? 1.f : 0.f, acc1 = 0.f;
-#pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4) {
-                if (4 * k4 < i) {
-                    const float4 l = *reinterpret_cast<const float4*>(Lr + 4 * k4);
-                    if (4 * k4 + 0 < i) acc0 = fmaf(-l.x, m[4 * k4 + 0], acc0);
-                    if (4 * k4 + 1 < i) acc1 = fmaf(-l.y, m[4 * k4 + 1], acc1);
-                    if (4 * k4 + 2 < i) acc0 = fmaf(-l.z, m[4 * k4 + 2], acc0);
-                    if (4 * k4 + 3 < i) acc1 = fmaf(-l.w, m[4 * k4 + 3], acc1);
-                }
-            }
-            m[i] = acc0 + acc1;
-        }
-        named_sync(bar, 256);   // every row of the diagonal blocks read
-#pragma unroll
-        for (int i = 0; i < 16; ++i) X[(o + i) * kLdX + o + jj] = m[i];
-    } else {
-        named_sync(bar, 256);
-    }
-    named_sync(bar, 256);
-    {   // 16 -> 32 for the pairs of diagonal blocks (0,1) and (2,3): one 16 x 8 tile for each of warps 0-3
-        const int p = (w >> 1) & 1, ct = w & 1, o = 32 * p;
-        float c[4];
-        if (w < 4) warp_mma_tf32_rn(X + (o + 16) * kLdX + o, kLdX, X + o * kLdX + o + 8 * ct, kLdX, 16, c);   // C A^{-1}
-        named_sync(bar, 256);
-        if (w < 4) store_tile_16x8(X + (o + 16) * kLdX + o + 8 * ct, kLdX, c, 1.f);
-        named_sync(bar, 256);
-        if (w < 4) warp_mma_tf32_rn(X + (o + 16) * kLdX + o + 16, kLdX, X + (o + 16) * kLdX + o + 8 * ct, kLdX, 16, c);
-        named_sync(bar, 256);
-        if (w < 4) store_tile_16x8(X + (o + 16) * kLdX + o + 8 * ct, kLdX, c, -1.f);
-        named_sync(bar, 256);
-    }
-    {   // 32 -> 64: rows 32-63, columns 0-31; one 16 x 8 tile per warp (row block 16 (w / 4), column block 8 (w % 4))
-        const int rb = w >> 2, cb = w & 3;
-        float c[4];
-        warp_mma_tf32_rn(X + (32 + 16 * rb) * kLdX, kLdX, X + 8 * cb, kLdX, 32, c);
-        named_sync(bar, 256);
-        store_tile_16x8(X + (32 + 16 * rb) * kLdX + 8 * cb, kLdX, c, 1.f);
-        named_sync(bar, 256);
-        warp_mma_tf32_rn(X + (32 + 16 * rb) * kLdX + 32, kLdX, X + 32 * kLdX + 8 * cb, kLdX, 32, c);
-        named_sync(bar, 256);
-        store_tile_16x8(X + (32 + 16 * rb) * kLdX + 8 * cb, kLdX, c, -1.f);
-        named_sync(bar, 256);
-    }
-}
 
 // ================================================================================================
 // Stage 1: chunk maps
@@ -258,18 +99,6 @@ struct K1Args {
     const float* decay; const float* beta;
     float* o; __nv_bfloat16* P; float* Cm; __nv_bfloat16* Qm; int* status;
 };
-
-// Bulk stores (shared -> global) by tensor map, and their completion.
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];"
-                 :: "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(src) : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void prefetch_l2_tile(const CUtensorMap* map, int x, int y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
-                 :: "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y) : "memory");
-}
 
 // Persistent: CTA b takes the units b, b + gridDim.x, ... in head-major order (chunk j of head bh is unit
 // bh * NC + j), so the CTAs running at once read neighbouring chunks. The next unit's inputs are prefetched
@@ -1032,18 +861,6 @@ hdla_chain_kernel(Plan pl, K2Args args, const __grid_constant__ CUtensorMap tm_P
 
 std::atomic<uint64_t> g_k1_smem_set{0}, g_k2_smem_set{0};
 
-// Number of SMs of the current device (looked up once per device).
-int sm_count() {
-    static std::atomic<int> cached[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-    int n = cached[dev].load(std::memory_order_relaxed);
-    if (n == 0) {
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-        cached[dev].store(n, std::memory_order_relaxed);
-    }
-    return n;
-}
 
 }  // namespace
 

@@ -27,6 +27,7 @@ struct Plan {
     int nb;                    // WY blocks per head = ceil(T / cw)
     int fused;                 // dplr_la_forward runs the fused per-head kernel (GDN)
     int tc;                    // the stages run the tensor-core HDLA kernels
+    int gtc;                   // stage 1 runs the tensor-core generic-mode kernel (32-token WY blocks)
     long long wait_cycles;     // limit (SM cycles) of a kernel's bounded waits on other roles
     size_t off_P, off_c, off_Q;
     size_t ws_stages;          // workspace of the two-stage entry points
@@ -67,6 +68,7 @@ inline cudaError_t set_smem_limit_once(const void* func, int bytes, std::atomic<
     if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
     return e;
 }
+int sm_count();   // SMs of the current device
 size_t prep_smem_bytes(const Plan& pl);
 size_t scan_smem_bytes(const Plan& pl);
 cudaError_t launch_chunk_maps(const Plan& pl, const ChunkMapArgs& a, cudaStream_t s);
@@ -84,6 +86,12 @@ void hdla_tc_offsets(const Plan& pl, size_t* off_P, size_t* off_c, size_t* off_Q
 cudaError_t launch_hdla_chunks(const Plan& pl, const void* q, const void* k, const void* v, const float* decay,
                                const float* beta, float* o, void* workspace, cudaStream_t s);
 cudaError_t launch_hdla_chain(const Plan& pl, const float* S0, float* o, float* ST, void* workspace, cudaStream_t s);
+
+// Tensor-core stage 1 of the generic mode (dk = dv = 64, r_ab <= 4, r_kv <= 2): writes the maps of
+// 32-token WY blocks in the layout of ChunkMapArgs; stage 2 is the fp32 scan.
+bool generic_tc_supported(const Plan& pl);
+int generic_tc_block();
+cudaError_t launch_generic_chunks(const Plan& pl, const ChunkMapArgs& a, void* workspace, cudaStream_t s);
 
 // Fused per-head kernel (structured modes, bf16 inputs, dk = dv = 128).
 bool fused_supported(const Plan& pl);

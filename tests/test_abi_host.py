@@ -57,7 +57,9 @@ def test_path_names(sdl):
     assert sdl.dplr_la_path(sdl.make_desc("gdn", "bf16", 8, 16, 8192, 128, 128)) == "gdn_fused_tcgen05"
     assert sdl.dplr_la_path(sdl.make_desc("hdla", "bf16", 1, 16, 131072, 128, 128)) == "hdla_tcgen05"
     assert sdl.dplr_la_path(sdl.make_desc("hdla", "bf16", 1, 1, 64, 64, 64)) == "two_stage_fp32"
-    assert sdl.dplr_la_path(sdl.make_desc("generic", "f32", 2, 8, 8192, 64, 64, 4, 2)) == "two_stage_fp32"
+    assert sdl.dplr_la_path(sdl.make_desc("generic", "f32", 2, 8, 8192, 64, 64, 4, 2)) == "generic_tcgen05"
+    assert sdl.dplr_la_path(sdl.make_desc("generic", "f32", 1, 1, 64, 64, 64, 8, 2)) == "two_stage_fp32"
+    assert sdl.dplr_la_path(sdl.make_desc("generic", "f32", 1, 1, 64, 32, 32, 4, 2)) == "two_stage_fp32"
     assert sdl.dplr_la_path(sdl.make_desc("gdn", "f32", 1, 1, 8, 48, 32)) == ""
 
 

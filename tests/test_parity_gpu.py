@@ -147,6 +147,41 @@ def test_generic_small(sdl, dtype, dk, dv, r, p, H, T):
     check(inp, o, ST)
 
 
+GENERIC_TC = [
+    # dtype, r, p, H, T  (dk = dv = 64: the tensor-core chunk kernel, 32-token WY blocks)
+    ("f32", 4, 2, 2, 100),    # several blocks and a ragged last one
+    ("f32", 1, 0, 1, 50),     # no write term
+    ("f32", 3, 1, 2, 77),     # 96 factor rows: zero-padded tiles
+    ("f32", 2, 2, 1, 32),     # exactly one block
+    ("f32", 4, 2, 1, 1),      # one token
+    ("f32", 4, 1, 3, 33),     # one token past a block
+    ("f32", 1, 2, 1, 129),
+    ("bf16", 4, 2, 2, 200),
+]
+
+
+@pytest.mark.parametrize("dtype,r,p,H,T", GENERIC_TC)
+def test_generic_tensor_core_path(sdl, dtype, r, p, H, T):
+    w = W("generic", dtype, 64, 64, r, p)
+    assert sdl.dplr_la_path(sdl.make_desc("generic", dtype, 1, H, T, 64, 64, r, p)) == "generic_tcgen05"
+    inp = gen_generic(w, H, T, seed=2000 + 10 * r + p)
+    inp["S0"] = (0.2 * np.random.default_rng(6).standard_normal((1, H, 64, 64))).astype(np.float32)
+    o, ST = run_gpu(sdl, inp)
+    check(inp, o, ST)
+
+
+def test_generic_tensor_core_slow_decay(sdl):
+    """Decay close to one (log-decay -0.005 per channel and token): the block's factors span e^{+-0.08} only, and
+    the chunk maps are far from contracting, so rounding in P_j carries over many blocks."""
+    w = W("generic", "f32", 64, 64, 4, 2)
+    inp = gen_generic(w, 1, 600, seed=2100)
+    inp["decay"] = np.full_like(inp["decay"], -0.005)
+    lam = np.exp(inp["decay"].astype(np.float64))[..., None, :]
+    inp["A"] = (lam * inp["Bm"].astype(np.float64) * 0.5).astype(np.float32)   # D - A B^T = Diag(lambda)(I - U U^T / 2)
+    o, ST = run_gpu(sdl, inp)
+    check(inp, o, ST)
+
+
 def test_config0_full(sdl):
     inp = workloads.generate(0)
     o, ST = run_gpu(sdl, inp)

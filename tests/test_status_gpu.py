@@ -123,3 +123,29 @@ def test_hdla_tensor_core_kernels_timeout_returns_and_reports(sdl):
     o_ref, S_ref = oracle.forward_inputs(inp)
     assert _rel(o.double().cpu().numpy(), o_ref) <= TAU
     assert _rel(ST.double().cpu().numpy(), S_ref) <= TAU
+
+
+def test_generic_tensor_core_kernel_timeout_returns_and_reports(sdl):
+    """The same for the generic mode's tensor-core chunk kernel (its waits on the tensor cores): limited to 1000
+    cycles, the launch ends and reports DPLR_ERR_TIMEOUT; with the default limit the same context is correct."""
+    import torch
+    from test_parity_gpu import W, gen_generic
+    w = W("generic", "f32", 64, 64, 4, 2)
+    inp = gen_generic(w, 2, 96, seed=31)
+    d = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to("cuda")
+    args = dict(q=d(inp["q"]), decay=d(inp["decay"]), A=d(inp["A"]), Bm=d(inp["Bm"]), K=d(inp["K"]), V=d(inp["V"]))
+    f = sdl.Forward("generic", torch.float32, 1, 2, 96, 64, 64, r_ab=4, r_kv=2)
+    assert f.path == "generic_tcgen05"
+    sdl.dplr_la_set_wait_limit(1000)
+    try:
+        f(**args)
+        torch.cuda.synchronize()
+        assert f.device_status(clear=True) == sdl.dplr.DPLR_ERR_TIMEOUT
+    finally:
+        sdl.dplr_la_set_wait_limit(0)
+    o, ST = f(**args)
+    torch.cuda.synchronize()
+    assert f.device_status() == sdl.DPLR_OK
+    o_ref, S_ref = oracle.forward_inputs(inp)
+    assert _rel(o.double().cpu().numpy(), o_ref) <= 1e-4
+    assert _rel(ST.double().cpu().numpy(), S_ref) <= 1e-4
