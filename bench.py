@@ -376,7 +376,7 @@ def run_ours(args, w):
         elif f.path == "hdla_tcgen05":
             kern = [("hdla_chunk_kernel", sum(k1) / K), ("hdla_chain_kernel", sum(k2) / K)]
         elif f.path == "generic_tcgen05":
-            kern = [("generic_chunk_kernel", sum(k1) / K), ("dplr_state_scan", sum(k2) / K)]
+            kern = [("generic_chunk_kernel", sum(k1) / K), ("generic_chain_kernel", sum(k2) / K)]
         else:
             kern = [("dplr_chunk_maps", sum(k1) / K), ("dplr_state_scan", sum(k2) / K)]
         dom_name, dom_ms = max(kern, key=lambda x: x[1])

@@ -119,11 +119,21 @@ dplr_status make_plan(const dplr_desc* d, Plan* pl) {
     p.fused = fused_supported(p) ? 1 : 0;
     p.tc = (!p.fused && hdla_tc_supported(p)) ? 1 : 0;
     p.gtc = (!p.fused && !p.tc && generic_tc_supported(p)) ? 1 : 0;
+    p.wait_cycles = g_wait_cycles.load(std::memory_order_relaxed);
     if (p.gtc) {
         p.cw = generic_tc_block();
         p.nb = (d->T + p.cw - 1) / p.cw;
+        const long long rows = bh * (long long)p.nb * 64;   // c_j rows, addressed as int by the copies
+        if (rows >= (1LL << 31)) return DPLR_ERR_UNSUPPORTED;
+        size_t total = 0, off_A = 0;
+        generic_tc_offsets(p, &off_A, &p.off_c, &total);
+        p.off_P = off_A;
+        p.off_Q = 0;
+        p.ws_stages = total;
+        p.ws_bytes = total;
+        *pl = p;
+        return DPLR_OK;
     }
-    p.wait_cycles = g_wait_cycles.load(std::memory_order_relaxed);
     if (p.tc) {
         // one unit per (head, 64-token chunk): P_j has 128 rows, addressed as int by the copies
         const long long rows = bh * (long long)((d->T + 63) / 64) * 128;
@@ -260,6 +270,11 @@ dplr_status dplr_la_state_scan(const dplr_desc* desc, const float* S0, float* o,
             return DPLR_ERR_CUDA;
         return DPLR_OK;
     }
+    if (pl.gtc) {
+        if (launch_generic_chain(pl, S0, o, S_T, workspace, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return DPLR_ERR_CUDA;
+        return DPLR_OK;
+    }
     const ScanArgs a = scan_args(pl, S0, o, S_T, workspace);
     if (launch_state_scan(pl, a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return DPLR_ERR_CUDA;
     return DPLR_OK;
@@ -287,8 +302,12 @@ dplr_status dplr_la_forward(const dplr_desc* desc, const void* q, const void* k,
         return DPLR_OK;
     }
     const ChunkMapArgs a = map_args(pl, q, k, v, decay, beta, A, Bm, K, V, o, workspace);
-    if ((pl.gtc ? launch_generic_chunks(pl, a, workspace, s) : launch_chunk_maps(pl, a, s)) != cudaSuccess)
-        return DPLR_ERR_CUDA;
+    if (pl.gtc) {
+        if (launch_generic_chunks(pl, a, workspace, s) != cudaSuccess) return DPLR_ERR_CUDA;
+        if (launch_generic_chain(pl, S0, o, S_T, workspace, s) != cudaSuccess) return DPLR_ERR_CUDA;
+        return DPLR_OK;
+    }
+    if (launch_chunk_maps(pl, a, s) != cudaSuccess) return DPLR_ERR_CUDA;
     if (launch_state_scan(pl, scan_args(pl, S0, o, S_T, workspace), s) != cudaSuccess) return DPLR_ERR_CUDA;
     return DPLR_OK;
 }

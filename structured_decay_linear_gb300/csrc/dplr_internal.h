@@ -87,11 +87,13 @@ cudaError_t launch_hdla_chunks(const Plan& pl, const void* q, const void* k, con
                                const float* beta, float* o, void* workspace, cudaStream_t s);
 cudaError_t launch_hdla_chain(const Plan& pl, const float* S0, float* o, float* ST, void* workspace, cudaStream_t s);
 
-// Tensor-core stage 1 of the generic mode (dk = dv = 64, r_ab <= 4, r_kv <= 2): writes the maps of
-// 32-token WY blocks in the layout of ChunkMapArgs; stage 2 is the fp32 scan.
+// Tensor-core stages of the generic mode (dk = dv = 64, r_ab <= 4, r_kv <= 2): maps of 32-token WY blocks, then
+// the chain over blocks.
 bool generic_tc_supported(const Plan& pl);
 int generic_tc_block();
+void generic_tc_offsets(const Plan& pl, size_t* off_A, size_t* off_c, size_t* total);
 cudaError_t launch_generic_chunks(const Plan& pl, const ChunkMapArgs& a, void* workspace, cudaStream_t s);
+cudaError_t launch_generic_chain(const Plan& pl, const float* S0, float* o, float* ST, void* workspace, cudaStream_t s);
 
 // Fused per-head kernel (structured modes, bf16 inputs, dk = dv = 128).
 bool fused_supported(const Plan& pl);

@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "sm100_ops.cuh"
 
@@ -62,6 +63,48 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& h, uint32_t
     l = pack_bf16(x0 - __uint_as_float(h << 16), x1 - __uint_as_float(h & 0xFFFF0000u));
 }
 
+// ---- fp16 hi + lo with a power-of-two scale. y = x * sc is split as hi = rn_fp16(y), lo = rn_fp16(y - hi);
+// with the scale chosen so that the largest magnitude of the operand lands in [2^14, 2^15) (fp16 overflows at
+// 65504), hi + lo carries ~22 significant bits for every value within 2^11 of the largest, and smaller values
+// keep an absolute error below 2^-25 of the scaled range.
+__device__ __forceinline__ void splith2(float x0, float x1, float sc, uint32_t& h, uint32_t& l) {
+    const float y0 = x0 * sc, y1 = x1 * sc;
+    const __half2 hh = __floats2half2_rn(y0, y1);
+    const float2 hf = __half22float2(hh);
+    const __half2 ll = __floats2half2_rn(y0 - hf.x, y1 - hf.y);
+    h = *reinterpret_cast<const uint32_t*>(&hh);
+    l = *reinterpret_cast<const uint32_t*>(&ll);
+}
+__device__ __forceinline__ void splith1(float x, float sc, uint16_t& h, uint16_t& l) {
+    const float y = x * sc;
+    const __half hh = __float2half_rn(y);
+    const __half ll = __float2half_rn(y - __half2float(hh));
+    h = *reinterpret_cast<const uint16_t*>(&hh);
+    l = *reinterpret_cast<const uint16_t*>(&ll);
+}
+__device__ __forceinline__ float half_value(uint16_t b) {
+    return __half2float(*reinterpret_cast<const __half*>(&b));
+}
+// The scale 2^(14 - floor(log2 m)) for a largest magnitude m (1 when m is zero, tiny or not finite), from the
+// exponent field.
+__device__ __forceinline__ float scale_for(float m) {
+    const int e = static_cast<int>((__float_as_uint(m) >> 23) & 255u) - 127;   // floor(log2 m) for normal m
+    if (!(m > 0.f) || e < -110 || e > 120) return 1.f;
+    return __uint_as_float(static_cast<uint32_t>(14 - e + 127) << 23);
+}
+// Maximum of v over the warp, folded into a shared slot (non-negative floats order like their bit patterns).
+// Every lane of the warp must call it.
+__device__ __forceinline__ void warp_max_to(unsigned int* slot, float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+    if ((threadIdx.x & 31) == 0) atomicMax(slot, __float_as_uint(v));
+}
+// Instruction descriptor for kind::f16 with fp16 A and B, fp32 accumulation.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b_mn) {
+    return (1u << 4) | (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // MMAs issued by lane 0 of a converged warp through a predicate (no divergence, so no costly
 // re-convergence after the issue).
 __device__ __forceinline__ void mma_ss_if(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc, uint32_t issue) {
@@ -98,47 +141,73 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Warp-level C[16x8] = A[16xK] B[Kx8] (mma.sync m16n8k8 tf32, fp32 accumulate); A, B row-major fp32
-// in shared memory. Fragments as in the PTX ISA. TERMS = 1: the operands rounded to tf32 (cvt.rna).
-// TERMS = 3: each operand split as x = hi + lo with both parts tf32, and the three products
-// hi*hi + hi*lo + lo*hi accumulated (the dropped lo*lo term is below fp32 rounding of the sum's
-// leading term by ~2^-22), which keeps the product close to fp32 accuracy.
+// One mma.sync m16n8k8 tf32 (fp32 accumulate) on fragments in registers. Not volatile: independent products
+// may be interleaved by the compiler.
+__device__ __forceinline__ void mma_tf32_frag(float (&c)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// Warp-level products C_i[16x8] = A_i[16xK] B[Kx8], i < NT, for NT row tiles A_i = A + 16 i lda sharing the
+// columns of B (mma.sync m16n8k8 tf32, fp32 accumulate); A, B row-major fp32 in shared memory, fragments as in
+// the PTX ISA. TERMS = 1: the operands rounded to tf32 (cvt.rna). TERMS = 3: each operand split as x = hi + lo
+// with both parts tf32, and hi*hi, hi*lo, lo*hi accumulated separately and added at the end (the dropped lo*lo
+// is ~2^-22 of the product), which keeps the product close to fp32 accuracy.
+template <int TERMS, int NT>
+__device__ __forceinline__ void warp_mma_tf32_tiles(const float* A, int lda, const float* B, int ldb, int K,
+                                                    float (&c)[NT][4]) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+    float acc[NT][TERMS][4];
+#pragma unroll
+    for (int i = 0; i < NT; ++i)
+#pragma unroll
+        for (int t = 0; t < TERMS; ++t) acc[i][t][0] = acc[i][t][1] = acc[i][t][2] = acc[i][t][3] = 0.f;
+#pragma unroll
+    for (int k0 = 0; k0 < K; k0 += 8) {
+        uint32_t bh[2], bl[2];
+        {
+            const float bf[2] = {B[(k0 + q) * ldb + g], B[(k0 + q + 4) * ldb + g]};
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float h = tf32_rn(bf[e]);
+                bh[e] = __float_as_uint(h);
+                bl[e] = __float_as_uint(tf32_rn(bf[e] - h));
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < NT; ++i) {
+            const float* Ai = A + 16 * i * lda;
+            const float af[4] = {Ai[g * lda + k0 + q], Ai[(g + 8) * lda + k0 + q], Ai[g * lda + k0 + q + 4],
+                                 Ai[(g + 8) * lda + k0 + q + 4]};
+            uint32_t ah[4], al[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float h = tf32_rn(af[e]);
+                ah[e] = __float_as_uint(h);
+                al[e] = __float_as_uint(tf32_rn(af[e] - h));
+            }
+            mma_tf32_frag(acc[i][0], ah, bh);
+            if (TERMS == 3) {
+                mma_tf32_frag(acc[i][1], ah, bl);
+                mma_tf32_frag(acc[i][2], al, bh);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < NT; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float v = acc[i][0][e];
+            if (TERMS == 3) v += acc[i][1][e] + acc[i][2][e];
+            c[i][e] = v;
+        }
+}
 template <int TERMS>
 __device__ __forceinline__ void warp_mma_tf32_x(const float* A, int lda, const float* B, int ldb, int K, float (&c)[4]) {
-    const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
-    c[0] = c[1] = c[2] = c[3] = 0.f;
-    for (int k0 = 0; k0 < K; k0 += 8) {
-        const float af[4] = {A[g * lda + k0 + q], A[(g + 8) * lda + k0 + q], A[g * lda + k0 + q + 4],
-                             A[(g + 8) * lda + k0 + q + 4]};
-        const float bf[2] = {B[(k0 + q) * ldb + g], B[(k0 + q + 4) * ldb + g]};
-        uint32_t ah[4], bh[2], al[4], bl[2];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float h = tf32_rn(af[i]);
-            ah[i] = __float_as_uint(h);
-            al[i] = __float_as_uint(tf32_rn(af[i] - h));
-        }
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const float h = tf32_rn(bf[i]);
-            bh[i] = __float_as_uint(h);
-            bl[i] = __float_as_uint(tf32_rn(bf[i] - h));
-        }
-        if (TERMS == 3) {
-            asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-                         "{%0,%1,%2,%3};"
-                         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-                         : "r"(al[0]), "r"(al[1]), "r"(al[2]), "r"(al[3]), "r"(bh[0]), "r"(bh[1]));
-            asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-                         "{%0,%1,%2,%3};"
-                         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-                         : "r"(ah[0]), "r"(ah[1]), "r"(ah[2]), "r"(ah[3]), "r"(bl[0]), "r"(bl[1]));
-        }
-        asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-                     "{%0,%1,%2,%3};"
-                     : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-                     : "r"(ah[0]), "r"(ah[1]), "r"(ah[2]), "r"(ah[3]), "r"(bh[0]), "r"(bh[1]));
-    }
+    float t[1][4];
+    warp_mma_tf32_tiles<TERMS, 1>(A, lda, B, ldb, K, t);
+    c[0] = t[0][0]; c[1] = t[0][1]; c[2] = t[0][2]; c[3] = t[0][3];
 }
 __device__ __forceinline__ void warp_mma_tf32_rn(const float* A, int lda, const float* B, int ldb, int K, float (&c)[4]) {
     warp_mma_tf32_x<1>(A, lda, B, ldb, K, c);
@@ -208,6 +277,11 @@ __device__ __forceinline__ void inv64_inplace(float* X, int t, uint32_t bar) {
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];"
                  :: "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(src) : "memory");
+}
+// Shared -> global bulk copy (16-byte aligned addresses, size a multiple of 16) in the current bulk group.
+__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 :: "l"(reinterpret_cast<uint64_t>(dst)), "r"(src), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
