@@ -398,8 +398,9 @@ def run_ours(args, w):
             "scaling": "weak",
             "vs_baseline": None,
             # arithmetic of the path's products: bf16 tensor-core operands (fp32 accumulation and state;
-            # bf16 hi + lo pairs where one term is too coarse) or fp32 on the CUDA cores
-            "dtype": "f32" if f.path == "two_stage_fp32" else "bf16",
+            # bf16 hi + lo pairs where one term is too coarse), fp16 hi + lo pairs with power-of-two scales
+            # (the generic path), or fp32 on the CUDA cores
+            "dtype": {"two_stage_fp32": "f32", "generic_tcgen05": "f16"}.get(f.path, "bf16"),
             "input_dtype": w.dtype,                        # storage type of q, k, v (A, B, K, V)
             "path": f.path,
             "data": "synthetic (seeded workload recipe, resident in HBM)",
