@@ -6,7 +6,9 @@ and shares no code with it.
 
 ``forward`` runs the plain serial token-by-token recurrence written in
 ``dplr_oracle.c`` (see that file for what each mode computes and the passages
-it follows). Inputs of any float dtype are upcast to float64 exactly.
+it follows); ``backward`` runs its reverse mode (the gradients of
+sum(do * o) + sum(dST * S_T) with respect to every input). Inputs of any float
+dtype are upcast to float64 exactly.
 """
 
 from __future__ import annotations
@@ -48,6 +50,8 @@ def _lib():
             dp = ctypes.POINTER(ctypes.c_double)
             lib.oracle_forward.restype = ctypes.c_int
             lib.oracle_forward.argtypes = [ctypes.c_int] * 8 + [dp] * 12 + [ctypes.c_int]
+            lib.oracle_backward.restype = ctypes.c_int
+            lib.oracle_backward.argtypes = [ctypes.c_int] * 8 + [dp] * 22 + [ctypes.c_int]
             lib.oracle_max_threads.restype = ctypes.c_int
             _handle = lib
     return _handle
@@ -107,3 +111,45 @@ def forward_inputs(inp: dict, threads: Optional[int] = None):
     w = inp["workload"]
     return forward(w.mode, inp["q"], inp["k"], inp["v"], inp["decay"], inp["beta"], inp["A"],
                    inp["Bm"], inp["K"], inp["V"], inp["S0"], threads=threads)
+
+
+def backward(mode: str, q, k=None, v=None, decay=None, beta=None, A=None, Bm=None, K=None, V=None,
+             S0=None, do=None, dST=None, threads: Optional[int] = None) -> dict:
+    """Reverse mode of ``forward``: the gradients of sum(do * o) + sum(dST * S_T) with respect to every
+    input, in float64. ``do`` [B,H,T,dv] is required, ``dST`` [B,H,dk,dv] may be None (zero). Returns a
+    dict with the inputs' names (q, k, v, decay, beta for the structured modes; q, decay, A, Bm, K, V for
+    the generic mode) and S0, each shaped like its input."""
+    m = MODES[mode]
+    q = _f64(q)
+    B, H, T, dk = q.shape
+    k, v, decay, beta = _f64(k), _f64(v), _f64(decay), _f64(beta)
+    A, Bm, K, V, S0 = _f64(A), _f64(Bm), _f64(K), _f64(V), _f64(S0)
+    do, dST = _f64(do), _f64(dST)
+    dv = do.shape[3]
+    if m == 3:
+        r = 0 if A is None else A.shape[3]
+        p = 0 if K is None else K.shape[3]
+    else:
+        r, p = 1, 0
+    z = lambda shape: np.zeros(shape, dtype=np.float64)
+    g = {"q": z(q.shape), "S0": z((B, H, dk, dv)), "decay": z(decay.shape)}
+    if m == 3:
+        g.update(A=z(A.shape) if A is not None else None, Bm=z(Bm.shape) if Bm is not None else None,
+                 K=z(K.shape) if K is not None else None, V=z(V.shape) if V is not None else None)
+    else:
+        g.update(k=z(k.shape), v=z(v.shape), beta=z(beta.shape))
+    rc = _lib().oracle_backward(m, B, H, T, dk, dv, r, p, _ptr(q), _ptr(k), _ptr(v), _ptr(decay), _ptr(beta),
+                                _ptr(A), _ptr(Bm), _ptr(K), _ptr(V), _ptr(S0), _ptr(do), _ptr(dST),
+                                _ptr(g["q"]), _ptr(g.get("k")), _ptr(g.get("v")), _ptr(g["decay"]),
+                                _ptr(g.get("beta")), _ptr(g.get("A")), _ptr(g.get("Bm")), _ptr(g.get("K")),
+                                _ptr(g.get("V")), _ptr(g["S0"]), int(threads or 0))
+    if rc != 0:
+        raise ValueError(f"oracle_backward rejected its arguments (code {rc})")
+    return g
+
+
+def backward_inputs(inp: dict, do, dST=None, threads: Optional[int] = None) -> dict:
+    """``backward`` on a dict produced by ``workloads.generate``."""
+    w = inp["workload"]
+    return backward(w.mode, inp["q"], inp["k"], inp["v"], inp["decay"], inp["beta"], inp["A"], inp["Bm"],
+                    inp["K"], inp["V"], inp["S0"], do, dST, threads=threads)

@@ -210,3 +210,329 @@ int oracle_max_threads(void)
     return 1;
 #endif
 }
+
+/*
+ * Reverse mode of the same serial recurrence: the gradients of a scalar loss
+ *   L = sum_t do_t . o_t + sum(dST * S_T)
+ * with respect to every input, given the upstream gradients do [B,H,T,dv] and
+ * dST [B,H,dk,dv] (NULL = zero). TEST INFRASTRUCTURE ONLY, like the forward.
+ *
+ * The forward pass is re-run and every state S_0 .. S_T of a head is kept
+ * (T+1 blocks of dk x dv doubles, so this is for small problems only); then the
+ * tokens are walked backwards with the adjoint state dS (the gradient of L with
+ * respect to S_t):
+ *   readout   o_t = S_t^T q_t      dq_t = S_t do_t,  dS += q_t do_t^T
+ *   update    S_t = F_t(S_{t-1})   each mode's update differentiated step by
+ *             step (the same steps as the forward), dS <- dF_t^T(dS)
+ * and dS0 is the final dS. Outputs (same layouts as the inputs, NULL = not
+ * wanted): dq, dk, dv, ddecay, dbeta, dA, dBm, dK, dV, dS0.
+ */
+typedef struct {
+    int mode, T, dk, dv, r, p;
+    const double *q, *k, *v, *decay, *beta, *A, *Bm, *K, *V, *S0, *dO, *dST;
+    double *dq, *dk_, *dv_, *ddecay, *dbeta, *dA, *dB, *dK, *dV, *dS0;
+} head_bwd;
+
+/* One token's forward update of the whole state (dk x dv), from Sp into Sn. */
+static void step_forward(const head_bwd* a, int t, const double* Sp, double* Sn, double* w)
+{
+    const int dk = a->dk, dv = a->dv, r = a->r, p = a->p;
+    if (a->mode == ORACLE_MODE_GENERIC) {
+        const double* At = a->A + (size_t)t * r * dk;
+        const double* Bt = a->Bm + (size_t)t * r * dk;
+        const double* lt = a->decay + (size_t)t * dk;
+        for (int i = 0; i < r; ++i)
+            for (int n = 0; n < dv; ++n) {
+                double s = 0.0;
+                for (int c = 0; c < dk; ++c) s += Bt[(size_t)i * dk + c] * Sp[(size_t)c * dv + n];
+                w[(size_t)i * dv + n] = s;
+            }
+        for (int c = 0; c < dk; ++c)
+            for (int n = 0; n < dv; ++n) {
+                double s = exp(lt[c]) * Sp[(size_t)c * dv + n];
+                for (int i = 0; i < r; ++i) s -= At[(size_t)i * dk + c] * w[(size_t)i * dv + n];
+                for (int l = 0; l < p; ++l)
+                    s += a->K[((size_t)t * p + l) * dk + c] * a->V[((size_t)t * p + l) * dv + n];
+                Sn[(size_t)c * dv + n] = s;
+            }
+        return;
+    }
+    const double* kt = a->k + (size_t)t * dk;
+    const double* vt = a->v + (size_t)t * dv;
+    const double bt = a->beta[t];
+    memcpy(Sn, Sp, sizeof(double) * (size_t)dk * dv);
+    if (a->mode == ORACLE_MODE_GDN) {
+        const double gate = exp(a->decay[t]);
+        for (int n = 0; n < dv; ++n) {
+            double s = 0.0;
+            for (int c = 0; c < dk; ++c) s += kt[c] * Sp[(size_t)c * dv + n];
+            w[n] = s;
+        }
+        for (int c = 0; c < dk; ++c)
+            for (int n = 0; n < dv; ++n)
+                Sn[(size_t)c * dv + n] = gate * (Sp[(size_t)c * dv + n] - bt * kt[c] * w[n]) + bt * kt[c] * vt[n];
+        return;
+    }
+    const double* lt = a->decay + (size_t)t * dk;   /* HDLA: erase, forget, erase + write */
+    for (int n = 0; n < dv; ++n) {
+        double s = 0.0;
+        for (int c = 0; c < dk; ++c) s += kt[c] * Sn[(size_t)c * dv + n];
+        w[n] = s;
+    }
+    for (int c = 0; c < dk; ++c)
+        for (int n = 0; n < dv; ++n) Sn[(size_t)c * dv + n] -= bt * kt[c] * w[n];
+    for (int c = 0; c < dk; ++c)
+        for (int n = 0; n < dv; ++n) Sn[(size_t)c * dv + n] *= exp(lt[c]);
+    for (int n = 0; n < dv; ++n) {
+        double s = 0.0;
+        for (int c = 0; c < dk; ++c) s += kt[c] * Sn[(size_t)c * dv + n];
+        w[n] = s - vt[n];
+    }
+    for (int c = 0; c < dk; ++c)
+        for (int n = 0; n < dv; ++n) Sn[(size_t)c * dv + n] -= bt * kt[c] * w[n];
+}
+
+/* Backward of an erase-and-write step  Sout = Sin - beta k (k^T Sin - u)^T  (u = v, or 0 for a pure erase):
+ * given dOut, adds to dk, dbeta (and du when wanted) and writes dIn. */
+static void erase_write_bwd(int dk, int dv, const double* kt, double bt, const double* Sin, const double* u,
+                            const double* dOut, double* dIn, double* dkt, double* dbt, double* dut, double* tmp)
+{
+    /* z = k^T Sin - u,  g = k^T dOut (both dv) */
+    double* z = tmp;
+    double* g = tmp + dv;
+    for (int n = 0; n < dv; ++n) {
+        double s = 0.0, h = 0.0;
+        for (int c = 0; c < dk; ++c) {
+            s += kt[c] * Sin[(size_t)c * dv + n];
+            h += kt[c] * dOut[(size_t)c * dv + n];
+        }
+        z[n] = s - (u ? u[n] : 0.0);
+        g[n] = h;
+    }
+    /* dbeta -= sum_n g_n z_n;  dk_c -= beta (sum_n dOut[c][n] z_n + sum_n Sin[c][n] g_n);  du += beta g */
+    double db = 0.0;
+    for (int n = 0; n < dv; ++n) db += g[n] * z[n];
+    *dbt -= db;
+    for (int c = 0; c < dk; ++c) {
+        double s = 0.0;
+        for (int n = 0; n < dv; ++n) s += dOut[(size_t)c * dv + n] * z[n] + Sin[(size_t)c * dv + n] * g[n];
+        dkt[c] -= bt * s;
+    }
+    if (dut)
+        for (int n = 0; n < dv; ++n) dut[n] += bt * g[n];
+    for (int c = 0; c < dk; ++c)
+        for (int n = 0; n < dv; ++n) dIn[(size_t)c * dv + n] = dOut[(size_t)c * dv + n] - bt * kt[c] * g[n];
+}
+
+static void run_head_bwd(const head_bwd* a, double* states, double* work)
+{
+    const int T = a->T, dk = a->dk, dv = a->dv, r = a->r, p = a->p;
+    const size_t SS = (size_t)dk * dv;
+    double* w = work;                         /* max(r,1) x dv */
+    double* dS = w + (size_t)(r > 1 ? r : 1) * dv;
+    double* dT = dS + SS;                     /* scratch state-sized blocks */
+    double* S1 = dT + SS;
+    double* S2 = S1 + SS;
+    double* tmp = S2 + SS;                    /* 2 dv + r dv */
+    for (size_t e = 0; e < SS; ++e) states[e] = a->S0 ? a->S0[e] : 0.0;
+    for (int t = 0; t < T; ++t) step_forward(a, t, states + (size_t)t * SS, states + (size_t)(t + 1) * SS, w);
+    for (size_t e = 0; e < SS; ++e) dS[e] = a->dST ? a->dST[e] : 0.0;
+
+    for (int t = T - 1; t >= 0; --t) {
+        const double* St = states + (size_t)(t + 1) * SS;
+        const double* Sp = states + (size_t)t * SS;
+        const double* qt = a->q + (size_t)t * dk;
+        const double* dot = a->dO + (size_t)t * dv;
+        /* readout */
+        if (a->dq)
+            for (int c = 0; c < dk; ++c) {
+                double s = 0.0;
+                for (int n = 0; n < dv; ++n) s += St[(size_t)c * dv + n] * dot[n];
+                a->dq[(size_t)t * dk + c] = s;
+            }
+        for (int c = 0; c < dk; ++c)
+            for (int n = 0; n < dv; ++n) dS[(size_t)c * dv + n] += qt[c] * dot[n];
+
+        if (a->mode == ORACLE_MODE_GENERIC) {
+            const double* At = a->A + (size_t)t * r * dk;
+            const double* Bt = a->Bm + (size_t)t * r * dk;
+            const double* lt = a->decay + (size_t)t * dk;
+            double* dW = tmp;   /* r x dv */
+            for (int i = 0; i < r; ++i)
+                for (int n = 0; n < dv; ++n) {
+                    double s = 0.0, h = 0.0;
+                    for (int c = 0; c < dk; ++c) {
+                        s += Bt[(size_t)i * dk + c] * Sp[(size_t)c * dv + n];
+                        h += At[(size_t)i * dk + c] * dS[(size_t)c * dv + n];
+                    }
+                    w[(size_t)i * dv + n] = s;      /* W = B^T S_{t-1} */
+                    dW[(size_t)i * dv + n] = -h;    /* dW = -A^T dS */
+                }
+            for (int c = 0; c < dk; ++c) {
+                const double lam = exp(lt[c]);
+                double dd = 0.0;
+                for (int n = 0; n < dv; ++n) dd += dS[(size_t)c * dv + n] * Sp[(size_t)c * dv + n];
+                if (a->ddecay) a->ddecay[(size_t)t * dk + c] = lam * dd;
+                for (int i = 0; i < r; ++i) {
+                    double sa = 0.0, sb = 0.0;
+                    for (int n = 0; n < dv; ++n) {
+                        sa += dS[(size_t)c * dv + n] * w[(size_t)i * dv + n];
+                        sb += Sp[(size_t)c * dv + n] * dW[(size_t)i * dv + n];
+                    }
+                    if (a->dA) a->dA[((size_t)t * r + i) * dk + c] = -sa;
+                    if (a->dB) a->dB[((size_t)t * r + i) * dk + c] = sb;
+                }
+                for (int l = 0; l < p; ++l) {
+                    double s = 0.0;
+                    for (int n = 0; n < dv; ++n) s += dS[(size_t)c * dv + n] * a->V[((size_t)t * p + l) * dv + n];
+                    if (a->dK) a->dK[((size_t)t * p + l) * dk + c] = s;
+                }
+            }
+            for (int l = 0; l < p; ++l)
+                for (int n = 0; n < dv; ++n) {
+                    double s = 0.0;
+                    for (int c = 0; c < dk; ++c) s += dS[(size_t)c * dv + n] * a->K[((size_t)t * p + l) * dk + c];
+                    if (a->dV) a->dV[((size_t)t * p + l) * dv + n] = s;
+                }
+            /* dS_{t-1} = D dS + B dW */
+            for (int c = 0; c < dk; ++c)
+                for (int n = 0; n < dv; ++n) {
+                    double s = exp(lt[c]) * dS[(size_t)c * dv + n];
+                    for (int i = 0; i < r; ++i) s += Bt[(size_t)i * dk + c] * dW[(size_t)i * dv + n];
+                    dT[(size_t)c * dv + n] = s;
+                }
+            memcpy(dS, dT, sizeof(double) * SS);
+            continue;
+        }
+        const double* kt = a->k + (size_t)t * dk;
+        const double* vt = a->v + (size_t)t * dv;
+        const double bt = a->beta[t];
+        double* dkt = tmp + 2 * (size_t)dv;   /* dk */
+        double* dvt = dkt + dk;               /* dv */
+        double dbt = 0.0;
+        for (int c = 0; c < dk; ++c) dkt[c] = 0.0;
+        for (int n = 0; n < dv; ++n) dvt[n] = 0.0;
+        if (a->mode == ORACLE_MODE_GDN) {
+            /* S_t = e^g X + beta k v^T with X = S_{t-1} - beta k (k^T S_{t-1})^T */
+            const double gate = exp(a->decay[t]);
+            memcpy(S1, Sp, sizeof(double) * SS);
+            for (int n = 0; n < dv; ++n) {
+                double s = 0.0;
+                for (int c = 0; c < dk; ++c) s += kt[c] * Sp[(size_t)c * dv + n];
+                w[n] = s;
+            }
+            for (int c = 0; c < dk; ++c)
+                for (int n = 0; n < dv; ++n) S1[(size_t)c * dv + n] -= bt * kt[c] * w[n];   /* X */
+            double dg = 0.0;
+            for (size_t e = 0; e < SS; ++e) dg += dS[e] * S1[e];
+            if (a->ddecay) a->ddecay[t] = gate * dg;
+            /* the write beta k v^T */
+            for (int n = 0; n < dv; ++n) {
+                double s = 0.0;
+                for (int c = 0; c < dk; ++c) s += kt[c] * dS[(size_t)c * dv + n];
+                dvt[n] += bt * s;
+                dbt += s * vt[n];
+            }
+            for (int c = 0; c < dk; ++c) {
+                double s = 0.0;
+                for (int n = 0; n < dv; ++n) s += dS[(size_t)c * dv + n] * vt[n];
+                dkt[c] += bt * s;
+            }
+            for (size_t e = 0; e < SS; ++e) dT[e] = gate * dS[e];   /* dX */
+            erase_write_bwd(dk, dv, kt, bt, Sp, NULL, dT, dS, dkt, &dbt, NULL, tmp);
+        } else {
+            /* HDLA: S1 = erase(S_{t-1}), S2 = Diag(lambda) S1, S_t = erase_write(S2, v) */
+            const double* lt = a->decay + (size_t)t * dk;
+            memcpy(S1, Sp, sizeof(double) * SS);
+            for (int n = 0; n < dv; ++n) {
+                double s = 0.0;
+                for (int c = 0; c < dk; ++c) s += kt[c] * Sp[(size_t)c * dv + n];
+                w[n] = s;
+            }
+            for (int c = 0; c < dk; ++c)
+                for (int n = 0; n < dv; ++n) S1[(size_t)c * dv + n] -= bt * kt[c] * w[n];
+            for (int c = 0; c < dk; ++c)
+                for (int n = 0; n < dv; ++n) S2[(size_t)c * dv + n] = exp(lt[c]) * S1[(size_t)c * dv + n];
+            erase_write_bwd(dk, dv, kt, bt, S2, vt, dS, dT, dkt, &dbt, dvt, tmp);   /* dT = dS2 */
+            for (int c = 0; c < dk; ++c) {
+                const double lam = exp(lt[c]);
+                double dd = 0.0;
+                for (int n = 0; n < dv; ++n) dd += dT[(size_t)c * dv + n] * S1[(size_t)c * dv + n];
+                if (a->ddecay) a->ddecay[(size_t)t * dk + c] = lam * dd;
+                for (int n = 0; n < dv; ++n) dT[(size_t)c * dv + n] *= lam;   /* dS1 */
+            }
+            erase_write_bwd(dk, dv, kt, bt, Sp, NULL, dT, dS, dkt, &dbt, NULL, tmp);
+        }
+        if (a->dk_) memcpy(a->dk_ + (size_t)t * dk, dkt, sizeof(double) * dk);
+        if (a->dv_) memcpy(a->dv_ + (size_t)t * dv, dvt, sizeof(double) * dv);
+        if (a->dbeta) a->dbeta[t] = dbt;
+    }
+    if (a->dS0) memcpy(a->dS0, dS, sizeof(double) * SS);
+}
+
+int oracle_backward(int mode, int B, int H, int T, int dk, int dv, int r, int p,
+                    const double* q, const double* k, const double* v,
+                    const double* decay, const double* beta,
+                    const double* A, const double* Bm, const double* K, const double* V,
+                    const double* S0, const double* dO, const double* dST,
+                    double* dq, double* dk_, double* dv_, double* ddecay, double* dbeta,
+                    double* dA, double* dBm, double* dK, double* dV, double* dS0, int nthreads)
+{
+    if (B < 0 || H < 0 || T < 0 || dk <= 0 || dv <= 0) return -1;
+    if (mode != ORACLE_MODE_GDN && mode != ORACLE_MODE_HDLA && mode != ORACLE_MODE_GENERIC) return -2;
+    if (mode == ORACLE_MODE_GENERIC) {
+        if (r < 0 || p < 0) return -3;
+        if (T > 0 && (!decay || !q || (r > 0 && (!A || !Bm)) || (p > 0 && (!K || !V)))) return -4;
+    } else {
+        r = 1;
+        p = 0;
+        if (T > 0 && (!q || !k || !v || !decay || !beta)) return -4;
+    }
+    if (T > 0 && !dO) return -4;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    const size_t SS = (size_t)dk * dv;
+    const long nheads = (long)B * H;
+    const int rw = r > 1 ? r : 1;
+#pragma omp parallel
+    {
+        double* states = (double*)malloc(sizeof(double) * SS * ((size_t)T + 1));
+        double* work = (double*)malloc(sizeof(double) * ((size_t)rw * dv + 4 * SS + 3 * (size_t)dv + (size_t)rw * dv + dk));
+#pragma omp for schedule(dynamic, 1)
+        for (long bh = 0; bh < nheads; ++bh) {
+            const size_t tk = (size_t)bh * T;
+            const int gd = mode == ORACLE_MODE_GDN;
+            head_bwd a;
+            a.mode = mode; a.T = T; a.dk = dk; a.dv = dv; a.r = r; a.p = p;
+            a.q = q ? q + tk * dk : NULL;
+            a.k = k ? k + tk * dk : NULL;
+            a.v = v ? v + tk * dv : NULL;
+            a.decay = decay ? decay + tk * (gd ? 1 : dk) : NULL;
+            a.beta = beta ? beta + tk : NULL;
+            a.A = A ? A + tk * r * dk : NULL;
+            a.Bm = Bm ? Bm + tk * r * dk : NULL;
+            a.K = K ? K + tk * p * dk : NULL;
+            a.V = V ? V + tk * p * dv : NULL;
+            a.S0 = S0 ? S0 + (size_t)bh * SS : NULL;
+            a.dO = dO ? dO + tk * dv : NULL;
+            a.dST = dST ? dST + (size_t)bh * SS : NULL;
+            a.dq = dq ? dq + tk * dk : NULL;
+            a.dk_ = dk_ ? dk_ + tk * dk : NULL;
+            a.dv_ = dv_ ? dv_ + tk * dv : NULL;
+            a.ddecay = ddecay ? ddecay + tk * (gd ? 1 : dk) : NULL;
+            a.dbeta = dbeta ? dbeta + tk : NULL;
+            a.dA = dA ? dA + tk * r * dk : NULL;
+            a.dB = dBm ? dBm + tk * r * dk : NULL;
+            a.dK = dK ? dK + tk * p * dk : NULL;
+            a.dV = dV ? dV + tk * p * dv : NULL;
+            a.dS0 = dS0 ? dS0 + (size_t)bh * SS : NULL;
+            if (states && work) run_head_bwd(&a, states, work);
+        }
+        free(states);
+        free(work);
+    }
+    return 0;
+}
