@@ -1,4 +1,5 @@
-"""Plants plausible mistakes in copies of the oracle (CPU only) and checks the pins catch each one.
+"""Plants plausible mistakes in copies of the oracle (CPU only) and checks the pins catch each one
+(the forward's pins for mistakes in the forward, the reverse mode's for mistakes in the reverse mode).
 
 Every mutant is compiled from a string-edited copy of ``oracle/dplr_oracle.c``
 into a temporary directory, swapped in for the real library, and run through
@@ -13,6 +14,7 @@ import subprocess
 import pytest
 
 import oracle
+import test_oracle_backward as bpins
 import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "dplr_oracle.c")
@@ -65,11 +67,41 @@ PIN_CALLS = [
 ]
 
 
-def _build_mutant(tmp_path, name, old, new):
+BWD_MARK = "/*\n * Reverse mode of the same serial recurrence"
+
+# Mistakes planted in the reverse mode (after BWD_MARK), caught by the finite-difference and closed-form pins.
+BWD_MUTANTS = {
+    "bwd_readout_adjoint_dropped": ("for (int n = 0; n < dv; ++n) dS[(size_t)c * dv + n] += qt[c] * dot[n];",
+                                    "for (int n = 0; n < dv; ++n) dS[(size_t)c * dv + n] += 0.0 * qt[c] * dot[n];"),
+    "bwd_generic_decay_not_transposed": ("double s = exp(lt[c]) * dS[(size_t)c * dv + n];",
+                                         "double s = dS[(size_t)c * dv + n];"),
+    "bwd_gdn_gate_on_write_adjoint": ("for (size_t e = 0; e < SS; ++e) dT[e] = gate * dS[e];   /* dX */",
+                                      "for (size_t e = 0; e < SS; ++e) dT[e] = dS[e];   /* dX */"),
+    "bwd_erase_beta_sign": ("    *dbt -= db;", "    *dbt += db;"),
+    "bwd_hdla_decay_grad_uses_wrong_state": ("for (int n = 0; n < dv; ++n) dd += dT[(size_t)c * dv + n] * S1[(size_t)c * dv + n];",
+                                             "for (int n = 0; n < dv; ++n) dd += dT[(size_t)c * dv + n] * S2[(size_t)c * dv + n];"),
+    "bwd_final_state_gradient_ignored": ("for (size_t e = 0; e < SS; ++e) dS[e] = a->dST ? a->dST[e] : 0.0;",
+                                         "for (size_t e = 0; e < SS; ++e) dS[e] = 0.0;"),
+}
+
+BWD_PIN_CALLS = [
+    bpins.test_gdn_backward_matches_finite_differences,
+    bpins.test_hdla_backward_matches_finite_differences,
+    lambda: bpins.test_generic_backward_matches_finite_differences(2, 1),
+    bpins.test_linear_attention_closed_form,
+    bpins.test_state_gradient_is_the_transposed_map,
+]
+
+
+def _build_mutant(tmp_path, name, old, new, backward=False):
     text = open(SRC).read()
-    assert text.count(old) == 1, f"mutation anchor for {name} not unique/found"
+    cut = text.index(BWD_MARK)
+    fwd, bwd = text[:cut], text[cut:]
+    part = bwd if backward else fwd
+    assert part.count(old) == 1, f"mutation anchor for {name} not unique/found"
+    part = part.replace(old, new)
     src = tmp_path / f"{name}.c"
-    src.write_text(text.replace(old, new))
+    src.write_text(fwd + part if backward else part + bwd)
     so = tmp_path / f"{name}.so"
     subprocess.run(["gcc", "-O1", "-std=c11", "-fopenmp", "-fPIC", "-shared", str(src), "-o", str(so), "-lm"],
                    check=True)
@@ -77,6 +109,8 @@ def _build_mutant(tmp_path, name, old, new):
     dp = ctypes.POINTER(ctypes.c_double)
     lib.oracle_forward.restype = ctypes.c_int
     lib.oracle_forward.argtypes = [ctypes.c_int] * 8 + [dp] * 12 + [ctypes.c_int]
+    lib.oracle_backward.restype = ctypes.c_int
+    lib.oracle_backward.argtypes = [ctypes.c_int] * 8 + [dp] * 22 + [ctypes.c_int]
     lib.oracle_max_threads.restype = ctypes.c_int
     return lib
 
@@ -89,6 +123,21 @@ def test_pins_catch_planted_mistake(name, tmp_path, monkeypatch):
     monkeypatch.setattr(oracle, "_handle", lib)
     caught = 0
     for call in PIN_CALLS:
+        try:
+            call()
+        except AssertionError:
+            caught += 1
+    assert caught > 0, f"no pin failed for mutant {name}"
+
+
+@pytest.mark.parametrize("name", sorted(BWD_MUTANTS))
+def test_backward_pins_catch_planted_mistake(name, tmp_path, monkeypatch):
+    old, new = BWD_MUTANTS[name]
+    lib = _build_mutant(tmp_path, name, old, new, backward=True)
+    oracle._lib()
+    monkeypatch.setattr(oracle, "_handle", lib)
+    caught = 0
+    for call in BWD_PIN_CALLS:
         try:
             call()
         except AssertionError:
