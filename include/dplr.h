@@ -176,12 +176,39 @@ DPLR_API dplr_status dplr_la_decode_step(const dplr_desc* desc,
                                 const void* A, const void* Bm, const void* K, const void* V,
                                 float* S, float* o, void* stream);
 
+/* Backward of dplr_la_forward: the gradients of a scalar loss L with respect to every input,
+ * given dO = dL/do [B,H,T,dv] and dST = dL/dS_T [B,H,dk,dv] (nullable: zero), for the same
+ * descriptor and inputs as the forward. The chunkwise algorithm exists for chunk-parallel
+ * training (HDLA page, Key design 3); its backward reuses the WY factors of every block:
+ * the forward again at blocks of cb tokens keeping the state before each block (cb = 32 for
+ * GDN, 16 for HDLA, the largest power of two with cb max(r_ab, r_kv) <= 32 in the generic mode,
+ * so ranks up to 8), the blocks' state gradients
+ * backwards through the transposed block maps, then every block's input gradients in parallel.
+ * Outputs, all fp32 whatever the input type, same layouts as the inputs:
+ *   dq [B,H,T,dk]; ddecay (GDN [B,H,T], HDLA/generic [B,H,T,dk]); dS0 [B,H,dk,dv] (nullable);
+ *   GDN, HDLA: dk [B,H,T,dk], dv [B,H,T,dv], dbeta [B,H,T];
+ *   generic:   dA, dBm [B,H,T,r_ab,dk], dK [B,H,T,r_kv,dk], dV [B,H,T,r_kv,dv].
+ * Unused outputs of a mode may be null. The arithmetic is fp32 on the CUDA cores. Workspace:
+ * dplr_la_backward_workspace_size(desc) bytes (the maps, states and state gradients of every
+ * block), 256-byte aligned, owned by the caller. Asynchronous on `stream`; allocates nothing.
+ * Errors: as dplr_la_forward; DPLR_ERR_UNSUPPORTED for dk or dv above 128. */
+DPLR_API size_t dplr_la_backward_workspace_size(const dplr_desc* desc);
+DPLR_API dplr_status dplr_la_backward(const dplr_desc* desc,
+                             const void* q, const void* k, const void* v,
+                             const float* decay, const float* beta,
+                             const void* A, const void* Bm, const void* K, const void* V,
+                             const float* S0, const float* dO, const float* dST,
+                             float* dq, float* dk, float* dv, float* ddecay, float* dbeta,
+                             float* dA, float* dBm, float* dK, float* dV, float* dS0,
+                             void* workspace, size_t ws_bytes, void* stream);
+
 /* Name of the kernel path that dplr_la_forward runs for `desc` (no counterpart in the
  * paper; static storage): "gdn_fused_tcgen05" (GDN, bf16, dk = dv = 128: one fused
  * per-head kernel on the tensor cores), "hdla_tcgen05" (HDLA, bf16, dk = dv = 128: the
- * chunk-map and chain kernels on the tensor cores), "two_stage_fp32" (every other case:
- * the chunk-map and state-scan kernels in fp32 on the CUDA cores), or "" if `desc` is
- * invalid or unsupported. */
+ * chunk-map and chain kernels on the tensor cores), "generic_tcgen05" (generic mode,
+ * dk = dv = 64, r_ab <= 4, r_kv <= 2: the generic chunk and chain kernels on the tensor
+ * cores), "two_stage_fp32" (every other case: the chunk-map and state-scan kernels in fp32
+ * on the CUDA cores), or "" if `desc` is invalid or unsupported. */
 DPLR_API const char* dplr_la_path(const dplr_desc* desc);
 
 /* Human-readable name of a status code (static storage). */

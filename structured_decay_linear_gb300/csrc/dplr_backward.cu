@@ -1,0 +1,583 @@
+// Backward of the chunkwise DPLR forward: the gradients of a scalar loss with respect to every input, given
+// the upstream gradients dO of the outputs and dS_T of the final state. The chunk-wise algorithm of
+// "Householder-Diagonalized Linear Attention" (Key design 3) exists for chunk-parallel training; its backward
+// reuses the same WY factors.
+//
+// Three passes over blocks of cb tokens (cb = the largest power of two with cb max(r, p) <= 32 in the generic form
+// of the mode: 32 for GDN, 16 for HDLA):
+//   1. the forward again, with the fp32 chunk-map and scan kernels at WY blocks of cb tokens, keeping the state
+//      before every block (the checkpoints S_{j-1});
+//   2. the block-boundary state gradients, backwards over the blocks with the transposed maps of pass 1:
+//         dS_{j-1} = P_j^T dS_j + Q'_j^T dO_j,    dS_{nb} = dS_T,   dS0 = dS_{-1} ... (the gradient of S0)
+//   3. every block in parallel: given S_{j-1}, dS_j and the block's dO, the gradients of its inputs through the
+//      block's WY algebra (below), then through the decay scaling and the mode's factor construction.
+//
+// Pass 3 in the generic form S_t = D_t S_{t-1} - A_t (B_t^T S_{t-1}) + K_t V_t^T, with the block's decay-scaled
+// factors (anchor a = G_C / 2, as in the forward) A~, B~, K~, Q~, its Gram blocks L = strict(B~ A~^T),
+// G = strict(B~ K~^T), QA = incl(Q~ A~^T), QK = incl(Q~ K~^T), M = (I + L)^{-1}, the scaled state S0 = e^a S_{j-1}
+// and the block's forward quantities H = B~ S0 + G V, E = M H:
+//   dS^ = e^a dS_j          dE = -A~ dS^ - QA^T dO          dH = M^T dE
+//   dA~ = -E dS^T + dQA^T Q~ + dL^T B~        dQA = incl(-dO E^T),   dL = strict(-dH E^T)
+//   dB~ = dH S0^T + dG K~ + dL A~             dG  = strict(dH V^T),  dQK = incl(dO V^T)
+//   dK~ = V dS^T + dQK^T Q~ + dG^T B~         dV  = K~ dS^ + QK^T dO + G^T dH
+//   dQ~ = dO S0^T + dQA A~ + dQK K~
+// then dA = e^{a - G_t} dA~ (and likewise for B, K, q), and the cumulative log-decay collects
+//   dG_t = -sum A~ dA~ - sum K~ dK~ + Q~ dQ~ + sum B~_{t+1} dB~_{t+1} (+ sum_n S_j dS_j at the block's end),
+// the log-decay's gradient being its reverse cumulative sum over the block. The state dimension is walked in
+// slices of 16 columns, so the block's matrices stay in shared memory. Pass 3 runs in fp32 on the CUDA cores.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "dplr_internal.h"
+
+namespace dplr {
+namespace {
+
+constexpr int BT = 256;      // threads of the block-backward kernel
+constexpr int BMX = 32;      // rows of A~ (R = cb r), K~ (P = cb p) and Q~ (cb) at most
+constexpr int BNS = 16;      // state columns per slice
+constexpr int BD = 128;      // dk, dv at most
+
+template <class T> __device__ __forceinline__ float ldg(const T* p, size_t i);
+template <> __device__ __forceinline__ float ldg<float>(const float* p, size_t i) { return p[i]; }
+template <> __device__ __forceinline__ float ldg<__nv_bfloat16>(const __nv_bfloat16* p, size_t i) {
+    return __bfloat162float(p[i]);
+}
+
+struct BwdArgs {
+    const void* q; const void* k; const void* v; const float* decay; const float* beta;
+    const void* A; const void* Bm; const void* K; const void* V;
+    const float* dO; const float* Sb; const float* dSb; const float* ST;
+    float* dq; float* dk; float* dv; float* ddecay; float* dbeta; float* dA; float* dBm; float* dK; float* dV;
+};
+
+// C[m][n] (=, +=) alpha sum_k A(m, k) B(k, n) over the CTA's threads, with A(m, k) = A[m lda + k] (ta: A[k lda + m])
+// and B(k, n) = B[k ldb + n] (tb: B[n ldb + k]); all in shared memory.
+__device__ __forceinline__ void mm(float* C, int ldc, const float* A, int lda, bool ta, const float* B, int ldb,
+                                   bool tb, int M, int N, int K, float alpha, bool acc) {
+    for (int idx = threadIdx.x; idx < M * N; idx += blockDim.x) {
+        const int m = idx / N, n = idx - m * N;
+        float s = 0.f;
+        for (int k = 0; k < K; ++k)
+            s = fmaf(ta ? A[k * lda + m] : A[m * lda + k], tb ? B[n * ldb + k] : B[k * ldb + n], s);
+        C[m * ldc + n] = acc ? C[m * ldc + n] + alpha * s : alpha * s;
+    }
+}
+
+// Keeps C[m][n] where (token of column n) < (token of row m) (strict) or <= (inclusive); zero elsewhere.
+__device__ __forceinline__ void mask(float* C, int ldc, int M, int N, int rdiv, int cdiv, bool strict) {
+    for (int idx = threadIdx.x; idx < M * N; idx += blockDim.x) {
+        const int m = idx / N, n = idx - m * N;
+        const int tm = m / rdiv, tn = n / cdiv;
+        if (strict ? !(tn < tm) : !(tn <= tm)) C[m * ldc + n] = 0.f;
+    }
+}
+
+template <int MODE, class IT>
+__global__ void __launch_bounds__(BT)
+block_bwd_kernel(Plan pl, BwdArgs a) {
+    extern __shared__ __align__(16) float sm[];
+    float* At = sm;                 // [BMX][BD] scaled factors
+    float* Bt = At + BMX * BD;
+    float* Kt = Bt + BMX * BD;
+    float* Qt = Kt + BMX * BD;
+    float* dAt = Qt + BMX * BD;     // their gradients
+    float* dBt = dAt + BMX * BD;
+    float* dKt = dBt + BMX * BD;
+    float* dQt = dKt + BMX * BD;
+    float* Mm = dQt + BMX * BD;     // [BMX][BMX] L, then M
+    float* Gm = Mm + BMX * BMX;
+    float* QA = Gm + BMX * BMX;
+    float* QK = QA + BMX * BMX;
+    float* dL = QK + BMX * BMX;
+    float* dG = dL + BMX * BMX;
+    float* dQA = dG + BMX * BMX;
+    float* dQK = dQA + BMX * BMX;
+    float* S0s = dQK + BMX * BMX;   // [BD][BNS] slice of e^a S_{j-1}; with dSs also the dG_t / d decay table later
+    float* dSs = S0s + BD * BNS;    // [BD][BNS] slice of e^a dS_j
+    float* dOs = dSs + BD * BNS;    // [BMX][BNS]
+    float* Vs = dOs + BMX * BNS;
+    float* Hs = Vs + BMX * BNS;
+    float* Es = Hs + BMX * BNS;
+    float* dEs = Es + BMX * BNS;
+    float* dHs = dEs + BMX * BNS;
+    float* Gc = dHs + BMX * BNS;    // [BMX][BD] inclusive cumulative log-decay G_t
+    float* va = Gc + BMX * BD;      // [BD] anchor a
+    float* sd = va + BD;            // [BD] sum_n S_j dS_j per row
+    float* ct = sd + BD;            // [BMX] HDLA: k^T Lambda k per token
+
+    const int tid = threadIdx.x, nth = blockDim.x, warp = tid >> 5, lane = tid & 31;
+    const int dk = pl.dk, dv = pl.dv, T = pl.T, nb = pl.nb, cb = pl.cw;
+    const int r = MODE == DPLR_GENERIC ? pl.r : (MODE == DPLR_GDN ? 1 : 2);
+    const int p = MODE == DPLR_GENERIC ? pl.p : 1;
+    const int R = cb * r, P = cb * p;
+    const int j = blockIdx.x % nb;
+    const size_t bh = blockIdx.x / nb;
+    const size_t tok0 = bh * (size_t)T + (size_t)j * cb;
+    const int valid = min(cb, T - j * cb);
+    const IT* q = static_cast<const IT*>(a.q);
+    const IT* kin = static_cast<const IT*>(a.k);
+    const IT* vin = static_cast<const IT*>(a.v);
+    const IT* Ain = static_cast<const IT*>(a.A);
+    const IT* Bin = static_cast<const IT*>(a.Bm);
+    const IT* Kin = static_cast<const IT*>(a.K);
+    const IT* Vin = static_cast<const IT*>(a.V);
+
+    // ---- the block's log-decay (identity padding past the end), its inclusive prefix per channel, the anchor
+    for (int i = tid; i < cb * dk; i += nth) {
+        const int t = i / dk, c = i - t * dk;
+        float d = 0.f;
+        if (t < valid) d = MODE == DPLR_GDN ? a.decay[tok0 + t] : a.decay[(tok0 + t) * dk + c];
+        Gc[t * BD + c] = d;
+    }
+    if (MODE == DPLR_HDLA)
+        for (int t = tid; t < cb; t += nth) ct[t] = 0.f;
+    __syncthreads();
+    for (int c = tid; c < dk; c += nth) {
+        float g = 0.f;
+        for (int t = 0; t < cb; ++t) {
+            g += Gc[t * BD + c];
+            Gc[t * BD + c] = g;
+        }
+        va[c] = 0.5f * g;
+    }
+    if (MODE == DPLR_HDLA) {   // c_t = k_t^T Lambda_t k_t (warp per token)
+        for (int t = warp; t < valid; t += nth / 32) {
+            float s = 0.f;
+            for (int c = lane; c < dk; c += 32) {
+                const float kk = ldg(kin, (tok0 + t) * dk + c);
+                s = fmaf(__expf(a.decay[(tok0 + t) * dk + c]) * kk, kk, s);
+            }
+            for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+            if (lane == 0) ct[t] = s;
+        }
+    }
+    __syncthreads();
+
+    // ---- the decay-scaled generic-form factors of the block's tokens
+    for (int i = tid; i < cb * dk; i += nth) {
+        const int t = i / dk, c = i - t * dk;
+        const float G = Gc[t * BD + c], Gx = t > 0 ? Gc[(t - 1) * BD + c] : 0.f, an = va[c];
+        const float er = __expf(an - G), ef = __expf(Gx - an), eq = __expf(G - an);
+        const bool ok = t < valid;
+        const size_t tg = tok0 + t;
+        Qt[t * BD + c] = ok ? eq * ldg(q, tg * dk + c) : 0.f;
+        if (MODE == DPLR_GENERIC) {
+            for (int e = 0; e < r; ++e) {
+                At[(t * r + e) * BD + c] = ok ? er * ldg(Ain, (tg * r + e) * dk + c) : 0.f;
+                Bt[(t * r + e) * BD + c] = ok ? ef * ldg(Bin, (tg * r + e) * dk + c) : 0.f;
+            }
+            for (int e = 0; e < p; ++e) Kt[(t * p + e) * BD + c] = ok ? er * ldg(Kin, (tg * p + e) * dk + c) : 0.f;
+        } else {
+            const float kk = ok ? ldg(kin, tg * dk + c) : 0.f, b = ok ? a.beta[tg] : 0.f;
+            if (MODE == DPLR_GDN) {
+                const float eg = ok ? __expf(a.decay[tg]) : 1.f;
+                At[t * BD + c] = er * eg * b * kk;
+                Bt[t * BD + c] = ef * kk;
+            } else {
+                const float lam = ok ? __expf(a.decay[tg * dk + c]) : 1.f;
+                At[(2 * t) * BD + c] = er * kk;
+                At[(2 * t + 1) * BD + c] = er * lam * kk;
+                Bt[(2 * t) * BD + c] = ef * (b * lam * kk - b * b * ct[t] * kk);
+                Bt[(2 * t + 1) * BD + c] = ef * b * kk;
+            }
+            Kt[t * BD + c] = er * b * kk;
+        }
+    }
+    __syncthreads();
+
+    // ---- Gram blocks and the WY inverse M = (I + L)^{-1} (forward substitution, one column per thread)
+    mm(Mm, BMX, Bt, BD, false, At, BD, true, R, R, dk, 1.f, false);
+    mm(Gm, BMX, Bt, BD, false, Kt, BD, true, R, P, dk, 1.f, false);
+    mm(QA, BMX, Qt, BD, false, At, BD, true, cb, R, dk, 1.f, false);
+    mm(QK, BMX, Qt, BD, false, Kt, BD, true, cb, P, dk, 1.f, false);
+    __syncthreads();
+    mask(Mm, BMX, R, R, r, r, true);
+    mask(Gm, BMX, R, P, r, p, true);
+    mask(QA, BMX, cb, R, 1, r, false);
+    mask(QK, BMX, cb, P, 1, p, false);
+    __syncthreads();
+    if (tid < R) {   // column tid of M into dL (scratch), then back over L
+        const int col = tid;
+        for (int i = 0; i < R; ++i) {
+            float s = i == col ? 1.f : 0.f;
+            for (int kx = 0; kx < i; ++kx) s = fmaf(-Mm[i * BMX + kx], dL[kx * BMX + col], s);
+            dL[i * BMX + col] = s;
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < R * BMX; i += nth) Mm[i] = dL[i];
+    for (int i = tid; i < BMX * BD; i += nth) dAt[i] = dBt[i] = dKt[i] = dQt[i] = 0.f;
+    for (int i = tid; i < BMX * BMX; i += nth) dL[i] = dG[i] = dQA[i] = dQK[i] = 0.f;
+    for (int c = tid; c < dk; c += nth) sd[c] = 0.f;
+    __syncthreads();
+
+    // ---- the state dimension in slices
+    const float* S0g = a.Sb + (bh * (size_t)nb + j) * (size_t)dk * dv;
+    const float* dSg = a.dSb + (bh * (size_t)nb + j) * (size_t)dk * dv;
+    const float* S1g = j + 1 < nb ? a.Sb + (bh * (size_t)nb + j + 1) * (size_t)dk * dv : a.ST + bh * (size_t)dk * dv;
+    for (int n0 = 0; n0 < dv; n0 += BNS) {
+        for (int i = tid; i < dk * BNS; i += nth) {
+            const int c = i / BNS, n = i - c * BNS;
+            const float e = __expf(va[c]);
+            S0s[i] = e * S0g[(size_t)c * dv + n0 + n];
+            const float ds = dSg[(size_t)c * dv + n0 + n];
+            dSs[i] = e * ds;
+            atomicAdd(&sd[c], S1g[(size_t)c * dv + n0 + n] * ds);
+        }
+        for (int i = tid; i < cb * BNS; i += nth) {
+            const int t = i / BNS, n = i - t * BNS;
+            dOs[i] = t < valid ? a.dO[(tok0 + t) * dv + n0 + n] : 0.f;
+        }
+        for (int i = tid; i < P * BNS; i += nth) {
+            const int u = i / BNS, n = i - u * BNS, t = u / p, e = u - t * p;
+            float x = 0.f;
+            if (t < valid) x = MODE == DPLR_GENERIC ? ldg(Vin, ((tok0 + t) * p + e) * dv + n0 + n) : ldg(vin, (tok0 + t) * dv + n0 + n);
+            Vs[i] = x;
+        }
+        __syncthreads();
+        mm(Hs, BNS, Bt, BD, false, S0s, BNS, false, R, BNS, dk, 1.f, false);
+        mm(dEs, BNS, At, BD, false, dSs, BNS, false, R, BNS, dk, -1.f, false);
+        __syncthreads();
+        mm(Hs, BNS, Gm, BMX, false, Vs, BNS, false, R, BNS, P, 1.f, true);
+        mm(dEs, BNS, QA, BMX, true, dOs, BNS, false, R, BNS, cb, -1.f, true);
+        __syncthreads();
+        mm(Es, BNS, Mm, BMX, false, Hs, BNS, false, R, BNS, R, 1.f, false);
+        mm(dHs, BNS, Mm, BMX, true, dEs, BNS, false, R, BNS, R, 1.f, false);
+        __syncthreads();
+        mm(dAt, BD, Es, BNS, false, dSs, BNS, true, R, dk, BNS, -1.f, true);
+        mm(dBt, BD, dHs, BNS, false, S0s, BNS, true, R, dk, BNS, 1.f, true);
+        mm(dKt, BD, Vs, BNS, false, dSs, BNS, true, P, dk, BNS, 1.f, true);
+        mm(dQt, BD, dOs, BNS, false, S0s, BNS, true, cb, dk, BNS, 1.f, true);
+        mm(dL, BMX, dHs, BNS, false, Es, BNS, true, R, R, BNS, -1.f, true);
+        mm(dG, BMX, dHs, BNS, false, Vs, BNS, true, R, P, BNS, 1.f, true);
+        mm(dQA, BMX, dOs, BNS, false, Es, BNS, true, cb, R, BNS, -1.f, true);
+        mm(dQK, BMX, dOs, BNS, false, Vs, BNS, true, cb, P, BNS, 1.f, true);
+        // dV = K~ dS^ + QK^T dO + G^T dH for this slice, straight to the output
+        for (int idx = tid; idx < P * BNS; idx += nth) {
+            const int u = idx / BNS, n = idx - u * BNS, t = u / p, e = u - t * p;
+            float s = 0.f;
+            for (int c = 0; c < dk; ++c) s = fmaf(Kt[u * BD + c], dSs[c * BNS + n], s);
+            for (int tt = 0; tt < cb; ++tt) s = fmaf(QK[tt * BMX + u], dOs[tt * BNS + n], s);
+            for (int m = 0; m < R; ++m) s = fmaf(Gm[m * BMX + u], dHs[m * BNS + n], s);
+            if (t < valid) {
+                if (MODE == DPLR_GENERIC) a.dV[((tok0 + t) * p + e) * dv + n0 + n] = s;
+                else a.dv[(tok0 + t) * dv + n0 + n] = s;
+            }
+        }
+        __syncthreads();
+    }
+
+    // ---- the remaining terms of the factor gradients
+    mask(dL, BMX, R, R, r, r, true);
+    mask(dG, BMX, R, P, r, p, true);
+    mask(dQA, BMX, cb, R, 1, r, false);
+    mask(dQK, BMX, cb, P, 1, p, false);
+    __syncthreads();
+    mm(dAt, BD, dQA, BMX, true, Qt, BD, false, R, dk, cb, 1.f, true);
+    mm(dBt, BD, dG, BMX, false, Kt, BD, false, R, dk, P, 1.f, true);
+    mm(dKt, BD, dQK, BMX, true, Qt, BD, false, P, dk, cb, 1.f, true);
+    mm(dQt, BD, dQA, BMX, false, At, BD, false, cb, dk, R, 1.f, true);
+    __syncthreads();
+    mm(dAt, BD, dL, BMX, true, Bt, BD, false, R, dk, R, 1.f, true);
+    mm(dBt, BD, dL, BMX, false, At, BD, false, R, dk, R, 1.f, true);
+    mm(dKt, BD, dG, BMX, true, Bt, BD, false, P, dk, R, 1.f, true);
+    mm(dQt, BD, dQK, BMX, false, Kt, BD, false, cb, dk, P, 1.f, true);
+    __syncthreads();
+
+    // ---- the cumulative log-decay's gradient dG_t (over S0s / dSs), then its reverse prefix: d decay
+    float* dGt = S0s;   // [BMX][BD]
+    for (int i = tid; i < cb * dk; i += nth) {
+        const int t = i / dk, c = i - t * dk;
+        float s = Qt[t * BD + c] * dQt[t * BD + c];
+        for (int e = 0; e < r; ++e) s -= At[(t * r + e) * BD + c] * dAt[(t * r + e) * BD + c];
+        for (int e = 0; e < p; ++e) s -= Kt[(t * p + e) * BD + c] * dKt[(t * p + e) * BD + c];
+        if (t + 1 < cb)
+            for (int e = 0; e < r; ++e) s += Bt[((t + 1) * r + e) * BD + c] * dBt[((t + 1) * r + e) * BD + c];
+        else
+            s += sd[c];
+        dGt[t * BD + c] = s;
+    }
+    __syncthreads();
+    for (int c = tid; c < dk; c += nth) {
+        float s = 0.f;
+        for (int t = cb - 1; t >= 0; --t) {
+            s += dGt[t * BD + c];
+            dGt[t * BD + c] = s;
+        }
+    }
+    __syncthreads();
+
+    // ---- unscaled gradients and the mode's factor construction: warp per token, lanes over channels
+    for (int t = warp; t < valid; t += nth / 32) {
+        const size_t tg = tok0 + t;
+        float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f;   // per-token sums over channels
+        for (int c = lane; c < dk; c += 32) {
+            const float G = Gc[t * BD + c], Gx = t > 0 ? Gc[(t - 1) * BD + c] : 0.f, an = va[c];
+            const float er = __expf(an - G), ef = __expf(Gx - an), eq = __expf(G - an);
+            const float dd = dGt[t * BD + c];
+            a.dq[tg * dk + c] = eq * dQt[t * BD + c];
+            if (MODE == DPLR_GENERIC) {
+                a.ddecay[tg * dk + c] = dd;
+                for (int e = 0; e < r; ++e) {
+                    a.dA[(tg * r + e) * dk + c] = er * dAt[(t * r + e) * BD + c];
+                    a.dBm[(tg * r + e) * dk + c] = ef * dBt[(t * r + e) * BD + c];
+                }
+                for (int e = 0; e < p; ++e) a.dK[(tg * p + e) * dk + c] = er * dKt[(t * p + e) * BD + c];
+            } else if (MODE == DPLR_GDN) {
+                const float kk = ldg(kin, tg * dk + c), b = a.beta[tg], eg = __expf(a.decay[tg]);
+                const float dA = er * dAt[t * BD + c], dB = ef * dBt[t * BD + c], dK = er * dKt[t * BD + c];
+                a.dk[tg * dk + c] = eg * b * dA + dB + b * dK;
+                acc0 = fmaf(kk, dA, acc0);   // k . dA
+                acc1 = fmaf(kk, dK, acc1);   // k . dK
+                acc2 += dd;                  // sum of the channels' decay gradients
+            } else {
+                const float kk = ldg(kin, tg * dk + c);
+                const float dB0 = ef * dBt[(2 * t) * BD + c];
+                acc0 = fmaf(kk, dB0, acc0);  // k . dB0 (needed before dk below)
+            }
+        }
+        for (int off = 16; off > 0; off >>= 1) {
+            acc0 += __shfl_xor_sync(0xffffffffu, acc0, off);
+            acc1 += __shfl_xor_sync(0xffffffffu, acc1, off);
+            acc2 += __shfl_xor_sync(0xffffffffu, acc2, off);
+        }
+        if (MODE == DPLR_GDN) {
+            if (lane == 0) {
+                const float b = a.beta[tg], eg = __expf(a.decay[tg]);
+                a.dbeta[tg] = eg * acc0 + acc1;
+                a.ddecay[tg] = eg * b * acc0 + acc2;
+            }
+        } else if (MODE == DPLR_HDLA) {
+            const float b = a.beta[tg], cc = ct[t], kb0 = acc0;
+            float db = 0.f;
+            for (int c = lane; c < dk; c += 32) {
+                const float G = Gc[t * BD + c], Gx = t > 0 ? Gc[(t - 1) * BD + c] : 0.f, an = va[c];
+                const float er = __expf(an - G), ef = __expf(Gx - an);
+                const float kk = ldg(kin, tg * dk + c), lam = __expf(a.decay[tg * dk + c]);
+                const float dA0 = er * dAt[(2 * t) * BD + c], dA1 = er * dAt[(2 * t + 1) * BD + c];
+                const float dB0 = ef * dBt[(2 * t) * BD + c], dB1 = ef * dBt[(2 * t + 1) * BD + c];
+                const float dK = er * dKt[t * BD + c];
+                a.dk[tg * dk + c] = dA0 + lam * dA1 + (b * lam - b * b * cc) * dB0 - 2.f * b * b * lam * kk * kb0 +
+                                    b * dB1 + b * dK;
+                const float dlam = kk * dA1 + b * kk * dB0 - b * b * kk * kk * kb0;
+                a.ddecay[tg * dk + c] = dGt[t * BD + c] + lam * dlam;
+                db = fmaf(lam * kk, dB0, db);
+                db = fmaf(kk, dB1 + dK, db);
+            }
+            for (int off = 16; off > 0; off >>= 1) db += __shfl_xor_sync(0xffffffffu, db, off);
+            if (lane == 0) a.dbeta[tg] = db - 2.f * b * cc * kb0;
+        }
+    }
+}
+
+size_t bwd_smem_bytes() {
+    return sizeof(float) * (size_t)(8 * BMX * BD + 8 * BMX * BMX + 2 * BD * BNS + 6 * BMX * BNS + BMX * BD + 2 * BD + BMX);
+}
+
+// ---- pass 2: the block-boundary state gradients, per (head, 16 state columns), blocks in reverse order
+constexpr int CBV = 16;
+
+__global__ void __launch_bounds__(256)
+chain_bwd_kernel(Plan pl, const float* Pm, const float* Qm, const float* dO, const float* dST, float* dSb,
+                 float* dS0) {
+    extern __shared__ __align__(16) float sm[];
+    const int dk = pl.dk, dv = pl.dv, cw = pl.cw, nb = pl.nb, T = pl.T;
+    const int ncb = dv / CBV;
+    const size_t bh = blockIdx.x / ncb;
+    const int n0 = (blockIdx.x % ncb) * CBV;
+    const int tid = threadIdx.x, nth = blockDim.x;
+    float* dS = sm;                     // [dk][CBV]
+    float* Ps = dS + dk * CBV;          // [dk][dk + 1]
+    float* Qs = Ps + dk * (dk + 1);     // [cw][dk]
+    float* Os = Qs + cw * dk;           // [cw][CBV]
+    for (int i = tid; i < dk * CBV; i += nth) {
+        const int c = i / CBV, n = i - c * CBV;
+        dS[i] = dST ? dST[(bh * dk + c) * dv + n0 + n] : 0.f;
+    }
+    for (int j = nb - 1; j >= 0; --j) {
+        __syncthreads();   // dS complete
+        float* dst = dSb + (bh * (size_t)nb + j) * (size_t)dk * dv + n0;   // gradient of the state after block j
+        for (int i = tid; i < dk * CBV; i += nth) dst[(size_t)(i / CBV) * dv + i % CBV] = dS[i];
+        const float* P = Pm + (bh * (size_t)nb + j) * (size_t)dk * dk;
+        const float* Q = Qm + (bh * (size_t)nb + j) * (size_t)cw * dk;
+        for (int i = tid; i < dk * dk; i += nth) Ps[(i / dk) * (dk + 1) + i % dk] = P[i];
+        for (int i = tid; i < cw * dk; i += nth) Qs[i] = Q[i];
+        for (int i = tid; i < cw * CBV; i += nth) {
+            const int t = i / CBV, n = i - t * CBV, tg = j * cw + t;
+            Os[i] = tg < T ? dO[(bh * (size_t)T + tg) * dv + n0 + n] : 0.f;
+        }
+        __syncthreads();
+        // dS_{j-1} = P_j^T dS_j + Q'_j^T dO_j
+        float acc[(128 * CBV + 255) / 256];
+        int m = 0;
+        for (int idx = tid; idx < dk * CBV; idx += nth, ++m) {
+            const int i = idx / CBV, n = idx - i * CBV;
+            float s = 0.f;
+            for (int c = 0; c < dk; ++c) s = fmaf(Ps[c * (dk + 1) + i], dS[c * CBV + n], s);
+            for (int t = 0; t < cw; ++t) s = fmaf(Qs[t * dk + i], Os[t * CBV + n], s);
+            acc[m] = s;
+        }
+        __syncthreads();
+        m = 0;
+        for (int idx = tid; idx < dk * CBV; idx += nth, ++m) dS[idx] = acc[m];
+    }
+    __syncthreads();
+    if (dS0)
+        for (int i = tid; i < dk * CBV; i += nth) {
+            const int c = i / CBV, n = i - c * CBV;
+            dS0[(bh * dk + c) * dv + n0 + n] = dS[i];
+        }
+}
+
+size_t chain_bwd_smem_bytes(const Plan& pl) {
+    return sizeof(float) * (size_t)(pl.dk * CBV + pl.dk * (pl.dk + 1) + pl.cw * pl.dk + pl.cw * CBV);
+}
+
+constexpr size_t kBwdAlign = 256;
+size_t bround(size_t x) { return (x + kBwdAlign - 1) / kBwdAlign * kBwdAlign; }
+
+// The backward's plan: the fp32 two-stage layout at WY blocks of cb tokens, and its workspace after the forward's
+// maps: scratch o, S_T, the checkpoints and the boundary gradients.
+struct BwdPlan {
+    Plan pl;
+    size_t off_o, off_ST, off_Sb, off_dSb, total;
+};
+
+dplr_status make_bwd_plan(const dplr_desc* d, BwdPlan* bp) {
+    Plan p;
+    dplr_status st = make_plan(d, &p);
+    if (st != DPLR_OK) return st;
+    if (p.dk > BD || p.dv > BD || p.dv % CBV != 0) return DPLR_ERR_UNSUPPORTED;
+    const int rg = p.mode == DPLR_GENERIC ? p.r : (p.mode == DPLR_GDN ? 1 : 2);
+    const int pg = p.mode == DPLR_GENERIC ? p.p : 1;
+    const int m = std::max(rg, std::max(pg, 1));
+    if (m > BMX) return DPLR_ERR_UNSUPPORTED;
+    p.fused = p.tc = p.gtc = 0;
+    // a power of two: the fp32 chunk-map kernel reads float4 rows, so its block dimensions (cw, cw r, cw p) must be
+    // multiples of 4, as the forward's WY blocks always are
+    int cb = BMX;
+    while (cb > 4 && cb * m > BMX) cb /= 2;
+    if (cb * m > BMX) return DPLR_ERR_UNSUPPORTED;
+    p.cw = cb;
+    p.nb = (p.T + p.cw - 1) / p.cw;
+    const size_t units = (size_t)p.BH * p.nb;
+    size_t off = kBwdAlign;   // the first 256 bytes hold the device status word
+    p.off_P = off; off = bround(off + units * (size_t)p.dk * p.dk * sizeof(float));
+    p.off_c = off; off = bround(off + units * (size_t)p.dk * p.dv * sizeof(float));
+    p.off_Q = off; off = bround(off + units * (size_t)p.cw * p.dk * sizeof(float));
+    p.ws_stages = off;
+    if (prep_smem_bytes(p) > 227 * 1024 || scan_smem_bytes(p) > 227 * 1024) return DPLR_ERR_UNSUPPORTED;
+    bp->off_o = off; off = bround(off + (size_t)p.BH * p.T * p.dv * sizeof(float));
+    bp->off_ST = off; off = bround(off + (size_t)p.BH * p.dk * p.dv * sizeof(float));
+    bp->off_Sb = off; off = bround(off + units * (size_t)p.dk * p.dv * sizeof(float));
+    bp->off_dSb = off; off = bround(off + units * (size_t)p.dk * p.dv * sizeof(float));
+    bp->total = off;
+    p.ws_bytes = off;
+    bp->pl = p;
+    return DPLR_OK;
+}
+
+std::atomic<uint64_t> g_bwd_smem[6] = {{0}, {0}, {0}, {0}, {0}, {0}};
+std::atomic<uint64_t> g_chain_bwd_smem{0};
+
+template <int MODE, class IT>
+cudaError_t launch_block_bwd(const Plan& pl, const BwdArgs& a, cudaStream_t s, int slot) {
+    const size_t smem = bwd_smem_bytes();
+    cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(block_bwd_kernel<MODE, IT>), (int)smem, g_bwd_smem[slot]);
+    if (e != cudaSuccess) return e;
+    block_bwd_kernel<MODE, IT><<<(unsigned)((size_t)pl.BH * pl.nb), BT, smem, s>>>(pl, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace dplr
+
+using namespace dplr;
+
+extern "C" size_t dplr_la_backward_workspace_size(const dplr_desc* desc) {
+    BwdPlan bp;
+    if (make_bwd_plan(desc, &bp) != DPLR_OK) return 0;
+    return bp.total;
+}
+
+extern "C" dplr_status dplr_la_backward(const dplr_desc* desc, const void* q, const void* k, const void* v,
+                                        const float* decay, const float* beta, const void* A, const void* Bm,
+                                        const void* K, const void* V, const float* S0, const float* dO,
+                                        const float* dST, float* dq, float* dk, float* dv, float* ddecay,
+                                        float* dbeta, float* dA, float* dBm, float* dK, float* dV, float* dS0,
+                                        void* workspace, size_t ws_bytes, void* stream) {
+    BwdPlan bp;
+    dplr_status st = make_bwd_plan(desc, &bp);
+    if (st != DPLR_OK) return st;
+    const Plan& pl = bp.pl;
+    auto al = [](const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    if (!al(q) || !al(k) || !al(v) || !al(decay) || !al(beta) || !al(A) || !al(Bm) || !al(K) || !al(V) || !al(S0) ||
+        !al(dO) || !al(dST) || !al(dq) || !al(dk) || !al(dv) || !al(ddecay) || !al(dbeta) || !al(dA) || !al(dBm) ||
+        !al(dK) || !al(dV) || !al(dS0))
+        return DPLR_ERR_INVALID_ARG;
+    if (pl.T > 0) {
+        if (!q || !decay || !dO || !dq || !ddecay) return DPLR_ERR_INVALID_ARG;
+        if (pl.mode == DPLR_GENERIC) {
+            if (!A || !Bm || !dA || !dBm) return DPLR_ERR_INVALID_ARG;
+            if (pl.p > 0 && (!K || !V || !dK || !dV)) return DPLR_ERR_INVALID_ARG;
+        } else if (!k || !v || !beta || !dk || !dv || !dbeta) {
+            return DPLR_ERR_INVALID_ARG;
+        }
+    }
+    if (!workspace || ws_bytes < bp.total || (reinterpret_cast<uintptr_t>(workspace) % kBwdAlign) != 0)
+        return DPLR_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* ws = static_cast<char*>(workspace);
+    float* o_scratch = reinterpret_cast<float*>(ws + bp.off_o);
+    float* ST = reinterpret_cast<float*>(ws + bp.off_ST);
+    float* Sb = reinterpret_cast<float*>(ws + bp.off_Sb);
+    float* dSb = reinterpret_cast<float*>(ws + bp.off_dSb);
+    if (pl.T == 0) {   // no tokens: the initial state's gradient is dS_T
+        if (dS0) {
+            const size_t bytes = (size_t)pl.BH * pl.dk * pl.dv * sizeof(float);
+            if ((dST ? cudaMemcpyAsync(dS0, dST, bytes, cudaMemcpyDeviceToDevice, s) : cudaMemsetAsync(dS0, 0, bytes, s)) !=
+                cudaSuccess)
+                return DPLR_ERR_CUDA;
+        }
+        return DPLR_OK;
+    }
+    // pass 1: the forward at blocks of cb tokens, with the state before every block
+    ChunkMapArgs ma;
+    ma.q = q; ma.k = k; ma.v = v; ma.decay = decay; ma.beta = beta;
+    ma.A = A; ma.Bm = Bm; ma.K = K; ma.V = V; ma.o = o_scratch;
+    ma.Pm = reinterpret_cast<float*>(ws + pl.off_P);
+    ma.Cm = reinterpret_cast<float*>(ws + pl.off_c);
+    ma.Qm = reinterpret_cast<float*>(ws + pl.off_Q);
+    if (launch_chunk_maps(pl, ma, s) != cudaSuccess) return DPLR_ERR_CUDA;
+    ScanArgs sa;
+    sa.S0 = S0; sa.o = o_scratch; sa.ST = ST;
+    sa.Pm = ma.Pm; sa.Cm = ma.Cm; sa.Qm = ma.Qm; sa.Sb = Sb;
+    if (launch_state_scan(pl, sa, s) != cudaSuccess) return DPLR_ERR_CUDA;
+    // pass 2: the boundary state gradients
+    {
+        const size_t smem = chain_bwd_smem_bytes(pl);
+        if (set_smem_limit_once(reinterpret_cast<const void*>(chain_bwd_kernel), 227 * 1024, g_chain_bwd_smem) != cudaSuccess)
+            return DPLR_ERR_CUDA;
+        chain_bwd_kernel<<<(unsigned)((size_t)pl.BH * (pl.dv / CBV)), 256, smem, s>>>(pl, ma.Pm, ma.Qm, dO, dST, dSb, dS0);
+        if (cudaGetLastError() != cudaSuccess) return DPLR_ERR_CUDA;
+    }
+    // pass 3: every block's input gradients
+    BwdArgs ba;
+    ba.q = q; ba.k = k; ba.v = v; ba.decay = decay; ba.beta = beta; ba.A = A; ba.Bm = Bm; ba.K = K; ba.V = V;
+    ba.dO = dO; ba.Sb = Sb; ba.dSb = dSb; ba.ST = ST;
+    ba.dq = dq; ba.dk = dk; ba.dv = dv; ba.ddecay = ddecay; ba.dbeta = dbeta; ba.dA = dA; ba.dBm = dBm; ba.dK = dK; ba.dV = dV;
+    cudaError_t e;
+    if (pl.bf16) {
+        e = pl.mode == DPLR_GDN    ? launch_block_bwd<DPLR_GDN, __nv_bfloat16>(pl, ba, s, 0)
+            : pl.mode == DPLR_HDLA ? launch_block_bwd<DPLR_HDLA, __nv_bfloat16>(pl, ba, s, 1)
+                                   : launch_block_bwd<DPLR_GENERIC, __nv_bfloat16>(pl, ba, s, 2);
+    } else {
+        e = pl.mode == DPLR_GDN    ? launch_block_bwd<DPLR_GDN, float>(pl, ba, s, 3)
+            : pl.mode == DPLR_HDLA ? launch_block_bwd<DPLR_HDLA, float>(pl, ba, s, 4)
+                                   : launch_block_bwd<DPLR_GENERIC, float>(pl, ba, s, 5);
+    }
+    return e == cudaSuccess ? DPLR_OK : DPLR_ERR_CUDA;
+}

@@ -48,6 +48,7 @@ struct ChunkMapArgs {
 struct ScanArgs {
     const float* S0; float* o; float* ST;
     const float* Pm; const float* Cm; const float* Qm;
+    float* Sb = nullptr;   // optional [BH, nb, dk, dv]: the state before each WY block (the backward's checkpoints)
 };
 
 dplr_status make_plan(const dplr_desc* d, Plan* plan);

@@ -112,6 +112,10 @@ state_scan_kernel(Plan pl, ScanArgs args) {
             cp_async_wait<0>();
         }
         __syncthreads();   // chunk j's maps (every thread's copies) and S_{j-1} in place
+        if (args.Sb) {     // the state before chunk j, for the backward
+            float* dst = args.Sb + (bh * (size_t)pl.nb + j) * (size_t)dk * dv + n0;
+            for (int i = tid; i < dk * nv; i += nth) dst[(size_t)(i / nv) * dv + i % nv] = S[i];
+        }
         const float* Pj = sm + Ly.P(b);
         const float* Qj = sm + Ly.Q(b);
         const float* cj = sm + Ly.C(b);

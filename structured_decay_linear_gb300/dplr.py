@@ -69,6 +69,10 @@ def library() -> ctypes.CDLL:
             lib.dplr_la_forward_noalloc.argtypes = [dp] + [_vp] * 12 + [_vp]
             lib.dplr_la_decode_step.restype = ctypes.c_int
             lib.dplr_la_decode_step.argtypes = [dp] + [_vp] * 11 + [_vp]
+            lib.dplr_la_backward_workspace_size.restype = ctypes.c_size_t
+            lib.dplr_la_backward_workspace_size.argtypes = [dp]
+            lib.dplr_la_backward.restype = ctypes.c_int
+            lib.dplr_la_backward.argtypes = [dp] + [_vp] * 22 + [_vp, ctypes.c_size_t, _vp]
             lib.dplr_la_path.restype = ctypes.c_char_p
             lib.dplr_la_path.argtypes = [dp]
             lib.dplr_la_set_wait_limit.restype = None
@@ -129,6 +133,17 @@ def dplr_la_kernel_count(desc: dplr_desc) -> int:
 def dplr_la_decode_step(desc, q, k, v, decay, beta, A, Bm, K, V, S, o, stream) -> int:
     """One recurrent step (desc.T == 1): S updated in place, o = S^T q."""
     return int(library().dplr_la_decode_step(ctypes.byref(desc), q, k, v, decay, beta, A, Bm, K, V, S, o, stream))
+
+
+def dplr_la_backward_workspace_size(desc: dplr_desc) -> int:
+    return int(library().dplr_la_backward_workspace_size(ctypes.byref(desc)))
+
+
+def dplr_la_backward(desc, q, k, v, decay, beta, A, Bm, K, V, S0, dO, dST, dq, dk, dv, ddecay, dbeta, dA, dBm, dK,
+                     dV, dS0, workspace, ws_bytes, stream) -> int:
+    """Gradients of every input given dO and dS_T (device pointers; see include/dplr.h)."""
+    return int(library().dplr_la_backward(ctypes.byref(desc), q, k, v, decay, beta, A, Bm, K, V, S0, dO, dST, dq, dk,
+                                          dv, ddecay, dbeta, dA, dBm, dK, dV, dS0, workspace, ws_bytes, stream))
 
 
 def dplr_la_path(desc: dplr_desc) -> str:
@@ -384,3 +399,45 @@ class Decode:
         if st != DPLR_OK:
             raise DplrError(st, "dplr_la_decode_step")
         return self.o
+
+
+class Backward:
+    """Prepared backward for one descriptor (dplr_la_backward): owns the workspace and the fp32 gradients."""
+
+    def __init__(self, mode: str, in_dtype: torch.dtype, B: int, H: int, T: int, dk: int, dv: int,
+                 r_ab: Optional[int] = None, r_kv: Optional[int] = None, chunk: int = 64,
+                 device: Optional[torch.device] = None):
+        self.mode = mode
+        self.desc = make_desc(mode, in_dtype, B, H, T, dk, dv, r_ab, r_kv, chunk)
+        self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        nbytes = dplr_la_backward_workspace_size(self.desc)
+        if nbytes == 0:
+            raise DplrError(dplr_la_check(self.desc) or 2, "dplr_la_backward_workspace_size")
+        self.ws = torch.empty(nbytes + 256, dtype=torch.uint8, device=self.device)
+        off = (-self.ws.data_ptr()) % 256
+        self.ws_ptr, self.ws_bytes = self.ws.data_ptr() + off, nbytes
+        r, p = self.desc.r_ab, self.desc.r_kv
+        f = lambda *shape: torch.zeros(shape, dtype=torch.float32, device=self.device)
+        g = {"q": f(B, H, T, dk), "S0": f(B, H, dk, dv)}
+        if mode == "generic":
+            g.update(decay=f(B, H, T, dk), A=f(B, H, T, r, dk), Bm=f(B, H, T, r, dk))
+            if p > 0:
+                g.update(K=f(B, H, T, p, dk), V=f(B, H, T, p, dv))
+        else:
+            g.update(k=f(B, H, T, dk), v=f(B, H, T, dv), beta=f(B, H, T),
+                     decay=f(B, H, T) if mode == "gdn" else f(B, H, T, dk))
+        self.grads = g
+
+    def __call__(self, dO, dST=None, q=None, k=None, v=None, decay=None, beta=None, A=None, Bm=None, K=None,
+                 V=None, S0=None, stream: Optional[torch.cuda.Stream] = None) -> dict:
+        """Gradients of the forward's inputs (dict of fp32 tensors, also kept in .grads)."""
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        g = self.grads
+        st = dplr_la_backward(self.desc, _ptr(q), _ptr(k), _ptr(v), _ptr(decay), _ptr(beta), _ptr(A), _ptr(Bm),
+                              _ptr(K), _ptr(V), _ptr(S0), _ptr(dO), _ptr(dST), _ptr(g["q"]), _ptr(g.get("k")),
+                              _ptr(g.get("v")), _ptr(g["decay"]), _ptr(g.get("beta")), _ptr(g.get("A")),
+                              _ptr(g.get("Bm")), _ptr(g.get("K")), _ptr(g.get("V")), _ptr(g["S0"]), self.ws_ptr,
+                              self.ws_bytes, s.cuda_stream)
+        if st != DPLR_OK:
+            raise DplrError(st, "dplr_la_backward")
+        return g
