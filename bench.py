@@ -17,6 +17,7 @@ from __future__ import annotations
 
 import argparse
 import csv
+import dataclasses
 import hashlib
 import io
 import json
@@ -555,6 +556,61 @@ def dataclasses_replace(w, **kw):
     return dataclasses.replace(w, **kw)
 
 
+def run_backward(args):
+    """Time of dplr_la_backward (the gradients of every input given dO and dS_T) on a workload at full size, with
+    the same recipe as the forward and random upstream gradients. Reports ms per backward and tokens/s, and the
+    algorithmic bytes per backward: the forward's inputs and S0 read, dO and dS_T read, every gradient written
+    once in fp32 (not a benchmark line; the JSON carries "mode": "backward")."""
+    import torch
+    import structured_decay_linear_gb300 as sdl
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = workloads.WORKLOADS[args.workload]
+    if args.seq_len:
+        w = dataclasses.replace(w, T=args.seq_len)
+    inp = workloads.generate(w)
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    t = {}
+    for k in ("q", "k", "v", "A", "Bm", "K", "V"):
+        t[k] = None if inp[k] is None else torch.from_numpy(np.ascontiguousarray(inp[k])).to(dev).to(dt)
+    for k in ("decay", "beta", "S0"):
+        t[k] = None if inp[k] is None else torch.from_numpy(np.ascontiguousarray(inp[k])).to(dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    dO = torch.randn((w.B, w.H, w.T, w.dv), device=dev, generator=g)
+    dST = torch.randn((w.B, w.H, w.dk, w.dv), device=dev, generator=g)
+    bw = sdl.Backward(w.mode, dt, w.B, w.H, w.T, w.dk, w.dv, w.r_ab if w.mode == "generic" else None,
+                      w.r_kv if w.mode == "generic" else None, device=dev)
+    call = lambda: bw(dO=dO, dST=dST, **t)
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        call()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / K
+    tokens = w.B * w.H * w.T
+    esz = 2 if w.dtype == "bf16" else 4
+    if w.mode == "generic":
+        per_tok = (w.dk + 2 * w.r_ab * w.dk + w.r_kv * (w.dk + w.dv)) * (esz + 4) + w.dk * 8 + w.dv * 4
+    else:
+        dec = 1 if w.mode == "gdn" else w.dk
+        per_tok = (2 * w.dk + w.dv) * (esz + 4) + 2 * (dec + 1) * 4 + w.dv * 4
+    nbytes = tokens * per_tok + w.B * w.H * w.dk * w.dv * 4 * 3
+    peaks, peak_kind = load_peaks()
+    finite = all(bool(torch.isfinite(x).all().item()) for x in bw.grads.values())
+    print(json.dumps({"mode": "backward", "workload": w.name, "steps": K, "ms_per_backward": ms,
+                      "tokens_per_s": tokens / (ms * 1e-3), "bytes_per_backward": nbytes,
+                      "achieved_gbs": nbytes / (ms * 1e-3) / 1e9, "frac_of_hbm_peak": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                      "peak": f"{peak_kind} hbm_gbs {peaks['hbm_gbs']}", "workspace_bytes": bw.ws_bytes,
+                      "gradients_finite": finite, "arithmetic": "f32 (CUDA cores)"}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -563,6 +619,8 @@ def main():
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--backward", action="store_true",
+                    help="time dplr_la_backward on the workload (not a benchmark line)")
     ap.add_argument("--decode", action="store_true",
                     help="time the one-token decode step (not a benchmark line)")
     ap.add_argument("--host-overhead", action="store_true",
@@ -572,6 +630,9 @@ def main():
     args = ap.parse_args()
     if args.host_overhead:
         run_host_overhead(args)
+        return
+    if args.backward:
+        run_backward(args)
         return
     if args.decode:
         run_decode(args)

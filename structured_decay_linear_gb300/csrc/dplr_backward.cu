@@ -39,6 +39,12 @@ constexpr int BT = 256;      // threads of the block-backward kernel
 constexpr int BMX = 32;      // rows of A~ (R = cb r), K~ (P = cb p) and Q~ (cb) at most
 constexpr int BNS = 16;      // state columns per slice
 constexpr int BD = 128;      // dk, dv at most
+// Row strides in shared memory, odd so that a warp reading a column (the transposed operand of a product) touches
+// 32 different banks.
+constexpr int LD = BD + 1;   // [*][dk] rows
+constexpr int LM = BMX + 1;  // [*][R] rows
+constexpr int LS = BNS + 1;  // [*][slice] rows
+static_assert(2 * BD * LS >= BMX * LD, "the decay-gradient table fits the two slice buffers");
 
 template <class T> __device__ __forceinline__ float ldg(const T* p, size_t i);
 template <> __device__ __forceinline__ float ldg<float>(const float* p, size_t i) { return p[i]; }
@@ -54,15 +60,37 @@ struct BwdArgs {
 };
 
 // C[m][n] (=, +=) alpha sum_k A(m, k) B(k, n) over the CTA's threads, with A(m, k) = A[m lda + k] (ta: A[k lda + m])
-// and B(k, n) = B[k ldb + n] (tb: B[n ldb + k]); all in shared memory.
+// and B(k, n) = B[k ldb + n] (tb: B[n ldb + k]); all in shared memory. M and N are multiples of 4: each thread takes
+// 4 x 4 tiles of C (8 shared loads per 16 FMAs).
 __device__ __forceinline__ void mm(float* C, int ldc, const float* A, int lda, bool ta, const float* B, int ldb,
                                    bool tb, int M, int N, int K, float alpha, bool acc) {
-    for (int idx = threadIdx.x; idx < M * N; idx += blockDim.x) {
-        const int m = idx / N, n = idx - m * N;
-        float s = 0.f;
-        for (int k = 0; k < K; ++k)
-            s = fmaf(ta ? A[k * lda + m] : A[m * lda + k], tb ? B[n * ldb + k] : B[k * ldb + n], s);
-        C[m * ldc + n] = acc ? C[m * ldc + n] + alpha * s : alpha * s;
+    const int nt = N >> 2, tiles = (M >> 2) * nt;
+    const int as = ta ? 1 : lda, ak = ta ? lda : 1;   // A(m, k) = A[m as + k ak]
+    const int bs = tb ? ldb : 1, bk = tb ? 1 : ldb;   // B(k, n) = B[k bk + n bs]
+    for (int tile = threadIdx.x; tile < tiles; tile += blockDim.x) {
+        const int m0 = (tile / nt) << 2, n0 = (tile % nt) << 2;
+        float c[4][4] = {};
+        const float* Ap = A + m0 * as;
+        const float* Bp = B + n0 * bs;
+        for (int k = 0; k < K; ++k) {
+            float a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                a[i] = Ap[i * as + k * ak];
+                b[i] = Bp[i * bs + k * bk];
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) c[i][jj] = fmaf(a[i], b[jj], c[i][jj]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                float* o = C + (m0 + i) * ldc + n0 + jj;
+                *o = acc ? *o + alpha * c[i][jj] : alpha * c[i][jj];
+            }
     }
 }
 
@@ -79,32 +107,32 @@ template <int MODE, class IT>
 __global__ void __launch_bounds__(BT)
 block_bwd_kernel(Plan pl, BwdArgs a) {
     extern __shared__ __align__(16) float sm[];
-    float* At = sm;                 // [BMX][BD] scaled factors
-    float* Bt = At + BMX * BD;
-    float* Kt = Bt + BMX * BD;
-    float* Qt = Kt + BMX * BD;
-    float* dAt = Qt + BMX * BD;     // their gradients
-    float* dBt = dAt + BMX * BD;
-    float* dKt = dBt + BMX * BD;
-    float* dQt = dKt + BMX * BD;
-    float* Mm = dQt + BMX * BD;     // [BMX][BMX] L, then M
-    float* Gm = Mm + BMX * BMX;
-    float* QA = Gm + BMX * BMX;
-    float* QK = QA + BMX * BMX;
-    float* dL = QK + BMX * BMX;
-    float* dG = dL + BMX * BMX;
-    float* dQA = dG + BMX * BMX;
-    float* dQK = dQA + BMX * BMX;
-    float* S0s = dQK + BMX * BMX;   // [BD][BNS] slice of e^a S_{j-1}; with dSs also the dG_t / d decay table later
-    float* dSs = S0s + BD * BNS;    // [BD][BNS] slice of e^a dS_j
-    float* dOs = dSs + BD * BNS;    // [BMX][BNS]
-    float* Vs = dOs + BMX * BNS;
-    float* Hs = Vs + BMX * BNS;
-    float* Es = Hs + BMX * BNS;
-    float* dEs = Es + BMX * BNS;
-    float* dHs = dEs + BMX * BNS;
-    float* Gc = dHs + BMX * BNS;    // [BMX][BD] inclusive cumulative log-decay G_t
-    float* va = Gc + BMX * BD;      // [BD] anchor a
+    float* At = sm;                 // [BMX][LD] scaled factors
+    float* Bt = At + BMX * LD;
+    float* Kt = Bt + BMX * LD;
+    float* Qt = Kt + BMX * LD;
+    float* dAt = Qt + BMX * LD;     // their gradients
+    float* dBt = dAt + BMX * LD;
+    float* dKt = dBt + BMX * LD;
+    float* dQt = dKt + BMX * LD;
+    float* Mm = dQt + BMX * LD;     // [BMX][LM] L, then M
+    float* Gm = Mm + BMX * LM;
+    float* QA = Gm + BMX * LM;
+    float* QK = QA + BMX * LM;
+    float* dL = QK + BMX * LM;
+    float* dG = dL + BMX * LM;
+    float* dQA = dG + BMX * LM;
+    float* dQK = dQA + BMX * LM;
+    float* S0s = dQK + BMX * LM;   // [BD][LS] slice of e^a S_{j-1}; with dSs also the dG_t / d decay table later
+    float* dSs = S0s + BD * LS;    // [BD][LS] slice of e^a dS_j
+    float* dOs = dSs + BD * LS;    // [BMX][LS]
+    float* Vs = dOs + BMX * LS;
+    float* Hs = Vs + BMX * LS;
+    float* Es = Hs + BMX * LS;
+    float* dEs = Es + BMX * LS;
+    float* dHs = dEs + BMX * LS;
+    float* Gc = dHs + BMX * LS;    // [BMX][LD] inclusive cumulative log-decay G_t
+    float* va = Gc + BMX * LD;      // [BD] anchor a
     float* sd = va + BD;            // [BD] sum_n S_j dS_j per row
     float* ct = sd + BD;            // [BMX] HDLA: k^T Lambda k per token
 
@@ -130,7 +158,7 @@ block_bwd_kernel(Plan pl, BwdArgs a) {
         const int t = i / dk, c = i - t * dk;
         float d = 0.f;
         if (t < valid) d = MODE == DPLR_GDN ? a.decay[tok0 + t] : a.decay[(tok0 + t) * dk + c];
-        Gc[t * BD + c] = d;
+        Gc[t * LD + c] = d;
     }
     if (MODE == DPLR_HDLA)
         for (int t = tid; t < cb; t += nth) ct[t] = 0.f;
@@ -138,8 +166,8 @@ block_bwd_kernel(Plan pl, BwdArgs a) {
     for (int c = tid; c < dk; c += nth) {
         float g = 0.f;
         for (int t = 0; t < cb; ++t) {
-            g += Gc[t * BD + c];
-            Gc[t * BD + c] = g;
+            g += Gc[t * LD + c];
+            Gc[t * LD + c] = g;
         }
         va[c] = 0.5f * g;
     }
@@ -159,58 +187,58 @@ block_bwd_kernel(Plan pl, BwdArgs a) {
     // ---- the decay-scaled generic-form factors of the block's tokens
     for (int i = tid; i < cb * dk; i += nth) {
         const int t = i / dk, c = i - t * dk;
-        const float G = Gc[t * BD + c], Gx = t > 0 ? Gc[(t - 1) * BD + c] : 0.f, an = va[c];
+        const float G = Gc[t * LD + c], Gx = t > 0 ? Gc[(t - 1) * LD + c] : 0.f, an = va[c];
         const float er = __expf(an - G), ef = __expf(Gx - an), eq = __expf(G - an);
         const bool ok = t < valid;
         const size_t tg = tok0 + t;
-        Qt[t * BD + c] = ok ? eq * ldg(q, tg * dk + c) : 0.f;
+        Qt[t * LD + c] = ok ? eq * ldg(q, tg * dk + c) : 0.f;
         if (MODE == DPLR_GENERIC) {
             for (int e = 0; e < r; ++e) {
-                At[(t * r + e) * BD + c] = ok ? er * ldg(Ain, (tg * r + e) * dk + c) : 0.f;
-                Bt[(t * r + e) * BD + c] = ok ? ef * ldg(Bin, (tg * r + e) * dk + c) : 0.f;
+                At[(t * r + e) * LD + c] = ok ? er * ldg(Ain, (tg * r + e) * dk + c) : 0.f;
+                Bt[(t * r + e) * LD + c] = ok ? ef * ldg(Bin, (tg * r + e) * dk + c) : 0.f;
             }
-            for (int e = 0; e < p; ++e) Kt[(t * p + e) * BD + c] = ok ? er * ldg(Kin, (tg * p + e) * dk + c) : 0.f;
+            for (int e = 0; e < p; ++e) Kt[(t * p + e) * LD + c] = ok ? er * ldg(Kin, (tg * p + e) * dk + c) : 0.f;
         } else {
             const float kk = ok ? ldg(kin, tg * dk + c) : 0.f, b = ok ? a.beta[tg] : 0.f;
             if (MODE == DPLR_GDN) {
                 const float eg = ok ? __expf(a.decay[tg]) : 1.f;
-                At[t * BD + c] = er * eg * b * kk;
-                Bt[t * BD + c] = ef * kk;
+                At[t * LD + c] = er * eg * b * kk;
+                Bt[t * LD + c] = ef * kk;
             } else {
                 const float lam = ok ? __expf(a.decay[tg * dk + c]) : 1.f;
-                At[(2 * t) * BD + c] = er * kk;
-                At[(2 * t + 1) * BD + c] = er * lam * kk;
-                Bt[(2 * t) * BD + c] = ef * (b * lam * kk - b * b * ct[t] * kk);
-                Bt[(2 * t + 1) * BD + c] = ef * b * kk;
+                At[(2 * t) * LD + c] = er * kk;
+                At[(2 * t + 1) * LD + c] = er * lam * kk;
+                Bt[(2 * t) * LD + c] = ef * (b * lam * kk - b * b * ct[t] * kk);
+                Bt[(2 * t + 1) * LD + c] = ef * b * kk;
             }
-            Kt[t * BD + c] = er * b * kk;
+            Kt[t * LD + c] = er * b * kk;
         }
     }
     __syncthreads();
 
     // ---- Gram blocks and the WY inverse M = (I + L)^{-1} (forward substitution, one column per thread)
-    mm(Mm, BMX, Bt, BD, false, At, BD, true, R, R, dk, 1.f, false);
-    mm(Gm, BMX, Bt, BD, false, Kt, BD, true, R, P, dk, 1.f, false);
-    mm(QA, BMX, Qt, BD, false, At, BD, true, cb, R, dk, 1.f, false);
-    mm(QK, BMX, Qt, BD, false, Kt, BD, true, cb, P, dk, 1.f, false);
+    mm(Mm, LM, Bt, LD, false, At, LD, true, R, R, dk, 1.f, false);
+    mm(Gm, LM, Bt, LD, false, Kt, LD, true, R, P, dk, 1.f, false);
+    mm(QA, LM, Qt, LD, false, At, LD, true, cb, R, dk, 1.f, false);
+    mm(QK, LM, Qt, LD, false, Kt, LD, true, cb, P, dk, 1.f, false);
     __syncthreads();
-    mask(Mm, BMX, R, R, r, r, true);
-    mask(Gm, BMX, R, P, r, p, true);
-    mask(QA, BMX, cb, R, 1, r, false);
-    mask(QK, BMX, cb, P, 1, p, false);
+    mask(Mm, LM, R, R, r, r, true);
+    mask(Gm, LM, R, P, r, p, true);
+    mask(QA, LM, cb, R, 1, r, false);
+    mask(QK, LM, cb, P, 1, p, false);
     __syncthreads();
     if (tid < R) {   // column tid of M into dL (scratch), then back over L
         const int col = tid;
         for (int i = 0; i < R; ++i) {
             float s = i == col ? 1.f : 0.f;
-            for (int kx = 0; kx < i; ++kx) s = fmaf(-Mm[i * BMX + kx], dL[kx * BMX + col], s);
-            dL[i * BMX + col] = s;
+            for (int kx = 0; kx < i; ++kx) s = fmaf(-Mm[i * LM + kx], dL[kx * LM + col], s);
+            dL[i * LM + col] = s;
         }
     }
     __syncthreads();
-    for (int i = tid; i < R * BMX; i += nth) Mm[i] = dL[i];
-    for (int i = tid; i < BMX * BD; i += nth) dAt[i] = dBt[i] = dKt[i] = dQt[i] = 0.f;
-    for (int i = tid; i < BMX * BMX; i += nth) dL[i] = dG[i] = dQA[i] = dQK[i] = 0.f;
+    for (int i = tid; i < R * LM; i += nth) Mm[i] = dL[i];
+    for (int i = tid; i < BMX * LD; i += nth) dAt[i] = dBt[i] = dKt[i] = dQt[i] = 0.f;
+    for (int i = tid; i < BMX * LM; i += nth) dL[i] = dG[i] = dQA[i] = dQK[i] = 0.f;
     for (int c = tid; c < dk; c += nth) sd[c] = 0.f;
     __syncthreads();
 
@@ -222,46 +250,46 @@ block_bwd_kernel(Plan pl, BwdArgs a) {
         for (int i = tid; i < dk * BNS; i += nth) {
             const int c = i / BNS, n = i - c * BNS;
             const float e = __expf(va[c]);
-            S0s[i] = e * S0g[(size_t)c * dv + n0 + n];
+            S0s[c * LS + n] = e * S0g[(size_t)c * dv + n0 + n];
             const float ds = dSg[(size_t)c * dv + n0 + n];
-            dSs[i] = e * ds;
+            dSs[c * LS + n] = e * ds;
             atomicAdd(&sd[c], S1g[(size_t)c * dv + n0 + n] * ds);
         }
         for (int i = tid; i < cb * BNS; i += nth) {
             const int t = i / BNS, n = i - t * BNS;
-            dOs[i] = t < valid ? a.dO[(tok0 + t) * dv + n0 + n] : 0.f;
+            dOs[t * LS + n] = t < valid ? a.dO[(tok0 + t) * dv + n0 + n] : 0.f;
         }
         for (int i = tid; i < P * BNS; i += nth) {
             const int u = i / BNS, n = i - u * BNS, t = u / p, e = u - t * p;
             float x = 0.f;
             if (t < valid) x = MODE == DPLR_GENERIC ? ldg(Vin, ((tok0 + t) * p + e) * dv + n0 + n) : ldg(vin, (tok0 + t) * dv + n0 + n);
-            Vs[i] = x;
+            Vs[u * LS + n] = x;
         }
         __syncthreads();
-        mm(Hs, BNS, Bt, BD, false, S0s, BNS, false, R, BNS, dk, 1.f, false);
-        mm(dEs, BNS, At, BD, false, dSs, BNS, false, R, BNS, dk, -1.f, false);
+        mm(Hs, LS, Bt, LD, false, S0s, LS, false, R, BNS, dk, 1.f, false);
+        mm(dEs, LS, At, LD, false, dSs, LS, false, R, BNS, dk, -1.f, false);
         __syncthreads();
-        mm(Hs, BNS, Gm, BMX, false, Vs, BNS, false, R, BNS, P, 1.f, true);
-        mm(dEs, BNS, QA, BMX, true, dOs, BNS, false, R, BNS, cb, -1.f, true);
+        mm(Hs, LS, Gm, LM, false, Vs, LS, false, R, BNS, P, 1.f, true);
+        mm(dEs, LS, QA, LM, true, dOs, LS, false, R, BNS, cb, -1.f, true);
         __syncthreads();
-        mm(Es, BNS, Mm, BMX, false, Hs, BNS, false, R, BNS, R, 1.f, false);
-        mm(dHs, BNS, Mm, BMX, true, dEs, BNS, false, R, BNS, R, 1.f, false);
+        mm(Es, LS, Mm, LM, false, Hs, LS, false, R, BNS, R, 1.f, false);
+        mm(dHs, LS, Mm, LM, true, dEs, LS, false, R, BNS, R, 1.f, false);
         __syncthreads();
-        mm(dAt, BD, Es, BNS, false, dSs, BNS, true, R, dk, BNS, -1.f, true);
-        mm(dBt, BD, dHs, BNS, false, S0s, BNS, true, R, dk, BNS, 1.f, true);
-        mm(dKt, BD, Vs, BNS, false, dSs, BNS, true, P, dk, BNS, 1.f, true);
-        mm(dQt, BD, dOs, BNS, false, S0s, BNS, true, cb, dk, BNS, 1.f, true);
-        mm(dL, BMX, dHs, BNS, false, Es, BNS, true, R, R, BNS, -1.f, true);
-        mm(dG, BMX, dHs, BNS, false, Vs, BNS, true, R, P, BNS, 1.f, true);
-        mm(dQA, BMX, dOs, BNS, false, Es, BNS, true, cb, R, BNS, -1.f, true);
-        mm(dQK, BMX, dOs, BNS, false, Vs, BNS, true, cb, P, BNS, 1.f, true);
+        mm(dAt, LD, Es, LS, false, dSs, LS, true, R, dk, BNS, -1.f, true);
+        mm(dBt, LD, dHs, LS, false, S0s, LS, true, R, dk, BNS, 1.f, true);
+        mm(dKt, LD, Vs, LS, false, dSs, LS, true, P, dk, BNS, 1.f, true);
+        mm(dQt, LD, dOs, LS, false, S0s, LS, true, cb, dk, BNS, 1.f, true);
+        mm(dL, LM, dHs, LS, false, Es, LS, true, R, R, BNS, -1.f, true);
+        mm(dG, LM, dHs, LS, false, Vs, LS, true, R, P, BNS, 1.f, true);
+        mm(dQA, LM, dOs, LS, false, Es, LS, true, cb, R, BNS, -1.f, true);
+        mm(dQK, LM, dOs, LS, false, Vs, LS, true, cb, P, BNS, 1.f, true);
         // dV = K~ dS^ + QK^T dO + G^T dH for this slice, straight to the output
         for (int idx = tid; idx < P * BNS; idx += nth) {
             const int u = idx / BNS, n = idx - u * BNS, t = u / p, e = u - t * p;
             float s = 0.f;
-            for (int c = 0; c < dk; ++c) s = fmaf(Kt[u * BD + c], dSs[c * BNS + n], s);
-            for (int tt = 0; tt < cb; ++tt) s = fmaf(QK[tt * BMX + u], dOs[tt * BNS + n], s);
-            for (int m = 0; m < R; ++m) s = fmaf(Gm[m * BMX + u], dHs[m * BNS + n], s);
+            for (int c = 0; c < dk; ++c) s = fmaf(Kt[u * LD + c], dSs[c * LS + n], s);
+            for (int tt = 0; tt < cb; ++tt) s = fmaf(QK[tt * LM + u], dOs[tt * LS + n], s);
+            for (int m = 0; m < R; ++m) s = fmaf(Gm[m * LM + u], dHs[m * LS + n], s);
             if (t < valid) {
                 if (MODE == DPLR_GENERIC) a.dV[((tok0 + t) * p + e) * dv + n0 + n] = s;
                 else a.dv[(tok0 + t) * dv + n0 + n] = s;
@@ -271,41 +299,41 @@ block_bwd_kernel(Plan pl, BwdArgs a) {
     }
 
     // ---- the remaining terms of the factor gradients
-    mask(dL, BMX, R, R, r, r, true);
-    mask(dG, BMX, R, P, r, p, true);
-    mask(dQA, BMX, cb, R, 1, r, false);
-    mask(dQK, BMX, cb, P, 1, p, false);
+    mask(dL, LM, R, R, r, r, true);
+    mask(dG, LM, R, P, r, p, true);
+    mask(dQA, LM, cb, R, 1, r, false);
+    mask(dQK, LM, cb, P, 1, p, false);
     __syncthreads();
-    mm(dAt, BD, dQA, BMX, true, Qt, BD, false, R, dk, cb, 1.f, true);
-    mm(dBt, BD, dG, BMX, false, Kt, BD, false, R, dk, P, 1.f, true);
-    mm(dKt, BD, dQK, BMX, true, Qt, BD, false, P, dk, cb, 1.f, true);
-    mm(dQt, BD, dQA, BMX, false, At, BD, false, cb, dk, R, 1.f, true);
+    mm(dAt, LD, dQA, LM, true, Qt, LD, false, R, dk, cb, 1.f, true);
+    mm(dBt, LD, dG, LM, false, Kt, LD, false, R, dk, P, 1.f, true);
+    mm(dKt, LD, dQK, LM, true, Qt, LD, false, P, dk, cb, 1.f, true);
+    mm(dQt, LD, dQA, LM, false, At, LD, false, cb, dk, R, 1.f, true);
     __syncthreads();
-    mm(dAt, BD, dL, BMX, true, Bt, BD, false, R, dk, R, 1.f, true);
-    mm(dBt, BD, dL, BMX, false, At, BD, false, R, dk, R, 1.f, true);
-    mm(dKt, BD, dG, BMX, true, Bt, BD, false, P, dk, R, 1.f, true);
-    mm(dQt, BD, dQK, BMX, false, Kt, BD, false, cb, dk, P, 1.f, true);
+    mm(dAt, LD, dL, LM, true, Bt, LD, false, R, dk, R, 1.f, true);
+    mm(dBt, LD, dL, LM, false, At, LD, false, R, dk, R, 1.f, true);
+    mm(dKt, LD, dG, LM, true, Bt, LD, false, P, dk, R, 1.f, true);
+    mm(dQt, LD, dQK, LM, false, Kt, LD, false, cb, dk, P, 1.f, true);
     __syncthreads();
 
     // ---- the cumulative log-decay's gradient dG_t (over S0s / dSs), then its reverse prefix: d decay
-    float* dGt = S0s;   // [BMX][BD]
+    float* dGt = S0s;   // [BMX][LD] (fits the two slices: 2 BD LS >= BMX LD)
     for (int i = tid; i < cb * dk; i += nth) {
         const int t = i / dk, c = i - t * dk;
-        float s = Qt[t * BD + c] * dQt[t * BD + c];
-        for (int e = 0; e < r; ++e) s -= At[(t * r + e) * BD + c] * dAt[(t * r + e) * BD + c];
-        for (int e = 0; e < p; ++e) s -= Kt[(t * p + e) * BD + c] * dKt[(t * p + e) * BD + c];
+        float s = Qt[t * LD + c] * dQt[t * LD + c];
+        for (int e = 0; e < r; ++e) s -= At[(t * r + e) * LD + c] * dAt[(t * r + e) * LD + c];
+        for (int e = 0; e < p; ++e) s -= Kt[(t * p + e) * LD + c] * dKt[(t * p + e) * LD + c];
         if (t + 1 < cb)
-            for (int e = 0; e < r; ++e) s += Bt[((t + 1) * r + e) * BD + c] * dBt[((t + 1) * r + e) * BD + c];
+            for (int e = 0; e < r; ++e) s += Bt[((t + 1) * r + e) * LD + c] * dBt[((t + 1) * r + e) * LD + c];
         else
             s += sd[c];
-        dGt[t * BD + c] = s;
+        dGt[t * LD + c] = s;
     }
     __syncthreads();
     for (int c = tid; c < dk; c += nth) {
         float s = 0.f;
         for (int t = cb - 1; t >= 0; --t) {
-            s += dGt[t * BD + c];
-            dGt[t * BD + c] = s;
+            s += dGt[t * LD + c];
+            dGt[t * LD + c] = s;
         }
     }
     __syncthreads();
@@ -315,27 +343,27 @@ block_bwd_kernel(Plan pl, BwdArgs a) {
         const size_t tg = tok0 + t;
         float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f;   // per-token sums over channels
         for (int c = lane; c < dk; c += 32) {
-            const float G = Gc[t * BD + c], Gx = t > 0 ? Gc[(t - 1) * BD + c] : 0.f, an = va[c];
+            const float G = Gc[t * LD + c], Gx = t > 0 ? Gc[(t - 1) * LD + c] : 0.f, an = va[c];
             const float er = __expf(an - G), ef = __expf(Gx - an), eq = __expf(G - an);
-            const float dd = dGt[t * BD + c];
-            a.dq[tg * dk + c] = eq * dQt[t * BD + c];
+            const float dd = dGt[t * LD + c];
+            a.dq[tg * dk + c] = eq * dQt[t * LD + c];
             if (MODE == DPLR_GENERIC) {
                 a.ddecay[tg * dk + c] = dd;
                 for (int e = 0; e < r; ++e) {
-                    a.dA[(tg * r + e) * dk + c] = er * dAt[(t * r + e) * BD + c];
-                    a.dBm[(tg * r + e) * dk + c] = ef * dBt[(t * r + e) * BD + c];
+                    a.dA[(tg * r + e) * dk + c] = er * dAt[(t * r + e) * LD + c];
+                    a.dBm[(tg * r + e) * dk + c] = ef * dBt[(t * r + e) * LD + c];
                 }
-                for (int e = 0; e < p; ++e) a.dK[(tg * p + e) * dk + c] = er * dKt[(t * p + e) * BD + c];
+                for (int e = 0; e < p; ++e) a.dK[(tg * p + e) * dk + c] = er * dKt[(t * p + e) * LD + c];
             } else if (MODE == DPLR_GDN) {
                 const float kk = ldg(kin, tg * dk + c), b = a.beta[tg], eg = __expf(a.decay[tg]);
-                const float dA = er * dAt[t * BD + c], dB = ef * dBt[t * BD + c], dK = er * dKt[t * BD + c];
+                const float dA = er * dAt[t * LD + c], dB = ef * dBt[t * LD + c], dK = er * dKt[t * LD + c];
                 a.dk[tg * dk + c] = eg * b * dA + dB + b * dK;
                 acc0 = fmaf(kk, dA, acc0);   // k . dA
                 acc1 = fmaf(kk, dK, acc1);   // k . dK
                 acc2 += dd;                  // sum of the channels' decay gradients
             } else {
                 const float kk = ldg(kin, tg * dk + c);
-                const float dB0 = ef * dBt[(2 * t) * BD + c];
+                const float dB0 = ef * dBt[(2 * t) * LD + c];
                 acc0 = fmaf(kk, dB0, acc0);  // k . dB0 (needed before dk below)
             }
         }
@@ -354,16 +382,16 @@ block_bwd_kernel(Plan pl, BwdArgs a) {
             const float b = a.beta[tg], cc = ct[t], kb0 = acc0;
             float db = 0.f;
             for (int c = lane; c < dk; c += 32) {
-                const float G = Gc[t * BD + c], Gx = t > 0 ? Gc[(t - 1) * BD + c] : 0.f, an = va[c];
+                const float G = Gc[t * LD + c], Gx = t > 0 ? Gc[(t - 1) * LD + c] : 0.f, an = va[c];
                 const float er = __expf(an - G), ef = __expf(Gx - an);
                 const float kk = ldg(kin, tg * dk + c), lam = __expf(a.decay[tg * dk + c]);
-                const float dA0 = er * dAt[(2 * t) * BD + c], dA1 = er * dAt[(2 * t + 1) * BD + c];
-                const float dB0 = ef * dBt[(2 * t) * BD + c], dB1 = ef * dBt[(2 * t + 1) * BD + c];
-                const float dK = er * dKt[t * BD + c];
+                const float dA0 = er * dAt[(2 * t) * LD + c], dA1 = er * dAt[(2 * t + 1) * LD + c];
+                const float dB0 = ef * dBt[(2 * t) * LD + c], dB1 = ef * dBt[(2 * t + 1) * LD + c];
+                const float dK = er * dKt[t * LD + c];
                 a.dk[tg * dk + c] = dA0 + lam * dA1 + (b * lam - b * b * cc) * dB0 - 2.f * b * b * lam * kk * kb0 +
                                     b * dB1 + b * dK;
                 const float dlam = kk * dA1 + b * kk * dB0 - b * b * kk * kk * kb0;
-                a.ddecay[tg * dk + c] = dGt[t * BD + c] + lam * dlam;
+                a.ddecay[tg * dk + c] = dGt[t * LD + c] + lam * dlam;
                 db = fmaf(lam * kk, dB0, db);
                 db = fmaf(kk, dB1 + dK, db);
             }
@@ -374,12 +402,13 @@ block_bwd_kernel(Plan pl, BwdArgs a) {
 }
 
 size_t bwd_smem_bytes() {
-    return sizeof(float) * (size_t)(8 * BMX * BD + 8 * BMX * BMX + 2 * BD * BNS + 6 * BMX * BNS + BMX * BD + 2 * BD + BMX);
+    return sizeof(float) * (size_t)(8 * BMX * LD + 8 * BMX * LM + 2 * BD * LS + 6 * BMX * LS + BMX * LD + 2 * BD + BMX);
 }
 
 // ---- pass 2: the block-boundary state gradients, per (head, 16 state columns), blocks in reverse order
-constexpr int CBV = 16;
+constexpr int CBV = 32;
 
+// 256 threads: the 4 x 4 tiles of a 128 x 32 block of dS (fewer rows leave threads idle).
 __global__ void __launch_bounds__(256)
 chain_bwd_kernel(Plan pl, const float* Pm, const float* Qm, const float* dO, const float* dST, float* dSb,
                  float* dS0) {
@@ -397,32 +426,69 @@ chain_bwd_kernel(Plan pl, const float* Pm, const float* Qm, const float* dO, con
         const int c = i / CBV, n = i - c * CBV;
         dS[i] = dST ? dST[(bh * dk + c) * dv + n0 + n] : 0.f;
     }
+    auto prefetch = [&](int jj) {   // block jj's maps into L2 (contiguous in the workspace)
+        const float* P = Pm + (bh * (size_t)nb + jj) * (size_t)dk * dk;
+        const float* Q = Qm + (bh * (size_t)nb + jj) * (size_t)cw * dk;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(reinterpret_cast<uint64_t>(P)), "r"((uint32_t)(dk * dk * 4)) : "memory");
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(reinterpret_cast<uint64_t>(Q)), "r"((uint32_t)(cw * dk * 4)) : "memory");
+    };
+    if (tid == 0)
+        for (int jj = nb - 1; jj >= 0 && jj >= nb - 4; --jj) prefetch(jj);
     for (int j = nb - 1; j >= 0; --j) {
         __syncthreads();   // dS complete
+        if (tid == 0 && j - 4 >= 0) prefetch(j - 4);
         float* dst = dSb + (bh * (size_t)nb + j) * (size_t)dk * dv + n0;   // gradient of the state after block j
         for (int i = tid; i < dk * CBV; i += nth) dst[(size_t)(i / CBV) * dv + i % CBV] = dS[i];
-        const float* P = Pm + (bh * (size_t)nb + j) * (size_t)dk * dk;
-        const float* Q = Qm + (bh * (size_t)nb + j) * (size_t)cw * dk;
-        for (int i = tid; i < dk * dk; i += nth) Ps[(i / dk) * (dk + 1) + i % dk] = P[i];
-        for (int i = tid; i < cw * dk; i += nth) Qs[i] = Q[i];
+        const float4* P4 = reinterpret_cast<const float4*>(Pm + (bh * (size_t)nb + j) * (size_t)dk * dk);
+        const float4* Q4 = reinterpret_cast<const float4*>(Qm + (bh * (size_t)nb + j) * (size_t)cw * dk);
+        for (int i = tid; i < dk * dk / 4; i += nth) {
+            const float4 x = P4[i];
+            const int row = (4 * i) / dk, col = (4 * i) % dk;
+            float* d = Ps + row * (dk + 1) + col;
+            d[0] = x.x; d[1] = x.y; d[2] = x.z; d[3] = x.w;
+        }
+        for (int i = tid; i < cw * dk / 4; i += nth) reinterpret_cast<float4*>(Qs)[i] = Q4[i];
         for (int i = tid; i < cw * CBV; i += nth) {
             const int t = i / CBV, n = i - t * CBV, tg = j * cw + t;
             Os[i] = tg < T ? dO[(bh * (size_t)T + tg) * dv + n0 + n] : 0.f;
         }
         __syncthreads();
-        // dS_{j-1} = P_j^T dS_j + Q'_j^T dO_j
-        float acc[(128 * CBV + 255) / 256];
-        int m = 0;
-        for (int idx = tid; idx < dk * CBV; idx += nth, ++m) {
-            const int i = idx / CBV, n = idx - i * CBV;
-            float s = 0.f;
-            for (int c = 0; c < dk; ++c) s = fmaf(Ps[c * (dk + 1) + i], dS[c * CBV + n], s);
-            for (int t = 0; t < cw; ++t) s = fmaf(Qs[t * dk + i], Os[t * CBV + n], s);
-            acc[m] = s;
+        // dS_{j-1} = P_j^T dS_j + Q'_j^T dO_j: thread tid takes rows 4 (tid / 8) .., columns 4 (tid % 8) .. (4 x 4)
+        const int i0 = 4 * (tid >> 3), c0 = 4 * (tid & 7);
+        const bool act = i0 < dk;
+        float acc[4][4] = {};
+        if (act) {
+            for (int c = 0; c < dk; ++c) {
+                float x[4], y[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    x[e] = Ps[c * (dk + 1) + i0 + e];
+                    y[e] = dS[c * CBV + c0 + e];
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+#pragma unroll
+                    for (int f = 0; f < 4; ++f) acc[e][f] = fmaf(x[e], y[f], acc[e][f]);
+            }
+            for (int t = 0; t < cw; ++t) {
+                float x[4], y[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    x[e] = Qs[t * dk + i0 + e];
+                    y[e] = Os[t * CBV + c0 + e];
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+#pragma unroll
+                    for (int f = 0; f < 4; ++f) acc[e][f] = fmaf(x[e], y[f], acc[e][f]);
+            }
         }
         __syncthreads();
-        m = 0;
-        for (int idx = tid; idx < dk * CBV; idx += nth, ++m) dS[idx] = acc[m];
+        if (act)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+#pragma unroll
+                for (int f = 0; f < 4; ++f) dS[(i0 + e) * CBV + c0 + f] = acc[e][f];
     }
     __syncthreads();
     if (dS0)
