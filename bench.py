@@ -604,7 +604,7 @@ def run_backward(args):
     nbytes = tokens * per_tok + w.B * w.H * w.dk * w.dv * 4 * 3
     peaks, peak_kind = load_peaks()
     finite = all(bool(torch.isfinite(x).all().item()) for x in bw.grads.values())
-    print(json.dumps({"mode": "backward", "workload": w.name, "steps": K, "ms_per_backward": ms,
+    print(json.dumps({"mode": "backward", "workload": w.name, "T": w.T, "steps": K, "ms_per_backward": ms,
                       "tokens_per_s": tokens / (ms * 1e-3), "bytes_per_backward": nbytes,
                       "achieved_gbs": nbytes / (ms * 1e-3) / 1e9, "frac_of_hbm_peak": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                       "peak": f"{peak_kind} hbm_gbs {peaks['hbm_gbs']}", "workspace_bytes": bw.ws_bytes,
