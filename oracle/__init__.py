@@ -7,8 +7,9 @@ and shares no code with it.
 ``forward`` runs the plain serial token-by-token recurrence written in
 ``dplr_oracle.c`` (see that file for what each mode computes and the passages
 it follows); ``backward`` runs its reverse mode (the gradients of
-sum(do * o) + sum(dST * S_T) with respect to every input). Inputs of any float
-dtype are upcast to float64 exactly.
+sum(do * o) + sum(dST * S_T) with respect to every input); ``hla`` runs HLA's
+query-gated composition of chunk transitions on the Gated DeltaNet update. Inputs
+of any float dtype are upcast to float64 exactly.
 """
 
 from __future__ import annotations
@@ -52,6 +53,8 @@ def _lib():
             lib.oracle_forward.argtypes = [ctypes.c_int] * 8 + [dp] * 12 + [ctypes.c_int]
             lib.oracle_backward.restype = ctypes.c_int
             lib.oracle_backward.argtypes = [ctypes.c_int] * 8 + [dp] * 22 + [ctypes.c_int]
+            lib.oracle_hla.restype = ctypes.c_int
+            lib.oracle_hla.argtypes = [ctypes.c_int] * 6 + [ctypes.c_double] + [dp] * 7 + [ctypes.c_int]
             lib.oracle_max_threads.restype = ctypes.c_int
             _handle = lib
     return _handle
@@ -153,3 +156,21 @@ def backward_inputs(inp: dict, do, dST=None, threads: Optional[int] = None) -> d
     w = inp["workload"]
     return backward(w.mode, inp["q"], inp["k"], inp["v"], inp["decay"], inp["beta"], inp["A"], inp["Bm"],
                     inp["K"], inp["V"], inp["S0"], do, dST, threads=threads)
+
+
+def hla(q, k, v, g, beta, W, L: int, theta: float = 0.0, threads: Optional[int] = None):
+    """HLA's query-gated composition of chunk transitions on the Gated DeltaNet update (see dplr_oracle.c):
+    q, k [B,H,T,dk]; v [B,H,T,dv]; g, beta [B,H,T]; gates W [B,H,T,N] with N = ceil(T / L) (only the entries of
+    earlier chunks are used; those below theta count as zero). Returns o [B,H,T,dv] in float64."""
+    q, k, v, g, beta, W = _f64(q), _f64(k), _f64(v), _f64(g), _f64(beta), _f64(W)
+    B, H, T, dk = q.shape
+    dv = v.shape[3]
+    N = (T + int(L) - 1) // int(L)
+    if W.shape != (B, H, T, N):
+        raise ValueError(f"gates W must be [B, H, T, ceil(T / L)] = {(B, H, T, N)}, got {W.shape}")
+    o = np.zeros((B, H, T, dv), dtype=np.float64)
+    rc = _lib().oracle_hla(B, H, T, dk, dv, int(L), float(theta), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                           _ptr(W), _ptr(o), int(threads or 0))
+    if rc != 0:
+        raise ValueError(f"oracle_hla rejected its arguments (code {rc})")
+    return o

@@ -536,3 +536,97 @@ int oracle_backward(int mode, int B, int H, int T, int dk, int dv, int r, int p,
     }
     return 0;
 }
+
+/*
+ * HLA's query-conditioned composition of chunk transitions ("HLA: Expressive Hybrid Linear Attention via
+ * Chunk-Wise Dynamic Mixing", Method steps 1, 2, 4 and 5), on the Gated DeltaNet token update above.
+ * TEST INFRASTRUCTURE ONLY, like the rest of this file.
+ *
+ * The sequence is cut into chunks of L tokens (the last may be shorter). Each chunk j has the exact affine
+ * summary S -> A_j S + B_j of its token updates (A_j the product of its P_t, B_j its state from zero). For query
+ * token i in chunk c, with gates w_ij (j < c; the gates of the current and later chunks are not used), gates
+ * below `theta` set to zero:
+ *   S_i = 0;  for j = 0 .. c-1:  S_i = ((1 - w_ij) I + w_ij A_j) S_i + w_ij B_j
+ *   then the tokens of chunk c up to i, one by one (the causal prefix of the current chunk),
+ *   o_i = S_i^T q_i.
+ * Layouts: q, k [B,H,T,dk]; v [B,H,T,dv]; g, beta [B,H,T]; W [B,H,T,N] with N = ceil(T / L); o [B,H,T,dv].
+ */
+static void gdn_token(int dk, int dv, const double* kt, const double* vt, double gt, double bt, double* S, double* w)
+{
+    const double gate = exp(gt);
+    for (int n = 0; n < dv; ++n) {
+        double s = 0.0;
+        for (int c = 0; c < dk; ++c) s += kt[c] * S[(size_t)c * dv + n];
+        w[n] = s;
+    }
+    for (int c = 0; c < dk; ++c)
+        for (int n = 0; n < dv; ++n)
+            S[(size_t)c * dv + n] = gate * (S[(size_t)c * dv + n] - bt * kt[c] * w[n]) + (vt ? bt * kt[c] * vt[n] : 0.0);
+}
+
+int oracle_hla(int B, int H, int T, int dk, int dv, int L, double theta,
+               const double* q, const double* k, const double* v, const double* g, const double* beta,
+               const double* W, double* o, int nthreads)
+{
+    if (B < 0 || H < 0 || T < 0 || dk <= 0 || dv <= 0 || L <= 0) return -1;
+    if (T > 0 && (!q || !k || !v || !g || !beta || !W || !o)) return -4;
+    const int N = (T + L - 1) / L;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    const long nheads = (long)B * H;
+    const size_t SS = (size_t)dk * dv, AA = (size_t)dk * dk;
+#pragma omp parallel
+    {
+        double* Am = (double*)malloc(sizeof(double) * AA * (N > 0 ? N : 1));   /* A_j */
+        double* Bm = (double*)malloc(sizeof(double) * SS * (N > 0 ? N : 1));   /* B_j */
+        double* S = (double*)malloc(sizeof(double) * SS);
+        double* X = (double*)malloc(sizeof(double) * (AA > SS ? AA : SS));
+        double* w = (double*)malloc(sizeof(double) * (dk > dv ? dk : dv));
+#pragma omp for schedule(dynamic, 1)
+        for (long bh = 0; bh < nheads; ++bh) {
+            const size_t tk = (size_t)bh * T;
+            /* chunk summaries: A_j by applying the token updates (no write) to the identity, B_j from zero */
+            for (int j = 0; j < N; ++j) {
+                double* A = Am + (size_t)j * AA;
+                double* Bj = Bm + (size_t)j * SS;
+                for (int r = 0; r < dk; ++r)
+                    for (int c = 0; c < dk; ++c) A[(size_t)r * dk + c] = r == c ? 1.0 : 0.0;
+                memset(Bj, 0, sizeof(double) * SS);
+                for (int t = j * L; t < T && t < (j + 1) * L; ++t) {
+                    gdn_token(dk, dk, k + (tk + t) * dk, NULL, g[tk + t], beta[tk + t], A, w);
+                    gdn_token(dk, dv, k + (tk + t) * dk, v + (tk + t) * dv, g[tk + t], beta[tk + t], Bj, w);
+                }
+            }
+            for (int i = 0; i < T; ++i) {
+                const int c = i / L;
+                memset(S, 0, sizeof(double) * SS);
+                for (int j = 0; j < c; ++j) {
+                    double wij = W[(tk + i) * N + j];
+                    if (wij < theta) wij = 0.0;
+                    if (wij == 0.0) continue;   /* (1 - 0) I: the state passes unchanged */
+                    const double* A = Am + (size_t)j * AA;
+                    const double* Bj = Bm + (size_t)j * SS;
+                    for (int r = 0; r < dk; ++r)
+                        for (int n = 0; n < dv; ++n) {
+                            double s = 0.0;
+                            for (int c2 = 0; c2 < dk; ++c2) s += A[(size_t)r * dk + c2] * S[(size_t)c2 * dv + n];
+                            X[(size_t)r * dv + n] = (1.0 - wij) * S[(size_t)r * dv + n] + wij * (s + Bj[(size_t)r * dv + n]);
+                        }
+                    memcpy(S, X, sizeof(double) * SS);
+                }
+                for (int t = c * L; t <= i; ++t)
+                    gdn_token(dk, dv, k + (tk + t) * dk, v + (tk + t) * dv, g[tk + t], beta[tk + t], S, w);
+                for (int n = 0; n < dv; ++n) {
+                    double s = 0.0;
+                    for (int c2 = 0; c2 < dk; ++c2) s += S[(size_t)c2 * dv + n] * q[(tk + i) * dk + c2];
+                    o[(tk + i) * dv + n] = s;
+                }
+            }
+        }
+        free(Am); free(Bm); free(S); free(X); free(w);
+    }
+    return 0;
+}

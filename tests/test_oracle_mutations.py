@@ -15,6 +15,7 @@ import pytest
 
 import oracle
 import test_oracle_backward as bpins
+import test_oracle_hla as hpins
 import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "dplr_oracle.c")
@@ -93,15 +94,36 @@ BWD_PIN_CALLS = [
 ]
 
 
-def _build_mutant(tmp_path, name, old, new, backward=False):
+HLA_MARK = "/*\n * HLA's query-conditioned composition"
+
+# Mistakes planted in the HLA composition (after HLA_MARK), caught by its pins.
+HLA_MUTANTS = {
+    "hla_gate_drops_retention": ("X[(size_t)r * dv + n] = (1.0 - wij) * S[(size_t)r * dv + n] + wij * (s + Bj[(size_t)r * dv + n]);",
+                                 "X[(size_t)r * dv + n] = wij * (s + Bj[(size_t)r * dv + n]);"),
+    "hla_gate_on_write_only": ("X[(size_t)r * dv + n] = (1.0 - wij) * S[(size_t)r * dv + n] + wij * (s + Bj[(size_t)r * dv + n]);",
+                               "X[(size_t)r * dv + n] = s + wij * Bj[(size_t)r * dv + n];"),
+    "hla_skips_current_prefix": ("for (int t = c * L; t <= i; ++t)", "for (int t = c * L; t < i; ++t)"),
+    "hla_threshold_inverted": ("if (wij < theta) wij = 0.0;", "if (wij > theta) wij = 0.0;"),
+}
+
+HLA_PIN_CALLS = [
+    hpins.test_all_gates_one_is_the_gdn_recurrence,
+    hpins.test_all_gates_zero_restarts_each_chunk,
+    hpins.test_one_gate_selects_one_chunk_of_history,
+    hpins.test_gates_below_the_threshold_are_zero,
+    hpins.test_output_is_affine_in_each_gate,
+]
+
+
+def _build_mutant(tmp_path, name, old, new, backward=False, hla=False):
     text = open(SRC).read()
-    cut = text.index(BWD_MARK)
-    fwd, bwd = text[:cut], text[cut:]
-    part = bwd if backward else fwd
-    assert part.count(old) == 1, f"mutation anchor for {name} not unique/found"
-    part = part.replace(old, new)
+    cut, cut2 = text.index(BWD_MARK), text.index(HLA_MARK)
+    parts = [text[:cut], text[cut:cut2], text[cut2:]]
+    k = 2 if hla else (1 if backward else 0)
+    assert parts[k].count(old) == 1, f"mutation anchor for {name} not unique/found"
+    parts[k] = parts[k].replace(old, new)
     src = tmp_path / f"{name}.c"
-    src.write_text(fwd + part if backward else part + bwd)
+    src.write_text("".join(parts))
     so = tmp_path / f"{name}.so"
     subprocess.run(["gcc", "-O1", "-std=c11", "-fopenmp", "-fPIC", "-shared", str(src), "-o", str(so), "-lm"],
                    check=True)
@@ -109,6 +131,8 @@ def _build_mutant(tmp_path, name, old, new, backward=False):
     dp = ctypes.POINTER(ctypes.c_double)
     lib.oracle_forward.restype = ctypes.c_int
     lib.oracle_forward.argtypes = [ctypes.c_int] * 8 + [dp] * 12 + [ctypes.c_int]
+    lib.oracle_hla.restype = ctypes.c_int
+    lib.oracle_hla.argtypes = [ctypes.c_int] * 6 + [ctypes.c_double] + [dp] * 7 + [ctypes.c_int]
     lib.oracle_backward.restype = ctypes.c_int
     lib.oracle_backward.argtypes = [ctypes.c_int] * 8 + [dp] * 22 + [ctypes.c_int]
     lib.oracle_max_threads.restype = ctypes.c_int
@@ -138,6 +162,21 @@ def test_backward_pins_catch_planted_mistake(name, tmp_path, monkeypatch):
     monkeypatch.setattr(oracle, "_handle", lib)
     caught = 0
     for call in BWD_PIN_CALLS:
+        try:
+            call()
+        except AssertionError:
+            caught += 1
+    assert caught > 0, f"no pin failed for mutant {name}"
+
+
+@pytest.mark.parametrize("name", sorted(HLA_MUTANTS))
+def test_hla_pins_catch_planted_mistake(name, tmp_path, monkeypatch):
+    old, new = HLA_MUTANTS[name]
+    lib = _build_mutant(tmp_path, name, old, new, hla=True)
+    oracle._lib()
+    monkeypatch.setattr(oracle, "_handle", lib)
+    caught = 0
+    for call in HLA_PIN_CALLS:
         try:
             call()
         except AssertionError:
