@@ -202,6 +202,21 @@ DPLR_API dplr_status dplr_la_backward(const dplr_desc* desc,
                              float* dA, float* dBm, float* dK, float* dV, float* dS0,
                              void* workspace, size_t ws_bytes, void* stream);
 
+/* HLA's query-conditioned composition of chunk transitions ("HLA: Expressive Hybrid Linear Attention via
+ * Chunk-Wise Dynamic Mixing", Method steps 1, 2, 4, 5) on the Gated DeltaNet update of `desc` (mode DPLR_GDN,
+ * dk, dv <= 128): the sequence is cut into chunks of L tokens (64, 128 or 256), chunk j summarised exactly as
+ * S -> A_j S + B_j; query token i of chunk c starts from a zero state, composes the earlier chunks in order as
+ * S <- ((1 - w_ij) I + w_ij A_j) S + w_ij B_j, runs its own chunk's causal prefix, and reads o_i = S^T q_i.
+ * W [B,H,T,N] fp32, N = ceil(T / L): the gates (only w_ij with j < c are used); gates below `theta` count as
+ * zero. q, k, v, g, beta as for dplr_la_forward (no initial state). o [B,H,T,dv] fp32. Workspace:
+ * dplr_hla_workspace_size(desc, L) bytes, 256-byte aligned. fp32 arithmetic on the CUDA cores. Asynchronous on
+ * `stream`; allocates nothing. Errors: DPLR_ERR_INVALID_ARG for another mode or a null / misaligned pointer,
+ * DPLR_ERR_UNSUPPORTED for another L or dk, dv > 128, DPLR_ERR_WORKSPACE, DPLR_ERR_CUDA. */
+DPLR_API size_t dplr_hla_workspace_size(const dplr_desc* desc, int L);
+DPLR_API dplr_status dplr_hla_forward(const dplr_desc* desc, const void* q, const void* k, const void* v,
+                             const float* g, const float* beta, const float* W, float theta, int L,
+                             float* o, void* workspace, size_t ws_bytes, void* stream);
+
 /* Name of the kernel path that dplr_la_forward runs for `desc` (no counterpart in the
  * paper; static storage): "gdn_fused_tcgen05" (GDN, bf16, dk = dv = 128: one fused
  * per-head kernel on the tensor cores), "hdla_tcgen05" (HDLA, bf16, dk = dv = 128: the

@@ -73,6 +73,10 @@ def library() -> ctypes.CDLL:
             lib.dplr_la_backward_workspace_size.argtypes = [dp]
             lib.dplr_la_backward.restype = ctypes.c_int
             lib.dplr_la_backward.argtypes = [dp] + [_vp] * 22 + [_vp, ctypes.c_size_t, _vp]
+            lib.dplr_hla_workspace_size.restype = ctypes.c_size_t
+            lib.dplr_hla_workspace_size.argtypes = [dp, ctypes.c_int]
+            lib.dplr_hla_forward.restype = ctypes.c_int
+            lib.dplr_hla_forward.argtypes = [dp] + [_vp] * 6 + [ctypes.c_float, ctypes.c_int, _vp, _vp, ctypes.c_size_t, _vp]
             lib.dplr_la_path.restype = ctypes.c_char_p
             lib.dplr_la_path.argtypes = [dp]
             lib.dplr_la_set_wait_limit.restype = None
@@ -144,6 +148,16 @@ def dplr_la_backward(desc, q, k, v, decay, beta, A, Bm, K, V, S0, dO, dST, dq, d
     """Gradients of every input given dO and dS_T (device pointers; see include/dplr.h)."""
     return int(library().dplr_la_backward(ctypes.byref(desc), q, k, v, decay, beta, A, Bm, K, V, S0, dO, dST, dq, dk,
                                           dv, ddecay, dbeta, dA, dBm, dK, dV, dS0, workspace, ws_bytes, stream))
+
+
+def dplr_hla_workspace_size(desc: dplr_desc, L: int) -> int:
+    return int(library().dplr_hla_workspace_size(ctypes.byref(desc), int(L)))
+
+
+def dplr_hla_forward(desc, q, k, v, g, beta, W, theta, L, o, workspace, ws_bytes, stream) -> int:
+    """HLA's query-gated composition of GDN chunk transitions (device pointers; see include/dplr.h)."""
+    return int(library().dplr_hla_forward(ctypes.byref(desc), q, k, v, g, beta, W, float(theta), int(L), o, workspace,
+                                          ws_bytes, stream))
 
 
 def dplr_la_path(desc: dplr_desc) -> str:
@@ -441,3 +455,29 @@ class Backward:
         if st != DPLR_OK:
             raise DplrError(st, "dplr_la_backward")
         return g
+
+
+class HLA:
+    """Prepared HLA forward (dplr_hla_forward) for one GDN descriptor and chunk length: owns workspace and output."""
+
+    def __init__(self, in_dtype: torch.dtype, B: int, H: int, T: int, dk: int, dv: int, L: int = 256,
+                 device: Optional[torch.device] = None):
+        self.desc = make_desc("gdn", in_dtype, B, H, T, dk, dv)
+        self.L = int(L)
+        self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        nbytes = dplr_hla_workspace_size(self.desc, self.L)
+        if nbytes == 0:
+            raise DplrError(2, "dplr_hla_workspace_size")
+        self.ws = torch.empty(nbytes + 256, dtype=torch.uint8, device=self.device)
+        off = (-self.ws.data_ptr()) % 256
+        self.ws_ptr, self.ws_bytes = self.ws.data_ptr() + off, nbytes
+        self.o = torch.empty((B, H, T, dv), dtype=torch.float32, device=self.device)
+
+    def __call__(self, q, k, v, g, beta, W, theta: float = 0.0,
+                 stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        st = dplr_hla_forward(self.desc, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(W), theta, self.L,
+                              _ptr(self.o), self.ws_ptr, self.ws_bytes, s.cuda_stream)
+        if st != DPLR_OK:
+            raise DplrError(st, "dplr_hla_forward")
+        return self.o

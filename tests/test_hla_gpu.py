@@ -1,0 +1,84 @@
+"""HLA's query-gated composition (dplr_hla_forward) against the float64 oracle (oracle.hla).
+
+Whole small problems, compared element by element: max |err| <= TAU * RMS of the oracle's output. The GPU path
+composes the exact chunk maps in fp32 from exact inputs (bf16 values upcast); TAU = 1e-3 allows for the fp32
+rounding of those products (the measured errors sit near 1e-6 to 1e-5).
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+TAU = 1e-3
+
+
+@pytest.fixture(scope="module")
+def sdl():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from structured_decay_linear_gb300 import build as nvbuild
+    nvbuild.build()
+    import structured_decay_linear_gb300 as s
+    s.library()
+    return s
+
+
+def _rel(a, ref):
+    return float(np.abs(a - ref).max() / max(np.sqrt(np.mean(ref ** 2)), 1e-30))
+
+
+def gates(H, T, L, seed, scale=2.0):
+    """Synthetic gates in (0, 1): sigmoid of N(-1, scale) per (query, chunk)."""
+    N = (T + L - 1) // L
+    z = np.random.default_rng(seed).standard_normal((1, H, T, N)) * scale - 1.0
+    return (1.0 / (1.0 + np.exp(-z))).astype(np.float32)
+
+
+CASES = [
+    # dtype, dk, dv, H, T, L, theta
+    ("bf16", 128, 128, 2, 700, 256, 0.1),
+    ("bf16", 128, 128, 2, 300, 64, 0.0),
+    ("f32", 64, 64, 2, 500, 128, 0.1),
+    ("f32", 64, 128, 1, 257, 256, 0.5),
+    ("bf16", 128, 64, 1, 64, 64, 0.1),
+]
+
+
+@pytest.mark.parametrize("dtype,dk,dv,H,T,L,theta", CASES)
+def test_hla_matches_oracle(sdl, dtype, dk, dv, H, T, L, theta):
+    import torch
+    w = workloads.Workload(89, "hla_gdn", "gdn", dtype, 1, 1, 0, dk, dv, 1, 1, 64, False)
+    inp = workloads.generate(w, heads=[(0, h) for h in range(H)], T=T)
+    W = gates(H, T, L, seed=T + L)
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    d = lambda x, t: torch.from_numpy(np.ascontiguousarray(x)).to("cuda").to(t)
+    f = sdl.HLA(dt, 1, H, T, dk, dv, L)
+    o = f(d(inp["q"], dt), d(inp["k"], dt), d(inp["v"], dt), d(inp["decay"], torch.float32),
+          d(inp["beta"], torch.float32), d(W, torch.float32), theta)
+    torch.cuda.synchronize()
+    ref = oracle.hla(inp["q"], inp["k"], inp["v"], inp["decay"], inp["beta"], W, L, theta)
+    e = _rel(o.double().cpu().numpy(), ref)
+    assert e <= TAU, f"max|err|/rms = {e:.3e}"
+
+
+def test_hla_all_gates_one_is_the_forward(sdl):
+    """With every gate 1 the composition is the plain GDN recurrence: dplr_hla_forward equals dplr_la_forward."""
+    import torch
+    w = workloads.Workload(88, "hla_gdn", "gdn", "bf16", 1, 1, 0, 128, 128, 1, 1, 64, False)
+    H, T, L = 2, 512, 128
+    inp = workloads.generate(w, heads=[(0, h) for h in range(H)], T=T)
+    d = lambda x, t: torch.from_numpy(np.ascontiguousarray(x)).to("cuda").to(t)
+    args = [d(inp["q"], torch.bfloat16), d(inp["k"], torch.bfloat16), d(inp["v"], torch.bfloat16),
+            d(inp["decay"], torch.float32), d(inp["beta"], torch.float32)]
+    o = sdl.HLA(torch.bfloat16, 1, H, T, 128, 128, L)(*args, d(np.ones((1, H, T, T // L)), torch.float32), 0.1)
+    f = sdl.Forward("gdn", torch.bfloat16, 1, H, T, 128, 128)
+    o2, _ = f(q=args[0], k=args[1], v=args[2], decay=args[3], beta=args[4])
+    torch.cuda.synchronize()
+    ref, _ = oracle.forward_inputs(inp)
+    assert _rel(o.double().cpu().numpy(), ref) <= TAU
+    assert _rel(o.double().cpu().numpy(), o2.double().cpu().numpy()) <= 2e-2
