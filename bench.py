@@ -556,6 +556,65 @@ def dataclasses_replace(w, **kw):
     return dataclasses.replace(w, **kw)
 
 
+def run_hla(args):
+    """Time of dplr_hla_forward (HLA's query-gated composition of GDN chunk transitions) on a synthetic HLA
+    workload: GDN inputs of the workload recipe (bf16, d = 128) at B=1 H=16 T=4096 (the HLA page's 4K context),
+    chunks of L = 256 tokens, gates sigmoid(N(-1, 2)) per (query, chunk) and the page's inference threshold 0.1.
+    Not a benchmark line; the JSON carries "mode": "hla"."""
+    import torch
+    import structured_decay_linear_gb300 as sdl
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    T = args.seq_len or 4096
+    L, theta, H = 256, 0.1, 16
+    w = workloads.Workload(98, "hla_gdn_bf16_b1h16", "gdn", "bf16", 1, H, T, 128, 128, 1, 1, 64, False)
+    inp = workloads.generate(w)
+    N = (T + L - 1) // L
+    z = np.random.default_rng(1).standard_normal((1, H, T, N)) * 2.0 - 1.0
+    W = (1.0 / (1.0 + np.exp(-z))).astype(np.float32)
+    d = lambda x, t: torch.from_numpy(np.ascontiguousarray(x)).to(dev).to(t)
+    args_t = [d(inp["q"], torch.bfloat16), d(inp["k"], torch.bfloat16), d(inp["v"], torch.bfloat16),
+              d(inp["decay"], torch.float32), d(inp["beta"], torch.float32), d(W, torch.float32)]
+    f = sdl.HLA(torch.bfloat16, 1, H, T, 128, 128, L, device=dev)
+    call = lambda: f(*args_t, theta)
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        call()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / K
+    # the gated pass's products: per 64-query block and history chunk with a gate >= theta, U A_j and U B_j
+    Wt = np.where(W >= theta, W, 0.0)
+    pairs = 0
+    for qb in range(T // 64):
+        c = (qb * 64) // L
+        blk = Wt[0, :, qb * 64:(qb + 1) * 64, :c]
+        pairs += int((blk.max(axis=1) > 0).sum())
+    flops = pairs * 2 * (2 * 64 * 128 * 128)
+    fwd = sdl.Forward("gdn", torch.bfloat16, 1, H, T, 128, 128, device=dev)
+    for _ in range(3):
+        fwd(q=args_t[0], k=args_t[1], v=args_t[2], decay=args_t[3], beta=args_t[4])
+    torch.cuda.synchronize(dev)
+    e0.record()
+    for _ in range(K):
+        fwd(q=args_t[0], k=args_t[1], v=args_t[2], decay=args_t[3], beta=args_t[4])
+    e1.record()
+    torch.cuda.synchronize(dev)
+    ms_fwd = e0.elapsed_time(e1) / K
+    print(json.dumps({"mode": "hla", "workload": f"hla_gdn_bf16_b1h{H}_t{T}_d128_L{L}", "steps": K, "ms_per_forward": ms,
+                      "tokens_per_s": H * T / (ms * 1e-3), "gate_pairs_kept": pairs,
+                      "gate_pairs_total": H * sum((qb * 64) // L for qb in range(T // 64)),
+                      "gated_pass_tflops": flops / (ms * 1e-3) / 1e12, "gdn_forward_ms": ms_fwd,
+                      "output_finite": bool(torch.isfinite(f.o).all().item()), "arithmetic": "f32 (CUDA cores)"}),
+          flush=True)
+
+
 def run_backward(args):
     """Time of dplr_la_backward (the gradients of every input given dO and dS_T) on a workload at full size, with
     the same recipe as the forward and random upstream gradients. Reports ms per backward and tokens/s, and the
@@ -619,6 +678,8 @@ def main():
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--hla", action="store_true",
+                    help="time HLA's query-gated composition (dplr_hla_forward); not a benchmark line")
     ap.add_argument("--backward", action="store_true",
                     help="time dplr_la_backward on the workload (not a benchmark line)")
     ap.add_argument("--decode", action="store_true",
@@ -630,6 +691,9 @@ def main():
     args = ap.parse_args()
     if args.host_overhead:
         run_host_overhead(args)
+        return
+    if args.hla:
+        run_hla(args)
         return
     if args.backward:
         run_backward(args)
