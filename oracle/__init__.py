@@ -8,8 +8,9 @@ and shares no code with it.
 ``dplr_oracle.c`` (see that file for what each mode computes and the passages
 it follows); ``backward`` runs its reverse mode (the gradients of
 sum(do * o) + sum(dST * S_T) with respect to every input); ``hla`` runs HLA's
-query-gated composition of chunk transitions on the Gated DeltaNet update. Inputs
-of any float dtype are upcast to float64 exactly.
+query-gated composition of chunk transitions on the Gated DeltaNet update; ``gdp``
+runs Gated DeltaProduct-style stacked Householders. Inputs of any float dtype are
+upcast to float64 exactly.
 """
 
 from __future__ import annotations
@@ -55,6 +56,8 @@ def _lib():
             lib.oracle_backward.argtypes = [ctypes.c_int] * 8 + [dp] * 22 + [ctypes.c_int]
             lib.oracle_hla.restype = ctypes.c_int
             lib.oracle_hla.argtypes = [ctypes.c_int] * 6 + [ctypes.c_double] + [dp] * 7 + [ctypes.c_int]
+            lib.oracle_gdp.restype = ctypes.c_int
+            lib.oracle_gdp.argtypes = [ctypes.c_int] * 6 + [dp] * 8 + [ctypes.c_int]
             lib.oracle_max_threads.restype = ctypes.c_int
             _handle = lib
     return _handle
@@ -174,3 +177,19 @@ def hla(q, k, v, g, beta, W, L: int, theta: float = 0.0, threads: Optional[int] 
     if rc != 0:
         raise ValueError(f"oracle_hla rejected its arguments (code {rc})")
     return o
+
+
+def gdp(q, k, v, g, beta, S0=None, threads: Optional[int] = None):
+    """Gated DeltaProduct-style stacked Householders (see dplr_oracle.c): per token the gate, then n_h delta-rule
+    steps. q [B,H,T,dk]; k [B,H,T,nh,dk]; v [B,H,T,nh,dv]; g [B,H,T]; beta [B,H,T,nh]; S0 [B,H,dk,dv] or None.
+    Returns (o [B,H,T,dv], S_T [B,H,dk,dv]) in float64."""
+    q, k, v, g, beta, S0 = _f64(q), _f64(k), _f64(v), _f64(g), _f64(beta), _f64(S0)
+    B, H, T, dk = q.shape
+    nh, dv = k.shape[3], v.shape[4]
+    o = np.zeros((B, H, T, dv), dtype=np.float64)
+    ST = np.zeros((B, H, dk, dv), dtype=np.float64)
+    rc = _lib().oracle_gdp(B, H, T, dk, dv, nh, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S0), _ptr(o),
+                           _ptr(ST), int(threads or 0))
+    if rc != 0:
+        raise ValueError(f"oracle_gdp rejected its arguments (code {rc})")
+    return o, ST

@@ -630,3 +630,61 @@ int oracle_hla(int B, int H, int T, int dk, int dv, int L, double theta,
     }
     return 0;
 }
+
+/*
+ * Gated DeltaProduct-style stacked Householders ("Householder-Diagonalized Linear Attention", research
+ * background and the computation table: GDP with n_h = 2, 3, r_ab = r_kv = n_h): per token the gate once, then
+ * n_h delta-rule steps, each an erase and a write with its own key, value and beta:
+ *   S <- e^{g_t} S;  for h = 1 .. n_h:  S <- S - beta_{t,h} k_{t,h} (k_{t,h}^T S - v_{t,h}^T)
+ * then o_t = S^T q_t. TEST INFRASTRUCTURE ONLY, like the rest of this file.
+ * Layouts: q [B,H,T,dk]; k [B,H,T,nh,dk]; v [B,H,T,nh,dv]; g [B,H,T]; beta [B,H,T,nh]; S0, ST [B,H,dk,dv].
+ */
+int oracle_gdp(int B, int H, int T, int dk, int dv, int nh, const double* q, const double* k, const double* v,
+               const double* g, const double* beta, const double* S0, double* o, double* ST, int nthreads)
+{
+    if (B < 0 || H < 0 || T < 0 || dk <= 0 || dv <= 0 || nh <= 0) return -1;
+    if (T > 0 && (!q || !k || !v || !g || !beta || !o)) return -4;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    const long nheads = (long)B * H;
+    const size_t SS = (size_t)dk * dv;
+#pragma omp parallel
+    {
+        double* S = (double*)malloc(sizeof(double) * SS);
+        double* w = (double*)malloc(sizeof(double) * dv);
+#pragma omp for schedule(dynamic, 1)
+        for (long bh = 0; bh < nheads; ++bh) {
+            const size_t tk = (size_t)bh * T;
+            for (size_t e = 0; e < SS; ++e) S[e] = S0 ? S0[(size_t)bh * SS + e] : 0.0;
+            for (int t = 0; t < T; ++t) {
+                const double gate = exp(g[tk + t]);
+                for (size_t e = 0; e < SS; ++e) S[e] *= gate;
+                for (int h = 0; h < nh; ++h) {
+                    const double* kt = k + ((tk + t) * nh + h) * dk;
+                    const double* vt = v + ((tk + t) * nh + h) * dv;
+                    const double bt = beta[(tk + t) * nh + h];
+                    for (int n = 0; n < dv; ++n) {
+                        double s = 0.0;
+                        for (int c = 0; c < dk; ++c) s += kt[c] * S[(size_t)c * dv + n];
+                        w[n] = s - vt[n];
+                    }
+                    for (int c = 0; c < dk; ++c)
+                        for (int n = 0; n < dv; ++n) S[(size_t)c * dv + n] -= bt * kt[c] * w[n];
+                }
+                for (int n = 0; n < dv; ++n) {
+                    double s = 0.0;
+                    for (int c = 0; c < dk; ++c) s += S[(size_t)c * dv + n] * q[(tk + t) * dk + c];
+                    o[(tk + t) * dv + n] = s;
+                }
+            }
+            if (ST)
+                for (size_t e = 0; e < SS; ++e) ST[(size_t)bh * SS + e] = S[e];
+        }
+        free(S);
+        free(w);
+    }
+    return 0;
+}

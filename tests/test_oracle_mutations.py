@@ -15,6 +15,7 @@ import pytest
 
 import oracle
 import test_oracle_backward as bpins
+import test_oracle_gdp as gpins
 import test_oracle_hla as hpins
 import test_oracle_pins as pins
 
@@ -106,6 +107,23 @@ HLA_MUTANTS = {
     "hla_threshold_inverted": ("if (wij < theta) wij = 0.0;", "if (wij > theta) wij = 0.0;"),
 }
 
+GDP_MARK = "/*\n * Gated DeltaProduct-style stacked Householders"
+
+# Mistakes planted in the stacked-Householder oracle (after GDP_MARK), caught by its pins.
+GDP_MUTANTS = {
+    "gdp_gate_per_step": ("for (size_t e = 0; e < SS; ++e) S[e] *= gate;\n                for (int h = 0; h < nh; ++h) {",
+                          "for (int h = 0; h < nh; ++h) {\n                for (size_t e = 0; e < SS; ++e) S[e] *= gate;"),
+    "gdp_write_sign": ("w[n] = s - vt[n];", "w[n] = s + vt[n];"),
+    "gdp_last_step_only": ("for (int h = 0; h < nh; ++h) {\n                    const double* kt", "for (int h = nh - 1; h < nh; ++h) {\n                    const double* kt"),
+}
+
+GDP_PIN_CALLS = [
+    gpins.test_one_step_is_gated_deltanet,
+    gpins.test_second_step_with_zero_beta_is_gated_deltanet,
+    gpins.test_explicit_transition_and_write,
+    gpins.test_rank_nh_transition_in_the_generic_form,
+]
+
 HLA_PIN_CALLS = [
     hpins.test_all_gates_one_is_the_gdn_recurrence,
     hpins.test_all_gates_zero_restarts_each_chunk,
@@ -115,11 +133,11 @@ HLA_PIN_CALLS = [
 ]
 
 
-def _build_mutant(tmp_path, name, old, new, backward=False, hla=False):
+def _build_mutant(tmp_path, name, old, new, backward=False, hla=False, gdp=False):
     text = open(SRC).read()
-    cut, cut2 = text.index(BWD_MARK), text.index(HLA_MARK)
-    parts = [text[:cut], text[cut:cut2], text[cut2:]]
-    k = 2 if hla else (1 if backward else 0)
+    cut, cut2, cut3 = text.index(BWD_MARK), text.index(HLA_MARK), text.index(GDP_MARK)
+    parts = [text[:cut], text[cut:cut2], text[cut2:cut3], text[cut3:]]
+    k = 3 if gdp else (2 if hla else (1 if backward else 0))
     assert parts[k].count(old) == 1, f"mutation anchor for {name} not unique/found"
     parts[k] = parts[k].replace(old, new)
     src = tmp_path / f"{name}.c"
@@ -131,6 +149,8 @@ def _build_mutant(tmp_path, name, old, new, backward=False, hla=False):
     dp = ctypes.POINTER(ctypes.c_double)
     lib.oracle_forward.restype = ctypes.c_int
     lib.oracle_forward.argtypes = [ctypes.c_int] * 8 + [dp] * 12 + [ctypes.c_int]
+    lib.oracle_gdp.restype = ctypes.c_int
+    lib.oracle_gdp.argtypes = [ctypes.c_int] * 6 + [dp] * 8 + [ctypes.c_int]
     lib.oracle_hla.restype = ctypes.c_int
     lib.oracle_hla.argtypes = [ctypes.c_int] * 6 + [ctypes.c_double] + [dp] * 7 + [ctypes.c_int]
     lib.oracle_backward.restype = ctypes.c_int
@@ -177,6 +197,21 @@ def test_hla_pins_catch_planted_mistake(name, tmp_path, monkeypatch):
     monkeypatch.setattr(oracle, "_handle", lib)
     caught = 0
     for call in HLA_PIN_CALLS:
+        try:
+            call()
+        except AssertionError:
+            caught += 1
+    assert caught > 0, f"no pin failed for mutant {name}"
+
+
+@pytest.mark.parametrize("name", sorted(GDP_MUTANTS))
+def test_gdp_pins_catch_planted_mistake(name, tmp_path, monkeypatch):
+    old, new = GDP_MUTANTS[name]
+    lib = _build_mutant(tmp_path, name, old, new, gdp=True)
+    oracle._lib()
+    monkeypatch.setattr(oracle, "_handle", lib)
+    caught = 0
+    for call in GDP_PIN_CALLS:
         try:
             call()
         except AssertionError:
