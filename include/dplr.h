@@ -217,6 +217,21 @@ DPLR_API dplr_status dplr_hla_forward(const dplr_desc* desc, const void* q, cons
                              const float* g, const float* beta, const float* W, float theta, int L,
                              float* o, void* workspace, size_t ws_bytes, void* stream);
 
+/* Gated DeltaProduct-style stacked Householders (HDLA page: research background and the computation table,
+ * GDP with n_h = r_ab = r_kv): per token the gate once, then n_h delta-rule steps with their own key, value and
+ * beta, S <- e^{g_t} S; S <- (I - b_h k_h k_h^T) S + b_h k_h v_h^T (h = 1 .. n_h); o_t = S^T q_t. `desc`: mode
+ * DPLR_GENERIC with r_ab = r_kv = n_h (1 .. 8), dk in {32, 64, 128}. Layouts: q [B,H,T,dk]; k [B,H,T,n_h,dk];
+ * v [B,H,T,n_h,dv] (in_dtype); g [B,H,T] and beta [B,H,T,n_h] fp32; S0 (nullable), S_T (nullable), o as for
+ * dplr_la_forward. The token's exact rank-n_h factors are built in fp32, then the generic-mode forward runs
+ * (dplr_gdp_path names its kernels). Workspace: dplr_gdp_workspace_size(desc) bytes, 256-byte aligned.
+ * Asynchronous on `stream`; allocates nothing. Errors as dplr_la_forward; DPLR_ERR_INVALID_ARG for another mode
+ * or r_ab != r_kv. */
+DPLR_API size_t dplr_gdp_workspace_size(const dplr_desc* desc);
+DPLR_API dplr_status dplr_gdp_forward(const dplr_desc* desc, const void* q, const void* k, const void* v,
+                             const float* g, const float* beta, const float* S0, float* o, float* S_T,
+                             void* workspace, size_t ws_bytes, void* stream);
+DPLR_API const char* dplr_gdp_path(const dplr_desc* desc);
+
 /* Name of the kernel path that dplr_la_forward runs for `desc` (no counterpart in the
  * paper; static storage): "gdn_fused_tcgen05" (GDN, bf16, dk = dv = 128: one fused
  * per-head kernel on the tensor cores), "hdla_tcgen05" (HDLA, bf16, dk = dv = 128: the

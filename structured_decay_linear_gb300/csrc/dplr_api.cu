@@ -145,6 +145,11 @@ dplr_status make_plan(const dplr_desc* d, Plan* pl) {
         p.ws_stages = total;
         p.ws_bytes = total;
     } else {
+        // fp32 stages: a shorter WY block when the block's tiles would not fit one CTA's shared memory
+        while (!p.fused && p.cw > 8 && prep_smem_bytes(p) > 227 * 1024) {
+            p.cw /= 2;
+            p.nb = (d->T + p.cw - 1) / p.cw;
+        }
         const size_t units = (size_t)p.BH * p.nb;
         size_t off = kAlign;   // the first 256 bytes hold the device status word
         p.off_P = off; off = round_up(off + units * (size_t)p.dk * p.dk * sizeof(float));

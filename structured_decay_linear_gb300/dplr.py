@@ -77,6 +77,12 @@ def library() -> ctypes.CDLL:
             lib.dplr_hla_workspace_size.argtypes = [dp, ctypes.c_int]
             lib.dplr_hla_forward.restype = ctypes.c_int
             lib.dplr_hla_forward.argtypes = [dp] + [_vp] * 6 + [ctypes.c_float, ctypes.c_int, _vp, _vp, ctypes.c_size_t, _vp]
+            lib.dplr_gdp_workspace_size.restype = ctypes.c_size_t
+            lib.dplr_gdp_workspace_size.argtypes = [dp]
+            lib.dplr_gdp_forward.restype = ctypes.c_int
+            lib.dplr_gdp_forward.argtypes = [dp] + [_vp] * 8 + [_vp, ctypes.c_size_t, _vp]
+            lib.dplr_gdp_path.restype = ctypes.c_char_p
+            lib.dplr_gdp_path.argtypes = [dp]
             lib.dplr_la_path.restype = ctypes.c_char_p
             lib.dplr_la_path.argtypes = [dp]
             lib.dplr_la_set_wait_limit.restype = None
@@ -158,6 +164,19 @@ def dplr_hla_forward(desc, q, k, v, g, beta, W, theta, L, o, workspace, ws_bytes
     """HLA's query-gated composition of GDN chunk transitions (device pointers; see include/dplr.h)."""
     return int(library().dplr_hla_forward(ctypes.byref(desc), q, k, v, g, beta, W, float(theta), int(L), o, workspace,
                                           ws_bytes, stream))
+
+
+def dplr_gdp_workspace_size(desc: dplr_desc) -> int:
+    return int(library().dplr_gdp_workspace_size(ctypes.byref(desc)))
+
+
+def dplr_gdp_forward(desc, q, k, v, g, beta, S0, o, S_T, workspace, ws_bytes, stream) -> int:
+    """Stacked-Householder (Gated DeltaProduct-style) forward (device pointers; see include/dplr.h)."""
+    return int(library().dplr_gdp_forward(ctypes.byref(desc), q, k, v, g, beta, S0, o, S_T, workspace, ws_bytes, stream))
+
+
+def dplr_gdp_path(desc: dplr_desc) -> str:
+    return library().dplr_gdp_path(ctypes.byref(desc)).decode()
 
 
 def dplr_la_path(desc: dplr_desc) -> str:
@@ -481,3 +500,29 @@ class HLA:
         if st != DPLR_OK:
             raise DplrError(st, "dplr_hla_forward")
         return self.o
+
+
+class GDP:
+    """Prepared stacked-Householder forward (dplr_gdp_forward) with n_h steps per token: owns workspace and outputs."""
+
+    def __init__(self, in_dtype: torch.dtype, B: int, H: int, T: int, dk: int, dv: int, nh: int,
+                 device: Optional[torch.device] = None):
+        self.desc = make_desc("generic", in_dtype, B, H, T, dk, dv, nh, nh)
+        self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        nbytes = dplr_gdp_workspace_size(self.desc)
+        if nbytes == 0:
+            raise DplrError(2, "dplr_gdp_workspace_size")
+        self.ws = torch.empty(nbytes + 256, dtype=torch.uint8, device=self.device)
+        off = (-self.ws.data_ptr()) % 256
+        self.ws_ptr, self.ws_bytes = self.ws.data_ptr() + off, nbytes
+        self.o = torch.empty((B, H, T, dv), dtype=torch.float32, device=self.device)
+        self.S_T = torch.empty((B, H, dk, dv), dtype=torch.float32, device=self.device)
+        self.path = dplr_gdp_path(self.desc)
+
+    def __call__(self, q, k, v, g, beta, S0=None, stream: Optional[torch.cuda.Stream] = None):
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        st = dplr_gdp_forward(self.desc, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S0), _ptr(self.o),
+                              _ptr(self.S_T), self.ws_ptr, self.ws_bytes, s.cuda_stream)
+        if st != DPLR_OK:
+            raise DplrError(st, "dplr_gdp_forward")
+        return self.o, self.S_T
