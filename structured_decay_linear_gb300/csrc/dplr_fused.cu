@@ -33,12 +33,13 @@
 // thread per tensor-memory lane) and one issuing warp run them concurrently:
 //   A  state chain: S' (hi, lo) and e^{G_C} S into tensor memory, then Es~ in place of E;
 //   B  WY build: L and QK~ from D, the triangular inverse, the M tiles;
-//   C  Y^T tiles and the chunk outputs o_t.
-// The issuer queues the MMAs of chunk j in the order E(j), O(j), X(j), then Y(j+1), D(j+2),
-// O~(j) and Z(j+1) = V^T (-M)^T, so the tensor cores run the chain's products as soon as
-// their operands exist and fill the CUDA-core phases of the chain (Es~ while O runs, S'
-// while the rest runs) with the others. The state S^T (lane n, column c) stays in tensor memory as the
-// accumulator of X for the whole sequence.
+//   C  the chunk outputs o_t, then the Y^T tile of the next chunk.
+// Group A issues E(j) and X(j) itself; the issuer queues O(j), D(j+2), O~(j), Y(j+1) and
+// Z(j+1) = V^T (-M)^T, so the tensor cores run the chain's products as soon as their operands
+// exist and fill the CUDA-core phases of the chain (Es~ while O runs, S' while the rest runs)
+// with the others. O~(j) goes before Y(j+1): Y(j+1) waits for the WY build of chunk j+1, and
+// the QK~ buffer that build writes is free only once O~(j-1) has run. The state S^T (lane n,
+// column c) stays in tensor memory as the accumulator of X for the whole sequence.
 //
 // Operand tiles. q, k and v arrive by TMA tensor copies of 64 tokens x 64 features
 // (128-byte rows) in the 128-byte swizzled layout: token t of a half-tile at t*128, its
@@ -511,15 +512,15 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
                 if ((j >= -1 && !wait1(d_free, (j + 1) & 1)) || !wait_kq(j + 2)) { failed = true; break; }
                 mma_D(j + 2);
             }
-            // Y(j+1): its Y^T tile gates E(j+1)
-            if (j >= -1 && next) {
-                if (!wait1(rdy_M, (j + 1) & 1)) { failed = true; break; }
-                mma_Y(j + 1);
-            }
             // O~(j) once Es~(j) is in place (after O(j), in this thread's order)
             if (j >= 0) {
                 if (!wait1(rdy_E, j & 1)) { failed = true; break; }
                 mma_Oes(j);
+            }
+            // Y(j+1), whose Y^T tile gates E(j+1), once its M tiles exist and group C has read Y(j)
+            if (j >= -1 && next) {
+                if (!wait1(rdy_M, (j + 1) & 1) || (j >= 0 && !wait1(rdy_Yt, j & 1))) { failed = true; break; }
+                mma_Y(j + 1);
             }
             // Z(j+1) reuses the E accumulator: after O~(j) (this thread) and X(j) (group A)
             if (j >= -1 && next) {
@@ -745,7 +746,7 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
         }
         if (failed && gt == 0) atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
     } else {
-        // ======================= group C: Y^T tiles and the chunk outputs =======================
+        // ======================= group C: the chunk outputs, then the next Y^T tile =======================
         float graw[4];
         if (warp == 8 && nchunk > 0) load_gates(0, graw);
         auto epi_Y = [&]() {
@@ -774,13 +775,6 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
                 vf[2 * lane + 1] = __expf(g.G1 - a);
                 if (j + 1 < nchunk) load_gates(j + 1, graw);
             }
-            if (j + 1 < nchunk) {   // Y^T of chunk j + 1 (its tile was read by E(j))
-                if (!group_wait(mbar_Y, (j + 1) & 1, kBarC) || !group_wait(mbar_E, j & 1, kBarC)) {
-                    failed = true;
-                    break;
-                }
-                epi_Y();
-            }
             if (!group_wait(mbar_O, j & 1, kBarC)) { failed = true; break; }   // also orders ef
             if (gt == 0) st_release_shared(o_seen, j + 1);
             {   // ---- o_t = ef_t O'_t
@@ -800,6 +794,13 @@ gdn_fused_head_kernel(Plan pl, FusedArgs args, const __grid_constant__ CUtensorM
             fence_before_sync();
             named_sync(kBarC, kGrp);
             if (gt == 0) mbar_arrive(o_free);
+            if (j + 1 < nchunk) {   // Y^T of chunk j + 1 (its tile was read by E(j)); Y(j + 2) waits for it
+                if (!group_wait(mbar_Y, (j + 1) & 1, kBarC) || !group_wait(mbar_E, j & 1, kBarC)) {
+                    failed = true;
+                    break;
+                }
+                epi_Y();
+            }
         }
         if (failed && gt == 0) atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
     }
