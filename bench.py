@@ -343,10 +343,10 @@ def run_ours(args, w):
     flops = flops_per_token(w) * w.B * w.H * w.T
     sbytes = step_bytes(w)
 
-    # end-to-end through the public C ABI with host buffers (pinned): dplr_la_forward_host copies
+    # end-to-end through the public C ABI with host buffers (pinned): dplr_la_forward_host_seq copies
     # every input in, runs the forward and copies o and S_T back, all inside the timed region
-    # (the copies of one group of heads overlap the forwards and copies of the others).
-    fh = sdl.ForwardHost(w.mode, dt, w.B, w.H, w.T, w.dk, w.dv, w.r_ab, w.r_kv, w.chunk, device=dev)
+    # (the sequence in segments: the copies of one segment overlap the forwards and copies of the others).
+    fh = sdl.ForwardHostSeq(w.mode, dt, w.B, w.H, w.T, w.dk, w.dv, w.r_ab, w.r_kv, w.chunk, device=dev)
     o_host, s_host = fh.o, fh.S_T
 
     def e2e_step():
@@ -422,8 +422,8 @@ def run_ours(args, w):
             "cpu_baseline": {"value": cpu_v, "unit": "tokens/s", "cores": cpu_cores, "kind": "oracle",
                              "sample": cpu_sample},
             "e2e": {"value": job_tokens_per_s(toks, world, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "call": "dplr_la_forward_host",
-                    "head_groups": fh.groups, "slots": fh.slots},
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "call": "dplr_la_forward_host_seq",
+                    "segments": fh.segments, "slots": fh.slots},
             "gpu_launches": K * f.kernels,
             "clocks": clocks,
             "wall_s_timed_region": t_wall,

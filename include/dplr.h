@@ -317,6 +317,32 @@ DPLR_API dplr_status dplr_la_forward_host(const dplr_desc* desc,
                                  void* staging, size_t staging_bytes, int groups, int slots,
                                  void* stream);
 
+/* Bytes of device staging area dplr_la_forward_host_seq needs for `desc` split into
+ * `segments` sequence segments with `slots` staging slots (1 <= slots <= 8); 0 if the
+ * descriptor or the counts are invalid. */
+DPLR_API size_t dplr_la_host_seq_workspace_size(const dplr_desc* desc, int segments, int slots);
+
+/* The whole forward with HOST inputs and outputs, as dplr_la_forward_host, but split along the
+ * sequence instead of over the heads (no counterpart in the paper; the state carry it relies on
+ * is the chunkwise recurrence's own, "Householder-Diagonalized Linear Attention", Key design 3).
+ * Segment g holds tokens [g Ts, (g + 1) Ts) of every head, with Ts = `segments`-th of T rounded up
+ * to a multiple of the 64-token chunk (so there are ceil(T / Ts) <= `segments` of them). Each
+ * segment's inputs are copied into one of `slots` staging slots by one 2-D copy per tensor (a row
+ * per head); its dplr_la_forward starts from the state the previous segment's forward left on the
+ * device (S0 for the first) and its outputs are copied back the same way; the final state goes to
+ * S_T. Segments are computed one after another (the state carries), each a short forward, while
+ * the copies of the others run; the result equals dplr_la_forward's up to the rounding of the
+ * chunk maps of the two-stage paths (the fused path gives the same bits). Pointers, staging
+ * (256-byte aligned, at least dplr_la_host_seq_workspace_size bytes), streams, ordering and
+ * errors as dplr_la_forward_host, with `segments` (>= 1) in place of `groups`. */
+DPLR_API dplr_status dplr_la_forward_host_seq(const dplr_desc* desc,
+                                 const void* q, const void* k, const void* v,
+                                 const float* decay, const float* beta,
+                                 const void* A, const void* Bm, const void* K, const void* V,
+                                 const float* S0, float* o, float* S_T,
+                                 void* staging, size_t staging_bytes, int segments, int slots,
+                                 void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -8,6 +8,12 @@
 // while group g computes, group g+1 is being copied in and group g-1 copied out, and
 // forwards of different groups run side by side on different SMs.
 //
+// dplr_la_forward_host_seq splits the sequence instead: segment g holds tokens [g Ts, (g+1) Ts) of every head
+// (Ts a multiple of the 64-token chunk). Its inputs arrive by one 2-D copy per tensor (a row per head), its
+// forward starts from the state the previous segment's forward left in one of two device state buffers,
+// and its outputs go back by 2-D copies. The forwards run one after another on one stream, each a short
+// one (Ts tokens), so the last copy out follows the last copy in by one short forward.
+//
 // The internal streams and events are created once per device (on the first call made
 // while that device is current) and reused; calls on one device are serialised by a lock
 // while they enqueue, and their GPU work runs in call order. Nothing here allocates device
@@ -92,6 +98,57 @@ bool sub_desc(const dplr_desc* desc, int groups, dplr_desc* sub) {
     sub->B = 1;
     sub->H = (int)(bh / groups);
     return dplr_la_check(sub) == DPLR_OK;
+}
+
+// Per-token row bytes of each host tensor, for the 2-D copies of sequence segments.
+struct RowBytes {
+    size_t q, k, v, decay, beta, A, Bm, K, V, o;
+};
+
+RowBytes row_bytes(const dplr_desc& d) {
+    const size_t e = d.in_dtype == DPLR_BF16 ? 2 : 4, dk = (size_t)d.dk, dv = (size_t)d.dv;
+    RowBytes r;
+    std::memset(&r, 0, sizeof(r));
+    r.q = dk * e;
+    r.o = dv * 4;
+    if (d.mode == DPLR_GENERIC) {
+        r.decay = dk * 4;
+        r.A = r.Bm = (size_t)d.r_ab * dk * e;
+        r.K = (size_t)d.r_kv * dk * e;
+        r.V = (size_t)d.r_kv * dv * e;
+    } else {
+        r.k = dk * e;
+        r.v = dv * e;
+        r.decay = d.mode == DPLR_GDN ? 4 : dk * 4;
+        r.beta = 4;
+    }
+    return r;
+}
+
+// Segment length (a multiple of the chunk) and count for `segments` requested segments.
+bool seq_split(const dplr_desc* desc, int segments, int* ts, int* nseg) {
+    if (desc == nullptr || segments < 1) return false;
+    const int C = 64;
+    const int T = desc->T;
+    const int per = (T + segments - 1) / segments;
+    *ts = T == 0 ? C : (per + C - 1) / C * C;
+    *nseg = T == 0 ? 1 : (T + *ts - 1) / *ts;
+    return true;
+}
+
+// Staging bytes of one segment slot (inputs, o and the workspace for ts tokens) and of the two state buffers.
+bool seq_bytes(const dplr_desc* desc, int ts, size_t* slot, size_t* state) {
+    dplr_desc sub = *desc;
+    sub.T = ts;
+    if (dplr_la_check(&sub) != DPLR_OK) return false;
+    const size_t ws = dplr_la_workspace_size(&sub);
+    if (ws == 0) return false;
+    const RowBytes r = row_bytes(*desc);
+    const size_t n = (size_t)desc->B * (size_t)desc->H * (size_t)ts;
+    *slot = up(n * r.q) + up(n * r.k) + up(n * r.v) + up(n * r.decay) + up(n * r.beta) + up(n * r.A) + up(n * r.Bm) +
+            up(n * r.K) + up(n * r.V) + up(n * r.o) + up(ws);
+    *state = up((size_t)desc->B * (size_t)desc->H * (size_t)desc->dk * (size_t)desc->dv * 4);
+    return true;
 }
 
 }  // namespace
@@ -188,6 +245,114 @@ extern "C" dplr_status dplr_la_forward_host(const dplr_desc* desc, const void* q
         DPLR_CK(cudaEventRecord(p.ev_free[si], p.out));
     }
     // the caller's stream resumes once the last copy back is done (it follows every forward)
+    DPLR_CK(cudaEventRecord(p.done, p.out));
+    DPLR_CK(cudaStreamWaitEvent(s, p.done, 0));
+#undef DPLR_CK
+    return DPLR_OK;
+}
+
+extern "C" size_t dplr_la_host_seq_workspace_size(const dplr_desc* desc, int segments, int slots) {
+    using namespace dplr;
+    int ts = 0, nseg = 0;
+    if (slots < 1 || slots > kMaxSlots || dplr_la_check(desc) != DPLR_OK || !seq_split(desc, segments, &ts, &nseg))
+        return 0;
+    size_t slot = 0, state = 0;
+    if (!seq_bytes(desc, ts, &slot, &state)) return 0;
+    return 2 * state + slot * (size_t)(slots < nseg ? slots : nseg);
+}
+
+extern "C" dplr_status dplr_la_forward_host_seq(const dplr_desc* desc, const void* q, const void* k, const void* v,
+                                                const float* decay, const float* beta, const void* A, const void* Bm,
+                                                const void* K, const void* V, const float* S0, float* o, float* S_T,
+                                                void* staging, size_t staging_bytes, int segments, int slots,
+                                                void* stream) {
+    using namespace dplr;
+    dplr_status st = dplr_la_check(desc);
+    if (st != DPLR_OK) return st;
+    int ts = 0, nseg = 0;
+    if (slots < 1 || slots > kMaxSlots || !seq_split(desc, segments, &ts, &nseg)) return DPLR_ERR_INVALID_ARG;
+    const bool generic = desc->mode == DPLR_GENERIC;
+    if (desc->T > 0) {   // (an empty sequence has no token tensors: only S0 -> S_T)
+        if (q == nullptr || decay == nullptr || o == nullptr) return DPLR_ERR_INVALID_ARG;
+        if (generic ? (A == nullptr || Bm == nullptr || (desc->r_kv > 0 && (K == nullptr || V == nullptr)))
+                    : (k == nullptr || v == nullptr || beta == nullptr))
+            return DPLR_ERR_INVALID_ARG;
+    }
+    size_t slot = 0, state = 0;
+    if (!seq_bytes(desc, ts, &slot, &state)) return DPLR_ERR_INVALID_ARG;
+    const int nslot = slots < nseg ? slots : nseg;
+    if (staging == nullptr || (reinterpret_cast<uintptr_t>(staging) % kAlign) != 0 ||
+        staging_bytes < 2 * state + slot * (size_t)nslot)
+        return DPLR_ERR_WORKSPACE;
+
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DPLR_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    HostPipe& p = g_pipe[dev];
+    if (!p.ready && make_pipe(p) != cudaSuccess) return DPLR_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaStream_t comp = p.comp[0];   // the forwards, one after another (each starts from the last one's state)
+
+#define DPLR_CK(x) do { if ((x) != cudaSuccess) return DPLR_ERR_CUDA; } while (0)
+    DPLR_CK(cudaEventRecord(p.start, s));
+    DPLR_CK(cudaStreamWaitEvent(p.in, p.start, 0));
+    DPLR_CK(cudaStreamWaitEvent(p.out, p.start, 0));
+    DPLR_CK(cudaStreamWaitEvent(comp, p.start, 0));
+
+    const RowBytes rb = row_bytes(*desc);
+    const size_t bh = (size_t)desc->B * (size_t)desc->H, T = (size_t)desc->T;
+    unsigned char* st_buf[2] = {static_cast<unsigned char*>(staging), static_cast<unsigned char*>(staging) + state};
+    const auto H2D = cudaMemcpyHostToDevice, D2H = cudaMemcpyDeviceToHost;
+    // state before segment 0: S0 (or none)
+    if (S0) DPLR_CK(cudaMemcpyAsync(st_buf[0], S0, bh * desc->dk * desc->dv * 4, H2D, p.in));
+    for (int gi = 0; gi < nseg; ++gi) {
+        const int si = gi % nslot;
+        const size_t t0 = (size_t)gi * (size_t)ts;
+        const size_t tg = T == 0 ? 0 : (t0 + (size_t)ts <= T ? (size_t)ts : T - t0);
+        dplr_desc sub = *desc;
+        sub.T = (int)tg;
+        unsigned char* base = st_buf[1] + state + (size_t)si * slot;
+        size_t off = 0;
+        const size_t nmax = bh * (size_t)ts;
+        auto carve = [&](size_t row) -> unsigned char* {
+            unsigned char* r = base + off;
+            off += up(nmax * row);
+            return r;
+        };
+        unsigned char *dq = carve(rb.q), *dk_ = carve(rb.k), *dv_ = carve(rb.v), *dd = carve(rb.decay),
+                      *db = carve(rb.beta), *dA = carve(rb.A), *dB = carve(rb.Bm), *dK = carve(rb.K), *dV = carve(rb.V),
+                      *dO = carve(rb.o);
+        unsigned char* dws = base + off;
+        const size_t ws = dplr_la_workspace_size(&sub);   // (at most the full segment's, which the slot holds)
+        if (ws > slot - off) return DPLR_ERR_WORKSPACE;
+        if (generic) dk_ = dv_ = db = nullptr;
+        else dA = dB = dK = dV = nullptr;
+        // tokens [t0, t0 + tg) of every head: one row of tg * row bytes per head
+        auto in_copy = [&](unsigned char* dst, const void* src, size_t row) -> bool {
+            if (!row || src == nullptr || tg == 0) return true;
+            return cudaMemcpy2DAsync(dst, tg * row, static_cast<const unsigned char*>(src) + t0 * row, T * row,
+                                     tg * row, bh, H2D, p.in) == cudaSuccess;
+        };
+        if (gi >= nslot) DPLR_CK(cudaStreamWaitEvent(p.in, p.ev_free[si], 0));   // the slot's outputs are out
+        if (!in_copy(dq, q, rb.q) || !in_copy(dk_, k, rb.k) || !in_copy(dv_, v, rb.v) || !in_copy(dd, decay, rb.decay) ||
+            !in_copy(db, beta, rb.beta) || !in_copy(dA, A, rb.A) || !in_copy(dB, Bm, rb.Bm) || !in_copy(dK, K, rb.K) ||
+            !in_copy(dV, V, rb.V))
+            return DPLR_ERR_CUDA;
+        if (ws) DPLR_CK(cudaMemsetAsync(dws, 0, ws < kAlign ? ws : kAlign, p.in));   // status word
+        DPLR_CK(cudaEventRecord(p.ev_in[si], p.in));
+        DPLR_CK(cudaStreamWaitEvent(comp, p.ev_in[si], 0));
+        const float* s_in = (gi == 0 && S0 == nullptr) ? nullptr : reinterpret_cast<const float*>(st_buf[gi & 1]);
+        float* s_out = reinterpret_cast<float*>(st_buf[(gi + 1) & 1]);
+        st = dplr_la_forward(&sub, dq, dk_, dv_, reinterpret_cast<const float*>(dd), reinterpret_cast<const float*>(db),
+                             dA, dB, dK, dV, s_in, reinterpret_cast<float*>(dO), s_out, dws, ws, comp);
+        if (st != DPLR_OK) return st;
+        DPLR_CK(cudaEventRecord(p.ev_comp[si], comp));
+        DPLR_CK(cudaStreamWaitEvent(p.out, p.ev_comp[si], 0));
+        if (tg) DPLR_CK(cudaMemcpy2DAsync(reinterpret_cast<unsigned char*>(o) + t0 * rb.o, T * rb.o, dO, tg * rb.o,
+                                          tg * rb.o, bh, D2H, p.out));
+        DPLR_CK(cudaEventRecord(p.ev_free[si], p.out));
+    }
+    if (S_T) DPLR_CK(cudaMemcpyAsync(S_T, st_buf[nseg & 1], bh * desc->dk * desc->dv * 4, D2H, p.out));
     DPLR_CK(cudaEventRecord(p.done, p.out));
     DPLR_CK(cudaStreamWaitEvent(s, p.done, 0));
 #undef DPLR_CK

@@ -96,6 +96,11 @@ def library() -> ctypes.CDLL:
             lib.dplr_la_forward_host.restype = ctypes.c_int
             lib.dplr_la_forward_host.argtypes = [dp] + [_vp] * 12 + [_vp, ctypes.c_size_t, ctypes.c_int,
                                                                      ctypes.c_int, _vp]
+            lib.dplr_la_host_seq_workspace_size.restype = ctypes.c_size_t
+            lib.dplr_la_host_seq_workspace_size.argtypes = [dp, ctypes.c_int, ctypes.c_int]
+            lib.dplr_la_forward_host_seq.restype = ctypes.c_int
+            lib.dplr_la_forward_host_seq.argtypes = [dp] + [_vp] * 12 + [_vp, ctypes.c_size_t, ctypes.c_int,
+                                                                         ctypes.c_int, _vp]
             _lib = lib
     return _lib
 
@@ -223,6 +228,17 @@ def dplr_la_forward_host(desc, q, k, v, decay, beta, A, Bm, K, V, S0, o, S_T, st
     """dplr_la_forward with host inputs and outputs; transfers overlapped over groups of heads."""
     return int(library().dplr_la_forward_host(ctypes.byref(desc), q, k, v, decay, beta, A, Bm, K, V, S0, o, S_T,
                                               staging, ctypes.c_size_t(staging_bytes), int(groups), int(slots),
+                                              stream))
+
+def dplr_la_host_seq_workspace_size(desc, segments: int, slots: int) -> int:
+    return int(library().dplr_la_host_seq_workspace_size(ctypes.byref(desc), int(segments), int(slots)))
+
+
+def dplr_la_forward_host_seq(desc, q, k, v, decay, beta, A, Bm, K, V, S0, o, S_T, staging, staging_bytes, segments,
+                         slots, stream) -> int:
+    """dplr_la_forward with host inputs and outputs; transfers overlapped over segments of heads."""
+    return int(library().dplr_la_forward_host_seq(ctypes.byref(desc), q, k, v, decay, beta, A, Bm, K, V, S0, o, S_T,
+                                              staging, ctypes.c_size_t(staging_bytes), int(segments), int(slots),
                                               stream))
 
 
@@ -391,6 +407,52 @@ class ForwardHost:
                                   self.staging_bytes, self.groups, self.slots, s.cuda_stream)
         if st != DPLR_OK:
             raise DplrError(st, "dplr_la_forward_host")
+        return self.o, self.S_T
+
+
+def default_segments(T: int) -> int:
+    """Sequence segments for dplr_la_forward_host_seq: 4 up to 32K tokens, then one per 8K tokens (at most 16).
+    Shorter segments shorten the tail after the last copy in, but each head's row of a 2-D copy shrinks
+    with them, and rows well under ~0.5 MB copy slowly."""
+    return 4 if T < 32768 else max(4, min(16, T // 8192))
+
+
+class ForwardHostSeq:
+    """Prepared forward from host (pinned) tensors through dplr_la_forward_host_seq (the sequence split
+    into segments whose forwards carry the state on the device): owns the device staging area and pinned
+    host outputs, so repeated calls allocate nothing."""
+
+    def __init__(self, mode: str, in_dtype: torch.dtype, B: int, H: int, T: int, dk: int, dv: int,
+                 r_ab: Optional[int] = None, r_kv: Optional[int] = None, chunk: int = 64,
+                 segments: Optional[int] = None, slots: int = 4, device: Optional[torch.device] = None):
+        self.desc = make_desc(mode, in_dtype, B, H, T, dk, dv, r_ab, r_kv, chunk)
+        st = dplr_la_check(self.desc)
+        if st != DPLR_OK:
+            raise DplrError(st, "dplr_la_check")
+        self.segments = segments if segments is not None else default_segments(T)
+        self.slots = slots
+        self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        self.staging_bytes = dplr_la_host_seq_workspace_size(self.desc, self.segments, self.slots)
+        if self.staging_bytes == 0:
+            raise DplrError(DPLR_ERR_INVALID_ARG, "dplr_la_host_seq_workspace_size")
+        self.staging = torch.empty(self.staging_bytes, dtype=torch.uint8, device=self.device)
+        self.o = torch.empty((B, H, T, dv), dtype=torch.float32).pin_memory()
+        self.S_T = torch.empty((B, H, dk, dv), dtype=torch.float32).pin_memory()
+
+    def __call__(self, q, k=None, v=None, decay=None, beta=None, A=None, Bm=None, K=None, V=None, S0=None,
+                 stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+        """Host tensors in, host tensors out (valid once `stream` has been synchronised)."""
+        for name, t in (("q", q), ("k", k), ("v", v), ("decay", decay), ("beta", beta), ("A", A), ("Bm", Bm),
+                        ("K", K), ("V", V), ("S0", S0)):
+            if t is not None and (t.device.type != "cpu" or not t.is_contiguous()):
+                raise ValueError(f"{name} must be a contiguous host tensor")
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        st = dplr_la_forward_host_seq(self.desc, _ptr(q), _ptr(k), _ptr(v), _ptr(decay), _ptr(beta), _ptr(A),
+                                      _ptr(Bm), _ptr(K), _ptr(V), _ptr(S0), _ptr(self.o), _ptr(self.S_T),
+                                      _ptr(self.staging), self.staging_bytes, self.segments, self.slots,
+                                      s.cuda_stream)
+        if st != DPLR_OK:
+            raise DplrError(st, "dplr_la_forward_host_seq")
         return self.o, self.S_T
 
 

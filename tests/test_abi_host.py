@@ -211,6 +211,46 @@ def test_forward_host_rejects_bad_arguments_before_launch(sdl):
     assert call(fake, need, 2, 2, no_k) == sdl.dplr.DPLR_ERR_INVALID_ARG  # k missing
 
 
+def test_host_seq_workspace_size(sdl):
+    """Staging of the sequence-segmented host path: two state buffers plus one slot per segment in flight."""
+    d = sdl.make_desc("gdn", "bf16", 2, 4, 1000, 128, 128)
+    assert sdl.dplr_la_host_seq_workspace_size(d, 0, 2) == 0
+    assert sdl.dplr_la_host_seq_workspace_size(d, 4, 0) == 0
+    assert sdl.dplr_la_host_seq_workspace_size(d, 4, 9) == 0
+    one, two = sdl.dplr_la_host_seq_workspace_size(d, 4, 1), sdl.dplr_la_host_seq_workspace_size(d, 4, 2)
+    state = 2 * 4 * 128 * 128 * 4
+    assert one > 2 * state and two - one == one - 2 * state          # slots add one slot each
+    # 1000 tokens in 4 segments: 256-token segments, so 4 of them; slots beyond that cost nothing
+    assert sdl.dplr_la_host_seq_workspace_size(d, 4, 8) == sdl.dplr_la_host_seq_workspace_size(d, 4, 4)
+    # 3 segments of 1000 tokens round up to 384 tokens each: 3 segments
+    assert sdl.dplr_la_host_seq_workspace_size(d, 3, 8) == sdl.dplr_la_host_seq_workspace_size(d, 3, 3)
+    assert sdl.dplr_la_host_seq_workspace_size(sdl.make_desc("gdn", "bf16", 1, 2, 0, 128, 128), 4, 2) > 0
+
+
+def test_host_path_default_segments(sdl):
+    """Sequence segments of the segmented host path: 4 up to 32K tokens, then one per 8K tokens, at most 16."""
+    ds = sdl.dplr.default_segments
+    assert [ds(t) for t in (64, 4096, 8192, 16384, 32767)] == [4] * 5
+    assert [ds(t) for t in (32768, 65536, 131072, 1 << 20)] == [4, 8, 16, 16]
+
+
+def test_forward_host_seq_rejects_bad_arguments_before_launch(sdl):
+    d = sdl.make_desc("gdn", "bf16", 1, 4, 128, 128, 128)
+    need = sdl.dplr_la_host_seq_workspace_size(d, 2, 2)
+    fake = 1 << 20      # never dereferenced: every check below comes first
+    args = [fake] * 5 + [None] * 4 + [None, fake, None]
+    call = lambda staging, nbytes, segments, slots, a=args: sdl.dplr_la_forward_host_seq(
+        d, *a, staging, nbytes, segments, slots, None)
+    assert call(fake, need, 0, 2) == sdl.dplr.DPLR_ERR_INVALID_ARG        # no segment
+    assert call(fake, need, 2, 0) == sdl.dplr.DPLR_ERR_INVALID_ARG        # no slot
+    assert call(fake, need, 2, 9) == sdl.dplr.DPLR_ERR_INVALID_ARG        # too many slots
+    assert call(fake, 4096, 2, 2) == sdl.dplr.DPLR_ERR_WORKSPACE          # staging too small
+    assert call(fake + 16, need, 2, 2) == sdl.dplr.DPLR_ERR_WORKSPACE     # staging misaligned
+    assert call(None, need, 2, 2) == sdl.dplr.DPLR_ERR_WORKSPACE
+    no_k = [fake, None] + [fake] * 3 + [None] * 4 + [None, fake, None]
+    assert call(fake, need, 2, 2, no_k) == sdl.dplr.DPLR_ERR_INVALID_ARG  # k missing
+
+
 def test_host_path_default_groups(sdl):
     """Head groups of the host-buffer path: at least 16 heads per group on the fused kernel, 32 on
     the two-stage kernels, and at most 16 groups."""
