@@ -34,10 +34,25 @@
 namespace dplr {
 namespace {
 
-template <class T> __device__ __forceinline__ float ld(const T* p, size_t i);
-template <> __device__ __forceinline__ float ld<float>(const float* p, size_t i) { return p[i]; }
-template <> __device__ __forceinline__ float ld<__nv_bfloat16>(const __nv_bfloat16* p, size_t i) {
-    return __bfloat162float(p[i]);
+// 16-byte loads: NV<T> consecutive elements from p + i (16-byte aligned: every row of the inputs is a
+// multiple of 32 elements and every pointer is 16-byte aligned), widened to fp32; zeros when !ok
+// (the padding tokens of a ragged last block).
+template <class T> constexpr int NV = 16 / sizeof(T);
+template <class T> __device__ __forceinline__ void ld16(const T* p, size_t i, bool ok, float (&x)[NV<T>]);
+template <> __device__ __forceinline__ void ld16<float>(const float* p, size_t i, bool ok, float (&x)[4]) {
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (ok) v = *reinterpret_cast<const float4*>(p + i);
+    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+}
+template <> __device__ __forceinline__ void ld16<__nv_bfloat16>(const __nv_bfloat16* p, size_t i, bool ok, float (&x)[8]) {
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (ok) v = *reinterpret_cast<const uint4*>(p + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        x[2 * e] = __uint_as_float(w[e] << 16);
+        x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+    }
 }
 
 // Block-wide fp32 products on shared-memory tiles, one 4 x 4 tile of C per thread per step,
@@ -225,24 +240,35 @@ chunk_maps_kernel(Plan pl, ChunkMapArgs args) {
     auto Gx = [&](int t, int c) { return t > 0 ? Gi(t - 1, c) : 0.f; };
     auto anc = [&](int c) { return 0.5f * G[(cw - 1) * dkg + (MODE == DPLR_GDN ? 0 : c)]; };
     const IT* qp = static_cast<const IT*>(args.q);
-    for (int i = tid; i < cw * dk; i += nth) {
-        const int t = i / dk, c = i % dk;
-        const float x = (t0 + t < T) ? ld(qp, (tok0 + t) * dk + c) : 0.f;
-        Qt[t * ldk + c] = x * expf(Gi(t, c) - anc(c));
+    constexpr int V = NV<IT>;   // elements per 16-byte load
+    for (int i = tid; i < cw * dk / V; i += nth) {
+        const int t = i * V / dk, c0 = i * V % dk;
+        float x[V];
+        ld16(qp, (tok0 + t) * dk + c0, t0 + t < T, x);
+#pragma unroll
+        for (int e = 0; e < V; ++e) Qt[t * ldk + c0 + e] = x[e] * expf(Gi(t, c0 + e) - anc(c0 + e));
     }
     if (MODE == DPLR_GDN) {
         const IT* kp = static_cast<const IT*>(args.k);
         const IT* vp = static_cast<const IT*>(args.v);
-        for (int i = tid; i < cw * dk; i += nth) {
-            const int t = i / dk, c = i % dk;
-            const float kk = (t0 + t < T) ? ld(kp, (tok0 + t) * dk + c) : 0.f;
-            const float gp = Gi(t, c) - anc(c);
-            At[t * ldk + c] = expf(-gp) * bet[t] * kk;   // A = beta k
-            Bt[t * ldk + c] = expf(gp) * kk;             // e^{G_{t-1}} B_t with B = e^{g} k
+        for (int i = tid; i < cw * dk / V; i += nth) {
+            const int t = i * V / dk, c0 = i * V % dk;
+            float kk[V];
+            ld16(kp, (tok0 + t) * dk + c0, t0 + t < T, kk);
+#pragma unroll
+            for (int e = 0; e < V; ++e) {
+                const int c = c0 + e;
+                const float gp = Gi(t, c) - anc(c);
+                At[t * ldk + c] = expf(-gp) * bet[t] * kk[e];   // A = beta k
+                Bt[t * ldk + c] = expf(gp) * kk[e];             // e^{G_{t-1}} B_t with B = e^{g} k
+            }
         }
-        for (int i = tid; i < cw * dv; i += nth) {
-            const int t = i / dv, n = i % dv;
-            Z[i] = (t0 + t < T) ? -ld(vp, (tok0 + t) * dv + n) : 0.f;   // -W, W = v
+        for (int i = tid; i < cw * dv / V; i += nth) {
+            const int t = i * V / dv, n0 = i * V % dv;
+            float x[V];
+            ld16(vp, (tok0 + t) * dv + n0, t0 + t < T, x);
+#pragma unroll
+            for (int e = 0; e < V; ++e) Z[t * dv + n0 + e] = -x[e];   // -W, W = v
         }
     } else if (MODE == DPLR_HDLA) {
         const IT* kp = static_cast<const IT*>(args.k);
@@ -253,50 +279,76 @@ chunk_maps_kernel(Plan pl, ChunkMapArgs args) {
         for (int t = warp; t < cw; t += nwarp) {
             float s = 0.f;
             if (t0 + t < T)
-                for (int c = lane; c < dk; c += 32) {
-                    const float kk = ld(kp, (tok0 + t) * dk + c);
-                    s += kk * kk * expf(lg[t * dk + c]);
+                for (int c0 = lane * V; c0 < dk; c0 += 32 * V) {
+                    float kk[V];
+                    ld16(kp, (tok0 + t) * dk + c0, true, kk);
+#pragma unroll
+                    for (int e = 0; e < V; ++e) s += kk[e] * kk[e] * expf(lg[t * dk + c0 + e]);
                 }
             for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
             if (lane == 0) cdot[t] = s;
         }
         __syncthreads();
-        for (int i = tid; i < cw * dk; i += nth) {
-            const int t = i / dk, c = i % dk;
-            const float kk = (t0 + t < T) ? ld(kp, (tok0 + t) * dk + c) : 0.f;
-            const float u = expf(lg[i]) * kk;             // Lambda k
+        for (int i = tid; i < cw * dk / V; i += nth) {
+            const int t = i * V / dk, c0 = i * V % dk;
+            float kk[V];
+            ld16(kp, (tok0 + t) * dk + c0, t0 + t < T, kk);
             const float b = bet[t];
-            const float ei = expf(-(Gi(t, c) - anc(c)));  // e^{-G'_t}
-            const float ex = expf(Gx(t, c) - anc(c));     // e^{G'_{t-1}}
-            At[(2 * t) * ldk + c] = ei * kk;
-            At[(2 * t + 1) * ldk + c] = ei * u;
-            Bt[(2 * t) * ldk + c] = ex * (b * u - b * b * cdot[t] * kk);
-            Bt[(2 * t + 1) * ldk + c] = ex * b * kk;
+#pragma unroll
+            for (int e = 0; e < V; ++e) {
+                const int c = c0 + e;
+                const float u = expf(lg[t * dk + c]) * kk[e];   // Lambda k
+                const float ei = expf(-(Gi(t, c) - anc(c)));     // e^{-G'_t}
+                const float ex = expf(Gx(t, c) - anc(c));        // e^{G'_{t-1}}
+                At[(2 * t) * ldk + c] = ei * kk[e];
+                At[(2 * t + 1) * ldk + c] = ei * u;
+                Bt[(2 * t) * ldk + c] = ex * (b * u - b * b * cdot[t] * kk[e]);
+                Bt[(2 * t + 1) * ldk + c] = ex * b * kk[e];
+            }
         }
-        for (int i = tid; i < cw * dv; i += nth) {
-            const int t = i / dv, n = i % dv;
-            Z[(2 * t) * dv + n] = (t0 + t < T) ? -bet[t] * ld(vp, (tok0 + t) * dv + n) : 0.f;
-            Z[(2 * t + 1) * dv + n] = 0.f;
+        for (int i = tid; i < cw * dv / V; i += nth) {
+            const int t = i * V / dv, n0 = i * V % dv;
+            float x[V];
+            ld16(vp, (tok0 + t) * dv + n0, t0 + t < T, x);
+#pragma unroll
+            for (int e = 0; e < V; ++e) {
+                Z[(2 * t) * dv + n0 + e] = -bet[t] * x[e];
+                Z[(2 * t + 1) * dv + n0 + e] = 0.f;
+            }
         }
     } else {
         const IT* Ap = static_cast<const IT*>(args.A);
         const IT* Bp = static_cast<const IT*>(args.Bm);
         const IT* Kp = static_cast<const IT*>(args.K);
         const IT* Vp = static_cast<const IT*>(args.V);
-        for (int i = tid; i < cr * dk; i += nth) {
-            const int row = i / dk, c = i % dk, t = row / R, j = row % R;
+        for (int i = tid; i < cr * dk / V; i += nth) {
+            const int row = i * V / dk, c0 = i * V % dk, t = row / R, j = row % R;
             const bool ok = t0 + t < T;
-            const size_t src = ((tok0 + t) * R + j) * dk + c;
-            At[row * ldk + c] = ok ? expf(-(Gi(t, c) - anc(c))) * ld(Ap, src) : 0.f;
-            Bt[row * ldk + c] = ok ? expf(Gx(t, c) - anc(c)) * ld(Bp, src) : 0.f;
+            const size_t src = ((tok0 + t) * R + j) * dk + c0;
+            float a[V], b[V];
+            ld16(Ap, src, ok, a);
+            ld16(Bp, src, ok, b);
+#pragma unroll
+            for (int e = 0; e < V; ++e) {
+                const int c = c0 + e;
+                At[row * ldk + c] = ok ? expf(-(Gi(t, c) - anc(c))) * a[e] : 0.f;
+                Bt[row * ldk + c] = ok ? expf(Gx(t, c) - anc(c)) * b[e] : 0.f;
+            }
         }
-        for (int i = tid; i < cp * dk; i += nth) {
-            const int row = i / dk, c = i % dk, t = row / Pd, l = row % Pd;
-            Kt[row * ldk + c] = (t0 + t < T) ? expf(-(Gi(t, c) - anc(c))) * ld(Kp, ((tok0 + t) * P + l) * dk + c) : 0.f;
+        for (int i = tid; i < cp * dk / V; i += nth) {
+            const int row = i * V / dk, c0 = i * V % dk, t = row / Pd, l = row % Pd;
+            const bool ok = t0 + t < T;
+            float x[V];
+            ld16(Kp, ((tok0 + t) * P + l) * dk + c0, ok, x);
+#pragma unroll
+            for (int e = 0; e < V; ++e) Kt[row * ldk + c0 + e] = ok ? expf(-(Gi(t, c0 + e) - anc(c0 + e))) * x[e] : 0.f;
         }
-        for (int i = tid; i < cp * dv; i += nth) {
-            const int row = i / dv, n = i % dv, t = row / Pd, l = row % Pd;
-            Vs[i] = (t0 + t < T) ? ld(Vp, ((tok0 + t) * P + l) * dv + n) : 0.f;
+        for (int i = tid; i < cp * dv / V; i += nth) {
+            const int row = i * V / dv, n0 = i * V % dv, t = row / Pd, l = row % Pd;
+            float x[V];
+            ld16(Vp, ((tok0 + t) * P + l) * dv + n0, t0 + t < T, x);
+#pragma unroll
+            for (int e = 0; e < V; ++e) Vs[row * dv + n0 + e] = x[e];
         }
     }
     __syncthreads();
