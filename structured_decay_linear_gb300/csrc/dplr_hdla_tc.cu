@@ -33,10 +33,11 @@
 // Stage 2, hdla_chain_kernel: one CTA per (head, 32 state columns). It walks the chunks in order,
 // S_j = P_j S_{j-1} + c_j with P_j as one bf16 term and S_{j-1} as bf16 hi + lo (the decay makes
 // P_j contracting, so its rounding does not accumulate from chunk to chunk), and o_t += Q'_t S_{j-1}
-// with both operands split into bf16 hi + lo. The kernel's warps take roles: a copy warp stages each chunk's
-// maps by TMA (after an L2 prefetch four chunks earlier), an issuing warp starts a chunk's products as soon as
-// S_{j-1} is in place, and four warps update the state and write the outputs while the tensor cores work.
-// The state stays in registers in fp32; P_j and Q'_j arrive by TMA two chunks ahead.
+// with both operands split into bf16 hi + lo. The kernel's warps take roles: two copy warps stage each chunk's
+// maps by TMA (P_j and c_j, and Q'_j and O_j, after an L2 prefetch four chunks earlier), an issuing warp starts
+// the chain's product of chunk j as soon as S_{j-1} is in place and then the output product of chunk j - 1, and
+// four warps update the state and, a chunk behind, write the outputs while the tensor cores work. The state
+// stays in registers in fp32; the maps arrive by TMA up to two chunks ahead.
 //
 // Every wait is bounded by Plan::wait_cycles; a wait that gives up sets DPLR_ERR_TIMEOUT in the
 // status word and the kernel drains its own copies and products before it frees tensor memory.
@@ -616,23 +617,29 @@ hdla_chunk_kernel(Plan pl, K1Args args, const __grid_constant__ CUtensorMap tm_q
 // ================================================================================================
 
 constexpr int NV = 32;       // state columns per chain CTA
-constexpr int K2T = 192;     // warps 0-3: the state (thread = key channel = tensor-memory lane); 4: copies; 5: MMAs
-constexpr int K2S = 2;       // stages of the per-chunk maps in shared memory
+constexpr int K2T = 224;     // warps 0-3: the state (thread = key channel = tensor-memory lane); 4: issuer;
+                             // 5: copies of P_j and c_j; 6: copies of Q'_j and O_j
 constexpr int K2PF = 4;      // chunks between the L2 prefetch of a chunk's maps and their copy into shared memory
+constexpr int K2SB = 3;      // state tile buffers: S_{j-1} is read by P(j) and by Q'(j), which runs after P(j+1)
 
-// Shared memory of the chain kernel. A stage holds one chunk's P_j (bf16 [128][128]), Q'_j (bf16 [128][128], hi/lo
-// rows interleaved by 16), this CTA's columns of c_j (fp32 [128][32]) and of the chunk-local outputs O_j
-// (fp32 [64][32]), all in the TMA's 128-byte swizzled layout.
+// Shared memory of the chain kernel, all TMA tiles in the 128-byte swizzled layout:
+// - two stages of the chain's maps: P_j (bf16 [128][128]) and this CTA's columns of c_j (fp32 [128][32]);
+// - two stages of the output maps: Q'_j (bf16 [128][128], hi/lo rows interleaved by 16) and this CTA's
+//   columns of the chunk-local outputs O_j (fp32 [64][32]);
+// - three buffers of S_{j-1} as bf16 hi and lo core-matrix tiles.
 struct K2Smem {
-    static constexpr int STAGE = 32768 + 32768 + 16384 + 8192;
-    static constexpr int P_ = 0, Q_ = 32768, C_ = 65536, O_ = 81920;
-    static constexpr int SB = K2S * STAGE;        // S_{j-1} hi: bf16 [128][NV] core-matrix tiles, two buffers
+    static constexpr int PC = 32768 + 16384, P_ = 0, C_ = 32768;   // a chain stage
+    static constexpr int QO = 32768 + 8192, Q_ = 0, O_ = 32768;    // an output stage
+    static constexpr int PCS = 0;
+    static constexpr int QOS = PCS + 2 * PC;
+    static constexpr int SB = QOS + 2 * QO;       // S_{j-1} hi: bf16 [128][NV] core-matrix tiles, K2SB buffers
     static constexpr int SBB = 128 * NV * 2;
-    static constexpr int SL = SB + 2 * SBB;       // S_{j-1} lo, two buffers
-    static constexpr int BAR = SL + 2 * SBB;
+    static constexpr int SL = SB + K2SB * SBB;    // S_{j-1} lo
+    static constexpr int BAR = SL + K2SB * SBB;
     static constexpr int TOTAL = BAR + 128;
 };
 static_assert(K2Smem::TOTAL <= 227 * 1024, "shared memory budget");
+static_assert(K2Smem::QOS % 1024 == 0 && K2Smem::PC % 1024 == 0 && K2Smem::QO % 1024 == 0, "swizzled tiles");
 
 struct K2Args {
     const float* S0; float* o; float* ST; int* status;
@@ -649,13 +656,15 @@ hdla_chain_kernel(Plan pl, K2Args args, const __grid_constant__ CUtensorMap tm_P
         return;
     }
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::BAR);
-    uint64_t* full = bars + 0;            // [K2S] a chunk's maps landed
-    uint64_t* freed = bars + K2S;         // [K2S] the stage was read by both products and by the state warps (2 arrivals)
-    uint64_t* mS = bars + 2 * K2S;        // the chain product of the chunk (issuer -> state warps)
-    uint64_t* mO = bars + 2 * K2S + 1;    // [2] the output product of the chunks using accumulator j % 2
-    uint64_t* ready = bars + 2 * K2S + 3; // S_{j-1} tiles written (4 arrivals, one per state warp; -> issuer)
-    uint64_t* drain = bars + 2 * K2S + 4;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * K2S + 5);
+    uint64_t* fullPC = bars + 0;    // [2] chunk j's P_j and c_j landed in stage j % 2
+    uint64_t* freedPC = bars + 2;   // [2] P(j) done (issuer) and c_j read (each state warp): 5 arrivals
+    uint64_t* fullQO = bars + 4;    // [2] chunk j's Q'_j and O_j landed in stage j % 2
+    uint64_t* freedQO = bars + 6;   // [2] Q'(j) done (issuer) and O_j read (each state warp): 5 arrivals
+    uint64_t* mS = bars + 8;        // P(j), the chain product of chunk j (issuer -> state warps)
+    uint64_t* mO = bars + 9;        // [2] Q'(j), the output product of the chunks using accumulator j % 2
+    uint64_t* ready = bars + 11;    // S_{j-1} tiles written (4 arrivals, one per state warp; -> issuer)
+    uint64_t* drain = bars + 12;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 13);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int T = pl.T;
@@ -667,9 +676,11 @@ hdla_chain_kernel(Plan pl, K2Args args, const __grid_constant__ CUtensorMap tm_P
     const long long wl = pl.wait_cycles;
 
     if (tid == 0) {
-        for (int u = 0; u < K2S; ++u) {
-            mbar_init(&full[u], 1);
-            mbar_init(&freed[u], 2);
+        for (int u = 0; u < 2; ++u) {
+            mbar_init(&fullPC[u], 1);
+            mbar_init(&freedPC[u], 5);
+            mbar_init(&fullQO[u], 1);
+            mbar_init(&freedQO[u], 5);
         }
         mbar_init(mS, 1);
         mbar_init(&mO[0], 1);
@@ -684,73 +695,92 @@ hdla_chain_kernel(Plan pl, K2Args args, const __grid_constant__ CUtensorMap tm_P
     fence_after_sync();
     const uint32_t tmem = *tmem_holder;   // columns 0-31: P_j S_{j-1}; 32-95: two output accumulators
     bool failed = false;
+    auto unit_row = [&](int jj) { return static_cast<int>(((size_t)jj * pl.BH + bh) * HD); };
 
-    if (warp == 4) {
-        // ---- copies. Chunk j's maps go to stage j % K2S once the stage's previous chunk is done with; the maps of
-        // chunk j + K2PF are prefetched into L2 at the same time.
-        auto unit_of = [&](int jj) { return (size_t)jj * pl.BH + bh; };
+    if (warp == 5 || warp == 6) {
+        // ---- copies: warp 5 the chain's maps (P_j, c_j), warp 6 the output maps (Q'_j, O_j). Chunk j goes to
+        // stage j % 2 once chunk j - 2 is done with it; chunk j + K2PF is prefetched into L2 at the same time.
+        const bool chain = warp == 5;
+        uint64_t* full = chain ? fullPC : fullQO;
+        uint64_t* freed = chain ? freedPC : freedQO;
         auto prefetch = [&](int jj) {
-            const int y = static_cast<int>(unit_of(jj) * HD);
-            prefetch_l2_tile(&tm_P, 0, y);
-            prefetch_l2_tile(&tm_P, 64, y);
-            prefetch_l2_tile(&tm_Q, 0, y);
-            prefetch_l2_tile(&tm_Q, 64, y);
-            prefetch_l2_tile(&tm_C, n0, y);
-            prefetch_l2_tile(&tm_O, n0, static_cast<int>(bh * T + (size_t)jj * HCK));
+            const int y = unit_row(jj);
+            if (chain) {
+                prefetch_l2_tile(&tm_P, 0, y);
+                prefetch_l2_tile(&tm_P, 64, y);
+                prefetch_l2_tile(&tm_C, n0, y);
+            } else {
+                prefetch_l2_tile(&tm_Q, 0, y);
+                prefetch_l2_tile(&tm_Q, 64, y);
+                prefetch_l2_tile(&tm_O, n0, static_cast<int>(bh * T + (size_t)jj * HCK));
+            }
         };
         int last = -1;
         if (lane == 0)
             for (int jj = 0; jj < K2PF && jj < NC; ++jj) prefetch(jj);
         for (int j = 0; j < NC && lane == 0; ++j) {
-            const int u = j % K2S;
-            if (j >= K2S && !mbar_wait(&freed[u], ((j - K2S) / K2S) & 1, wl)) { failed = true; break; }
+            const int u = j & 1;
+            if (j >= 2 && !mbar_wait(&freed[u], ((j - 2) >> 1) & 1, wl)) { failed = true; break; }
             if (j + K2PF < NC) prefetch(j + K2PF);
-            mbar_expect_tx(&full[u], S::STAGE);
-            const int y = static_cast<int>(unit_of(j) * HD);
-            unsigned char* st = smem + u * S::STAGE;
-            for (int h = 0; h < 2; ++h) {
-                tma_load_2d(st + S::P_ + h * 16384, &tm_P, 64 * h, y, &full[u]);
-                tma_load_2d(st + S::Q_ + h * 16384, &tm_Q, 64 * h, y, &full[u]);
+            const int y = unit_row(j);
+            if (chain) {
+                unsigned char* st = smem + S::PCS + u * S::PC;
+                mbar_expect_tx(&full[u], S::PC);
+                tma_load_2d(st + S::P_, &tm_P, 0, y, &full[u]);
+                tma_load_2d(st + S::P_ + 16384, &tm_P, 64, y, &full[u]);
+                tma_load_2d(st + S::C_, &tm_C, n0, y, &full[u]);
+            } else {
+                unsigned char* st = smem + S::QOS + u * S::QO;
+                mbar_expect_tx(&full[u], S::QO);
+                tma_load_2d(st + S::Q_, &tm_Q, 0, y, &full[u]);
+                tma_load_2d(st + S::Q_ + 16384, &tm_Q, 64, y, &full[u]);
+                // rows past the end of the sequence read the next head's rows (or zeros past the tensor): unused
+                tma_load_2d(st + S::O_, &tm_O, n0, static_cast<int>(bh * T + (size_t)j * HCK), &full[u]);
             }
-            tma_load_2d(st + S::C_, &tm_C, n0, y, &full[u]);
-            // rows past the end of the sequence read the next head's rows (or zeros past the tensor): unused
-            tma_load_2d(st + S::O_, &tm_O, n0, static_cast<int>(bh * T + (size_t)j * HCK), &full[u]);
             last = j;
         }
         if (failed) {   // (lane 0) wait for the copies in flight before leaving
             atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
-            for (int jj = last - K2S + 1; jj <= last; ++jj)
-                if (jj >= 0) mbar_wait(&full[jj % K2S], (jj / K2S) & 1, 400000000LL);
+            for (int jj = last - 1; jj <= last; ++jj)
+                if (jj >= 0) mbar_wait(&full[jj & 1], (jj >> 1) & 1, 400000000LL);
         }
         __syncwarp();
-    } else if (warp == 5) {
-        // ---- the products of chunk j, issued by lane 0 once S_{j-1} is in place and the maps have landed:
-        // P_j (S_hi + S_lo) into columns 0-31, then [Q'_hi; Q'_lo] (S_hi + S_lo) into accumulator j % 2
+    } else if (warp == 4) {
+        // ---- the products, issued by lane 0: P(j) = P_j (S_hi + S_lo) into columns 0-31 as soon as S_{j-1} is in
+        // place, then Q'(j-1) = [Q'_hi; Q'_lo] (S_hi + S_lo) of the previous chunk into accumulator (j - 1) % 2. The
+        // chain's product never waits behind the output product of its own chunk. (A second issuing warp for the
+        // output products, so that P(j+1) need not wait for the issue of Q'(j), was slower: the two share the
+        // tensor pipe.)
         const uint32_t idS = idesc_bf16(128, NV, false, true);
-        for (int j = 0; j < NC && lane == 0; ++j) {
-            const int u = j % K2S;
-            if (!mbar_wait(ready, j & 1, wl) || !mbar_wait(&full[u], (j / K2S) & 1, wl)) { failed = true; break; }
+        auto products = [&](uint32_t d, uint64_t a, int buf) {
+            const uint64_t bH = smem_desc(sb + S::SB + buf * S::SBB, (NV / 8) * 128, 128);
+            const uint64_t bL = smem_desc(sb + S::SL + buf * S::SBB, (NV / 8) * 128, 128);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t ao = (kk >> 2) * 16384 + (kk & 3) * 32, bo = kk * 2 * (NV / 8) * 128;
+                mma_bf16(d, dadd(a, ao), dadd(bH, bo), idS, kk > 0);
+                mma_bf16(d, dadd(a, ao), dadd(bL, bo), idS, 1u);
+            }
+        };
+        auto output_product = [&](int jj) -> bool {   // Q'(jj), from S_{jj-1} in buffer jj % 3
+            const int u = jj & 1;
+            if (!mbar_wait(&fullQO[u], (jj >> 1) & 1, wl)) return false;
             fence_after_sync();
-            const uint64_t aS = smem_desc_sw128(sb + u * S::STAGE + S::P_, 16, 1024);
-            const uint64_t aO = smem_desc_sw128(sb + u * S::STAGE + S::Q_, 16, 1024);
-            const uint64_t bH = smem_desc(sb + S::SB + (j & 1) * S::SBB, (NV / 8) * 128, 128);
-            const uint64_t bL = smem_desc(sb + S::SL + (j & 1) * S::SBB, (NV / 8) * 128, 128);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t ao = (kk >> 2) * 16384 + (kk & 3) * 32, bo = kk * 2 * (NV / 8) * 128;
-                mma_bf16(tmem, dadd(aS, ao), dadd(bH, bo), idS, kk > 0);
-                mma_bf16(tmem, dadd(aS, ao), dadd(bL, bo), idS, 1u);
-            }
+            products(tmem + 32 + 32 * u, smem_desc_sw128(sb + S::QOS + u * S::QO + S::Q_, 16, 1024), jj % K2SB);
+            mma_commit(&mO[u]);
+            mma_commit(&freedQO[u]);
+            return true;
+        };
+        for (int j = 0; j < NC && lane == 0; ++j) {
+            const int u = j & 1;
+            if (!mbar_wait(ready, j & 1, wl) || !mbar_wait(&fullPC[u], (j >> 1) & 1, wl)) { failed = true; break; }
+            fence_after_sync();
+            products(tmem, smem_desc_sw128(sb + S::PCS + u * S::PC + S::P_, 16, 1024), j % K2SB);
             mma_commit(mS);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t ao = (kk >> 2) * 16384 + (kk & 3) * 32, bo = kk * 2 * (NV / 8) * 128;
-                mma_bf16(tmem + 32 + 32 * (j & 1), dadd(aO, ao), dadd(bH, bo), idS, kk > 0);
-                mma_bf16(tmem + 32 + 32 * (j & 1), dadd(aO, ao), dadd(bL, bo), idS, 1u);
-            }
-            mma_commit(&mO[j & 1]);
-            mma_commit(&freed[u]);
+            mma_commit(&freedPC[u]);
+            if (j >= 1 && !output_product(j - 1)) { failed = true; break; }
         }
+        if (lane == 0 && !failed && NC > 0 && !output_product(NC - 1)) failed = true;
         if (failed) {   // (lane 0) no product may outlive the tensor memory
             atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
             mma_commit(drain);
@@ -784,20 +814,50 @@ hdla_chain_kernel(Plan pl, K2Args args, const __grid_constant__ CUtensorMap tm_P
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             return !named_sync_or(1, 128, !ok);
         };
-        // output rows: warp g, lane l holds token t = 16 g + (l % 16) and writes columns 16 (l / 16) .. + 15
+        // o_t = O_t + Q'_t S_{jj-1} for chunk jj: a token's hi and lo partial outputs sit in lanes l and l + 16;
+        // warp g, lane l holds token t = 16 g + (l % 16) and writes columns 16 (l / 16) .. + 15
         const int tok = 16 * warp + (lane & 15), cseg = 16 * (lane >> 4);
+        auto outputs = [&](int jj) -> bool {
+            const int u = jj & 1;
+            if (!wait_all(&mO[u], (jj >> 1) & 1, &fullQO[u], (jj >> 1) & 1)) return false;
+            fence_after_sync();
+            const uint32_t stg = sb + S::QOS + u * S::QO;
+            float x[32];
+            tmem_ld32(tmem + lane_base + 32 + 32 * u, x);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) x[e] += __shfl_xor_sync(0xffffffffu, x[e], 16);
+            const int valid = min(HCK, T - jj * HCK);
+            if (tok < valid) {
+                const bool upper = lane >= 16;   // (selects keep x in registers)
+                float4* orow = reinterpret_cast<float4*>(args.o + (bh * (size_t)T + (size_t)jj * HCK + tok) * HD + n0 + cseg);
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    float4 ol;
+                    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(ol.x), "=f"(ol.y), "=f"(ol.z), "=f"(ol.w)
+                                 : "r"(stg + S::O_ + swz(tok, 4 * (lane >> 4) + q4)));
+                    orow[q4] = make_float4(ol.x + (upper ? x[16 + 4 * q4] : x[4 * q4]),
+                                           ol.y + (upper ? x[17 + 4 * q4] : x[4 * q4 + 1]),
+                                           ol.z + (upper ? x[18 + 4 * q4] : x[4 * q4 + 2]),
+                                           ol.w + (upper ? x[19 + 4 * q4] : x[4 * q4 + 3]));
+                }
+            }
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&freedQO[u]);   // this warp is done with O_jj and the accumulator
+            return true;
+        };
         write_state(0);
         fence_async_smem();
         fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(ready);
         for (int j = 0; j < NC; ++j) {
-            const int u = j % K2S;
-            const uint32_t stg = sb + u * S::STAGE;
+            const int u = j & 1;
             // S_j = P_j S_{j-1} + c_j
-            if (!wait_all(mS, j & 1, &full[u], (j / K2S) & 1)) { failed = true; break; }
+            if (!wait_all(mS, j & 1, &fullPC[u], (j >> 1) & 1)) { failed = true; break; }
             fence_after_sync();
             {
+                const uint32_t stg = sb + S::PCS + u * S::PC;
                 float x[32];
                 tmem_ld32(tmem + lane_base, x);
 #pragma unroll
@@ -811,41 +871,22 @@ hdla_chain_kernel(Plan pl, K2Args args, const __grid_constant__ CUtensorMap tm_P
                     st[4 * ch + 3] = x[4 * ch + 3] + c4.w;
                 }
             }
+            // buffer (j + 1) % 3 was last read by Q'(j - 2), which the issuer queued before P(j) (and which
+            // outputs(j - 2) saw complete)
             if (j + 1 < NC) {
-                write_state((j + 1) & 1);
+                write_state((j + 1) % K2SB);
                 fence_async_smem();
             }
             fence_before_sync();
             __syncwarp();
-            if (lane == 0 && j + 1 < NC) mbar_arrive(ready);
-            // o_t = O_t + Q'_t S_{j-1}: a token's hi and lo partial outputs sit in lanes l and l + 16
-            if (!wait_all(&mO[j & 1], (j >> 1) & 1, nullptr, 0)) { failed = true; break; }
-            fence_after_sync();
-            {
-                float x[32];
-                tmem_ld32(tmem + lane_base + 32 + 32 * (j & 1), x);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) x[e] += __shfl_xor_sync(0xffffffffu, x[e], 16);
-                const int valid = min(HCK, T - j * HCK);
-                if (tok < valid) {
-                    const bool upper = lane >= 16;   // (selects keep x in registers)
-                    float4* orow = reinterpret_cast<float4*>(args.o + (bh * (size_t)T + (size_t)j * HCK + tok) * HD + n0 + cseg);
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        float4 ol;
-                        asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(ol.x), "=f"(ol.y), "=f"(ol.z), "=f"(ol.w)
-                                     : "r"(stg + S::O_ + swz(tok, 4 * (lane >> 4) + q4)));
-                        orow[q4] = make_float4(ol.x + (upper ? x[16 + 4 * q4] : x[4 * q4]),
-                                               ol.y + (upper ? x[17 + 4 * q4] : x[4 * q4 + 1]),
-                                               ol.z + (upper ? x[18 + 4 * q4] : x[4 * q4 + 2]),
-                                               ol.w + (upper ? x[19 + 4 * q4] : x[4 * q4 + 3]));
-                    }
-                }
+            if (lane == 0) {
+                if (j + 1 < NC) mbar_arrive(ready);
+                mbar_arrive(&freedPC[u]);   // this warp is done with c_j and with the chain accumulator
             }
-            fence_before_sync();
-            named_sync(1, 128);   // every state warp is done with the stage's c_j and O_j
-            if (tid == 0) mbar_arrive(&freed[u]);
+            // the outputs of the previous chunk, whose product the issuer queued after P(j)
+            if (j >= 1 && !outputs(j - 1)) { failed = true; break; }
         }
+        if (!failed && NC > 0 && !outputs(NC - 1)) failed = true;
         if (!failed && args.ST) {
             float* dst = args.ST + (bh * HD + i) * HD + n0;
 #pragma unroll
