@@ -610,8 +610,10 @@ def run_hla(args):
     print(json.dumps({"mode": "hla", "workload": f"hla_gdn_bf16_b1h{H}_t{T}_d128_L{L}", "steps": K, "ms_per_forward": ms,
                       "tokens_per_s": H * T / (ms * 1e-3), "gate_pairs_kept": pairs,
                       "gate_pairs_total": H * sum((qb * 64) // L for qb in range(T // 64)),
-                      "gated_pass_tflops": flops / (ms * 1e-3) / 1e12, "gdn_forward_ms": ms_fwd,
-                      "output_finite": bool(torch.isfinite(f.o).all().item()), "arithmetic": "f32 (CUDA cores)"}),
+                      "gated_pass_tflops_over_the_call": flops / (ms * 1e-3) / 1e12, "gdn_forward_ms": ms_fwd,
+                      "output_finite": bool(torch.isfinite(f.o).all().item()), "path": f.path,
+                      "arithmetic": ("chunk summaries f32 (CUDA cores); gated composition bf16 hi + lo on tcgen05, "
+                                     "f32 accumulate" if f.path == "hla_gated_tcgen05" else "f32 (CUDA cores)")}),
           flush=True)
 
 

@@ -209,13 +209,22 @@ DPLR_API dplr_status dplr_la_backward(const dplr_desc* desc,
  * S <- ((1 - w_ij) I + w_ij A_j) S + w_ij B_j, runs its own chunk's causal prefix, and reads o_i = S^T q_i.
  * W [B,H,T,N] fp32, N = ceil(T / L): the gates (only w_ij with j < c are used); gates below `theta` count as
  * zero. q, k, v, g, beta as for dplr_la_forward (no initial state). o [B,H,T,dv] fp32. Workspace:
- * dplr_hla_workspace_size(desc, L) bytes, 256-byte aligned. fp32 arithmetic on the CUDA cores. Asynchronous on
- * `stream`; allocates nothing. Errors: DPLR_ERR_INVALID_ARG for another mode or a null / misaligned pointer,
- * DPLR_ERR_UNSUPPORTED for another L or dk, dv > 128, DPLR_ERR_WORKSPACE, DPLR_ERR_CUDA. */
+ * dplr_hla_workspace_size(desc, L) bytes, 256-byte aligned; its first 256 bytes are a status word, zeroed by the
+ * call, into which a bounded wait of the tensor-core pass that gives up writes DPLR_ERR_TIMEOUT (read it with
+ * dplr_la_read_status). The chunk summaries are formed in fp32 on the CUDA cores; the gated composition runs on
+ * the tensor cores for dk = dv = 128 (bf16 hi + lo operands, fp32 accumulation; dplr_hla_path) and in fp32 on
+ * the CUDA cores otherwise. Asynchronous on `stream`; allocates nothing. Errors: DPLR_ERR_INVALID_ARG for another
+ * mode or a null / misaligned pointer, DPLR_ERR_UNSUPPORTED for another L or dk, dv > 128, DPLR_ERR_WORKSPACE,
+ * DPLR_ERR_CUDA. */
 DPLR_API size_t dplr_hla_workspace_size(const dplr_desc* desc, int L);
 DPLR_API dplr_status dplr_hla_forward(const dplr_desc* desc, const void* q, const void* k, const void* v,
                              const float* g, const float* beta, const float* W, float theta, int L,
                              float* o, void* workspace, size_t ws_bytes, void* stream);
+
+/* The kernel path dplr_hla_forward takes for `desc` and `L`: "hla_gated_tcgen05" (the gated composition on
+ * the tensor cores, dk = dv = 128 and at most 256 chunks of L tokens), "hla_gated_fp32" (on the CUDA cores),
+ * or "" if the arguments are invalid. */
+DPLR_API const char* dplr_hla_path(const dplr_desc* desc, int L);
 
 /* Gated DeltaProduct-style stacked Householders (HDLA page: research background and the computation table,
  * GDP with n_h = r_ab = r_kv): per token the gate once, then n_h delta-rule steps with their own key, value and

@@ -15,11 +15,19 @@
 //      query's row U_t = Q'_t (the composition of its chunk's earlier blocks), its output O_t updated;
 //   3. per 64 queries of one chunk, the history chunks newest first: two products per chunk, U A_j and U B_j,
 //      with the gates applied per query; a chunk whose gates are all zero for the 64 queries is skipped.
-// Passes 2 and 3 run in fp32 on the CUDA cores, with 4 x 4 register tiles.
+// Pass 2 runs in fp32 on the CUDA cores, with 4 x 4 register tiles. Pass 3 runs on the tensor cores for
+// dk = dv = 128 (tcgen05, bf16 hi + lo operands, three partial products, fp32 accumulators in tensor memory:
+// the products keep ~16 significant bits of each operand, against the 1e-3 of the output RMS this composition
+// is held to), after a small pass that splits each chunk's A_j and B_j into bf16 hi/lo operand tiles once;
+// on the CUDA cores otherwise.
+#include <cuda_bf16.h>
+
 #include <algorithm>
 #include <cstring>
 
 #include "dplr_internal.h"
+#include "sm100_ops.cuh"
+#include "tc_common.cuh"
 
 namespace dplr {
 namespace {
@@ -30,7 +38,8 @@ constexpr int HT = 256;      // threads
 struct HlaPlan {
     Plan pl;          // the fp32 two-stage plan at WY blocks of 64 tokens (GDN)
     int L, m, N;      // chunk length, WY blocks per chunk, chunks per head
-    size_t off_A, off_B, total;   // L-chunk summaries (L > 64; else the blocks' own maps)
+    int tc;           // pass 3 on the tensor cores
+    size_t off_A, off_B, off_T, total;   // L-chunk summaries (L > 64; else the blocks' own maps); operand tiles
 };
 
 __device__ __forceinline__ void l2_prefetch(const void* p, uint32_t bytes) {
@@ -257,6 +266,260 @@ hla_gated_kernel(Plan pl, int L, int N, float theta, const float* Um, const floa
     }
 }
 
+// ---- pass 3 on the tensor cores (dk = dv = 128)
+using namespace tc;
+
+constexpr int HD2 = 128;                          // dk = dv
+constexpr uint32_t kOpTile = HD2 * HD2 * 2;       // one bf16 [128][128] operand tile
+constexpr int kGT = 192;                          // warps 0-3: U (thread = feature = tensor-memory lane); 4: MMAs; 5: copies
+constexpr int kHlaMaxChunks = 256;                // history chunks per query block that fit the step list
+
+// Each chunk's A_j and B_j (fp32 [128][128], row k = the contracted index) as bf16 hi and lo tiles in the
+// 128-byte swizzled layout, row k and column n at sw_bf16(k, n, 128): the MN-major A operand of
+// X^T = A_j^T U^T and of o^T += B_j^T (w U)^T. Tiles [A hi | A lo | B hi | B lo] per (head, chunk).
+__global__ void __launch_bounds__(256)
+hla_split_kernel(int N, const float* Acs, const float* Bcs, unsigned char* tiles) {
+    const size_t unit = blockIdx.x;   // (head, chunk)
+    unsigned char* dst = tiles + unit * 4 * kOpTile;
+    for (int e = 0; e < 2; ++e) {
+        const float* src = (e == 0 ? Acs : Bcs) + unit * HD2 * HD2;
+        unsigned char* th = dst + (2 * e) * kOpTile;
+        unsigned char* tl = th + kOpTile;
+        for (int i = threadIdx.x; i < HD2 * HD2 / 8; i += blockDim.x) {   // 8 columns of one row per item
+            const int k = i >> 4, n = (i & 15) * 8;
+            const float4 a = *reinterpret_cast<const float4*>(src + (size_t)k * HD2 + n);
+            const float4 b = *reinterpret_cast<const float4*>(src + (size_t)k * HD2 + n + 4);
+            uint32_t h[4], l[4];
+            split2(a.x, a.y, h[0], l[0]);
+            split2(a.z, a.w, h[1], l[1]);
+            split2(b.x, b.y, h[2], l[2]);
+            split2(b.z, b.w, h[3], l[3]);
+            const uint32_t off = sw_bf16(k, n, HD2);
+            *reinterpret_cast<uint4*>(th + off) = make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4*>(tl + off) = make_uint4(l[0], l[1], l[2], l[3]);
+        }
+    }
+}
+
+struct GSm {
+    static constexpr int OPS = 0;                          // the step's A_j^T hi, lo, B_j^T hi, lo
+    static constexpr int UTB = HD2 * HQ * 2;               // bf16 [128 k][64 q] MN-major B operand
+    // U^T hi, lo, then (w U)^T hi, lo in two buffers by step parity: the o^T products of a step may still read
+    // theirs while the next step's tiles are written (X^T's completion, which the state warps wait for, implies
+    // that of the previous step's o^T products: one thread issues them all, in order)
+    static constexpr int UT = OPS + 4 * (int)kOpTile;
+    static constexpr int WB = UT + 6 * UTB;                // the step's gates [64]
+    static constexpr int FLAGS = WB + HQ * 4;              // per history chunk, per query warp: some gate >= theta
+    static constexpr int LIST = FLAGS + 2 * kHlaMaxChunks; // the history chunks that are composed, newest first
+    static constexpr int BAR = LIST + kHlaMaxChunks * 4;
+    static constexpr int TOTAL = BAR + 128;
+};
+static_assert(GSm::TOTAL <= 227 * 1024, "shared memory budget");
+
+struct GatedArgs {
+    const float* Um; const float* W; const unsigned char* tiles; float* o; int* status;
+};
+
+// One CTA per (head, 64 queries of one chunk c). The chunks j < c with some gate >= theta among the CTA's
+// queries are walked newest first; per chunk (a step) the issuer runs X^T = A_j^T U^T and o^T += B_j^T (w U)^T,
+// both M = 128 (the feature), N = 64 (the query), K = 128, in three terms (hi hi + lo hi + hi lo), while the
+// state warps keep U^T in fp32 registers (thread = feature) and update it, U <- U + w (X - U), once X^T is done.
+// o^T accumulates in tensor memory over the steps and is added to o (the chunk-local part of pass 1/2) at the end.
+__global__ void __launch_bounds__(kGT, 1)
+hla_gated_tc_kernel(Plan pl, int L, int N, float theta, GatedArgs args) {
+    using S = GSm;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const uint32_t sb = smem_addr(smem);
+    if (sb & 1023u) {
+        if (threadIdx.x == 0) atomicExch(args.status, (int)DPLR_ERR_CUDA);
+        return;
+    }
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::BAR);
+    uint64_t* full = bars + 0;     // the step's operand tiles landed
+    uint64_t* freed = bars + 1;    // the step's products are done with the operand tiles
+    uint64_t* ready = bars + 2;    // the step's U^T and (w U)^T tiles written (4 arrivals, one per state warp)
+    uint64_t* mX = bars + 3;       // the step's X^T is complete
+    uint64_t* drain = bars + 4;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 5);
+    int* nsteps = reinterpret_cast<int*>(bars + 6);
+    int* list = reinterpret_cast<int*>(smem + S::LIST);
+    float* wb = reinterpret_cast<float*>(smem + S::WB);
+    unsigned char* flags = smem + S::FLAGS;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int T = pl.T, nb = pl.nb;
+    const int qb = blockIdx.x % nb;
+    const size_t bh = blockIdx.x / nb;
+    const int t0 = qb * HQ, c = t0 / L;
+    const long long wl = pl.wait_cycles;
+    auto gate = [&](int q, int l) -> float {   // w_ql, with gates below theta (and absent queries) as zero
+        if (t0 + q >= T) return 0.f;
+        const float x = args.W[(bh * (size_t)T + t0 + q) * N + l];
+        return x >= theta ? x : 0.f;
+    };
+
+    // ---- the steps: history chunks, newest first, with some gate >= theta among the 64 queries
+    if (warp < 2) {
+        const int q = tid;
+        for (int l = c - 1; l >= 0; --l) {
+            const unsigned any = __ballot_sync(0xffffffffu, gate(q, l) != 0.f);
+            if (lane == 0) flags[warp * kHlaMaxChunks + (c - 1 - l)] = any != 0u;
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int n = 0;
+        for (int s = 0; s < c; ++s)
+            if (flags[s] | flags[kHlaMaxChunks + s]) list[n++] = c - 1 - s;
+        *nsteps = n;
+        mbar_init(full, 1);
+        mbar_init(freed, 1);
+        mbar_init(ready, 4);
+        mbar_init(mX, 1);
+        mbar_init(drain, 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    const int ns = *nsteps;
+    if (ns == 0) return;   // every query's history is gated off: o keeps the chunk-local part
+    if (warp == 0) tmem_alloc(tmem_holder, 128);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tmem_holder;   // columns 0-63: X^T; 64-127: o^T
+    bool failed = false;
+
+    if (warp == 5) {
+        // ---- copies of each step's operand tiles, once the previous step's products are done with them
+        int last = -1;
+        for (int st = 0; st < ns && lane == 0; ++st) {
+            if (st >= 1 && !mbar_wait(freed, (st - 1) & 1, wl)) { failed = true; break; }
+            const unsigned char* src = args.tiles + (bh * (size_t)N + list[st]) * 4 * kOpTile;
+            mbar_expect_tx(full, 4 * kOpTile);
+            for (int e = 0; e < 4; ++e) bulk_g2s(smem + S::OPS + e * kOpTile, src + e * kOpTile, kOpTile, full);
+            if (st + 1 < ns) {
+                const unsigned char* nx = args.tiles + (bh * (size_t)N + list[st + 1]) * 4 * kOpTile;
+                for (int e = 0; e < 4; ++e)
+                    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(reinterpret_cast<uint64_t>(nx + e * kOpTile)),
+                                 "r"(kOpTile) : "memory");
+            }
+            last = st;
+        }
+        if (failed) {   // (lane 0) no copy may land after the CTA has exited
+            atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
+            if (last >= 0) mbar_wait(full, last & 1, 400000000LL);
+        }
+        __syncwarp();
+    } else if (warp == 4) {
+        // ---- the products of each step, issued by lane 0
+        const uint32_t id = idesc_bf16(128, HQ, true, true);
+        for (int st = 0; st < ns && lane == 0; ++st) {
+            if (!mbar_wait(ready, st & 1, wl) || !mbar_wait(full, st & 1, wl)) { failed = true; break; }
+            fence_after_sync();
+            // (A operand: 64-column halves 16 KB apart, K = 16 rows per slice; B: one 64-query atom per row)
+            const uint64_t aH = smem_desc_sw128(sb + S::OPS, 16384, 1024), aL = dadd(aH, kOpTile);
+            const uint64_t bH = aH + ((uint64_t)(2 * kOpTile) >> 4), bL = dadd(bH, kOpTile);
+            const uint64_t uH = smem_desc_sw128(sb + S::UT, 16384, 1024), uL = dadd(uH, S::UTB);
+            const uint64_t wH = dadd(uH, (2 + 2 * (st & 1)) * S::UTB), wL = dadd(wH, S::UTB);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {   // X^T = A^T U^T
+                const uint32_t o = kk * 2048;
+                mma_bf16(tmem, dadd(aH, o), dadd(uH, o), id, kk > 0);
+                mma_bf16(tmem, dadd(aL, o), dadd(uH, o), id, 1u);
+                mma_bf16(tmem, dadd(aH, o), dadd(uL, o), id, 1u);
+            }
+            mma_commit(mX);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {   // o^T += B^T (w U)^T
+                const uint32_t o = kk * 2048;
+                mma_bf16(tmem + 64, dadd(bH, o), dadd(wH, o), id, (st > 0 || kk > 0) ? 1u : 0u);
+                mma_bf16(tmem + 64, dadd(bL, o), dadd(wH, o), id, 1u);
+                mma_bf16(tmem + 64, dadd(bH, o), dadd(wL, o), id, 1u);
+            }
+            mma_commit(freed);
+        }
+        if (failed) {   // (lane 0) no product may outlive the tensor memory
+            atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
+            mma_commit(drain);
+            mbar_wait(drain, 0, 400000000LL);
+        }
+        __syncwarp();
+    } else {
+        // ---- U^T, row d = this thread (the feature), 64 queries, in fp32 registers
+        const int d = tid;
+        const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
+        float u[HQ];
+        const float* U0 = args.Um + (bh * (size_t)nb + qb) * HQ * HD2;
+#pragma unroll
+        for (int q = 0; q < HQ; ++q) u[q] = U0[(size_t)q * HD2 + d];
+        // a wait of the four state warps: each warp's lane 0 polls, and the group takes one decision
+        auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait(bar, parity, wl);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            return !named_sync_or(1, 128, !ok);
+        };
+        for (int st = 0; st < ns; ++st) {
+            // the step's gates, then the U^T and (w U)^T tiles: row d, query q at sw_bf16(d, q, 128)
+            if (tid < HQ) wb[tid] = gate(tid, list[st]);
+            named_sync(1, 128);
+#pragma unroll
+            for (int ch = 0; ch < HQ / 8; ++ch) {
+                uint32_t h[4], l[4], wh[4], wlo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int q = 8 * ch + 2 * e;
+                    split2(u[q], u[q + 1], h[e], l[e]);
+                    split2(wb[q] * u[q], wb[q + 1] * u[q + 1], wh[e], wlo[e]);
+                }
+                const uint32_t off = sw_bf16(d, 8 * ch, HD2), wbuf = sb + S::UT + (2 + 2 * (st & 1)) * S::UTB;
+                sts128(sb + S::UT + off, h[0], h[1], h[2], h[3]);
+                sts128(sb + S::UT + S::UTB + off, l[0], l[1], l[2], l[3]);
+                sts128(wbuf + off, wh[0], wh[1], wh[2], wh[3]);
+                sts128(wbuf + S::UTB + off, wlo[0], wlo[1], wlo[2], wlo[3]);
+            }
+            fence_async_smem();
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ready);
+            // X^T of this step, then U <- U + w (X - U)
+            if (!wait_all(mX, st & 1)) { failed = true; break; }
+            fence_after_sync();
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                float x[32];
+                tmem_ld32(tmem + lane_base + 32 * hf, x);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int q = 32 * hf + e;
+                    u[q] = fmaf(wb[q], x[e] - u[q], u[q]);
+                }
+            }
+            fence_before_sync();
+            named_sync(1, 128);   // every state warp has read the gates and X^T (the next step rewrites both)
+        }
+        // o += o^T once the last step's products are done
+        if (!failed && !wait_all(freed, (ns - 1) & 1)) failed = true;
+        if (!failed) {
+            fence_after_sync();
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                float x[32];
+                tmem_ld32(tmem + lane_base + 64 + 32 * hf, x);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int q = 32 * hf + e;
+                    if (t0 + q < T) args.o[(bh * (size_t)T + t0 + q) * HD2 + d] += x[e];
+                }
+            }
+        }
+        if (failed && lane == 0) atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
 constexpr size_t kHAlign = 256;
 size_t hround(size_t x) { return (x + kHAlign - 1) / kHAlign * kHAlign; }
 
@@ -288,13 +551,16 @@ dplr_status make_hla_plan(const dplr_desc* d, int L, HlaPlan* hp) {
         hp->off_A = p.off_P;
         hp->off_B = p.off_c;
     }
+    hp->tc = (p.dk == HD2 && p.dv == HD2 && hp->N <= kHlaMaxChunks) ? 1 : 0;
+    hp->off_T = off;
+    if (hp->tc) off = hround(off + (size_t)p.BH * hp->N * 4 * kOpTile);
     hp->total = off;
     p.ws_bytes = off;
     hp->pl = p;
     return DPLR_OK;
 }
 
-std::atomic<uint64_t> g_hla_smem[2] = {{0}, {0}};
+std::atomic<uint64_t> g_hla_smem[3] = {{0}, {0}, {0}};
 
 }  // namespace
 }  // namespace dplr
@@ -321,6 +587,7 @@ extern "C" dplr_status dplr_hla_forward(const dplr_desc* desc, const void* q, co
         return DPLR_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char* ws = static_cast<char*>(workspace);
+    if (cudaMemsetAsync(ws, 0, kHAlign, s) != cudaSuccess) return DPLR_ERR_CUDA;   // the status word
     ChunkMapArgs ma;
     ma.q = q; ma.k = k; ma.v = v; ma.decay = g; ma.beta = beta;
     ma.A = nullptr; ma.Bm = nullptr; ma.K = nullptr; ma.V = nullptr; ma.o = o;
@@ -337,7 +604,17 @@ extern "C" dplr_status dplr_hla_forward(const dplr_desc* desc, const void* q, co
         hla_compose_kernel<<<(unsigned)((size_t)pl.BH * hp.N), HT, smem, s>>>(pl, hp.m, hp.N, ma.Pm, ma.Cm, ma.Qm, o, Acs, Bcs);
         if (cudaGetLastError() != cudaSuccess) return DPLR_ERR_CUDA;
     }
-    {   // pass 3
+    if (hp.tc) {   // pass 3 on the tensor cores: the chunks' operand tiles, then the gated composition
+        unsigned char* tiles = reinterpret_cast<unsigned char*>(ws + hp.off_T);
+        hla_split_kernel<<<(unsigned)((size_t)pl.BH * hp.N), 256, 0, s>>>(hp.N, Acs, Bcs, tiles);
+        if (cudaGetLastError() != cudaSuccess) return DPLR_ERR_CUDA;
+        if (set_smem_limit_once(reinterpret_cast<const void*>(hla_gated_tc_kernel), GSm::TOTAL, g_hla_smem[2]) != cudaSuccess)
+            return DPLR_ERR_CUDA;
+        GatedArgs ga;
+        ga.Um = ma.Qm; ga.W = W; ga.tiles = tiles; ga.o = o; ga.status = reinterpret_cast<int*>(ws);
+        hla_gated_tc_kernel<<<(unsigned)((size_t)pl.BH * pl.nb), kGT, GSm::TOTAL, s>>>(pl, hp.L, hp.N, theta, ga);
+        if (cudaGetLastError() != cudaSuccess) return DPLR_ERR_CUDA;
+    } else {   // pass 3 on the CUDA cores
         const size_t smem = sizeof(float) * (size_t)(HQ * pl.dk + pl.dk * pl.dk + pl.dk * pl.dv + HQ);
         if (set_smem_limit_once(reinterpret_cast<const void*>(hla_gated_kernel), 227 * 1024, g_hla_smem[1]) != cudaSuccess)
             return DPLR_ERR_CUDA;
@@ -345,4 +622,10 @@ extern "C" dplr_status dplr_hla_forward(const dplr_desc* desc, const void* q, co
         if (cudaGetLastError() != cudaSuccess) return DPLR_ERR_CUDA;
     }
     return DPLR_OK;
+}
+
+extern "C" const char* dplr_hla_path(const dplr_desc* desc, int L) {
+    HlaPlan hp;
+    if (make_hla_plan(desc, L, &hp) != DPLR_OK) return "";
+    return hp.tc ? "hla_gated_tcgen05" : "hla_gated_fp32";
 }

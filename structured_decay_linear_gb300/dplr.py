@@ -77,6 +77,8 @@ def library() -> ctypes.CDLL:
             lib.dplr_hla_workspace_size.argtypes = [dp, ctypes.c_int]
             lib.dplr_hla_forward.restype = ctypes.c_int
             lib.dplr_hla_forward.argtypes = [dp] + [_vp] * 6 + [ctypes.c_float, ctypes.c_int, _vp, _vp, ctypes.c_size_t, _vp]
+            lib.dplr_hla_path.restype = ctypes.c_char_p
+            lib.dplr_hla_path.argtypes = [dp, ctypes.c_int]
             lib.dplr_gdp_workspace_size.restype = ctypes.c_size_t
             lib.dplr_gdp_workspace_size.argtypes = [dp]
             lib.dplr_gdp_forward.restype = ctypes.c_int
@@ -169,6 +171,10 @@ def dplr_hla_forward(desc, q, k, v, g, beta, W, theta, L, o, workspace, ws_bytes
     """HLA's query-gated composition of GDN chunk transitions (device pointers; see include/dplr.h)."""
     return int(library().dplr_hla_forward(ctypes.byref(desc), q, k, v, g, beta, W, float(theta), int(L), o, workspace,
                                           ws_bytes, stream))
+
+
+def dplr_hla_path(desc, L: int) -> str:
+    return library().dplr_hla_path(ctypes.byref(desc), int(L)).decode()
 
 
 def dplr_gdp_workspace_size(desc: dplr_desc) -> int:
@@ -553,6 +559,15 @@ class HLA:
         off = (-self.ws.data_ptr()) % 256
         self.ws_ptr, self.ws_bytes = self.ws.data_ptr() + off, nbytes
         self.o = torch.empty((B, H, T, dv), dtype=torch.float32, device=self.device)
+        self.path = dplr_hla_path(self.desc, self.L)
+
+    def device_status(self, clear: bool = False) -> int:
+        """The workspace's status word (0, or DPLR_ERR_TIMEOUT after a bounded wait gave up), read synchronously."""
+        s = torch.cuda.current_stream(self.device)
+        st, word = dplr_la_read_status(self.ws_ptr, self.ws_bytes, clear, s.cuda_stream)
+        if st != DPLR_OK:
+            raise DplrError(st, "dplr_la_read_status")
+        return word
 
     def __call__(self, q, k, v, g, beta, W, theta: float = 0.0,
                  stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:

@@ -1,8 +1,9 @@
 """HLA's query-gated composition (dplr_hla_forward) against the float64 oracle (oracle.hla).
 
 Whole small problems, compared element by element: max |err| <= TAU * RMS of the oracle's output. The GPU path
-composes the exact chunk maps in fp32 from exact inputs (bf16 values upcast); TAU = 1e-3 allows for the fp32
-rounding of those products (the measured errors sit near 1e-6 to 1e-5).
+composes the exact chunk maps in fp32 from exact inputs (bf16 values upcast), and the gated composition either in
+fp32 (CUDA cores) or, for dk = dv = 128, on the tensor cores with bf16 hi + lo operands (~16 significant bits);
+TAU = 1e-3 allows for the rounding of those products (the measured errors sit near 1e-6 to 1e-5).
 """
 
 import numpy as np
@@ -40,9 +41,10 @@ def gates(H, T, L, seed, scale=2.0):
 
 
 CASES = [
-    # dtype, dk, dv, H, T, L, theta
+    # dtype, dk, dv, H, T, L, theta  (dk = dv = 128: the tensor-core gated pass)
     ("bf16", 128, 128, 2, 700, 256, 0.1),
     ("bf16", 128, 128, 2, 300, 64, 0.0),
+    ("f32", 128, 128, 1, 830, 64, 0.5),
     ("f32", 64, 64, 2, 500, 128, 0.1),
     ("f32", 64, 128, 1, 257, 256, 0.5),
     ("bf16", 128, 64, 1, 64, 64, 0.1),
@@ -82,3 +84,42 @@ def test_hla_all_gates_one_is_the_forward(sdl):
     ref, _ = oracle.forward_inputs(inp)
     assert _rel(o.double().cpu().numpy(), ref) <= TAU
     assert _rel(o.double().cpu().numpy(), o2.double().cpu().numpy()) <= 2e-2
+
+
+def test_hla_paths(sdl):
+    """dk = dv = 128 takes the tensor-core gated pass (up to 256 chunks); other sizes the fp32 pass."""
+    import torch
+    p = lambda dk, dv, T, L: sdl.dplr_hla_path(sdl.make_desc("gdn", torch.bfloat16, 1, 2, T, dk, dv), L)
+    assert p(128, 128, 4096, 256) == "hla_gated_tcgen05"
+    assert p(128, 128, 16384, 64) == "hla_gated_tcgen05"
+    assert p(128, 128, 16448, 64) == "hla_gated_fp32"      # 257 chunks
+    assert p(64, 64, 4096, 256) == "hla_gated_fp32"
+    assert p(128, 64, 4096, 256) == "hla_gated_fp32"
+    assert p(128, 128, 4096, 100) == ""
+
+
+def test_hla_tensor_core_pass_timeout_returns_and_reports(sdl):
+    """The tensor-core gated pass's waits, limited to 1000 cycles, end the launch with DPLR_ERR_TIMEOUT in the
+    status word; with the default limit the same context gives a correct composition."""
+    import torch
+    w = workloads.Workload(87, "hla_gdn", "gdn", "bf16", 1, 1, 0, 128, 128, 1, 1, 64, False)
+    H, T, L = 2, 1024, 128
+    inp = workloads.generate(w, heads=[(0, h) for h in range(H)], T=T)
+    W = gates(H, T, L, seed=5)
+    d = lambda x, t: torch.from_numpy(np.ascontiguousarray(x)).to("cuda").to(t)
+    args = [d(inp["q"], torch.bfloat16), d(inp["k"], torch.bfloat16), d(inp["v"], torch.bfloat16),
+            d(inp["decay"], torch.float32), d(inp["beta"], torch.float32), d(W, torch.float32), 0.1]
+    f = sdl.HLA(torch.bfloat16, 1, H, T, 128, 128, L)
+    assert f.path == "hla_gated_tcgen05"
+    sdl.dplr_la_set_wait_limit(1000)
+    try:
+        f(*args)
+        torch.cuda.synchronize()
+        assert f.device_status() == sdl.dplr.DPLR_ERR_TIMEOUT
+    finally:
+        sdl.dplr_la_set_wait_limit(0)
+    o = f(*args)
+    torch.cuda.synchronize()
+    assert f.device_status() == sdl.DPLR_OK
+    ref = oracle.hla(inp["q"], inp["k"], inp["v"], inp["decay"], inp["beta"], W, L, 0.1)
+    assert _rel(o.double().cpu().numpy(), ref) <= TAU
