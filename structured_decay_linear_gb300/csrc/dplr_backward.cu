@@ -37,6 +37,7 @@ namespace dplr {
 namespace {
 
 using smem::mm;
+using smem::mm_ksplit;
 
 constexpr int BT = 256;      // threads of the block-backward kernel
 constexpr int BMX = 32;      // rows of A~ (R = cb r), K~ (P = cb p) and Q~ (cb) at most
@@ -103,6 +104,8 @@ block_bwd_kernel(Plan pl, BwdArgs a) {
     float* va = Gc + BMX * LD;      // [BD] anchor a
     float* sd = va + BD;            // [BD] sum_n S_j dS_j per row
     float* ct = sd + BD;            // [BMX] HDLA: k^T Lambda k per token
+    float* ks = ct + BMX;           // [8][BMX][BNS] partial tiles of the slice's small products (K split 8 ways)
+    float* dVt = ks + 8 * BMX * BNS; // [BMX][BNS] the slice of dV
 
     const int tid = threadIdx.x, nth = blockDim.x, warp = tid >> 5, lane = tid & 31;
     const int dk = pl.dk, dv = pl.dv, T = pl.T, nb = pl.nb, cb = pl.cw;
@@ -185,11 +188,19 @@ block_bwd_kernel(Plan pl, BwdArgs a) {
     __syncthreads();
 
     // ---- Gram blocks and the WY inverse M = (I + L)^{-1} (forward substitution, one column per thread)
-    mm(Mm, LM, Bt, LD, false, At, LD, true, R, R, dk, 1.f, false);
-    mm(Gm, LM, Bt, LD, false, Kt, LD, true, R, P, dk, 1.f, false);
-    mm(QA, LM, Qt, LD, false, At, LD, true, cb, R, dk, 1.f, false);
-    mm(QK, LM, Qt, LD, false, Kt, LD, true, cb, P, dk, 1.f, false);
+    // (few tiles each, K = dk: split over every thread)
+    mm_ksplit(Mm, LM, Bt, LD, false, At, LD, true, R, R, dk, 1.f, false, ks);
     __syncthreads();
+    if (P > 0) {
+        mm_ksplit(Gm, LM, Bt, LD, false, Kt, LD, true, R, P, dk, 1.f, false, ks);
+        __syncthreads();
+    }
+    mm_ksplit(QA, LM, Qt, LD, false, At, LD, true, cb, R, dk, 1.f, false, ks);
+    __syncthreads();
+    if (P > 0) {
+        mm_ksplit(QK, LM, Qt, LD, false, Kt, LD, true, cb, P, dk, 1.f, false, ks);
+        __syncthreads();
+    }
     mask(Mm, LM, R, R, r, r, true);
     mask(Gm, LM, R, P, r, p, true);
     mask(QA, LM, cb, R, 1, r, false);
@@ -234,14 +245,18 @@ block_bwd_kernel(Plan pl, BwdArgs a) {
             Vs[u * LS + n] = x;
         }
         __syncthreads();
-        mm(Hs, LS, Bt, LD, false, S0s, LS, false, R, BNS, dk, 1.f, false);
-        mm(dEs, LS, At, LD, false, dSs, LS, false, R, BNS, dk, -1.f, false);
+        // the slice's R x 16 products have few tiles: their K is split over every thread
+        mm_ksplit(Hs, LS, Bt, LD, false, S0s, LS, false, R, BNS, dk, 1.f, false, ks);
         __syncthreads();
-        mm(Hs, LS, Gm, LM, false, Vs, LS, false, R, BNS, P, 1.f, true);
-        mm(dEs, LS, QA, LM, true, dOs, LS, false, R, BNS, cb, -1.f, true);
+        mm_ksplit(dEs, LS, At, LD, false, dSs, LS, false, R, BNS, dk, -1.f, false, ks);
         __syncthreads();
-        mm(Es, LS, Mm, LM, false, Hs, LS, false, R, BNS, R, 1.f, false);
-        mm(dHs, LS, Mm, LM, true, dEs, LS, false, R, BNS, R, 1.f, false);
+        mm_ksplit(Hs, LS, Gm, LM, false, Vs, LS, false, R, BNS, P, 1.f, true, ks);
+        __syncthreads();
+        mm_ksplit(dEs, LS, QA, LM, true, dOs, LS, false, R, BNS, cb, -1.f, true, ks);
+        __syncthreads();
+        mm_ksplit(Es, LS, Mm, LM, false, Hs, LS, false, R, BNS, R, 1.f, false, ks);
+        __syncthreads();
+        mm_ksplit(dHs, LS, Mm, LM, true, dEs, LS, false, R, BNS, R, 1.f, false, ks);
         __syncthreads();
         mm(dAt, LD, Es, LS, false, dSs, LS, true, R, dk, BNS, -1.f, true);
         mm(dBt, LD, dHs, LS, false, S0s, LS, true, R, dk, BNS, 1.f, true);
@@ -251,16 +266,21 @@ block_bwd_kernel(Plan pl, BwdArgs a) {
         mm(dG, LM, dHs, LS, false, Vs, LS, true, R, P, BNS, 1.f, true);
         mm(dQA, LM, dOs, LS, false, Es, LS, true, cb, R, BNS, -1.f, true);
         mm(dQK, LM, dOs, LS, false, Vs, LS, true, cb, P, BNS, 1.f, true);
-        // dV = K~ dS^ + QK^T dO + G^T dH for this slice, straight to the output
+        __syncthreads();
+        // dV = K~ dS^ + QK^T dO + G^T dH for this slice, then to the output (a generic mode may have no K, V)
+        if (P > 0) {
+            mm_ksplit(dVt, BNS, Kt, LD, false, dSs, LS, false, P, BNS, dk, 1.f, false, ks);
+            __syncthreads();
+            mm_ksplit(dVt, BNS, QK, LM, true, dOs, LS, false, P, BNS, cb, 1.f, true, ks);
+            __syncthreads();
+            mm_ksplit(dVt, BNS, Gm, LM, true, dHs, LS, false, P, BNS, R, 1.f, true, ks);
+            __syncthreads();
+        }
         for (int idx = tid; idx < P * BNS; idx += nth) {
             const int u = idx / BNS, n = idx - u * BNS, t = u / p, e = u - t * p;
-            float s = 0.f;
-            for (int c = 0; c < dk; ++c) s = fmaf(Kt[u * LD + c], dSs[c * LS + n], s);
-            for (int tt = 0; tt < cb; ++tt) s = fmaf(QK[tt * LM + u], dOs[tt * LS + n], s);
-            for (int m = 0; m < R; ++m) s = fmaf(Gm[m * LM + u], dHs[m * LS + n], s);
             if (t < valid) {
-                if (MODE == DPLR_GENERIC) a.dV[((tok0 + t) * p + e) * dv + n0 + n] = s;
-                else a.dv[(tok0 + t) * dv + n0 + n] = s;
+                if (MODE == DPLR_GENERIC) a.dV[((tok0 + t) * p + e) * dv + n0 + n] = dVt[idx];
+                else a.dv[(tok0 + t) * dv + n0 + n] = dVt[idx];
             }
         }
         __syncthreads();
@@ -370,7 +390,8 @@ block_bwd_kernel(Plan pl, BwdArgs a) {
 }
 
 size_t bwd_smem_bytes() {
-    return sizeof(float) * (size_t)(8 * BMX * LD + 8 * BMX * LM + 2 * BD * LS + 6 * BMX * LS + BMX * LD + 2 * BD + BMX);
+    return sizeof(float) * (size_t)(8 * BMX * LD + 8 * BMX * LM + 2 * BD * LS + 6 * BMX * LS + BMX * LD + 2 * BD + BMX +
+                                    9 * BMX * BNS);
 }
 
 // ---- pass 2: the block-boundary state gradients, per (head, 16 state columns), blocks in reverse order
