@@ -626,16 +626,16 @@ constexpr int K2SB = 3;      // state tile buffers: S_{j-1} is read by P(j) and 
 // - two stages of the chain's maps: P_j (bf16 [128][128]) and this CTA's columns of c_j (fp32 [128][32]);
 // - two stages of the output maps: Q'_j (bf16 [128][128], hi/lo rows interleaved by 16) and this CTA's
 //   columns of the chunk-local outputs O_j (fp32 [64][32]);
-// - three buffers of S_{j-1} as bf16 hi and lo core-matrix tiles.
+// - three buffers of S_{j-1} as one bf16 core-matrix tile [128][64]: hi in columns 0-31, lo in 32-63, so that one
+//   MMA of N = 64 forms the product with both parts.
 struct K2Smem {
     static constexpr int PC = 32768 + 16384, P_ = 0, C_ = 32768;   // a chain stage
     static constexpr int QO = 32768 + 8192, Q_ = 0, O_ = 32768;    // an output stage
     static constexpr int PCS = 0;
     static constexpr int QOS = PCS + 2 * PC;
-    static constexpr int SB = QOS + 2 * QO;       // S_{j-1} hi: bf16 [128][NV] core-matrix tiles, K2SB buffers
-    static constexpr int SBB = 128 * NV * 2;
-    static constexpr int SL = SB + K2SB * SBB;    // S_{j-1} lo
-    static constexpr int BAR = SL + K2SB * SBB;
+    static constexpr int SB = QOS + 2 * QO;       // S_{j-1} [hi | lo]: bf16 [128][2 NV] core-matrix tiles, K2SB buffers
+    static constexpr int SBB = 128 * 2 * NV * 2;
+    static constexpr int BAR = SB + K2SB * SBB;
     static constexpr int TOTAL = BAR + 128;
 };
 static_assert(K2Smem::TOTAL <= 227 * 1024, "shared memory budget");
@@ -689,11 +689,12 @@ hdla_chain_kernel(Plan pl, K2Args args, const __grid_constant__ CUtensorMap tm_P
         mbar_init(drain, 1);
         mbar_fence_init();
     }
-    if (warp == 0) tmem_alloc(tmem_holder, 128);
+    if (warp == 0) tmem_alloc(tmem_holder, 256);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    const uint32_t tmem = *tmem_holder;   // columns 0-31: P_j S_{j-1}; 32-95: two output accumulators
+    // columns 0-63: P_j [S_hi | S_lo]; 64-191: two output accumulators [Q'_hi; Q'_lo] [S_hi | S_lo]
+    const uint32_t tmem = *tmem_holder;
     bool failed = false;
     auto unit_row = [&](int jj) { return static_cast<int>(((size_t)jj * pl.BH + bh) * HD); };
 
@@ -746,27 +747,25 @@ hdla_chain_kernel(Plan pl, K2Args args, const __grid_constant__ CUtensorMap tm_P
         }
         __syncwarp();
     } else if (warp == 4) {
-        // ---- the products, issued by lane 0: P(j) = P_j (S_hi + S_lo) into columns 0-31 as soon as S_{j-1} is in
-        // place, then Q'(j-1) = [Q'_hi; Q'_lo] (S_hi + S_lo) of the previous chunk into accumulator (j - 1) % 2. The
+        // ---- the products, issued by lane 0: P(j) = P_j [S_hi | S_lo] into columns 0-63 as soon as S_{j-1} is in
+        // place, then Q'(j-1) = [Q'_hi; Q'_lo] [S_hi | S_lo] of the previous chunk into accumulator (j - 1) % 2. The
         // chain's product never waits behind the output product of its own chunk. (A second issuing warp for the
         // output products, so that P(j+1) need not wait for the issue of Q'(j), was slower: the two share the
         // tensor pipe.)
-        const uint32_t idS = idesc_bf16(128, NV, false, true);
-        auto products = [&](uint32_t d, uint64_t a, int buf) {
-            const uint64_t bH = smem_desc(sb + S::SB + buf * S::SBB, (NV / 8) * 128, 128);
-            const uint64_t bL = smem_desc(sb + S::SL + buf * S::SBB, (NV / 8) * 128, 128);
+        const uint32_t idS = idesc_bf16(128, 2 * NV, false, true);
+        auto products = [&](uint32_t d, uint64_t a, int buf) {   // 8 MMAs, M = 128, N = 64, K = 16 each
+            const uint64_t b = smem_desc(sb + S::SB + buf * S::SBB, (2 * NV / 8) * 128, 128);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t ao = (kk >> 2) * 16384 + (kk & 3) * 32, bo = kk * 2 * (NV / 8) * 128;
-                mma_bf16(d, dadd(a, ao), dadd(bH, bo), idS, kk > 0);
-                mma_bf16(d, dadd(a, ao), dadd(bL, bo), idS, 1u);
+                const uint32_t ao = (kk >> 2) * 16384 + (kk & 3) * 32, bo = kk * 2 * (2 * NV / 8) * 128;
+                mma_bf16(d, dadd(a, ao), dadd(b, bo), idS, kk > 0);
             }
         };
         auto output_product = [&](int jj) -> bool {   // Q'(jj), from S_{jj-1} in buffer jj % 3
             const int u = jj & 1;
             if (!mbar_wait(&fullQO[u], (jj >> 1) & 1, wl)) return false;
             fence_after_sync();
-            products(tmem + 32 + 32 * u, smem_desc_sw128(sb + S::QOS + u * S::QO + S::Q_, 16, 1024), jj % K2SB);
+            products(tmem + 64 + 64 * u, smem_desc_sw128(sb + S::QOS + u * S::QO + S::Q_, 16, 1024), jj % K2SB);
             mma_commit(&mO[u]);
             mma_commit(&freedQO[u]);
             return true;
@@ -794,16 +793,16 @@ hdla_chain_kernel(Plan pl, K2Args args, const __grid_constant__ CUtensorMap tm_P
         float st[NV];
 #pragma unroll
         for (int n = 0; n < NV; ++n) st[n] = args.S0 ? args.S0[(bh * HD + i) * HD + n0 + n] : 0.f;
-        // S_{j-1} into buffer b as bf16 hi + lo, core-matrix layout (MN-major operand: K = row i)
+        // S_{j-1} into buffer b as bf16 [hi | lo], core-matrix layout (MN-major operand: K = row i, N = 64)
         auto write_state = [&](int b) {
-            const uint32_t r0 = (i >> 3) * (NV / 8) * 128 + (i & 7) * 16;
+            const uint32_t r0 = (i >> 3) * (2 * NV / 8) * 128 + (i & 7) * 16;
 #pragma unroll
             for (int ch = 0; ch < NV / 8; ++ch) {
                 uint32_t h[4], l[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) split2(st[8 * ch + 2 * e], st[8 * ch + 2 * e + 1], h[e], l[e]);
                 sts128(sb + S::SB + b * S::SBB + r0 + ch * 128, h[0], h[1], h[2], h[3]);
-                sts128(sb + S::SL + b * S::SBB + r0 + ch * 128, l[0], l[1], l[2], l[3]);
+                sts128(sb + S::SB + b * S::SBB + r0 + (ch + NV / 8) * 128, l[0], l[1], l[2], l[3]);
             }
         };
         // a wait of the four state warps: each warp's lane 0 polls, and the group takes one decision (a warp
@@ -822,10 +821,14 @@ hdla_chain_kernel(Plan pl, K2Args args, const __grid_constant__ CUtensorMap tm_P
             if (!wait_all(&mO[u], (jj >> 1) & 1, &fullQO[u], (jj >> 1) & 1)) return false;
             fence_after_sync();
             const uint32_t stg = sb + S::QOS + u * S::QO;
-            float x[32];
-            tmem_ld32(tmem + lane_base + 32 + 32 * u, x);
+            float x[32], y[32];
+            tmem_ld32(tmem + lane_base + 64 + 64 * u, x);        // x S_hi
+            tmem_ld32(tmem + lane_base + 64 + 64 * u + 32, y);   // x S_lo
 #pragma unroll
-            for (int e = 0; e < 32; ++e) x[e] += __shfl_xor_sync(0xffffffffu, x[e], 16);
+            for (int e = 0; e < 32; ++e) {
+                x[e] += y[e];
+                x[e] += __shfl_xor_sync(0xffffffffu, x[e], 16);
+            }
             const int valid = min(HCK, T - jj * HCK);
             if (tok < valid) {
                 const bool upper = lane >= 16;   // (selects keep x in registers)
@@ -858,17 +861,18 @@ hdla_chain_kernel(Plan pl, K2Args args, const __grid_constant__ CUtensorMap tm_P
             fence_after_sync();
             {
                 const uint32_t stg = sb + S::PCS + u * S::PC;
-                float x[32];
-                tmem_ld32(tmem + lane_base, x);
+                float x[32], y[32];
+                tmem_ld32(tmem + lane_base, x);        // P_j S_hi
+                tmem_ld32(tmem + lane_base + 32, y);   // P_j S_lo
 #pragma unroll
                 for (int ch = 0; ch < NV / 4; ++ch) {   // c_j row i, columns 4 ch .. 4 ch + 3 (fp32 swizzled box)
                     float4 c4;
                     asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(c4.x), "=f"(c4.y), "=f"(c4.z), "=f"(c4.w)
                                  : "r"(stg + S::C_ + swz(i, ch)));
-                    st[4 * ch + 0] = x[4 * ch + 0] + c4.x;
-                    st[4 * ch + 1] = x[4 * ch + 1] + c4.y;
-                    st[4 * ch + 2] = x[4 * ch + 2] + c4.z;
-                    st[4 * ch + 3] = x[4 * ch + 3] + c4.w;
+                    st[4 * ch + 0] = (x[4 * ch + 0] + y[4 * ch + 0]) + c4.x;
+                    st[4 * ch + 1] = (x[4 * ch + 1] + y[4 * ch + 1]) + c4.y;
+                    st[4 * ch + 2] = (x[4 * ch + 2] + y[4 * ch + 2]) + c4.z;
+                    st[4 * ch + 3] = (x[4 * ch + 3] + y[4 * ch + 3]) + c4.w;
                 }
             }
             // buffer (j + 1) % 3 was last read by Q'(j - 2), which the issuer queued before P(j) (and which
@@ -897,7 +901,7 @@ hdla_chain_kernel(Plan pl, K2Args args, const __grid_constant__ CUtensorMap tm_P
     }
     fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 128);
+    if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
 std::atomic<uint64_t> g_k1_smem_set{0}, g_k2_smem_set{0};
