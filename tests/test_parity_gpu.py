@@ -411,3 +411,30 @@ def test_forward_host_seq_matches_device_forward(sdl, mode, T, segments, slots, 
             for x, y in ((o, o_ref), (S, S_ref)):
                 scale = float(y.double().pow(2).mean().sqrt()) or 1.0
                 assert float((x.double() - y.double()).abs().max()) <= 1e-5 * scale
+
+
+@pytest.mark.parametrize("dtype,r,p,T,segments", [("f32", 4, 2, 700, 3), ("bf16", 2, 1, 260, 2), ("f32", 3, 0, 130, 2)])
+def test_forward_host_seq_generic_matches_device_forward(sdl, dtype, r, p, T, segments):
+    """dplr_la_forward_host_seq in the generic mode (the tensor-core generic stages at d = 64, and a rank-3
+    case without K and V on the fp32 stages) gives dplr_la_forward's result within 1e-5 of the RMS."""
+    import torch
+    w = workloads.Workload(96, "generic_host_seq", "generic", dtype, 1, 2, T, 64, 64, r, p, 64, False)
+    inp = gen_generic(w, 2, T, seed=T + r)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    host = {}
+    for key in ("q", "decay", "A", "Bm", "K", "V"):
+        x = inp[key]
+        if x is None:
+            host[key] = None
+            continue
+        t = torch.from_numpy(np.ascontiguousarray(x))
+        host[key] = (t.to(tdt) if key != "decay" else t).pin_memory()
+    dev = {k_: (None if t is None else t.to("cuda")) for k_, t in host.items()}
+    ref = sdl.Forward("generic", tdt, 1, 2, T, 64, 64, r, p)
+    o_ref, S_ref = [x.clone().cpu() for x in ref(**dev)]
+    fh = sdl.ForwardHostSeq("generic", tdt, 1, 2, T, 64, 64, r, p, segments=segments, slots=2)
+    o, S = fh(**host)
+    torch.cuda.current_stream().synchronize()
+    for x, y in ((o, o_ref), (S, S_ref)):
+        scale = float(y.double().pow(2).mean().sqrt()) or 1.0
+        assert float((x.double() - y.double()).abs().max()) <= 1e-5 * scale
