@@ -98,7 +98,7 @@ def step_bytes(w):
 
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,clocks.mem")
 
 
 class ClockSampler:
@@ -115,7 +115,8 @@ class ClockSampler:
 
     def stop(self):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "mem_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
         time.sleep(0.25)
         self.proc.terminate()
         try:
@@ -124,7 +125,7 @@ class ClockSampler:
             self.proc.kill()
             out, _ = self.proc.communicate()
         rows = [r for r in csv.reader(io.StringIO(out)) if len(r) >= 9]
-        sm, smax, reasons = [], None, set()
+        sm, smax, mem, reasons = [], None, [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
             try:
@@ -135,8 +136,12 @@ class ClockSampler:
             for name, val in zip(names, r[5:9]):
                 if val.strip().lower() == "active":
                     reasons.add(name)
+            try:
+                mem.append(float(r[9]))
+            except (IndexError, ValueError):
+                pass
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "mem_mhz": statistics.median(mem) if mem else None, "reasons": sorted(reasons), "samples": len(sm)}
 
 
 # ----------------------------------------------------------------------------
@@ -429,6 +434,8 @@ def run_ours(args, w):
             "wall_s_timed_region": t_wall,
             "output_finite": finite,
             "library": os.path.relpath(lib_path, ROOT),
+            "device": {"name": torch.cuda.get_device_name(dev),
+                       "sm_count": torch.cuda.get_device_properties(dev).multi_processor_count},
         }
         print(json.dumps(line), flush=True)
     if world > 1:
