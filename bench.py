@@ -144,6 +144,25 @@ class ClockSampler:
                 "mem_mhz": statistics.median(mem) if mem else None, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def effective_sm_mhz(dev, cycles=20_000_000):
+    """SM clock cycles (clock64) per microsecond of a spin of `cycles` cycles, timed with CUDA events:
+    the clock the kernels actually ran at, next to the clock nvidia-smi reports. Median of three."""
+    import torch
+    if not hasattr(torch.cuda, "_sleep"):
+        return None
+    with torch.cuda.device(dev):
+        torch.cuda._sleep(cycles // 20)
+        vals = []
+        for _ in range(3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch.cuda._sleep(cycles)
+            e1.record()
+            torch.cuda.synchronize(dev)
+            vals.append(cycles / (e0.elapsed_time(e1) * 1e3))
+    return round(statistics.median(vals), 1)
+
+
 # ----------------------------------------------------------------------------
 # Helpers.
 # ----------------------------------------------------------------------------
@@ -340,6 +359,7 @@ def run_ours(args, w):
     barrier()
     t_wall = time.perf_counter() - t_wall
     clocks = sampler.stop()
+    clocks["sm_mhz_effective"] = effective_sm_mhz(dev)
     k1 = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     k2 = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
     step_ms = slowest_ms(sum(a + b for a, b in zip(k1, k2)) / K, world, dev)
