@@ -41,11 +41,16 @@ __device__ __forceinline__ void mm(float* C, int ldc, const float* A, int lda, b
 
 // The same product for a small C (few 4 x 4 tiles) and a longer K: the CTA's threads split K into G groups
 // (G = threads / tiles), each thread one tile over its group's part of K, partial tiles into scratch
-// [G][M][N]; then every element of C sums its G partials in group order (a fixed order: the result does not
-// depend on the timing). The caller's threads must all call it; it ends with the sums written (no barrier after).
+// [G][M][N] (at most 16 blockDim.x floats); then every element of C sums its G partials in group order (a fixed
+// order: the result does not depend on the timing). The caller's threads must all call it; it ends with the sums
+// written (no barrier after). With more tiles than threads it is mm itself.
 __device__ __forceinline__ void mm_ksplit(float* C, int ldc, const float* A, int lda, bool ta, const float* B, int ldb,
                                           bool tb, int M, int N, int K, float alpha, bool acc, float* scratch) {
     const int nt = N >> 2, tiles = (M >> 2) * nt;
+    if (tiles > (int)blockDim.x) {
+        mm(C, ldc, A, lda, ta, B, ldb, tb, M, N, K, alpha, acc);
+        return;
+    }
     const int G = max(1, (int)blockDim.x / tiles), kc = (K + G - 1) / G;
     const int g = threadIdx.x / tiles, tile = threadIdx.x - g * tiles;
     const int as = ta ? 1 : lda, ak = ta ? lda : 1;
