@@ -639,8 +639,9 @@ def run_hla(args):
                       "gate_pairs_total": H * sum((qb * 64) // L for qb in range(T // 64)),
                       "gated_pass_tflops_over_the_call": flops / (ms * 1e-3) / 1e12, "gdn_forward_ms": ms_fwd,
                       "output_finite": bool(torch.isfinite(f.o).all().item()), "path": f.path,
-                      "arithmetic": ("chunk summaries f32 (CUDA cores); gated composition bf16 hi + lo on tcgen05, "
-                                     "f32 accumulate" if f.path == "hla_gated_tcgen05" else "f32 (CUDA cores)")}),
+                      "arithmetic": ("64-token block maps f32 (CUDA cores); chunk composition and gated composition "
+                                     "bf16 hi + lo on tcgen05, f32 accumulate" if f.path == "hla_gated_tcgen05"
+                                     else "f32 (CUDA cores)")}),
           flush=True)
 
 

@@ -15,11 +15,11 @@
 //      query's row U_t = Q'_t (the composition of its chunk's earlier blocks), its output O_t updated;
 //   3. per 64 queries of one chunk, the history chunks newest first: two products per chunk, U A_j and U B_j,
 //      with the gates applied per query; a chunk whose gates are all zero for the 64 queries is skipped.
-// Pass 2 runs in fp32 on the CUDA cores, with 4 x 4 register tiles. Pass 3 runs on the tensor cores for
-// dk = dv = 128 (tcgen05, bf16 hi + lo operands, three partial products, fp32 accumulators in tensor memory:
-// the products keep ~16 significant bits of each operand, against the 1e-3 of the output RMS this composition
-// is held to), after a small pass that splits each chunk's A_j and B_j into bf16 hi/lo operand tiles once;
-// on the CUDA cores otherwise.
+// For dk = dv = 128, passes 2 and 3 run on the tensor cores (tcgen05, bf16 hi + lo operands, three partial
+// products, fp32 accumulators in tensor memory: the products keep ~16 significant bits of each operand, against
+// the 1e-3 of the output RMS this composition is held to); pass 3 after a small pass that splits each chunk's A_j
+// and B_j into bf16 hi/lo operand tiles once. Otherwise both run in fp32 on the CUDA cores (4 x 4 register
+// tiles).
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -301,6 +301,213 @@ hla_split_kernel(int N, const float* Acs, const float* Bcs, unsigned char* tiles
     }
 }
 
+// ---- pass 2 on the tensor cores (dk = dv = 128): one CTA per (head, L-chunk) walks the chunk's blocks b = b0 + 1 ..
+// with the composition of its earlier blocks, A (dk x dk) and B (dk x dv), held in tensor memory:
+//     U^T = A^T Q'_b^T,  O^T = B^T Q'_b^T     (M = 128 features, N = 64 tokens, K = 128)
+//     A <- P_b A,        B <- P_b B + c_b      (M = N = K = 128, c_b written into B's accumulator first)
+// Every product takes three bf16 terms (hi hi + hi lo + lo hi) into fp32 accumulators (tensor-memory columns 0-127 A,
+// 128-255 B, 256-319 U^T, 320-383 O^T). P_b and Q'_b are split from fp32 into K-major tiles, row r and column n at
+// sw_bf16(r, n, rows); A and B into one pair of tiles at sw_bf16(k, n, 128) (row k the contracted index), which is
+// the MN-major B operand of P_b A and the MN-major A operand of A^T Q'^T alike.
+struct CSm {
+    static constexpr int PH = 0, PL = PH + (int)kOpTile;                  // P_b hi, lo: bf16 [128][128]
+    static constexpr int XH = PL + (int)kOpTile, XL = XH + (int)kOpTile;  // A or B: bf16 [128][128]
+    static constexpr int QH = XL + (int)kOpTile, QL = QH + HQ * HD2 * 2;  // Q'_b hi, lo: bf16 [64][128]
+    static constexpr int BAR = QL + HQ * HD2 * 2;
+    static constexpr int TOTAL = BAR + 64;
+};
+static_assert(CSm::TOTAL <= 227 * 1024, "shared memory budget");
+constexpr int kCT = 256;   // threads: warp w takes tensor-memory lanes 32 (w % 4) .. + 31 and column half w / 4
+
+__global__ void __launch_bounds__(kCT, 1)
+hla_compose_tc_kernel(Plan pl, int m, int N, const float* Pm, const float* Cm, float* Qm, float* o, float* Aout,
+                      float* Bout, int* status) {
+    using S = CSm;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const uint32_t sb = smem_addr(smem);
+    if (sb & 1023u) {
+        if (threadIdx.x == 0) atomicExch(status, (int)DPLR_ERR_CUDA);
+        return;
+    }
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::BAR);
+    uint64_t* mb = bars + 0;
+    uint64_t* drain = bars + 1;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int row = 32 * (warp & 3) + lane;   // tensor-memory lane: a row of A, B and P_b; a feature of U^T and O^T
+    const int hf = warp >> 2;                 // column half
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const int T = pl.T, nb = pl.nb;
+    const int c = blockIdx.x % N;
+    const size_t bh = blockIdx.x / N;
+    const int b0 = c * m, nbc = min(m, nb - b0);
+    const long long wl = pl.wait_cycles;
+    auto unit = [&](int b) { return bh * (size_t)nb + b; };
+    float* Ag = Aout + (bh * (size_t)N + c) * HD2 * HD2;
+    float* Bg = Bout + (bh * (size_t)N + c) * HD2 * HD2;
+    if (nbc == 1) {   // a chunk of one block is that block
+        const float4* P4 = reinterpret_cast<const float4*>(Pm + unit(b0) * HD2 * HD2);
+        const float4* C4 = reinterpret_cast<const float4*>(Cm + unit(b0) * HD2 * HD2);
+        for (int i = tid; i < HD2 * HD2 / 4; i += kCT) {
+            reinterpret_cast<float4*>(Ag)[i] = P4[i];
+            reinterpret_cast<float4*>(Bg)[i] = C4[i];
+        }
+        return;
+    }
+    constexpr uint32_t TA = 0, TB = 128, TU = 256, TO = 320;
+    if (tid == 0) {
+        mbar_init(mb, 1);
+        mbar_init(drain, 1);
+        mbar_fence_init();
+    }
+    if (warp == 0) tmem_alloc(tmem_holder, 512);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tmem_holder;
+
+    // fp32 rows [rows][128] from global memory into bf16 hi / lo tiles, row r and column n at sw_bf16(r, n, rows)
+    auto split_rows = [&](const float* src, int rows, uint32_t th, uint32_t tl) {
+        for (int i = tid; i < rows * 16; i += kCT) {
+            const int r = i >> 4, n = (i & 15) * 8;
+            const float4 a = *reinterpret_cast<const float4*>(src + (size_t)r * HD2 + n);
+            const float4 b = *reinterpret_cast<const float4*>(src + (size_t)r * HD2 + n + 4);
+            uint32_t h[4], l[4];
+            split2(a.x, a.y, h[0], l[0]);
+            split2(a.z, a.w, h[1], l[1]);
+            split2(b.x, b.y, h[2], l[2]);
+            split2(b.z, b.w, h[3], l[3]);
+            const uint32_t off = sw_bf16(r, n, rows);
+            sts128(th + off, h[0], h[1], h[2], h[3]);
+            sts128(tl + off, l[0], l[1], l[2], l[3]);
+        }
+    };
+    // this thread's row and column half of the accumulator at col0 into the A / B operand tiles
+    auto tmem_to_x = [&](uint32_t col0) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            float x[32];
+            tmem_ld32(tmem + lane_base + col0 + 64 * hf + 32 * q, x);
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t h[4], l[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) split2(x[8 * ch + 2 * e], x[8 * ch + 2 * e + 1], h[e], l[e]);
+                const uint32_t off = sw_bf16(row, 64 * hf + 32 * q + 8 * ch, HD2);
+                sts128(sb + S::XH + off, h[0], h[1], h[2], h[3]);
+                sts128(sb + S::XL + off, l[0], l[1], l[2], l[3]);
+            }
+        }
+    };
+    // X^T Q'^T into columns dst, then P_b X into columns acc (onto its content when acc_in), issued by lane 0 of
+    // warp 0 and committed to mb
+    auto products = [&](uint32_t dst, uint32_t acc, uint32_t acc_in) {
+        if (warp != 0) return;
+        const uint32_t lead = lane == 0;
+        const uint32_t idT = idesc_bf16(128, HQ, true, false), idP = idesc_bf16(128, 128, false, true);
+        const uint64_t xh = smem_desc_sw128(sb + S::XH, 16384, 1024), xl = smem_desc_sw128(sb + S::XL, 16384, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {   // Q'_b: 64-column halves of 64 rows (8 KB)
+            const uint32_t ko = (kk >> 2) * 8192 + (kk & 3) * 32;
+            const uint64_t qh = smem_desc_sw128(sb + S::QH + ko, 16, 1024), ql = smem_desc_sw128(sb + S::QL + ko, 16, 1024);
+            mma_ss_if(tmem + dst, dadd(xh, 2048 * kk), qh, idT, kk > 0 ? 1u : 0u, lead);
+            mma_ss_if(tmem + dst, dadd(xh, 2048 * kk), ql, idT, 1u, lead);
+            mma_ss_if(tmem + dst, dadd(xl, 2048 * kk), qh, idT, 1u, lead);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {   // P_b: 64-column halves of 128 rows (16 KB)
+            const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+            const uint64_t ph = smem_desc_sw128(sb + S::PH + ko, 16, 1024), pq = smem_desc_sw128(sb + S::PL + ko, 16, 1024);
+            mma_ss_if(tmem + acc, ph, dadd(xh, 2048 * kk), idP, (acc_in || kk > 0) ? 1u : 0u, lead);
+            mma_ss_if(tmem + acc, ph, dadd(xl, 2048 * kk), idP, 1u, lead);
+            mma_ss_if(tmem + acc, pq, dadd(xh, 2048 * kk), idP, 1u, lead);
+        }
+        commit_if(mb, lead);
+    };
+    uint32_t phase = 0;
+    bool failed = false;
+    auto wait_products = [&]() -> bool {   // every thread polls; the CTA takes one decision
+        const bool ok = mbar_wait(mb, phase & 1, wl);
+        ++phase;
+        const bool bad = __syncthreads_or(!ok);
+        fence_after_sync();
+        return !bad;
+    };
+    auto operands_ready = [&]() {
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+    };
+    for (int k = 1; k < nbc; ++k) {
+        const size_t u = unit(b0 + k);
+        split_rows(Qm + u * HQ * HD2, HQ, sb + S::QH, sb + S::QL);
+        split_rows(Pm + u * HD2 * HD2, HD2, sb + S::PH, sb + S::PL);
+        if (k == 1) split_rows(Pm + unit(b0) * HD2 * HD2, HD2, sb + S::XH, sb + S::XL);
+        else tmem_to_x(TA);
+        operands_ready();
+        products(TU, TA, 0u);
+        if (!wait_products()) { failed = true; break; }
+        // X = B (its tiles free now), and c_b into B's accumulator, this thread's row and column half
+        if (k == 1) split_rows(Cm + unit(b0) * HD2 * HD2, HD2, sb + S::XH, sb + S::XL);
+        else tmem_to_x(TB);
+        {
+            const float* cr = Cm + u * HD2 * HD2 + (size_t)row * HD2 + 64 * hf;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                uint32_t r[32];
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                    const float4 v = *reinterpret_cast<const float4*>(cr + 32 * q + e);
+                    r[e] = __float_as_uint(v.x); r[e + 1] = __float_as_uint(v.y);
+                    r[e + 2] = __float_as_uint(v.z); r[e + 3] = __float_as_uint(v.w);
+                }
+                tmem_st32(tmem + lane_base + TB + 64 * hf + 32 * q, r);
+            }
+            tmem_wait_st();
+        }
+        operands_ready();
+        products(TO, TB, 1u);
+        if (!wait_products()) { failed = true; break; }
+        // the block's query rows: U_t over Q'_t in the workspace, O_t added to o (tokens of the sequence)
+        {
+            const int t0 = (b0 + k) * HQ;
+            float x[32];
+            tmem_ld32(tmem + lane_base + TU + 32 * hf, x);
+            float* qr = Qm + u * HQ * HD2 + row;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) qr[(size_t)(32 * hf + e) * HD2] = x[e];
+            tmem_ld32(tmem + lane_base + TO + 32 * hf, x);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const int t = t0 + 32 * hf + e;
+                if (t < T) o[(bh * (size_t)T + t) * HD2 + row] += x[e];
+            }
+        }
+    }
+    if (!failed) {   // the chunk's summary, A then B
+#pragma unroll
+        for (int e2 = 0; e2 < 2; ++e2) {
+            float* dst = (e2 ? Bg : Ag) + (size_t)row * HD2 + 64 * hf;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                float x[32];
+                tmem_ld32(tmem + lane_base + (e2 ? TB : TA) + 64 * hf + 32 * q, x);
+#pragma unroll
+                for (int e = 0; e < 32; e += 4)
+                    *reinterpret_cast<float4*>(dst + 32 * q + e) = make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
+            }
+        }
+    } else if (tid == 0) {   // no product may outlive the tensor memory
+        atomicExch(status, (int)DPLR_ERR_TIMEOUT);
+        mma_commit(drain);
+        mbar_wait(drain, 0, 400000000LL);
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
 struct GSm {
     static constexpr int OPS = 0;                          // the step's A_j^T hi, lo, B_j^T hi, lo
     static constexpr int UTB = HD2 * HQ * 2;               // bf16 [128 k][64 q] MN-major B operand
@@ -560,7 +767,7 @@ dplr_status make_hla_plan(const dplr_desc* d, int L, HlaPlan* hp) {
     return DPLR_OK;
 }
 
-std::atomic<uint64_t> g_hla_smem[3] = {{0}, {0}, {0}};
+std::atomic<uint64_t> g_hla_smem[4] = {{0}, {0}, {0}, {0}};
 
 }  // namespace
 }  // namespace dplr
@@ -597,7 +804,13 @@ extern "C" dplr_status dplr_hla_forward(const dplr_desc* desc, const void* q, co
     if (launch_chunk_maps(pl, ma, s) != cudaSuccess) return DPLR_ERR_CUDA;   // pass 1 (o <- O_t)
     float* Acs = reinterpret_cast<float*>(ws + hp.off_A);
     float* Bcs = reinterpret_cast<float*>(ws + hp.off_B);
-    if (hp.m > 1) {   // pass 2
+    if (hp.m > 1 && pl.dk == HD2 && pl.dv == HD2) {   // pass 2 on the tensor cores
+        if (set_smem_limit_once(reinterpret_cast<const void*>(hla_compose_tc_kernel), CSm::TOTAL, g_hla_smem[3]) != cudaSuccess)
+            return DPLR_ERR_CUDA;
+        hla_compose_tc_kernel<<<(unsigned)((size_t)pl.BH * hp.N), kCT, CSm::TOTAL, s>>>(pl, hp.m, hp.N, ma.Pm, ma.Cm, ma.Qm, o,
+                                                                                       Acs, Bcs, reinterpret_cast<int*>(ws));
+        if (cudaGetLastError() != cudaSuccess) return DPLR_ERR_CUDA;
+    } else if (hp.m > 1) {   // pass 2 on the CUDA cores
         const size_t smem = sizeof(float) * (size_t)(2 * pl.dk * pl.dk + pl.dk * pl.dv + HQ * pl.dk);
         if (set_smem_limit_once(reinterpret_cast<const void*>(hla_compose_kernel), 227 * 1024, g_hla_smem[0]) != cudaSuccess)
             return DPLR_ERR_CUDA;

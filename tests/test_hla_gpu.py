@@ -41,8 +41,9 @@ def gates(H, T, L, seed, scale=2.0):
 
 
 CASES = [
-    # dtype, dk, dv, H, T, L, theta  (dk = dv = 128: the tensor-core gated pass)
+    # dtype, dk, dv, H, T, L, theta  (dk = dv = 128: the tensor-core composition and gated passes)
     ("bf16", 128, 128, 2, 700, 256, 0.1),
+    ("f32", 128, 128, 1, 450, 128, 0.1),
     ("bf16", 128, 128, 2, 300, 64, 0.0),
     ("f32", 128, 128, 1, 830, 64, 0.5),
     ("f32", 64, 64, 2, 500, 128, 0.1),
