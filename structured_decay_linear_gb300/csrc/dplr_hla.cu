@@ -23,6 +23,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <type_traits>
 #include <cstring>
 
 #include "dplr_internal.h"
@@ -366,21 +367,39 @@ hla_compose_tc_kernel(Plan pl, int m, int N, const float* Pm, const float* Cm, f
     fence_after_sync();
     const uint32_t tmem = *tmem_holder;
 
-    // fp32 rows [rows][128] from global memory into bf16 hi / lo tiles, row r and column n at sw_bf16(r, n, rows)
-    auto split_rows = [&](const float* src, int rows, uint32_t th, uint32_t tl) {
-        for (int i = tid; i < rows * 16; i += kCT) {
-            const int r = i >> 4, n = (i & 15) * 8;
-            const float4 a = *reinterpret_cast<const float4*>(src + (size_t)r * HD2 + n);
-            const float4 b = *reinterpret_cast<const float4*>(src + (size_t)r * HD2 + n + 4);
+    // fp32 rows [ROWS][128] from global memory into bf16 hi / lo tiles, row r and column n at sw_bf16(r, n, ROWS):
+    // every load of the thread is issued before the first store
+    auto split_rows = [&](auto rows_tag, const float* src, uint32_t th, uint32_t tl) {
+        constexpr int ROWS = decltype(rows_tag)::value, IT = ROWS * 16 / kCT;
+        float4 a[IT], b[IT];
+#pragma unroll
+        for (int it = 0; it < IT; ++it) {
+            const int i = tid + it * kCT, r = i >> 4, n = (i & 15) * 8;
+            a[it] = *reinterpret_cast<const float4*>(src + (size_t)r * HD2 + n);
+            b[it] = *reinterpret_cast<const float4*>(src + (size_t)r * HD2 + n + 4);
+        }
+#pragma unroll
+        for (int it = 0; it < IT; ++it) {
+            const int i = tid + it * kCT, r = i >> 4, n = (i & 15) * 8;
             uint32_t h[4], l[4];
-            split2(a.x, a.y, h[0], l[0]);
-            split2(a.z, a.w, h[1], l[1]);
-            split2(b.x, b.y, h[2], l[2]);
-            split2(b.z, b.w, h[3], l[3]);
-            const uint32_t off = sw_bf16(r, n, rows);
+            split2(a[it].x, a[it].y, h[0], l[0]);
+            split2(a[it].z, a[it].w, h[1], l[1]);
+            split2(b[it].x, b[it].y, h[2], l[2]);
+            split2(b[it].z, b[it].w, h[3], l[3]);
+            const uint32_t off = sw_bf16(r, n, ROWS);
             sts128(th + off, h[0], h[1], h[2], h[3]);
             sts128(tl + off, l[0], l[1], l[2], l[3]);
         }
+    };
+    using Rows64 = std::integral_constant<int, HQ>;
+    using Rows128 = std::integral_constant<int, HD2>;
+    // the maps of block b into L2, for the step that reads them next
+    auto prefetch_block = [&](int b) {
+        if (tid != 0 || b >= b0 + nbc) return;
+        const size_t ub = unit(b);
+        l2_prefetch(Pm + ub * HD2 * HD2, HD2 * HD2 * 4);
+        l2_prefetch(Cm + ub * HD2 * HD2, HD2 * HD2 * 4);
+        l2_prefetch(Qm + ub * HQ * HD2, HQ * HD2 * 4);
     };
     // this thread's row and column half of the accumulator at col0 into the A / B operand tiles
     auto tmem_to_x = [&](uint32_t col0) {
@@ -441,15 +460,16 @@ hla_compose_tc_kernel(Plan pl, int m, int N, const float* Pm, const float* Cm, f
     };
     for (int k = 1; k < nbc; ++k) {
         const size_t u = unit(b0 + k);
-        split_rows(Qm + u * HQ * HD2, HQ, sb + S::QH, sb + S::QL);
-        split_rows(Pm + u * HD2 * HD2, HD2, sb + S::PH, sb + S::PL);
-        if (k == 1) split_rows(Pm + unit(b0) * HD2 * HD2, HD2, sb + S::XH, sb + S::XL);
+        prefetch_block(b0 + k + 1);
+        split_rows(Rows64{}, Qm + u * HQ * HD2, sb + S::QH, sb + S::QL);
+        split_rows(Rows128{}, Pm + u * HD2 * HD2, sb + S::PH, sb + S::PL);
+        if (k == 1) split_rows(Rows128{}, Pm + unit(b0) * HD2 * HD2, sb + S::XH, sb + S::XL);
         else tmem_to_x(TA);
         operands_ready();
         products(TU, TA, 0u);
         if (!wait_products()) { failed = true; break; }
         // X = B (its tiles free now), and c_b into B's accumulator, this thread's row and column half
-        if (k == 1) split_rows(Cm + unit(b0) * HD2 * HD2, HD2, sb + S::XH, sb + S::XL);
+        if (k == 1) split_rows(Rows128{}, Cm + unit(b0) * HD2 * HD2, sb + S::XH, sb + S::XL);
         else tmem_to_x(TB);
         {
             const float* cr = Cm + u * HD2 * HD2 + (size_t)row * HD2 + 64 * hf;
@@ -478,11 +498,14 @@ hla_compose_tc_kernel(Plan pl, int m, int N, const float* Pm, const float* Cm, f
 #pragma unroll
             for (int e = 0; e < 32; ++e) qr[(size_t)(32 * hf + e) * HD2] = x[e];
             tmem_ld32(tmem + lane_base + TO + 32 * hf, x);
+            float* orow = o + (bh * (size_t)T + t0 + 32 * hf) * HD2 + row;
+            const int nv = min(32, T - t0 - 32 * hf);   // tokens of the sequence in this half
+            float ov[32];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int t = t0 + 32 * hf + e;
-                if (t < T) o[(bh * (size_t)T + t) * HD2 + row] += x[e];
-            }
+            for (int e = 0; e < 32; ++e) ov[e] = e < nv ? orow[(size_t)e * HD2] : 0.f;   // every load, then the stores
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+                if (e < nv) orow[(size_t)e * HD2] = ov[e] + x[e];
         }
     }
     if (!failed) {   // the chunk's summary, A then B
@@ -713,11 +736,14 @@ hla_gated_tc_kernel(Plan pl, int L, int N, float theta, GatedArgs args) {
             for (int hf = 0; hf < 2; ++hf) {
                 float x[32];
                 tmem_ld32(tmem + lane_base + 64 + 32 * hf, x);
+                float* orow = args.o + (bh * (size_t)T + t0 + 32 * hf) * HD2 + d;
+                const int nv = min(32, T - t0 - 32 * hf);   // queries of the sequence in this half
+                float ov[32];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int q = 32 * hf + e;
-                    if (t0 + q < T) args.o[(bh * (size_t)T + t0 + q) * HD2 + d] += x[e];
-                }
+                for (int e = 0; e < 32; ++e) ov[e] = e < nv ? orow[(size_t)e * HD2] : 0.f;   // every load, then the stores
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    if (e < nv) orow[(size_t)e * HD2] = ov[e] + x[e];
             }
         }
         if (failed && lane == 0) atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
