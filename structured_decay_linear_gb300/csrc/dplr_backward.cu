@@ -124,6 +124,37 @@ block_bwd_kernel(Plan pl, BwdArgs a) {
     const IT* Kin = static_cast<const IT*>(a.K);
     const IT* Vin = static_cast<const IT*>(a.V);
 
+    // The block's rows of every input, its dO rows and the three states it reads are contiguous: thread 0 asks
+    // for them in L2 first, so that the loads below wait on L2 rather than on DRAM.
+    const float* S0g = a.Sb + (bh * (size_t)nb + j) * (size_t)dk * dv;
+    const float* dSg = a.dSb + (bh * (size_t)nb + j) * (size_t)dk * dv;
+    const float* S1g = j + 1 < nb ? a.Sb + (bh * (size_t)nb + j + 1) * (size_t)dk * dv : a.ST + bh * (size_t)dk * dv;
+    if (tid == 0) {
+        auto pf = [&](const void* p, size_t bytes) {
+            if (p != nullptr && bytes > 0 && bytes % 16 == 0)
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                             :: "l"(reinterpret_cast<uint64_t>(p)), "r"((uint32_t)bytes) : "memory");
+        };
+        const size_t nt = (size_t)valid;
+        pf(q == nullptr ? nullptr : q + tok0 * dk, nt * dk * sizeof(IT));
+        if (MODE == DPLR_GENERIC) {
+            pf(Ain == nullptr ? nullptr : Ain + tok0 * r * dk, nt * r * dk * sizeof(IT));
+            pf(Bin == nullptr ? nullptr : Bin + tok0 * r * dk, nt * r * dk * sizeof(IT));
+            if (p > 0) {
+                pf(Kin == nullptr ? nullptr : Kin + tok0 * p * dk, nt * p * dk * sizeof(IT));
+                pf(Vin == nullptr ? nullptr : Vin + tok0 * p * dv, nt * p * dv * sizeof(IT));
+            }
+        } else {
+            pf(kin + tok0 * dk, nt * dk * sizeof(IT));
+            pf(vin + tok0 * dv, nt * dv * sizeof(IT));
+        }
+        if (MODE != DPLR_GDN) pf(a.decay + tok0 * dk, nt * dk * sizeof(float));
+        pf(a.dO + tok0 * dv, nt * dv * sizeof(float));
+        pf(S0g, (size_t)dk * dv * sizeof(float));
+        pf(dSg, (size_t)dk * dv * sizeof(float));
+        pf(S1g, (size_t)dk * dv * sizeof(float));
+    }
+
     // ---- the block's log-decay (identity padding past the end), its inclusive prefix per channel, the anchor
     for (int i = tid; i < cb * dk; i += nth) {
         const int t = i / dk, c = i - t * dk;
@@ -222,22 +253,27 @@ block_bwd_kernel(Plan pl, BwdArgs a) {
     __syncthreads();
 
     // ---- the state dimension in slices
-    const float* S0g = a.Sb + (bh * (size_t)nb + j) * (size_t)dk * dv;
-    const float* dSg = a.dSb + (bh * (size_t)nb + j) * (size_t)dk * dv;
-    const float* S1g = j + 1 < nb ? a.Sb + (bh * (size_t)nb + j + 1) * (size_t)dk * dv : a.ST + bh * (size_t)dk * dv;
     for (int n0 = 0; n0 < dv; n0 += BNS) {
+        // (BNS = 16 and nth a multiple of 32: the 16 lanes of a half-warp take the 16 columns of one row c, so
+        // the row's sum of S_j dS_j over the slice is a half-warp shuffle reduction, added by its first lane)
+#pragma unroll 4
         for (int i = tid; i < dk * BNS; i += nth) {
             const int c = i / BNS, n = i - c * BNS;
             const float e = __expf(va[c]);
             S0s[c * LS + n] = e * S0g[(size_t)c * dv + n0 + n];
             const float ds = dSg[(size_t)c * dv + n0 + n];
             dSs[c * LS + n] = e * ds;
-            atomicAdd(&sd[c], S1g[(size_t)c * dv + n0 + n] * ds);
+            float x = S1g[(size_t)c * dv + n0 + n] * ds;
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+            if (n == 0) sd[c] += x;
         }
+#pragma unroll 4
         for (int i = tid; i < cb * BNS; i += nth) {
             const int t = i / BNS, n = i - t * BNS;
             dOs[t * LS + n] = t < valid ? a.dO[(tok0 + t) * dv + n0 + n] : 0.f;
         }
+#pragma unroll 4
         for (int i = tid; i < P * BNS; i += nth) {
             const int u = i / BNS, n = i - u * BNS, t = u / p, e = u - t * p;
             float x = 0.f;

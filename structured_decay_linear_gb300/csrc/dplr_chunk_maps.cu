@@ -214,6 +214,30 @@ chunk_maps_kernel(Plan pl, ChunkMapArgs args) {
     const size_t tok0 = bh * (size_t)T + t0;   // flat token index of the block's first token
     const int tid = threadIdx.x, nth = blockDim.x;
 
+    // The block's token rows are contiguous in every input: thread 0 asks for them in L2 first, so that the
+    // staging loads below wait on L2 rather than on DRAM.
+    if (tid == 0) {
+        const size_t nt = (size_t)min(cw, T - t0);
+        auto pf = [&](const void* p, size_t row_bytes) {
+            if (p != nullptr && row_bytes % 16 == 0)
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                             :: "l"(reinterpret_cast<uint64_t>(static_cast<const char*>(p) + tok0 * row_bytes)),
+                                "r"((uint32_t)(nt * row_bytes)) : "memory");
+        };
+        pf(args.q, dk * sizeof(IT));
+        if (MODE == DPLR_GENERIC) {
+            pf(args.A, (size_t)R * dk * sizeof(IT));
+            pf(args.Bm, (size_t)R * dk * sizeof(IT));
+            if (P > 0) {
+                pf(args.K, (size_t)P * dk * sizeof(IT));
+                pf(args.V, (size_t)P * dv * sizeof(IT));
+            }
+        } else {
+            pf(args.k, dk * sizeof(IT));
+            pf(args.v, dv * sizeof(IT));
+        }
+        if (MODE != DPLR_GDN) pf(args.decay, dk * sizeof(float));
+    }
     // ---- a1/a2: stage decay and beta; inclusive cumulative log-decay per channel.
     for (int i = tid; i < cw * dkg; i += nth) {
         const int t = i / dkg, c = i % dkg;
@@ -241,6 +265,7 @@ chunk_maps_kernel(Plan pl, ChunkMapArgs args) {
     auto anc = [&](int c) { return 0.5f * G[(cw - 1) * dkg + (MODE == DPLR_GDN ? 0 : c)]; };
     const IT* qp = static_cast<const IT*>(args.q);
     constexpr int V = NV<IT>;   // elements per 16-byte load
+#pragma unroll 4
     for (int i = tid; i < cw * dk / V; i += nth) {
         const int t = i * V / dk, c0 = i * V % dk;
         float x[V];
@@ -251,6 +276,7 @@ chunk_maps_kernel(Plan pl, ChunkMapArgs args) {
     if (MODE == DPLR_GDN) {
         const IT* kp = static_cast<const IT*>(args.k);
         const IT* vp = static_cast<const IT*>(args.v);
+#pragma unroll 4
         for (int i = tid; i < cw * dk / V; i += nth) {
             const int t = i * V / dk, c0 = i * V % dk;
             float kk[V];
@@ -263,6 +289,7 @@ chunk_maps_kernel(Plan pl, ChunkMapArgs args) {
                 Bt[t * ldk + c] = expf(gp) * kk[e];             // e^{G_{t-1}} B_t with B = e^{g} k
             }
         }
+#pragma unroll 4
         for (int i = tid; i < cw * dv / V; i += nth) {
             const int t = i * V / dv, n0 = i * V % dv;
             float x[V];
@@ -289,6 +316,7 @@ chunk_maps_kernel(Plan pl, ChunkMapArgs args) {
             if (lane == 0) cdot[t] = s;
         }
         __syncthreads();
+#pragma unroll 4
         for (int i = tid; i < cw * dk / V; i += nth) {
             const int t = i * V / dk, c0 = i * V % dk;
             float kk[V];
@@ -306,6 +334,7 @@ chunk_maps_kernel(Plan pl, ChunkMapArgs args) {
                 Bt[(2 * t + 1) * ldk + c] = ex * b * kk[e];
             }
         }
+#pragma unroll 4
         for (int i = tid; i < cw * dv / V; i += nth) {
             const int t = i * V / dv, n0 = i * V % dv;
             float x[V];
@@ -321,6 +350,7 @@ chunk_maps_kernel(Plan pl, ChunkMapArgs args) {
         const IT* Bp = static_cast<const IT*>(args.Bm);
         const IT* Kp = static_cast<const IT*>(args.K);
         const IT* Vp = static_cast<const IT*>(args.V);
+#pragma unroll 4
         for (int i = tid; i < cr * dk / V; i += nth) {
             const int row = i * V / dk, c0 = i * V % dk, t = row / R, j = row % R;
             const bool ok = t0 + t < T;
@@ -335,6 +365,7 @@ chunk_maps_kernel(Plan pl, ChunkMapArgs args) {
                 Bt[row * ldk + c] = ok ? expf(Gx(t, c) - anc(c)) * b[e] : 0.f;
             }
         }
+#pragma unroll 4
         for (int i = tid; i < cp * dk / V; i += nth) {
             const int row = i * V / dk, c0 = i * V % dk, t = row / Pd, l = row % Pd;
             const bool ok = t0 + t < T;
@@ -343,6 +374,7 @@ chunk_maps_kernel(Plan pl, ChunkMapArgs args) {
 #pragma unroll
             for (int e = 0; e < V; ++e) Kt[row * ldk + c0 + e] = ok ? expf(-(Gi(t, c0 + e) - anc(c0 + e))) * x[e] : 0.f;
         }
+#pragma unroll 4
         for (int i = tid; i < cp * dv / V; i += nth) {
             const int row = i * V / dv, n0 = i * V % dv, t = row / Pd, l = row % Pd;
             float x[V];
