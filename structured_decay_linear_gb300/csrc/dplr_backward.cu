@@ -38,6 +38,9 @@ namespace {
 
 using smem::mm;
 using smem::mm_ksplit;
+using smem::mm_ksplit_out;
+using smem::KOut;
+using smem::KTerm;
 
 constexpr int BT = 256;      // threads of the block-backward kernel
 constexpr int BMX = 32;      // rows of A~ (R = cb r), K~ (P = cb p) and Q~ (cb) at most
@@ -281,18 +284,19 @@ block_bwd_kernel(Plan pl, BwdArgs a) {
             Vs[u * LS + n] = x;
         }
         __syncthreads();
-        // the slice's R x 16 products have few tiles: their K is split over every thread
-        mm_ksplit(Hs, LS, Bt, LD, false, S0s, LS, false, R, BNS, dk, 1.f, false, ks);
+        // the slice's R x 16 products have few tiles: their K is split over the threads, two outputs at a time
+        {   // H = B~ S0 + G V and dE = -(A~ dS^ + QA^T dO)
+            const KOut ko[2] = {
+                {Hs, LS, R, BNS, 1.f, false, 2, {{Bt, LD, false, S0s, LS, false, dk}, {Gm, LM, false, Vs, LS, false, P}, {}}},
+                {dEs, LS, R, BNS, -1.f, false, 2, {{At, LD, false, dSs, LS, false, dk}, {QA, LM, true, dOs, LS, false, cb}, {}}}};
+            mm_ksplit_out(ko, ks);
+        }
         __syncthreads();
-        mm_ksplit(dEs, LS, At, LD, false, dSs, LS, false, R, BNS, dk, -1.f, false, ks);
-        __syncthreads();
-        mm_ksplit(Hs, LS, Gm, LM, false, Vs, LS, false, R, BNS, P, 1.f, true, ks);
-        __syncthreads();
-        mm_ksplit(dEs, LS, QA, LM, true, dOs, LS, false, R, BNS, cb, -1.f, true, ks);
-        __syncthreads();
-        mm_ksplit(Es, LS, Mm, LM, false, Hs, LS, false, R, BNS, R, 1.f, false, ks);
-        __syncthreads();
-        mm_ksplit(dHs, LS, Mm, LM, true, dEs, LS, false, R, BNS, R, 1.f, false, ks);
+        {   // E = M H and dH = M^T dE
+            const KOut ko[2] = {{Es, LS, R, BNS, 1.f, false, 1, {{Mm, LM, false, Hs, LS, false, R}, {}, {}}},
+                                {dHs, LS, R, BNS, 1.f, false, 1, {{Mm, LM, true, dEs, LS, false, R}, {}, {}}}};
+            mm_ksplit_out(ko, ks);
+        }
         __syncthreads();
         mm(dAt, LD, Es, LS, false, dSs, LS, true, R, dk, BNS, -1.f, true);
         mm(dBt, LD, dHs, LS, false, S0s, LS, true, R, dk, BNS, 1.f, true);
@@ -305,11 +309,10 @@ block_bwd_kernel(Plan pl, BwdArgs a) {
         __syncthreads();
         // dV = K~ dS^ + QK^T dO + G^T dH for this slice, then to the output (a generic mode may have no K, V)
         if (P > 0) {
-            mm_ksplit(dVt, BNS, Kt, LD, false, dSs, LS, false, P, BNS, dk, 1.f, false, ks);
-            __syncthreads();
-            mm_ksplit(dVt, BNS, QK, LM, true, dOs, LS, false, P, BNS, cb, 1.f, true, ks);
-            __syncthreads();
-            mm_ksplit(dVt, BNS, Gm, LM, true, dHs, LS, false, P, BNS, R, 1.f, true, ks);
+            const KOut ko[1] = {{dVt, BNS, P, BNS, 1.f, false, 3,
+                                 {{Kt, LD, false, dSs, LS, false, dk}, {QK, LM, true, dOs, LS, false, cb},
+                                  {Gm, LM, true, dHs, LS, false, R}}}};
+            mm_ksplit_out(ko, ks);
             __syncthreads();
         }
         for (int idx = tid; idx < P * BNS; idx += nth) {
