@@ -37,7 +37,6 @@ namespace dplr {
 namespace {
 
 using smem::mm;
-using smem::mm_ksplit;
 using smem::mm_ksplit_out;
 using smem::KOut;
 using smem::KTerm;
@@ -223,17 +222,21 @@ block_bwd_kernel(Plan pl, BwdArgs a) {
 
     // ---- Gram blocks and the WY inverse M = (I + L)^{-1} (forward substitution, one column per thread)
     // (few tiles each, K = dk: split over every thread)
-    mm_ksplit(Mm, LM, Bt, LD, false, At, LD, true, R, R, dk, 1.f, false, ks);
-    __syncthreads();
-    if (P > 0) {
-        mm_ksplit(Gm, LM, Bt, LD, false, Kt, LD, true, R, P, dk, 1.f, false, ks);
-        __syncthreads();
-    }
-    mm_ksplit(QA, LM, Qt, LD, false, At, LD, true, cb, R, dk, 1.f, false, ks);
-    __syncthreads();
-    if (P > 0) {
-        mm_ksplit(QK, LM, Qt, LD, false, Kt, LD, true, cb, P, dk, 1.f, false, ks);
-        __syncthreads();
+    {
+        const KOut kl = {Mm, LM, R, R, 1.f, false, 1, {{Bt, LD, false, At, LD, true, dk}, {}, {}}};
+        const KOut kq = {QA, LM, cb, R, 1.f, false, 1, {{Qt, LD, false, At, LD, true, dk}, {}, {}}};
+        if (P > 0) {   // two at a time
+            const KOut g1[2] = {kl, {Gm, LM, R, P, 1.f, false, 1, {{Bt, LD, false, Kt, LD, true, dk}, {}, {}}}};
+            mm_ksplit_out(g1, ks);
+            __syncthreads();
+            const KOut g2[2] = {kq, {QK, LM, cb, P, 1.f, false, 1, {{Qt, LD, false, Kt, LD, true, dk}, {}, {}}}};
+            mm_ksplit_out(g2, ks);
+            __syncthreads();
+        } else {
+            const KOut g1[2] = {kl, kq};
+            mm_ksplit_out(g1, ks);
+            __syncthreads();
+        }
     }
     mask(Mm, LM, R, R, r, r, true);
     mask(Gm, LM, R, P, r, p, true);

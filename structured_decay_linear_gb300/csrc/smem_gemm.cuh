@@ -1,4 +1,5 @@
-// A block-wide fp32 product in shared memory (CUDA cores), shared by the backward and the HLA kernels.
+// Block-wide fp32 products in shared memory (CUDA cores): mm, and mm_ksplit_out for products with few tiles
+// and a long K. Shared by the backward and the HLA kernels.
 #pragma once
 
 namespace dplr {
@@ -36,56 +37,6 @@ __device__ __forceinline__ void mm(float* C, int ldc, const float* A, int lda, b
                 float* o = C + (m0 + i) * ldc + n0 + jj;
                 *o = acc ? *o + alpha * c[i][jj] : alpha * c[i][jj];
             }
-    }
-}
-
-// The same product for a small C (few 4 x 4 tiles) and a longer K: the CTA's threads split K into G groups
-// (G = threads / tiles), each thread one tile over its group's part of K, partial tiles into scratch
-// [G][M][N] (at most 16 blockDim.x floats); then every element of C sums its G partials in group order (a fixed
-// order: the result does not depend on the timing). The caller's threads must all call it; it ends with the sums
-// written (no barrier after). With more tiles than threads it is mm itself.
-__device__ __forceinline__ void mm_ksplit(float* C, int ldc, const float* A, int lda, bool ta, const float* B, int ldb,
-                                          bool tb, int M, int N, int K, float alpha, bool acc, float* scratch) {
-    const int nt = N >> 2, tiles = (M >> 2) * nt;
-    if (tiles > (int)blockDim.x) {
-        mm(C, ldc, A, lda, ta, B, ldb, tb, M, N, K, alpha, acc);
-        return;
-    }
-    const int G = max(1, (int)blockDim.x / tiles), kc = (K + G - 1) / G;
-    const int g = threadIdx.x / tiles, tile = threadIdx.x - g * tiles;
-    const int as = ta ? 1 : lda, ak = ta ? lda : 1;
-    const int bs = tb ? ldb : 1, bk = tb ? 1 : ldb;
-    if (g < G) {
-        const int m0 = (tile / nt) << 2, n0 = (tile % nt) << 2;
-        const int k0 = g * kc, k1 = min(K, k0 + kc);
-        float c[4][4] = {};
-        const float* Ap = A + m0 * as;
-        const float* Bp = B + n0 * bs;
-        for (int k = k0; k < k1; ++k) {
-            float a[4], b[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                a[i] = Ap[i * as + k * ak];
-                b[i] = Bp[i * bs + k * bk];
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) c[i][jj] = fmaf(a[i], b[jj], c[i][jj]);
-        }
-        float* P = scratch + (size_t)g * M * N;
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) P[(m0 + i) * N + n0 + jj] = c[i][jj];
-    }
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < M * N; idx += blockDim.x) {
-        float sum = 0.f;
-        for (int gg = 0; gg < G; ++gg) sum += scratch[(size_t)gg * M * N + idx];
-        const int m = idx / N, n = idx - m * N;
-        float* o = C + m * ldc + n;
-        *o = acc ? *o + alpha * sum : alpha * sum;
     }
 }
 
