@@ -305,10 +305,12 @@ block_bwd_kernel(Plan pl, BwdArgs a) {
         mm(dBt, LD, dHs, LS, false, S0s, LS, true, R, dk, BNS, 1.f, true);
         mm(dKt, LD, Vs, LS, false, dSs, LS, true, P, dk, BNS, 1.f, true);
         mm(dQt, LD, dOs, LS, false, S0s, LS, true, cb, dk, BNS, 1.f, true);
-        mm(dL, LM, dHs, LS, false, Es, LS, true, R, R, BNS, -1.f, true);
-        mm(dG, LM, dHs, LS, false, Vs, LS, true, R, P, BNS, 1.f, true);
-        mm(dQA, LM, dOs, LS, false, Es, LS, true, cb, R, BNS, -1.f, true);
-        mm(dQK, LM, dOs, LS, false, Vs, LS, true, cb, P, BNS, 1.f, true);
+        // (four small products, at most 64 tiles each: a quarter of the threads each)
+        const int q4 = nth / 4;
+        mm(dL, LM, dHs, LS, false, Es, LS, true, R, R, BNS, -1.f, true, 0, q4);
+        mm(dG, LM, dHs, LS, false, Vs, LS, true, R, P, BNS, 1.f, true, q4, q4);
+        mm(dQA, LM, dOs, LS, false, Es, LS, true, cb, R, BNS, -1.f, true, 2 * q4, q4);
+        mm(dQK, LM, dOs, LS, false, Vs, LS, true, cb, P, BNS, 1.f, true, 3 * q4, q4);
         __syncthreads();
         // dV = K~ dS^ + QK^T dO + G^T dH for this slice, then to the output (a generic mode may have no K, V)
         if (P > 0) {

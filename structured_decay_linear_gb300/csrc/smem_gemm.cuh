@@ -5,15 +5,18 @@
 namespace dplr {
 namespace smem {
 
-// C[m][n] (=, +=) alpha sum_k A(m, k) B(k, n) over the CTA's threads, with A(m, k) = A[m lda + k] (ta: A[k lda + m])
-// and B(k, n) = B[k ldb + n] (tb: B[n ldb + k]); all in shared memory. M and N are multiples of 4: each thread takes
+// C[m][n] (=, +=) alpha sum_k A(m, k) B(k, n) over the CTA's threads (or over threads t0 .. t0 + nt_ - 1 only, so
+// that independent small products can run side by side), with A(m, k) = A[m lda + k] (ta: A[k lda + m]) and
+// B(k, n) = B[k ldb + n] (tb: B[n ldb + k]); all in shared memory. M and N are multiples of 4: each thread takes
 // 4 x 4 tiles of C (8 shared loads per 16 FMAs).
 __device__ __forceinline__ void mm(float* C, int ldc, const float* A, int lda, bool ta, const float* B, int ldb,
-                                   bool tb, int M, int N, int K, float alpha, bool acc) {
+                                   bool tb, int M, int N, int K, float alpha, bool acc, int t0 = 0, int nt_ = 0) {
     const int nt = N >> 2, tiles = (M >> 2) * nt;
     const int as = ta ? 1 : lda, ak = ta ? lda : 1;   // A(m, k) = A[m as + k ak]
     const int bs = tb ? ldb : 1, bk = tb ? 1 : ldb;   // B(k, n) = B[k bk + n bs]
-    for (int tile = threadIdx.x; tile < tiles; tile += blockDim.x) {
+    const int step = nt_ > 0 ? nt_ : (int)blockDim.x, me = (int)threadIdx.x - t0;
+    if (me < 0 || me >= step) return;
+    for (int tile = me; tile < tiles; tile += step) {
         const int m0 = (tile / nt) << 2, n0 = (tile % nt) << 2;
         float c[4][4] = {};
         const float* Ap = A + m0 * as;
