@@ -17,7 +17,7 @@ namespace dplr {
 constexpr int kMaxStackedRows = 64;
 constexpr int kPrepThreads = 256;
 constexpr int kScanThreads = 256;
-constexpr int kScanCols = 16;  // state columns per scan CTA (dv split)
+constexpr int kScanCols = 32;  // state columns per scan CTA (dv split)
 
 // Everything the launches need, derived from a validated descriptor.
 struct Plan {
