@@ -420,6 +420,7 @@ def run_ours(args, w):
             "steps": K,
             "warmup": max(args.warmup, 3),
             "ms_per_step": step_ms,
+            "ms_per_step_median": statistics.median(a + b for a, b in zip(k1, k2)),   # this rank's steps
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
