@@ -152,6 +152,20 @@ hdla_chunk_kernel(Plan pl, K1Args args, const __grid_constant__ CUtensorMap tm_q
     const int s = tid & 127;   // tensor-memory lane of this thread (row of the chunk's 128-row tiles)
     const int qd = tid >> 7;   // which quarter of the columns this thread takes in the lane-mapped phases
 
+    // the TMA copies of unit ux's k, q, v (into R0 and V) and log-decay (thread 0)
+    auto stage_in = [&](long long ux) {
+        if (tid != 0) return;
+        const int jx = static_cast<int>(ux % NC);
+        const int y = static_cast<int>((ux / NC) * pl.T + (long long)jx * HCK);
+        mbar_expect_tx(mb_tma, 3 * 16384 + 32768);
+        for (int h = 0; h < 2; ++h) {
+            tma_load_2d(smem + S::K_ + h * 8192, &tm_k, 64 * h, y, mb_tma);
+            tma_load_2d(smem + S::Q_ + h * 8192, &tm_q, 64 * h, y, mb_tma);
+            tma_load_2d(smem + S::V + h * 8192, &tm_v, 64 * h, y, mb_tma);
+        }
+        for (int b = 0; b < 4; ++b) tma_load_2d(smem + S::LAM + b * 8192, &tm_l, 32 * b, y, mb_tma);
+    };
+    bool staged = false;   // this unit's copies were issued during the previous unit
   for (long long uidx = blockIdx.x; uidx < total && !failed; uidx += gridDim.x) {
     const int j = static_cast<int>(uidx % NC);
     const size_t bh = static_cast<size_t>(uidx / NC);
@@ -173,18 +187,10 @@ hdla_chunk_kernel(Plan pl, K1Args args, const __grid_constant__ CUtensorMap tm_q
         }
     }
 
-    // ---- a1: stage k, q, v and the log-decay of the chunk (TMA; plain loads for a ragged chunk)
+    // ---- a1: stage k, q, v and the log-decay of the chunk (TMA, issued during the previous unit's epilogue when
+    // there was one; plain loads for a ragged chunk)
     if (full) {
-        if (tid == 0) {
-            mbar_expect_tx(mb_tma, 3 * 16384 + 32768);
-            const int y = static_cast<int>(tok0);
-            for (int h = 0; h < 2; ++h) {
-                tma_load_2d(smem + S::K_ + h * 8192, &tm_k, 64 * h, y, mb_tma);
-                tma_load_2d(smem + S::Q_ + h * 8192, &tm_q, 64 * h, y, mb_tma);
-                tma_load_2d(smem + S::V + h * 8192, &tm_v, 64 * h, y, mb_tma);
-            }
-            for (int b = 0; b < 4; ++b) tma_load_2d(smem + S::LAM + b * 8192, &tm_l, 32 * b, y, mb_tma);
-        }
+        if (!staged) stage_in(uidx);
     } else {   // identity padding past the end: k = q = v = 0, log-decay 0, beta 0
         for (int i = tid; i < HCK * 16; i += K1T) {
             const int t = i >> 4, cb = i & 15;
@@ -519,6 +525,16 @@ hdla_chunk_kernel(Plan pl, K1Args args, const __grid_constant__ CUtensorMap tm_q
             ++mma_phase;
             if (__syncthreads_or(!ok)) failed = true;
             fence_after_sync();
+        }
+    }
+    // the last products have read R0 and V: the next unit's copies can land there during the epilogue
+    staged = false;
+    if (!failed && uidx + gridDim.x < total) {
+        const long long nx = uidx + gridDim.x;
+        if (pl.T - static_cast<int>(nx % NC) * HCK >= HCK) {
+            stage_in(nx);
+            staged = true;
+            tma_pending = true;
         }
     }
 
