@@ -44,6 +44,8 @@ CASES = [
     # dtype, dk, dv, H, T, L, theta  (dk = dv = 128: the tensor-core composition and gated passes)
     ("bf16", 128, 128, 2, 700, 256, 0.1),
     ("f32", 128, 128, 1, 450, 128, 0.1),
+    ("bf16", 128, 128, 1, 266, 256, 0.0),    # the last chunk a single ragged block
+    ("bf16", 128, 128, 2, 50, 256, 0.1),     # one chunk of one block: no history
     ("bf16", 128, 128, 2, 300, 64, 0.0),
     ("f32", 128, 128, 1, 830, 64, 0.5),
     ("f32", 64, 64, 2, 500, 128, 0.1),
