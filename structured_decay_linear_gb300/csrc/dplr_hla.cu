@@ -302,6 +302,341 @@ hla_split_kernel(int N, const float* Acs, const float* Bcs, unsigned char* tiles
     }
 }
 
+// ---- pass 1 on the tensor cores (Gated DeltaNet, bf16, dk = dv = 128): the exact maps of one 64-token block,
+// the same quantities as the fp32 chunk-map kernel. With G_t the inclusive cumulative log-gate, a = G_C / 2,
+// eb_t = e^{G_t - a}, w_t = e^{a - G_t} beta_t and D = [K; Q] K^T (raw bf16 k, q: exact):
+//     L_ts = e^{G_t - G_s} beta_s (k_t . k_s)  (s < t),   QA_ts = e^{G_t - G_s} beta_s (q_t . k_s)  (s <= t)
+//     M = (I + L)^{-1},  Y = M Diag(eb) K,  U = -M V
+//     P = e^{G_C} (I - K^T Diag(w) Y),  c = -e^{G_C - a} K^T Diag(w) U
+//     Q'_t = e^{G_t} q_t - e^{a} (QA Y)_t,  O = -QA U
+// D on the tensor cores in one term; L and QA scaled in fp32; M by the blocked fp32 inverse (three-term tf32
+// merges); then Y^T = K^T (M Diag(eb))^T and U^T = V^T (-M)^T, P and c as K^T [Diag(w) Y] and K^T [Diag(w) U],
+// and (Q A Y)^T, (QA U)^T, each with the rounded operand in bf16 hi + lo (the raw k and v are exact in bf16).
+// Tensor-memory columns: D, then (QA Y)^T (0-63); Y^T (64-127); U^T (128-191); P (192-319); c (320-447);
+// (QA U)^T (448-511).
+struct BSm {
+    static constexpr int KQ = 0;                  // [k 0-63 | q 0-63 | k 64-127 | q 64-127] features, 64 tokens each
+    static constexpr int VT = KQ + 32768;         // v: two halves of 64 features (8 KB each)
+    static constexpr int X = VT + 16384;          // fp32 [64][kLdX]: L, then M
+    static constexpr int QAF = X + 64 * kLdX * 4; // fp32 [64][kLdX]: QA
+    static constexpr int MB = QAF + 64 * kLdX * 4;   // M Diag(eb): hi, lo [64][64] (8 KB each)
+    static constexpr int MN = MB + 16384;         // -M: hi, lo
+    static constexpr int QT = MN + 16384;         // QA: hi, lo [64 t][64 s]
+    static constexpr int YW = QT + 16384;         // Diag(w) Y, then Y, as [128 k][64 t]: hi, lo (16 KB each)
+    static constexpr int UW = YW + 32768;         // Diag(w) U, then -U, as [128 n][64 t]: hi, lo
+    static constexpr int VEC = UW + 32768;        // G [64], eb [64], w [64], e^{G_C}, e^{G_C - a}, e^a
+    static constexpr int BAR = VEC + 1024;
+    static constexpr int TOTAL = BAR + 64;
+};
+static_assert(BSm::TOTAL <= 227 * 1024, "shared memory budget");
+static_assert(BSm::MB % 1024 == 0 && BSm::YW % 1024 == 0 && BSm::UW % 1024 == 0 && BSm::QT % 1024 == 0,
+              "swizzled tiles are 1024-byte aligned");
+constexpr int kBT = 256;   // threads: warp w takes tensor-memory lanes 32 (w % 4) .. + 31 and column half w / 4
+
+__global__ void __launch_bounds__(kBT, 1)
+hla_block_maps_tc_kernel(Plan pl, const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv_bfloat16* v,
+                         const float* g, const float* beta, float* Pm, float* Cm, float* Qm, float* o, int* status) {
+    using S = BSm;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const uint32_t sb = smem_addr(smem);
+    if (sb & 1023u) {
+        if (threadIdx.x == 0) atomicExch(status, (int)DPLR_ERR_CUDA);
+        return;
+    }
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::BAR);
+    uint64_t* mb = bars + 0;
+    uint64_t* drain = bars + 1;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2);
+    float* X = reinterpret_cast<float*>(smem + S::X);
+    float* QAf = reinterpret_cast<float*>(smem + S::QAF);
+    float* vG = reinterpret_cast<float*>(smem + S::VEC);
+    float* veb = vG + 64;
+    float* vw = vG + 128;
+    float* vsc = vG + 192;   // e^{G_C}, e^{G_C - a}, e^a
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int row = 32 * (warp & 3) + lane, hf = warp >> 2;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const int T = pl.T, nb = pl.nb;
+    const int blk = blockIdx.x % nb;
+    const size_t bh = blockIdx.x / nb;
+    const int t0 = blk * HQ, valid = min(HQ, T - t0);
+    const size_t tok0 = bh * (size_t)T + t0;
+    const size_t unit = bh * (size_t)nb + blk;
+    const long long wl = pl.wait_cycles;
+    constexpr uint32_t TD = 0, TY = 64, TU = 128, TP = 192, TC = 320, TO = 448;
+
+    if (tid == 0) {
+        mbar_init(mb, 1);
+        mbar_init(drain, 1);
+        mbar_fence_init();
+    }
+    if (warp == 0) tmem_alloc(tmem_holder, 512);
+    // ---- k, q, v of the block (zeros past the sequence), in the 128-byte swizzled layout
+    for (int i = tid; i < HQ * 16; i += kBT) {
+        const int t = i >> 4, cb = i & 15;
+        uint4 zk = make_uint4(0, 0, 0, 0), zq = zk, zv = zk;
+        if (t < valid) {
+            const size_t gix = (tok0 + t) * HD2 + 8 * cb;
+            zk = *reinterpret_cast<const uint4*>(k + gix);
+            zq = *reinterpret_cast<const uint4*>(q + gix);
+            zv = *reinterpret_cast<const uint4*>(v + gix);
+        }
+        const uint32_t off = swz(t, cb & 7);
+        sts128(sb + S::KQ + (cb >> 3) * 16384 + off, zk.x, zk.y, zk.z, zk.w);
+        sts128(sb + S::KQ + (cb >> 3) * 16384 + 8192 + off, zq.x, zq.y, zq.z, zq.w);
+        sts128(sb + S::VT + (cb >> 3) * 8192 + off, zv.x, zv.y, zv.z, zv.w);
+    }
+    // ---- the gates (warp 0: tokens 2 lane, 2 lane + 1; identity past the sequence)
+    if (warp == 0) {
+        const int ta = 2 * lane, tb = ta + 1;
+        const float g0 = ta < valid ? g[tok0 + ta] : 0.f, g1 = tb < valid ? g[tok0 + tb] : 0.f;
+        const float b0 = ta < valid ? beta[tok0 + ta] : 0.f, b1 = tb < valid ? beta[tok0 + tb] : 0.f;
+        float sum = g0 + g1;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, sum, off);
+            if (lane >= off) sum += y;
+        }
+        const float GC = __shfl_sync(0xffffffffu, sum, 31), G1 = sum, G0 = sum - g1, a = 0.5f * GC;
+        vG[ta] = G0; vG[tb] = G1;
+        veb[ta] = __expf(G0 - a); veb[tb] = __expf(G1 - a);
+        vw[ta] = __expf(a - G0) * b0; vw[tb] = __expf(a - G1) * b1;
+        if (lane == 0) {
+            vsc[0] = __expf(GC);
+            vsc[1] = __expf(GC - a);
+            vsc[2] = __expf(a);
+        }
+    }
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tmem_holder;
+    uint32_t phase = 0;
+    bool failed = false;
+    auto wait_products = [&]() -> bool {
+        const bool ok = mbar_wait(mb, phase & 1, wl);
+        ++phase;
+        const bool bad = __syncthreads_or(!ok);
+        fence_after_sync();
+        return !bad;
+    };
+    auto operands_ready = [&]() {
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+    };
+    const uint32_t lead = (warp == 0 && lane == 0) ? 1u : 0u;
+    // Kt: K^T (or V^T) as the MN-major A operand over the tokens; halves of 64 features `half` bytes apart
+    auto mn_desc = [&](uint32_t base, uint32_t half) { return smem_desc_sw128(sb + base, half, 1024); };
+
+    // ---- D = [K; Q] K^T
+    if (warp == 0) {
+        const uint32_t id = idesc_bf16(128, 64, false, false);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+            const uint64_t ad = smem_desc_sw128(sb + S::KQ + ko, 16, 1024);
+            mma_ss_if(tmem + TD, ad, ad, id, kk > 0 ? 1u : 0u, lead);   // B: the first 64 rows (k) of the same tile
+        }
+        commit_if(mb, lead);
+    }
+    if (!wait_products()) failed = true;
+
+    if (!failed) {
+        // ---- L (rows 0-63, lanes of k) and QA (rows 64-127, lanes of q), this thread's half of the columns s
+        float x[32];
+        tmem_ld32(tmem + lane_base + TD + 32 * hf, x);
+        const int t = row & 63;
+        const float Gt = vG[t];
+        if (row < 64) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+                const int s0 = 32 * hf + e;
+                float4 y;
+                y.x = s0 + 0 < t ? __expf(Gt - vG[s0 + 0]) * vw[s0 + 0] * veb[s0 + 0] * x[e + 0] : 0.f;
+                y.y = s0 + 1 < t ? __expf(Gt - vG[s0 + 1]) * vw[s0 + 1] * veb[s0 + 1] * x[e + 1] : 0.f;
+                y.z = s0 + 2 < t ? __expf(Gt - vG[s0 + 2]) * vw[s0 + 2] * veb[s0 + 2] * x[e + 2] : 0.f;
+                y.w = s0 + 3 < t ? __expf(Gt - vG[s0 + 3]) * vw[s0 + 3] * veb[s0 + 3] * x[e + 3] : 0.f;
+                *reinterpret_cast<float4*>(X + t * kLdX + s0) = y;
+            }
+        } else {
+            float qa[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const int s0 = 32 * hf + e;
+                qa[e] = s0 <= t ? __expf(Gt - vG[s0]) * vw[s0] * veb[s0] * x[e] : 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+                *reinterpret_cast<float4*>(QAf + t * kLdX + 32 * hf + e) = make_float4(qa[e], qa[e + 1], qa[e + 2], qa[e + 3]);
+#pragma unroll
+            for (int c8 = 0; c8 < 4; ++c8) {   // QA as the K-major B operand [t][s]: hi, lo
+                uint32_t h[4], l[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) split2(qa[8 * c8 + 2 * e], qa[8 * c8 + 2 * e + 1], h[e], l[e]);
+                const uint32_t off = swz(t, 4 * hf + c8);
+                sts128(sb + S::QT + off, h[0], h[1], h[2], h[3]);
+                sts128(sb + S::QT + 8192 + off, l[0], l[1], l[2], l[3]);
+            }
+        }
+        __syncthreads();
+        // ---- M = (I + L)^{-1} in place
+        inv64_inplace<3>(X, tid, 1);
+        __syncthreads();
+        // ---- M Diag(eb) and -M as K-major B operands [s][u]: hi, lo
+        for (int i = tid; i < 64 * 8; i += kBT) {
+            const int r = i >> 3, c8 = i & 7;
+            const float4 m0 = *reinterpret_cast<const float4*>(X + r * kLdX + 8 * c8);
+            const float4 m1 = *reinterpret_cast<const float4*>(X + r * kLdX + 8 * c8 + 4);
+            const float mv[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+            uint32_t bh_[4], bl_[4], nh[4], nl[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int u = 8 * c8 + 2 * e;
+                split2(mv[2 * e] * veb[u], mv[2 * e + 1] * veb[u + 1], bh_[e], bl_[e]);
+                split2(-mv[2 * e], -mv[2 * e + 1], nh[e], nl[e]);
+            }
+            const uint32_t off = swz(r, c8);
+            sts128(sb + S::MB + off, bh_[0], bh_[1], bh_[2], bh_[3]);
+            sts128(sb + S::MB + 8192 + off, bl_[0], bl_[1], bl_[2], bl_[3]);
+            sts128(sb + S::MN + off, nh[0], nh[1], nh[2], nh[3]);
+            sts128(sb + S::MN + 8192 + off, nl[0], nl[1], nl[2], nl[3]);
+        }
+        operands_ready();
+        // ---- Y^T = K^T (M Diag(eb))^T and U^T = V^T (-M)^T
+        if (warp == 0) {
+            const uint32_t id = idesc_bf16(128, 64, true, false);
+            const uint64_t ak = mn_desc(S::KQ, 16384), av = mn_desc(S::VT, 8192);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t bh_ = smem_desc_sw128(sb + S::MB + 32 * kk, 16, 1024), bl_ = dadd(bh_, 8192);
+                const uint64_t nh = smem_desc_sw128(sb + S::MN + 32 * kk, 16, 1024), nl = dadd(nh, 8192);
+                mma_ss_if(tmem + TY, dadd(ak, 2048 * kk), bh_, id, kk > 0 ? 1u : 0u, lead);
+                mma_ss_if(tmem + TY, dadd(ak, 2048 * kk), bl_, id, 1u, lead);
+                mma_ss_if(tmem + TU, dadd(av, 2048 * kk), nh, id, kk > 0 ? 1u : 0u, lead);
+                mma_ss_if(tmem + TU, dadd(av, 2048 * kk), nl, id, 1u, lead);
+            }
+            commit_if(mb, lead);
+        }
+        if (!wait_products()) failed = true;
+    }
+    // this thread's row of Y^T (or U^T), tokens 32 hf .., times f_t, as bf16 hi / lo at row `row` of the tiles
+    auto rows_out = [&](uint32_t col, uint32_t tile, const float* f, float sgn) {
+        float x[32];
+        tmem_ld32(tmem + lane_base + col + 32 * hf, x);
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8) {
+            uint32_t h[4], l[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int t = 32 * hf + 8 * c8 + 2 * e;
+                const float f0 = f ? f[t] : 1.f, f1 = f ? f[t + 1] : 1.f;
+                split2(sgn * f0 * x[8 * c8 + 2 * e], sgn * f1 * x[8 * c8 + 2 * e + 1], h[e], l[e]);
+            }
+            const uint32_t off = swz(row, 4 * hf + c8);
+            sts128(sb + tile + off, h[0], h[1], h[2], h[3]);
+            sts128(sb + tile + 16384 + off, l[0], l[1], l[2], l[3]);
+        }
+    };
+    if (!failed) {
+        rows_out(TY, S::YW, vw, 1.f);   // Diag(w) Y, row k
+        rows_out(TU, S::UW, vw, 1.f);   // Diag(w) U, row n
+        operands_ready();
+        // ---- K^T [Diag(w) Y] and K^T [Diag(w) U]
+        if (warp == 0) {
+            const uint32_t id = idesc_bf16(128, 128, true, false);
+            const uint64_t ak = mn_desc(S::KQ, 16384);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t yh = smem_desc_sw128(sb + S::YW + 32 * kk, 16, 1024), yl = dadd(yh, 16384);
+                const uint64_t uh = smem_desc_sw128(sb + S::UW + 32 * kk, 16, 1024), ul = dadd(uh, 16384);
+                mma_ss_if(tmem + TP, dadd(ak, 2048 * kk), yh, id, kk > 0 ? 1u : 0u, lead);
+                mma_ss_if(tmem + TP, dadd(ak, 2048 * kk), yl, id, 1u, lead);
+                mma_ss_if(tmem + TC, dadd(ak, 2048 * kk), uh, id, kk > 0 ? 1u : 0u, lead);
+                mma_ss_if(tmem + TC, dadd(ak, 2048 * kk), ul, id, 1u, lead);
+            }
+            commit_if(mb, lead);
+        }
+        if (!wait_products()) failed = true;
+    }
+    if (!failed) {
+        rows_out(TY, S::YW, nullptr, 1.f);    // Y, row k (the A operand of (QA Y)^T)
+        rows_out(TU, S::UW, nullptr, -1.f);   // -U, row n
+        operands_ready();
+        // ---- (QA Y)^T = Y^T QA^T and O^T = (-U)^T QA^T
+        if (warp == 0) {
+            const uint32_t id = idesc_bf16(128, 64, false, false);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t yh = smem_desc_sw128(sb + S::YW + 32 * kk, 16, 1024), yl = dadd(yh, 16384);
+                const uint64_t uh = smem_desc_sw128(sb + S::UW + 32 * kk, 16, 1024), ul = dadd(uh, 16384);
+                const uint64_t qh = smem_desc_sw128(sb + S::QT + 32 * kk, 16, 1024), ql = dadd(qh, 8192);
+                mma_ss_if(tmem + TD, yh, qh, id, kk > 0 ? 1u : 0u, lead);
+                mma_ss_if(tmem + TD, yh, ql, id, 1u, lead);
+                mma_ss_if(tmem + TD, yl, qh, id, 1u, lead);
+                mma_ss_if(tmem + TO, uh, qh, id, kk > 0 ? 1u : 0u, lead);
+                mma_ss_if(tmem + TO, uh, ql, id, 1u, lead);
+                mma_ss_if(tmem + TO, ul, qh, id, 1u, lead);
+            }
+            commit_if(mb, lead);
+        }
+        if (!wait_products()) failed = true;
+    }
+    if (!failed) {
+        // ---- the maps: P and c rows (lane = row i, this thread's half of the columns), Q' and O columns
+        const float eGC = vsc[0], eGCa = vsc[1], ea = vsc[2];
+        float* Pr = Pm + unit * HD2 * HD2 + (size_t)row * HD2 + 64 * hf;
+        float* Cr = Cm + unit * HD2 * HD2 + (size_t)row * HD2 + 64 * hf;
+#pragma unroll
+        for (int qq = 0; qq < 2; ++qq) {
+            float x[32];
+            tmem_ld32(tmem + lane_base + TP + 64 * hf + 32 * qq, x);
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+                const int c0 = 64 * hf + 32 * qq + e;
+                float4 y;
+                y.x = eGC * ((c0 + 0 == row ? 1.f : 0.f) - x[e + 0]);
+                y.y = eGC * ((c0 + 1 == row ? 1.f : 0.f) - x[e + 1]);
+                y.z = eGC * ((c0 + 2 == row ? 1.f : 0.f) - x[e + 2]);
+                y.w = eGC * ((c0 + 3 == row ? 1.f : 0.f) - x[e + 3]);
+                *reinterpret_cast<float4*>(Pr + 32 * qq + e) = y;
+            }
+            tmem_ld32(tmem + lane_base + TC + 64 * hf + 32 * qq, x);
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+                *reinterpret_cast<float4*>(Cr + 32 * qq + e) =
+                    make_float4(-eGCa * x[e], -eGCa * x[e + 1], -eGCa * x[e + 2], -eGCa * x[e + 3]);
+        }
+        {   // Q'[t][k] = e^{G_t} q_t[k] - e^a (QA Y)[t][k] (lane = k), O[t][n] (lane = n): tokens 32 hf ..
+            float x[32];
+            tmem_ld32(tmem + lane_base + TD + 32 * hf, x);
+            float* Qc = Qm + unit * HQ * HD2 + row;
+            const uint32_t qrow = sb + S::KQ + (row >> 6) * 16384 + 8192 + ((row & 7) << 1);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const int t = 32 * hf + e;
+                const float qt = lds_bf16(qrow + swz(t, (row & 63) >> 3));
+                Qc[(size_t)t * HD2] = __expf(vG[t]) * qt - ea * x[e];
+            }
+            tmem_ld32(tmem + lane_base + TO + 32 * hf, x);
+            float* oc = o + (tok0 + 32 * hf) * HD2 + row;
+            const int nv = min(32, valid - 32 * hf);
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+                if (e < nv) oc[(size_t)e * HD2] = x[e];
+        }
+    } else if (tid == 0) {   // no product may outlive the tensor memory
+        atomicExch(status, (int)DPLR_ERR_TIMEOUT);
+        mma_commit(drain);
+        mbar_wait(drain, 0, 400000000LL);
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
 // ---- pass 2 on the tensor cores (dk = dv = 128): one CTA per (head, L-chunk) walks the chunk's blocks b = b0 + 1 ..
 // with the composition of its earlier blocks, A (dk x dk) and B (dk x dv), held in tensor memory:
 //     U^T = A^T Q'_b^T,  O^T = B^T Q'_b^T     (M = 128 features, N = 64 tokens, K = 128)
@@ -793,7 +1128,7 @@ dplr_status make_hla_plan(const dplr_desc* d, int L, HlaPlan* hp) {
     return DPLR_OK;
 }
 
-std::atomic<uint64_t> g_hla_smem[4] = {{0}, {0}, {0}, {0}};
+std::atomic<uint64_t> g_hla_smem[5] = {{0}, {0}, {0}, {0}, {0}};
 
 }  // namespace
 }  // namespace dplr
@@ -827,7 +1162,16 @@ extern "C" dplr_status dplr_hla_forward(const dplr_desc* desc, const void* q, co
     ma.Pm = reinterpret_cast<float*>(ws + pl.off_P);
     ma.Cm = reinterpret_cast<float*>(ws + pl.off_c);
     ma.Qm = reinterpret_cast<float*>(ws + pl.off_Q);
-    if (launch_chunk_maps(pl, ma, s) != cudaSuccess) return DPLR_ERR_CUDA;   // pass 1 (o <- O_t)
+    if (pl.bf16 && pl.dk == HD2 && pl.dv == HD2) {   // pass 1 on the tensor cores (o <- O_t)
+        if (set_smem_limit_once(reinterpret_cast<const void*>(hla_block_maps_tc_kernel), BSm::TOTAL, g_hla_smem[4]) != cudaSuccess)
+            return DPLR_ERR_CUDA;
+        hla_block_maps_tc_kernel<<<(unsigned)((size_t)pl.BH * pl.nb), kBT, BSm::TOTAL, s>>>(
+            pl, static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v),
+            g, beta, ma.Pm, ma.Cm, ma.Qm, o, reinterpret_cast<int*>(ws));
+        if (cudaGetLastError() != cudaSuccess) return DPLR_ERR_CUDA;
+    } else if (launch_chunk_maps(pl, ma, s) != cudaSuccess) {   // pass 1 in fp32 (o <- O_t)
+        return DPLR_ERR_CUDA;
+    }
     float* Acs = reinterpret_cast<float*>(ws + hp.off_A);
     float* Bcs = reinterpret_cast<float*>(ws + hp.off_B);
     if (hp.m > 1 && pl.dk == HD2 && pl.dv == HD2) {   // pass 2 on the tensor cores
