@@ -640,8 +640,8 @@ def run_hla(args):
                       "gate_pairs_total": H * sum((qb * 64) // L for qb in range(T // 64)),
                       "gated_pass_tflops_over_the_call": flops / (ms * 1e-3) / 1e12, "gdn_forward_ms": ms_fwd,
                       "output_finite": bool(torch.isfinite(f.o).all().item()), "path": f.path,
-                      "arithmetic": ("64-token block maps f32 (CUDA cores); chunk composition and gated composition "
-                                     "bf16 hi + lo on tcgen05, f32 accumulate" if f.path == "hla_gated_tcgen05"
+                      "arithmetic": ("block maps, chunk composition and gated composition bf16 hi + lo on tcgen05, "
+                                     "f32 accumulate and inverse" if f.path == "hla_gated_tcgen05"
                                      else "f32 (CUDA cores)")}),
           flush=True)
 

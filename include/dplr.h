@@ -211,10 +211,10 @@ DPLR_API dplr_status dplr_la_backward(const dplr_desc* desc,
  * zero. q, k, v, g, beta as for dplr_la_forward (no initial state). o [B,H,T,dv] fp32. Workspace:
  * dplr_hla_workspace_size(desc, L) bytes, 256-byte aligned; its first 256 bytes are a status word, zeroed by the
  * call, into which a bounded wait of the tensor-core pass that gives up writes DPLR_ERR_TIMEOUT (read it with
- * dplr_la_read_status). The maps of 64-token blocks are formed in fp32 on the CUDA cores. For dk = dv = 128 the
- * L-chunk summaries are composed from them on the tensor cores, and so is the gated composition when there are
- * at most 256 chunks (bf16 hi + lo operands, fp32 accumulation; dplr_hla_path); in fp32 on the CUDA cores
- * otherwise. Asynchronous on `stream`; allocates nothing. Errors: DPLR_ERR_INVALID_ARG for another
+ * dplr_la_read_status). For dk = dv = 128 the maps of 64-token blocks (bf16 inputs), the L-chunk summaries
+ * composed from them, and the gated composition (at most 256 chunks; dplr_hla_path) run on the tensor cores (bf16
+ * hi + lo operands, fp32 accumulation); in fp32 on the CUDA cores otherwise. Asynchronous on `stream`; allocates
+ * nothing. Errors: DPLR_ERR_INVALID_ARG for another
  * mode or a null / misaligned pointer, DPLR_ERR_UNSUPPORTED for another L or dk, dv > 128, DPLR_ERR_WORKSPACE,
  * DPLR_ERR_CUDA. */
 DPLR_API size_t dplr_hla_workspace_size(const dplr_desc* desc, int L);

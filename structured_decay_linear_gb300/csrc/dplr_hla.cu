@@ -10,7 +10,7 @@
 // prefix) and O_i its output from a zero state. Unrolling the composition from the newest chunk backwards:
 //     o_i = O_i;  for j = c - 1 .. 0:  o_i += w_ij U_i B_j;  U_i <- (1 - w_ij) U_i + w_ij U_i A_j
 // (the page's reverse-order history readout). Three passes:
-//   1. the fp32 chunk-map kernel at WY blocks of 64 tokens: P_b, c_b, the readout rows Q'_t and O_t;
+//   1. the maps of the WY blocks of 64 tokens: P_b, c_b, the readout rows Q'_t and O_t;
 //   2. (L > 64) the L-chunk summaries composed from their blocks, A = P_{m-1} .. P_0, B likewise, and each
 //      query's row U_t = Q'_t (the composition of its chunk's earlier blocks), its output O_t updated;
 //   3. per 64 queries of one chunk, the history chunks newest first: two products per chunk, U A_j and U B_j,
@@ -18,8 +18,8 @@
 // For dk = dv = 128, passes 2 and 3 run on the tensor cores (tcgen05, bf16 hi + lo operands, three partial
 // products, fp32 accumulators in tensor memory: the products keep ~16 significant bits of each operand, against
 // the 1e-3 of the output RMS this composition is held to); pass 3 after a small pass that splits each chunk's A_j
-// and B_j into bf16 hi/lo operand tiles once. Otherwise both run in fp32 on the CUDA cores (4 x 4 register
-// tiles).
+// and B_j into bf16 hi/lo operand tiles once. Pass 1 runs there too when the inputs are bf16. Otherwise the
+// passes run in fp32 on the CUDA cores (4 x 4 register tiles).
 #include <cuda_bf16.h>
 
 #include <algorithm>
