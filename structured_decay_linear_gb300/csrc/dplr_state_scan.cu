@@ -10,6 +10,8 @@
 // so each CTA owns a block of kScanCols state columns of one head and walks all
 // chunks. The next chunk's maps are copied in (cp.async) while the current one is
 // applied.
+#include <algorithm>
+
 #include "dplr_internal.h"
 
 namespace dplr {
@@ -69,7 +71,7 @@ __device__ __forceinline__ void tile_4x4(const float* A, int lda, const float* S
     }
 }
 
-__global__ void __launch_bounds__(kScanThreads)
+__global__ void __launch_bounds__(2 * kScanThreads, 1)
 state_scan_kernel(Plan pl, ScanArgs args) {
     extern __shared__ __align__(16) float sm[];
     const int dk = pl.dk, dv = pl.dv, cw = pl.cw, T = pl.T;
@@ -178,7 +180,10 @@ cudaError_t launch_state_scan(const Plan& pl, const ScanArgs& a, cudaStream_t s)
     cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(state_scan_kernel), 227 * 1024, done);
     if (e != cudaSuccess) return e;
     const long long grid = (long long)pl.BH * (pl.dv / nv);
-    state_scan_kernel<<<(unsigned)grid, kScanThreads, smem, s>>>(pl, a);
+    // one 4 x 4 tile per thread: the state update's and the readout's tiles side by side, not one after the other
+    const int tiles = (pl.dk / 4) * (nv / 4) + (pl.cw / 4) * (nv / 4);
+    const int nth = std::min(2 * kScanThreads, std::max(kScanThreads, (tiles + 31) / 32 * 32));
+    state_scan_kernel<<<(unsigned)grid, nth, smem, s>>>(pl, a);
     return cudaGetLastError();
 }
 
