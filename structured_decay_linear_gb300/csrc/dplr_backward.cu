@@ -301,10 +301,50 @@ block_bwd_kernel(Plan pl, BwdArgs a) {
             mm_ksplit_out(ko, ks);
         }
         __syncthreads();
-        mm(dAt, LD, Es, LS, false, dSs, LS, true, R, dk, BNS, -1.f, true);
-        mm(dBt, LD, dHs, LS, false, S0s, LS, true, R, dk, BNS, 1.f, true);
-        mm(dKt, LD, Vs, LS, false, dSs, LS, true, P, dk, BNS, 1.f, true);
-        mm(dQt, LD, dOs, LS, false, S0s, LS, true, cb, dk, BNS, 1.f, true);
+        if (R == cb && P == cb) {   // (rank 1) the four in one pass: dS^ and S0 columns loaded once for two each
+            const int nt = dk >> 2;
+            for (int tile = tid; tile < (cb >> 2) * nt; tile += nth) {
+                const int m0 = (tile / nt) << 2, n0 = (tile % nt) << 2;
+                float cA[4][4] = {}, cB[4][4] = {}, cK[4][4] = {}, cQ[4][4] = {};
+#pragma unroll 4
+                for (int kx = 0; kx < BNS; ++kx) {
+                    float e[4], h[4], vv[4], oo[4], ds[4], s0[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        e[i] = Es[(m0 + i) * LS + kx];
+                        h[i] = dHs[(m0 + i) * LS + kx];
+                        vv[i] = Vs[(m0 + i) * LS + kx];
+                        oo[i] = dOs[(m0 + i) * LS + kx];
+                        ds[i] = dSs[(n0 + i) * LS + kx];
+                        s0[i] = S0s[(n0 + i) * LS + kx];
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) {
+                            cA[i][jj] = fmaf(e[i], ds[jj], cA[i][jj]);
+                            cK[i][jj] = fmaf(vv[i], ds[jj], cK[i][jj]);
+                            cB[i][jj] = fmaf(h[i], s0[jj], cB[i][jj]);
+                            cQ[i][jj] = fmaf(oo[i], s0[jj], cQ[i][jj]);
+                        }
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const int ix = (m0 + i) * LD + n0 + jj;
+                        dAt[ix] -= cA[i][jj];
+                        dBt[ix] += cB[i][jj];
+                        dKt[ix] += cK[i][jj];
+                        dQt[ix] += cQ[i][jj];
+                    }
+            }
+        } else {
+            mm(dAt, LD, Es, LS, false, dSs, LS, true, R, dk, BNS, -1.f, true);
+            mm(dBt, LD, dHs, LS, false, S0s, LS, true, R, dk, BNS, 1.f, true);
+            mm(dKt, LD, Vs, LS, false, dSs, LS, true, P, dk, BNS, 1.f, true);
+            mm(dQt, LD, dOs, LS, false, S0s, LS, true, cb, dk, BNS, 1.f, true);
+        }
         // (four small products, at most 64 tiles each: a quarter of the threads each)
         const int q4 = nth / 4;
         mm(dL, LM, dHs, LS, false, Es, LS, true, R, R, BNS, -1.f, true, 0, q4);
