@@ -376,15 +376,62 @@ block_bwd_kernel(Plan pl, BwdArgs a) {
     mask(dQA, LM, cb, R, 1, r, false);
     mask(dQK, LM, cb, P, 1, p, false);
     __syncthreads();
-    mm(dAt, LD, dQA, LM, true, Qt, LD, false, R, dk, cb, 1.f, true);
-    mm(dBt, LD, dG, LM, false, Kt, LD, false, R, dk, P, 1.f, true);
-    mm(dKt, LD, dQK, LM, true, Qt, LD, false, P, dk, cb, 1.f, true);
-    mm(dQt, LD, dQA, LM, false, At, LD, false, cb, dk, R, 1.f, true);
-    __syncthreads();
-    mm(dAt, LD, dL, LM, true, Bt, LD, false, R, dk, R, 1.f, true);
-    mm(dBt, LD, dL, LM, false, At, LD, false, R, dk, R, 1.f, true);
-    mm(dKt, LD, dG, LM, true, Bt, LD, false, P, dk, R, 1.f, true);
-    mm(dQt, LD, dQK, LM, false, Kt, LD, false, cb, dk, P, 1.f, true);
+    if (R == cb && P == cb) {   // (rank 1) the eight in one pass over the block's tokens
+        const int nt = dk >> 2;
+        for (int tile = tid; tile < (cb >> 2) * nt; tile += nth) {
+            const int m0 = (tile / nt) << 2, n0 = (tile % nt) << 2;
+            float cA[4][4] = {}, cB[4][4] = {}, cK[4][4] = {}, cQ[4][4] = {};
+#pragma unroll 2
+            for (int kx = 0; kx < cb; ++kx) {
+                float qv[4], kv[4], av[4], bv[4];
+                float qaT[4], lT[4], qkT[4], gT[4], gR[4], lR[4], qaR[4], qkR[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    qv[i] = Qt[kx * LD + n0 + i];
+                    kv[i] = Kt[kx * LD + n0 + i];
+                    av[i] = At[kx * LD + n0 + i];
+                    bv[i] = Bt[kx * LD + n0 + i];
+                    qaT[i] = dQA[kx * LM + m0 + i];
+                    lT[i] = dL[kx * LM + m0 + i];
+                    qkT[i] = dQK[kx * LM + m0 + i];
+                    gT[i] = dG[kx * LM + m0 + i];
+                    gR[i] = dG[(m0 + i) * LM + kx];
+                    lR[i] = dL[(m0 + i) * LM + kx];
+                    qaR[i] = dQA[(m0 + i) * LM + kx];
+                    qkR[i] = dQK[(m0 + i) * LM + kx];
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        cA[i][jj] = fmaf(qaT[i], qv[jj], fmaf(lT[i], bv[jj], cA[i][jj]));
+                        cB[i][jj] = fmaf(gR[i], kv[jj], fmaf(lR[i], av[jj], cB[i][jj]));
+                        cK[i][jj] = fmaf(qkT[i], qv[jj], fmaf(gT[i], bv[jj], cK[i][jj]));
+                        cQ[i][jj] = fmaf(qaR[i], av[jj], fmaf(qkR[i], kv[jj], cQ[i][jj]));
+                    }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const int ix = (m0 + i) * LD + n0 + jj;
+                    dAt[ix] += cA[i][jj];
+                    dBt[ix] += cB[i][jj];
+                    dKt[ix] += cK[i][jj];
+                    dQt[ix] += cQ[i][jj];
+                }
+        }
+    } else {
+        mm(dAt, LD, dQA, LM, true, Qt, LD, false, R, dk, cb, 1.f, true);
+        mm(dBt, LD, dG, LM, false, Kt, LD, false, R, dk, P, 1.f, true);
+        mm(dKt, LD, dQK, LM, true, Qt, LD, false, P, dk, cb, 1.f, true);
+        mm(dQt, LD, dQA, LM, false, At, LD, false, cb, dk, R, 1.f, true);
+        __syncthreads();
+        mm(dAt, LD, dL, LM, true, Bt, LD, false, R, dk, R, 1.f, true);
+        mm(dBt, LD, dL, LM, false, At, LD, false, R, dk, R, 1.f, true);
+        mm(dKt, LD, dG, LM, true, Bt, LD, false, P, dk, R, 1.f, true);
+        mm(dQt, LD, dQK, LM, false, Kt, LD, false, cb, dk, P, 1.f, true);
+    }
     __syncthreads();
 
     // ---- the cumulative log-decay's gradient dG_t (over S0s / dSs), then its reverse prefix: d decay
