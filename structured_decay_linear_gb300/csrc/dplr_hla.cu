@@ -900,8 +900,10 @@ hla_gated_tc_kernel(Plan pl, int L, int N, float theta, GatedArgs args) {
         return;
     }
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::BAR);
-    uint64_t* full = bars + 0;     // the step's operand tiles landed
-    uint64_t* freed = bars + 1;    // the step's products are done with the operand tiles
+    uint64_t* full = bars + 0;     // the step's A_j tiles landed
+    uint64_t* freed = bars + 1;    // the step's products are done (with the B_j tiles last)
+    uint64_t* fullB = bars + 7;    // the step's B_j tiles landed
+    uint64_t* freedA = bars + 8;   // the step's X^T is done with the A_j tiles (the next A_j may land)
     uint64_t* ready = bars + 2;    // the step's U^T and (w U)^T tiles written (4 arrivals, one per state warp)
     uint64_t* mX = bars + 3;       // the step's X^T is complete
     uint64_t* drain = bars + 4;
@@ -939,6 +941,8 @@ hla_gated_tc_kernel(Plan pl, int L, int N, float theta, GatedArgs args) {
         *nsteps = n;
         mbar_init(full, 1);
         mbar_init(freed, 1);
+        mbar_init(fullB, 1);
+        mbar_init(freedA, 1);
         mbar_init(ready, 4);
         mbar_init(mX, 1);
         mbar_init(drain, 1);
@@ -955,24 +959,30 @@ hla_gated_tc_kernel(Plan pl, int L, int N, float theta, GatedArgs args) {
     bool failed = false;
 
     if (warp == 5) {
-        // ---- copies of each step's operand tiles, once the previous step's products are done with them
-        int last = -1;
+        // ---- copies of each step's operand tiles: the A_j pair once the previous step's X^T is done with its own,
+        // the B_j pair once the previous step's o^T products are
+        int lastA = -1, lastB = -1;
         for (int st = 0; st < ns && lane == 0; ++st) {
-            if (st >= 1 && !mbar_wait(freed, (st - 1) & 1, wl)) { failed = true; break; }
             const unsigned char* src = args.tiles + (bh * (size_t)N + list[st]) * 4 * kOpTile;
-            mbar_expect_tx(full, 4 * kOpTile);
-            for (int e = 0; e < 4; ++e) bulk_g2s(smem + S::OPS + e * kOpTile, src + e * kOpTile, kOpTile, full);
+            if (st >= 1 && !mbar_wait(freedA, (st - 1) & 1, wl)) { failed = true; break; }
+            mbar_expect_tx(full, 2 * kOpTile);
+            for (int e = 0; e < 2; ++e) bulk_g2s(smem + S::OPS + e * kOpTile, src + e * kOpTile, kOpTile, full);
+            lastA = st;
+            if (st >= 1 && !mbar_wait(freed, (st - 1) & 1, wl)) { failed = true; break; }
+            mbar_expect_tx(fullB, 2 * kOpTile);
+            for (int e = 2; e < 4; ++e) bulk_g2s(smem + S::OPS + e * kOpTile, src + e * kOpTile, kOpTile, fullB);
+            lastB = st;
             if (st + 1 < ns) {
                 const unsigned char* nx = args.tiles + (bh * (size_t)N + list[st + 1]) * 4 * kOpTile;
                 for (int e = 0; e < 4; ++e)
                     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(reinterpret_cast<uint64_t>(nx + e * kOpTile)),
                                  "r"(kOpTile) : "memory");
             }
-            last = st;
         }
         if (failed) {   // (lane 0) no copy may land after the CTA has exited
             atomicExch(args.status, (int)DPLR_ERR_TIMEOUT);
-            if (last >= 0) mbar_wait(full, last & 1, 400000000LL);
+            if (lastA >= 0) mbar_wait(full, lastA & 1, 400000000LL);
+            if (lastB >= 0) mbar_wait(fullB, lastB & 1, 400000000LL);
         }
         __syncwarp();
     } else if (warp == 4) {
@@ -994,6 +1004,9 @@ hla_gated_tc_kernel(Plan pl, int L, int N, float theta, GatedArgs args) {
                 mma_bf16(tmem, dadd(aH, o), dadd(uL, o), id, 1u);
             }
             mma_commit(mX);
+            mma_commit(freedA);
+            if (!mbar_wait(fullB, st & 1, wl)) { failed = true; break; }
+            fence_after_sync();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {   // o^T += B^T (w U)^T
                 const uint32_t o = kk * 2048;
