@@ -105,7 +105,7 @@ block_bwd_kernel(Plan pl, BwdArgs a) {
     float* Gc = dHs + BMX * LS;    // [BMX][LD] inclusive cumulative log-decay G_t
     float* va = Gc + BMX * LD;      // [BD] anchor a
     float* sd = va + BD;            // [BD] sum_n S_j dS_j per row
-    float* ct = sd + BD;            // [BMX] HDLA: k^T Lambda k per token
+    float* ct = sd + BD;            // [BMX] HDLA: k^T Lambda k per token; GDN: e^{-g_t}
     float* ks = ct + BMX;           // [8][BMX][BNS] partial tiles of the slice's small products (K split 8 ways)
     float* dVt = ks + 8 * BMX * BNS; // [BMX][BNS] the slice of dV
 
@@ -208,6 +208,7 @@ block_bwd_kernel(Plan pl, BwdArgs a) {
                 const float eg = ok ? __expf(a.decay[tg]) : 1.f;
                 At[t * LD + c] = er * eg * b * kk;
                 Bt[t * LD + c] = ef * kk;
+                if (c == 0) ct[t] = ok ? __expf(-a.decay[tg]) : 1.f;   // K~_t = e^{-g_t} A~_t
             } else {
                 const float lam = ok ? __expf(a.decay[tg * dk + c]) : 1.f;
                 At[(2 * t) * LD + c] = er * kk;
@@ -225,7 +226,17 @@ block_bwd_kernel(Plan pl, BwdArgs a) {
     {
         const KOut kl = {Mm, LM, R, R, 1.f, false, 1, {{Bt, LD, false, At, LD, true, dk}, {}, {}}};
         const KOut kq = {QA, LM, cb, R, 1.f, false, 1, {{Qt, LD, false, At, LD, true, dk}, {}, {}}};
-        if (P > 0) {   // two at a time
+        if (MODE == DPLR_GDN) {   // K~ = Diag(e^{-g}) A~: G = L Diag(e^{-g}) and QK = QA Diag(e^{-g})
+            const KOut g1[2] = {kl, kq};
+            mm_ksplit_out(g1, ks);
+            __syncthreads();
+            for (int i = tid; i < cb * cb; i += nth) {
+                const int t = i / cb, s2 = i - t * cb;
+                Gm[t * LM + s2] = Mm[t * LM + s2] * ct[s2];
+                QK[t * LM + s2] = QA[t * LM + s2] * ct[s2];
+            }
+            __syncthreads();
+        } else if (P > 0) {   // two at a time
             const KOut g1[2] = {kl, {Gm, LM, R, P, 1.f, false, 1, {{Bt, LD, false, Kt, LD, true, dk}, {}, {}}}};
             mm_ksplit_out(g1, ks);
             __syncthreads();
