@@ -268,6 +268,12 @@ block_bwd_kernel(Plan pl, BwdArgs a) {
     for (int i = tid; i < BMX * LM; i += nth) dL[i] = dG[i] = dQA[i] = dQK[i] = 0.f;
     for (int c = tid; c < dk; c += nth) sd[c] = 0.f;
     __syncthreads();
+    if (MODE == DPLR_GDN) {   // W = QA M over QA: the slices' dH takes W^T dO for M^T QA^T dO
+        mm(ks, LM, QA, LM, false, Mm, LM, false, cb, R, R, 1.f, false);
+        __syncthreads();
+        for (int i = tid; i < cb * LM; i += nth) QA[i] = ks[i];
+        __syncthreads();
+    }
 
     // ---- the state dimension in slices
     for (int n0 = 0; n0 < dv; n0 += BNS) {
@@ -299,19 +305,38 @@ block_bwd_kernel(Plan pl, BwdArgs a) {
         }
         __syncthreads();
         // the slice's R x 16 products have few tiles: their K is split over the threads, two outputs at a time
-        {   // H = B~ S0 + G V and dE = -(A~ dS^ + QA^T dO)
-            const KOut ko[2] = {
-                {Hs, LS, R, BNS, 1.f, false, 2, {{Bt, LD, false, S0s, LS, false, dk}, {Gm, LM, false, Vs, LS, false, P}, {}}},
-                {dEs, LS, R, BNS, -1.f, false, 2, {{At, LD, false, dSs, LS, false, dk}, {QA, LM, true, dOs, LS, false, cb}, {}}}};
-            mm_ksplit_out(ko, ks);
+        if (MODE == DPLR_GDN) {
+            // H = B~ S0 + G V, and X = A~ dS^ (over dE): dE = -(X + QA^T dO), so dH = M^T dE = -(M^T X + W^T dO), and
+            // the dV term K~ dS^ is e^{-g} X (K~ = Diag(e^{-g}) A~)
+            {
+                const KOut ko[2] = {
+                    {Hs, LS, R, BNS, 1.f, false, 2, {{Bt, LD, false, S0s, LS, false, dk}, {Gm, LM, false, Vs, LS, false, P}, {}}},
+                    {dEs, LS, R, BNS, 1.f, false, 1, {{At, LD, false, dSs, LS, false, dk}, {}, {}}}};
+                mm_ksplit_out(ko, ks);
+            }
+            __syncthreads();
+            {
+                const KOut ko[2] = {{Es, LS, R, BNS, 1.f, false, 1, {{Mm, LM, false, Hs, LS, false, R}, {}, {}}},
+                                    {dHs, LS, R, BNS, -1.f, false, 2,
+                                     {{Mm, LM, true, dEs, LS, false, R}, {QA, LM, true, dOs, LS, false, cb}, {}}}};
+                mm_ksplit_out(ko, ks);
+            }
+            __syncthreads();
+        } else {
+            {   // H = B~ S0 + G V and dE = -(A~ dS^ + QA^T dO)
+                const KOut ko[2] = {
+                    {Hs, LS, R, BNS, 1.f, false, 2, {{Bt, LD, false, S0s, LS, false, dk}, {Gm, LM, false, Vs, LS, false, P}, {}}},
+                    {dEs, LS, R, BNS, -1.f, false, 2, {{At, LD, false, dSs, LS, false, dk}, {QA, LM, true, dOs, LS, false, cb}, {}}}};
+                mm_ksplit_out(ko, ks);
+            }
+            __syncthreads();
+            {   // E = M H and dH = M^T dE
+                const KOut ko[2] = {{Es, LS, R, BNS, 1.f, false, 1, {{Mm, LM, false, Hs, LS, false, R}, {}, {}}},
+                                    {dHs, LS, R, BNS, 1.f, false, 1, {{Mm, LM, true, dEs, LS, false, R}, {}, {}}}};
+                mm_ksplit_out(ko, ks);
+            }
+            __syncthreads();
         }
-        __syncthreads();
-        {   // E = M H and dH = M^T dE
-            const KOut ko[2] = {{Es, LS, R, BNS, 1.f, false, 1, {{Mm, LM, false, Hs, LS, false, R}, {}, {}}},
-                                {dHs, LS, R, BNS, 1.f, false, 1, {{Mm, LM, true, dEs, LS, false, R}, {}, {}}}};
-            mm_ksplit_out(ko, ks);
-        }
-        __syncthreads();
         if (R == cb && P == cb) {   // (rank 1) the four in one pass: dS^ and S0 columns loaded once for two each
             const int nt = dk >> 2;
             for (int tile = tid; tile < (cb >> 2) * nt; tile += nth) {
@@ -364,7 +389,12 @@ block_bwd_kernel(Plan pl, BwdArgs a) {
         mm(dQK, LM, dOs, LS, false, Vs, LS, true, cb, P, BNS, 1.f, true, 3 * q4, q4);
         __syncthreads();
         // dV = K~ dS^ + QK^T dO + G^T dH for this slice, then to the output (a generic mode may have no K, V)
-        if (P > 0) {
+        if (MODE == DPLR_GDN) {   // K~ dS^ = e^{-g} X, X over dE
+            const KOut ko[1] = {{dVt, BNS, P, BNS, 1.f, false, 2,
+                                 {{QK, LM, true, dOs, LS, false, cb}, {Gm, LM, true, dHs, LS, false, R}, {}}}};
+            mm_ksplit_out(ko, ks);
+            __syncthreads();
+        } else if (P > 0) {
             const KOut ko[1] = {{dVt, BNS, P, BNS, 1.f, false, 3,
                                  {{Kt, LD, false, dSs, LS, false, dk}, {QK, LM, true, dOs, LS, false, cb},
                                   {Gm, LM, true, dHs, LS, false, R}}}};
@@ -375,6 +405,7 @@ block_bwd_kernel(Plan pl, BwdArgs a) {
             const int u = idx / BNS, n = idx - u * BNS, t = u / p, e = u - t * p;
             if (t < valid) {
                 if (MODE == DPLR_GENERIC) a.dV[((tok0 + t) * p + e) * dv + n0 + n] = dVt[idx];
+                else if (MODE == DPLR_GDN) a.dv[(tok0 + t) * dv + n0 + n] = dVt[idx] + ct[t] * dEs[t * LS + n];
                 else a.dv[(tok0 + t) * dv + n0 + n] = dVt[idx];
             }
         }
