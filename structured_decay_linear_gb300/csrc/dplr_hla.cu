@@ -357,11 +357,7 @@ hla_block_maps_tc_kernel(Plan pl, const __nv_bfloat16* q, const __nv_bfloat16* k
     const int row = 32 * (warp & 3) + lane, hf = warp >> 2;
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const int T = pl.T, nb = pl.nb;
-    const int blk = blockIdx.x % nb;
-    const size_t bh = blockIdx.x / nb;
-    const int t0 = blk * HQ, valid = min(HQ, T - t0);
-    const size_t tok0 = bh * (size_t)T + t0;
-    const size_t unit = bh * (size_t)nb + blk;
+    const long long total = (long long)pl.BH * nb;
     const long long wl = pl.wait_cycles;
     constexpr uint32_t TD = 0, TY = 64, TU = 128, TP = 192, TC = 320, TO = 448;
 
@@ -371,6 +367,44 @@ hla_block_maps_tc_kernel(Plan pl, const __nv_bfloat16* q, const __nv_bfloat16* k
         mbar_fence_init();
     }
     if (warp == 0) tmem_alloc(tmem_holder, 512);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tmem_holder;
+    uint32_t phase = 0;
+    bool failed = false;
+    auto wait_products = [&]() -> bool {
+        const bool ok = mbar_wait(mb, phase & 1, wl);
+        ++phase;
+        const bool bad = __syncthreads_or(!ok);
+        fence_after_sync();
+        return !bad;
+    };
+    auto operands_ready = [&]() {
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+    };
+    const uint32_t lead = (warp == 0 && lane == 0) ? 1u : 0u;
+    // Kt: K^T (or V^T) as the MN-major A operand over the tokens; halves of 64 features `half` bytes apart
+    auto mn_desc = [&](uint32_t base, uint32_t half) { return smem_desc_sw128(sb + base, half, 1024); };
+
+  // persistent: CTA b takes the blocks b, b + gridDim.x, ... (the next one's rows asked for in L2 first)
+  for (long long ux = blockIdx.x; ux < total && !failed; ux += gridDim.x) {
+    const int blk = static_cast<int>(ux % nb);
+    const size_t bh = static_cast<size_t>(ux / nb);
+    const int t0 = blk * HQ, valid = min(HQ, T - t0);
+    const size_t tok0 = bh * (size_t)T + t0;
+    const size_t unit = bh * (size_t)nb + blk;
+    if (tid == 0 && ux + gridDim.x < total) {
+        const long long nx = ux + gridDim.x;
+        const int nt0 = static_cast<int>(nx % nb) * HQ, nvalid = min(HQ, T - nt0);
+        const size_t ntok = (size_t)(nx / nb) * T + nt0;
+        for (const __nv_bfloat16* src : {k, q, v})
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                         :: "l"(reinterpret_cast<uint64_t>(src + ntok * HD2)), "r"((uint32_t)(nvalid * HD2 * 2)) : "memory");
+    }
     // ---- k, q, v of the block (zeros past the sequence), in the 128-byte swizzled layout
     for (int i = tid; i < HQ * 16; i += kBT) {
         const int t = i >> 4, cb = i & 15;
@@ -411,25 +445,6 @@ hla_block_maps_tc_kernel(Plan pl, const __nv_bfloat16* q, const __nv_bfloat16* k
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    const uint32_t tmem = *tmem_holder;
-    uint32_t phase = 0;
-    bool failed = false;
-    auto wait_products = [&]() -> bool {
-        const bool ok = mbar_wait(mb, phase & 1, wl);
-        ++phase;
-        const bool bad = __syncthreads_or(!ok);
-        fence_after_sync();
-        return !bad;
-    };
-    auto operands_ready = [&]() {
-        fence_async_smem();
-        fence_before_sync();
-        __syncthreads();
-        fence_after_sync();
-    };
-    const uint32_t lead = (warp == 0 && lane == 0) ? 1u : 0u;
-    // Kt: K^T (or V^T) as the MN-major A operand over the tokens; halves of 64 features `half` bytes apart
-    auto mn_desc = [&](uint32_t base, uint32_t half) { return smem_desc_sw128(sb + base, half, 1024); };
 
     // ---- D = [K; Q] K^T
     if (warp == 0) {
@@ -627,7 +642,12 @@ hla_block_maps_tc_kernel(Plan pl, const __nv_bfloat16* q, const __nv_bfloat16* k
             for (int e = 0; e < 32; ++e)
                 if (e < nv) oc[(size_t)e * HD2] = x[e];
         }
-    } else if (tid == 0) {   // no product may outlive the tensor memory
+    }
+    fence_before_sync();
+    __syncthreads();   // every read of this block's tiles and accumulators done before the next block's loads
+    fence_after_sync();
+  }   // blocks
+    if (failed && tid == 0) {   // no product may outlive the tensor memory
         atomicExch(status, (int)DPLR_ERR_TIMEOUT);
         mma_commit(drain);
         mbar_wait(drain, 0, 400000000LL);
@@ -1178,7 +1198,7 @@ extern "C" dplr_status dplr_hla_forward(const dplr_desc* desc, const void* q, co
     if (pl.bf16 && pl.dk == HD2 && pl.dv == HD2) {   // pass 1 on the tensor cores (o <- O_t)
         if (set_smem_limit_once(reinterpret_cast<const void*>(hla_block_maps_tc_kernel), BSm::TOTAL, g_hla_smem[4]) != cudaSuccess)
             return DPLR_ERR_CUDA;
-        hla_block_maps_tc_kernel<<<(unsigned)((size_t)pl.BH * pl.nb), kBT, BSm::TOTAL, s>>>(
+        hla_block_maps_tc_kernel<<<(unsigned)std::min<long long>((long long)pl.BH * pl.nb, sm_count()), kBT, BSm::TOTAL, s>>>(
             pl, static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v),
             g, beta, ma.Pm, ma.Cm, ma.Qm, o, reinterpret_cast<int*>(ws));
         if (cudaGetLastError() != cudaSuccess) return DPLR_ERR_CUDA;
