@@ -632,6 +632,20 @@ hdla_chunk_kernel(Plan pl, K1Args args, const __grid_constant__ CUtensorMap tm_q
 // Stage 2: the chain over chunks, per (head, block of state columns)
 // ================================================================================================
 
+// A bounded wait that polls (mbarrier.test_wait) instead of suspending: for the chain's hand-offs, where the
+// waiting warps have nothing else to do and the wake-up of a suspended wait is on the critical path.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* mbar, uint32_t parity, long long max_cycles) {
+    const uint32_t a = smem_addr(mbar);
+    const long long t0 = clock64();
+    for (;;) {
+        uint32_t done;
+        asm volatile("{\n\t.reg .pred q;\n\tmbarrier.test_wait.parity.shared::cta.b64 q, [%1], %2;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+                     : "=r"(done) : "r"(a), "r"(parity) : "memory");
+        if (done) return true;
+        if (clock64() - t0 > max_cycles) return false;
+    }
+}
+
 constexpr int NV = 32;       // state columns per chain CTA
 constexpr int K2T = 224;     // warps 0-3: the state (thread = key channel = tensor-memory lane); 4: issuer;
                              // 5: copies of P_j and c_j; 6: copies of Q'_j and O_j
@@ -788,7 +802,7 @@ hdla_chain_kernel(Plan pl, K2Args args, const __grid_constant__ CUtensorMap tm_P
         };
         for (int j = 0; j < NC && lane == 0; ++j) {
             const int u = j & 1;
-            if (!mbar_wait(ready, j & 1, wl) || !mbar_wait(&fullPC[u], (j >> 1) & 1, wl)) { failed = true; break; }
+            if (!mbar_wait_spin(ready, j & 1, wl) || !mbar_wait(&fullPC[u], (j >> 1) & 1, wl)) { failed = true; break; }
             fence_after_sync();
             products(tmem, smem_desc_sw128(sb + S::PCS + u * S::PC + S::P_, 16, 1024), j % K2SB);
             mma_commit(mS);
@@ -825,7 +839,7 @@ hdla_chain_kernel(Plan pl, K2Args args, const __grid_constant__ CUtensorMap tm_P
         // must not leave the loop while the others go on to the group barrier)
         auto wait_all = [&](uint64_t* bar, uint32_t parity, uint64_t* bar2, uint32_t parity2) -> bool {
             bool ok = true;
-            if (lane == 0) ok = mbar_wait(bar, parity, wl) && (bar2 == nullptr || mbar_wait(bar2, parity2, wl));
+            if (lane == 0) ok = mbar_wait_spin(bar, parity, wl) && (bar2 == nullptr || mbar_wait(bar2, parity2, wl));
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             return !named_sync_or(1, 128, !ok);
         };
