@@ -632,20 +632,6 @@ hdla_chunk_kernel(Plan pl, K1Args args, const __grid_constant__ CUtensorMap tm_q
 // Stage 2: the chain over chunks, per (head, block of state columns)
 // ================================================================================================
 
-// A bounded wait that polls (mbarrier.test_wait) instead of suspending: for the chain's hand-offs, where the
-// waiting warps have nothing else to do and the wake-up of a suspended wait is on the critical path.
-__device__ __forceinline__ bool mbar_wait_spin(uint64_t* mbar, uint32_t parity, long long max_cycles) {
-    const uint32_t a = smem_addr(mbar);
-    const long long t0 = clock64();
-    for (;;) {
-        uint32_t done;
-        asm volatile("{\n\t.reg .pred q;\n\tmbarrier.test_wait.parity.shared::cta.b64 q, [%1], %2;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-                     : "=r"(done) : "r"(a), "r"(parity) : "memory");
-        if (done) return true;
-        if (clock64() - t0 > max_cycles) return false;
-    }
-}
-
 constexpr int NV = 32;       // state columns per chain CTA
 constexpr int K2T = 224;     // warps 0-3: the state (thread = key channel = tensor-memory lane); 4: issuer;
                              // 5: copies of P_j and c_j; 6: copies of Q'_j and O_j

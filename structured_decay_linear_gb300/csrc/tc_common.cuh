@@ -273,6 +273,20 @@ __device__ __forceinline__ void inv64_inplace(float* X, int t, uint32_t bar) {
     }
 }
 
+// A bounded wait that polls (mbarrier.test_wait) instead of suspending: for the chain's hand-offs, where the
+// waiting warps have nothing else to do and the wake-up of a suspended wait is on the critical path.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* mbar, uint32_t parity, long long max_cycles) {
+    const uint32_t a = smem_addr(mbar);
+    const long long t0 = clock64();
+    for (;;) {
+        uint32_t done;
+        asm volatile("{\n\t.reg .pred q;\n\tmbarrier.test_wait.parity.shared::cta.b64 q, [%1], %2;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+                     : "=r"(done) : "r"(a), "r"(parity) : "memory");
+        if (done) return true;
+        if (clock64() - t0 > max_cycles) return false;
+    }
+}
+
 // Bulk stores (shared -> global) by tensor map, and their completion.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];"
