@@ -1,5 +1,5 @@
 // Block-wide fp32 products in shared memory (CUDA cores): mm, and mm_ksplit_out for products with few tiles
-// and a long K. Shared by the backward and the HLA kernels.
+// and a long K. Used by the backward kernels.
 #pragma once
 
 namespace dplr {
