@@ -110,3 +110,32 @@ def test_backward_without_final_state_gradient(sdl):
     g = _run(sdl, "gdn", "bf16", inp, do, None)
     ref = oracle.backward_inputs(inp, do, None)
     _check(g, ref, ["q", "k", "v", "decay", "beta", "S0"])
+
+
+def test_backward_full_size_workload_sampled_heads(sdl):
+    """The backward workload the benchmark times, at full size (Gated DeltaNet bf16 B8 H16 T8192 d128), in one call
+    over every head: every gradient finite, and two sampled heads compared with the float64 reverse mode over the
+    whole sequence."""
+    import torch
+    w = workloads.WORKLOADS[2]
+    inp = workloads.generate(w)
+    rng = np.random.default_rng(21)
+    do = rng.standard_normal((w.B, w.H, w.T, w.dv), dtype=np.float32)
+    dST = rng.standard_normal((w.B, w.H, w.dk, w.dv), dtype=np.float32)
+    d = lambda x, t: None if x is None else torch.from_numpy(np.ascontiguousarray(x)).to("cuda").to(t)
+    bw = sdl.Backward("gdn", torch.bfloat16, w.B, w.H, w.T, w.dk, w.dv)
+    g = bw(dO=d(do, torch.float32), dST=d(dST, torch.float32), q=d(inp["q"], torch.bfloat16),
+           k=d(inp["k"], torch.bfloat16), v=d(inp["v"], torch.bfloat16), decay=d(inp["decay"], torch.float32),
+           beta=d(inp["beta"], torch.float32), S0=d(inp["S0"], torch.float32))
+    torch.cuda.synchronize()
+    for name, x in g.items():
+        if x is not None:
+            assert bool(torch.isfinite(x).all()), f"d{name} not finite"
+    pairs = [(0, 0), (7, 9)]
+    sub = workloads.generate(w, heads=pairs)
+    idx = (np.array([b for b, _ in pairs]), np.array([h for _, h in pairs]))
+    ref = oracle.backward_inputs(sub, do[idx][None], dST[idx][None])
+    for i, (b, h) in enumerate(pairs):
+        for name in ("q", "k", "v", "decay", "beta", "S0"):
+            e = _rel(g[name][b, h].double().cpu().numpy(), ref[name][0, i])
+            assert e <= TAU, f"head {(b, h)} d{name}: max|err|/rms = {e:.3e}"

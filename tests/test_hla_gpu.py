@@ -126,3 +126,39 @@ def test_hla_tensor_core_pass_timeout_returns_and_reports(sdl):
     assert f.device_status() == sdl.DPLR_OK
     ref = oracle.hla(inp["q"], inp["k"], inp["v"], inp["decay"], inp["beta"], W, L, 0.1)
     assert _rel(o.double().cpu().numpy(), ref) <= TAU
+
+
+def test_hla_full_size_gates_one_and_zero(sdl):
+    """The HLA workload the benchmark times, at full size (Gated DeltaNet bf16 B1 H16 T4096 d128, L = 256), through
+    two properties that hold at any size. With every gate 1 the composition is the plain recurrence: two sampled
+    heads against the float64 forward, every head against the fused forward. With every gate 0 no history enters,
+    so each 256-token chunk starts from a zero state: every head against the fused forward of the chunks taken as
+    separate sequences."""
+    import torch
+    H, T, L = 16, 4096, 256
+    N = T // L
+    w = workloads.Workload(98, "hla_gdn_bf16_b1h16", "gdn", "bf16", 1, H, T, 128, 128, 1, 1, 64, False)
+    inp = workloads.generate(w)
+    d = lambda x, t: torch.from_numpy(np.ascontiguousarray(x)).to("cuda").to(t)
+    args = [d(inp["q"], torch.bfloat16), d(inp["k"], torch.bfloat16), d(inp["v"], torch.bfloat16),
+            d(inp["decay"], torch.float32), d(inp["beta"], torch.float32)]
+    f = sdl.HLA(torch.bfloat16, 1, H, T, 128, 128, L)
+    assert f.path == "hla_gated_tcgen05"
+    o1 = f(*args, torch.ones(1, H, T, N, device="cuda"), 0.1).clone()
+    o0 = f(*args, torch.zeros(1, H, T, N, device="cuda"), 0.1).clone()
+    fwd = sdl.Forward("gdn", torch.bfloat16, 1, H, T, 128, 128)
+    of, _ = fwd(q=args[0], k=args[1], v=args[2], decay=args[3], beta=args[4])
+    of = of.clone()
+    chunks = lambda x: x.reshape(1, H * N, L, *x.shape[3:]).contiguous()
+    fl = sdl.Forward("gdn", torch.bfloat16, 1, H * N, L, 128, 128)
+    ol, _ = fl(q=chunks(args[0]), k=chunks(args[1]), v=chunks(args[2]), decay=chunks(args[3]), beta=chunks(args[4]))
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(o1).all()) and bool(torch.isfinite(o0).all())
+    host = lambda x: x.double().cpu().numpy()
+    assert _rel(host(o1), host(of)) <= 2e-2
+    assert _rel(host(o0), host(ol.reshape(1, H, T, 128))) <= 2e-2
+    pairs = [(0, 0), (0, 11)]
+    ref, _ = oracle.forward_inputs(workloads.generate(w, heads=pairs))
+    for i, (b, h) in enumerate(pairs):
+        e = _rel(host(o1[b, h]), ref[0, i])
+        assert e <= TAU, f"head {(b, h)}: max|err|/rms = {e:.3e}"
