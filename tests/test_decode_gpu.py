@@ -125,3 +125,16 @@ def test_decode_rejects_bad_arguments(sdl):
     d = sdl.make_desc("gdn", "bf16", 1, 1, 1, 128, 128)
     assert sdl.dplr_la_decode_step(d, p, p, p, p, p, None, None, None, None, None, p, s) == sdl.dplr.DPLR_ERR_INVALID_ARG
     assert sdl.dplr_la_decode_step(d, p + 4, p, p, p, p, None, None, None, None, p, p, s) == sdl.dplr.DPLR_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("wid", [2, 4])
+def test_decode_full_head_count(sdl, wid):
+    """The head counts the decode benchmark times (Gated DeltaNet bf16 B8 H16 d128; HDLA bf16 B1 H16 d128): eight
+    tokens decoded from a random state for every head, every head against the float64 recurrence."""
+    w = workloads.WORKLOADS[wid]
+    inp = workloads.generate(w, T=8)
+    S0 = (0.1 * np.random.default_rng(9).standard_normal((w.B, w.H, w.dk, w.dv))).astype(np.float32)
+    inp["S0"] = S0
+    o, S = _decode(sdl, inp, w.mode, w.dtype, S0)
+    o_ref, S_ref = oracle.forward_inputs(inp)
+    assert _rel(o, o_ref) <= TAU_STEP and _rel(S, S_ref) <= TAU_STEP
