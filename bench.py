@@ -35,17 +35,10 @@ import numpy as np  # noqa: E402
 import workloads  # noqa: E402
 
 DEFAULT_WORKLOAD = 2
-METRIC = None            # filled from the baseline record's metric string
+# The headline metric: forward tokens/s (and TFLOP/s) at T = 8K-128K on one GB300, with the fraction of the roofline.
+METRIC = "fwd tokens/s & TFLOP/s at T=8K\u2013128K on 1 GB300; % of roofline"
 L2_BYTES = 129 * 2 ** 20
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-
-
-def load_metric():
-    try:
-        with open(os.path.join(ROOT, "BASELINE.json")) as f:
-            return json.load(f)["metric"]
-    except Exception:
-        return "fwd tokens/s & TFLOP/s at T=8K-128K on 1 GB300; % of roofline"
 
 
 def load_peaks():
@@ -272,7 +265,7 @@ def run_reference(args, w):
     value = toks / dt
     sample = f"{len(heads)} heads x {T_s} tokens of the workload recipe per step"
     line = {
-        "impl": "reference", "metric": load_metric(), "value": value, "unit": "tokens/s", "n_gpus": world,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": steps, "warmup": warm, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "mode": w.mode, "B": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv,
@@ -413,7 +406,7 @@ def run_ours(args, w):
         else:
             cpu_v, cpu_cores, cpu_sample = None, None, "not run (rank 0 at N=1 only)"
         line = {
-            "metric": load_metric(),
+            "metric": METRIC,
             "value": value,
             "unit": "tokens/s",
             "n_gpus": world,
