@@ -157,6 +157,8 @@ GENERIC_TC = [
     ("f32", 4, 1, 3, 33),     # one token past a block
     ("f32", 1, 2, 1, 129),
     ("bf16", 4, 2, 2, 200),
+    ("f32", 1, 0, 2, 8192),   # the generic workload's sequence length at other ranks
+    ("f32", 3, 1, 2, 8192),
 ]
 
 
