@@ -639,6 +639,45 @@ def run_hla(args):
           flush=True)
 
 
+def run_gdp(args):
+    """Time of dplr_gdp_forward (stacked Householders in the Gated DeltaProduct style: per token the gate, then n_h
+    erase-and-write steps) at the generic workload's shape, B=2 H=8 T=8192 d=64, fp32 inputs, for n_h = 2 (the
+    tensor-core generic stages) and n_h = 3 (the fp32 stages). Synthetic inputs: unit-norm k, beta in (0, 2),
+    log-gates -softplus(-(N(0, 1) + 3)). Not a benchmark line; the JSON carries "mode": "gdp"."""
+    import torch
+    import structured_decay_linear_gb300 as sdl
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    B, H, T, d = 2, 8, args.seq_len or 8192, 64
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    rn = lambda *shape: torch.randn(*shape, device=dev, generator=g)
+    lines = []
+    for nh in (2, 3):
+        k = torch.nn.functional.normalize(rn(B, H, T, nh, d), dim=-1)
+        x = dict(q=rn(B, H, T, d) / d ** 0.5, k=k, v=rn(B, H, T, nh, d),
+                 g=-torch.nn.functional.softplus(-(rn(B, H, T) + 3)), beta=2 * torch.sigmoid(rn(B, H, T, nh)),
+                 S0=0.1 * rn(B, H, d, d))
+        f = sdl.GDP(torch.float32, B, H, T, d, d, nh, device=dev)
+        call = lambda: f(**x)
+        for _ in range(max(args.warmup, 3)):
+            call()
+        torch.cuda.synchronize(dev)
+        K = args.steps
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(K):
+            call()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / K
+        lines.append({"workload": f"gdp_nh{nh}_f32_b{B}h{H}_t{T}_d{d}", "n_h": nh, "path": f.path, "ms_per_forward": ms,
+                      "tokens_per_s": B * H * T / (ms * 1e-3),
+                      "output_finite": bool(torch.isfinite(f.o).all().item() and torch.isfinite(f.S_T).all().item())})
+    print(json.dumps({"mode": "gdp", "steps": args.steps, "results": lines}), flush=True)
+
+
 def run_backward(args):
     """Time of dplr_la_backward (the gradients of every input given dO and dS_T) on a workload at full size, with
     the same recipe as the forward and random upstream gradients. Reports ms per backward and tokens/s, and the
@@ -702,6 +741,8 @@ def main():
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gdp", action="store_true",
+                    help="time the stacked-Householder forward, n_h = 2 and 3 (not a benchmark line)")
     ap.add_argument("--hla", action="store_true",
                     help="time HLA's query-gated composition (dplr_hla_forward); not a benchmark line")
     ap.add_argument("--backward", action="store_true",
@@ -715,6 +756,9 @@ def main():
     args = ap.parse_args()
     if args.host_overhead:
         run_host_overhead(args)
+        return
+    if args.gdp:
+        run_gdp(args)
         return
     if args.hla:
         run_hla(args)
